@@ -44,8 +44,9 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB)
+        # A planted-mistake test points this at a mutated build of the oracle.
+        path = os.environ.get("QMOE_ORACLE_LIB") or build()
+        L = ctypes.CDLL(path)
         d, u8, u16, i64, i32, vp = (
             ctypes.c_double, ctypes.c_uint8, ctypes.c_uint16, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p)
         for name in ("oracle_bf16_to_double", "oracle_fp16_to_double"):
