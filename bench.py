@@ -1,0 +1,439 @@
+"""Benchmark of the quantized MoE expert path on GB300.
+
+One step = the whole path over one batch of routed tokens: routing sort,
+activation quantisation, grouped gate/up GEMM + SwiGLU (+ intermediate
+quantisation), grouped down GEMM, weighted combine.  Default workload: the
+MXFP4 x FP8 prefill layer at T=4096 (hidden 4096, 512 experts, top-10,
+inter 1024).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica on its own tokens (weak
+scaling; the layer needs no exchange between ranks).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_mixture_experts_moe_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "grouped-MoE prefill TFLOP/s & tokens/s at T=4096; % of tensor/HBM roofline"
+UNIT = "TFLOP/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mxfp4_T4096")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work for the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def weight_bytes_per_row(scheme, K):
+    if scheme == "w4a16":
+        return K // 2 + 2 * (K // 32)
+    if scheme == "mxfp4":
+        return K // 2 + K // 32
+    return K + 4
+
+
+def act_bytes_per_row(scheme, K):
+    if scheme == "w4a16":
+        return 2 * K
+    if scheme == "mxfp4":
+        return K + K // 32
+    return K + 4
+
+
+def touched_experts(ids, E):
+    return int(np.count_nonzero(np.bincount(ids.reshape(-1), minlength=E)))
+
+
+def algorithmic(w, ids):
+    """Per-launch algorithmic bytes and flops of the two grouped GEMMs:
+    weights (with scales) of the experts the batch touches, activations read
+    once per pair, intermediate written/read once, y written once."""
+    Et = touched_experts(ids, w.E)
+    P = w.P
+    g1_bytes = (Et * 2 * w.I * weight_bytes_per_row(w.scheme, w.H) + w.T * act_bytes_per_row(w.scheme, w.H)
+                + P * act_bytes_per_row(w.scheme, w.I))
+    g2_bytes = (Et * w.H * weight_bytes_per_row(w.scheme, w.I) + P * act_bytes_per_row(w.scheme, w.I)
+                + P * w.H * 4)
+    return dict(experts_touched=Et, gemm1_bytes=g1_bytes, gemm2_bytes=g2_bytes,
+                gemm1_flops=4.0 * P * w.H * w.I, gemm2_flops=2.0 * P * w.H * w.I)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=smax, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+
+def cpu_oracle_rate(w, d, seconds, rng_seed=0):
+    """Times the oracle (as it stands) on a bounded sample of tokens of the
+    same workload; returns (flops/s, tokens/s, cores, sample description)."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.num_threads()
+    rng = np.random.default_rng(rng_seed)
+    n = max(1, min(w.T, cores))
+    toks = np.sort(rng.choice(w.T, n, replace=False))
+    dims = (w.T, w.k, w.H, w.I, w.E)
+    t0 = time.perf_counter()
+    oracle.moe_forward(w.scheme, dims, d, tokens=toks)
+    dt = time.perf_counter() - t0
+    # grow the sample to about `seconds` of work
+    want = int(min(w.T, max(n, n * seconds / max(dt, 1e-3))))
+    if want > n:
+        toks = np.sort(rng.choice(w.T, want, replace=False))
+        t0 = time.perf_counter()
+        oracle.moe_forward(w.scheme, dims, d, tokens=toks)
+        dt = time.perf_counter() - t0
+        n = want
+    flops = 6.0 * n * w.k * w.H * w.I
+    return flops / dt, n / dt, cores, f"{n} of {w.T} tokens (all k={w.k} pairs each), {dt:.1f} s wall"
+
+
+# ------------------------------------------------------------------ reference arm (the CPU oracle)
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    d = gen.make_all(w)
+    import oracle
+
+    oracle.build()
+    cores = oracle.num_threads()
+    rng = np.random.default_rng(1)
+    dims = (w.T, w.k, w.H, w.I, w.E)
+    # size each step to ~ (budget / (steps + warmup)) seconds of oracle work
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    probe = np.sort(rng.choice(w.T, max(1, min(w.T, cores)), replace=False))
+    t0 = time.perf_counter()
+    oracle.moe_forward(w.scheme, dims, d, tokens=probe)
+    dt = time.perf_counter() - t0
+    n = int(min(w.T, max(len(probe), len(probe) * per_step / max(dt, 1e-3))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        toks = np.sort(rng.choice(w.T, n, replace=False))
+        t0 = time.perf_counter()
+        oracle.moe_forward(w.scheme, dims, d, tokens=toks)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = 6.0 * n * w.k * w.H * w.I / t / 1e12
+    sample = f"{n} of {w.T} tokens per step (all k={w.k} pairs each)"
+    line = dict(metric=METRIC, value=value, unit=UNIT, impl="reference", n_gpus=args.gpus, steps=args.steps,
+                warmup=args.warmup, ms_per_step=t * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic",
+                config=dict(workload=w.name, scheme=w.scheme, T=w.T, H=w.H, E=w.E, k=w.k, I=w.I,
+                            sample=sample),
+                tokens_per_s=n / t,
+                cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle", sample=sample),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, w):
+    import torch
+
+    from quantized_mixture_experts_moe_gb300 import binding as qb
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    qb.lib()
+
+    # each rank: its own tokens (seed + rank), the same expert weights
+    wr = gen.Workload(w.name, w.scheme, w.T, w.H, w.E, w.k, w.I, w.routing, w.seed + 7919 * rank, w.wseed)
+    d = gen.make_all(wr)
+    T, k, H, I, E, P = wr.T, wr.k, wr.H, wr.I, wr.E, wr.P
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    t = {key: to_dev(v) for key, v in d.items()}
+    dims = qb.dims(T, k, H, I, E)
+    stream = torch.cuda.current_stream(dev)
+
+    # persistent buffers for the stage-by-stage step
+    E_ = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+    counts, offsets = E_(E, torch.int32), E_(E + 1, torch.int32)
+    sorted_ids, slot = E_(P, torch.int32), E_(P, torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = qb.alloc_workspace(qb.workspace_bytes(dims), dev)
+    y = E_((P, H), torch.float32)
+    out = E_((T, H), torch.int16)
+    if w.scheme == "mxfp4":
+        xq, xs = E_((T, H), torch.uint8), E_((T, H // 32), torch.uint8)
+        hq, hs = E_((P, I), torch.uint8), E_((P, I // 32), torch.uint8)
+    elif w.scheme == "w8a8":
+        xq, xs = E_((T, H), torch.int8), E_(T, torch.float32)
+        h32 = E_((P, I), torch.float32)
+        hq, hs = E_((P, I), torch.int8), E_(P, torch.float32)
+    else:
+        h16 = E_((P, I), torch.int16)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    g1_pairs, g2_pairs = [], []
+
+    def step(record=False):
+        qb.qmoe_align_sort(dims, t["topk_ids"], counts, offsets, sorted_ids, slot, status, ws)
+        if w.scheme == "mxfp4":
+            qb.qmoe_quant_act_mxfp8(t["x"], xq, xs)
+        elif w.scheme == "w8a8":
+            qb.qmoe_quant_rows_int8_bf16(t["x"], xq, xs)
+        a, b, c = (ev(), ev(), ev()) if record else (None, None, None)
+        if record:
+            a.record(stream)
+        if w.scheme == "mxfp4":
+            qb.qmoe_gemm1_swiglu_mxfp4(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, hq, hs, ws)
+        elif w.scheme == "w8a8":
+            qb.qmoe_gemm1_swiglu_w8a8(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h32, None, ws)
+        else:
+            qb.qmoe_gemm1_swiglu_w4a16(dims, t["x"], t["w1"], t["w1_s"], offsets, sorted_ids, h16, ws)
+        if record:
+            b.record(stream)
+        if w.scheme == "mxfp4":
+            qb.qmoe_gemm2_mxfp4(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, ws)
+        elif w.scheme == "w8a8":
+            qb.qmoe_quant_rows_int8_f32(h32, hq, hs)
+            qb.qmoe_gemm2_w8a8(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, None, ws)
+        else:
+            qb.qmoe_gemm2_w4a16(dims, h16, t["w2"], t["w2_s"], offsets, y, ws)
+        if record:
+            c.record(stream)
+            g1_pairs.append((a, b))
+            g2_pairs.append((b, c))
+        qb.qmoe_combine(dims, y, t["topk_w"], slot, out)
+
+    launches_per_step = 3 + (1 if w.scheme != "w4a16" else 0) + 2 + (1 if w.scheme == "w8a8" else 0) + 1
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    start, end = ev(), ev()
+    barrier()
+    start.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    g1_ms = statistics.mean(a.elapsed_time(b) for a, b in g1_pairs)
+    g2_ms = statistics.mean(a.elapsed_time(b) for a, b in g2_pairs)
+    if world > 1:
+        import torch.distributed as dist
+
+        tm = torch.tensor([ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms = float(tm.item())
+    assert int(status.item()) == 0, "device status flagged an error"
+
+    alg = algorithmic(wr, d["topk_ids"])
+    pk = peaks()
+    flops_step = wr.flops()
+    value = flops_step * world / (ms * 1e-3) / 1e12
+    tokens_per_s = T * world / (ms * 1e-3)
+    # dominant kernel: the gate/up GEMM (2/3 of the weight bytes and flops)
+    t_hbm = alg["gemm1_bytes"] / (pk["hbm"] * 1e9)
+    fp8_peak = 2.0 * pk["bf16"]
+    tensor_peak = fp8_peak if w.scheme == "mxfp4" else pk["bf16"]
+    t_tc = alg["gemm1_flops"] / (tensor_peak * 1e12)
+    if t_hbm >= t_tc:
+        achieved = alg["gemm1_bytes"] / (g1_ms * 1e-3) / 1e9
+        roof = dict(kernel="gemm1_swiglu", bound="hbm", achieved=achieved, peak=pk["hbm"], unit="GB/s",
+                    frac=achieved / pk["hbm"], traffic=None,
+                    peak_source=f"{pk['source']} (hbm_gbs, copy)")
+    else:
+        achieved = alg["gemm1_flops"] / (g1_ms * 1e-3) / 1e12
+        src = "measured bf16 x2 (nominal fp8:bf16 ratio)" if w.scheme == "mxfp4" else "measured bf16"
+        roof = dict(kernel="gemm1_swiglu", bound="tensor", achieved=achieved, peak=tensor_peak, unit="TFLOP/s",
+                    frac=achieved / tensor_peak, traffic=None, peak_source=f"{pk['source']} {src}")
+    roof["gemm1_ms"] = g1_ms
+    roof["gemm2_ms"] = g2_ms
+    roof["gemm1_alg_bytes"] = alg["gemm1_bytes"]
+    roof["gemm2_alg_bytes"] = alg["gemm2_bytes"]
+    roof["gemm2_hbm_frac"] = alg["gemm2_bytes"] / (g2_ms * 1e-3) / 1e9 / pk["hbm"]
+
+    # end to end through the whole-layer entry point with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = t["x"].cpu().pin_memory()
+        hid = t["topk_ids"].cpu().pin_memory()
+        hw = t["topk_w"].cpu().pin_memory()
+        hout = torch.empty((T, H), dtype=torch.int16).pin_memory()
+        dx, did, dw = torch.empty_like(t["x"]), torch.empty_like(t["topk_ids"]), torch.empty_like(t["topk_w"])
+        fws = qb.alloc_workspace(qb.forward_workspace_bytes(dims, w.scheme), dev)
+        dout = E_((T, H), torch.int16)
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            did.copy_(hid, non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            qb.qmoe_moe_forward(w.scheme, dims, dx, did, dw, t["w1"], t["w1_s"], t["w2"], t["w2_s"], dout, status,
+                                fws)
+            hout.copy_(dout, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier()
+        s2, e2 = ev(), ev()
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record(stream)
+        barrier()
+        ems = s2.elapsed_time(e2) / args.steps
+        if world > 1:
+            import torch.distributed as dist
+
+            tm = torch.tensor([ems], device=dev)
+            dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+            ems = float(tm.item())
+        h2d = hx.numel() * 2 + hid.numel() * 4 + hw.numel() * 4
+        e2e = dict(value=flops_step * world / (ems * 1e-3) / 1e12, unit=UNIT, ms_per_step=ems,
+                   h2d_bytes_per_step=h2d, d2h_bytes_per_step=hout.numel() * 2,
+                   api="qmoe_moe_forward (C ABI) with pinned host buffers")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, tps, cores, sample = cpu_oracle_rate(wr, d, args.cpu_seconds)
+        cpu = dict(value=fl / 1e12, unit=UNIT, cores=cores, kind="oracle", sample=sample, tokens_per_s=tps)
+
+    if rank == 0:
+        line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                    ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype=dict(
+                        mxfp4="e4m3 x e2m1 (fp32 accumulate)", w4a16="bf16 (fp32 accumulate)",
+                        w8a8="int8 (int32 accumulate)")[w.scheme], data="synthetic",
+                    config=dict(workload=w.name, scheme=w.scheme, T=T, H=H, E=E, k=k, I=I,
+                                experts_touched=alg["experts_touched"],
+                                l2="inputs larger than L2: each step streams the touched experts' weights "
+                                   f"({(alg['gemm1_bytes'] + alg['gemm2_bytes']) / 1e9:.2f} GB)",
+                                parallelism=f"replicas x{world}"),
+                    tokens_per_s=tokens_per_s, roofline=roof, cpu_baseline=cpu, e2e=e2e,
+                    gpu_launches=launches_per_step * args.steps, clocks=clk)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

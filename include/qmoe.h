@@ -1,0 +1,217 @@
+/*
+ * qmoe.h -- C ABI of the GB300 (sm_103a) quantized Mixture-of-Experts expert
+ * path: routed top-k pairs -> expert-sorted order -> grouped gate/up GEMM with
+ * fused SwiGLU -> grouped down GEMM over packed low-bit expert weights ->
+ * top-k-weighted combine in a fixed order.
+ *
+ * Sources the operations follow:
+ *   [hip-ep]  "perf(qmoe): group prefill expert matmuls" -- description:
+ *             grouped expert projections over symmetric int4 weights, one
+ *             launch for all experts, deterministic scatter order.
+ *   [gfx1151] "Evaluate native IU4/IU8 WMMA for grouped-INT MoE prefill on
+ *             gfx1151" -- Problem (dequantise-then-dot for W4A16, decode is
+ *             GEMV-like), Constraint (int8 x int8 -> int32 needs quantised
+ *             activations: W8A8).
+ *   [aiter]   the tuned grouped-fmoe config page for an MXFP4 model on
+ *             gfx1250 -- Changes (fp8 activations, MXFP4 weights, two-stage
+ *             grouped kernel), Test Plan (stage1/stage2 tiles, rel L2 check,
+ *             K tiles larger than inter_dim excluded).
+ *
+ * Notation: T tokens, k = top_k, P = T*k routed pairs (pair p = t*k + j),
+ * H hidden size, I intermediate size, E experts.  A "slot" is a position in
+ * expert-sorted order; slot-ordered buffers hold one row per valid pair.
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers unless stated otherwise.  The
+ *     caller owns every buffer, including the workspace; the library never
+ *     allocates, frees or synchronises (except qmoe_moe_forward_host, which
+ *     is documented below).
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *   - Host-side checks run before any launch: a NULL pointer, a dimension
+ *     <= 0 (T may be 0), H or I not a multiple of 32, or a pointer not
+ *     16-byte aligned returns QMOE_ERR_ARG; shapes beyond the kernels'
+ *     limits return QMOE_ERR_UNSUPPORTED; a failed launch returns
+ *     QMOE_ERR_LAUNCH.  Nothing is launched after an error.
+ *   - Device-side errors never trap: a routing id outside [0, E) sets bit
+ *     QMOE_DEV_BAD_EXPERT_ID of *dev_status (which the caller zeroes before
+ *     the first call and reads after synchronising); that pair then takes no
+ *     slot and contributes nothing to the output.
+ *   - Calls on different streams are independent when they use different
+ *     output and workspace buffers.
+ *
+ * Storage formats (K = the reduction axis, always contiguous):
+ *   bf16      uint16 bit patterns.
+ *   int4      W [rows, K/2] bytes; element 2i in the low nibble of byte i,
+ *             2i+1 in the high nibble; stored n = q + 8, value (n - 8) * s;
+ *             scales fp16 [rows, K/32].
+ *   E2M1      same nibble order; OCP MX element encoding; scales E8M0
+ *             [rows, K/32] (value 2^(b-127)).
+ *   E4M3      OCP "fn" fp8 (max 448, no infinities).
+ *   int8      W int8 [rows, K], fp32 scale per output row.
+ * Weight tensors: W1 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up), W2 [E, H, I].
+ */
+#ifndef QMOE_H
+#define QMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* qmoe_stream_t;
+
+typedef enum {
+    QMOE_OK = 0,
+    QMOE_ERR_ARG = -1,
+    QMOE_ERR_UNSUPPORTED = -2,
+    QMOE_ERR_LAUNCH = -3,
+    QMOE_ERR_CUDA = -4
+} qmoe_status;
+
+/* Bits of the device status word. */
+enum { QMOE_DEV_BAD_EXPERT_ID = 1, QMOE_DEV_WAIT_TIMEOUT = 2 };
+
+typedef struct {
+    int32_t T, k, H, I, E;
+} qmoe_dims;
+
+/* Human-readable name of a qmoe_status code (static string). */
+const char* qmoe_status_str(int code);
+
+/* Library version string (static). */
+const char* qmoe_version(void);
+
+/* ---------------------------------------------------------------- routing
+ *
+ * Bytes of device workspace the routing and GEMM calls need for dims *d
+ * (scratch for per-chunk histograms and the GEMM tile schedule). */
+size_t qmoe_workspace_bytes(const qmoe_dims* d);
+
+/* qmoe_align_sort -- expert-sorted permutation of the routed pairs.
+ * [hip-ep] description ("grouped" launches with a "deterministic scatter
+ * order"); [aiter] Changes (two-stage grouped kernel over sorted tokens).
+ *
+ * in   topk_ids        int32 [T, k], expert id of pair p = t*k + j
+ * out  counts          int32 [E], pairs routed to each expert
+ * out  offsets         int32 [E+1], exclusive prefix sum of counts;
+ *                      offsets[E] = number of valid pairs
+ * out  sorted_pair_ids int32 [P]; slot s -> pair id, ascending p within an
+ *                      expert (a stable sort); slots >= offsets[E] hold -1
+ * out  pair_slot       int32 [P]; pair id -> slot, -1 for an invalid id
+ * i/o  dev_status      int32 [1]; bit QMOE_DEV_BAD_EXPERT_ID is OR-ed in
+ * ws   workspace of qmoe_workspace_bytes(d) bytes, 256-byte aligned
+ * The result is bit-identical run to run (no atomics decide an order). */
+int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+                    int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, void* ws,
+                    size_t ws_bytes, qmoe_stream_t stream);
+
+/* ---------------------------------------------------------------- activation quantisation
+ *
+ * qmoe_quant_act_mxfp8 -- bf16 rows to E4M3 codes with one E8M0 scale per 32
+ * consecutive columns (the fp8 activations of [aiter] Changes).  Per block:
+ * X = 2^(floor(log2 amax) - 8), code = nearest-even E4M3 of v / X saturated
+ * to +-448; amax = 0 gives scale byte 127 and zero codes (OCP MX v1.0).
+ * in x_bf16 [rows, cols]; out x_q uint8 [rows, cols], x_s uint8 [rows, cols/32].
+ * cols must be a multiple of 32. */
+int qmoe_quant_act_mxfp8(int64_t rows, int64_t cols, const uint16_t* x_bf16, uint8_t* x_q, uint8_t* x_s,
+                         qmoe_stream_t stream);
+
+/* qmoe_quant_rows_int8_{bf16,f32} -- per-row symmetric int8 quantisation,
+ * the activation-quantised W8A8 scheme of [gfx1151] Constraint: s = amax/127
+ * (1 when amax = 0), q = clamp(rint(v / s), -127, 127), all in fp32.
+ * in x [rows, cols] (bf16 bits or fp32); out q int8 [rows, cols], s fp32 [rows]. */
+int qmoe_quant_rows_int8_bf16(int64_t rows, int64_t cols, const uint16_t* x, int8_t* q, float* s,
+                              qmoe_stream_t stream);
+int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t* q, float* s,
+                             qmoe_stream_t stream);
+
+/* ---------------------------------------------------------------- stage 1: gate/up + SwiGLU
+ *
+ * For every expert e and slot s in [offsets[e], offsets[e+1]), with
+ * a = the activation row of token sorted_pair_ids[s] / k:
+ *   g[n] = W1[e][n] . a,  u[n] = W1[e][I+n] . a,  h[s][n] = silu(g[n]) * u[n]
+ * for n < I, silu(v) = v / (1 + exp(-v)); then h is quantised per scheme.
+ * [hip-ep] description (grouped projections, all experts in one launch);
+ * [aiter] Changes/Test Plan (stage 1 of the grouped a8w4 kernel).
+ * Only slots < offsets[E] are written.
+ *
+ * W4A16: x bf16 [T, H]; w1 int4 [E, 2I, H/2]; w1_s fp16 [E, 2I, H/32];
+ *        out h bf16 [P, I] (round to nearest even from fp32). */
+int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const uint8_t* w1, const uint16_t* w1_s,
+                            const int32_t* offsets, const int32_t* sorted_pair_ids, uint16_t* h_bf16, void* ws,
+                            size_t ws_bytes, qmoe_stream_t stream);
+
+/* MXFP4 x FP8: x_q E4M3 [T, H] + x_s E8M0 [T, H/32] (from qmoe_quant_act_mxfp8);
+ *        w1 E2M1 [E, 2I, H/2]; w1_s E8M0 [E, 2I, H/32];
+ *        out h_q E4M3 [P, I] + h_s E8M0 [P, I/32]: the fp32 h quantised with
+ *        the rule of qmoe_quant_act_mxfp8 along I. */
+int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1,
+                            const uint8_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
+                            uint8_t* h_q, uint8_t* h_s, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+
+/* W8A8: x_q int8 [T, H] + x_s fp32 [T] (from qmoe_quant_rows_int8_bf16);
+ *        w1 int8 [E, 2I, H]; w1_s fp32 [E, 2I].  Accumulation is exact int32;
+ *        g = ((float)acc * x_s[t]) * w1_s[e][n] in fp32, likewise u;
+ *        out h fp32 [P, I]; dbg_acc (nullable) int32 [P, 2I] receives the raw
+ *        gate/up accumulators. */
+int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x_s, const int8_t* w1,
+                           const float* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids, float* h,
+                           int32_t* dbg_acc, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+
+/* ---------------------------------------------------------------- stage 2: down projection
+ *
+ * y[s][c] = W2[e][c] . hq[s] for c < H, slots of expert e as above; y fp32
+ * [P, H] in slot order.  [aiter] Test Plan ("stage2 tiles"; K tiles larger
+ * than inter_dim read out of bounds, so the kernels never let a K tile pass
+ * the end of I).
+ *
+ * W4A16: h bf16 [P, I]; w2 int4 [E, H, I/2]; w2_s fp16 [E, H, I/32]. */
+int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
+                     const int32_t* offsets, float* y, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+
+/* MXFP4 x FP8: h_q E4M3 [P, I] + h_s E8M0 [P, I/32]; w2 E2M1 [E, H, I/2];
+ *        w2_s E8M0 [E, H, I/32]. */
+int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2,
+                     const uint8_t* w2_s, const int32_t* offsets, float* y, void* ws, size_t ws_bytes,
+                     qmoe_stream_t stream);
+
+/* W8A8: h_q int8 [P, I] + h_s fp32 [P] (qmoe_quant_rows_int8_f32 of h);
+ *        w2 int8 [E, H, I]; w2_s fp32 [E, H]; y = ((float)acc * h_s[s]) * w2_s[e][c];
+ *        dbg_acc (nullable) int32 [P, H]. */
+int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2, const float* w2_s,
+                    const int32_t* offsets, float* y, int32_t* dbg_acc, void* ws, size_t ws_bytes,
+                    qmoe_stream_t stream);
+
+/* ---------------------------------------------------------------- combine
+ *
+ * qmoe_combine -- out[t][c] = bf16( sum_{j=0..k-1} topk_w[t][j] * y[pair_slot[t*k+j]][c] ),
+ * summed in fp32 with j ascending from 0 (a fixed order, so the result is
+ * reproducible bit for bit: [hip-ep] description, "deterministic scatter
+ * order").  Pairs with pair_slot = -1 contribute nothing.
+ * in y fp32 [P, H] (slot order), topk_w fp32 [T, k], pair_slot int32 [P];
+ * out out_bf16 [T, H]. */
+int qmoe_combine(const qmoe_dims* d, const float* y, const float* topk_w, const int32_t* pair_slot,
+                 uint16_t* out_bf16, qmoe_stream_t stream);
+
+/* ---------------------------------------------------------------- whole layer
+ *
+ * One call for the whole path: routing, activation quantisation (MXFP4,
+ * W8A8), stage 1, intermediate quantisation (W8A8), stage 2 and combine, all
+ * launched in order on `stream`.  scheme: 0 = W4A16, 1 = MXFP4 x FP8,
+ * 2 = W8A8.  Weights and scales as for the per-stage calls.  All
+ * intermediates live in the caller's workspace of
+ * qmoe_forward_workspace_bytes(d, scheme) bytes (256-byte aligned).
+ * dev_status as for qmoe_align_sort. */
+size_t qmoe_forward_workspace_bytes(const qmoe_dims* d, int scheme);
+int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* topk_ids,
+                     const float* topk_w, const void* w1, const void* w1_s, const void* w2, const void* w2_s,
+                     uint16_t* out_bf16, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMOE_H */

@@ -73,6 +73,8 @@ def lib():
         L.oracle_moe_forward.argtypes = [i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp,
                                          vp, vp, vp, vp, vp]
         L.oracle_moe_forward.restype = i64
+        L.oracle_combine.argtypes = [i64, i32, i32, vp, vp, vp, vp]
+        L.oracle_combine.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = i32
         _lib = L
@@ -205,3 +207,14 @@ def stage2(scheme: str, H: int, I: int, E: int, experts, h, h_s, w2, w2_s, acc: 
     if rc != 0:
         raise RuntimeError(f"oracle_stage2 failed: {rc}")
     return (y, acc2) if acc else y
+
+
+def combine(y: np.ndarray, topk_w: np.ndarray, pair_slot: np.ndarray):
+    """Top-k weighted sum of fp32 rows y[slot] (j ascending, double)."""
+    T, k = topk_w.shape
+    H = y.shape[1]
+    out = np.zeros((T, H), np.float64)
+    c = lambda a, dt: np.ascontiguousarray(a, dtype=dt)
+    lib().oracle_combine(T, k, H, _p(c(y, np.float32)), _p(c(topk_w, np.float32)), _p(c(pair_slot, np.int32)),
+                         _p(out))
+    return out

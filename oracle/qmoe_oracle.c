@@ -475,3 +475,20 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* The top-k weighted sum on its own: out[t][c] = sum_j w[t][j] * y[slot][c],
+ * slot = pair_slot[t*k + j] (skipped when -1), j ascending, in double.
+ * y fp32 [rows, H]; out double [T, H]. */
+void oracle_combine(int64_t T, int k, int H, const float* y, const float* topk_w, const int32_t* pair_slot,
+                    double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int c = 0; c < H; ++c) out[t * H + c] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int32_t s = pair_slot[t * k + j];
+            if (s < 0) continue;
+            double w = (double)topk_w[t * k + j];
+            for (int c = 0; c < H; ++c) out[t * H + c] += w * (double)y[(int64_t)s * H + c];
+        }
+    }
+}

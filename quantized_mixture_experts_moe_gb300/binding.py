@@ -1,0 +1,215 @@
+"""Thin ctypes binding over libqmoe.so (declared in include/qmoe.h).
+
+Argument marshalling only: every function passes device pointers of torch
+tensors, the sizes and the current CUDA stream to the C entry point of the
+same name and raises QmoeError on a non-zero status.  There is no fallback:
+when the CUDA library is missing or fails to load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmoe.so")
+
+SCHEME_ID = {"w4a16": 0, "mxfp4": 1, "w8a8": 2}
+DEV_BAD_EXPERT_ID = 1
+DEV_WAIT_TIMEOUT = 2
+
+
+class QmoeError(RuntimeError):
+    pass
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("k", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("E", ctypes.c_int32)]
+
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_DP = ctypes.POINTER(Dims)
+
+# name -> (argtypes, restype)
+SIGNATURES = {
+    "qmoe_status_str": ([_i32], ctypes.c_char_p),
+    "qmoe_version": ([], ctypes.c_char_p),
+    "qmoe_workspace_bytes": ([_DP], _sz),
+    "qmoe_align_sort": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_quant_act_mxfp8": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
+    "qmoe_quant_rows_int8_bf16": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
+    "qmoe_quant_rows_int8_f32": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
+    "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_combine": ([_DP, _vp, _vp, _vp, _vp, _vp], _i32),
+    "qmoe_forward_workspace_bytes": ([_DP, _i32], _sz),
+    "qmoe_moe_forward": ([_i32, _DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+}
+
+_lib = None
+
+
+def lib():
+    """Load libqmoe.so (raises when it is missing: there is no CPU path)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise QmoeError(f"{LIB_PATH} is not built; run quantized_mixture_experts_moe_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise QmoeError("qmoe kernels take device tensors")
+    if not t.is_contiguous():
+        raise QmoeError("qmoe kernels take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise QmoeError(f"{name} failed: {rc} ({lib().qmoe_status_str(rc).decode()})")
+
+
+def dims(T, k, H, I, E) -> Dims:
+    return Dims(T, k, H, I, E)
+
+
+def status_str(code: int) -> str:
+    return lib().qmoe_status_str(code).decode()
+
+
+def version() -> str:
+    return lib().qmoe_version().decode()
+
+
+def workspace_bytes(d: Dims) -> int:
+    return int(lib().qmoe_workspace_bytes(ctypes.byref(d)))
+
+
+def forward_workspace_bytes(d: Dims, scheme: str) -> int:
+    return int(lib().qmoe_forward_workspace_bytes(ctypes.byref(d), SCHEME_ID[scheme]))
+
+
+def qmoe_align_sort(d, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status, ws, stream=None):
+    rc = lib().qmoe_align_sort(ctypes.byref(d), _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(sorted_pair_ids),
+                               _ptr(pair_slot), _ptr(dev_status), _ptr(ws), ws.numel() * ws.element_size(),
+                               _stream(stream))
+    _check(rc, "qmoe_align_sort")
+
+
+def qmoe_quant_act_mxfp8(x_bf16, x_q, x_s, stream=None):
+    rows, cols = x_bf16.shape
+    _check(lib().qmoe_quant_act_mxfp8(rows, cols, _ptr(x_bf16), _ptr(x_q), _ptr(x_s), _stream(stream)),
+           "qmoe_quant_act_mxfp8")
+
+
+def qmoe_quant_rows_int8_bf16(x, q, s, stream=None):
+    rows, cols = x.shape
+    _check(lib().qmoe_quant_rows_int8_bf16(rows, cols, _ptr(x), _ptr(q), _ptr(s), _stream(stream)),
+           "qmoe_quant_rows_int8_bf16")
+
+
+def qmoe_quant_rows_int8_f32(x, q, s, stream=None):
+    rows, cols = x.shape
+    _check(lib().qmoe_quant_rows_int8_f32(rows, cols, _ptr(x), _ptr(q), _ptr(s), _stream(stream)),
+           "qmoe_quant_rows_int8_f32")
+
+
+def _ws(ws):
+    return _ptr(ws), (0 if ws is None else ws.numel() * ws.element_size())
+
+
+def qmoe_gemm1_swiglu_w4a16(d, x, w1, w1_s, offsets, sorted_pair_ids, h, ws=None, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), _ptr(x), _ptr(w1), _ptr(w1_s), _ptr(offsets),
+                                         _ptr(sorted_pair_ids), _ptr(h), wp, wn, _stream(stream)),
+           "qmoe_gemm1_swiglu_w4a16")
+
+
+def qmoe_gemm1_swiglu_mxfp4(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, ws=None, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_mxfp4(ctypes.byref(d), _ptr(x_q), _ptr(x_s), _ptr(w1), _ptr(w1_s), _ptr(offsets),
+                                         _ptr(sorted_pair_ids), _ptr(h_q), _ptr(h_s), wp, wn, _stream(stream)),
+           "qmoe_gemm1_swiglu_mxfp4")
+
+
+def qmoe_gemm1_swiglu_w8a8(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h, dbg_acc=None, ws=None, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_w8a8(ctypes.byref(d), _ptr(x_q), _ptr(x_s), _ptr(w1), _ptr(w1_s), _ptr(offsets),
+                                        _ptr(sorted_pair_ids), _ptr(h), _ptr(dbg_acc), wp, wn, _stream(stream)),
+           "qmoe_gemm1_swiglu_w8a8")
+
+
+def qmoe_gemm2_w4a16(d, h, w2, w2_s, offsets, y, ws=None, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm2_w4a16(ctypes.byref(d), _ptr(h), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y), wp, wn,
+                                  _stream(stream)), "qmoe_gemm2_w4a16")
+
+
+def qmoe_gemm2_mxfp4(d, h_q, h_s, w2, w2_s, offsets, y, ws=None, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm2_mxfp4(ctypes.byref(d), _ptr(h_q), _ptr(h_s), _ptr(w2), _ptr(w2_s), _ptr(offsets),
+                                  _ptr(y), wp, wn, _stream(stream)), "qmoe_gemm2_mxfp4")
+
+
+def qmoe_gemm2_w8a8(d, h_q, h_s, w2, w2_s, offsets, y, dbg_acc=None, ws=None, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm2_w8a8(ctypes.byref(d), _ptr(h_q), _ptr(h_s), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
+                                 _ptr(dbg_acc), wp, wn, _stream(stream)), "qmoe_gemm2_w8a8")
+
+
+def qmoe_combine(d, y, topk_w, pair_slot, out, stream=None):
+    _check(lib().qmoe_combine(ctypes.byref(d), _ptr(y), _ptr(topk_w), _ptr(pair_slot), _ptr(out), _stream(stream)),
+           "qmoe_combine")
+
+
+def qmoe_moe_forward(scheme, d, x, topk_ids, topk_w, w1, w1_s, w2, w2_s, out, dev_status, ws, stream=None):
+    rc = lib().qmoe_moe_forward(SCHEME_ID[scheme], ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w1),
+                                _ptr(w1_s), _ptr(w2), _ptr(w2_s), _ptr(out), _ptr(dev_status), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "qmoe_moe_forward")
+
+
+# ------------------------------------------------------------------ conveniences (torch allocation only)
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte-aligned byte workspace (torch allocations are 512-aligned)."""
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def moe_forward(scheme, x, topk_ids, topk_w, w1, w1_s, w2, w2_s, H=None, I=None, E=None, ws=None, stream=None):
+    """Whole layer through qmoe_moe_forward; returns (out bf16-bits [T, H], dev_status)."""
+    T, H_ = x.shape
+    k = topk_ids.shape[1]
+    E_ = w1.shape[0] if E is None else E
+    I_ = (w1.shape[1] // 2) if I is None else I
+    d = dims(T, k, H_, I_, E_)
+    if ws is None:
+        ws = alloc_workspace(forward_workspace_bytes(d, scheme), x.device)
+    out = torch.empty((T, H_), dtype=torch.int16, device=x.device)
+    status = torch.zeros(1, dtype=torch.int32, device=x.device)
+    qmoe_moe_forward(scheme, d, x, topk_ids, topk_w, w1, w1_s, w2, w2_s, out, status, ws, stream)
+    return out, status

@@ -1,0 +1,187 @@
+// Expert-sorted permutation of routed top-k pairs (qmoe_align_sort).
+//
+// Grouping all experts' projections into one launch needs the pairs ordered by
+// expert, and the scatter back must keep a deterministic order ("perf(qmoe):
+// group prefill expert matmuls", description).  The order here is the stable
+// one: within an expert, slots follow ascending pair id p = t*k + j.
+//
+// Three launches, none of which lets an atomic decide an order:
+//   1. hist:    each warp owns a contiguous chunk of kChunk pairs and builds
+//               its per-expert histogram in shared memory (warp match-any
+//               groups equal ids; the group leader adds the group size).
+//   2. scan:    one CTA turns the [chunk][expert] histograms into per-chunk
+//               base slots (exclusive over chunks within an expert, plus the
+//               expert's offset) and writes counts and offsets.
+//   3. scatter: each warp walks its chunk again in 32-pair steps; a pair's
+//               slot is its chunk base + the running count of earlier equal
+//               ids, so the result is the stable counting sort.
+#include "qmoe_common.cuh"
+
+namespace qmoe {
+
+constexpr int kChunk = 2048;          // pairs per warp chunk
+constexpr int kWarpsPerCta = 8;       // warps (chunks) per CTA in hist/scatter
+constexpr int kMaxExperts = 4096;     // shared-memory histogram bound
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+align_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks, int32_t* __restrict__ hist,
+                  int32_t* __restrict__ dev_status) {
+    extern __shared__ int32_t smem_hist[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x * kWarpsPerCta + warp;
+    int32_t* h = smem_hist + (size_t)warp * E;
+    for (int e = lane; e < E; e += 32) h[e] = 0;
+    __syncwarp();
+    if (chunk >= nchunks) return;
+    bool bad = false;
+    const int64_t p0 = (int64_t)chunk * kChunk;
+    for (int step = 0; step < kChunk / 32; ++step) {
+        const int64_t p = p0 + step * 32 + lane;
+        int e = -1;
+        if (p < P) e = ids[p];
+        const bool valid = (e >= 0 && e < E);
+        bad |= (p < P) && !valid;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+        if (valid && (peers & lanemask_lt()) == 0) h[e] += __popc(peers);
+        __syncwarp();
+    }
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(dev_status, QMOE_DEV_BAD_EXPERT_ID);
+    int32_t* out = hist + (size_t)chunk * E;
+    for (int e = lane; e < E; e += 32) out[e] = h[e];
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int32_t* __restrict__ counts,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t total_valid;
+    const int tid = threadIdx.x;
+    const int per = (E + kScanThreads - 1) / kScanThreads;
+    const int e0 = tid * per, e1 = min(E, e0 + per);
+    // per-expert totals, chunk bases made exclusive over chunks
+    int local = 0;
+    for (int e = e0; e < e1; ++e) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            int32_t v = hist[(size_t)c * E + e];
+            hist[(size_t)c * E + e] = run;
+            run += v;
+        }
+        counts[e] = run;
+        local += run;
+    }
+    // exclusive block scan of the per-thread expert sums
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+        int wi = w;
+        for (int o = 1; o < 32; o <<= 1) {
+            int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += v;
+        }
+        warp_sums[lane] = wi - w;
+        if (lane == 31) total_valid = wi;
+    }
+    __syncthreads();
+    int base = warp_sums[warp] + incl - local;
+    for (int e = e0; e < e1; ++e) {
+        offsets[e] = base;
+        for (int c = 0; c < nchunks; ++c) hist[(size_t)c * E + e] += base;
+        base += counts[e];
+    }
+    if (tid == 0) offsets[E] = total_valid;
+    for (int64_t s = (int64_t)total_valid + tid; s < P; s += kScanThreads) sorted_pair_ids[s] = -1;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
+                     const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_pair_ids,
+                     int32_t* __restrict__ pair_slot) {
+    extern __shared__ int32_t smem_cursor[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x * kWarpsPerCta + warp;
+    if (chunk >= nchunks) return;
+    int32_t* cur = smem_cursor + (size_t)warp * E;
+    const int32_t* base = hist + (size_t)chunk * E;
+    for (int e = lane; e < E; e += 32) cur[e] = base[e];
+    __syncwarp();
+    const int64_t p0 = (int64_t)chunk * kChunk;
+    for (int step = 0; step < kChunk / 32; ++step) {
+        const int64_t p = p0 + step * 32 + lane;
+        if (p0 + step * 32 >= P) break;  // warp-uniform
+        int e = -1;
+        if (p < P) e = ids[p];
+        const bool valid = (e >= 0 && e < E);
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+        int slot = -1;
+        if (valid) slot = cur[e] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (valid && (peers & lanemask_lt()) == 0) cur[e] += __popc(peers);
+        __syncwarp();
+        if (p < P) {
+            pair_slot[p] = slot;
+            if (valid) sorted_pair_ids[slot] = (int32_t)p;
+        }
+    }
+}
+
+size_t align_ws_bytes(int64_t P, int E) {
+    const int64_t nchunks = (P + kChunk - 1) / kChunk;
+    return (size_t)((nchunks * E * 4 + 255) / 256 * 256);
+}
+
+int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                      int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
+                      cudaStream_t stream) {
+    const int nchunks = (int)((P + kChunk - 1) / kChunk);
+    const size_t smem = (size_t)kWarpsPerCta * E * sizeof(int32_t);
+    const int ctas = (nchunks + kWarpsPerCta - 1) / kWarpsPerCta;
+    if (smem > 48 * 1024) {
+        cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    }
+    if (ctas > 0) align_hist_kernel<<<ctas, kWarpsPerCta * 32, smem, stream>>>(ids, P, E, nchunks, hist, dev_status);
+    align_scan_kernel<<<1, kScanThreads, 0, stream>>>(hist, P, E, nchunks, counts, offsets, sorted_pair_ids);
+    if (ctas > 0)
+        align_scatter_kernel<<<ctas, kWarpsPerCta * 32, smem, stream>>>(ids, P, E, nchunks, hist, sorted_pair_ids,
+                                                                         pair_slot);
+    return launch_status();
+}
+
+}  // namespace qmoe
+
+extern "C" size_t qmoe_workspace_bytes(const qmoe_dims* d) {
+    if (!qmoe::dims_ok(d)) return 0;
+    const int64_t P = (int64_t)d->T * d->k;
+    // histograms + room for the GEMM schedule (tile offsets over experts)
+    return qmoe::align_ws_bytes(P, d->E) + (size_t)((d->E + 1 + 64) * 4 + 255) / 256 * 256;
+}
+
+extern "C" int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+                               int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, void* ws,
+                               size_t ws_bytes, qmoe_stream_t stream) {
+    using namespace qmoe;
+    if (!dims_ok(d)) return QMOE_ERR_ARG;
+    const int64_t P = (int64_t)d->T * d->k;
+    if (!counts || !offsets || !dev_status || !ws) return QMOE_ERR_ARG;
+    if (P > 0 && (!topk_ids || !sorted_pair_ids || !pair_slot)) return QMOE_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return QMOE_ERR_ARG;
+    if (d->E > kMaxExperts) return QMOE_ERR_UNSUPPORTED;
+    if (ws_bytes < align_ws_bytes(P, d->E)) return QMOE_ERR_ARG;
+    return align_sort_launch(P, d->E, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status,
+                             static_cast<int32_t*>(ws), (cudaStream_t)stream);
+}

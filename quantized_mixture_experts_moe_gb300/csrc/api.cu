@@ -1,0 +1,207 @@
+// C-ABI entry points of the grouped expert GEMMs, status strings and the
+// whole-layer call.  Argument checks run on the host before any launch.
+#include "qmoe_common.cuh"
+#include "gemm_simt.cuh"
+
+namespace qmoe {
+size_t align_ws_bytes(int64_t P, int E);
+int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                      int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
+                      cudaStream_t stream);
+int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
+template <typename In>
+int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float* s, cudaStream_t st);
+int combine_launch(const qmoe_dims* d, const float* y, const float* topk_w, const int32_t* pair_slot, uint16_t* out,
+                   cudaStream_t st);
+
+static int gemm_args_ok(const qmoe_dims* d, std::initializer_list<const void*> ptrs) {
+    if (!dims_ok(d)) return QMOE_ERR_ARG;
+    if ((int64_t)d->T * d->k == 0) return QMOE_OK;
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return QMOE_ERR_ARG;
+    return QMOE_OK;
+}
+
+static SimtArgs make_args(const qmoe_dims* d) {
+    SimtArgs a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    return a;
+}
+
+}  // namespace qmoe
+
+using namespace qmoe;
+
+extern "C" const char* qmoe_status_str(int code) {
+    switch (code) {
+        case QMOE_OK: return "ok";
+        case QMOE_ERR_ARG: return "invalid argument (null or misaligned pointer, bad dimension, small workspace)";
+        case QMOE_ERR_UNSUPPORTED: return "shape outside the kernels' limits";
+        case QMOE_ERR_LAUNCH: return "kernel launch failed";
+        case QMOE_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+extern "C" const char* qmoe_version(void) { return "qmoe-gb300 0.1 (sm_103a)"; }
+
+extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const uint8_t* w1,
+                                       const uint16_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
+                                       uint16_t* h_bf16, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    int rc = gemm_args_ok(d, {x_bf16, w1, w1_s, offsets, sorted_pair_ids, h_bf16});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    SimtArgs a = make_args(d);
+    a.act = x_bf16; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids; a.out = h_bf16;
+    return gemm_simt(0, 1, a, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1,
+                                       const uint8_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
+                                       uint8_t* h_q, uint8_t* h_s, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    SimtArgs a = make_args(d);
+    a.act = x_q; a.act_s = x_s; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids;
+    a.out = h_q; a.out_s = h_s;
+    return gemm_simt(1, 1, a, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x_s, const int8_t* w1,
+                                      const float* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
+                                      float* h, int32_t* dbg_acc, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
+    SimtArgs a = make_args(d);
+    a.act = x_q; a.act_s = x_s; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids;
+    a.out = h; a.dbg_acc = dbg_acc;
+    return gemm_simt(2, 1, a, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
+                                const int32_t* offsets, float* y, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    int rc = gemm_args_ok(d, {h_bf16, w2, w2_s, offsets, y});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    SimtArgs a = make_args(d);
+    a.act = h_bf16; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y;
+    return gemm_simt(0, 2, a, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2,
+                                const uint8_t* w2_s, const int32_t* offsets, float* y, void* ws, size_t ws_bytes,
+                                qmoe_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    SimtArgs a = make_args(d);
+    a.act = h_q; a.act_s = h_s; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y;
+    return gemm_simt(1, 2, a, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2,
+                               const float* w2_s, const int32_t* offsets, float* y, int32_t* dbg_acc, void* ws,
+                               size_t ws_bytes, qmoe_stream_t stream) {
+    (void)ws; (void)ws_bytes;
+    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
+    SimtArgs a = make_args(d);
+    a.act = h_q; a.act_s = h_s; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y; a.dbg_acc = dbg_acc;
+    return gemm_simt(2, 2, a, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ whole layer
+
+namespace {
+
+struct FwdLayout {
+    size_t counts, offsets, sorted, slot, xq, xs, h, hs, hq8, hs8, y, align_ws, total;
+};
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
+    const size_t T = d->T, P = (size_t)d->T * d->k, H = d->H, I = d->I, E = d->E;
+    FwdLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
+    L.counts = take(4 * E);
+    L.offsets = take(4 * (E + 1));
+    L.sorted = take(4 * P);
+    L.slot = take(4 * P);
+    L.xq = take(scheme == 0 ? 0 : T * H);
+    L.xs = take(scheme == 1 ? T * (H / 32) : (scheme == 2 ? 4 * T : 0));
+    L.h = take(scheme == 0 ? 2 * P * I : (scheme == 1 ? P * I : 4 * P * I));
+    L.hs = take(scheme == 1 ? P * (I / 32) : 0);
+    L.hq8 = take(scheme == 2 ? P * I : 0);
+    L.hs8 = take(scheme == 2 ? 4 * P : 0);
+    L.y = take(4 * P * H);
+    L.align_ws = take(qmoe_workspace_bytes(d));
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+
+extern "C" size_t qmoe_forward_workspace_bytes(const qmoe_dims* d, int scheme) {
+    if (!dims_ok(d) || scheme < 0 || scheme > 2) return 0;
+    return fwd_layout(d, scheme).total;
+}
+
+extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* topk_ids,
+                                const float* topk_w, const void* w1, const void* w1_s, const void* w2,
+                                const void* w2_s, uint16_t* out_bf16, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                qmoe_stream_t stream) {
+    if (!dims_ok(d) || scheme < 0 || scheme > 2) return QMOE_ERR_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || !dev_status) return QMOE_ERR_ARG;
+    const FwdLayout L = fwd_layout(d, scheme);
+    if (ws_bytes < L.total) return QMOE_ERR_ARG;
+    if (d->T > 0 && (!x_bf16 || !topk_ids || !topk_w || !w1 || !w1_s || !w2 || !w2_s || !out_bf16)) return QMOE_ERR_ARG;
+    char* base = static_cast<char*>(ws);
+    auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+    int32_t* counts = (int32_t*)at(L.counts);
+    int32_t* offsets = (int32_t*)at(L.offsets);
+    int32_t* sorted = (int32_t*)at(L.sorted);
+    int32_t* slot = (int32_t*)at(L.slot);
+    void* aws = at(L.align_ws);
+    const size_t aws_bytes = qmoe_workspace_bytes(d);
+    int rc = qmoe_align_sort(d, topk_ids, counts, offsets, sorted, slot, dev_status, aws, aws_bytes, stream);
+    if (rc != QMOE_OK) return rc;
+    if (d->T == 0) return QMOE_OK;
+    const int64_t P = (int64_t)d->T * d->k;
+    float* y = (float*)at(L.y);
+    if (scheme == 0) {
+        rc = qmoe_gemm1_swiglu_w4a16(d, x_bf16, (const uint8_t*)w1, (const uint16_t*)w1_s, offsets, sorted,
+                                     (uint16_t*)at(L.h), aws, aws_bytes, stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_gemm2_w4a16(d, (const uint16_t*)at(L.h), (const uint8_t*)w2, (const uint16_t*)w2_s, offsets, y,
+                                  aws, aws_bytes, stream);
+    } else if (scheme == 1) {
+        rc = qmoe_quant_act_mxfp8(d->T, d->H, x_bf16, (uint8_t*)at(L.xq), (uint8_t*)at(L.xs), stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_gemm1_swiglu_mxfp4(d, (const uint8_t*)at(L.xq), (const uint8_t*)at(L.xs), (const uint8_t*)w1,
+                                         (const uint8_t*)w1_s, offsets, sorted, (uint8_t*)at(L.h), (uint8_t*)at(L.hs),
+                                         aws, aws_bytes, stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_gemm2_mxfp4(d, (const uint8_t*)at(L.h), (const uint8_t*)at(L.hs), (const uint8_t*)w2,
+                                  (const uint8_t*)w2_s, offsets, y, aws, aws_bytes, stream);
+    } else {
+        rc = qmoe_quant_rows_int8_bf16(d->T, d->H, x_bf16, (int8_t*)at(L.xq), (float*)at(L.xs), stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_gemm1_swiglu_w8a8(d, (const int8_t*)at(L.xq), (const float*)at(L.xs), (const int8_t*)w1,
+                                        (const float*)w1_s, offsets, sorted, (float*)at(L.h), nullptr, aws, aws_bytes,
+                                        stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_quant_rows_int8_f32(P, d->I, (const float*)at(L.h), (int8_t*)at(L.hq8), (float*)at(L.hs8),
+                                          stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_gemm2_w8a8(d, (const int8_t*)at(L.hq8), (const float*)at(L.hs8), (const int8_t*)w2,
+                                 (const float*)w2_s, offsets, y, nullptr, aws, aws_bytes, stream);
+    }
+    if (rc != QMOE_OK) return rc;
+    return qmoe_combine(d, y, topk_w, slot, out_bf16, stream);
+}

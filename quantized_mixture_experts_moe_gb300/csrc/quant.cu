@@ -1,0 +1,125 @@
+// Activation / intermediate quantisation kernels.
+//
+//  * MX (E4M3 codes + one E8M0 scale per 32 columns) for the fp8 activations
+//    that feed the MXFP4 expert GEMMs (aiter tuned grouped-fmoe page,
+//    Changes: "fp8 act, MXFP4 weight").  Rule (OCP MX v1.0): per block,
+//    X = 2^(floor(log2 amax) - 8), code = nearest-even E4M3 of v / X,
+//    saturated to +-448; amax = 0 -> scale byte 127, zero codes.
+//  * Per-row symmetric int8 for the W8A8 scheme ("Evaluate native IU4/IU8
+//    WMMA ... on gfx1151", Constraint: integer MMAs need quantised
+//    activations): s = amax / 127 (1 if amax = 0), q = clamp(rint(v/s), +-127),
+//    all in fp32 with IEEE division.
+#include "qmoe_common.cuh"
+
+namespace qmoe {
+
+// One thread per 8 consecutive bf16 values; 4 lanes form one 32-block.
+__global__ void __launch_bounds__(256)
+quant_mx_bf16_kernel(const uint4* __restrict__ x, int64_t n8, uint2* __restrict__ q, uint8_t* __restrict__ s) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool active = i < n8;
+    uint4 v = active ? x[i] : make_uint4(0, 0, 0, 0);
+    float f[8];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = __uint_as_float(w[j] << 16);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    if (!active) return;
+    uint2 codes = make_uint2(0, 0);
+    uint8_t sb = 127;
+    if (amax > 0.f) {
+        const int X = mx_block_exponent(amax);
+        const float m = exp2i(-X);
+        sb = (uint8_t)(X + 127);
+        codes.x = (uint32_t)e4m3x2_from_float(f[0] * m, f[1] * m) | ((uint32_t)e4m3x2_from_float(f[2] * m, f[3] * m) << 16);
+        codes.y = (uint32_t)e4m3x2_from_float(f[4] * m, f[5] * m) | ((uint32_t)e4m3x2_from_float(f[6] * m, f[7] * m) << 16);
+    }
+    q[i] = codes;
+    if ((threadIdx.x & 3) == 0) s[i >> 2] = sb;
+}
+
+template <typename In>
+__device__ __forceinline__ float load_as_float(const In* p, int64_t i);
+template <>
+__device__ __forceinline__ float load_as_float<uint16_t>(const uint16_t* p, int64_t i) {
+    return bf16_bits_to_float(p[i]);
+}
+template <>
+__device__ __forceinline__ float load_as_float<float>(const float* p, int64_t i) {
+    return p[i];
+}
+
+// One CTA per row.
+template <typename In>
+__global__ void __launch_bounds__(256)
+quant_rows_int8_kernel(const In* __restrict__ x, int64_t cols, int8_t* __restrict__ q, float* __restrict__ s) {
+    __shared__ float red[8];
+    const int64_t row = blockIdx.x;
+    const In* xr = x + row * cols;
+    float amax = 0.f;
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) amax = fmaxf(amax, fabsf(load_as_float(xr, c)));
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+    const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+    int8_t* qr = q + row * cols;
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) {
+        float t = rintf(__fdiv_rn(load_as_float(xr, c), sc));
+        t = fminf(fmaxf(t, -127.f), 127.f);
+        qr[c] = (int8_t)(int)t;
+    }
+    if (threadIdx.x == 0) s[row] = sc;
+}
+
+int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st) {
+    const int64_t n8 = rows * cols / 8;
+    if (n8 == 0) return QMOE_OK;
+    const int64_t blocks = (n8 + 255) / 256;
+    quant_mx_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n8,
+                                                          reinterpret_cast<uint2*>(q), s);
+    return launch_status();
+}
+
+template <typename In>
+int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float* s, cudaStream_t st) {
+    if (rows == 0) return QMOE_OK;
+    quant_rows_int8_kernel<In><<<(unsigned)rows, 256, 0, st>>>(x, cols, q, s);
+    return launch_status();
+}
+template int quant_int8_launch<uint16_t>(int64_t, int64_t, const uint16_t*, int8_t*, float*, cudaStream_t);
+template int quant_int8_launch<float>(int64_t, int64_t, const float*, int8_t*, float*, cudaStream_t);
+
+}  // namespace qmoe
+
+extern "C" int qmoe_quant_act_mxfp8(int64_t rows, int64_t cols, const uint16_t* x_bf16, uint8_t* x_q, uint8_t* x_s,
+                                    qmoe_stream_t stream) {
+    using namespace qmoe;
+    if (rows < 0 || cols <= 0 || cols % 32 != 0 || rows > (1ll << 31)) return QMOE_ERR_ARG;
+    if (rows > 0 && (!x_bf16 || !x_q || !x_s || !aligned16(x_bf16) || !aligned16(x_q))) return QMOE_ERR_ARG;
+    return quant_mx_launch(rows, cols, x_bf16, x_q, x_s, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_quant_rows_int8_bf16(int64_t rows, int64_t cols, const uint16_t* x, int8_t* q, float* s,
+                                         qmoe_stream_t stream) {
+    using namespace qmoe;
+    if (rows < 0 || cols <= 0 || rows > (1ll << 31)) return QMOE_ERR_ARG;
+    if (rows > 0 && (!x || !q || !s)) return QMOE_ERR_ARG;
+    return quant_int8_launch<uint16_t>(rows, cols, x, q, s, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t* q, float* s,
+                                        qmoe_stream_t stream) {
+    using namespace qmoe;
+    if (rows < 0 || cols <= 0 || rows > (1ll << 31)) return QMOE_ERR_ARG;
+    if (rows > 0 && (!x || !q || !s)) return QMOE_ERR_ARG;
+    return quant_int8_launch<float>(rows, cols, x, q, s, (cudaStream_t)stream);
+}

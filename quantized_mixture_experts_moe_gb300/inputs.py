@@ -37,8 +37,9 @@ class Workload:
     E: int
     k: int
     I: int
-    routing: str  # "uniform" (k distinct experts per token), "zipf", or "skew"
-    seed: int
+    routing: str  # "uniform" (k distinct experts per token) or "zipf"
+    seed: int     # routing and activations
+    wseed: int    # expert weights (shared by the members of a T sweep)
 
     @property
     def P(self) -> int:
@@ -49,8 +50,8 @@ class Workload:
         return 6.0 * self.P * self.H * self.I
 
 
-def _mk(name, scheme, T, H, E, k, I, routing, seed):
-    return Workload(name, scheme, T, H, E, k, I, routing, seed)
+def _mk(name, scheme, T, H, E, k, I, routing, seed, wseed=None):
+    return Workload(name, scheme, T, H, E, k, I, routing, seed, seed if wseed is None else wseed)
 
 
 # Seeds are 1000 + the workload family index; sweep members add T.
@@ -60,12 +61,12 @@ WORKLOADS = {
         _mk("tiny_w4a16", "w4a16", 16, 256, 8, 2, 128, "uniform", 1000),
         _mk("w4a16_T2048", "w4a16", 2048, 2048, 128, 8, 768, "uniform", 1001),
         *[
-            _mk(f"mxfp4_T{T}", "mxfp4", T, 4096, 512, 10, 1024, "uniform", 1002 + T)
+            _mk(f"mxfp4_T{T}", "mxfp4", T, 4096, 512, 10, 1024, "uniform", 1002 + T, 1002)
             for T in (256, 1024, 4096, 8192)
         ],
         _mk("w8a8_T8192", "w8a8", 8192, 4096, 64, 8, 1408, "uniform", 1003),
         *[
-            _mk(f"decode_T{T}", "mxfp4", T, 4096, 512, 10, 1024, "zipf", 1004 + T)
+            _mk(f"decode_T{T}", "mxfp4", T, 4096, 512, 10, 1024, "zipf", 1004 + T, 1002)
             for T in (1, 4, 16, 64)
         ],
     ]
@@ -74,7 +75,7 @@ WORKLOADS = {
 
 def custom(name, scheme, T, H, E, k, I, routing="uniform", seed=7):
     """A workload outside the fixed table (small parity and edge cases)."""
-    return Workload(name, scheme, T, H, E, k, I, routing, seed)
+    return Workload(name, scheme, T, H, E, k, I, routing, seed, seed)
 
 
 def rng_for(w: Workload, stream: int = 0) -> np.random.Generator:
@@ -200,7 +201,7 @@ def make_weights(w: Workload):
 
     W1 is [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up), W2 is [E, H, I]; K is the
     last (contiguous) axis in both.  Packed 4-bit formats hold K/2 bytes/row."""
-    rng = rng_for(w, 3)
+    rng = np.random.Generator(np.random.PCG64([w.wseed, 3]))
     E, H, I = w.E, w.H, w.I
     if w.scheme == "w4a16":
         return dict(

@@ -1,0 +1,77 @@
+"""CPU checks of the C ABI: the CUDA library loads, exports every function
+include/qmoe.h declares, and rejects bad arguments on the host before any
+launch (these calls touch no GPU)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from quantized_mixture_experts_moe_gb300 import binding as qb
+from quantized_mixture_experts_moe_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(qmoe_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qb.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["qmoe_align_sort", "qmoe_gemm1_swiglu_w4a16", "qmoe_gemm1_swiglu_mxfp4", "qmoe_gemm1_swiglu_w8a8",
+                     "qmoe_gemm2_w4a16", "qmoe_gemm2_mxfp4", "qmoe_gemm2_w8a8", "qmoe_combine"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    assert set(declared_functions()) <= set(qb.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4):
+        assert qb.status_str(code)
+    assert "sm_103a" in qb.version()
+
+
+def test_workspace_bytes_host_only(lib):
+    d = qb.dims(4096, 10, 4096, 1024, 512)
+    n = qb.workspace_bytes(d)
+    assert n >= 4 * 512 * ((40960 + 2047) // 2048)
+    assert qb.forward_workspace_bytes(d, "mxfp4") > 40960 * 4096 * 4  # holds y
+    bad = qb.dims(16, 2, 250, 128, 8)  # H not a multiple of 32
+    assert qb.workspace_bytes(bad) == 0
+
+
+def test_host_checks_reject_before_launch(lib):
+    d = qb.dims(16, 2, 256, 128, 8)
+    null = None
+    # null pointers and bad dims return QMOE_ERR_ARG without touching the GPU
+    assert lib.qmoe_align_sort(ctypes.byref(d), null, null, null, null, null, null, null, 0, null) == -1
+    assert lib.qmoe_combine(ctypes.byref(d), null, null, null, null, null) == -1
+    bad = qb.dims(16, 2, 256, 100, 8)
+    assert lib.qmoe_gemm2_w4a16(ctypes.byref(bad), null, null, null, null, null, null, 0, null) == -1
+    assert lib.qmoe_quant_act_mxfp8(4, 48, null, null, null, null) == -1
+    misaligned = ctypes.c_void_p(0x1000 + 4)
+    ok = ctypes.c_void_p(0x1000)
+    assert lib.qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), misaligned, ok, ok, ok, ok, ok, null, 0, null) == -1
+    assert lib.qmoe_moe_forward(7, ctypes.byref(d), *([null] * 10), 0, null) == -1

@@ -1,0 +1,353 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: the permutation, offsets, activation quantisation codes, W8A8
+int32 accumulators (and the W8A8 down projection, whose fp32 dequantisation
+follows the same operation order on both sides).  Float outputs: relative L2
+below 5e-3 (rel L2 = ||gpu - oracle|| / ||oracle|| over all elements,
+computed in float64).  Intermediate quantisation codes are compared through
+their dequantised values plus a mismatch-rate bound, because fp32 and double
+intermediates may straddle a rounding boundary.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_mixture_experts_moe_gb300 import binding as qb
+from quantized_mixture_experts_moe_gb300 import inputs as gen
+from tests import gpu_pipeline as gp
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 5e-3
+
+
+def rel_l2(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.linalg.norm(ref)
+    return np.linalg.norm(got - ref) / (den if den > 0 else 1.0)
+
+
+def dims(w):
+    return (w.T, w.k, w.H, w.I, w.E)
+
+
+# ------------------------------------------------------------------ routing
+
+ROUTINGS = [
+    ("uniform_small", lambda r: gen.routing_uniform(r, 16, 8, 2), 8),
+    ("uniform_c3", lambda r: gen.routing_uniform(r, 4096, 512, 10), 512),
+    ("zipf_decode", lambda r: gen.routing_zipf(r, 64, 512, 10), 512),
+    ("single_token", lambda r: gen.routing_uniform(r, 1, 512, 10), 512),
+    ("ragged_loads", lambda r: gen.routing_with_counts(r, [0, 1, 127, 129, 0, 3], 2), 6),
+    ("many_chunks", lambda r: gen.routing_uniform(r, 8192, 64, 8), 64),
+    ("one_expert_hot", lambda r: np.zeros((5000, 1), np.int32), 4),
+]
+
+
+@pytest.mark.parametrize("name,make,E", ROUTINGS, ids=[r[0] for r in ROUTINGS])
+def test_align_sort_bit_exact(name, make, E):
+    ids = make(np.random.default_rng(42))
+    T, k = ids.shape
+    got = gp.align(ids, E, T, k)
+    ref = oracle.align_sort(ids, E)
+    for key in ("counts", "offsets", "sorted_pair_ids", "pair_slot"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert got["status"] == 0
+
+
+def test_align_sort_invalid_ids_set_status():
+    ids = np.array([[0, 5], [-1, 2], [9, 0], [3, 3]], np.int32)
+    got = gp.align(ids, 6, 4, 2)
+    ref = oracle.align_sort(ids, 6)
+    assert got["status"] & qb.DEV_BAD_EXPERT_ID
+    for key in ("counts", "offsets", "sorted_pair_ids", "pair_slot"):
+        assert np.array_equal(got[key], ref[key]), key
+
+
+def test_align_sort_empty():
+    got = gp.align(np.zeros((0, 4), np.int32), 16, 0, 4)
+    assert not got["counts"].any() and not got["offsets"].any()
+
+
+def test_align_sort_deterministic():
+    ids = gen.routing_uniform(np.random.default_rng(3), 4096, 512, 10)
+    a = gp.align(ids, 512, 4096, 10)
+    b = gp.align(ids, 512, 4096, 10)
+    assert all(np.array_equal(a[key], b[key]) for key in ("sorted_pair_ids", "pair_slot"))
+
+
+# ------------------------------------------------------------------ activation quantisation
+
+def _x(rows, cols, seed=0, zero_rows=()):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((rows, cols)).astype(np.float32) * rng.uniform(0.01, 30, (rows, 1)).astype(np.float32)
+    for r in zero_rows:
+        v[r] = 0
+    return gen.bf16_bits_from_f32(v)
+
+
+def test_quant_act_mxfp8_bit_exact():
+    x = _x(77, 4096, zero_rows=(3,))
+    x[5, 64:96] = 0x8000  # a block of negative zeros
+    xq, xs = gp.empty((77, 4096), torch.uint8), gp.empty((77, 128), torch.uint8)
+    qb.qmoe_quant_act_mxfp8(gp.dev(x), xq, xs)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_act("mxfp4", x)
+    assert np.array_equal(gp.host(xs), rs)
+    assert np.array_equal(gp.host(xq), rq)
+
+
+@pytest.mark.parametrize("src", ["bf16", "f32"])
+def test_quant_rows_int8_bit_exact(src):
+    rows, cols = 65, 1408
+    xb = _x(rows, cols, seed=1, zero_rows=(7,))
+    q, s = gp.empty((rows, cols), torch.int8), gp.empty(rows, torch.float32)
+    if src == "bf16":
+        qb.qmoe_quant_rows_int8_bf16(gp.dev(xb), q, s)
+        xf = gp.bf16_to_f64(xb).astype(np.float32)
+    else:
+        xf = (np.random.default_rng(2).standard_normal((rows, cols)) * 3).astype(np.float32)
+        xf[7] = 0
+        qb.qmoe_quant_rows_int8_f32(gp.dev(xf), q, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.int8_quant(xf)
+    assert np.array_equal(gp.host(s), rs)
+    assert np.array_equal(gp.host(q), rq)
+
+
+# ------------------------------------------------------------------ stage 1
+
+S1_CASES = [
+    gen.custom("s1_w4a16", "w4a16", 40, 512, 6, 3, 192, seed=21),
+    gen.custom("s1_mxfp4", "mxfp4", 40, 512, 6, 3, 192, seed=22),
+    gen.custom("s1_w8a8", "w8a8", 40, 512, 6, 3, 192, seed=23),
+]
+
+
+@pytest.mark.parametrize("w", S1_CASES, ids=[w.name for w in S1_CASES])
+def test_stage1_against_oracle(w):
+    d = gen.make_all(w)
+    g = gp.run_layer(w, d, keep=True)
+    ref_out, dbg, _ = oracle.moe_forward(w.scheme, dims(w), d, debug=True)
+    ro = oracle.align_sort(d["topk_ids"], w.E)
+    assert np.array_equal(g["sorted_pair_ids"], ro["sorted_pair_ids"])
+    order = ro["sorted_pair_ids"]  # slot -> pair: oracle rows are pair-ordered
+    if w.scheme == "w4a16":
+        got = gp.bf16_to_f64(g["h"])
+        ref = gp.bf16_to_f64(dbg["hq"][order])
+        assert rel_l2(got, ref) < 1e-3
+    elif w.scheme == "mxfp4":
+        rq, rs = oracle.quant_act("mxfp4", d["x"])
+        assert np.array_equal(g["xq"], rq) and np.array_equal(g["xs"], rs)
+        deq = lambda q, s: np.vectorize(oracle.e4m3_to_double)(q) * np.repeat(np.exp2(s.astype(np.float64) - 127),
+                                                                              32, axis=1)
+        got = deq(g["hq"], g["hs"])
+        ref = deq(dbg["hq"][order], dbg["hs"][order])
+        assert rel_l2(got, ref) < REL_L2
+        assert np.mean(g["hq"] != dbg["hq"][order]) < 1e-3
+    else:
+        assert np.array_equal(g["acc1"], dbg["acc1"][order])
+        assert rel_l2(g["h"], dbg["h"][order]) < 1e-5
+    assert rel_l2(gp.bf16_to_f64(g["out"]), ref_out) < REL_L2
+
+
+# ------------------------------------------------------------------ stage 2 on generator intermediates
+
+S2_CASES = [
+    gen.custom("s2_w4a16", "w4a16", 1, 320, 5, 1, 256, seed=31),
+    gen.custom("s2_mxfp4", "mxfp4", 1, 320, 5, 1, 256, seed=32),
+    gen.custom("s2_w8a8", "w8a8", 1, 320, 5, 1, 256, seed=33),
+]
+
+
+@pytest.mark.parametrize("w", S2_CASES, ids=[w.name for w in S2_CASES])
+def test_stage2_against_oracle(w):
+    rows = 300
+    wts = gen.make_weights(w)
+    s2 = gen.make_stage2_inputs(w, rows)
+    experts = s2["experts"]
+    counts = np.bincount(experts, minlength=w.E).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    d = qb.dims(rows, 1, w.H, w.I, w.E)
+    y = gp.empty((rows, w.H), torch.float32)
+    t_off = gp.dev(offsets)
+    if w.scheme == "w4a16":
+        qb.qmoe_gemm2_w4a16(d, gp.dev(s2["h"]), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), t_off, y)
+        ref = oracle.stage2("w4a16", w.H, w.I, w.E, experts, s2["h"], None, wts["w2"], wts["w2_s"])
+        torch.cuda.synchronize()
+        assert rel_l2(gp.host(y), ref) < 1e-5
+    elif w.scheme == "mxfp4":
+        qb.qmoe_gemm2_mxfp4(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), t_off, y)
+        ref = oracle.stage2("mxfp4", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"])
+        torch.cuda.synchronize()
+        assert rel_l2(gp.host(y), ref) < 1e-5
+    else:
+        acc = gp.empty((rows, w.H), torch.int32)
+        qb.qmoe_gemm2_w8a8(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), t_off, y,
+                           acc)
+        ref, racc = oracle.stage2("w8a8", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"],
+                                  acc=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(gp.host(acc), racc)
+        assert np.array_equal(gp.host(y).astype(np.float64), ref)
+
+
+def test_w8a8_adversarial_accumulators_exact():
+    # all-+-127 operands: the largest-magnitude int32 sums a K=4096 row makes
+    w = gen.custom("adv", "w8a8", 1, 4096, 2, 1, 1024, seed=5)
+    rows = 64
+    h = np.full((rows, w.I), 127, np.int8)
+    h[1::2] = -127
+    w2 = np.full((w.E, w.H, w.I), 127, np.int8)
+    w2[:, ::3] = -127
+    hs = np.full(rows, 1e-3, np.float32)
+    w2s = np.full((w.E, w.H), 1e-3, np.float32)
+    experts = np.repeat(np.arange(w.E, dtype=np.int32), rows // w.E)
+    offsets = np.array([0, rows // 2, rows], np.int32)
+    d = qb.dims(rows, 1, w.H, w.I, w.E)
+    y, acc = gp.empty((rows, w.H), torch.float32), gp.empty((rows, w.H), torch.int32)
+    qb.qmoe_gemm2_w8a8(d, gp.dev(h), gp.dev(hs), gp.dev(w2), gp.dev(w2s), gp.dev(offsets), y, acc)
+    torch.cuda.synchronize()
+    _, racc = oracle.stage2("w8a8", w.H, w.I, w.E, experts, h, hs, w2, w2s, acc=True)
+    assert np.array_equal(gp.host(acc), racc)
+    assert np.abs(racc).max() == 127 * 127 * w.I
+
+
+# ------------------------------------------------------------------ combine
+
+def test_combine_against_oracle_and_deterministic():
+    T, k, H = 300, 10, 1024
+    rng = np.random.default_rng(9)
+    ids = gen.routing_uniform(rng, T, 64, k)
+    ids[5, 3] = 99  # one invalid pair: slot -1
+    ro = oracle.align_sort(ids, 64)
+    y = rng.standard_normal((T * k, H)).astype(np.float32)
+    tw = gen.routing_weights(rng, T, k)
+    d = qb.dims(T, k, H, 32, 64)
+    outs = []
+    for _ in range(2):
+        out = gp.empty((T, H), torch.int16)
+        qb.qmoe_combine(d, gp.dev(y), gp.dev(tw), gp.dev(ro["pair_slot"]), out)
+        torch.cuda.synchronize()
+        outs.append(gp.host(out, np.uint16))
+    assert np.array_equal(outs[0], outs[1])
+    ref = oracle.combine(y, tw, ro["pair_slot"])
+    assert rel_l2(gp.bf16_to_f64(outs[0]), ref) < REL_L2
+
+
+# ------------------------------------------------------------------ whole layer
+
+SMALL = [
+    gen.WORKLOADS["tiny_w4a16"],
+    gen.custom("e2e_mxfp4_ragged", "mxfp4", 50, 1024, 12, 4, 160, seed=41),
+    gen.custom("e2e_w8a8_ragged", "w8a8", 50, 1024, 12, 4, 160, seed=42),
+    gen.custom("e2e_w4a16_ragged", "w4a16", 50, 1024, 12, 4, 160, seed=43),
+    gen.custom("e2e_zipf_mxfp4", "mxfp4", 64, 512, 64, 8, 128, routing="zipf", seed=44),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_layer_small(w):
+    d = gen.make_all(w)
+    g = gp.run_layer(w, d)
+    ref = oracle.moe_forward(w.scheme, dims(w), d)
+    assert g["status"] == 0
+    assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
+
+
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
+def test_layer_ragged_expert_loads(scheme):
+    # expert loads 0, 1, 127, 129 (tile tails on both sides of 128) plus empties
+    counts = [0, 1, 127, 129, 0, 2, 0, 4]
+    rng = np.random.default_rng(77)
+    ids = gen.routing_with_counts(rng, counts, 2)
+    T = ids.shape[0]
+    w = gen.custom(f"ragged_{scheme}", scheme, T, 256, len(counts), 2, 96, seed=78)
+    d = gen.make_all(w, routing=(ids, gen.routing_weights(rng, T, 2)))
+    g = gp.run_layer(w, d)
+    ref = oracle.moe_forward(scheme, dims(w), d)
+    assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
+
+
+def test_layer_invalid_ids_flagged_and_skipped():
+    w = gen.custom("bad_ids", "mxfp4", 20, 256, 8, 2, 64, seed=51)
+    d = gen.make_all(w)
+    d["topk_ids"] = d["topk_ids"].copy()
+    d["topk_ids"][3, 1] = 8
+    d["topk_ids"][7, 0] = -2
+    g = gp.run_layer(w, d)
+    ref = oracle.moe_forward(w.scheme, dims(w), d)
+    assert g["status"] & qb.DEV_BAD_EXPERT_ID
+    assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
+
+
+def test_layer_zero_tokens():
+    w = gen.custom("empty", "w4a16", 0, 256, 8, 2, 128, seed=1)
+    d = gen.make_all(w)
+    out, status = qb.moe_forward("w4a16", gp.empty((0, 256), torch.int16), gp.empty((0, 2), torch.int32),
+                                 gp.empty((0, 2), torch.float32), gp.dev(d["w1"]), gp.dev(d["w1_s"]),
+                                 gp.dev(d["w2"]), gp.dev(d["w2_s"]))
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256) and int(status.item()) == 0
+
+
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
+def test_forward_entry_point_matches_stagewise_and_is_deterministic(scheme):
+    w = gen.custom(f"fwd_{scheme}", scheme, 33, 512, 10, 4, 128, seed=61)
+    d = gen.make_all(w)
+    stage = gp.run_layer(w, d)
+    outs = []
+    for _ in range(2):
+        out, status = qb.moe_forward(scheme, gp.dev(d["x"]), gp.dev(d["topk_ids"]), gp.dev(d["topk_w"]),
+                                     gp.dev(d["w1"]), gp.dev(d["w1_s"]), gp.dev(d["w2"]), gp.dev(d["w2_s"]))
+        torch.cuda.synchronize()
+        outs.append(gp.host(out, np.uint16))
+        assert int(status.item()) == 0
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], stage["out"])
+
+
+def test_argument_errors_raise():
+    w = gen.custom("err", "w4a16", 4, 256, 4, 2, 64, seed=1)
+    d = gen.make_all(w)
+    with pytest.raises(qb.QmoeError):
+        qb.qmoe_combine(qb.dims(4, 2, 250, 64, 4), gp.empty((8, 250), torch.float32), gp.dev(d["topk_w"]),
+                        gp.empty(8, torch.int32), gp.empty((4, 250), torch.int16))
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled rows)
+
+_WEIGHT_CACHE = {}
+
+
+def _full_inputs(w):
+    key = (w.scheme, w.H, w.I, w.E, w.wseed)
+    if key not in _WEIGHT_CACHE:
+        _WEIGHT_CACHE.clear()
+        _WEIGHT_CACHE[key] = gen.make_weights(w)
+    ids, tw = gen.make_routing(w)
+    d = dict(x=gen.make_activations(w), topk_ids=ids, topk_w=tw)
+    d.update(_WEIGHT_CACHE[key])
+    return d
+
+
+FULL = ["decode_T1", "decode_T4", "decode_T16", "decode_T64", "mxfp4_T256", "mxfp4_T1024", "mxfp4_T4096",
+        "mxfp4_T8192", "w4a16_T2048", "w8a8_T8192"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name):
+    w = gen.WORKLOADS[name]
+    d = _full_inputs(w)
+    g = gp.run_layer(w, d)
+    assert g["status"] == 0
+    n = min(w.T, 48)
+    rows = np.sort(np.random.default_rng(w.seed).choice(w.T, n, replace=False))
+    ref = oracle.moe_forward(w.scheme, dims(w), d, tokens=rows)
+    assert rel_l2(gp.bf16_to_f64(g["out"][rows]), ref) < REL_L2
+    # every row is finite and the layer is not trivially zero
+    allout = gp.bf16_to_f64(g["out"])
+    assert np.isfinite(allout).all() and np.abs(allout).max() > 0
