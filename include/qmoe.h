@@ -108,6 +108,35 @@ int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts
                     int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, void* ws,
                     size_t ws_bytes, qmoe_stream_t stream);
 
+/* qmoe_align_sort_static_scratch -- the same sort as qmoe_align_sort, for
+ * callers that cannot allocate device memory.  The source pages have no
+ * counterpart to this call; it exists for integrations where cudaMalloc is
+ * not available when tokens are routed: a host framework that owns every
+ * device allocation through its own pool, a plugin that may not allocate
+ * after start-up, or a latency path where allocating is forbidden.
+ *
+ * The caller still passes every input and output (same meaning and layout as
+ * qmoe_align_sort); the histogram scratch is a fixed array of
+ * QMOE_STATIC_SCRATCH_BYTES inside the library, present on every GPU that
+ * loads the library until the process exits.  No cudaMalloc, cudaFree or
+ * other allocating call is made.
+ *
+ * Limits: E <= 4096 and ceil(T*k / 2048) * E * 4 <= QMOE_STATIC_SCRATCH_BYTES
+ * (for example T*k <= 81920 with E = 512 uses 80 KiB); larger shapes return
+ * QMOE_ERR_UNSUPPORTED before any launch -- use qmoe_align_sort with a
+ * workspace for them.
+ *
+ * The first call on a device looks up the array's device address on the
+ * current device (once per device); make that first call before any stream
+ * capture.  Every call on a device shares the one array and it keeps the last
+ * call's contents; nothing in it needs to start at zero (each call rewrites
+ * all it reads).  Calls whose executions overlap on the GPU (different
+ * streams, or different host threads) race on the array: serialise them. */
+#define QMOE_STATIC_SCRATCH_BYTES (1u << 20)
+int qmoe_align_sort_static_scratch(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+                                   int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status,
+                                   qmoe_stream_t stream);
+
 /* ---------------------------------------------------------------- activation quantisation
  *
  * qmoe_quant_act_mxfp8 -- bf16 rows to E4M3 codes with one E8M0 scale per 32

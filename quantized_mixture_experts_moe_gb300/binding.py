@@ -39,6 +39,7 @@ SIGNATURES = {
     "qmoe_version": ([], ctypes.c_char_p),
     "qmoe_workspace_bytes": ([_DP], _sz),
     "qmoe_align_sort": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_align_sort_static_scratch": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "qmoe_quant_act_mxfp8": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
     "qmoe_quant_rows_int8_bf16": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
     "qmoe_quant_rows_int8_f32": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
@@ -118,6 +119,18 @@ def qmoe_align_sort(d, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, de
                                _ptr(pair_slot), _ptr(dev_status), _ptr(ws), ws.numel() * ws.element_size(),
                                _stream(stream))
     _check(rc, "qmoe_align_sort")
+
+
+STATIC_SCRATCH_BYTES = 1 << 20
+
+
+def qmoe_align_sort_static_scratch(d, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status,
+                                   stream=None):
+    """The routing sort with the library's built-in scratch (no workspace)."""
+    rc = lib().qmoe_align_sort_static_scratch(ctypes.byref(d), _ptr(topk_ids), _ptr(counts), _ptr(offsets),
+                                              _ptr(sorted_pair_ids), _ptr(pair_slot), _ptr(dev_status),
+                                              _stream(stream))
+    _check(rc, "qmoe_align_sort_static_scratch")
 
 
 def qmoe_quant_act_mxfp8(x_bf16, x_q, x_s, stream=None):
