@@ -248,6 +248,9 @@ def run_ours(args, w):
         return torch.from_numpy(a).to(dev)
 
     t = {key: to_dev(v) for key, v in d.items()}
+    if w.scheme == "mxfp4":  # one-time weight preparation (not part of a step)
+        t["w1_s"] = qb.prepack_mx_scales(t["w1_s"], H)
+        t["w2_s"] = qb.prepack_mx_scales(t["w2_s"], I)
     dims = qb.dims(T, k, H, I, E)
     stream = torch.cuda.current_stream(dev)
 
@@ -282,20 +285,20 @@ def run_ours(args, w):
         if record:
             a.record(stream)
         if w.scheme == "mxfp4":
-            qb.qmoe_gemm1_swiglu_mxfp4(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, hq, hs, ws)
+            qb.qmoe_gemm1_swiglu_mxfp4(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, hq, hs, status, ws)
         elif w.scheme == "w8a8":
-            qb.qmoe_gemm1_swiglu_w8a8(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h32, None, ws)
+            qb.qmoe_gemm1_swiglu_w8a8(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h32, None, status, ws)
         else:
-            qb.qmoe_gemm1_swiglu_w4a16(dims, t["x"], t["w1"], t["w1_s"], offsets, sorted_ids, h16, ws)
+            qb.qmoe_gemm1_swiglu_w4a16(dims, t["x"], t["w1"], t["w1_s"], offsets, sorted_ids, h16, status, ws)
         if record:
             b.record(stream)
         if w.scheme == "mxfp4":
-            qb.qmoe_gemm2_mxfp4(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, ws)
+            qb.qmoe_gemm2_mxfp4(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, status, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_quant_rows_int8_f32(h32, hq, hs)
-            qb.qmoe_gemm2_w8a8(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, None, ws)
+            qb.qmoe_gemm2_w8a8(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, None, status, ws)
         else:
-            qb.qmoe_gemm2_w4a16(dims, h16, t["w2"], t["w2_s"], offsets, y, ws)
+            qb.qmoe_gemm2_w4a16(dims, h16, t["w2"], t["w2_s"], offsets, y, status, ws)
         if record:
             c.record(stream)
             g1_pairs.append((a, b))

@@ -24,8 +24,7 @@
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers unless stated otherwise.  The
  *     caller owns every buffer, including the workspace; the library never
- *     allocates, frees or synchronises (except qmoe_moe_forward_host, which
- *     is documented below).
+ *     allocates, frees or synchronises.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *   - Host-side checks run before any launch: a NULL pointer, a dimension
  *     <= 0 (T may be 0), H or I not a multiple of 32, or a pointer not
@@ -35,7 +34,9 @@
  *   - Device-side errors never trap: a routing id outside [0, E) sets bit
  *     QMOE_DEV_BAD_EXPERT_ID of *dev_status (which the caller zeroes before
  *     the first call and reads after synchronising); that pair then takes no
- *     slot and contributes nothing to the output.
+ *     slot and contributes nothing to the output.  A tensor-core kernel whose
+ *     pipeline wait exceeds its time limit sets QMOE_DEV_WAIT_TIMEOUT, stops
+ *     and releases its resources; its outputs are then undefined.
  *   - Calls on different streams are independent when they use different
  *     output and workspace buffers.
  *
@@ -45,7 +46,8 @@
  *             2i+1 in the high nibble; stored n = q + 8, value (n - 8) * s;
  *             scales fp16 [rows, K/32].
  *   E2M1      same nibble order; OCP MX element encoding; scales E8M0
- *             [rows, K/32] (value 2^(b-127)).
+ *             (value 2^(b-127)), one per 32 K elements, given to the GEMMs
+ *             pre-packed by qmoe_prepack_mx_scales (see there).
  *   E4M3      OCP "fn" fp8 (max 448, no infinities).
  *   int8      W int8 [rows, K], fp32 scale per output row.
  * Weight tensors: W1 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up), W2 [E, H, I].
@@ -157,6 +159,20 @@ int qmoe_quant_rows_int8_bf16(int64_t rows, int64_t cols, const uint16_t* x, int
 int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t* q, float* s,
                              qmoe_stream_t stream);
 
+/* ---------------------------------------------------------------- weight preparation
+ *
+ * qmoe_prepack_mx_scales -- one-time rearrangement of E8M0 weight scales
+ * [rows, K/32] (row-major, one byte per 32 K elements) into the order the
+ * block-scaled tensor-core MMA consumes: 512-byte atoms, one per (128-row
+ * tile, group of 4 scale blocks), group index fastest; inside an atom, row r
+ * (0..127) and block b (0..3) at byte 16*(r%32) + 4*(r/32) + b.  Padding rows
+ * and blocks hold 127 (scale 1).  The MXFP4 GEMMs take their weight scales in
+ * this form.  Output size: qmoe_mx_scales_packed_bytes(rows, K) bytes,
+ * 16-byte aligned.  No counterpart on the pages: it is a storage-order
+ * choice for this hardware, like any weight repacking at load time. */
+size_t qmoe_mx_scales_packed_bytes(int64_t rows, int64_t K);
+int qmoe_prepack_mx_scales(int64_t rows, int64_t K, const uint8_t* s_rowmajor, uint8_t* s_packed, qmoe_stream_t stream);
+
 /* ---------------------------------------------------------------- stage 1: gate/up + SwiGLU
  *
  * For every expert e and slot s in [offsets[e], offsets[e+1]), with
@@ -170,8 +186,8 @@ int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t*
  * W4A16: x bf16 [T, H]; w1 int4 [E, 2I, H/2]; w1_s fp16 [E, 2I, H/32];
  *        out h bf16 [P, I] (round to nearest even from fp32). */
 int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const uint8_t* w1, const uint16_t* w1_s,
-                            const int32_t* offsets, const int32_t* sorted_pair_ids, uint16_t* h_bf16, void* ws,
-                            size_t ws_bytes, qmoe_stream_t stream);
+                            const int32_t* offsets, const int32_t* sorted_pair_ids, uint16_t* h_bf16,
+                            int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
 /* MXFP4 x FP8: x_q E4M3 [T, H] + x_s E8M0 [T, H/32] (from qmoe_quant_act_mxfp8);
  *        w1 E2M1 [E, 2I, H/2]; w1_s E8M0 [E, 2I, H/32];
@@ -179,7 +195,8 @@ int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const ui
  *        the rule of qmoe_quant_act_mxfp8 along I. */
 int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1,
                             const uint8_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                            uint8_t* h_q, uint8_t* h_s, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+                            uint8_t* h_q, uint8_t* h_s, int32_t* dev_status, void* ws, size_t ws_bytes,
+                            qmoe_stream_t stream);
 
 /* W8A8: x_q int8 [T, H] + x_s fp32 [T] (from qmoe_quant_rows_int8_bf16);
  *        w1 int8 [E, 2I, H]; w1_s fp32 [E, 2I].  Accumulation is exact int32;
@@ -188,7 +205,7 @@ int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, const uint8_
  *        gate/up accumulators. */
 int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x_s, const int8_t* w1,
                            const float* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids, float* h,
-                           int32_t* dbg_acc, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+                           int32_t* dbg_acc, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
 /* ---------------------------------------------------------------- stage 2: down projection
  *
@@ -199,20 +216,21 @@ int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x
  *
  * W4A16: h bf16 [P, I]; w2 int4 [E, H, I/2]; w2_s fp16 [E, H, I/32]. */
 int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
-                     const int32_t* offsets, float* y, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+                     const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                     qmoe_stream_t stream);
 
 /* MXFP4 x FP8: h_q E4M3 [P, I] + h_s E8M0 [P, I/32]; w2 E2M1 [E, H, I/2];
  *        w2_s E8M0 [E, H, I/32]. */
 int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2,
-                     const uint8_t* w2_s, const int32_t* offsets, float* y, void* ws, size_t ws_bytes,
-                     qmoe_stream_t stream);
+                     const uint8_t* w2_s, const int32_t* offsets, float* y, int32_t* dev_status, void* ws,
+                     size_t ws_bytes, qmoe_stream_t stream);
 
 /* W8A8: h_q int8 [P, I] + h_s fp32 [P] (qmoe_quant_rows_int8_f32 of h);
  *        w2 int8 [E, H, I]; w2_s fp32 [E, H]; y = ((float)acc * h_s[s]) * w2_s[e][c];
  *        dbg_acc (nullable) int32 [P, H]. */
 int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2, const float* w2_s,
-                    const int32_t* offsets, float* y, int32_t* dbg_acc, void* ws, size_t ws_bytes,
-                    qmoe_stream_t stream);
+                    const int32_t* offsets, float* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
+                    size_t ws_bytes, qmoe_stream_t stream);
 
 /* ---------------------------------------------------------------- combine
  *
@@ -230,7 +248,8 @@ int qmoe_combine(const qmoe_dims* d, const float* y, const float* topk_w, const 
  * One call for the whole path: routing, activation quantisation (MXFP4,
  * W8A8), stage 1, intermediate quantisation (W8A8), stage 2 and combine, all
  * launched in order on `stream`.  scheme: 0 = W4A16, 1 = MXFP4 x FP8,
- * 2 = W8A8.  Weights and scales as for the per-stage calls.  All
+ * 2 = W8A8.  Weights and scales as for the per-stage calls (MXFP4 weight
+ * scales pre-packed).  All
  * intermediates live in the caller's workspace of
  * qmoe_forward_workspace_bytes(d, scheme) bytes (256-byte aligned).
  * dev_status as for qmoe_align_sort. */

@@ -43,12 +43,14 @@ SIGNATURES = {
     "qmoe_quant_act_mxfp8": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
     "qmoe_quant_rows_int8_bf16": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
     "qmoe_quant_rows_int8_f32": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
-    "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm1_swiglu_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_mx_scales_packed_bytes": ([_i64, _i64], _sz),
+    "qmoe_prepack_mx_scales": ([_i64, _i64, _vp, _vp, _vp], _i32),
+    "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_combine": ([_DP, _vp, _vp, _vp, _vp, _vp], _i32),
     "qmoe_forward_workspace_bytes": ([_DP, _i32], _sz),
     "qmoe_moe_forward": ([_i32, _DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -155,43 +157,76 @@ def _ws(ws):
     return _ptr(ws), (0 if ws is None else ws.numel() * ws.element_size())
 
 
-def qmoe_gemm1_swiglu_w4a16(d, x, w1, w1_s, offsets, sorted_pair_ids, h, ws=None, stream=None):
+def _status(st, device=None):
+    if st is None:
+        st = torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+    return st
+
+
+def mx_scales_packed_bytes(rows: int, K: int) -> int:
+    return int(lib().qmoe_mx_scales_packed_bytes(rows, K))
+
+
+def qmoe_prepack_mx_scales(s_rowmajor, s_packed, rows: int, K: int, stream=None):
+    _check(lib().qmoe_prepack_mx_scales(rows, K, _ptr(s_rowmajor), _ptr(s_packed), _stream(stream)),
+           "qmoe_prepack_mx_scales")
+
+
+def prepack_mx_scales(s_rowmajor, K: int, stream=None):
+    """E8M0 scales [..., K/32] (rows = all leading dims) -> packed byte tensor."""
+    rows = s_rowmajor.numel() // (K // 32)
+    out = torch.empty(max(mx_scales_packed_bytes(rows, K), 16), dtype=torch.uint8, device=s_rowmajor.device)
+    qmoe_prepack_mx_scales(s_rowmajor.contiguous(), out, rows, K, stream)
+    return out
+
+
+def qmoe_gemm1_swiglu_w4a16(d, x, w1, w1_s, offsets, sorted_pair_ids, h, status=None, ws=None, stream=None):
     wp, wn = _ws(ws)
+    status = _status(status, x.device)
     _check(lib().qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), _ptr(x), _ptr(w1), _ptr(w1_s), _ptr(offsets),
-                                         _ptr(sorted_pair_ids), _ptr(h), wp, wn, _stream(stream)),
+                                         _ptr(sorted_pair_ids), _ptr(h), _ptr(status), wp, wn, _stream(stream)),
            "qmoe_gemm1_swiglu_w4a16")
 
 
-def qmoe_gemm1_swiglu_mxfp4(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, ws=None, stream=None):
+def qmoe_gemm1_swiglu_mxfp4(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, status=None, ws=None,
+                            stream=None):
     wp, wn = _ws(ws)
+    status = _status(status, x_q.device)
     _check(lib().qmoe_gemm1_swiglu_mxfp4(ctypes.byref(d), _ptr(x_q), _ptr(x_s), _ptr(w1), _ptr(w1_s), _ptr(offsets),
-                                         _ptr(sorted_pair_ids), _ptr(h_q), _ptr(h_s), wp, wn, _stream(stream)),
+                                         _ptr(sorted_pair_ids), _ptr(h_q), _ptr(h_s), _ptr(status), wp, wn,
+                                         _stream(stream)),
            "qmoe_gemm1_swiglu_mxfp4")
 
 
-def qmoe_gemm1_swiglu_w8a8(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h, dbg_acc=None, ws=None, stream=None):
+def qmoe_gemm1_swiglu_w8a8(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h, dbg_acc=None, status=None, ws=None,
+                           stream=None):
     wp, wn = _ws(ws)
+    status = _status(status, x_q.device)
     _check(lib().qmoe_gemm1_swiglu_w8a8(ctypes.byref(d), _ptr(x_q), _ptr(x_s), _ptr(w1), _ptr(w1_s), _ptr(offsets),
-                                        _ptr(sorted_pair_ids), _ptr(h), _ptr(dbg_acc), wp, wn, _stream(stream)),
+                                        _ptr(sorted_pair_ids), _ptr(h), _ptr(dbg_acc), _ptr(status), wp, wn,
+                                        _stream(stream)),
            "qmoe_gemm1_swiglu_w8a8")
 
 
-def qmoe_gemm2_w4a16(d, h, w2, w2_s, offsets, y, ws=None, stream=None):
+def qmoe_gemm2_w4a16(d, h, w2, w2_s, offsets, y, status=None, ws=None, stream=None):
     wp, wn = _ws(ws)
-    _check(lib().qmoe_gemm2_w4a16(ctypes.byref(d), _ptr(h), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y), wp, wn,
-                                  _stream(stream)), "qmoe_gemm2_w4a16")
+    status = _status(status, h.device)
+    _check(lib().qmoe_gemm2_w4a16(ctypes.byref(d), _ptr(h), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
+                                  _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_w4a16")
 
 
-def qmoe_gemm2_mxfp4(d, h_q, h_s, w2, w2_s, offsets, y, ws=None, stream=None):
+def qmoe_gemm2_mxfp4(d, h_q, h_s, w2, w2_s, offsets, y, status=None, ws=None, stream=None):
     wp, wn = _ws(ws)
+    status = _status(status, h_q.device)
     _check(lib().qmoe_gemm2_mxfp4(ctypes.byref(d), _ptr(h_q), _ptr(h_s), _ptr(w2), _ptr(w2_s), _ptr(offsets),
-                                  _ptr(y), wp, wn, _stream(stream)), "qmoe_gemm2_mxfp4")
+                                  _ptr(y), _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_mxfp4")
 
 
-def qmoe_gemm2_w8a8(d, h_q, h_s, w2, w2_s, offsets, y, dbg_acc=None, ws=None, stream=None):
+def qmoe_gemm2_w8a8(d, h_q, h_s, w2, w2_s, offsets, y, dbg_acc=None, status=None, ws=None, stream=None):
     wp, wn = _ws(ws)
+    status = _status(status, h_q.device)
     _check(lib().qmoe_gemm2_w8a8(ctypes.byref(d), _ptr(h_q), _ptr(h_s), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
-                                 _ptr(dbg_acc), wp, wn, _stream(stream)), "qmoe_gemm2_w8a8")
+                                 _ptr(dbg_acc), _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_w8a8")
 
 
 def qmoe_combine(d, y, topk_w, pair_slot, out, stream=None):

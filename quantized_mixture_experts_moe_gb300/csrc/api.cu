@@ -13,6 +13,12 @@ template <typename In>
 int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float* s, cudaStream_t st);
 int combine_launch(const qmoe_dims* d, const float* y, const float* topk_w, const int32_t* pair_slot, uint16_t* out,
                    cudaStream_t st);
+bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2);
+int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1, const uint8_t* w1_s,
+                const int32_t* offsets, const int32_t* sorted, uint8_t* h_q, uint8_t* h_s, int32_t* status,
+                cudaStream_t st);
+int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2, const uint8_t* w2_s,
+                const int32_t* offsets, float* y, int32_t* status, cudaStream_t st);
 
 static int gemm_args_ok(const qmoe_dims* d, std::initializer_list<const void*> ptrs) {
     if (!dims_ok(d)) return QMOE_ERR_ARG;
@@ -47,9 +53,10 @@ extern "C" const char* qmoe_version(void) { return "qmoe-gb300 0.1 (sm_103a)"; }
 
 extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const uint8_t* w1,
                                        const uint16_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                                       uint16_t* h_bf16, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+                                       uint16_t* h_bf16, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                       qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {x_bf16, w1, w1_s, offsets, sorted_pair_ids, h_bf16});
+    int rc = gemm_args_ok(d, {x_bf16, w1, w1_s, offsets, sorted_pair_ids, h_bf16, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     SimtArgs a = make_args(d);
     a.act = x_bf16; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids; a.out = h_bf16;
@@ -58,10 +65,14 @@ extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf1
 
 extern "C" int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1,
                                        const uint8_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                                       uint8_t* h_q, uint8_t* h_s, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+                                       uint8_t* h_q, uint8_t* h_s, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                       qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s});
+    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (mx_tc_ok(d, w1, nullptr))
+        return mx_tc_gemm1(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, dev_status,
+                           (cudaStream_t)stream);
     SimtArgs a = make_args(d);
     a.act = x_q; a.act_s = x_s; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids;
     a.out = h_q; a.out_s = h_s;
@@ -70,9 +81,10 @@ extern "C" int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, c
 
 extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x_s, const int8_t* w1,
                                       const float* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                                      float* h, int32_t* dbg_acc, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+                                      float* h, int32_t* dbg_acc, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                      qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h});
+    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
     SimtArgs a = make_args(d);
@@ -82,9 +94,10 @@ extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, con
 }
 
 extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
-                                const int32_t* offsets, float* y, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+                                const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {h_bf16, w2, w2_s, offsets, y});
+    int rc = gemm_args_ok(d, {h_bf16, w2, w2_s, offsets, y, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     SimtArgs a = make_args(d);
     a.act = h_bf16; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y;
@@ -92,21 +105,23 @@ extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, cons
 }
 
 extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2,
-                                const uint8_t* w2_s, const int32_t* offsets, float* y, void* ws, size_t ws_bytes,
-                                qmoe_stream_t stream) {
+                                const uint8_t* w2_s, const int32_t* offsets, float* y, int32_t* dev_status, void* ws,
+                                size_t ws_bytes, qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y});
+    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (mx_tc_ok(d, nullptr, w2))
+        return mx_tc_gemm2(d, h_q, h_s, w2, w2_s, offsets, y, dev_status, (cudaStream_t)stream);
     SimtArgs a = make_args(d);
     a.act = h_q; a.act_s = h_s; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y;
     return gemm_simt(1, 2, a, (cudaStream_t)stream);
 }
 
 extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2,
-                               const float* w2_s, const int32_t* offsets, float* y, int32_t* dbg_acc, void* ws,
-                               size_t ws_bytes, qmoe_stream_t stream) {
+                               const float* w2_s, const int32_t* offsets, float* y, int32_t* dbg_acc,
+                               int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y});
+    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
     SimtArgs a = make_args(d);
@@ -176,31 +191,31 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     float* y = (float*)at(L.y);
     if (scheme == 0) {
         rc = qmoe_gemm1_swiglu_w4a16(d, x_bf16, (const uint8_t*)w1, (const uint16_t*)w1_s, offsets, sorted,
-                                     (uint16_t*)at(L.h), aws, aws_bytes, stream);
+                                     (uint16_t*)at(L.h), dev_status, aws, aws_bytes, stream);
         if (rc == QMOE_OK)
             rc = qmoe_gemm2_w4a16(d, (const uint16_t*)at(L.h), (const uint8_t*)w2, (const uint16_t*)w2_s, offsets, y,
-                                  aws, aws_bytes, stream);
+                                  dev_status, aws, aws_bytes, stream);
     } else if (scheme == 1) {
         rc = qmoe_quant_act_mxfp8(d->T, d->H, x_bf16, (uint8_t*)at(L.xq), (uint8_t*)at(L.xs), stream);
         if (rc == QMOE_OK)
             rc = qmoe_gemm1_swiglu_mxfp4(d, (const uint8_t*)at(L.xq), (const uint8_t*)at(L.xs), (const uint8_t*)w1,
                                          (const uint8_t*)w1_s, offsets, sorted, (uint8_t*)at(L.h), (uint8_t*)at(L.hs),
-                                         aws, aws_bytes, stream);
+                                         dev_status, aws, aws_bytes, stream);
         if (rc == QMOE_OK)
             rc = qmoe_gemm2_mxfp4(d, (const uint8_t*)at(L.h), (const uint8_t*)at(L.hs), (const uint8_t*)w2,
-                                  (const uint8_t*)w2_s, offsets, y, aws, aws_bytes, stream);
+                                  (const uint8_t*)w2_s, offsets, y, dev_status, aws, aws_bytes, stream);
     } else {
         rc = qmoe_quant_rows_int8_bf16(d->T, d->H, x_bf16, (int8_t*)at(L.xq), (float*)at(L.xs), stream);
         if (rc == QMOE_OK)
             rc = qmoe_gemm1_swiglu_w8a8(d, (const int8_t*)at(L.xq), (const float*)at(L.xs), (const int8_t*)w1,
-                                        (const float*)w1_s, offsets, sorted, (float*)at(L.h), nullptr, aws, aws_bytes,
-                                        stream);
+                                        (const float*)w1_s, offsets, sorted, (float*)at(L.h), nullptr, dev_status, aws,
+                                        aws_bytes, stream);
         if (rc == QMOE_OK)
             rc = qmoe_quant_rows_int8_f32(P, d->I, (const float*)at(L.h), (int8_t*)at(L.hq8), (float*)at(L.hs8),
                                           stream);
         if (rc == QMOE_OK)
             rc = qmoe_gemm2_w8a8(d, (const int8_t*)at(L.hq8), (const float*)at(L.hs8), (const int8_t*)w2,
-                                 (const float*)w2_s, offsets, y, nullptr, aws, aws_bytes, stream);
+                                 (const float*)w2_s, offsets, y, nullptr, dev_status, aws, aws_bytes, stream);
     }
     if (rc != QMOE_OK) return rc;
     return qmoe_combine(d, y, topk_w, slot, out_bf16, stream);

@@ -1,0 +1,455 @@
+// Grouped MXFP4-weight x FP8-activation expert GEMMs on the 5th-generation
+// tensor cores (tcgen05, block-scaled kind::mxf8f6f4, E8M0 scales).
+//
+// The aiter tuned grouped-fmoe page (Changes, Test Plan) runs a two-stage
+// grouped a8w4 kernel with fp8 activations and MXFP4 weights; this is that
+// computation written for sm_103a:
+//   stage 1: h = silu(W1_gate . x) * (W1_up . x), then MX-quantised to
+//            E4M3 codes + E8M0 scales per 32 columns of I;
+//   stage 2: y = W2 . h in fp32.
+//
+// Structure (one persistent CTA per SM, 7 warps):
+//   warp 0     TMA producer: 128-row FP4 weight tiles (the tensor map unpacks
+//              FP4 into the 16-byte-aligned form the MMA reads) and the
+//              matching pre-packed 512-byte scale atoms (bulk copies).
+//   warp 1     activation producer: gathers the unit's token rows (stage 1:
+//              token = sorted pair id / k; stage 2: contiguous slots) with
+//              cp.async into the 128-byte-swizzled K-major layout, and their
+//              E8M0 scales into atom layout.
+//   warp 2     allocates tensor memory; one lane copies the stage's scale
+//              atoms into TMEM and issues the MMAs (M = 128 weight rows,
+//              N = tokens rounded up to 16, K = 32 per instruction).
+//   warps 3-6  epilogue: TMEM -> registers, SwiGLU + MX quantisation (stage
+//              1) or fp32 stores (stage 2).
+// The weights are the A operand ("swap AB"): per-expert token counts are
+// small at prefill sizes (about 80 at T = 4096), so tokens take the MMA's
+// N dimension, which can be as small as 16, instead of padding them to M.
+//
+// A work unit is (expert, tile of up to 128 of its tokens, 128 output
+// columns); units are ordered with the column block fastest so concurrent
+// CTAs share the same activation rows through L2, and every unit streams a
+// disjoint slice of the expert weights exactly once.
+#include "qmoe_common.cuh"
+#include "tc_ptx.cuh"
+
+#include <mutex>
+
+namespace qmoe {
+
+namespace mx {
+
+constexpr int NMAX = 128;   // tokens per unit
+constexpr int THREADS = 224;
+constexpr int KSTAGE = 128; // K elements per pipeline stage (4 MMAs of K = 32)
+constexpr uint32_t FP4_TILE_TX = 128 * 64;  // bytes a 128x128 FP4 tile moves (packed)
+
+template <int STAGE>
+struct Cfg {
+    static constexpr int STAGES = (STAGE == 1) ? 4 : 6;
+    static constexpr int AT = (STAGE == 1) ? 2 : 1;  // weight tiles per stage (gate + up)
+    static constexpr int LAG = STAGES - 2;             // cp.async stages in flight
+    static constexpr int A_BYTES = AT * 128 * 128;
+    static constexpr int B_BYTES = NMAX * 128;
+    static constexpr int SFA_BYTES = AT * 512;
+    static constexpr int SFB_BYTES = 512;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
+    static constexpr int SFA_OFF = B_OFF + STAGES * B_BYTES;
+    static constexpr int SFB_OFF = SFA_OFF + STAGES * SFA_BYTES;
+    static constexpr int BAR_OFF = SFB_OFF + STAGES * SFB_BYTES;
+    static constexpr int NBAR = 2 * STAGES + 2;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int SCHED_OFF = MISC_OFF + 64;
+    static size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
+    // TMEM columns: accumulators (AT * NMAX), then per-stage scale slots
+    static constexpr uint32_t SFA_COL = AT * NMAX;
+    static constexpr uint32_t SFB_COL = SFA_COL + STAGES * AT * 4;
+    static_assert(SFB_COL + STAGES * 4 <= 512, "TMEM budget");
+};
+
+struct Args {
+    int T, k, H, I, E;
+    const uint8_t* act;       // stage 1: x_q [T, H]; stage 2: h_q [P, I]
+    const uint8_t* act_s;     // stage 1: x_s [T, H/32]; stage 2: h_s [P, I/32]
+    const uint8_t* w_s;       // pre-packed weight scale atoms
+    const int32_t* offsets;   // [E+1]
+    const int32_t* sorted;    // [P] (stage 1)
+    uint8_t* h_q;             // stage 1 outputs
+    uint8_t* h_s;
+    float* y;                 // stage 2 output
+    int32_t* status;
+};
+
+__device__ __forceinline__ void decode_unit(int u, int NB, const int* tile_start, int E, const int32_t* offsets,
+                                            int& e, int& m0, int& ntok, int& nb) {
+    const int t = u / NB;
+    nb = u - t * NB;
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tile_start[mid] <= t) lo = mid; else hi = mid;
+    }
+    e = lo;
+    m0 = offsets[e] + (t - tile_start[e]) * NMAX;
+    ntok = min(NMAX, offsets[e + 1] - m0);
+}
+
+__device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
+    *flag = 1;
+    atomicOr(status, QMOE_DEV_WAIT_TIMEOUT);
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(THREADS, 1)
+mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
+    using C = Cfg<STAGE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem + C::A_OFF;
+    uint8_t* sB = smem + C::B_OFF;
+    uint8_t* sSFA = smem + C::SFA_OFF;
+    uint8_t* sSFB = smem + C::SFB_OFF;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* acc_full = empty + C::STAGES;
+    uint64_t* acc_empty = acc_full + 1;
+    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
+    int* tile_start = reinterpret_cast<int*>(smem + C::SCHED_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E;
+    const int K = (STAGE == 1) ? a.H : a.I;            // reduction length
+    const int NOUT = (STAGE == 1) ? a.I : a.H;          // output columns
+    const int NB = NOUT / 128;
+    const int KT = K / KSTAGE;
+
+    // ---- schedule: tiles of up to NMAX tokens per expert, prefix over experts
+    if (warp == 0) {
+        int running = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int cnt = (e < E) ? a.offsets[e + 1] - a.offsets[e] : 0;
+            const int tiles = (cnt + NMAX - 1) / NMAX;
+            int incl = tiles;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (e < E) tile_start[e] = running + incl - tiles;
+            running += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) tile_start[E] = running;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            tc::mbar_init(&full[s], 2);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(acc_full, 1);
+        tc::mbar_init(acc_empty, 4);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    const int total_units = tile_start[E] * NB;
+    if ((int)blockIdx.x >= total_units) return;  // no work: nothing allocated yet
+
+    if (warp == 2) {
+        tc::tmem_alloc(tmem_base_smem, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tm = *tmem_base_smem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ weight producer (TMA)
+        if (lane == 0) {
+            tc::prefetch_tensormap(&mapW);
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+                int e, m0, ntok, nb;
+                decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+                const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
+                const int row0 = e * rows_per_e + nb * 128;
+                const int row1 = e * rows_per_e + a.I + nb * 128;  // up rows (stage 1)
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
+                    tc::mbar_arrive_expect_tx(&full[stage], C::AT * (FP4_TILE_TX + 512));
+                    uint8_t* dA = sA + stage * C::A_BYTES;
+                    uint8_t* dS = sSFA + stage * C::SFA_BYTES;
+                    tc::tma_load_2d(dA, &mapW, &full[stage], kt * KSTAGE, row0);
+                    tc::bulk_load(dS, a.w_s + ((int64_t)(row0 / 128) * KT + kt) * 512, 512, &full[stage]);
+                    if (STAGE == 1) {
+                        tc::tma_load_2d(dA + 128 * 128, &mapW, &full[stage], kt * KSTAGE, row1);
+                        tc::bulk_load(dS + 512, a.w_s + ((int64_t)(row1 / 128) * KT + kt) * 512, 512, &full[stage]);
+                    }
+                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ activation producer (cp.async gather)
+        int stage = 0, pending = 0;
+        uint32_t phase = 0;
+        const int rowbytes = K;        // activation row bytes (one E4M3 code per element)
+        const int srowbytes = K / 32;  // scale bytes per row
+        for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+            int e, m0, ntok, nb;
+            decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+            int64_t src_row[NMAX / 32];
+#pragma unroll
+            for (int i = 0; i < NMAX / 32; ++i) {
+                const int r = lane + 32 * i;
+                src_row[i] = -1;
+                if (r < ntok) src_row[i] = (STAGE == 1) ? (int64_t)(a.sorted[m0 + r] / a.k) : (int64_t)(m0 + r);
+            }
+            bool ok = true;
+            for (int kt = 0; kt < KT; ++kt) {
+                int w = 1;
+                if (lane == 0) w = tc::mbar_wait(&empty[stage], phase ^ 1) ? 1 : 0;
+                w = __shfl_sync(0xFFFFFFFFu, w, 0);
+                if (!w) { if (lane == 0) set_abort(abort_flag, a.status); ok = false; break; }
+                uint8_t* dB = sB + stage * C::B_BYTES;
+                uint8_t* dS = sSFB + stage * C::SFB_BYTES;
+#pragma unroll
+                for (int i = 0; i < NMAX / 32; ++i) {
+                    if (src_row[i] < 0) continue;
+                    const int r = lane + 32 * i;
+                    const uint8_t* src = a.act + src_row[i] * rowbytes + kt * KSTAGE;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) tc::cp_async_16(dB + tc::sw128_offset(r, c), src + 16 * c);
+                    tc::cp_async_4(dS + 16 * (r & 31) + 4 * (r >> 5), a.act_s + src_row[i] * srowbytes + kt * 4);
+                }
+                tc::cp_async_commit();
+                ++pending;
+                if (pending > C::LAG) {
+                    tc::cp_async_wait<C::LAG>();
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    const int old = (stage - C::LAG + C::STAGES) % C::STAGES;
+                    if (lane == 0) tc::mbar_arrive(&full[old]);
+                    --pending;
+                }
+                if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+        }
+        // drain: signal the stages still pending
+        tc::cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        for (int p = pending; p > 0; --p) {
+            const int old = (stage - p + C::STAGES) % C::STAGES;
+            if (lane == 0) tc::mbar_arrive(&full[old]);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+                int e, m0, ntok, nb;
+                decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+                const int nmma = (ntok + 15) & ~15;
+                if (!tc::mbar_wait(acc_empty, acc_phase ^ 1)) { set_abort(abort_flag, a.status); break; }
+                tc::tc_fence_after();
+                bool ok = true;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!tc::mbar_wait(&full[stage], phase)) { set_abort(abort_flag, a.status); ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t sfa_col = C::SFA_COL + stage * C::AT * 4;
+                    const uint32_t sfb_col = C::SFB_COL + stage * 4;
+                    const uint32_t sfa_addr = tc::smem_u32(sSFA + stage * C::SFA_BYTES);
+                    tc::tmem_cp_32x128b_warpx4(tm + sfa_col, tc::smem_desc(sfa_addr, 0, 128, 0));
+                    if (STAGE == 1) tc::tmem_cp_32x128b_warpx4(tm + sfa_col + 4, tc::smem_desc(sfa_addr + 512, 0, 128, 0));
+                    tc::tmem_cp_32x128b_warpx4(tm + sfb_col,
+                                               tc::smem_desc(tc::smem_u32(sSFB + stage * C::SFB_BYTES), 0, 128, 0));
+                    const uint32_t a0 = tc::smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b0 = tc::smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t idesc = tc::idesc_mxf8f6f4(128, nmma, 5, 0, kk, kk);
+                        const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+                        const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + 32 * kk);
+                        tc::mma_mxf8f6f4(tm, tc::sdesc_kmajor_sw128(a0 + 32 * kk), bd, idesc, tm + sfa_col,
+                                         tm + sfb_col, acc);
+                        if (STAGE == 1)
+                            tc::mma_mxf8f6f4(tm + NMAX, tc::sdesc_kmajor_sw128(a0 + 128 * 128 + 32 * kk), bd, idesc,
+                                             tm + sfa_col + 4, tm + sfb_col, acc);
+                    }
+                    tc::mma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit(acc_full);
+                acc_phase ^= 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 3..6)
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+            int e, m0, ntok, nb;
+            decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+            int w = 1;
+            if (lane == 0) w = tc::mbar_wait(acc_full, acc_phase) ? 1 : 0;
+            w = __shfl_sync(0xFFFFFFFFu, w, 0);
+            if (!w) { if (lane == 0) set_abort(abort_flag, a.status); break; }
+            tc::tc_fence_after();
+            const int n = nb * 128 + q * 32 + lane;  // this lane's output column
+            for (int c0 = 0; c0 < ntok; c0 += 16) {
+                uint32_t g[16];
+                tc::tmem_ld_32x32b_x16(tm + lane_addr + c0, g);
+                if (STAGE == 1) {
+                    uint32_t uu[16];
+                    tc::tmem_ld_32x32b_x16(tm + lane_addr + NMAX + c0, uu);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int c = c0 + j;
+                        if (c >= ntok) break;  // warp-uniform
+                        const float h = silu_mul(__uint_as_float(g[j]), __uint_as_float(uu[j]));
+                        float amax = fabsf(h);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                        uint8_t code = 0, sb = 127;
+                        if (amax > 0.f) {
+                            const int X = mx_block_exponent(amax);
+                            sb = (uint8_t)(X + 127);
+                            code = (uint8_t)(e4m3x2_from_float(h * exp2i(-X), 0.f) & 0xFF);
+                        }
+                        const int64_t slot = m0 + c;
+                        a.h_q[slot * a.I + n] = code;
+                        if (lane == 0) a.h_s[slot * (a.I / 32) + (n >> 5)] = sb;
+                    }
+                } else {
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int c = c0 + j;
+                        if (c >= ntok) break;
+                        a.y[(int64_t)(m0 + c) * a.H + n] = __uint_as_float(g[j]);
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(acc_empty);
+            acc_phase ^= 1;
+        }
+    }
+
+    // ---- wind down: on an abort, give in-flight copies time to land
+    if (*abort_flag) {
+        tc::cp_async_wait<0>();
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000ll) { }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tm, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// FP4 weight matrix [rows, K] (K/2 bytes per row) as a tensor map whose
+// 128x128 boxes land in shared memory unpacked to 16-byte-aligned groups,
+// 128-byte swizzled.
+static int make_fp4_map(CUtensorMap* map, const void* w, int64_t rows, int64_t K) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return QMOE_ERR_CUDA;
+    cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)(K / 2)};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(w), gdim, gstride, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QMOE_OK : QMOE_ERR_UNSUPPORTED;
+}
+
+bool mx_tc_supported(const qmoe_dims* d, const void* w1, const void* w2) {
+    auto a32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+    return d->H % 128 == 0 && d->I % 128 == 0 && d->E <= 4096 && (int64_t)d->E * 2 * d->I < (1ll << 31) &&
+           (int64_t)d->E * d->H < (1ll << 31) && (!w1 || a32(w1)) && (!w2 || a32(w2));
+}
+
+template <int STAGE>
+static int launch(const qmoe_dims* d, const void* w, Args a, cudaStream_t st) {
+    using C = Cfg<STAGE>;
+    CUtensorMap map;
+    const int64_t rows = (STAGE == 1) ? (int64_t)d->E * 2 * d->I : (int64_t)d->E * d->H;
+    const int64_t K = (STAGE == 1) ? d->H : d->I;
+    int rc = make_fp4_map(&map, w, rows, K);
+    if (rc != QMOE_OK) return rc;
+    const size_t smem = C::smem_bytes(d->E);
+    static std::once_flag attr_once;
+    std::call_once(attr_once, [smem] {
+        cudaFuncSetAttribute(mx_gemm_kernel<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::smem_bytes(4096));
+    });
+    const int grid = num_sms();
+    if (grid <= 0) return QMOE_ERR_CUDA;
+    mx_gemm_kernel<STAGE><<<grid, THREADS, smem, st>>>(map, a);
+    return launch_status();
+}
+
+}  // namespace mx
+
+int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1, const uint8_t* w1_s,
+                const int32_t* offsets, const int32_t* sorted, uint8_t* h_q, uint8_t* h_s, int32_t* status,
+                cudaStream_t st) {
+    mx::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.act = x_q; a.act_s = x_s; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted;
+    a.h_q = h_q; a.h_s = h_s; a.status = status;
+    return mx::launch<1>(d, w1, a, st);
+}
+
+int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2, const uint8_t* w2_s,
+                const int32_t* offsets, float* y, int32_t* status, cudaStream_t st) {
+    mx::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.act = h_q; a.act_s = h_s; a.w_s = w2_s; a.offsets = offsets; a.y = y; a.status = status;
+    return mx::launch<2>(d, w2, a, st);
+}
+
+bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2) { return mx::mx_tc_supported(d, w1, w2); }
+
+}  // namespace qmoe

@@ -117,8 +117,13 @@ __device__ __forceinline__ void load_w(const SimtArgs& a, int64_t wrow, int K, i
         float s;
         if constexpr (SCHEME == S_W4A16)
             s = __half2float(__ushort_as_half(static_cast<const uint16_t*>(a.w_s)[wrow * (K / 32) + kk / 32]));
-        else
-            s = e8m0_to_float(static_cast<const uint8_t*>(a.w_s)[wrow * (K / 32) + kk / 32]);
+        else {
+            // pre-packed scale atoms: (row tile, group of 4 blocks) x 512 bytes
+            const int64_t kb = kk / 32, KG = (K + 127) / 128;
+            const int64_t atom = (wrow / 128) * KG + kb / 4;
+            const int r = (int)(wrow & 127);
+            s = e8m0_to_float(static_cast<const uint8_t*>(a.w_s)[atom * 512 + 16 * (r & 31) + 4 * (r >> 5) + (kb & 3)]);
+        }
 #pragma unroll
         for (int i = 0; i < NE; ++i) {
             const uint32_t nib = (v[i / 8] >> (4 * (i % 8))) & 15u;  // element 2b in the low nibble of byte b

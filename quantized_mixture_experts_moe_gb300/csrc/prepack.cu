@@ -1,0 +1,48 @@
+// One-time weight preparation: E8M0 block scales rearranged into the order
+// in which the block-scaled tensor-core MMA consumes them.
+//
+// Row-major scales s[row][kb] (one byte per 32 K elements) become 512-byte
+// atoms, one per (128-row tile rt, group of 4 scale blocks kg), stored atom
+// after atom with kg fastest.  Inside an atom the byte for tile row r and
+// block kb (0..3) sits at 16*(r % 32) + 4*(r / 32) + kb: copying an atom to
+// tensor memory with one 32x128b.warpx4 copy places the scale of row r in
+// lane r, column r / 32, byte kb -- where the MMA reads it.  Rows and blocks
+// beyond the tensor are padded with 127 (scale 1.0).
+#include "qmoe_common.cuh"
+
+namespace qmoe {
+
+__host__ __device__ inline int64_t mx_packed_bytes(int64_t rows, int64_t K) {
+    return ((rows + 127) / 128) * ((K + 127) / 128) * 512;
+}
+
+__global__ void prepack_mx_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows,
+                                         int64_t KB, int64_t KG, int64_t total) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int64_t atom = i >> 9;
+    const int off = (int)(i & 511);
+    const int64_t rt = atom / KG, kg = atom - rt * KG;
+    const int r = (off >> 4) + 32 * ((off >> 2) & 3);
+    const int kb = off & 3;
+    const int64_t row = rt * 128 + r, blk = kg * 4 + kb;
+    dst[i] = (row < rows && blk < KB) ? src[row * KB + blk] : (uint8_t)127;
+}
+
+}  // namespace qmoe
+
+extern "C" size_t qmoe_mx_scales_packed_bytes(int64_t rows, int64_t K) {
+    if (rows <= 0 || K <= 0 || K % 32 != 0) return 0;
+    return (size_t)qmoe::mx_packed_bytes(rows, K);
+}
+
+extern "C" int qmoe_prepack_mx_scales(int64_t rows, int64_t K, const uint8_t* s_rowmajor, uint8_t* s_packed,
+                                      qmoe_stream_t stream) {
+    using namespace qmoe;
+    if (rows <= 0 || K <= 0 || K % 32 != 0 || !s_rowmajor || !s_packed || !aligned16(s_packed)) return QMOE_ERR_ARG;
+    const int64_t total = mx_packed_bytes(rows, K);
+    const int64_t blocks = (total + 255) / 256;
+    prepack_mx_scales_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(s_rowmajor, s_packed, rows, K / 32,
+                                                                                (K + 127) / 128, total);
+    return launch_status();
+}

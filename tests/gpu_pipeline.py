@@ -46,6 +46,15 @@ def align(ids: np.ndarray, E: int, T: int, k: int, H=32, I=32):
                 pair_slot=host(slot)[:P], status=int(status.item()))
 
 
+def device_weights(w, inp):
+    """Weights as the library takes them (MXFP4 scales pre-packed)."""
+    t = {key: dev(inp[key]) for key in ("w1", "w1_s", "w2", "w2_s")}
+    if w.scheme == "mxfp4":
+        t["w1_s"] = qb.prepack_mx_scales(t["w1_s"], w.H)
+        t["w2_s"] = qb.prepack_mx_scales(t["w2_s"], w.I)
+    return t
+
+
 def run_layer(w, inp, keep=False):
     """The whole path, one call per stage; returns out (bf16 bits) and, with
     keep=True, every intermediate."""
@@ -62,26 +71,28 @@ def run_layer(w, inp, keep=False):
     res = {}
     if w.scheme == "w4a16":
         h = empty((P, I), torch.int16)
-        qb.qmoe_gemm1_swiglu_w4a16(d, t["x"], t["w1"], t["w1_s"], offsets, sorted_ids, h, ws)
-        qb.qmoe_gemm2_w4a16(d, h, t["w2"], t["w2_s"], offsets, y, ws)
+        qb.qmoe_gemm1_swiglu_w4a16(d, t["x"], t["w1"], t["w1_s"], offsets, sorted_ids, h, status, ws)
+        qb.qmoe_gemm2_w4a16(d, h, t["w2"], t["w2_s"], offsets, y, status, ws)
         res["h"] = h
     elif w.scheme == "mxfp4":
         xq, xs = empty((T, H), torch.uint8), empty((T, H // 32), torch.uint8)
         qb.qmoe_quant_act_mxfp8(t["x"], xq, xs)
         hq, hs = empty((P, I), torch.uint8), empty((P, I // 32), torch.uint8)
-        qb.qmoe_gemm1_swiglu_mxfp4(d, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, hq, hs, ws)
-        qb.qmoe_gemm2_mxfp4(d, hq, hs, t["w2"], t["w2_s"], offsets, y, ws)
+        w1p = qb.prepack_mx_scales(t["w1_s"], H)
+        w2p = qb.prepack_mx_scales(t["w2_s"], I)
+        qb.qmoe_gemm1_swiglu_mxfp4(d, xq, xs, t["w1"], w1p, offsets, sorted_ids, hq, hs, status, ws)
+        qb.qmoe_gemm2_mxfp4(d, hq, hs, t["w2"], w2p, offsets, y, status, ws)
         res.update(xq=xq, xs=xs, hq=hq, hs=hs)
     else:
         xq, xs = empty((T, H), torch.int8), empty(T, torch.float32)
         qb.qmoe_quant_rows_int8_bf16(t["x"], xq, xs)
         h = empty((P, I), torch.float32)
         acc1 = empty((P, 2 * I), torch.int32) if keep else None
-        qb.qmoe_gemm1_swiglu_w8a8(d, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h, acc1, ws)
+        qb.qmoe_gemm1_swiglu_w8a8(d, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h, acc1, status, ws)
         hq, hs = empty((P, I), torch.int8), empty(P, torch.float32)
         qb.qmoe_quant_rows_int8_f32(h, hq, hs)
         acc2 = empty((P, H), torch.int32) if keep else None
-        qb.qmoe_gemm2_w8a8(d, hq, hs, t["w2"], t["w2_s"], offsets, y, acc2, ws)
+        qb.qmoe_gemm2_w8a8(d, hq, hs, t["w2"], t["w2_s"], offsets, y, acc2, status, ws)
         res.update(xq=xq, xs=xs, h=h, hq=hq, hs=hs, acc1=acc1, acc2=acc2)
     out = empty((T, H), torch.int16)
     qb.qmoe_combine(d, y, t["topk_w"], slot, out)

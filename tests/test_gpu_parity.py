@@ -123,6 +123,8 @@ def test_quant_rows_int8_bit_exact(src):
 S1_CASES = [
     gen.custom("s1_w4a16", "w4a16", 40, 512, 6, 3, 192, seed=21),
     gen.custom("s1_mxfp4", "mxfp4", 40, 512, 6, 3, 192, seed=22),
+    gen.custom("s1_mxfp4_tc", "mxfp4", 60, 512, 6, 3, 256, seed=24),
+    gen.custom("s1_mxfp4_tc_multitile", "mxfp4", 200, 256, 3, 2, 128, seed=25),
     gen.custom("s1_w8a8", "w8a8", 40, 512, 6, 3, 192, seed=23),
 ]
 
@@ -159,6 +161,7 @@ def test_stage1_against_oracle(w):
 S2_CASES = [
     gen.custom("s2_w4a16", "w4a16", 1, 320, 5, 1, 256, seed=31),
     gen.custom("s2_mxfp4", "mxfp4", 1, 320, 5, 1, 256, seed=32),
+    gen.custom("s2_mxfp4_tc", "mxfp4", 1, 384, 5, 1, 256, seed=34),
     gen.custom("s2_w8a8", "w8a8", 1, 320, 5, 1, 256, seed=33),
 ]
 
@@ -180,7 +183,8 @@ def test_stage2_against_oracle(w):
         torch.cuda.synchronize()
         assert rel_l2(gp.host(y), ref) < 1e-5
     elif w.scheme == "mxfp4":
-        qb.qmoe_gemm2_mxfp4(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), t_off, y)
+        w2p = qb.prepack_mx_scales(gp.dev(wts["w2_s"]), w.I)
+        qb.qmoe_gemm2_mxfp4(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), gp.dev(wts["w2"]), w2p, t_off, y)
         ref = oracle.stage2("mxfp4", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"])
         torch.cuda.synchronize()
         assert rel_l2(gp.host(y), ref) < 1e-5
@@ -246,6 +250,8 @@ SMALL = [
     gen.custom("e2e_w8a8_ragged", "w8a8", 50, 1024, 12, 4, 160, seed=42),
     gen.custom("e2e_w4a16_ragged", "w4a16", 50, 1024, 12, 4, 160, seed=43),
     gen.custom("e2e_zipf_mxfp4", "mxfp4", 64, 512, 64, 8, 128, routing="zipf", seed=44),
+    gen.custom("e2e_mxfp4_tc", "mxfp4", 96, 1024, 16, 4, 384, seed=45),
+    gen.custom("e2e_mxfp4_tc_big_tiles", "mxfp4", 700, 512, 8, 2, 256, seed=46),
 ]
 
 
@@ -265,7 +271,8 @@ def test_layer_ragged_expert_loads(scheme):
     rng = np.random.default_rng(77)
     ids = gen.routing_with_counts(rng, counts, 2)
     T = ids.shape[0]
-    w = gen.custom(f"ragged_{scheme}", scheme, T, 256, len(counts), 2, 96, seed=78)
+    I = 128 if scheme == "mxfp4" else 96  # MXFP4: the tensor-core path (I, H multiples of 128)
+    w = gen.custom(f"ragged_{scheme}", scheme, T, 256, len(counts), 2, I, seed=78)
     d = gen.make_all(w, routing=(ids, gen.routing_weights(rng, T, 2)))
     g = gp.run_layer(w, d)
     ref = oracle.moe_forward(scheme, dims(w), d)
@@ -300,9 +307,10 @@ def test_forward_entry_point_matches_stagewise_and_is_deterministic(scheme):
     d = gen.make_all(w)
     stage = gp.run_layer(w, d)
     outs = []
+    wt = gp.device_weights(w, d)
     for _ in range(2):
         out, status = qb.moe_forward(scheme, gp.dev(d["x"]), gp.dev(d["topk_ids"]), gp.dev(d["topk_w"]),
-                                     gp.dev(d["w1"]), gp.dev(d["w1_s"]), gp.dev(d["w2"]), gp.dev(d["w2_s"]))
+                                     wt["w1"], wt["w1_s"], wt["w2"], wt["w2_s"])
         torch.cuda.synchronize()
         outs.append(gp.host(out, np.uint16))
         assert int(status.item()) == 0
