@@ -69,9 +69,13 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.qmoe_align_sort(ctypes.byref(d), null, null, null, null, null, null, null, 0, null) == -1
     assert lib.qmoe_combine(ctypes.byref(d), null, null, null, null, null) == -1
     bad = qb.dims(16, 2, 256, 100, 8)
-    assert lib.qmoe_gemm2_w4a16(ctypes.byref(bad), null, null, null, null, null, null, 0, null) == -1
+    assert lib.qmoe_gemm2_w4a16(ctypes.byref(bad), null, null, null, null, null, null, null, 0, null) == -1
     assert lib.qmoe_quant_act_mxfp8(4, 48, null, null, null, null) == -1
     misaligned = ctypes.c_void_p(0x1000 + 4)
     ok = ctypes.c_void_p(0x1000)
-    assert lib.qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), misaligned, ok, ok, ok, ok, ok, null, 0, null) == -1
+    assert lib.qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), misaligned, ok, ok, ok, ok, ok, ok, null, 0, null) == -1
     assert lib.qmoe_moe_forward(7, ctypes.byref(d), *([null] * 10), 0, null) == -1
+    # MXFP4 scale pre-pack: bad K, null pointers
+    assert lib.qmoe_prepack_mx_scales(128, 100, ok, ok, null) == -1
+    assert lib.qmoe_prepack_mx_scales(128, 128, null, ok, null) == -1
+    assert qb.mx_scales_packed_bytes(300, 4096) == 3 * 32 * 512
