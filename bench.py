@@ -249,8 +249,8 @@ def run_ours(args, w):
 
     t = {key: to_dev(v) for key, v in d.items()}
     if w.scheme == "mxfp4":  # one-time weight preparation (not part of a step)
-        t["w1_s"] = qb.prepack_mx_scales(t["w1_s"], H)
-        t["w2_s"] = qb.prepack_mx_scales(t["w2_s"], I)
+        t["w1"], t["w1_s"], t["w2"], t["w2_s"] = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
+        torch.cuda.synchronize(dev)
     dims = qb.dims(T, k, H, I, E)
     stream = torch.cuda.current_stream(dev)
 

@@ -46,8 +46,9 @@
  *             2i+1 in the high nibble; stored n = q + 8, value (n - 8) * s;
  *             scales fp16 [rows, K/32].
  *   E2M1      same nibble order; OCP MX element encoding; scales E8M0
- *             (value 2^(b-127)), one per 32 K elements, given to the GEMMs
- *             pre-packed by qmoe_prepack_mx_scales (see there).
+ *             (value 2^(b-127)), one per 32 K elements.  The MXFP4 GEMMs take
+ *             weights and scales pre-packed (qmoe_prepack_fp4_weights,
+ *             qmoe_prepack_mx_scales).
  *   E4M3      OCP "fn" fp8 (max 448, no infinities).
  *   int8      W int8 [rows, K], fp32 scale per output row.
  * Weight tensors: W1 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up), W2 [E, H, I].
@@ -173,6 +174,18 @@ int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t*
 size_t qmoe_mx_scales_packed_bytes(int64_t rows, int64_t K);
 int qmoe_prepack_mx_scales(int64_t rows, int64_t K, const uint8_t* s_rowmajor, uint8_t* s_packed, qmoe_stream_t stream);
 
+/* qmoe_prepack_fp4_weights -- one-time rearrangement of packed 4-bit weights
+ * [rows, K/2 bytes] (element 2i in the low nibble of byte i) into tile-major
+ * order: every 128-row x 128-element tile becomes one contiguous 8 KiB block,
+ * tile (rt, kt) at (rt * ceil(K/128) + kt) * 8192, tile row r at r * 64 in it,
+ * nibble order unchanged; padding is zero.  The MXFP4 GEMMs take their E2M1
+ * weights in this form (a tile is then one contiguous read from HBM).
+ * Output size: qmoe_fp4_weights_packed_bytes(rows, K), 32-byte aligned.  No
+ * counterpart on the pages (a storage-order choice, made at load time). */
+size_t qmoe_fp4_weights_packed_bytes(int64_t rows, int64_t K);
+int qmoe_prepack_fp4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor, uint8_t* w_packed,
+                             qmoe_stream_t stream);
+
 /* ---------------------------------------------------------------- stage 1: gate/up + SwiGLU
  *
  * For every expert e and slot s in [offsets[e], offsets[e+1]), with
@@ -248,8 +261,8 @@ int qmoe_combine(const qmoe_dims* d, const float* y, const float* topk_w, const 
  * One call for the whole path: routing, activation quantisation (MXFP4,
  * W8A8), stage 1, intermediate quantisation (W8A8), stage 2 and combine, all
  * launched in order on `stream`.  scheme: 0 = W4A16, 1 = MXFP4 x FP8,
- * 2 = W8A8.  Weights and scales as for the per-stage calls (MXFP4 weight
- * scales pre-packed).  All
+ * 2 = W8A8.  Weights and scales as for the per-stage calls (MXFP4 weights
+ * and scales pre-packed).  All
  * intermediates live in the caller's workspace of
  * qmoe_forward_workspace_bytes(d, scheme) bytes (256-byte aligned).
  * dev_status as for qmoe_align_sort. */

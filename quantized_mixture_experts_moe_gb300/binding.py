@@ -44,6 +44,8 @@ SIGNATURES = {
     "qmoe_quant_rows_int8_bf16": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
     "qmoe_quant_rows_int8_f32": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
     "qmoe_mx_scales_packed_bytes": ([_i64, _i64], _sz),
+    "qmoe_fp4_weights_packed_bytes": ([_i64, _i64], _sz),
+    "qmoe_prepack_fp4_weights": ([_i64, _i64, _vp, _vp, _vp], _i32),
     "qmoe_prepack_mx_scales": ([_i64, _i64, _vp, _vp, _vp], _i32),
     "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -170,6 +172,29 @@ def mx_scales_packed_bytes(rows: int, K: int) -> int:
 def qmoe_prepack_mx_scales(s_rowmajor, s_packed, rows: int, K: int, stream=None):
     _check(lib().qmoe_prepack_mx_scales(rows, K, _ptr(s_rowmajor), _ptr(s_packed), _stream(stream)),
            "qmoe_prepack_mx_scales")
+
+
+def fp4_weights_packed_bytes(rows: int, K: int) -> int:
+    return int(lib().qmoe_fp4_weights_packed_bytes(rows, K))
+
+
+def qmoe_prepack_fp4_weights(w_rowmajor, w_packed, rows: int, K: int, stream=None):
+    _check(lib().qmoe_prepack_fp4_weights(rows, K, _ptr(w_rowmajor), _ptr(w_packed), _stream(stream)),
+           "qmoe_prepack_fp4_weights")
+
+
+def prepack_fp4_weights(w_rowmajor, K: int, stream=None):
+    """Packed 4-bit weights [..., K/2] (rows = all leading dims) -> tile-major byte tensor."""
+    rows = w_rowmajor.numel() // (K // 2)
+    out = torch.empty(max(fp4_weights_packed_bytes(rows, K), 16), dtype=torch.uint8, device=w_rowmajor.device)
+    qmoe_prepack_fp4_weights(w_rowmajor.contiguous(), out, rows, K, stream)
+    return out
+
+
+def prepack_mxfp4(w1, w1_s, w2, w2_s, H: int, I: int, stream=None):
+    """All four MXFP4 weight tensors in the form the GEMMs take."""
+    return (prepack_fp4_weights(w1, H, stream), prepack_mx_scales(w1_s, H, stream),
+            prepack_fp4_weights(w2, I, stream), prepack_mx_scales(w2_s, I, stream))
 
 
 def prepack_mx_scales(s_rowmajor, K: int, stream=None):

@@ -9,26 +9,31 @@
 //   stage 2: y = W2 . h in fp32.
 //
 // Structure (one persistent CTA per SM, 7 warps):
-//   warp 0     TMA producer: 128-row FP4 weight tiles (the tensor map unpacks
-//              FP4 into the 16-byte-aligned form the MMA reads) and the
-//              matching pre-packed 512-byte scale atoms (bulk copies).
+//   warp 0     weight producer: TMA loads of 128-row x 128-element FP4 tiles
+//              (tile-major pre-packed weights: one contiguous 8 KiB read per
+//              tile; the tensor map unpacks FP4 to the 16-byte-aligned form
+//              the MMA reads) plus the matching 512-byte scale atoms.
 //   warp 1     activation producer: gathers the unit's token rows (stage 1:
 //              token = sorted pair id / k; stage 2: contiguous slots) with
 //              cp.async into the 128-byte-swizzled K-major layout, and their
 //              E8M0 scales into atom layout.
-//   warp 2     allocates tensor memory; one lane copies the stage's scale
-//              atoms into TMEM and issues the MMAs (M = 128 weight rows,
-//              N = tokens rounded up to 16, K = 32 per instruction).
+//   warp 2     allocates tensor memory; one lane copies the scale atoms into
+//              TMEM and issues the MMAs (M = 128 weight rows, N = tokens
+//              rounded up to 16, K = 32 per instruction).
 //   warps 3-6  epilogue: TMEM -> registers, SwiGLU + MX quantisation (stage
 //              1) or fp32 stores (stage 2).
-// The weights are the A operand ("swap AB"): per-expert token counts are
-// small at prefill sizes (about 80 at T = 4096), so tokens take the MMA's
-// N dimension, which can be as small as 16, instead of padding them to M.
+// Weights and activations flow through separate shared-memory rings: the
+// weight ring is deep (HBM latency), the activation ring shallow (its rows
+// come from L2).  With two accumulator buffers in TMEM, the epilogue of one
+// unit overlaps the MMAs of the next.
 //
-// A work unit is (expert, tile of up to 128 of its tokens, 128 output
-// columns); units are ordered with the column block fastest so concurrent
-// CTAs share the same activation rows through L2, and every unit streams a
-// disjoint slice of the expert weights exactly once.
+// The weights are the A operand ("swap AB"): per-expert token counts are
+// small at prefill sizes (about 80 at T = 4096), so tokens take the MMA's N
+// dimension (a multiple of 16) instead of being padded to M = 128.  A work
+// unit is (expert, tile of up to NMAX of its tokens, 128 output columns);
+// units are ordered with the column block fastest so concurrent CTAs share
+// activation rows through L2, and each unit streams a disjoint slice of the
+// expert's weights exactly once.
 #include "qmoe_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -38,34 +43,41 @@ namespace qmoe {
 
 namespace mx {
 
-constexpr int NMAX = 128;   // tokens per unit
 constexpr int THREADS = 224;
-constexpr int KSTAGE = 128; // K elements per pipeline stage (4 MMAs of K = 32)
-constexpr uint32_t FP4_TILE_TX = 128 * 64;  // bytes a 128x128 FP4 tile moves (packed)
+constexpr int KSTAGE = 128;                 // K elements per pipeline step (4 MMAs of K = 32)
+constexpr uint32_t FP4_TILE_TX = 128 * 64;  // bytes one 128x128 FP4 tile moves (packed)
 
-template <int STAGE>
+template <int STAGE, int NMAX_>
 struct Cfg {
-    static constexpr int STAGES = (STAGE == 1) ? 4 : 6;
-    static constexpr int AT = (STAGE == 1) ? 2 : 1;  // weight tiles per stage (gate + up)
-    static constexpr int LAG = STAGES - 2;             // cp.async stages in flight
+    static constexpr int NMAX = NMAX_;
+    static constexpr int AT = (STAGE == 1) ? 2 : 1;     // weight tiles per step (gate + up)
+    static constexpr int ACC_BUFS = (AT * NMAX * 2 <= 448) ? 2 : 1;
+    static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : 8;  // weight ring depth
+    static constexpr int SB = (STAGE == 1) ? 3 : 3;     // activation ring depth
+    static constexpr int LAG = 1;                        // cp.async steps in flight beyond the current one
+    static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
-    static constexpr int B_BYTES = NMAX * 128;
+    static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
     static constexpr int SFA_BYTES = AT * 512;
-    static constexpr int SFB_BYTES = 512;
+    static constexpr int SFB_BYTES = NSFB * 512;
     static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
-    static constexpr int SFA_OFF = B_OFF + STAGES * B_BYTES;
-    static constexpr int SFB_OFF = SFA_OFF + STAGES * SFA_BYTES;
-    static constexpr int BAR_OFF = SFB_OFF + STAGES * SFB_BYTES;
-    static constexpr int NBAR = 2 * STAGES + 2;
+    static constexpr int B_OFF = A_OFF + SA * A_BYTES;
+    static constexpr int SFA_OFF = B_OFF + SB * B_BYTES;
+    static constexpr int SFB_OFF = SFA_OFF + SA * SFA_BYTES;
+    static constexpr int BAR_OFF = SFB_OFF + SB * SFB_BYTES;
+    static constexpr int NBAR = 2 * SA + 2 * SB + 2 * ACC_BUFS;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SCHED_OFF = MISC_OFF + 64;
     static size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
-    // TMEM columns: accumulators (AT * NMAX), then per-stage scale slots
-    static constexpr uint32_t SFA_COL = AT * NMAX;
-    static constexpr uint32_t SFB_COL = SFA_COL + STAGES * AT * 4;
-    static_assert(SFB_COL + STAGES * 4 <= 512, "TMEM budget");
+    // TMEM columns: accumulators, then a 2-slot ring for scale factors
+    static constexpr uint32_t ACC_COLS = AT * NMAX;
+    static constexpr uint32_t SF_COL = ACC_BUFS * ACC_COLS;
+    static constexpr uint32_t SF_SLOT = AT * 4 + NSFB * 4;
+    static_assert(SF_COL + 2 * SF_SLOT <= 512, "TMEM budget");
+    static_assert(NMAX % 16 == 0 && NMAX <= 256, "N tile");
 };
+
+constexpr int MAX_E = 1024;  // schedule prefix kept in shared memory
 
 struct Args {
     int T, k, H, I, E;
@@ -80,6 +92,7 @@ struct Args {
     int32_t* status;
 };
 
+template <int NMAX>
 __device__ __forceinline__ void decode_unit(int u, int NB, const int* tile_start, int E, const int32_t* offsets,
                                             int& e, int& m0, int& ntok, int& nb) {
     const int t = u / NB;
@@ -99,20 +112,28 @@ __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
     atomicOr(status, QMOE_DEV_WAIT_TIMEOUT);
 }
 
-template <int STAGE>
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
+    int w = 1;
+    if (lane == 0) w = tc::mbar_wait(bar, parity) ? 1 : 0;
+    return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+}
+
+template <int STAGE, int NMAX>
 __global__ void __launch_bounds__(THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
-    using C = Cfg<STAGE>;
+    using C = Cfg<STAGE, NMAX>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::A_OFF;
     uint8_t* sB = smem + C::B_OFF;
     uint8_t* sSFA = smem + C::SFA_OFF;
     uint8_t* sSFB = smem + C::SFB_OFF;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-    uint64_t* empty = full + C::STAGES;
-    uint64_t* acc_full = empty + C::STAGES;
-    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* fullA = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* emptyA = fullA + C::SA;
+    uint64_t* fullB = emptyA + C::SA;
+    uint64_t* emptyB = fullB + C::SB;
+    uint64_t* acc_full = emptyB + C::SB;
+    uint64_t* acc_empty = acc_full + C::ACC_BUFS;
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
     int* tile_start = reinterpret_cast<int*>(smem + C::SCHED_OFF);
@@ -142,13 +163,19 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         }
         if (lane == 0) tile_start[E] = running;
     }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            tc::mbar_init(&full[s], 2);
-            tc::mbar_init(&empty[s], 1);
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < C::SA; ++s) {
+            tc::mbar_init(&fullA[s], 1);
+            tc::mbar_init(&emptyA[s], 1);
         }
-        tc::mbar_init(acc_full, 1);
-        tc::mbar_init(acc_empty, 4);
+        for (int s = 0; s < C::SB; ++s) {
+            tc::mbar_init(&fullB[s], 1);
+            tc::mbar_init(&emptyB[s], 1);
+        }
+        for (int b = 0; b < C::ACC_BUFS; ++b) {
+            tc::mbar_init(&acc_full[b], 1);
+            tc::mbar_init(&acc_empty[b], 4);
+        }
         *abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -171,24 +198,26 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             tc::prefetch_tensormap(&mapW);
             int stage = 0;
             uint32_t phase = 0;
+            const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb;
-                decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
-                const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
-                const int row0 = e * rows_per_e + nb * 128;
-                const int row1 = e * rows_per_e + a.I + nb * 128;  // up rows (stage 1)
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+                const int rt0 = (e * rows_per_e + nb * 128) / 128;
+                const int rt1 = (e * rows_per_e + a.I + nb * 128) / 128;  // up rows (stage 1)
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
-                    tc::mbar_arrive_expect_tx(&full[stage], C::AT * (FP4_TILE_TX + 512));
+                    if (!tc::mbar_wait(&emptyA[stage], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
+                    tc::mbar_arrive_expect_tx(&fullA[stage], C::AT * (FP4_TILE_TX + 512));
                     uint8_t* dA = sA + stage * C::A_BYTES;
                     uint8_t* dS = sSFA + stage * C::SFA_BYTES;
-                    tc::tma_load_2d(dA, &mapW, &full[stage], kt * KSTAGE, row0);
-                    tc::bulk_load(dS, a.w_s + ((int64_t)(row0 / 128) * KT + kt) * 512, 512, &full[stage]);
+                    const int64_t t0 = (int64_t)rt0 * KT + kt;
+                    tc::tma_load_2d(dA, &mapW, &fullA[stage], 0, (int)(t0 * 128));
+                    tc::bulk_load(dS, a.w_s + t0 * 512, 512, &fullA[stage]);
                     if (STAGE == 1) {
-                        tc::tma_load_2d(dA + 128 * 128, &mapW, &full[stage], kt * KSTAGE, row1);
-                        tc::bulk_load(dS + 512, a.w_s + ((int64_t)(row1 / 128) * KT + kt) * 512, 512, &full[stage]);
+                        const int64_t t1 = (int64_t)rt1 * KT + kt;
+                        tc::tma_load_2d(dA + 128 * 128, &mapW, &fullA[stage], 0, (int)(t1 * 128));
+                        tc::bulk_load(dS + 512, a.w_s + t1 * 512, 512, &fullA[stage]);
                     }
-                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == C::SA) { stage = 0; phase ^= 1; }
                 }
             }
         }
@@ -196,34 +225,37 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // ------------------------------------------------ activation producer (cp.async gather)
         int stage = 0, pending = 0;
         uint32_t phase = 0;
-        const int rowbytes = K;        // activation row bytes (one E4M3 code per element)
-        const int srowbytes = K / 32;  // scale bytes per row
+        const int rowbytes = K;        // one E4M3 code per element
+        const int srowbytes = K / 32;  // one E8M0 scale per 32 elements
+        constexpr int RPL = (NMAX + 31) / 32;  // rows per lane
         for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb;
-            decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
-            int64_t src_row[NMAX / 32];
+            decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+            int64_t src_row[RPL];
 #pragma unroll
-            for (int i = 0; i < NMAX / 32; ++i) {
+            for (int i = 0; i < RPL; ++i) {
                 const int r = lane + 32 * i;
                 src_row[i] = -1;
                 if (r < ntok) src_row[i] = (STAGE == 1) ? (int64_t)(a.sorted[m0 + r] / a.k) : (int64_t)(m0 + r);
             }
             bool ok = true;
             for (int kt = 0; kt < KT; ++kt) {
-                int w = 1;
-                if (lane == 0) w = tc::mbar_wait(&empty[stage], phase ^ 1) ? 1 : 0;
-                w = __shfl_sync(0xFFFFFFFFu, w, 0);
-                if (!w) { if (lane == 0) set_abort(abort_flag, a.status); ok = false; break; }
+                if (!warp_wait(&emptyB[stage], phase ^ 1, lane)) {
+                    if (lane == 0) set_abort(abort_flag, a.status);
+                    ok = false;
+                    break;
+                }
                 uint8_t* dB = sB + stage * C::B_BYTES;
                 uint8_t* dS = sSFB + stage * C::SFB_BYTES;
 #pragma unroll
-                for (int i = 0; i < NMAX / 32; ++i) {
+                for (int i = 0; i < RPL; ++i) {
                     if (src_row[i] < 0) continue;
                     const int r = lane + 32 * i;
                     const uint8_t* src = a.act + src_row[i] * rowbytes + kt * KSTAGE;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) tc::cp_async_16(dB + tc::sw128_offset(r, c), src + 16 * c);
-                    tc::cp_async_4(dS + 16 * (r & 31) + 4 * (r >> 5), a.act_s + src_row[i] * srowbytes + kt * 4);
+                    tc::cp_async_4(dS + (r >> 7) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3),
+                                   a.act_s + src_row[i] * srowbytes + kt * 4);
                 }
                 tc::cp_async_commit();
                 ++pending;
@@ -231,63 +263,73 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                     tc::cp_async_wait<C::LAG>();
                     tc::fence_proxy_async_smem();
                     __syncwarp();
-                    const int old = (stage - C::LAG + C::STAGES) % C::STAGES;
-                    if (lane == 0) tc::mbar_arrive(&full[old]);
+                    const int old = (stage - C::LAG + C::SB) % C::SB;
+                    if (lane == 0) tc::mbar_arrive(&fullB[old]);
                     --pending;
                 }
-                if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                if (++stage == C::SB) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
         }
-        // drain: signal the stages still pending
         tc::cp_async_wait<0>();
         tc::fence_proxy_async_smem();
         __syncwarp();
         for (int p = pending; p > 0; --p) {
-            const int old = (stage - p + C::STAGES) % C::STAGES;
-            if (lane == 0) tc::mbar_arrive(&full[old]);
+            const int old = (stage - p + C::SB) % C::SB;
+            if (lane == 0) tc::mbar_arrive(&fullB[old]);
         }
     } else if (warp == 2) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int sa = 0, sb = 0, sf = 0, ab = 0;
+            uint32_t pa = 0, pb = 0, pacc = 0;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb;
-                decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
                 const int nmma = (ntok + 15) & ~15;
-                if (!tc::mbar_wait(acc_empty, acc_phase ^ 1)) { set_abort(abort_flag, a.status); break; }
+                if (!tc::mbar_wait(&acc_empty[ab], pacc ^ 1)) { set_abort(abort_flag, a.status); break; }
                 tc::tc_fence_after();
+                const uint32_t dcol = ab * C::ACC_COLS;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!tc::mbar_wait(&full[stage], phase)) { set_abort(abort_flag, a.status); ok = false; break; }
+                    if (!tc::mbar_wait(&fullA[sa], pa) || !tc::mbar_wait(&fullB[sb], pb)) {
+                        set_abort(abort_flag, a.status);
+                        ok = false;
+                        break;
+                    }
                     tc::tc_fence_after();
-                    const uint32_t sfa_col = C::SFA_COL + stage * C::AT * 4;
-                    const uint32_t sfb_col = C::SFB_COL + stage * 4;
-                    const uint32_t sfa_addr = tc::smem_u32(sSFA + stage * C::SFA_BYTES);
-                    tc::tmem_cp_32x128b_warpx4(tm + sfa_col, tc::smem_desc(sfa_addr, 0, 128, 0));
-                    if (STAGE == 1) tc::tmem_cp_32x128b_warpx4(tm + sfa_col + 4, tc::smem_desc(sfa_addr + 512, 0, 128, 0));
-                    tc::tmem_cp_32x128b_warpx4(tm + sfb_col,
-                                               tc::smem_desc(tc::smem_u32(sSFB + stage * C::SFB_BYTES), 0, 128, 0));
-                    const uint32_t a0 = tc::smem_u32(sA + stage * C::A_BYTES);
-                    const uint32_t b0 = tc::smem_u32(sB + stage * C::B_BYTES);
+                    const uint32_t sfa_col = C::SF_COL + sf * C::SF_SLOT;
+                    const uint32_t sfb_col = sfa_col + C::AT * 4;
+                    const uint32_t sfa_addr = tc::smem_u32(sSFA + sa * C::SFA_BYTES);
+                    const uint32_t sfb_addr = tc::smem_u32(sSFB + sb * C::SFB_BYTES);
+#pragma unroll
+                    for (int t = 0; t < C::AT; ++t)
+                        tc::tmem_cp_32x128b_warpx4(tm + sfa_col + 4 * t, tc::smem_desc(sfa_addr + 512 * t, 0, 128, 0));
+#pragma unroll
+                    for (int t = 0; t < C::NSFB; ++t)
+                        tc::tmem_cp_32x128b_warpx4(tm + sfb_col + 4 * t, tc::smem_desc(sfb_addr + 512 * t, 0, 128, 0));
+                    const uint32_t a0 = tc::smem_u32(sA + sa * C::A_BYTES);
+                    const uint32_t b0 = tc::smem_u32(sB + sb * C::B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t idesc = tc::idesc_mxf8f6f4(128, nmma, 5, 0, kk, kk);
                         const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
                         const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + 32 * kk);
-                        tc::mma_mxf8f6f4(tm, tc::sdesc_kmajor_sw128(a0 + 32 * kk), bd, idesc, tm + sfa_col,
+                        tc::mma_mxf8f6f4(tm + dcol, tc::sdesc_kmajor_sw128(a0 + 32 * kk), bd, idesc, tm + sfa_col,
                                          tm + sfb_col, acc);
                         if (STAGE == 1)
-                            tc::mma_mxf8f6f4(tm + NMAX, tc::sdesc_kmajor_sw128(a0 + 128 * 128 + 32 * kk), bd, idesc,
-                                             tm + sfa_col + 4, tm + sfb_col, acc);
+                            tc::mma_mxf8f6f4(tm + dcol + NMAX, tc::sdesc_kmajor_sw128(a0 + 128 * 128 + 32 * kk), bd,
+                                             idesc, tm + sfa_col + 4, tm + sfb_col, acc);
                     }
-                    tc::mma_commit(&empty[stage]);
-                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                    tc::mma_commit(&emptyA[sa]);
+                    tc::mma_commit(&emptyB[sb]);
+                    if (++sa == C::SA) { sa = 0; pa ^= 1; }
+                    if (++sb == C::SB) { sb = 0; pb ^= 1; }
+                    sf ^= 1;
                 }
                 if (!ok) break;
-                tc::mma_commit(acc_full);
-                acc_phase ^= 1;
+                tc::mma_commit(&acc_full[ab]);
+                if (++ab == C::ACC_BUFS) { ab = 0; pacc ^= 1; }
             }
         }
         __syncwarp();
@@ -295,28 +337,31 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // ------------------------------------------------ epilogue (warps 3..6)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        uint32_t acc_phase = 0;
+        int ab = 0;
+        uint32_t pacc = 0;
         for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb;
-            decode_unit(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
-            int w = 1;
-            if (lane == 0) w = tc::mbar_wait(acc_full, acc_phase) ? 1 : 0;
-            w = __shfl_sync(0xFFFFFFFFu, w, 0);
-            if (!w) { if (lane == 0) set_abort(abort_flag, a.status); break; }
+            decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+            if (!warp_wait(&acc_full[ab], pacc, lane)) {
+                if (lane == 0) set_abort(abort_flag, a.status);
+                break;
+            }
             tc::tc_fence_after();
+            const uint32_t dcol = ab * C::ACC_COLS;
             const int n = nb * 128 + q * 32 + lane;  // this lane's output column
             for (int c0 = 0; c0 < ntok; c0 += 16) {
                 uint32_t g[16];
-                tc::tmem_ld_32x32b_x16(tm + lane_addr + c0, g);
+                tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + c0, g);
                 if (STAGE == 1) {
                     uint32_t uu[16];
-                    tc::tmem_ld_32x32b_x16(tm + lane_addr + NMAX + c0, uu);
+                    tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + NMAX + c0, uu);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int c = c0 + j;
                         if (c >= ntok) break;  // warp-uniform
-                        const float h = silu_mul(__uint_as_float(g[j]), __uint_as_float(uu[j]));
+                        const float gv = __uint_as_float(g[j]);
+                        const float h = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(uu[j]);
                         float amax = fabsf(h);
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -342,8 +387,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             }
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(acc_empty);
-            acc_phase ^= 1;
+            if (lane == 0) tc::mbar_arrive(&acc_empty[ab]);
+            if (++ab == C::ACC_BUFS) { ab = 0; pacc ^= 1; }
         }
     }
 
@@ -381,21 +426,15 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-int num_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
-// FP4 weight matrix [rows, K] (K/2 bytes per row) as a tensor map whose
-// 128x128 boxes land in shared memory unpacked to 16-byte-aligned groups,
-// 128-byte swizzled.
-static int make_fp4_map(CUtensorMap* map, const void* w, int64_t rows, int64_t K) {
+// Tile-major pre-packed FP4 weights viewed as a 2D tensor of 64-byte rows
+// (128 elements), one 128-row box per 128x128 tile: each box is a contiguous
+// 8 KiB read, unpacked by the TMA to 16-byte-aligned groups and 128-byte
+// swizzled in shared memory.
+static int make_fp4_map(CUtensorMap* map, const void* w, int64_t tiles) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return QMOE_ERR_CUDA;
-    cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t gstride[1] = {(cuuint64_t)(K / 2)};
+    cuuint64_t gdim[2] = {128, (cuuint64_t)(tiles * 128)};
+    cuuint64_t gstride[1] = {64};
     cuuint32_t box[2] = {128, 128};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(w), gdim, gstride, box, estr,
@@ -404,31 +443,42 @@ static int make_fp4_map(CUtensorMap* map, const void* w, int64_t rows, int64_t K
     return r == CUDA_SUCCESS ? QMOE_OK : QMOE_ERR_UNSUPPORTED;
 }
 
-bool mx_tc_supported(const qmoe_dims* d, const void* w1, const void* w2) {
-    auto a32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
-    return d->H % 128 == 0 && d->I % 128 == 0 && d->E <= 4096 && (int64_t)d->E * 2 * d->I < (1ll << 31) &&
-           (int64_t)d->E * d->H < (1ll << 31) && (!w1 || a32(w1)) && (!w2 || a32(w2));
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
 }
 
-template <int STAGE>
-static int launch(const qmoe_dims* d, const void* w, Args a, cudaStream_t st) {
-    using C = Cfg<STAGE>;
+bool mx_tc_supported(const qmoe_dims* d, const void* w1, const void* w2) {
+    auto a32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+    const int64_t tiles1 = (int64_t)d->E * 2 * d->I / 128 * (d->H / 128);
+    const int64_t tiles2 = (int64_t)d->E * d->H / 128 * (d->I / 128);
+    return d->H % 128 == 0 && d->I % 128 == 0 && d->E <= MAX_E && tiles1 * 128 < (1ll << 31) &&
+           tiles2 * 128 < (1ll << 31) && (!w1 || a32(w1)) && (!w2 || a32(w2));
+}
+
+template <int STAGE, int NMAX>
+static int launch_cfg(const void* w, int64_t tiles, const Args& a, cudaStream_t st) {
+    using C = Cfg<STAGE, NMAX>;
     CUtensorMap map;
-    const int64_t rows = (STAGE == 1) ? (int64_t)d->E * 2 * d->I : (int64_t)d->E * d->H;
-    const int64_t K = (STAGE == 1) ? d->H : d->I;
-    int rc = make_fp4_map(&map, w, rows, K);
+    int rc = make_fp4_map(&map, w, tiles);
     if (rc != QMOE_OK) return rc;
-    const size_t smem = C::smem_bytes(d->E);
-    static std::once_flag attr_once;
-    std::call_once(attr_once, [smem] {
-        cudaFuncSetAttribute(mx_gemm_kernel<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::smem_bytes(4096));
-    });
+    const size_t smem = C::smem_bytes(a.E);
+    if (cudaFuncSetAttribute(mx_gemm_kernel<STAGE, NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::smem_bytes(MAX_E)) != cudaSuccess)
+        return QMOE_ERR_LAUNCH;
     const int grid = num_sms();
     if (grid <= 0) return QMOE_ERR_CUDA;
-    mx_gemm_kernel<STAGE><<<grid, THREADS, smem, st>>>(map, a);
+    mx_gemm_kernel<STAGE, NMAX><<<grid, THREADS, smem, st>>>(map, a);
     return launch_status();
 }
+
+// Token-tile size: the average expert load decides (the grid never syncs
+// with the host to look at the real counts).  Up to ~100 tokens per expert a
+// 112-token tile with two accumulator buffers; above, 224-token tiles so an
+// expert's weights are still streamed once.
+static bool big_tiles(const qmoe_dims* d) { return (int64_t)d->T * d->k > (int64_t)96 * d->E; }
 
 }  // namespace mx
 
@@ -439,7 +489,8 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, cons
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = x_q; a.act_s = x_s; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted;
     a.h_q = h_q; a.h_s = h_s; a.status = status;
-    return mx::launch<1>(d, w1, a, st);
+    const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * (d->H / 128);
+    return mx::big_tiles(d) ? mx::launch_cfg<1, 224>(w1, tiles, a, st) : mx::launch_cfg<1, 112>(w1, tiles, a, st);
 }
 
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2, const uint8_t* w2_s,
@@ -447,7 +498,8 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, cons
     mx::Args a{};
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = h_q; a.act_s = h_s; a.w_s = w2_s; a.offsets = offsets; a.y = y; a.status = status;
-    return mx::launch<2>(d, w2, a, st);
+    const int64_t tiles = (int64_t)d->E * d->H / 128 * (d->I / 128);
+    return mx::launch_cfg<2, 224>(w2, tiles, a, st);
 }
 
 bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2) { return mx::mx_tc_supported(d, w1, w2); }

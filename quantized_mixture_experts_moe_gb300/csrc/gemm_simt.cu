@@ -106,7 +106,15 @@ __device__ __forceinline__ void load_w(const SimtArgs& a, int64_t wrow, int K, i
 #pragma unroll
         for (int i = 0; i < NE; ++i) o[i] = (int32_t)(int8_t)(v[i / 4] >> (8 * (i % 4)));
     } else {
-        const uint8_t* p = static_cast<const uint8_t*>(a.w) + wrow * (K / 2) + kk / 2;
+        const uint8_t* p;
+        if constexpr (SCHEME == S_W4A16) {
+            p = static_cast<const uint8_t*>(a.w) + wrow * (K / 2) + kk / 2;
+        } else {
+            // tile-major pre-packed: 128x128 tiles of 8 KiB, 64 bytes per tile row
+            const int64_t KT = (K + 127) / 128;
+            p = static_cast<const uint8_t*>(a.w) + ((wrow / 128) * KT + kk / 128) * 8192 + (wrow & 127) * 64 +
+                (kk & 127) / 2;
+        }
         uint32_t v[NE / 8];
         if constexpr (NE == 16) {
             const uint2 t = *reinterpret_cast<const uint2*>(p);

@@ -46,3 +46,48 @@ extern "C" int qmoe_prepack_mx_scales(int64_t rows, int64_t K, const uint8_t* s_
                                                                                 (K + 127) / 128, total);
     return launch_status();
 }
+
+// ------------------------------------------------------------------ 4-bit weights, tile-major
+//
+// Packed 4-bit weights W[rows][K/2 bytes] (element 2i in the low nibble of
+// byte i) rearranged so that every 128-row x 128-element tile is one
+// contiguous 8 KiB block: tile (rt, kt) at ((rt * KT) + kt) * 8192, tile row r
+// at r * 64 inside it, same nibble order.  A tensor-core kernel then streams
+// each tile with one contiguous read instead of 128 scattered 64-byte pieces.
+// Rows and columns beyond the tensor are zero.
+namespace qmoe {
+
+__global__ void prepack_fp4_kernel(const uint8_t* __restrict__ src, uint4* __restrict__ dst, int64_t rows,
+                                   int64_t Kbytes, int64_t KT, int64_t total16) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total16) return;
+    const int64_t tile = i >> 9;          // 512 chunks of 16 B per tile
+    const int within = (int)(i & 511);
+    const int r = within >> 2, part = within & 3;
+    const int64_t rt = tile / KT, kt = tile - rt * KT;
+    const int64_t row = rt * 128 + r;
+    const int64_t b0 = kt * 64 + part * 16;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < rows && b0 + 16 <= Kbytes) v = *reinterpret_cast<const uint4*>(src + row * Kbytes + b0);
+    dst[i] = v;
+}
+
+}  // namespace qmoe
+
+extern "C" size_t qmoe_fp4_weights_packed_bytes(int64_t rows, int64_t K) {
+    if (rows <= 0 || K <= 0 || K % 32 != 0) return 0;
+    return (size_t)(((rows + 127) / 128) * ((K + 127) / 128) * 8192);
+}
+
+extern "C" int qmoe_prepack_fp4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor, uint8_t* w_packed,
+                                        qmoe_stream_t stream) {
+    using namespace qmoe;
+    if (rows <= 0 || K <= 0 || K % 32 != 0 || !w_rowmajor || !w_packed || !aligned16(w_rowmajor) ||
+        !aligned16(w_packed))
+        return QMOE_ERR_ARG;
+    const int64_t KT = (K + 127) / 128;
+    const int64_t total16 = ((rows + 127) / 128) * KT * 512;
+    prepack_fp4_kernel<<<(unsigned)((total16 + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+        w_rowmajor, reinterpret_cast<uint4*>(w_packed), rows, K / 2, KT, total16);
+    return launch_status();
+}

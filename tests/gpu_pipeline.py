@@ -50,8 +50,7 @@ def device_weights(w, inp):
     """Weights as the library takes them (MXFP4 scales pre-packed)."""
     t = {key: dev(inp[key]) for key in ("w1", "w1_s", "w2", "w2_s")}
     if w.scheme == "mxfp4":
-        t["w1_s"] = qb.prepack_mx_scales(t["w1_s"], w.H)
-        t["w2_s"] = qb.prepack_mx_scales(t["w2_s"], w.I)
+        t["w1"], t["w1_s"], t["w2"], t["w2_s"] = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], w.H, w.I)
     return t
 
 
@@ -78,10 +77,9 @@ def run_layer(w, inp, keep=False):
         xq, xs = empty((T, H), torch.uint8), empty((T, H // 32), torch.uint8)
         qb.qmoe_quant_act_mxfp8(t["x"], xq, xs)
         hq, hs = empty((P, I), torch.uint8), empty((P, I // 32), torch.uint8)
-        w1p = qb.prepack_mx_scales(t["w1_s"], H)
-        w2p = qb.prepack_mx_scales(t["w2_s"], I)
-        qb.qmoe_gemm1_swiglu_mxfp4(d, xq, xs, t["w1"], w1p, offsets, sorted_ids, hq, hs, status, ws)
-        qb.qmoe_gemm2_mxfp4(d, hq, hs, t["w2"], w2p, offsets, y, status, ws)
+        w1, w1p, w2, w2p = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
+        qb.qmoe_gemm1_swiglu_mxfp4(d, xq, xs, w1, w1p, offsets, sorted_ids, hq, hs, status, ws)
+        qb.qmoe_gemm2_mxfp4(d, hq, hs, w2, w2p, offsets, y, status, ws)
         res.update(xq=xq, xs=xs, hq=hq, hs=hs)
     else:
         xq, xs = empty((T, H), torch.int8), empty(T, torch.float32)

@@ -184,7 +184,8 @@ def test_stage2_against_oracle(w):
         assert rel_l2(gp.host(y), ref) < 1e-5
     elif w.scheme == "mxfp4":
         w2p = qb.prepack_mx_scales(gp.dev(wts["w2_s"]), w.I)
-        qb.qmoe_gemm2_mxfp4(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), gp.dev(wts["w2"]), w2p, t_off, y)
+        w2w = qb.prepack_fp4_weights(gp.dev(wts["w2"]), w.I)
+        qb.qmoe_gemm2_mxfp4(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), w2w, w2p, t_off, y)
         ref = oracle.stage2("mxfp4", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"])
         torch.cuda.synchronize()
         assert rel_l2(gp.host(y), ref) < 1e-5
@@ -303,14 +304,14 @@ def test_layer_zero_tokens():
 
 @pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
 def test_forward_entry_point_matches_stagewise_and_is_deterministic(scheme):
-    w = gen.custom(f"fwd_{scheme}", scheme, 33, 512, 10, 4, 128, seed=61)
+    w = gen.custom(f"fwd_{scheme}", scheme, 33, 512, 10, 4, 128, seed=61)  # I, H multiples of 128
     d = gen.make_all(w)
     stage = gp.run_layer(w, d)
     outs = []
     wt = gp.device_weights(w, d)
     for _ in range(2):
         out, status = qb.moe_forward(scheme, gp.dev(d["x"]), gp.dev(d["topk_ids"]), gp.dev(d["topk_w"]),
-                                     wt["w1"], wt["w1_s"], wt["w2"], wt["w2_s"])
+                                     wt["w1"], wt["w1_s"], wt["w2"], wt["w2_s"], I=w.I, E=w.E)
         torch.cuda.synchronize()
         outs.append(gp.host(out, np.uint16))
         assert int(status.item()) == 0
