@@ -8,7 +8,7 @@
 //            E4M3 codes + E8M0 scales per 32 columns of I;
 //   stage 2: y = W2 . h in fp32.
 //
-// Structure (one persistent CTA per SM, 7 warps):
+// Structure (one persistent CTA per SM, 11 warps):
 //   warp 0     weight producer: TMA loads of 128-row x 128-element FP4 tiles
 //              (tile-major pre-packed weights: one contiguous 8 KiB read per
 //              tile; the tensor map unpacks FP4 to the 16-byte-aligned form
@@ -20,8 +20,9 @@
 //   warp 2     allocates tensor memory; one lane copies the scale atoms into
 //              TMEM and issues the MMAs (M = 128 weight rows, N = tokens
 //              rounded up to 16, K = 32 per instruction).
-//   warps 3-6  epilogue: TMEM -> registers, SwiGLU + MX quantisation (stage
-//              1) or fp32 stores (stage 2).
+//   warps 3-10 epilogue (two warps per TMEM lane quadrant, alternating
+//              16-token chunks): TMEM -> registers, SwiGLU + MX quantisation
+//              (stage 1) or fp32 stores (stage 2).
 // Weights and activations flow through separate shared-memory rings: the
 // weight ring is deep (HBM latency), the activation ring shallow (its rows
 // come from L2).  With two accumulator buffers in TMEM, the epilogue of one
@@ -43,7 +44,8 @@ namespace qmoe {
 
 namespace mx {
 
-constexpr int THREADS = 224;
+constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant, splitting the token columns
+constexpr int THREADS = (3 + EPI_WARPS) * 32;
 constexpr int KSTAGE = 128;                 // K elements per pipeline step (4 MMAs of K = 32)
 constexpr uint32_t FP4_TILE_TX = 128 * 64;  // bytes one 128x128 FP4 tile moves (packed)
 
@@ -52,9 +54,12 @@ struct Cfg {
     static constexpr int NMAX = NMAX_;
     static constexpr int AT = (STAGE == 1) ? 2 : 1;     // weight tiles per step (gate + up)
     static constexpr int ACC_BUFS = (AT * NMAX * 2 <= 448) ? 2 : 1;
-    static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : 8;  // weight ring depth
-    static constexpr int SB = (STAGE == 1) ? 3 : 3;     // activation ring depth
-    static constexpr int LAG = 1;                        // cp.async steps in flight beyond the current one
+    // ring depths: weights come from HBM (deep), activations from L2; the
+    // activation producer keeps LAG cp.async steps in flight behind the one
+    // it is issuing.  Sized to the 227 KB of shared memory per CTA.
+    static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : 8;
+    static constexpr int SB = (NMAX <= 128) ? ((STAGE == 1) ? 4 : 6) : 3;
+    static constexpr int LAG = SB - 1;
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
@@ -77,7 +82,7 @@ struct Cfg {
     static_assert(NMAX % 16 == 0 && NMAX <= 256, "N tile");
 };
 
-constexpr int MAX_E = 1024;  // schedule prefix kept in shared memory
+constexpr int MAX_E = 512;  // schedule prefix kept in shared memory
 
 struct Args {
     int T, k, H, I, E;
@@ -174,7 +179,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         }
         for (int b = 0; b < C::ACC_BUFS; ++b) {
             tc::mbar_init(&acc_full[b], 1);
-            tc::mbar_init(&acc_empty[b], 4);
+            tc::mbar_init(&acc_empty[b], EPI_WARPS);
         }
         *abort_flag = 0;
         tc::fence_barrier_init();
@@ -334,8 +339,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 3..6)
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        // ------------------------------------------------ epilogue (warps 3..10)
+        const int q = warp & 3;               // TMEM lane quadrant this warp may access
+        const int half = (warp - 3) >> 2;     // which 16-column chunks it takes
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int ab = 0;
         uint32_t pacc = 0;
@@ -349,7 +355,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             tc::tc_fence_after();
             const uint32_t dcol = ab * C::ACC_COLS;
             const int n = nb * 128 + q * 32 + lane;  // this lane's output column
-            for (int c0 = 0; c0 < ntok; c0 += 16) {
+            for (int c0 = 16 * half; c0 < ntok; c0 += 32) {
                 uint32_t g[16];
                 tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + c0, g);
                 if (STAGE == 1) {
@@ -499,7 +505,7 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, cons
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = h_q; a.act_s = h_s; a.w_s = w2_s; a.offsets = offsets; a.y = y; a.status = status;
     const int64_t tiles = (int64_t)d->E * d->H / 128 * (d->I / 128);
-    return mx::launch_cfg<2, 224>(w2, tiles, a, st);
+    return mx::big_tiles(d) ? mx::launch_cfg<2, 224>(w2, tiles, a, st) : mx::launch_cfg<2, 112>(w2, tiles, a, st);
 }
 
 bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2) { return mx::mx_tc_supported(d, w1, w2); }
