@@ -54,12 +54,10 @@ struct Cfg {
     static constexpr int NMAX = NMAX_;
     static constexpr int AT = (STAGE == 1) ? 2 : 1;     // weight tiles per step (gate + up)
     static constexpr int ACC_BUFS = (AT * NMAX * 2 <= 448) ? 2 : 1;
-    // ring depths: weights come from HBM (deep), activations from L2; the
-    // activation producer keeps LAG cp.async steps in flight behind the one
-    // it is issuing.  Sized to the 227 KB of shared memory per CTA.
+    // ring depths: weights come from HBM (deep), activations from L2.  Sized
+    // to the 227 KB of shared memory per CTA.
     static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : 8;
     static constexpr int SB = (NMAX <= 128) ? ((STAGE == 1) ? 4 : 6) : 3;
-    static constexpr int LAG = SB - 1;
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
@@ -228,12 +226,25 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         }
     } else if (warp == 1) {
         // ------------------------------------------------ activation producer (cp.async gather)
+        // Each step's copies form one cp.async group.  A step is published
+        // (fence + arrive on fullB) as soon as its group has landed; the
+        // producer publishes finished groups whenever it would otherwise wait
+        // for a free slot, so completed data never waits behind new issues.
         int stage = 0, pending = 0;
         uint32_t phase = 0;
         const int rowbytes = K;        // one E4M3 code per element
         const int srowbytes = K / 32;  // one E8M0 scale per 32 elements
         constexpr int RPL = (NMAX + 31) / 32;  // rows per lane
-        for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+        auto publish_oldest = [&]() {
+            tc::cp_async_wait_dyn(pending - 1);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            const int old = (stage - pending + C::SB) % C::SB;
+            if (lane == 0) tc::mbar_arrive(&fullB[old]);
+            --pending;
+        };
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb;
             decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
             int64_t src_row[RPL];
@@ -243,13 +254,20 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 src_row[i] = -1;
                 if (r < ntok) src_row[i] = (STAGE == 1) ? (int64_t)(a.sorted[m0 + r] / a.k) : (int64_t)(m0 + r);
             }
-            bool ok = true;
             for (int kt = 0; kt < KT; ++kt) {
-                if (!warp_wait(&emptyB[stage], phase ^ 1, lane)) {
-                    if (lane == 0) set_abort(abort_flag, a.status);
-                    ok = false;
+                // wait for a free slot, publishing finished steps meanwhile
+                while (true) {
+                    int free_slot = 0;
+                    if (lane == 0) free_slot = tc::mbar_try_wait(&emptyB[stage], phase ^ 1) ? 1 : 0;
+                    if (__shfl_sync(0xFFFFFFFFu, free_slot, 0)) break;
+                    if (pending > 0) { publish_oldest(); continue; }
+                    if (!warp_wait(&emptyB[stage], phase ^ 1, lane)) {
+                        if (lane == 0) set_abort(abort_flag, a.status);
+                        ok = false;
+                    }
                     break;
                 }
+                if (!ok) break;
                 uint8_t* dB = sB + stage * C::B_BYTES;
                 uint8_t* dS = sSFB + stage * C::SFB_BYTES;
 #pragma unroll
@@ -264,25 +282,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 }
                 tc::cp_async_commit();
                 ++pending;
-                if (pending > C::LAG) {
-                    tc::cp_async_wait<C::LAG>();
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    const int old = (stage - C::LAG + C::SB) % C::SB;
-                    if (lane == 0) tc::mbar_arrive(&fullB[old]);
-                    --pending;
-                }
                 if (++stage == C::SB) { stage = 0; phase ^= 1; }
             }
-            if (!ok) break;
         }
-        tc::cp_async_wait<0>();
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        for (int p = pending; p > 0; --p) {
-            const int old = (stage - p + C::SB) % C::SB;
-            if (lane == 0) tc::mbar_arrive(&fullB[old]);
-        }
+        while (pending > 0) publish_oldest();
     } else if (warp == 2) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -348,7 +351,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb;
             decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
-            if (!warp_wait(&acc_full[ab], pacc, lane)) {
+            int w = 1;
+            if (lane == 0) w = tc::mbar_wait_sleep(&acc_full[ab], pacc) ? 1 : 0;
+            if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {
                 if (lane == 0) set_abort(abort_flag, a.status);
                 break;
             }
