@@ -58,6 +58,7 @@ struct Cfg {
     // to the 227 KB of shared memory per CTA.
     static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : 8;
     static constexpr int SB = (NMAX <= 128) ? ((STAGE == 1) ? 4 : 6) : 3;
+    static constexpr int PF = 2 * SA;                    // L2 prefetch distance (steps)
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
@@ -202,6 +203,34 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             int stage = 0;
             uint32_t phase = 0;
             const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
+            // L2 prefetch cursor, PF steps ahead of the shared-memory loads:
+            // the ring's loads then hit L2 while DRAM sees PF more tiles in flight.
+            int pu = blockIdx.x, pkt = 0, prt0 = 0, prt1 = 0;
+            auto pf_decode = [&]() {
+                if (pu >= total_units) return;
+                int e_, m0_, nt_, nb_;
+                decode_unit<NMAX>(pu, NB, tile_start, E, a.offsets, e_, m0_, nt_, nb_);
+                prt0 = (e_ * rows_per_e + nb_ * 128) / 128;
+                prt1 = (e_ * rows_per_e + a.I + nb_ * 128) / 128;
+            };
+            auto pf_issue = [&]() {
+                if (pu >= total_units) return;
+                const int64_t t0 = (int64_t)prt0 * KT + pkt;
+                tc::tma_prefetch_2d(&mapW, 0, (int)(t0 * 128));
+                tc::bulk_prefetch_l2(a.w_s + t0 * 512, 512);
+                if (STAGE == 1) {
+                    const int64_t t1 = (int64_t)prt1 * KT + pkt;
+                    tc::tma_prefetch_2d(&mapW, 0, (int)(t1 * 128));
+                    tc::bulk_prefetch_l2(a.w_s + t1 * 512, 512);
+                }
+                if (++pkt == KT) {
+                    pkt = 0;
+                    pu += gridDim.x;
+                    pf_decode();
+                }
+            };
+            pf_decode();
+            for (int i = 0; i < C::PF; ++i) pf_issue();
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb;
                 decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
@@ -220,6 +249,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                         tc::tma_load_2d(dA + 128 * 128, &mapW, &fullA[stage], 0, (int)(t1 * 128));
                         tc::bulk_load(dS + 512, a.w_s + t1 * 512, 512, &fullA[stage]);
                     }
+                    pf_issue();
                     if (++stage == C::SA) { stage = 0; phase ^= 1; }
                 }
             }
