@@ -8,19 +8,20 @@
 //            E4M3 codes + E8M0 scales per 32 columns of I;
 //   stage 2: y = W2 . h in fp32.
 //
-// Structure (one persistent CTA per SM, 11 warps):
+// Structure (one persistent CTA per SM, 14 warps):
 //   warp 0     weight producer: TMA loads of 128-row x 128-element FP4 tiles
 //              (tile-major pre-packed weights: one contiguous 8 KiB read per
 //              tile; the tensor map unpacks FP4 to the 16-byte-aligned form
 //              the MMA reads) plus the matching 512-byte scale atoms.
-//   warp 1     activation producer: gathers the unit's token rows (stage 1:
-//              token = sorted pair id / k; stage 2: contiguous slots) with
-//              cp.async into the 128-byte-swizzled K-major layout, and their
-//              E8M0 scales into atom layout.
-//   warp 2     allocates tensor memory; one lane copies the scale atoms into
+//   warps 1-4  activation producers, taking pipeline steps round-robin:
+//              gather the unit's token rows (stage 1: token = sorted pair id
+//              / k; stage 2: contiguous slots) with cp.async into the
+//              128-byte-swizzled K-major layout, and their E8M0 scales into
+//              atom layout.
+//   warp 5     allocates tensor memory; one lane copies the scale atoms into
 //              TMEM and issues the MMAs (M = 128 weight rows, N = tokens
 //              rounded up to 16, K = 32 per instruction).
-//   warps 3-10 epilogue (two warps per TMEM lane quadrant, alternating
+//   warps 6-13 epilogue (two warps per TMEM lane quadrant, alternating
 //              16-token chunks): TMEM -> registers, SwiGLU + MX quantisation
 //              (stage 1) or fp32 stores (stage 2).
 // Weights and activations flow through separate shared-memory rings: the
@@ -44,8 +45,13 @@ namespace qmoe {
 
 namespace mx {
 
+// warp roles
+constexpr int WARP_A = 0;                   // weight producer (TMA)
+constexpr int WARP_B0 = 1, NBW = 4;         // activation producers, steps taken round-robin
+constexpr int WARP_MMA = WARP_B0 + NBW;     // TMEM owner + MMA issuer
+constexpr int WARP_EPI0 = WARP_MMA + 1;     // epilogue warps
 constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant, splitting the token columns
-constexpr int THREADS = (3 + EPI_WARPS) * 32;
+constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
 constexpr int KSTAGE = 128;                 // K elements per pipeline step (4 MMAs of K = 32)
 constexpr uint32_t FP4_TILE_TX = 128 * 64;  // bytes one 128x128 FP4 tile moves (packed)
 
@@ -56,8 +62,8 @@ struct Cfg {
     static constexpr int ACC_BUFS = (AT * NMAX * 2 <= 448) ? 2 : 1;
     // ring depths: weights come from HBM (deep), activations from L2.  Sized
     // to the 227 KB of shared memory per CTA.
-    static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : 8;
-    static constexpr int SB = (NMAX <= 128) ? ((STAGE == 1) ? 4 : 6) : 3;
+    static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : (NMAX <= 128 ? 8 : 6);
+    static constexpr int SB = (NMAX <= 128) ? ((STAGE == 1) ? 4 : 6) : ((STAGE == 1) ? 3 : 4);
     static constexpr int PF = 2 * SA;                    // L2 prefetch distance (steps)
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
@@ -72,7 +78,7 @@ struct Cfg {
     static constexpr int NBAR = 2 * SA + 2 * SB + 2 * ACC_BUFS;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SCHED_OFF = MISC_OFF + 64;
-    static size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
+    static constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
     // TMEM columns: accumulators, then a 2-slot ring for scale factors
     static constexpr uint32_t ACC_COLS = AT * NMAX;
     static constexpr uint32_t SF_COL = ACC_BUFS * ACC_COLS;
@@ -82,6 +88,9 @@ struct Cfg {
 };
 
 constexpr int MAX_E = 512;  // schedule prefix kept in shared memory
+static_assert(Cfg<1, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<1, 224>::smem_bytes(MAX_E) <= 232448 &&
+                  Cfg<2, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<2, 224>::smem_bytes(MAX_E) <= 232448,
+              "shared memory per CTA");
 
 struct Args {
     int T, k, H, I, E;
@@ -167,7 +176,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         }
         if (lane == 0) tile_start[E] = running;
     }
-    if (threadIdx.x == 32) {
+    if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::SA; ++s) {
             tc::mbar_init(&fullA[s], 1);
             tc::mbar_init(&emptyA[s], 1);
@@ -187,7 +196,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     const int total_units = tile_start[E] * NB;
     if ((int)blockIdx.x >= total_units) return;  // no work: nothing allocated yet
 
-    if (warp == 2) {
+    if (warp == WARP_MMA) {
         tc::tmem_alloc(tmem_base_smem, 512);
         tc::tmem_relinquish();
     }
@@ -196,7 +205,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     tc::tc_fence_after();
     const uint32_t tm = *tmem_base_smem;
 
-    if (warp == 0) {
+    if (warp == WARP_A) {
         // ------------------------------------------------ weight producer (TMA)
         if (lane == 0) {
             tc::prefetch_tensormap(&mapW);
@@ -254,25 +263,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ activation producer (cp.async gather)
-        // Each step's copies form one cp.async group.  A step is published
-        // (fence + arrive on fullB) as soon as its group has landed; the
-        // producer publishes finished groups whenever it would otherwise wait
-        // for a free slot, so completed data never waits behind new issues.
-        int stage = 0, pending = 0;
-        uint32_t phase = 0;
+    } else if (warp < WARP_MMA) {
+        // ------------------------------------------------ activation producers (cp.async gather)
+        // NBW warps take the pipeline steps round-robin.  A warp waits for its
+        // slot, issues the step's copies as one cp.async group, waits for that
+        // group, fences the writes to the async proxy and publishes the step:
+        // NBW L2 round trips are in flight at once.
+        const int wb = warp - WARP_B0;
         const int rowbytes = K;        // one E4M3 code per element
         const int srowbytes = K / 32;  // one E8M0 scale per 32 elements
         constexpr int RPL = (NMAX + 31) / 32;  // rows per lane
-        auto publish_oldest = [&]() {
-            tc::cp_async_wait_dyn(pending - 1);
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            const int old = (stage - pending + C::SB) % C::SB;
-            if (lane == 0) tc::mbar_arrive(&fullB[old]);
-            --pending;
-        };
+        int64_t step = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb;
@@ -284,22 +285,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 src_row[i] = -1;
                 if (r < ntok) src_row[i] = (STAGE == 1) ? (int64_t)(a.sorted[m0 + r] / a.k) : (int64_t)(m0 + r);
             }
-            for (int kt = 0; kt < KT; ++kt) {
-                // wait for a free slot, publishing finished steps meanwhile
-                while (true) {
-                    int free_slot = 0;
-                    if (lane == 0) free_slot = tc::mbar_try_wait(&emptyB[stage], phase ^ 1) ? 1 : 0;
-                    if (__shfl_sync(0xFFFFFFFFu, free_slot, 0)) break;
-                    if (pending > 0) { publish_oldest(); continue; }
-                    if (!warp_wait(&emptyB[stage], phase ^ 1, lane)) {
-                        if (lane == 0) set_abort(abort_flag, a.status);
-                        ok = false;
-                    }
+            for (int kt = 0; kt < KT; ++kt, ++step) {
+                if ((int)(step % NBW) != wb) continue;
+                const int slot = (int)(step % C::SB);
+                const uint32_t parity = (uint32_t)((step / C::SB) & 1) ^ 1u;
+                if (!warp_wait(&emptyB[slot], parity, lane)) {
+                    if (lane == 0) set_abort(abort_flag, a.status);
+                    ok = false;
                     break;
                 }
-                if (!ok) break;
-                uint8_t* dB = sB + stage * C::B_BYTES;
-                uint8_t* dS = sSFB + stage * C::SFB_BYTES;
+                uint8_t* dB = sB + slot * C::B_BYTES;
+                uint8_t* dS = sSFB + slot * C::SFB_BYTES;
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) {
                     if (src_row[i] < 0) continue;
@@ -311,12 +307,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                                    a.act_s + src_row[i] * srowbytes + kt * 4);
                 }
                 tc::cp_async_commit();
-                ++pending;
-                if (++stage == C::SB) { stage = 0; phase ^= 1; }
+                tc::cp_async_wait<0>();
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&fullB[slot]);
             }
         }
-        while (pending > 0) publish_oldest();
-    } else if (warp == 2) {
+    } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             int sa = 0, sb = 0, sf = 0, ab = 0;
@@ -372,9 +369,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 3..10)
-        const int q = warp & 3;               // TMEM lane quadrant this warp may access
-        const int half = (warp - 3) >> 2;     // which 16-column chunks it takes
+        // ------------------------------------------------ epilogue warps
+        const int q = warp & 3;                       // TMEM lane quadrant this warp may access
+        const int half = (warp - WARP_EPI0) >> 2;     // which 16-column chunks it takes
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int ab = 0;
         uint32_t pacc = 0;
@@ -441,7 +438,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == WARP_MMA) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tm, 512);
     }
