@@ -65,6 +65,11 @@ struct Cfg {
     static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : (NMAX <= 128 ? 8 : 6);
     static constexpr int SB = (NMAX <= 128) ? ((STAGE == 1) ? 4 : 6) : ((STAGE == 1) ? 3 : 4);
     static constexpr int PF = 2 * SA;                    // L2 prefetch distance (steps)
+    // Active activation producers.  A producer's next step lands NBW steps
+    // later; with NBW <= SB the slot it waits for is at most one phase behind,
+    // so the parity wait cannot alias an older phase.
+    static constexpr int NBW_ACTIVE = (SB < NBW) ? SB : NBW;
+    static_assert(NBW_ACTIVE <= SB, "producer count vs activation slots");
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
@@ -270,12 +275,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // group, fences the writes to the async proxy and publishes the step:
         // NBW L2 round trips are in flight at once.
         const int wb = warp - WARP_B0;
+        constexpr int NBA = C::NBW_ACTIVE;
         const int rowbytes = K;        // one E4M3 code per element
         const int srowbytes = K / 32;  // one E8M0 scale per 32 elements
         constexpr int RPL = (NMAX + 31) / 32;  // rows per lane
         int64_t step = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units && ok && wb < NBA && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb;
             decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
             int64_t src_row[RPL];
@@ -286,7 +292,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 if (r < ntok) src_row[i] = (STAGE == 1) ? (int64_t)(a.sorted[m0 + r] / a.k) : (int64_t)(m0 + r);
             }
             for (int kt = 0; kt < KT; ++kt, ++step) {
-                if ((int)(step % NBW) != wb) continue;
+                if ((int)(step % NBA) != wb) continue;
                 const int slot = (int)(step % C::SB);
                 const uint32_t parity = (uint32_t)((step / C::SB) & 1) ^ 1u;
                 if (!warp_wait(&emptyB[slot], parity, lane)) {
