@@ -9,25 +9,29 @@
 //   stage 2: y = W2 . h in fp32.
 //
 // Structure (one persistent CTA per SM, 14 warps):
-//   warp 0     weight producer: TMA loads of 128-row x 128-element FP4 tiles
-//              (tile-major pre-packed weights: one contiguous 8 KiB read per
-//              tile; the tensor map unpacks FP4 to the 16-byte-aligned form
-//              the MMA reads) plus the matching 512-byte scale atoms.
+//   warp 0     weight producer: per pipeline step one TMA load of the step's
+//              FP4 weight tiles (stage 1: gate and up tiles together, one 4D
+//              box) from tile-major pre-packed weights -- each 128x128 tile
+//              is one contiguous 8 KiB read, unpacked by the tensor map into
+//              the 16-byte-aligned form the MMA reads -- plus bulk copies of
+//              the matching 512-byte scale atoms.
 //   warps 1-4  activation producers, taking pipeline steps round-robin:
 //              gather the unit's token rows (stage 1: token = sorted pair id
 //              / k; stage 2: contiguous slots) with cp.async into the
 //              128-byte-swizzled K-major layout, and their E8M0 scales into
-//              atom layout.
+//              atom layout; each publishes its step after its copies land.
 //   warp 5     allocates tensor memory; one lane copies the scale atoms into
 //              TMEM and issues the MMAs (M = 128 weight rows, N = tokens
-//              rounded up to 16, K = 32 per instruction).
+//              rounded up to 16, K = 32 per instruction), one commit per step.
 //   warps 6-13 epilogue (two warps per TMEM lane quadrant, alternating
 //              16-token chunks): TMEM -> registers, SwiGLU + MX quantisation
 //              (stage 1) or fp32 stores (stage 2).
-// Weights and activations flow through separate shared-memory rings: the
-// weight ring is deep (HBM latency), the activation ring shallow (its rows
-// come from L2).  With two accumulator buffers in TMEM, the epilogue of one
-// unit overlaps the MMAs of the next.
+// Every tcgen05 or TMA instruction costs the issuing thread on the order of
+// a hundred cycles, so a step carries as much data per instruction as the
+// hardware allows: one ring slot holds a whole step (weights, activations,
+// both scale sets) behind a single full/empty barrier pair.  Two accumulator
+// buffers in TMEM (112-token tiles) let the epilogue of one unit overlap the
+// MMAs of the next.
 //
 // The weights are the A operand ("swap AB"): per-expert token counts are
 // small at prefill sizes (about 80 at T = 4096), so tokens take the MMA's N
@@ -60,27 +64,21 @@ struct Cfg {
     static constexpr int NMAX = NMAX_;
     static constexpr int AT = (STAGE == 1) ? 2 : 1;     // weight tiles per step (gate + up)
     static constexpr int ACC_BUFS = (AT * NMAX * 2 <= 448) ? 2 : 1;
-    // ring depths: weights come from HBM (deep), activations from L2.  Sized
-    // to the 227 KB of shared memory per CTA.
-    static constexpr int SA = (STAGE == 1) ? (NMAX <= 128 ? 5 : 4) : (NMAX <= 128 ? 8 : 6);
-    static constexpr int SB = (NMAX <= 128) ? ((STAGE == 1) ? 4 : 6) : ((STAGE == 1) ? 3 : 4);
-    static constexpr int PF = 2 * SA;                    // L2 prefetch distance (steps)
-    // Active activation producers.  A producer's next step lands NBW steps
-    // later; with NBW <= SB the slot it waits for is at most one phase behind,
-    // so the parity wait cannot alias an older phase.
-    static constexpr int NBW_ACTIVE = (SB < NBW) ? SB : NBW;
-    static_assert(NBW_ACTIVE <= SB, "producer count vs activation slots");
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
     static constexpr int SFA_BYTES = AT * 512;
     static constexpr int SFB_BYTES = NSFB * 512;
+    static constexpr int SLOT_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    // ring depth: as many whole steps as fit in the 227 KB of shared memory
+    static constexpr int S = (220 * 1024 - 8 * 1024) / SLOT_BYTES;
+    static constexpr int NBA = (S < NBW) ? S : NBW;      // active activation producers (<= S: no parity aliasing)
     static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = A_OFF + SA * A_BYTES;
-    static constexpr int SFA_OFF = B_OFF + SB * B_BYTES;
-    static constexpr int SFB_OFF = SFA_OFF + SA * SFA_BYTES;
-    static constexpr int BAR_OFF = SFB_OFF + SB * SFB_BYTES;
-    static constexpr int NBAR = 2 * SA + 2 * SB + 2 * ACC_BUFS;
+    static constexpr int B_OFF = A_OFF + S * A_BYTES;
+    static constexpr int SFA_OFF = B_OFF + S * B_BYTES;
+    static constexpr int SFB_OFF = SFA_OFF + S * SFA_BYTES;
+    static constexpr int BAR_OFF = SFB_OFF + S * SFB_BYTES;
+    static constexpr int NBAR = 2 * S + 2 * ACC_BUFS;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SCHED_OFF = MISC_OFF + 64;
     static constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
@@ -90,6 +88,7 @@ struct Cfg {
     static constexpr uint32_t SF_SLOT = AT * 4 + NSFB * 4;
     static_assert(SF_COL + 2 * SF_SLOT <= 512, "TMEM budget");
     static_assert(NMAX % 16 == 0 && NMAX <= 256, "N tile");
+    static_assert(S >= 2 && NBA <= S, "ring");
 };
 
 constexpr int MAX_E = 512;  // schedule prefix kept in shared memory
@@ -146,11 +145,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     uint8_t* sB = smem + C::B_OFF;
     uint8_t* sSFA = smem + C::SFA_OFF;
     uint8_t* sSFB = smem + C::SFB_OFF;
-    uint64_t* fullA = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-    uint64_t* emptyA = fullA + C::SA;
-    uint64_t* fullB = emptyA + C::SA;
-    uint64_t* emptyB = fullB + C::SB;
-    uint64_t* acc_full = emptyB + C::SB;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* empty = full + C::S;
+    uint64_t* acc_full = empty + C::S;
     uint64_t* acc_empty = acc_full + C::ACC_BUFS;
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
@@ -182,13 +179,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         if (lane == 0) tile_start[E] = running;
     }
     if (threadIdx.x == 32 * WARP_MMA) {
-        for (int s = 0; s < C::SA; ++s) {
-            tc::mbar_init(&fullA[s], 1);
-            tc::mbar_init(&emptyA[s], 1);
-        }
-        for (int s = 0; s < C::SB; ++s) {
-            tc::mbar_init(&fullB[s], 1);
-            tc::mbar_init(&emptyB[s], 1);
+        for (int s = 0; s < C::S; ++s) {
+            tc::mbar_init(&full[s], 2);   // weight producer (with tx bytes) + activation producer
+            tc::mbar_init(&empty[s], 1);  // MMA commit
         }
         for (int b = 0; b < C::ACC_BUFS; ++b) {
             tc::mbar_init(&acc_full[b], 1);
@@ -214,74 +207,45 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // ------------------------------------------------ weight producer (TMA)
         if (lane == 0) {
             tc::prefetch_tensormap(&mapW);
-            int stage = 0;
+            int slot = 0;
             uint32_t phase = 0;
             const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
-            // L2 prefetch cursor, PF steps ahead of the shared-memory loads:
-            // the ring's loads then hit L2 while DRAM sees PF more tiles in flight.
-            int pu = blockIdx.x, pkt = 0, prt0 = 0, prt1 = 0;
-            auto pf_decode = [&]() {
-                if (pu >= total_units) return;
-                int e_, m0_, nt_, nb_;
-                decode_unit<NMAX>(pu, NB, tile_start, E, a.offsets, e_, m0_, nt_, nb_);
-                prt0 = (e_ * rows_per_e + nb_ * 128) / 128;
-                prt1 = (e_ * rows_per_e + a.I + nb_ * 128) / 128;
-            };
-            auto pf_issue = [&]() {
-                if (pu >= total_units) return;
-                const int64_t t0 = (int64_t)prt0 * KT + pkt;
-                tc::tma_prefetch_2d(&mapW, 0, (int)(t0 * 128));
-                tc::bulk_prefetch_l2(a.w_s + t0 * 512, 512);
-                if (STAGE == 1) {
-                    const int64_t t1 = (int64_t)prt1 * KT + pkt;
-                    tc::tma_prefetch_2d(&mapW, 0, (int)(t1 * 128));
-                    tc::bulk_prefetch_l2(a.w_s + t1 * 512, 512);
-                }
-                if (++pkt == KT) {
-                    pkt = 0;
-                    pu += gridDim.x;
-                    pf_decode();
-                }
-            };
-            pf_decode();
-            for (int i = 0; i < C::PF; ++i) pf_issue();
+            const int64_t up_tiles = (int64_t)(a.I / 128) * KT;  // gate tile -> up tile distance (stage 1)
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb;
                 decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
                 const int rt0 = (e * rows_per_e + nb * 128) / 128;
-                const int rt1 = (e * rows_per_e + a.I + nb * 128) / 128;  // up rows (stage 1)
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!tc::mbar_wait(&emptyA[stage], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
-                    tc::mbar_arrive_expect_tx(&fullA[stage], C::AT * (FP4_TILE_TX + 512));
-                    uint8_t* dA = sA + stage * C::A_BYTES;
-                    uint8_t* dS = sSFA + stage * C::SFA_BYTES;
+                    if (!tc::mbar_wait(&empty[slot], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
+                    tc::mbar_arrive_expect_tx(&full[slot], C::AT * (FP4_TILE_TX + 512));
+                    uint8_t* dS = sSFA + slot * C::SFA_BYTES;
                     const int64_t t0 = (int64_t)rt0 * KT + kt;
-                    tc::tma_load_2d(dA, &mapW, &fullA[stage], 0, (int)(t0 * 128));
-                    tc::bulk_load(dS, a.w_s + t0 * 512, 512, &fullA[stage]);
                     if (STAGE == 1) {
-                        const int64_t t1 = (int64_t)rt1 * KT + kt;
-                        tc::tma_load_2d(dA + 128 * 128, &mapW, &fullA[stage], 0, (int)(t1 * 128));
-                        tc::bulk_load(dS + 512, a.w_s + t1 * 512, 512, &fullA[stage]);
+                        // 4D view {row bytes, rows within a half, gate/up half, expert}: one box = both tiles
+                        tc::tma_load_4d(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, (nb * KT + kt) * 128, 0, e);
+                        tc::bulk_load(dS, a.w_s + t0 * 512, 512, &full[slot]);
+                        tc::bulk_load(dS + 512, a.w_s + (t0 + up_tiles) * 512, 512, &full[slot]);
+                    } else {
+                        tc::tma_load_2d(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, (int)(t0 * 128));
+                        tc::bulk_load(dS, a.w_s + t0 * 512, 512, &full[slot]);
                     }
-                    pf_issue();
-                    if (++stage == C::SA) { stage = 0; phase ^= 1; }
+                    if (++slot == C::S) { slot = 0; phase ^= 1; }
                 }
             }
         }
     } else if (warp < WARP_MMA) {
         // ------------------------------------------------ activation producers (cp.async gather)
-        // NBW warps take the pipeline steps round-robin.  A warp waits for its
-        // slot, issues the step's copies as one cp.async group, waits for that
-        // group, fences the writes to the async proxy and publishes the step:
-        // NBW L2 round trips are in flight at once.
+        // The NBA active warps take steps round-robin.  A warp waits for its
+        // slot, issues the step's copies as one cp.async group, waits for
+        // that group, fences the writes to the async proxy and publishes the
+        // step: NBA L2 round trips are in flight at once.
         const int wb = warp - WARP_B0;
-        constexpr int NBA = C::NBW_ACTIVE;
         const int rowbytes = K;        // one E4M3 code per element
         const int srowbytes = K / 32;  // one E8M0 scale per 32 elements
         constexpr int RPL = (NMAX + 31) / 32;  // rows per lane
         int64_t step = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok && wb < NBA && !*abort_flag; u += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units && ok && wb < C::NBA && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb;
             decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
             int64_t src_row[RPL];
@@ -292,10 +256,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 if (r < ntok) src_row[i] = (STAGE == 1) ? (int64_t)(a.sorted[m0 + r] / a.k) : (int64_t)(m0 + r);
             }
             for (int kt = 0; kt < KT; ++kt, ++step) {
-                if ((int)(step % NBA) != wb) continue;
-                const int slot = (int)(step % C::SB);
-                const uint32_t parity = (uint32_t)((step / C::SB) & 1) ^ 1u;
-                if (!warp_wait(&emptyB[slot], parity, lane)) {
+                if ((int)(step % C::NBA) != wb) continue;
+                const int slot = (int)(step % C::S);
+                const uint32_t parity = (uint32_t)((step / C::S) & 1) ^ 1u;
+                if (!warp_wait(&empty[slot], parity, lane)) {
                     if (lane == 0) set_abort(abort_flag, a.status);
                     ok = false;
                     break;
@@ -316,14 +280,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 tc::cp_async_wait<0>();
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&fullB[slot]);
+                if (lane == 0) tc::mbar_arrive(&full[slot]);
             }
         }
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int sa = 0, sb = 0, sf = 0, ab = 0;
-            uint32_t pa = 0, pb = 0, pacc = 0;
+            int slot = 0, sf = 0, ab = 0;
+            uint32_t phase = 0, pacc = 0;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb;
                 decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
@@ -333,24 +297,20 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 const uint32_t dcol = ab * C::ACC_COLS;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!tc::mbar_wait(&fullA[sa], pa) || !tc::mbar_wait(&fullB[sb], pb)) {
-                        set_abort(abort_flag, a.status);
-                        ok = false;
-                        break;
-                    }
+                    if (!tc::mbar_wait(&full[slot], phase)) { set_abort(abort_flag, a.status); ok = false; break; }
                     tc::tc_fence_after();
                     const uint32_t sfa_col = C::SF_COL + sf * C::SF_SLOT;
                     const uint32_t sfb_col = sfa_col + C::AT * 4;
-                    const uint32_t sfa_addr = tc::smem_u32(sSFA + sa * C::SFA_BYTES);
-                    const uint32_t sfb_addr = tc::smem_u32(sSFB + sb * C::SFB_BYTES);
+                    const uint32_t sfa_addr = tc::smem_u32(sSFA + slot * C::SFA_BYTES);
+                    const uint32_t sfb_addr = tc::smem_u32(sSFB + slot * C::SFB_BYTES);
 #pragma unroll
                     for (int t = 0; t < C::AT; ++t)
                         tc::tmem_cp_32x128b_warpx4(tm + sfa_col + 4 * t, tc::smem_desc(sfa_addr + 512 * t, 0, 128, 0));
 #pragma unroll
                     for (int t = 0; t < C::NSFB; ++t)
                         tc::tmem_cp_32x128b_warpx4(tm + sfb_col + 4 * t, tc::smem_desc(sfb_addr + 512 * t, 0, 128, 0));
-                    const uint32_t a0 = tc::smem_u32(sA + sa * C::A_BYTES);
-                    const uint32_t b0 = tc::smem_u32(sB + sb * C::B_BYTES);
+                    const uint32_t a0 = tc::smem_u32(sA + slot * C::A_BYTES);
+                    const uint32_t b0 = tc::smem_u32(sB + slot * C::B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t idesc = tc::idesc_mxf8f6f4(128, nmma, 5, 0, kk, kk);
@@ -362,10 +322,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                             tc::mma_mxf8f6f4(tm + dcol + NMAX, tc::sdesc_kmajor_sw128(a0 + 128 * 128 + 32 * kk), bd,
                                              idesc, tm + sfa_col + 4, tm + sfb_col, acc);
                     }
-                    tc::mma_commit(&emptyA[sa]);
-                    tc::mma_commit(&emptyB[sb]);
-                    if (++sa == C::SA) { sa = 0; pa ^= 1; }
-                    if (++sb == C::SB) { sb = 0; pb ^= 1; }
+                    tc::mma_commit(&empty[slot]);
+                    if (++slot == C::S) { slot = 0; phase ^= 1; }
                     sf ^= 1;
                 }
                 if (!ok) break;
@@ -470,20 +428,34 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tile-major pre-packed FP4 weights viewed as a 2D tensor of 64-byte rows
-// (128 elements), one 128-row box per 128x128 tile: each box is a contiguous
-// 8 KiB read, unpacked by the TMA to 16-byte-aligned groups and 128-byte
-// swizzled in shared memory.
-static int make_fp4_map(CUtensorMap* map, const void* w, int64_t tiles) {
+// Tile-major pre-packed FP4 weights viewed as 64-byte rows (128 elements),
+// one 128-row box per 128x128 tile: each box is a contiguous 8 KiB read,
+// unpacked by the TMA to 16-byte-aligned groups and 128-byte swizzled in
+// shared memory.  With half_bytes > 0 (the gate/up weights of stage 1) the
+// map is 4D, {row bytes, rows within a half, half, expert}: an expert's gate
+// tiles occupy the first half_bytes of its block and the up tiles the next,
+// so one 128 x 128 x 2 box brings a gate tile and its up partner.
+static int make_fp4_map(CUtensorMap* map, const void* w, int64_t tiles, int64_t half_bytes, int E) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return QMOE_ERR_CUDA;
-    cuuint64_t gdim[2] = {128, (cuuint64_t)(tiles * 128)};
-    cuuint64_t gstride[1] = {64};
-    cuuint32_t box[2] = {128, 128};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(w), gdim, gstride, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (half_bytes > 0) {
+        cuuint64_t gdim[4] = {128, (cuuint64_t)(half_bytes / 64), 2, (cuuint64_t)E};
+        cuuint64_t gstride[3] = {64, (cuuint64_t)half_bytes, (cuuint64_t)(2 * half_bytes)};
+        cuuint32_t box[4] = {128, 128, 2, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(w), gdim, gstride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t gdim[2] = {128, (cuuint64_t)(tiles * 128)};
+        cuuint64_t gstride[1] = {64};
+        cuuint32_t box[2] = {128, 128};
+        cuuint32_t estr[2] = {1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(w), gdim, gstride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS ? QMOE_OK : QMOE_ERR_UNSUPPORTED;
 }
 
@@ -503,10 +475,10 @@ bool mx_tc_supported(const qmoe_dims* d, const void* w1, const void* w2) {
 }
 
 template <int STAGE, int NMAX>
-static int launch_cfg(const void* w, int64_t tiles, const Args& a, cudaStream_t st) {
+static int launch_cfg(const void* w, int64_t tiles, int64_t half_bytes, const Args& a, cudaStream_t st) {
     using C = Cfg<STAGE, NMAX>;
     CUtensorMap map;
-    int rc = make_fp4_map(&map, w, tiles);
+    int rc = make_fp4_map(&map, w, tiles, half_bytes, a.E);
     if (rc != QMOE_OK) return rc;
     const size_t smem = C::smem_bytes(a.E);
     if (cudaFuncSetAttribute(mx_gemm_kernel<STAGE, NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -521,7 +493,7 @@ static int launch_cfg(const void* w, int64_t tiles, const Args& a, cudaStream_t 
 // Token-tile size: the average expert load decides (the grid never syncs
 // with the host to look at the real counts).  Up to ~100 tokens per expert a
 // 112-token tile with two accumulator buffers; above, 224-token tiles so an
-// expert's weights are still streamed once.
+// expert's weights are still streamed once.  Both stages use the same tiles.
 static bool big_tiles(const qmoe_dims* d) { return (int64_t)d->T * d->k > (int64_t)96 * d->E; }
 
 }  // namespace mx
@@ -533,8 +505,11 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, cons
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = x_q; a.act_s = x_s; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted;
     a.h_q = h_q; a.h_s = h_s; a.status = status;
-    const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * (d->H / 128);
-    return mx::big_tiles(d) ? mx::launch_cfg<1, 224>(w1, tiles, a, st) : mx::launch_cfg<1, 112>(w1, tiles, a, st);
+    const int64_t KT = d->H / 128;
+    const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * KT;
+    const int64_t pair = (int64_t)(d->I / 128) * KT * 8192;  // bytes of one expert's gate (or up) tiles
+    return mx::big_tiles(d) ? mx::launch_cfg<1, 224>(w1, tiles, pair, a, st)
+                            : mx::launch_cfg<1, 112>(w1, tiles, pair, a, st);
 }
 
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2, const uint8_t* w2_s,
@@ -543,7 +518,7 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, cons
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = h_q; a.act_s = h_s; a.w_s = w2_s; a.offsets = offsets; a.y = y; a.status = status;
     const int64_t tiles = (int64_t)d->E * d->H / 128 * (d->I / 128);
-    return mx::big_tiles(d) ? mx::launch_cfg<2, 224>(w2, tiles, a, st) : mx::launch_cfg<2, 112>(w2, tiles, a, st);
+    return mx::big_tiles(d) ? mx::launch_cfg<2, 224>(w2, tiles, 0, a, st) : mx::launch_cfg<2, 112>(w2, tiles, 0, a, st);
 }
 
 bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2) { return mx::mx_tc_supported(d, w1, w2); }
