@@ -8,7 +8,7 @@
 //            E4M3 codes + E8M0 scales per 32 columns of I;
 //   stage 2: y = W2 . h in fp32.
 //
-// Structure (one persistent CTA per SM, 14 warps):
+// Structure (one persistent CTA per SM, 15 warps):
 //   warp 0     weight producer: per pipeline step one TMA load of the step's
 //              FP4 weight tiles (stage 1: gate and up tiles together, one 4D
 //              box) from tile-major pre-packed weights -- each 128x128 tile
@@ -20,10 +20,13 @@
 //              / k; stage 2: contiguous slots) with cp.async into the
 //              128-byte-swizzled K-major layout, and their E8M0 scales into
 //              atom layout; each publishes its step after its copies land.
-//   warp 5     allocates tensor memory; one lane copies the scale atoms into
-//              TMEM and issues the MMAs (M = 128 weight rows, N = tokens
-//              rounded up to 16, K = 32 per instruction), one commit per step.
-//   warps 6-13 epilogue (two warps per TMEM lane quadrant, alternating
+//   warps 5-6  MMA issuers (warp 5 also owns tensor memory): one lane copies
+//              the scale atoms into TMEM and issues the MMAs (M = 128 weight
+//              rows, N = tokens rounded up to 16, K = 32 per instruction),
+//              one commit per step.  Stage 1 splits the gate and up
+//              accumulators between the two issuers, halving the serial
+//              instruction stream each one issues.
+//   warps 7-14 epilogue (two warps per TMEM lane quadrant, alternating
 //              16-token chunks): TMEM -> registers, SwiGLU + MX quantisation
 //              (stage 1) or fp32 stores (stage 2).
 // Every tcgen05 or TMA instruction costs the issuing thread on the order of
@@ -52,8 +55,9 @@ namespace mx {
 // warp roles
 constexpr int WARP_A = 0;                   // weight producer (TMA)
 constexpr int WARP_B0 = 1, NBW = 4;         // activation producers, steps taken round-robin
-constexpr int WARP_MMA = WARP_B0 + NBW;     // TMEM owner + MMA issuer
-constexpr int WARP_EPI0 = WARP_MMA + 1;     // epilogue warps
+constexpr int WARP_MMA = WARP_B0 + NBW;     // TMEM owner + MMA issuer (stage 1: gate accumulator)
+constexpr int WARP_MMA2 = WARP_MMA + 1;     // stage 1: second issuer (up accumulator)
+constexpr int WARP_EPI0 = WARP_MMA2 + 1;    // epilogue warps
 constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant, splitting the token columns
 constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
 constexpr int KSTAGE = 128;                 // K elements per pipeline step (4 MMAs of K = 32)
@@ -85,8 +89,9 @@ struct Cfg {
     // TMEM columns: accumulators, then a 2-slot ring for scale factors
     static constexpr uint32_t ACC_COLS = AT * NMAX;
     static constexpr uint32_t SF_COL = ACC_BUFS * ACC_COLS;
-    static constexpr uint32_t SF_SLOT = AT * 4 + NSFB * 4;
-    static_assert(SF_COL + 2 * SF_SLOT <= 512, "TMEM budget");
+    // one scale-factor column block per issuer: its weight atom + the activation atoms
+    static constexpr uint32_t SF_SLOT = 4 + NSFB * 4;
+    static_assert(SF_COL + 2 * AT * SF_SLOT <= 512, "TMEM budget");
     static_assert(NMAX % 16 == 0 && NMAX <= 256, "N tile");
     static_assert(S >= 2 && NBA <= S, "ring");
 };
@@ -180,11 +185,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     }
     if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::S; ++s) {
-            tc::mbar_init(&full[s], 2);   // weight producer (with tx bytes) + activation producer
-            tc::mbar_init(&empty[s], 1);  // MMA commit
+            tc::mbar_init(&full[s], 2);        // weight producer (with tx bytes) + activation producer
+            tc::mbar_init(&empty[s], C::AT);   // one commit per MMA issuer
         }
         for (int b = 0; b < C::ACC_BUFS; ++b) {
-            tc::mbar_init(&acc_full[b], 1);
+            tc::mbar_init(&acc_full[b], C::AT);
             tc::mbar_init(&acc_empty[b], EPI_WARPS);
         }
         *abort_flag = 0;
@@ -283,44 +288,44 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 if (lane == 0) tc::mbar_arrive(&full[slot]);
             }
         }
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+    } else if (warp == WARP_MMA || warp == WARP_MMA2) {
+        // ------------------------------------------------ MMA issuers
+        // Stage 1 has two issuers, one per accumulator (gate rows, up rows):
+        // each copies its own scale atoms to TMEM, issues its four MMAs per
+        // step and commits; the slot frees after both commits.  Stage 2 uses
+        // the first issuer only.
+        const int iss = warp - WARP_MMA;  // 0: gate (or the only) accumulator, 1: up
+        if (lane == 0 && iss < C::AT) {
             int slot = 0, sf = 0, ab = 0;
             uint32_t phase = 0, pacc = 0;
+            const uint32_t sf_base = C::SF_COL + iss * 2 * C::SF_SLOT;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb;
                 decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
                 const int nmma = (ntok + 15) & ~15;
                 if (!tc::mbar_wait(&acc_empty[ab], pacc ^ 1)) { set_abort(abort_flag, a.status); break; }
                 tc::tc_fence_after();
-                const uint32_t dcol = ab * C::ACC_COLS;
+                const uint32_t dcol = ab * C::ACC_COLS + iss * NMAX;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&full[slot], phase)) { set_abort(abort_flag, a.status); ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t sfa_col = C::SF_COL + sf * C::SF_SLOT;
-                    const uint32_t sfb_col = sfa_col + C::AT * 4;
-                    const uint32_t sfa_addr = tc::smem_u32(sSFA + slot * C::SFA_BYTES);
+                    const uint32_t sfa_col = sf_base + sf * C::SF_SLOT;
+                    const uint32_t sfb_col = sfa_col + 4;
+                    const uint32_t sfa_addr = tc::smem_u32(sSFA + slot * C::SFA_BYTES + iss * 512);
                     const uint32_t sfb_addr = tc::smem_u32(sSFB + slot * C::SFB_BYTES);
-#pragma unroll
-                    for (int t = 0; t < C::AT; ++t)
-                        tc::tmem_cp_32x128b_warpx4(tm + sfa_col + 4 * t, tc::smem_desc(sfa_addr + 512 * t, 0, 128, 0));
+                    tc::tmem_cp_32x128b_warpx4(tm + sfa_col, tc::smem_desc(sfa_addr, 0, 128, 0));
 #pragma unroll
                     for (int t = 0; t < C::NSFB; ++t)
                         tc::tmem_cp_32x128b_warpx4(tm + sfb_col + 4 * t, tc::smem_desc(sfb_addr + 512 * t, 0, 128, 0));
-                    const uint32_t a0 = tc::smem_u32(sA + slot * C::A_BYTES);
+                    const uint32_t a0 = tc::smem_u32(sA + slot * C::A_BYTES + iss * 128 * 128);
                     const uint32_t b0 = tc::smem_u32(sB + slot * C::B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t idesc = tc::idesc_mxf8f6f4(128, nmma, 5, 0, kk, kk);
-                        const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
-                        const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + 32 * kk);
-                        tc::mma_mxf8f6f4(tm + dcol, tc::sdesc_kmajor_sw128(a0 + 32 * kk), bd, idesc, tm + sfa_col,
-                                         tm + sfb_col, acc);
-                        if (STAGE == 1)
-                            tc::mma_mxf8f6f4(tm + dcol + NMAX, tc::sdesc_kmajor_sw128(a0 + 128 * 128 + 32 * kk), bd,
-                                             idesc, tm + sfa_col + 4, tm + sfb_col, acc);
+                        tc::mma_mxf8f6f4(tm + dcol, tc::sdesc_kmajor_sw128(a0 + 32 * kk),
+                                         tc::sdesc_kmajor_sw128(b0 + 32 * kk), idesc, tm + sfa_col, tm + sfb_col,
+                                         (kt > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(&empty[slot]);
                     if (++slot == C::S) { slot = 0; phase ^= 1; }
