@@ -9,9 +9,10 @@
 //   stage 2: y = W2 . h in fp32.
 //
 // Structure (one persistent CTA per SM, 15 warps):
-//   warp 0     weight producer: per pipeline step one TMA load of the step's
-//              FP4 weight tiles (stage 1: gate and up tiles together, one 4D
-//              box) from tile-major pre-packed weights -- each 128x128 tile
+//   warp 0     weight producer: per pipeline step one TMA load (a 4D box) of
+//              the step's two FP4 weight tiles (stage 1: a gate tile and its
+//              up partner; stage 2: two adjacent row tiles of W2) from
+//              tile-major pre-packed weights -- each 128x128 tile
 //              is one contiguous 8 KiB read, unpacked by the tensor map into
 //              the 16-byte-aligned form the MMA reads -- plus bulk copies of
 //              the matching 512-byte scale atoms.
@@ -20,12 +21,11 @@
 //              / k; stage 2: contiguous slots) with cp.async into the
 //              128-byte-swizzled K-major layout, and their E8M0 scales into
 //              atom layout; each publishes its step after its copies land.
-//   warps 5-6  MMA issuers (warp 5 also owns tensor memory): one lane copies
-//              the scale atoms into TMEM and issues the MMAs (M = 128 weight
-//              rows, N = tokens rounded up to 16, K = 32 per instruction),
-//              one commit per step.  Stage 1 splits the gate and up
-//              accumulators between the two issuers, halving the serial
-//              instruction stream each one issues.
+//   warps 5-6  MMA issuers (warp 5 also owns tensor memory), one per weight
+//              tile: one lane copies its scale atoms into TMEM and issues the
+//              MMAs (M = 128 weight rows, N = tokens rounded up to 16, K = 32
+//              per instruction), one commit per step.  Two issuers halve the
+//              serial instruction stream each thread issues.
 //   warps 7-14 epilogue (two warps per TMEM lane quadrant, alternating
 //              16-token chunks): TMEM -> registers, SwiGLU + MX quantisation
 //              (stage 1) or fp32 stores (stage 2).
@@ -39,7 +39,8 @@
 // The weights are the A operand ("swap AB"): per-expert token counts are
 // small at prefill sizes (about 80 at T = 4096), so tokens take the MMA's N
 // dimension (a multiple of 16) instead of being padded to M = 128.  A work
-// unit is (expert, tile of up to NMAX of its tokens, 128 output columns);
+// unit is (expert, tile of up to NMAX of its tokens, 128 output columns of h
+// in stage 1 / 256 columns of y in stage 2);
 // units are ordered with the column block fastest so concurrent CTAs share
 // activation rows through L2, and each unit streams a disjoint slice of the
 // expert's weights exactly once.
@@ -66,7 +67,9 @@ constexpr uint32_t FP4_TILE_TX = 128 * 64;  // bytes one 128x128 FP4 tile moves 
 template <int STAGE, int NMAX_>
 struct Cfg {
     static constexpr int NMAX = NMAX_;
-    static constexpr int AT = (STAGE == 1) ? 2 : 1;     // weight tiles per step (gate + up)
+    // weight tiles per step, one per MMA issuer: stage 1 gate + up, stage 2
+    // two adjacent 128-column blocks of W2; both share the step's activations
+    static constexpr int AT = 2;
     static constexpr int ACC_BUFS = (AT * NMAX * 2 <= 448) ? 2 : 1;
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
@@ -162,7 +165,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     const int E = a.E;
     const int K = (STAGE == 1) ? a.H : a.I;            // reduction length
     const int NOUT = (STAGE == 1) ? a.I : a.H;          // output columns
-    const int NB = NOUT / 128;
+    const int NB = (STAGE == 1) ? NOUT / 128 : NOUT / 256;  // stage 2 units cover two column blocks
     const int KT = K / KSTAGE;
 
     // ---- schedule: tiles of up to NMAX tokens per expert, prefix over experts
@@ -219,7 +222,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb;
                 decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
-                const int rt0 = (e * rows_per_e + nb * 128) / 128;
+                const int rt0 = (STAGE == 1) ? (e * rows_per_e + nb * 128) / 128 : (e * rows_per_e + nb * 256) / 128;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&empty[slot], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
                     tc::mbar_arrive_expect_tx(&full[slot], C::AT * (FP4_TILE_TX + 512));
@@ -231,8 +234,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                         tc::bulk_load(dS, a.w_s + t0 * 512, 512, &full[slot]);
                         tc::bulk_load(dS + 512, a.w_s + (t0 + up_tiles) * 512, 512, &full[slot]);
                     } else {
-                        tc::tma_load_2d(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, (int)(t0 * 128));
+                        // 4D view {row bytes, tile rows, K tile, row tile}: one box = row tiles rt0, rt0 + 1
+                        tc::tma_load_4d(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, 0, kt, rt0);
                         tc::bulk_load(dS, a.w_s + t0 * 512, 512, &full[slot]);
+                        tc::bulk_load(dS + 512, a.w_s + (t0 + KT) * 512, 512, &full[slot]);
                     }
                     if (++slot == C::S) { slot = 0; phase ^= 1; }
                 }
@@ -290,11 +295,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         }
     } else if (warp == WARP_MMA || warp == WARP_MMA2) {
         // ------------------------------------------------ MMA issuers
-        // Stage 1 has two issuers, one per accumulator (gate rows, up rows):
-        // each copies its own scale atoms to TMEM, issues its four MMAs per
-        // step and commits; the slot frees after both commits.  Stage 2 uses
-        // the first issuer only.
-        const int iss = warp - WARP_MMA;  // 0: gate (or the only) accumulator, 1: up
+        // Two issuers, one per accumulator (stage 1: gate rows, up rows;
+        // stage 2: the unit's two column blocks): each copies its own scale
+        // atoms to TMEM, issues its four MMAs per step and commits; the slot
+        // frees after both commits.
+        const int iss = warp - WARP_MMA;
         if (lane == 0 && iss < C::AT) {
             int slot = 0, sf = 0, ab = 0;
             uint32_t phase = 0, pacc = 0;
@@ -383,12 +388,18 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                         if (lane == 0) a.h_s[slot * (a.I / 32) + (n >> 5)] = sb;
                     }
                 } else {
+                    // stage 2: column blocks 2nb (accumulator 0) and 2nb + 1 (accumulator 1)
+                    uint32_t g2[16];
+                    tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + NMAX + c0, g2);
                     tc::tmem_ld_wait();
+                    const int n0 = 2 * nb * 128 + q * 32 + lane;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int c = c0 + j;
                         if (c >= ntok) break;
-                        a.y[(int64_t)(m0 + c) * a.H + n] = __uint_as_float(g[j]);
+                        float* yr = a.y + (int64_t)(m0 + c) * a.H;
+                        yr[n0] = __uint_as_float(g[j]);
+                        yr[n0 + 128] = __uint_as_float(g2[j]);
                     }
                 }
             }
@@ -440,7 +451,7 @@ static EncodeTiledFn encode_fn() {
 // map is 4D, {row bytes, rows within a half, half, expert}: an expert's gate
 // tiles occupy the first half_bytes of its block and the up tiles the next,
 // so one 128 x 128 x 2 box brings a gate tile and its up partner.
-static int make_fp4_map(CUtensorMap* map, const void* w, int64_t tiles, int64_t half_bytes, int E) {
+static int make_fp4_map(CUtensorMap* map, const void* w, int64_t tiles, int64_t half_bytes, int E, int64_t KT) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return QMOE_ERR_CUDA;
     CUresult r;
@@ -453,11 +464,12 @@ static int make_fp4_map(CUtensorMap* map, const void* w, int64_t tiles, int64_t 
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
-        cuuint64_t gdim[2] = {128, (cuuint64_t)(tiles * 128)};
-        cuuint64_t gstride[1] = {64};
-        cuuint32_t box[2] = {128, 128};
-        cuuint32_t estr[2] = {1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(w), gdim, gstride, box, estr,
+        // {row bytes, tile rows, K tile, row tile}: a 128 x 128 x 1 x 2 box brings row tiles rt, rt + 1
+        cuuint64_t gdim[4] = {128, 128, (cuuint64_t)KT, (cuuint64_t)(tiles / KT)};
+        cuuint64_t gstride[3] = {64, 8192, (cuuint64_t)(KT * 8192)};
+        cuuint32_t box[4] = {128, 128, 1, 2};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(w), gdim, gstride, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
@@ -475,7 +487,7 @@ bool mx_tc_supported(const qmoe_dims* d, const void* w1, const void* w2) {
     auto a32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
     const int64_t tiles1 = (int64_t)d->E * 2 * d->I / 128 * (d->H / 128);
     const int64_t tiles2 = (int64_t)d->E * d->H / 128 * (d->I / 128);
-    return d->H % 128 == 0 && d->I % 128 == 0 && d->E <= MAX_E && tiles1 * 128 < (1ll << 31) &&
+    return d->H % 256 == 0 && d->I % 128 == 0 && d->E <= MAX_E && tiles1 * 128 < (1ll << 31) &&
            tiles2 * 128 < (1ll << 31) && (!w1 || a32(w1)) && (!w2 || a32(w2));
 }
 
@@ -483,7 +495,8 @@ template <int STAGE, int NMAX>
 static int launch_cfg(const void* w, int64_t tiles, int64_t half_bytes, const Args& a, cudaStream_t st) {
     using C = Cfg<STAGE, NMAX>;
     CUtensorMap map;
-    int rc = make_fp4_map(&map, w, tiles, half_bytes, a.E);
+    const int64_t KT = (STAGE == 1) ? a.H / 128 : a.I / 128;
+    int rc = make_fp4_map(&map, w, tiles, half_bytes, a.E, KT);
     if (rc != QMOE_OK) return rc;
     const size_t smem = C::smem_bytes(a.E);
     if (cudaFuncSetAttribute(mx_gemm_kernel<STAGE, NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -161,7 +161,7 @@ def test_stage1_against_oracle(w):
 S2_CASES = [
     gen.custom("s2_w4a16", "w4a16", 1, 320, 5, 1, 256, seed=31),
     gen.custom("s2_mxfp4", "mxfp4", 1, 320, 5, 1, 256, seed=32),
-    gen.custom("s2_mxfp4_tc", "mxfp4", 1, 384, 5, 1, 256, seed=34),
+    gen.custom("s2_mxfp4_tc", "mxfp4", 1, 512, 5, 1, 256, seed=34),
     gen.custom("s2_w8a8", "w8a8", 1, 320, 5, 1, 256, seed=33),
 ]
 
