@@ -263,8 +263,8 @@ def run_ours(args, w):
     y = E_((P, H), torch.float32)
     out = E_((T, H), torch.int16)
     if w.scheme == "mxfp4":
-        xq, xs = E_((T, H), torch.uint8), E_((T, H // 32), torch.uint8)
-        hq, hs = E_((P, I), torch.uint8), E_((P, I // 32), torch.uint8)
+        xt = E_(qb.mx_tiles_bytes(dims, H), torch.uint8)
+        ht = E_(qb.mx_tiles_bytes(dims, I), torch.uint8)
     elif w.scheme == "w8a8":
         xq, xs = E_((T, H), torch.int8), E_(T, torch.float32)
         h32 = E_((P, I), torch.float32)
@@ -278,14 +278,14 @@ def run_ours(args, w):
     def step(record=False):
         qb.qmoe_align_sort(dims, t["topk_ids"], counts, offsets, sorted_ids, slot, status, ws)
         if w.scheme == "mxfp4":
-            qb.qmoe_quant_act_mxfp8(t["x"], xq, xs)
+            qb.qmoe_permute_quant_mxfp8(dims, t["x"], sorted_ids, offsets, xt, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_quant_rows_int8_bf16(t["x"], xq, xs)
         a, b, c = (ev(), ev(), ev()) if record else (None, None, None)
         if record:
             a.record(stream)
         if w.scheme == "mxfp4":
-            qb.qmoe_gemm1_swiglu_mxfp4(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, hq, hs, status, ws)
+            qb.qmoe_gemm1_swiglu_mxfp4(dims, xt, t["w1"], t["w1_s"], offsets, ht, status, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_gemm1_swiglu_w8a8(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h32, None, status, ws)
         else:
@@ -293,7 +293,7 @@ def run_ours(args, w):
         if record:
             b.record(stream)
         if w.scheme == "mxfp4":
-            qb.qmoe_gemm2_mxfp4(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, status, ws)
+            qb.qmoe_gemm2_mxfp4(dims, ht, t["w2"], t["w2_s"], offsets, y, status, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_quant_rows_int8_f32(h32, hq, hs)
             qb.qmoe_gemm2_w8a8(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, None, status, ws)
@@ -305,7 +305,7 @@ def run_ours(args, w):
             g2_pairs.append((b, c))
         qb.qmoe_combine(dims, y, t["topk_w"], slot, out)
 
-    launches_per_step = 3 + (1 if w.scheme != "w4a16" else 0) + 2 + (1 if w.scheme == "w8a8" else 0) + 1
+    launches_per_step = 4 + (1 if w.scheme != "w4a16" else 0) + 2 + (1 if w.scheme == "w8a8" else 0) + 1
 
     def barrier():
         if world > 1:

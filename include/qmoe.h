@@ -105,7 +105,8 @@ size_t qmoe_workspace_bytes(const qmoe_dims* d);
  *                      expert (a stable sort); slots >= offsets[E] hold -1
  * out  pair_slot       int32 [P]; pair id -> slot, -1 for an invalid id
  * i/o  dev_status      int32 [1]; bit QMOE_DEV_BAD_EXPERT_ID is OR-ed in
- * ws   workspace of qmoe_workspace_bytes(d) bytes, 256-byte aligned
+ * ws   workspace of qmoe_workspace_bytes(d) bytes, 256-byte aligned; besides
+ *      scratch it receives the token-tile schedule the MXFP4 calls read
  * The result is bit-identical run to run (no atomics decide an order). */
 int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
                     int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, void* ws,
@@ -150,6 +151,30 @@ int qmoe_align_sort_static_scratch(const qmoe_dims* d, const int32_t* topk_ids, 
  * cols must be a multiple of 32. */
 int qmoe_quant_act_mxfp8(int64_t rows, int64_t cols, const uint16_t* x_bf16, uint8_t* x_q, uint8_t* x_s,
                          qmoe_stream_t stream);
+
+/* MX activation tiles -- the layout in which the MXFP4 GEMMs take their
+ * activations (x for stage 1, h for stage 2).  The valid slots of each expert
+ * are cut into token tiles of NMAX rows (NMAX = 112, or 224 when T*k > 96*E;
+ * tile_start = prefix over experts of ceil(count / NMAX), kept by
+ * qmoe_align_sort in its workspace).  For reduction length K the buffer holds,
+ * per (tile t, K step kt of 128), a block of NMAX*128 + ceil(NMAX/128)*512
+ * bytes at ((t * K/128) + kt) * that size:
+ *   row r's 128 E4M3 codes at r*128, 16-byte chunk c at ((c ^ (r % 8)) * 16);
+ *   then the E8M0 scales, row r / block b (0..3 of the step) at
+ *   NMAX*128 + (r/128)*512 + 16*(r%32) + 4*((r%128)/32) + b.
+ * Rows past a tile's token count are unspecified.
+ *
+ * qmoe_mx_tiles_bytes -- bytes of such a buffer for dims *d and length K. */
+size_t qmoe_mx_tiles_bytes(const qmoe_dims* d, int64_t K);
+
+/* qmoe_permute_quant_mxfp8 -- the expert-sorted permutation of the routed
+ * activations and their MX quantisation (rule of qmoe_quant_act_mxfp8) in one
+ * pass: slot s of expert e (offsets[e] <= s < offsets[e+1]) gets the codes of
+ * token sorted_pair_ids[s] / k, written as MX activation tiles with K = H.
+ * ws = the workspace qmoe_align_sort filled for this routing. */
+int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+                             const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
+                             qmoe_stream_t stream);
 
 /* qmoe_quant_rows_int8_{bf16,f32} -- per-row symmetric int8 quantisation,
  * the activation-quantised W8A8 scheme of [gfx1151] Constraint: s = amax/127
@@ -202,14 +227,17 @@ int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const ui
                             const int32_t* offsets, const int32_t* sorted_pair_ids, uint16_t* h_bf16,
                             int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
-/* MXFP4 x FP8: x_q E4M3 [T, H] + x_s E8M0 [T, H/32] (from qmoe_quant_act_mxfp8);
- *        w1 E2M1 [E, 2I, H/2]; w1_s E8M0 [E, 2I, H/32];
- *        out h_q E4M3 [P, I] + h_s E8M0 [P, I/32]: the fp32 h quantised with
- *        the rule of qmoe_quant_act_mxfp8 along I. */
-int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1,
-                            const uint8_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                            uint8_t* h_q, uint8_t* h_s, int32_t* dev_status, void* ws, size_t ws_bytes,
-                            qmoe_stream_t stream);
+/* MXFP4 x FP8 (tensor cores; needs H % 256 == 0, I % 128 == 0, E <= 512):
+ *        x_tiles = qmoe_permute_quant_mxfp8 output (MX activation tiles, K = H);
+ *        w1 = qmoe_prepack_fp4_weights of the E2M1 [E*2I, H/2] bytes (32-byte
+ *        aligned); w1_s = qmoe_prepack_mx_scales of the E8M0 [E*2I, H/32] scales;
+ *        out h_tiles: the fp32 h quantised with the rule of
+ *        qmoe_quant_act_mxfp8 along I, stored as MX activation tiles (K = I),
+ *        qmoe_mx_tiles_bytes(d, I) bytes.  ws = the workspace that
+ *        qmoe_align_sort filled for this routing (it holds the tile schedule). */
+int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const uint8_t* w1_s,
+                            const int32_t* offsets, uint8_t* h_tiles, int32_t* dev_status, void* ws,
+                            size_t ws_bytes, qmoe_stream_t stream);
 
 /* W8A8: x_q int8 [T, H] + x_s fp32 [T] (from qmoe_quant_rows_int8_bf16);
  *        w1 int8 [E, 2I, H]; w1_s fp32 [E, 2I].  Accumulation is exact int32;
@@ -232,11 +260,12 @@ int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* 
                      const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
                      qmoe_stream_t stream);
 
-/* MXFP4 x FP8: h_q E4M3 [P, I] + h_s E8M0 [P, I/32]; w2 E2M1 [E, H, I/2];
- *        w2_s E8M0 [E, H, I/32]. */
-int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2,
-                     const uint8_t* w2_s, const int32_t* offsets, float* y, int32_t* dev_status, void* ws,
-                     size_t ws_bytes, qmoe_stream_t stream);
+/* MXFP4 x FP8: h_tiles from qmoe_gemm1_swiglu_mxfp4; w2 = qmoe_prepack_fp4_weights
+ *        of the E2M1 [E*H, I/2] bytes; w2_s = qmoe_prepack_mx_scales of the
+ *        E8M0 [E*H, I/32] scales; ws as for stage 1. */
+int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
+                     const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                     qmoe_stream_t stream);
 
 /* W8A8: h_q int8 [P, I] + h_s fp32 [P] (qmoe_quant_rows_int8_f32 of h);
  *        w2 int8 [E, H, I]; w2_s fp32 [E, H]; y = ((float)acc * h_s[s]) * w2_s[e][c];

@@ -48,10 +48,12 @@ SIGNATURES = {
     "qmoe_prepack_fp4_weights": ([_i64, _i64, _vp, _vp, _vp], _i32),
     "qmoe_prepack_mx_scales": ([_i64, _i64, _vp, _vp, _vp], _i32),
     "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_mx_tiles_bytes": ([_DP, _i64], _sz),
+    "qmoe_permute_quant_mxfp8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_combine": ([_DP, _vp, _vp, _vp, _vp, _vp], _i32),
     "qmoe_forward_workspace_bytes": ([_DP, _i32], _sz),
@@ -213,13 +215,20 @@ def qmoe_gemm1_swiglu_w4a16(d, x, w1, w1_s, offsets, sorted_pair_ids, h, status=
            "qmoe_gemm1_swiglu_w4a16")
 
 
-def qmoe_gemm1_swiglu_mxfp4(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, status=None, ws=None,
-                            stream=None):
+def mx_tiles_bytes(d: Dims, K: int) -> int:
+    return int(lib().qmoe_mx_tiles_bytes(ctypes.byref(d), K))
+
+
+def qmoe_permute_quant_mxfp8(d, x, sorted_pair_ids, offsets, x_tiles, ws, stream=None):
     wp, wn = _ws(ws)
-    status = _status(status, x_q.device)
-    _check(lib().qmoe_gemm1_swiglu_mxfp4(ctypes.byref(d), _ptr(x_q), _ptr(x_s), _ptr(w1), _ptr(w1_s), _ptr(offsets),
-                                         _ptr(sorted_pair_ids), _ptr(h_q), _ptr(h_s), _ptr(status), wp, wn,
-                                         _stream(stream)),
+    _check(lib().qmoe_permute_quant_mxfp8(ctypes.byref(d), _ptr(x), _ptr(sorted_pair_ids), _ptr(offsets),
+                                          _ptr(x_tiles), wp, wn, _stream(stream)), "qmoe_permute_quant_mxfp8")
+
+
+def qmoe_gemm1_swiglu_mxfp4(d, x_tiles, w1, w1_s, offsets, h_tiles, status, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_mxfp4(ctypes.byref(d), _ptr(x_tiles), _ptr(w1), _ptr(w1_s), _ptr(offsets),
+                                         _ptr(h_tiles), _ptr(status), wp, wn, _stream(stream)),
            "qmoe_gemm1_swiglu_mxfp4")
 
 
@@ -240,11 +249,10 @@ def qmoe_gemm2_w4a16(d, h, w2, w2_s, offsets, y, status=None, ws=None, stream=No
                                   _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_w4a16")
 
 
-def qmoe_gemm2_mxfp4(d, h_q, h_s, w2, w2_s, offsets, y, status=None, ws=None, stream=None):
+def qmoe_gemm2_mxfp4(d, h_tiles, w2, w2_s, offsets, y, status, ws, stream=None):
     wp, wn = _ws(ws)
-    status = _status(status, h_q.device)
-    _check(lib().qmoe_gemm2_mxfp4(ctypes.byref(d), _ptr(h_q), _ptr(h_s), _ptr(w2), _ptr(w2_s), _ptr(offsets),
-                                  _ptr(y), _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_mxfp4")
+    _check(lib().qmoe_gemm2_mxfp4(ctypes.byref(d), _ptr(h_tiles), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
+                                  _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_mxfp4")
 
 
 def qmoe_gemm2_w8a8(d, h_q, h_s, w2, w2_s, offsets, y, dbg_acc=None, status=None, ws=None, stream=None):

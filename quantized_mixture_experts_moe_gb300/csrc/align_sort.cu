@@ -16,6 +16,7 @@
 //               slot is its chunk base + the running count of earlier equal
 //               ids, so the result is the stable counting sort.
 #include "qmoe_common.cuh"
+#include "mx_tiles.cuh"
 
 namespace qmoe {
 
@@ -139,6 +140,41 @@ align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchu
     }
 }
 
+// Token-tile schedule for the tensor-core GEMMs: tile_start[e] = prefix over
+// experts of ceil(counts[e] / nmax), tile_start[E] = number of tiles.  One CTA.
+__global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ offsets, int E, int nmax,
+                                                             int32_t* __restrict__ tile_start) {
+    __shared__ int32_t warp_sums[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (E + 1023) / 1024;
+    const int e0 = tid * per, e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += (offsets[e + 1] - offsets[e] + nmax - 1) / nmax;
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = warp_sums[lane];
+        int wi = w;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += v;
+        }
+        warp_sums[lane] = wi - w;
+        if (lane == 31) tile_start[E] = wi;
+    }
+    __syncthreads();
+    int base = warp_sums[warp] + incl - local;
+    for (int e = e0; e < e1; ++e) {
+        tile_start[e] = base;
+        base += (offsets[e + 1] - offsets[e] + nmax - 1) / nmax;
+    }
+}
+
 size_t align_ws_bytes(int64_t P, int E) {
     const int64_t nchunks = (P + kChunk - 1) / kChunk;
     return (size_t)((nchunks * E * 4 + 255) / 256 * 256);
@@ -162,6 +198,11 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
     return launch_status();
 }
 
+// Where the tile schedule lives inside the routing workspace.
+int32_t* tile_schedule_in(void* ws, const qmoe_dims* d) {
+    return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + align_ws_bytes((int64_t)d->T * d->k, d->E));
+}
+
 }  // namespace qmoe
 
 extern "C" size_t qmoe_workspace_bytes(const qmoe_dims* d) {
@@ -182,6 +223,10 @@ extern "C" int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int3
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return QMOE_ERR_ARG;
     if (d->E > kMaxExperts) return QMOE_ERR_UNSUPPORTED;
     if (ws_bytes < align_ws_bytes(P, d->E)) return QMOE_ERR_ARG;
-    return align_sort_launch(P, d->E, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status,
-                             static_cast<int32_t*>(ws), (cudaStream_t)stream);
+    if (ws_bytes < qmoe_workspace_bytes(d)) return QMOE_ERR_ARG;
+    int rc = align_sort_launch(P, d->E, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status,
+                               static_cast<int32_t*>(ws), (cudaStream_t)stream);
+    if (rc != QMOE_OK) return rc;
+    tile_schedule_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(offsets, d->E, mxt::nmax_for(d), tile_schedule_in(ws, d));
+    return launch_status();
 }

@@ -2,6 +2,7 @@
 // whole-layer call.  Argument checks run on the host before any launch.
 #include "qmoe_common.cuh"
 #include "gemm_simt.cuh"
+#include "mx_tiles.cuh"
 
 namespace qmoe {
 size_t align_ws_bytes(int64_t P, int E);
@@ -14,11 +15,14 @@ int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float*
 int combine_launch(const qmoe_dims* d, const float* y, const float* topk_w, const int32_t* pair_slot, uint16_t* out,
                    cudaStream_t st);
 bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2);
-int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1, const uint8_t* w1_s,
-                const int32_t* offsets, const int32_t* sorted, uint8_t* h_q, uint8_t* h_s, int32_t* status,
+int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const uint8_t* w1_s,
+                const int32_t* offsets, const int32_t* tile_start, uint8_t* h_tiles, int32_t* status,
                 cudaStream_t st);
-int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2, const uint8_t* w2_s,
-                const int32_t* offsets, float* y, int32_t* status, cudaStream_t st);
+int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
+                const int32_t* offsets, const int32_t* tile_start, float* y, int32_t* status, cudaStream_t st);
+int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
+                            const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
+int32_t* tile_schedule_in(void* ws, const qmoe_dims* d);
 
 static int gemm_args_ok(const qmoe_dims* d, std::initializer_list<const void*> ptrs) {
     if (!dims_ok(d)) return QMOE_ERR_ARG;
@@ -63,20 +67,35 @@ extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf1
     return gemm_simt(0, 1, a, (cudaStream_t)stream);
 }
 
-extern "C" int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1,
-                                       const uint8_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                                       uint8_t* h_q, uint8_t* h_s, int32_t* dev_status, void* ws, size_t ws_bytes,
-                                       qmoe_stream_t stream) {
-    (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, dev_status});
+extern "C" size_t qmoe_mx_tiles_bytes(const qmoe_dims* d, int64_t K) {
+    if (!dims_ok(d) || K <= 0 || K % 128 != 0) return 0;
+    return (size_t)mxt::buffer_bytes(d, K);
+}
+
+static bool mx_ws_ok(const qmoe_dims* d, const void* ws, size_t ws_bytes) {
+    return ws && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && ws_bytes >= qmoe_workspace_bytes(d);
+}
+
+extern "C" int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+                                        const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
+                                        qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_bf16, sorted_pair_ids, offsets, x_tiles});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
-    if (mx_tc_ok(d, w1, nullptr))
-        return mx_tc_gemm1(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h_q, h_s, dev_status,
-                           (cudaStream_t)stream);
-    SimtArgs a = make_args(d);
-    a.act = x_q; a.act_s = x_s; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids;
-    a.out = h_q; a.out_s = h_s;
-    return gemm_simt(1, 1, a, (cudaStream_t)stream);
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (d->H % 128 != 0) return QMOE_ERR_UNSUPPORTED;
+    return permute_quant_mx_launch(d, x_bf16, sorted_pair_ids, offsets,
+                                   tile_schedule_in(const_cast<void*>(ws), d), x_tiles, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1,
+                                       const uint8_t* w1_s, const int32_t* offsets, uint8_t* h_tiles,
+                                       int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_tiles, w1, w1_s, offsets, h_tiles, dev_status});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!mx_tc_ok(d, w1, nullptr)) return QMOE_ERR_UNSUPPORTED;
+    return mx_tc_gemm1(d, x_tiles, w1, w1_s, offsets, tile_schedule_in(ws, d), h_tiles, dev_status,
+                       (cudaStream_t)stream);
 }
 
 extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x_s, const int8_t* w1,
@@ -104,17 +123,14 @@ extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, cons
     return gemm_simt(0, 2, a, (cudaStream_t)stream);
 }
 
-extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2,
-                                const uint8_t* w2_s, const int32_t* offsets, float* y, int32_t* dev_status, void* ws,
-                                size_t ws_bytes, qmoe_stream_t stream) {
-    (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y, dev_status});
+extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
+                                const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {h_tiles, w2, w2_s, offsets, y, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
-    if (mx_tc_ok(d, nullptr, w2))
-        return mx_tc_gemm2(d, h_q, h_s, w2, w2_s, offsets, y, dev_status, (cudaStream_t)stream);
-    SimtArgs a = make_args(d);
-    a.act = h_q; a.act_s = h_s; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y;
-    return gemm_simt(1, 2, a, (cudaStream_t)stream);
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!mx_tc_ok(d, nullptr, w2)) return QMOE_ERR_UNSUPPORTED;
+    return mx_tc_gemm2(d, h_tiles, w2, w2_s, offsets, tile_schedule_in(ws, d), y, dev_status, (cudaStream_t)stream);
 }
 
 extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2,
@@ -148,10 +164,10 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
     L.offsets = take(4 * (E + 1));
     L.sorted = take(4 * P);
     L.slot = take(4 * P);
-    L.xq = take(scheme == 0 ? 0 : T * H);
-    L.xs = take(scheme == 1 ? T * (H / 32) : (scheme == 2 ? 4 * T : 0));
-    L.h = take(scheme == 0 ? 2 * P * I : (scheme == 1 ? P * I : 4 * P * I));
-    L.hs = take(scheme == 1 ? P * (I / 32) : 0);
+    L.xq = take(scheme == 0 ? 0 : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : T * H));
+    L.xs = take(scheme == 2 ? 4 * T : 0);
+    L.h = take(scheme == 0 ? 2 * P * I : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
+    L.hs = 0;
     L.hq8 = take(scheme == 2 ? P * I : 0);
     L.hs8 = take(scheme == 2 ? 4 * P : 0);
     L.y = take(4 * P * H);
@@ -196,14 +212,13 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
             rc = qmoe_gemm2_w4a16(d, (const uint16_t*)at(L.h), (const uint8_t*)w2, (const uint16_t*)w2_s, offsets, y,
                                   dev_status, aws, aws_bytes, stream);
     } else if (scheme == 1) {
-        rc = qmoe_quant_act_mxfp8(d->T, d->H, x_bf16, (uint8_t*)at(L.xq), (uint8_t*)at(L.xs), stream);
+        rc = qmoe_permute_quant_mxfp8(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm1_swiglu_mxfp4(d, (const uint8_t*)at(L.xq), (const uint8_t*)at(L.xs), (const uint8_t*)w1,
-                                         (const uint8_t*)w1_s, offsets, sorted, (uint8_t*)at(L.h), (uint8_t*)at(L.hs),
-                                         dev_status, aws, aws_bytes, stream);
+            rc = qmoe_gemm1_swiglu_mxfp4(d, (const uint8_t*)at(L.xq), (const uint8_t*)w1, (const uint8_t*)w1_s,
+                                         offsets, (uint8_t*)at(L.h), dev_status, aws, aws_bytes, stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm2_mxfp4(d, (const uint8_t*)at(L.h), (const uint8_t*)at(L.hs), (const uint8_t*)w2,
-                                  (const uint8_t*)w2_s, offsets, y, dev_status, aws, aws_bytes, stream);
+            rc = qmoe_gemm2_mxfp4(d, (const uint8_t*)at(L.h), (const uint8_t*)w2, (const uint8_t*)w2_s, offsets, y,
+                                  dev_status, aws, aws_bytes, stream);
     } else {
         rc = qmoe_quant_rows_int8_bf16(d->T, d->H, x_bf16, (int8_t*)at(L.xq), (float*)at(L.xs), stream);
         if (rc == QMOE_OK)

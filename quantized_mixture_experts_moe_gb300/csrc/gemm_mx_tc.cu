@@ -45,6 +45,7 @@
 // activation rows through L2, and each unit streams a disjoint slice of the
 // expert's weights exactly once.
 #include "qmoe_common.cuh"
+#include "mx_tiles.cuh"
 #include "tc_ptx.cuh"
 
 #include <mutex>
@@ -55,8 +56,8 @@ namespace mx {
 
 // warp roles
 constexpr int WARP_A = 0;                   // weight producer (TMA)
-constexpr int WARP_B0 = 1, NBW = 4;         // activation producers, steps taken round-robin
-constexpr int WARP_MMA = WARP_B0 + NBW;     // TMEM owner + MMA issuer (stage 1: gate accumulator)
+constexpr int WARP_B = 1;                   // activation producer (bulk copies of stage-ready tiles)
+constexpr int WARP_MMA = 2;                 // TMEM owner + MMA issuer for weight tile 0
 constexpr int WARP_MMA2 = WARP_MMA + 1;     // stage 1: second issuer (up accumulator)
 constexpr int WARP_EPI0 = WARP_MMA2 + 1;    // epilogue warps
 constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant, splitting the token columns
@@ -79,7 +80,6 @@ struct Cfg {
     static constexpr int SLOT_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     // ring depth: as many whole steps as fit in the 227 KB of shared memory
     static constexpr int S = (220 * 1024 - 8 * 1024) / SLOT_BYTES;
-    static constexpr int NBA = (S < NBW) ? S : NBW;      // active activation producers (<= S: no parity aliasing)
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + S * A_BYTES;
     static constexpr int SFA_OFF = B_OFF + S * B_BYTES;
@@ -96,7 +96,7 @@ struct Cfg {
     static constexpr uint32_t SF_SLOT = 4 + NSFB * 4;
     static_assert(SF_COL + 2 * AT * SF_SLOT <= 512, "TMEM budget");
     static_assert(NMAX % 16 == 0 && NMAX <= 256, "N tile");
-    static_assert(S >= 2 && NBA <= S, "ring");
+    static_assert(S >= 2, "ring");
 };
 
 constexpr int MAX_E = 512;  // schedule prefix kept in shared memory
@@ -106,21 +106,19 @@ static_assert(Cfg<1, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<1, 224>::smem_byte
 
 struct Args {
     int T, k, H, I, E;
-    const uint8_t* act;       // stage 1: x_q [T, H]; stage 2: h_q [P, I]
-    const uint8_t* act_s;     // stage 1: x_s [T, H/32]; stage 2: h_s [P, I/32]
-    const uint8_t* w_s;       // pre-packed weight scale atoms
-    const int32_t* offsets;   // [E+1]
-    const int32_t* sorted;    // [P] (stage 1)
-    uint8_t* h_q;             // stage 1 outputs
-    uint8_t* h_s;
-    float* y;                 // stage 2 output
+    const uint8_t* act;         // MX activation tiles: stage 1 x (K = H), stage 2 h (K = I)
+    const uint8_t* w_s;         // pre-packed weight scale atoms
+    const int32_t* offsets;     // [E+1]
+    const int32_t* tile_start;  // [E+1] token-tile schedule (from the routing workspace)
+    uint8_t* h_tiles;           // stage 1 output: h as MX activation tiles (K = I)
+    float* y;                   // stage 2 output, slot order
     int32_t* status;
 };
 
 template <int NMAX>
 __device__ __forceinline__ void decode_unit(int u, int NB, const int* tile_start, int E, const int32_t* offsets,
-                                            int& e, int& m0, int& ntok, int& nb) {
-    const int t = u / NB;
+                                            int& e, int& m0, int& ntok, int& nb, int& t) {
+    t = u / NB;
     nb = u - t * NB;
     int lo = 0, hi = E;
     while (hi - lo > 1) {
@@ -168,24 +166,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     const int NB = (STAGE == 1) ? NOUT / 128 : NOUT / 256;  // stage 2 units cover two column blocks
     const int KT = K / KSTAGE;
 
-    // ---- schedule: tiles of up to NMAX tokens per expert, prefix over experts
-    if (warp == 0) {
-        int running = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const int cnt = (e < E) ? a.offsets[e + 1] - a.offsets[e] : 0;
-            const int tiles = (cnt + NMAX - 1) / NMAX;
-            int incl = tiles;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (e < E) tile_start[e] = running + incl - tiles;
-            running += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-        if (lane == 0) tile_start[E] = running;
-    }
+    // ---- token-tile schedule (computed with the routing sort)
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = a.tile_start[i];
     if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::S; ++s) {
             tc::mbar_init(&full[s], 2);        // weight producer (with tx bytes) + activation producer
@@ -220,8 +202,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
             const int64_t up_tiles = (int64_t)(a.I / 128) * KT;  // gate tile -> up tile distance (stage 1)
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
-                int e, m0, ntok, nb;
-                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+                int e, m0, ntok, nb, t;
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
                 const int rt0 = (STAGE == 1) ? (e * rows_per_e + nb * 128) / 128 : (e * rows_per_e + nb * 256) / 128;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&empty[slot], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
@@ -243,54 +225,26 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 }
             }
         }
-    } else if (warp < WARP_MMA) {
-        // ------------------------------------------------ activation producers (cp.async gather)
-        // The NBA active warps take steps round-robin.  A warp waits for its
-        // slot, issues the step's copies as one cp.async group, waits for
-        // that group, fences the writes to the async proxy and publishes the
-        // step: NBA L2 round trips are in flight at once.
-        const int wb = warp - WARP_B0;
-        const int rowbytes = K;        // one E4M3 code per element
-        const int srowbytes = K / 32;  // one E8M0 scale per 32 elements
-        constexpr int RPL = (NMAX + 31) / 32;  // rows per lane
-        int64_t step = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok && wb < C::NBA && !*abort_flag; u += gridDim.x) {
-            int e, m0, ntok, nb;
-            decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
-            int64_t src_row[RPL];
-#pragma unroll
-            for (int i = 0; i < RPL; ++i) {
-                const int r = lane + 32 * i;
-                src_row[i] = -1;
-                if (r < ntok) src_row[i] = (STAGE == 1) ? (int64_t)(a.sorted[m0 + r] / a.k) : (int64_t)(m0 + r);
-            }
-            for (int kt = 0; kt < KT; ++kt, ++step) {
-                if ((int)(step % C::NBA) != wb) continue;
-                const int slot = (int)(step % C::S);
-                const uint32_t parity = (uint32_t)((step / C::S) & 1) ^ 1u;
-                if (!warp_wait(&empty[slot], parity, lane)) {
-                    if (lane == 0) set_abort(abort_flag, a.status);
-                    ok = false;
-                    break;
+    } else if (warp == WARP_B) {
+        // ------------------------------------------------ activation producer (bulk copies)
+        // A step's activations are one block of the MX tile layout: the
+        // first nmma rows of codes (already swizzled) and the scale atoms.
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t phase = 0;
+            const int64_t bb = mxt::block_bytes(NMAX);
+            for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+                int e, m0, ntok, nb, t;
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
+                const uint32_t rows_bytes = (uint32_t)((ntok + 15) & ~15) * 128u;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!tc::mbar_wait(&empty[slot], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
+                    tc::mbar_arrive_expect_tx(&full[slot], rows_bytes + C::SFB_BYTES);
+                    const uint8_t* blk = a.act + ((int64_t)t * KT + kt) * bb;
+                    tc::bulk_load(sB + slot * C::B_BYTES, blk, rows_bytes, &full[slot]);
+                    tc::bulk_load(sSFB + slot * C::SFB_BYTES, blk + NMAX * 128, C::SFB_BYTES, &full[slot]);
+                    if (++slot == C::S) { slot = 0; phase ^= 1; }
                 }
-                uint8_t* dB = sB + slot * C::B_BYTES;
-                uint8_t* dS = sSFB + slot * C::SFB_BYTES;
-#pragma unroll
-                for (int i = 0; i < RPL; ++i) {
-                    if (src_row[i] < 0) continue;
-                    const int r = lane + 32 * i;
-                    const uint8_t* src = a.act + src_row[i] * rowbytes + kt * KSTAGE;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) tc::cp_async_16(dB + tc::sw128_offset(r, c), src + 16 * c);
-                    tc::cp_async_4(dS + (r >> 7) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3),
-                                   a.act_s + src_row[i] * srowbytes + kt * 4);
-                }
-                tc::cp_async_commit();
-                tc::cp_async_wait<0>();
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&full[slot]);
             }
         }
     } else if (warp == WARP_MMA || warp == WARP_MMA2) {
@@ -305,8 +259,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             uint32_t phase = 0, pacc = 0;
             const uint32_t sf_base = C::SF_COL + iss * 2 * C::SF_SLOT;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
-                int e, m0, ntok, nb;
-                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+                int e, m0, ntok, nb, t;
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
                 const int nmma = (ntok + 15) & ~15;
                 if (!tc::mbar_wait(&acc_empty[ab], pacc ^ 1)) { set_abort(abort_flag, a.status); break; }
                 tc::tc_fence_after();
@@ -350,8 +304,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         int ab = 0;
         uint32_t pacc = 0;
         for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
-            int e, m0, ntok, nb;
-            decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb);
+            int e, m0, ntok, nb, t;
+            decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
             int w = 1;
             if (lane == 0) w = tc::mbar_wait_sleep(&acc_full[ab], pacc) ? 1 : 0;
             if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {
@@ -360,7 +314,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             }
             tc::tc_fence_after();
             const uint32_t dcol = ab * C::ACC_COLS;
-            const int n = nb * 128 + q * 32 + lane;  // this lane's output column
+            // stage 1 writes h block (tile t, K step nb of the down projection)
+            uint8_t* hblk = (STAGE == 1) ? a.h_tiles + ((int64_t)t * (a.I / 128) + nb) * mxt::block_bytes(NMAX) : nullptr;
             for (int c0 = 16 * half; c0 < ntok; c0 += 32) {
                 uint32_t g[16];
                 tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + c0, g);
@@ -383,9 +338,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                             sb = (uint8_t)(X + 127);
                             code = (uint8_t)(e4m3x2_from_float(h * exp2i(-X), 0.f) & 0xFF);
                         }
-                        const int64_t slot = m0 + c;
-                        a.h_q[slot * a.I + n] = code;
-                        if (lane == 0) a.h_s[slot * (a.I / 32) + (n >> 5)] = sb;
+                        hblk[mxt::code_offset(c, q * 32 + lane)] = code;
+                        if (lane == 0) hblk[mxt::scale_offset(NMAX, c, q)] = sb;
                     }
                 } else {
                     // stage 2: column blocks 2nb (accumulator 0) and 2nb + 1 (accumulator 1)
@@ -508,37 +462,38 @@ static int launch_cfg(const void* w, int64_t tiles, int64_t half_bytes, const Ar
     return launch_status();
 }
 
-// Token-tile size: the average expert load decides (the grid never syncs
-// with the host to look at the real counts).  Up to ~100 tokens per expert a
-// 112-token tile with two accumulator buffers; above, 224-token tiles so an
-// expert's weights are still streamed once.  Both stages use the same tiles.
-static bool big_tiles(const qmoe_dims* d) { return (int64_t)d->T * d->k > (int64_t)96 * d->E; }
-
 }  // namespace mx
 
-int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const uint8_t* w1, const uint8_t* w1_s,
-                const int32_t* offsets, const int32_t* sorted, uint8_t* h_q, uint8_t* h_s, int32_t* status,
+// Token-tile size (mx_tiles.cuh): the average expert load decides, since the
+// grid never syncs with the host to look at the real counts.  Up to ~100
+// tokens per expert 112-token tiles with two accumulator buffers; above,
+// 224-token tiles so an expert's weights are still streamed once.  Both
+// stages and the permute/quantise kernel use the same tiles.
+int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const uint8_t* w1_s,
+                const int32_t* offsets, const int32_t* tile_start, uint8_t* h_tiles, int32_t* status,
                 cudaStream_t st) {
     mx::Args a{};
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
-    a.act = x_q; a.act_s = x_s; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted;
-    a.h_q = h_q; a.h_s = h_s; a.status = status;
+    a.act = x_tiles; a.w_s = w1_s; a.offsets = offsets; a.tile_start = tile_start;
+    a.h_tiles = h_tiles; a.status = status;
     const int64_t KT = d->H / 128;
     const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * KT;
-    const int64_t pair = (int64_t)(d->I / 128) * KT * 8192;  // bytes of one expert's gate (or up) tiles
-    return mx::big_tiles(d) ? mx::launch_cfg<1, 224>(w1, tiles, pair, a, st)
-                            : mx::launch_cfg<1, 112>(w1, tiles, pair, a, st);
+    const int64_t half = (int64_t)(d->I / 128) * KT * 8192;  // bytes of one expert's gate (or up) tiles
+    return mxt::nmax_for(d) == 224 ? mx::launch_cfg<1, 224>(w1, tiles, half, a, st)
+                                   : mx::launch_cfg<1, 112>(w1, tiles, half, a, st);
 }
 
-int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_q, const uint8_t* h_s, const uint8_t* w2, const uint8_t* w2_s,
-                const int32_t* offsets, float* y, int32_t* status, cudaStream_t st) {
+int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
+                const int32_t* offsets, const int32_t* tile_start, float* y, int32_t* status, cudaStream_t st) {
     mx::Args a{};
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
-    a.act = h_q; a.act_s = h_s; a.w_s = w2_s; a.offsets = offsets; a.y = y; a.status = status;
+    a.act = h_tiles; a.w_s = w2_s; a.offsets = offsets; a.tile_start = tile_start; a.y = y; a.status = status;
     const int64_t tiles = (int64_t)d->E * d->H / 128 * (d->I / 128);
-    return mx::big_tiles(d) ? mx::launch_cfg<2, 224>(w2, tiles, 0, a, st) : mx::launch_cfg<2, 112>(w2, tiles, 0, a, st);
+    return mxt::nmax_for(d) == 224 ? mx::launch_cfg<2, 224>(w2, tiles, 0, a, st)
+                                   : mx::launch_cfg<2, 112>(w2, tiles, 0, a, st);
 }
 
 bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2) { return mx::mx_tc_supported(d, w1, w2); }
+
 
 }  // namespace qmoe

@@ -318,8 +318,6 @@ int gemm_simt(int scheme, int stage, const SimtArgs& a, cudaStream_t st) {
     switch (scheme * 2 + (stage - 1)) {
         case 0: return gemm_simt_launch<S_W4A16, 1>(a, st);
         case 1: return gemm_simt_launch<S_W4A16, 2>(a, st);
-        case 2: return gemm_simt_launch<S_MXFP4, 1>(a, st);
-        case 3: return gemm_simt_launch<S_MXFP4, 2>(a, st);
         case 4: return gemm_simt_launch<S_W8A8, 1>(a, st);
         case 5: return gemm_simt_launch<S_W8A8, 2>(a, st);
     }

@@ -1,0 +1,43 @@
+// The MX activation tile layout shared by the permute/quantise kernel and the
+// block-scaled tensor-core GEMMs.
+//
+// Tokens of an expert are cut into tiles of up to NMAX slots (NMAX = 112, or
+// 224 when the average expert load exceeds 96 pairs); tile_start[e] is the
+// prefix over experts of ceil(count[e] / NMAX).  For a reduction length K an
+// activation buffer holds, per (tile t, K step kt of 128 elements), one block
+//   [NMAX rows x 128 bytes]  E4M3 codes, row r at r*128, its 16-byte chunk c
+//                            at ((c ^ (r & 7)) * 16)  (128-byte swizzle)
+//   [NSFB x 512 bytes]       E8M0 scales: row r, block b (0..3) of the step at
+//                            (r / 128) * 512 + 16 * (r % 32) + 4 * ((r % 128) / 32) + b
+// so a GEMM step fetches its activations with two contiguous bulk copies and
+// hands them to the MMA unchanged.
+#pragma once
+#include <stdint.h>
+
+#include "../../include/qmoe.h"
+
+namespace qmoe {
+namespace mxt {
+
+__host__ __device__ inline int nmax_for(const qmoe_dims* d) {
+    return ((int64_t)d->T * d->k > (int64_t)96 * d->E) ? 224 : 112;
+}
+__host__ __device__ inline int nsfb(int nmax) { return (nmax + 127) / 128; }
+__host__ __device__ inline int64_t block_bytes(int nmax) { return (int64_t)nmax * 128 + nsfb(nmax) * 512; }
+__host__ __device__ inline int64_t max_tiles(const qmoe_dims* d, int nmax) {
+    return ((int64_t)d->T * d->k + nmax - 1) / nmax + d->E;
+}
+__host__ __device__ inline int64_t buffer_bytes(const qmoe_dims* d, int64_t K) {
+    const int nmax = nmax_for(d);
+    return max_tiles(d, nmax) * (K / 128) * block_bytes(nmax);
+}
+__host__ __device__ inline uint32_t code_offset(int r, int col_in_step) {
+    return (uint32_t)r * 128u + (((uint32_t)(col_in_step >> 4) ^ (uint32_t)(r & 7)) << 4) + (uint32_t)(col_in_step & 15);
+}
+__host__ __device__ inline uint32_t scale_offset(int nmax, int r, int block_in_step) {
+    return (uint32_t)nmax * 128u + (uint32_t)(r >> 7) * 512u + 16u * (uint32_t)(r & 31) + 4u * (uint32_t)((r >> 5) & 3) +
+           (uint32_t)block_in_step;
+}
+
+}  // namespace mxt
+}  // namespace qmoe

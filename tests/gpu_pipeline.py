@@ -74,13 +74,13 @@ def run_layer(w, inp, keep=False):
         qb.qmoe_gemm2_w4a16(d, h, t["w2"], t["w2_s"], offsets, y, status, ws)
         res["h"] = h
     elif w.scheme == "mxfp4":
-        xq, xs = empty((T, H), torch.uint8), empty((T, H // 32), torch.uint8)
-        qb.qmoe_quant_act_mxfp8(t["x"], xq, xs)
-        hq, hs = empty((P, I), torch.uint8), empty((P, I // 32), torch.uint8)
+        xt = empty(qb.mx_tiles_bytes(d, H), torch.uint8)
+        ht = empty(qb.mx_tiles_bytes(d, I), torch.uint8)
+        qb.qmoe_permute_quant_mxfp8(d, t["x"], sorted_ids, offsets, xt, ws)
         w1, w1p, w2, w2p = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
-        qb.qmoe_gemm1_swiglu_mxfp4(d, xq, xs, w1, w1p, offsets, sorted_ids, hq, hs, status, ws)
-        qb.qmoe_gemm2_mxfp4(d, hq, hs, w2, w2p, offsets, y, status, ws)
-        res.update(xq=xq, xs=xs, hq=hq, hs=hs)
+        qb.qmoe_gemm1_swiglu_mxfp4(d, xt, w1, w1p, offsets, ht, status, ws)
+        qb.qmoe_gemm2_mxfp4(d, ht, w2, w2p, offsets, y, status, ws)
+        res.update(xt=xt, ht=ht)
     else:
         xq, xs = empty((T, H), torch.int8), empty(T, torch.float32)
         qb.qmoe_quant_rows_int8_bf16(t["x"], xq, xs)
@@ -101,4 +101,63 @@ def run_layer(w, inp, keep=False):
         for key, v in res.items():
             if v is not None:
                 r[key] = host(v, np.uint16) if v.dtype == torch.int16 else host(v)
+        if w.scheme == "mxfp4":
+            nmax = tile_nmax(T, k, E)
+            r["xq"], r["xs"] = unpack_tiles(r.pop("xt"), r["offsets"], nmax, H)
+            r["hq"], r["hs"] = unpack_tiles(r.pop("ht"), r["offsets"], nmax, I)
     return r
+
+
+# ------------------------------------------------------------------ MX activation tile layout (include/qmoe.h)
+
+def tile_nmax(T, k, E):
+    return 224 if T * k > 96 * E else 112
+
+
+def tile_schedule(offsets, nmax):
+    cnt = np.diff(offsets.astype(np.int64))
+    tiles = (cnt + nmax - 1) // nmax
+    return np.concatenate([[0], np.cumsum(tiles)]).astype(np.int64)
+
+
+def _tile_index(offsets, nmax, slots):
+    ts = tile_schedule(offsets, nmax)
+    e = np.searchsorted(offsets, slots, side="right") - 1
+    local = slots - offsets[e]
+    return ts[e] + local // nmax, local % nmax
+
+
+def _layout(nmax, K, t, r):
+    """Byte offsets [rows, K] of codes and [rows, K/32] of scales."""
+    nsfb = (nmax + 127) // 128
+    bb = nmax * 128 + nsfb * 512
+    KT = K // 128
+    col = np.arange(K)
+    kt, cin = col // 128, col % 128
+    chunk, byte = cin // 16, cin % 16
+    base = (t[:, None] * KT + kt[None, :]) * bb
+    code_off = base + r[:, None] * 128 + ((chunk[None, :] ^ (r[:, None] & 7)) << 4) + byte[None, :]
+    blk = np.arange(K // 32)
+    sbase = (t[:, None] * KT + (blk // 4)[None, :]) * bb
+    scale_off = (sbase + nmax * 128 + (r[:, None] // 128) * 512 + 16 * (r[:, None] % 32) +
+                 4 * ((r[:, None] % 128) // 32) + (blk % 4)[None, :])
+    return code_off, scale_off
+
+
+def unpack_tiles(buf, offsets, nmax, K):
+    """MX activation tiles -> slot-order codes [P_valid, K] and scales [P_valid, K/32]."""
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    co, so = _layout(nmax, K, t, r)
+    return buf[co], buf[so]
+
+
+def pack_tiles(codes, scales, offsets, nmax, K, nbytes):
+    """Slot-order codes/scales -> an MX activation tile buffer of nbytes."""
+    buf = np.zeros(nbytes, np.uint8)
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    co, so = _layout(nmax, K, t, r)
+    buf[co] = codes[:len(slots)]
+    buf[so] = scales[:len(slots)]
+    return buf
