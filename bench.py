@@ -84,7 +84,7 @@ def algorithmic(w, ids):
     g1_bytes = (Et * 2 * w.I * weight_bytes_per_row(w.scheme, w.H) + w.T * act_bytes_per_row(w.scheme, w.H)
                 + P * act_bytes_per_row(w.scheme, w.I))
     g2_bytes = (Et * w.H * weight_bytes_per_row(w.scheme, w.I) + P * act_bytes_per_row(w.scheme, w.I)
-                + P * w.H * 4)
+                + P * w.H * 2)
     return dict(experts_touched=Et, gemm1_bytes=g1_bytes, gemm2_bytes=g2_bytes,
                 gemm1_flops=4.0 * P * w.H * w.I, gemm2_flops=2.0 * P * w.H * w.I)
 
@@ -260,7 +260,7 @@ def run_ours(args, w):
     sorted_ids, slot = E_(P, torch.int32), E_(P, torch.int32)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = qb.alloc_workspace(qb.workspace_bytes(dims), dev)
-    y = E_((P, H), torch.float32)
+    y = E_((P, H), torch.int16)  # bf16 bits
     out = E_((T, H), torch.int16)
     if w.scheme == "mxfp4":
         xt = E_(qb.mx_tiles_bytes(dims, H), torch.uint8)

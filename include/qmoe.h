@@ -250,28 +250,28 @@ int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x
 
 /* ---------------------------------------------------------------- stage 2: down projection
  *
- * y[s][c] = W2[e][c] . hq[s] for c < H, slots of expert e as above; y fp32
- * [P, H] in slot order.  [aiter] Test Plan ("stage2 tiles"; K tiles larger
+ * y[s][c] = W2[e][c] . hq[s] for c < H, slots of expert e as above, summed
+ * in fp32 and stored as bf16 (round to nearest even) [P, H] in slot order.  [aiter] Test Plan ("stage2 tiles"; K tiles larger
  * than inter_dim read out of bounds, so the kernels never let a K tile pass
  * the end of I).
  *
  * W4A16: h bf16 [P, I]; w2 int4 [E, H, I/2]; w2_s fp16 [E, H, I/32]. */
 int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
-                     const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                     const int32_t* offsets, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes,
                      qmoe_stream_t stream);
 
 /* MXFP4 x FP8: h_tiles from qmoe_gemm1_swiglu_mxfp4; w2 = qmoe_prepack_fp4_weights
  *        of the E2M1 [E*H, I/2] bytes; w2_s = qmoe_prepack_mx_scales of the
  *        E8M0 [E*H, I/32] scales; ws as for stage 1. */
 int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
-                     const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                     const int32_t* offsets, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes,
                      qmoe_stream_t stream);
 
 /* W8A8: h_q int8 [P, I] + h_s fp32 [P] (qmoe_quant_rows_int8_f32 of h);
  *        w2 int8 [E, H, I]; w2_s fp32 [E, H]; y = ((float)acc * h_s[s]) * w2_s[e][c];
  *        dbg_acc (nullable) int32 [P, H]. */
 int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2, const float* w2_s,
-                    const int32_t* offsets, float* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
+                    const int32_t* offsets, uint16_t* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
                     size_t ws_bytes, qmoe_stream_t stream);
 
 /* ---------------------------------------------------------------- combine
@@ -280,9 +280,9 @@ int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, con
  * summed in fp32 with j ascending from 0 (a fixed order, so the result is
  * reproducible bit for bit: [hip-ep] description, "deterministic scatter
  * order").  Pairs with pair_slot = -1 contribute nothing.
- * in y fp32 [P, H] (slot order), topk_w fp32 [T, k], pair_slot int32 [P];
+ * in y bf16 [P, H] (slot order), topk_w fp32 [T, k], pair_slot int32 [P];
  * out out_bf16 [T, H]. */
-int qmoe_combine(const qmoe_dims* d, const float* y, const float* topk_w, const int32_t* pair_slot,
+int qmoe_combine(const qmoe_dims* d, const uint16_t* y, const float* topk_w, const int32_t* pair_slot,
                  uint16_t* out_bf16, qmoe_stream_t stream);
 
 /* ---------------------------------------------------------------- whole layer

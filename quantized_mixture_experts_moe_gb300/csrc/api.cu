@@ -12,14 +12,14 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
 int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
 template <typename In>
 int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float* s, cudaStream_t st);
-int combine_launch(const qmoe_dims* d, const float* y, const float* topk_w, const int32_t* pair_slot, uint16_t* out,
-                   cudaStream_t st);
+int combine_launch(const qmoe_dims* d, const uint16_t* y, const float* topk_w, const int32_t* pair_slot,
+                   uint16_t* out, cudaStream_t st);
 bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2);
 int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const uint8_t* w1_s,
                 const int32_t* offsets, const int32_t* tile_start, uint8_t* h_tiles, int32_t* status,
                 cudaStream_t st);
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
-                const int32_t* offsets, const int32_t* tile_start, float* y, int32_t* status, cudaStream_t st);
+                const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st);
 int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
                             const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
 int32_t* tile_schedule_in(void* ws, const qmoe_dims* d);
@@ -113,7 +113,7 @@ extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, con
 }
 
 extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
-                                const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                const int32_t* offsets, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes,
                                 qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
     int rc = gemm_args_ok(d, {h_bf16, w2, w2_s, offsets, y, dev_status});
@@ -124,7 +124,7 @@ extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, cons
 }
 
 extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
-                                const int32_t* offsets, float* y, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                const int32_t* offsets, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes,
                                 qmoe_stream_t stream) {
     int rc = gemm_args_ok(d, {h_tiles, w2, w2_s, offsets, y, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
@@ -134,7 +134,7 @@ extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, cons
 }
 
 extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2,
-                               const float* w2_s, const int32_t* offsets, float* y, int32_t* dbg_acc,
+                               const float* w2_s, const int32_t* offsets, uint16_t* y, int32_t* dbg_acc,
                                int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
     (void)ws; (void)ws_bytes;
     int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y, dev_status});
@@ -170,7 +170,7 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
     L.hs = 0;
     L.hq8 = take(scheme == 2 ? P * I : 0);
     L.hs8 = take(scheme == 2 ? 4 * P : 0);
-    L.y = take(4 * P * H);
+    L.y = take(2 * P * H);
     L.align_ws = take(qmoe_workspace_bytes(d));
     L.total = o;
     return L;
@@ -204,7 +204,7 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     if (rc != QMOE_OK) return rc;
     if (d->T == 0) return QMOE_OK;
     const int64_t P = (int64_t)d->T * d->k;
-    float* y = (float*)at(L.y);
+    uint16_t* y = (uint16_t*)at(L.y);
     if (scheme == 0) {
         rc = qmoe_gemm1_swiglu_w4a16(d, x_bf16, (const uint8_t*)w1, (const uint16_t*)w1_s, offsets, sorted,
                                      (uint16_t*)at(L.h), dev_status, aws, aws_bytes, stream);

@@ -6,7 +6,7 @@
 // computation written for sm_103a:
 //   stage 1: h = silu(W1_gate . x) * (W1_up . x), then MX-quantised to
 //            E4M3 codes + E8M0 scales per 32 columns of I;
-//   stage 2: y = W2 . h in fp32.
+//   stage 2: y = W2 . h, accumulated in fp32, stored as bf16.
 //
 // Structure (one persistent CTA per SM, 15 warps):
 //   warp 0     weight producer: per pipeline step one TMA load (a 4D box) of
@@ -111,7 +111,7 @@ struct Args {
     const int32_t* offsets;     // [E+1]
     const int32_t* tile_start;  // [E+1] token-tile schedule (from the routing workspace)
     uint8_t* h_tiles;           // stage 1 output: h as MX activation tiles (K = I)
-    float* y;                   // stage 2 output, slot order
+    uint16_t* y;                // stage 2 output: bf16, slot order
     int32_t* status;
 };
 
@@ -351,9 +351,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                     for (int j = 0; j < 16; ++j) {
                         const int c = c0 + j;
                         if (c >= ntok) break;
-                        float* yr = a.y + (int64_t)(m0 + c) * a.H;
-                        yr[n0] = __uint_as_float(g[j]);
-                        yr[n0 + 128] = __uint_as_float(g2[j]);
+                        uint16_t* yr = a.y + (int64_t)(m0 + c) * a.H;
+                        yr[n0] = float_to_bf16_bits(__uint_as_float(g[j]));
+                        yr[n0 + 128] = float_to_bf16_bits(__uint_as_float(g2[j]));
                     }
                 }
             }
@@ -484,7 +484,7 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
 }
 
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
-                const int32_t* offsets, const int32_t* tile_start, float* y, int32_t* status, cudaStream_t st) {
+                const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st) {
     mx::Args a{};
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = h_tiles; a.w_s = w2_s; a.offsets = offsets; a.tile_start = tile_start; a.y = y; a.status = status;

@@ -7,7 +7,8 @@
 // W8A8) in shared memory, so this path is also the exact reference point for
 // the tensor-core kernels.  Stage 1 computes the gate rows n and the up rows
 // I + n of the same 64 columns and applies SwiGLU and the scheme's
-// intermediate quantisation in the epilogue; stage 2 writes fp32 y rows.
+// intermediate quantisation in the epilogue; stage 2 writes y rows (fp32
+// sums stored as bf16).
 #include "qmoe_common.cuh"
 #include "gemm_simt.cuh"
 
@@ -240,8 +241,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) o[c] = (float)acc[0][r][c];
             }
-            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (int64_t)slot * a.H + col) =
-                make_float4(o[0], o[1], o[2], o[3]);
+            uint2 ob;
+            ob.x = (uint32_t)float_to_bf16_bits(o[0]) | ((uint32_t)float_to_bf16_bits(o[1]) << 16);
+            ob.y = (uint32_t)float_to_bf16_bits(o[2]) | ((uint32_t)float_to_bf16_bits(o[3]) << 16);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + (int64_t)slot * a.H + col) = ob;
             continue;
         }
         // stage 1 epilogue: SwiGLU, then the scheme's intermediate format

@@ -13,7 +13,7 @@ struct SimtArgs {
     const void* w_s;        // weight scales
     const int32_t* offsets; // [E+1]
     const int32_t* sorted;  // [P] slot -> pair id (stage 1)
-    void* out;              // stage 1: intermediate; stage 2: y fp32 [P, H]
+    void* out;              // stage 1: intermediate; stage 2: y bf16 [P, H]
     void* out_s;            // stage 1 MXFP4: intermediate scales
     int32_t* dbg_acc;       // W8A8: raw int32 accumulators (nullable)
 };

@@ -66,7 +66,7 @@ def run_layer(w, inp, keep=False):
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     ws = qb.alloc_workspace(qb.workspace_bytes(d))
     qb.qmoe_align_sort(d, t["topk_ids"], counts, offsets, sorted_ids, slot, status, ws)
-    y = empty((P, H), torch.float32)
+    y = empty((P, H), torch.int16)  # bf16 bits
     res = {}
     if w.scheme == "w4a16":
         h = empty((P, I), torch.int16)
@@ -97,7 +97,7 @@ def run_layer(w, inp, keep=False):
     torch.cuda.synchronize()
     r = dict(out=host(out, np.uint16), status=int(status.item()))
     if keep:
-        r.update(offsets=host(offsets), sorted_pair_ids=host(sorted_ids), pair_slot=host(slot), y=host(y))
+        r.update(offsets=host(offsets), sorted_pair_ids=host(sorted_ids), pair_slot=host(slot), y=host(y, np.uint16))
         for key, v in res.items():
             if v is not None:
                 r[key] = host(v, np.uint16) if v.dtype == torch.int16 else host(v)

@@ -176,13 +176,14 @@ def test_stage2_against_oracle(w):
     counts = np.bincount(experts, minlength=w.E).astype(np.int32)
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     d = qb.dims(rows, 1, w.H, w.I, w.E)
-    y = gp.empty((rows, w.H), torch.float32)
+    y = gp.empty((rows, w.H), torch.int16)  # bf16 bits
     t_off = gp.dev(offsets)
+    yv = lambda: gp.bf16_to_f64(gp.host(y, np.uint16))
     if w.scheme == "w4a16":
         qb.qmoe_gemm2_w4a16(d, gp.dev(s2["h"]), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), t_off, y)
         ref = oracle.stage2("w4a16", w.H, w.I, w.E, experts, s2["h"], None, wts["w2"], wts["w2_s"])
         torch.cuda.synchronize()
-        assert rel_l2(gp.host(y), ref) < 1e-5
+        assert rel_l2(yv(), ref) < 5e-3
     elif w.scheme == "mxfp4":
         # the routing sort fills the workspace's tile schedule for these expert loads
         ids = experts.reshape(rows, 1)
@@ -197,7 +198,7 @@ def test_stage2_against_oracle(w):
         qb.qmoe_gemm2_mxfp4(d, gp.dev(ht), w2w, w2p, off_t, y, st, ws)
         ref = oracle.stage2("mxfp4", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"])
         torch.cuda.synchronize()
-        assert rel_l2(gp.host(y), ref) < 1e-5
+        assert rel_l2(yv(), ref) < 5e-3
     else:
         acc = gp.empty((rows, w.H), torch.int32)
         qb.qmoe_gemm2_w8a8(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), t_off, y,
@@ -206,7 +207,9 @@ def test_stage2_against_oracle(w):
                                   acc=True)
         torch.cuda.synchronize()
         assert np.array_equal(gp.host(acc), racc)
-        assert np.array_equal(gp.host(y).astype(np.float64), ref)
+        # y = ((float)acc * s_h) * s_w is exact fp32 on both sides; both round it to bf16
+        ref_bf16 = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+        assert np.array_equal(gp.host(y), ref_bf16)
 
 
 def test_w8a8_adversarial_accumulators_exact():
@@ -222,7 +225,7 @@ def test_w8a8_adversarial_accumulators_exact():
     experts = np.repeat(np.arange(w.E, dtype=np.int32), rows // w.E)
     offsets = np.array([0, rows // 2, rows], np.int32)
     d = qb.dims(rows, 1, w.H, w.I, w.E)
-    y, acc = gp.empty((rows, w.H), torch.float32), gp.empty((rows, w.H), torch.int32)
+    y, acc = gp.empty((rows, w.H), torch.int16), gp.empty((rows, w.H), torch.int32)
     qb.qmoe_gemm2_w8a8(d, gp.dev(h), gp.dev(hs), gp.dev(w2), gp.dev(w2s), gp.dev(offsets), y, acc)
     torch.cuda.synchronize()
     _, racc = oracle.stage2("w8a8", w.H, w.I, w.E, experts, h, hs, w2, w2s, acc=True)
@@ -238,7 +241,7 @@ def test_combine_against_oracle_and_deterministic():
     ids = gen.routing_uniform(rng, T, 64, k)
     ids[5, 3] = 99  # one invalid pair: slot -1
     ro = oracle.align_sort(ids, 64)
-    y = rng.standard_normal((T * k, H)).astype(np.float32)
+    y = gen.bf16_bits_from_f32(rng.standard_normal((T * k, H)).astype(np.float32))
     tw = gen.routing_weights(rng, T, k)
     d = qb.dims(T, k, H, 32, 64)
     outs = []
@@ -248,7 +251,7 @@ def test_combine_against_oracle_and_deterministic():
         torch.cuda.synchronize()
         outs.append(gp.host(out, np.uint16))
     assert np.array_equal(outs[0], outs[1])
-    ref = oracle.combine(y, tw, ro["pair_slot"])
+    ref = oracle.combine(gp.bf16_to_f64(y).astype(np.float32), tw, ro["pair_slot"])
     assert rel_l2(gp.bf16_to_f64(outs[0]), ref) < REL_L2
 
 
