@@ -6,23 +6,23 @@
 // one: within an expert, slots follow ascending pair id p = t*k + j.
 //
 // Three launches, none of which lets an atomic decide an order:
-//   1. hist:    each warp owns a contiguous chunk of kChunk pairs and builds
-//               its per-expert histogram in shared memory (warp match-any
-//               groups equal ids; the group leader adds the group size).
+//   1. hist:    each CTA owns a contiguous chunk of kChunk pairs and counts
+//               them per expert (shared-memory counters).
 //   2. scan:    one CTA turns the [chunk][expert] histograms into per-chunk
 //               base slots (exclusive over chunks within an expert, plus the
 //               expert's offset) and writes counts and offsets.
-//   3. scatter: each warp walks its chunk again in 32-pair steps; a pair's
-//               slot is its chunk base + the running count of earlier equal
-//               ids, so the result is the stable counting sort.
+//   3. scatter: each CTA walks its chunk again in pair order; a pair's slot
+//               is its chunk base + the running count of earlier equal ids,
+//               so the result is the stable counting sort.
+// (A fourth, tiny launch derives the GEMMs' token-tile schedule.)
 #include "qmoe_common.cuh"
 #include "mx_tiles.cuh"
 
 namespace qmoe {
 
-constexpr int kChunk = 2048;          // pairs per warp chunk
-constexpr int kWarpsPerCta = 8;       // warps (chunks) per CTA in hist/scatter
-constexpr int kMaxExperts = 4096;     // shared-memory histogram bound
+constexpr int kChunk = 2048;          // pairs per chunk (one CTA)
+constexpr int kThreads = 1024;        // threads per CTA in hist/scatter (two rounds per chunk)
+constexpr int kMaxExperts = 4096;     // shared-memory counter bound
 constexpr int kScanThreads = 1024;
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -31,33 +31,34 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+// Per-chunk expert histogram: counts do not depend on order, so shared-memory
+// atomics are fine here.
+__global__ void __launch_bounds__(kThreads)
 align_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks, int32_t* __restrict__ hist,
                   int32_t* __restrict__ dev_status) {
-    extern __shared__ int32_t smem_hist[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunk = blockIdx.x * kWarpsPerCta + warp;
-    int32_t* h = smem_hist + (size_t)warp * E;
-    for (int e = lane; e < E; e += 32) h[e] = 0;
-    __syncwarp();
-    if (chunk >= nchunks) return;
-    bool bad = false;
-    const int64_t p0 = (int64_t)chunk * kChunk;
-    for (int step = 0; step < kChunk / 32; ++step) {
-        const int64_t p = p0 + step * 32 + lane;
-        int e = -1;
-        if (p < P) e = ids[p];
-        const bool valid = (e >= 0 && e < E);
-        bad |= (p < P) && !valid;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
-        if (valid && (peers & lanemask_lt()) == 0) h[e] += __popc(peers);
-        __syncwarp();
+    extern __shared__ int32_t cnt[];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
+    __syncthreads();
+    const int64_t p0 = (int64_t)blockIdx.x * kChunk;
+    int bad = 0;
+    for (int i = tid; i < kChunk; i += kThreads) {
+        const int64_t p = p0 + i;
+        if (p < P) {
+            const int e = ids[p];
+            if (e >= 0 && e < E)
+                atomicAdd(&cnt[e], 1);
+            else
+                bad = 1;
+        }
     }
-    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(dev_status, QMOE_DEV_BAD_EXPERT_ID);
-    int32_t* out = hist + (size_t)chunk * E;
-    for (int e = lane; e < E; e += 32) out[e] = h[e];
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(dev_status, QMOE_DEV_BAD_EXPERT_ID);
+    int32_t* out = hist + (size_t)blockIdx.x * E;
+    for (int e = tid; e < E; e += kThreads) out[e] = cnt[e];
 }
 
+// One CTA: per expert, chunk bases exclusive over chunks (loads issued eight
+// at a time so they overlap), counts, offsets, and the -1 tail of sorted ids.
 __global__ void __launch_bounds__(kScanThreads)
 align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int32_t* __restrict__ counts,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids) {
@@ -66,14 +67,18 @@ align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int
     const int tid = threadIdx.x;
     const int per = (E + kScanThreads - 1) / kScanThreads;
     const int e0 = tid * per, e1 = min(E, e0 + per);
-    // per-expert totals, chunk bases made exclusive over chunks
     int local = 0;
     for (int e = e0; e < e1; ++e) {
         int run = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            int32_t v = hist[(size_t)c * E + e];
-            hist[(size_t)c * E + e] = run;
-            run += v;
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+            int32_t v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = (c0 + j < nchunks) ? hist[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (c0 + j < nchunks) hist[(size_t)(c0 + j) * E + e] = run;
+                run += v[j];
+            }
         }
         counts[e] = run;
         local += run;
@@ -108,31 +113,37 @@ align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int
     for (int64_t s = (int64_t)total_valid + tid; s < P; s += kScanThreads) sorted_pair_ids[s] = -1;
 }
 
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+// Stable scatter: the CTA walks its chunk in two rounds of 1024 pairs; inside
+// a round the 32 warps take turns (in pair order) on the per-expert cursors,
+// each warp ranking equal ids among its lanes with match-any.  A pair's slot
+// is therefore its chunk base + the number of earlier pairs of the same
+// expert in the chunk: the stable counting sort.
+__global__ void __launch_bounds__(kThreads)
 align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
                      const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_pair_ids,
                      int32_t* __restrict__ pair_slot) {
-    extern __shared__ int32_t smem_cursor[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunk = blockIdx.x * kWarpsPerCta + warp;
-    if (chunk >= nchunks) return;
-    int32_t* cur = smem_cursor + (size_t)warp * E;
-    const int32_t* base = hist + (size_t)chunk * E;
-    for (int e = lane; e < E; e += 32) cur[e] = base[e];
-    __syncwarp();
-    const int64_t p0 = (int64_t)chunk * kChunk;
-    for (int step = 0; step < kChunk / 32; ++step) {
-        const int64_t p = p0 + step * 32 + lane;
-        if (p0 + step * 32 >= P) break;  // warp-uniform
+    extern __shared__ int32_t cur[];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int32_t* base = hist + (size_t)blockIdx.x * E;
+    for (int e = tid; e < E; e += kThreads) cur[e] = base[e];
+    __syncthreads();
+    const int64_t p0 = (int64_t)blockIdx.x * kChunk;
+    for (int round = 0; round < kChunk / kThreads; ++round) {
+        const int64_t p = p0 + round * kThreads + tid;
         int e = -1;
         if (p < P) e = ids[p];
-        const bool valid = (e >= 0 && e < E);
+        const bool valid = (p < P) && e >= 0 && e < E;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+        const uint32_t before = peers & lanemask_lt();
         int slot = -1;
-        if (valid) slot = cur[e] + __popc(peers & lanemask_lt());
-        __syncwarp();
-        if (valid && (peers & lanemask_lt()) == 0) cur[e] += __popc(peers);
-        __syncwarp();
+        for (int w = 0; w < kThreads / 32; ++w) {
+            if (warp == w) {
+                if (valid) slot = cur[e] + __popc(before);
+                __syncwarp();
+                if (valid && before == 0) cur[e] += __popc(peers);
+            }
+            __syncthreads();
+        }
         if (p < P) {
             pair_slot[p] = slot;
             if (valid) sorted_pair_ids[slot] = (int32_t)p;
@@ -184,17 +195,16 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
                       int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
                       cudaStream_t stream) {
     const int nchunks = (int)((P + kChunk - 1) / kChunk);
-    const size_t smem = (size_t)kWarpsPerCta * E * sizeof(int32_t);
-    const int ctas = (nchunks + kWarpsPerCta - 1) / kWarpsPerCta;
+    const size_t smem = (size_t)E * sizeof(int32_t);
     if (smem > 48 * 1024) {
         cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     }
-    if (ctas > 0) align_hist_kernel<<<ctas, kWarpsPerCta * 32, smem, stream>>>(ids, P, E, nchunks, hist, dev_status);
+    if (nchunks > 0) align_hist_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, dev_status);
     align_scan_kernel<<<1, kScanThreads, 0, stream>>>(hist, P, E, nchunks, counts, offsets, sorted_pair_ids);
-    if (ctas > 0)
-        align_scatter_kernel<<<ctas, kWarpsPerCta * 32, smem, stream>>>(ids, P, E, nchunks, hist, sorted_pair_ids,
-                                                                         pair_slot);
+    if (nchunks > 0)
+        align_scatter_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, sorted_pair_ids,
+                                                                  pair_slot);
     return launch_status();
 }
 

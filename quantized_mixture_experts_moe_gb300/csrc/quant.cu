@@ -81,76 +81,94 @@ quant_rows_int8_kernel(const In* __restrict__ x, int64_t cols, int8_t* __restric
     if (threadIdx.x == 0) s[row] = sc;
 }
 
-// Permute + MX-quantise: one CTA per expert-sorted slot.  The slot's token
-// row of bf16 x is quantised with the same rule as quant_mx_bf16_kernel and
-// written straight into the MX activation tile layout (mx_tiles.cuh), so the
-// tensor-core GEMM reads it with bulk copies.  Each thread owns 16
-// consecutive elements; two neighbouring threads form one 32-element block.
-__global__ void __launch_bounds__(256)
+// Permute + MX-quantise: one warp per expert-sorted slot (8 per CTA).  The
+// slot's token row of bf16 x is quantised with the same rule as
+// quant_mx_bf16_kernel and written straight into the MX activation tile
+// layout (mx_tiles.cuh), so the tensor-core GEMM reads it with bulk copies.
+// A lane owns 16 consecutive elements per pass; neighbouring lanes pair up
+// into one 32-element block.
+constexpr int kPqWarps = 8;
+
+__device__ __forceinline__ void mx_quant16(const uint4 v0, const uint4 v1, uint4& codes, uint8_t& sb) {
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    codes = make_uint4(0, 0, 0, 0);
+    sb = 127;
+    if (amax > 0.f) {
+        const int X = mx_block_exponent(amax);
+        const float m = exp2i(-X);
+        sb = (uint8_t)(X + 127);
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = (uint32_t)e4m3x2_from_float(f[4 * i] * m, f[4 * i + 1] * m) |
+                   ((uint32_t)e4m3x2_from_float(f[4 * i + 2] * m, f[4 * i + 3] * m) << 16);
+        codes = make_uint4(c[0], c[1], c[2], c[3]);
+    }
+}
+
+__global__ void __launch_bounds__(kPqWarps * 32)
 permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
-                        int H, int nmax, uint8_t* __restrict__ tiles) {
-    __shared__ int s_tile, s_row, s_tok;
-    const int64_t slot = blockIdx.x;
-    if (threadIdx.x == 0) {
-        s_tile = -1;
-        if (slot < offsets[E]) {
-            int lo = 0, hi = E;  // largest e with offsets[e] <= slot
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (offsets[mid] <= slot) lo = mid; else hi = mid;
-            }
-            const int local = (int)(slot - offsets[lo]);
-            s_tile = tile_start[lo] + local / nmax;
-            s_row = local % nmax;
-            s_tok = sorted_pair_ids[slot] / k;
+                        int H, int nmax, int64_t P, uint8_t* __restrict__ tiles) {
+    const int lane = threadIdx.x & 31;
+    const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
+    int tile = -1, row = 0, tok = 0;
+    if (lane == 0 && slot < P && slot < offsets[E]) {
+        int lo = 0, hi = E;  // largest e with offsets[e] <= slot
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (offsets[mid] <= slot) lo = mid; else hi = mid;
         }
+        const int local = (int)(slot - offsets[lo]);
+        tile = tile_start[lo] + local / nmax;
+        row = local % nmax;
+        tok = sorted_pair_ids[slot] / k;
     }
-    __syncthreads();
-    if (s_tile < 0) return;
-    const int r = s_row;
-    const uint16_t* xr = x + (int64_t)s_tok * H;
+    tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
+    if (tile < 0) return;  // warp-uniform
+    row = __shfl_sync(0xFFFFFFFFu, row, 0);
+    tok = __shfl_sync(0xFFFFFFFFu, tok, 0);
+    const uint16_t* xr = x + (int64_t)tok * H;
     const int KT = H / 128;
     const int64_t bb = mxt::block_bytes(nmax);
-    uint8_t* tbase = tiles + (int64_t)s_tile * KT * bb;
+    uint8_t* tbase = tiles + (int64_t)tile * KT * bb;
+    const int nchunk = H / 16;
     // warp-uniform trip count: every lane reaches the pairwise shuffle
-    for (int j0 = 0; j0 < H / 16; j0 += blockDim.x) {
-        const int j = j0 + threadIdx.x;  // 16-element chunk
-        const bool active = j < H / 16;
-        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-        if (active) {
-            v0 = *reinterpret_cast<const uint4*>(xr + 16 * j);
-            v1 = *reinterpret_cast<const uint4*>(xr + 16 * j + 8);
+    for (int j0 = 0; j0 < nchunk; j0 += 64) {
+        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
+        const int ja = j0 + lane, jb = j0 + 32 + lane;
+        if (ja < nchunk) {
+            a0 = *reinterpret_cast<const uint4*>(xr + 16 * ja);
+            a1 = *reinterpret_cast<const uint4*>(xr + 16 * ja + 8);
         }
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        float f[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        if (jb < nchunk) {
+            b0 = *reinterpret_cast<const uint4*>(xr + 16 * jb);
+            b1 = *reinterpret_cast<const uint4*>(xr + 16 * jb + 8);
         }
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        if (!active) continue;
-        uint4 codes = make_uint4(0, 0, 0, 0);
-        uint8_t sb = 127;
-        if (amax > 0.f) {
-            const int X = mx_block_exponent(amax);
-            const float m = exp2i(-X);
-            sb = (uint8_t)(X + 127);
-            uint32_t c[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                c[i] = (uint32_t)e4m3x2_from_float(f[4 * i] * m, f[4 * i + 1] * m) |
-                       ((uint32_t)e4m3x2_from_float(f[4 * i + 2] * m, f[4 * i + 3] * m) << 16);
-            codes = make_uint4(c[0], c[1], c[2], c[3]);
+        uint4 ca, cb;
+        uint8_t sa, sbb;
+        mx_quant16(a0, a1, ca, sa);
+        mx_quant16(b0, b1, cb, sbb);
+        if (ja < nchunk) {
+            uint8_t* blk = tbase + (int64_t)(ja >> 3) * bb;
+            *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (ja & 7) * 16)) = ca;
+            if ((ja & 1) == 0) blk[mxt::scale_offset(nmax, row, (ja >> 1) & 3)] = sa;
         }
-        const int kt = j >> 3, col = (j & 7) * 16;
-        uint8_t* blk = tbase + (int64_t)kt * bb;
-        *reinterpret_cast<uint4*>(blk + mxt::code_offset(r, col)) = codes;
-        if ((j & 1) == 0) blk[mxt::scale_offset(nmax, r, (j >> 1) & 3)] = sb;
+        if (jb < nchunk) {
+            uint8_t* blk = tbase + (int64_t)(jb >> 3) * bb;
+            *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (jb & 7) * 16)) = cb;
+            if ((jb & 1) == 0) blk[mxt::scale_offset(nmax, row, (jb >> 1) & 3)] = sbb;
+        }
     }
 }
 
@@ -158,8 +176,9 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
                             const int32_t* tile_start, uint8_t* tiles, cudaStream_t st) {
     const int64_t P = (int64_t)d->T * d->k;
     if (P == 0) return QMOE_OK;
-    permute_quant_mx_kernel<<<(unsigned)P, 256, 0, st>>>(x, sorted, offsets, tile_start, d->E, d->k, d->H,
-                                                         mxt::nmax_for(d), tiles);
+    const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
+    permute_quant_mx_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, sorted, offsets, tile_start, d->E, d->k,
+                                                                       d->H, mxt::nmax_for(d), P, tiles);
     return launch_status();
 }
 
