@@ -251,6 +251,10 @@ def run_ours(args, w):
     if w.scheme == "mxfp4":  # one-time weight preparation (not part of a step)
         t["w1"], t["w1_s"], t["w2"], t["w2_s"] = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
         torch.cuda.synchronize(dev)
+    elif w.scheme == "w4a16":  # codes and scales pre-packed together
+        t["w1"], t["w2"] = qb.prepack_w4a16(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
+        t["w1_s"] = t["w2_s"] = None
+        torch.cuda.synchronize(dev)
     dims = qb.dims(T, k, H, I, E)
     stream = torch.cuda.current_stream(dev)
 
@@ -270,7 +274,8 @@ def run_ours(args, w):
         h32 = E_((P, I), torch.float32)
         hq, hs = E_((P, I), torch.int8), E_(P, torch.float32)
     else:
-        h16 = E_((P, I), torch.int16)
+        xt = E_(qb.bf16_tiles_bytes(dims, H), torch.uint8)
+        ht = E_(qb.bf16_tiles_bytes(dims, I), torch.uint8)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
     g1_pairs, g2_pairs = [], []
@@ -281,6 +286,8 @@ def run_ours(args, w):
             qb.qmoe_permute_quant_mxfp8(dims, t["x"], sorted_ids, offsets, xt, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_quant_rows_int8_bf16(t["x"], xq, xs)
+        else:
+            qb.qmoe_permute_bf16(dims, t["x"], sorted_ids, offsets, xt, ws)
         a, b, c = (ev(), ev(), ev()) if record else (None, None, None)
         if record:
             a.record(stream)
@@ -289,7 +296,7 @@ def run_ours(args, w):
         elif w.scheme == "w8a8":
             qb.qmoe_gemm1_swiglu_w8a8(dims, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h32, None, status, ws)
         else:
-            qb.qmoe_gemm1_swiglu_w4a16(dims, t["x"], t["w1"], t["w1_s"], offsets, sorted_ids, h16, status, ws)
+            qb.qmoe_gemm1_swiglu_w4a16(dims, xt, t["w1"], offsets, ht, status, ws)
         if record:
             b.record(stream)
         if w.scheme == "mxfp4":
@@ -298,14 +305,14 @@ def run_ours(args, w):
             qb.qmoe_quant_rows_int8_f32(h32, hq, hs)
             qb.qmoe_gemm2_w8a8(dims, hq, hs, t["w2"], t["w2_s"], offsets, y, None, status, ws)
         else:
-            qb.qmoe_gemm2_w4a16(dims, h16, t["w2"], t["w2_s"], offsets, y, status, ws)
+            qb.qmoe_gemm2_w4a16(dims, ht, t["w2"], offsets, y, status, ws)
         if record:
             c.record(stream)
             g1_pairs.append((a, b))
             g2_pairs.append((b, c))
         qb.qmoe_combine(dims, y, t["topk_w"], slot, out)
 
-    launches_per_step = 4 + (1 if w.scheme != "w4a16" else 0) + 2 + (1 if w.scheme == "w8a8" else 0) + 1
+    launches_per_step = 4 + 1 + 2 + (1 if w.scheme == "w8a8" else 0) + 1
 
     def barrier():
         if world > 1:

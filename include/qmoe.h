@@ -44,7 +44,8 @@
  *   bf16      uint16 bit patterns.
  *   int4      W [rows, K/2] bytes; element 2i in the low nibble of byte i,
  *             2i+1 in the high nibble; stored n = q + 8, value (n - 8) * s;
- *             scales fp16 [rows, K/32].
+ *             scales fp16 [rows, K/32].  The W4A16 GEMMs take codes and
+ *             scales pre-packed together (qmoe_prepack_int4_weights).
  *   E2M1      same nibble order; OCP MX element encoding; scales E8M0
  *             (value 2^(b-127)), one per 32 K elements.  The MXFP4 GEMMs take
  *             weights and scales pre-packed (qmoe_prepack_fp4_weights,
@@ -176,6 +177,26 @@ int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const i
                              const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                              qmoe_stream_t stream);
 
+/* bf16 activation tiles -- the layout in which the W4A16 GEMMs take their
+ * activations (x for stage 1, h for stage 2): the token tiles of the MX
+ * layout above (same NMAX and tile_start), per (tile t, K step kt of 64
+ * elements) one block of NMAX*128 bytes at ((t * K/64) + kt) * NMAX*128,
+ * row r's 64 bf16 values at r*128 with 16-byte chunk c at ((c ^ (r % 8)) * 16).
+ * Rows past a tile's token count are unspecified.
+ *
+ * qmoe_bf16_tiles_bytes -- bytes of such a buffer for dims *d and length K
+ * (K a multiple of 64; 0 otherwise). */
+size_t qmoe_bf16_tiles_bytes(const qmoe_dims* d, int64_t K);
+
+/* qmoe_permute_bf16 -- the expert-sorted permutation of the routed bf16
+ * activations, written as bf16 activation tiles with K = H: slot s of expert
+ * e gets row sorted_pair_ids[s] / k of x_bf16 [T, H] ([hip-ep] description:
+ * one grouped launch over all experts' routed tokens).  H % 64 == 0.
+ * ws = the workspace qmoe_align_sort filled for this routing. */
+int qmoe_permute_bf16(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+                      const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
+                      qmoe_stream_t stream);
+
 /* qmoe_quant_rows_int8_{bf16,f32} -- per-row symmetric int8 quantisation,
  * the activation-quantised W8A8 scheme of [gfx1151] Constraint: s = amax/127
  * (1 when amax = 0), q = clamp(rint(v / s), -127, 127), all in fp32.
@@ -211,6 +232,21 @@ size_t qmoe_fp4_weights_packed_bytes(int64_t rows, int64_t K);
 int qmoe_prepack_fp4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor, uint8_t* w_packed,
                              qmoe_stream_t stream);
 
+/* qmoe_prepack_int4_weights -- one-time rearrangement of symmetric int4
+ * weights (codes [rows, K/2] bytes, nibble order as above, n = q + 8) and
+ * their fp16 scales [rows, K/32] into the blocks the W4A16 GEMMs read: per
+ * (128-row tile rt, 64-element K step kt) one 4608-byte block at
+ * (rt * ceil(K/64) + kt) * 4608 holding row r's 32 code bytes at r*32 and
+ * then, at 4096 + r*4, its two fp16 scales of the step.  Inside each 32-bit
+ * code word (8 elements) the nibbles are reordered so that nibble j holds
+ * element 2j and nibble 4+j element 2j+1 (j = 0..3).  Padding codes are 8
+ * (value 0), padding scales 0.  K % 32 == 0; packed 16-byte aligned, codes
+ * 4-byte aligned.  Output size: qmoe_int4_weights_packed_bytes(rows, K).
+ * No counterpart on the pages (a storage-order choice, made at load time). */
+size_t qmoe_int4_weights_packed_bytes(int64_t rows, int64_t K);
+int qmoe_prepack_int4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor, const uint16_t* s_fp16,
+                              uint8_t* packed, qmoe_stream_t stream);
+
 /* ---------------------------------------------------------------- stage 1: gate/up + SwiGLU
  *
  * For every expert e and slot s in [offsets[e], offsets[e+1]), with
@@ -221,11 +257,17 @@ int qmoe_prepack_fp4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor,
  * [aiter] Changes/Test Plan (stage 1 of the grouped a8w4 kernel).
  * Only slots < offsets[E] are written.
  *
- * W4A16: x bf16 [T, H]; w1 int4 [E, 2I, H/2]; w1_s fp16 [E, 2I, H/32];
- *        out h bf16 [P, I] (round to nearest even from fp32). */
-int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const uint8_t* w1, const uint16_t* w1_s,
-                            const int32_t* offsets, const int32_t* sorted_pair_ids, uint16_t* h_bf16,
-                            int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+ * W4A16 (tensor cores, bf16 MMAs; needs H % 256 == 0, I % 128 == 0,
+ *        E <= 512): x_tiles = qmoe_permute_bf16 output (bf16 activation
+ *        tiles, K = H); w1 = qmoe_prepack_int4_weights of the int4 [E*2I, H/2]
+ *        codes and their fp16 [E*2I, H/32] scales.  Each weight is
+ *        dequantised on chip to bf16 as bf16(bf16(s) * (n - 8)) ([gfx1151]
+ *        Problem: dequantise to bf16, then a bf16 dot), products summed in
+ *        fp32; out h_tiles: h rounded to bf16 (nearest even), stored as bf16
+ *        activation tiles with K = I, qmoe_bf16_tiles_bytes(d, I) bytes.
+ *        ws = the workspace that qmoe_align_sort filled for this routing. */
+int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const int32_t* offsets,
+                            uint8_t* h_tiles, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
 /* MXFP4 x FP8 (tensor cores; needs H % 256 == 0, I % 128 == 0, E <= 512):
  *        x_tiles = qmoe_permute_quant_mxfp8 output (MX activation tiles, K = H);
@@ -255,10 +297,12 @@ int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x
  * than inter_dim read out of bounds, so the kernels never let a K tile pass
  * the end of I).
  *
- * W4A16: h bf16 [P, I]; w2 int4 [E, H, I/2]; w2_s fp16 [E, H, I/32]. */
-int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
-                     const int32_t* offsets, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes,
-                     qmoe_stream_t stream);
+ * W4A16: h_tiles from qmoe_gemm1_swiglu_w4a16 (bf16 activation tiles,
+ *        K = I); w2 = qmoe_prepack_int4_weights of the int4 [E*H, I/2] codes
+ *        and fp16 [E*H, I/32] scales, dequantised as in stage 1; ws as for
+ *        stage 1. */
+int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
+                     uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
 /* MXFP4 x FP8: h_tiles from qmoe_gemm1_swiglu_mxfp4; w2 = qmoe_prepack_fp4_weights
  *        of the E2M1 [E*H, I/2] bytes; w2_s = qmoe_prepack_mx_scales of the
@@ -291,7 +335,8 @@ int qmoe_combine(const qmoe_dims* d, const uint16_t* y, const float* topk_w, con
  * W8A8), stage 1, intermediate quantisation (W8A8), stage 2 and combine, all
  * launched in order on `stream`.  scheme: 0 = W4A16, 1 = MXFP4 x FP8,
  * 2 = W8A8.  Weights and scales as for the per-stage calls (MXFP4 weights
- * and scales pre-packed).  All
+ * and scales pre-packed; W4A16 weights pre-packed with their scales, so
+ * w1_s and w2_s are ignored and may be NULL for scheme 0).  All
  * intermediates live in the caller's workspace of
  * qmoe_forward_workspace_bytes(d, scheme) bytes (256-byte aligned).
  * dev_status as for qmoe_align_sort. */

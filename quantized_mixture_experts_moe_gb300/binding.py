@@ -47,12 +47,16 @@ SIGNATURES = {
     "qmoe_fp4_weights_packed_bytes": ([_i64, _i64], _sz),
     "qmoe_prepack_fp4_weights": ([_i64, _i64, _vp, _vp, _vp], _i32),
     "qmoe_prepack_mx_scales": ([_i64, _i64, _vp, _vp, _vp], _i32),
-    "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_int4_weights_packed_bytes": ([_i64, _i64], _sz),
+    "qmoe_prepack_int4_weights": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
+    "qmoe_bf16_tiles_bytes": ([_DP, _i64], _sz),
+    "qmoe_permute_bf16": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_mx_tiles_bytes": ([_DP, _i64], _sz),
     "qmoe_permute_quant_mxfp8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_combine": ([_DP, _vp, _vp, _vp, _vp, _vp], _i32),
@@ -207,12 +211,42 @@ def prepack_mx_scales(s_rowmajor, K: int, stream=None):
     return out
 
 
-def qmoe_gemm1_swiglu_w4a16(d, x, w1, w1_s, offsets, sorted_pair_ids, h, status=None, ws=None, stream=None):
+def int4_weights_packed_bytes(rows: int, K: int) -> int:
+    return int(lib().qmoe_int4_weights_packed_bytes(rows, K))
+
+
+def qmoe_prepack_int4_weights(w_rowmajor, s_fp16, packed, rows: int, K: int, stream=None):
+    _check(lib().qmoe_prepack_int4_weights(rows, K, _ptr(w_rowmajor), _ptr(s_fp16), _ptr(packed), _stream(stream)),
+           "qmoe_prepack_int4_weights")
+
+
+def prepack_int4_weights(w_rowmajor, s_fp16, K: int, stream=None):
+    """int4 codes [..., K/2] + fp16 scales [..., K/32] (rows = all leading dims) -> packed byte tensor."""
+    rows = w_rowmajor.numel() // (K // 2)
+    out = torch.empty(max(int4_weights_packed_bytes(rows, K), 16), dtype=torch.uint8, device=w_rowmajor.device)
+    qmoe_prepack_int4_weights(w_rowmajor.contiguous(), s_fp16.contiguous(), out, rows, K, stream)
+    return out
+
+
+def prepack_w4a16(w1, w1_s, w2, w2_s, H: int, I: int, stream=None):
+    """Both W4A16 weight tensors (codes with their scales) in the form the GEMMs take."""
+    return prepack_int4_weights(w1, w1_s, H, stream), prepack_int4_weights(w2, w2_s, I, stream)
+
+
+def bf16_tiles_bytes(d: Dims, K: int) -> int:
+    return int(lib().qmoe_bf16_tiles_bytes(ctypes.byref(d), K))
+
+
+def qmoe_permute_bf16(d, x, sorted_pair_ids, offsets, x_tiles, ws, stream=None):
     wp, wn = _ws(ws)
-    status = _status(status, x.device)
-    _check(lib().qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), _ptr(x), _ptr(w1), _ptr(w1_s), _ptr(offsets),
-                                         _ptr(sorted_pair_ids), _ptr(h), _ptr(status), wp, wn, _stream(stream)),
-           "qmoe_gemm1_swiglu_w4a16")
+    _check(lib().qmoe_permute_bf16(ctypes.byref(d), _ptr(x), _ptr(sorted_pair_ids), _ptr(offsets), _ptr(x_tiles),
+                                   wp, wn, _stream(stream)), "qmoe_permute_bf16")
+
+
+def qmoe_gemm1_swiglu_w4a16(d, x_tiles, w1, offsets, h_tiles, status, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), _ptr(x_tiles), _ptr(w1), _ptr(offsets), _ptr(h_tiles),
+                                         _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm1_swiglu_w4a16")
 
 
 def mx_tiles_bytes(d: Dims, K: int) -> int:
@@ -242,11 +276,10 @@ def qmoe_gemm1_swiglu_w8a8(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h, d
            "qmoe_gemm1_swiglu_w8a8")
 
 
-def qmoe_gemm2_w4a16(d, h, w2, w2_s, offsets, y, status=None, ws=None, stream=None):
+def qmoe_gemm2_w4a16(d, h_tiles, w2, offsets, y, status, ws, stream=None):
     wp, wn = _ws(ws)
-    status = _status(status, h.device)
-    _check(lib().qmoe_gemm2_w4a16(ctypes.byref(d), _ptr(h), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
-                                  _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_w4a16")
+    _check(lib().qmoe_gemm2_w4a16(ctypes.byref(d), _ptr(h_tiles), _ptr(w2), _ptr(offsets), _ptr(y), _ptr(status),
+                                  wp, wn, _stream(stream)), "qmoe_gemm2_w4a16")
 
 
 def qmoe_gemm2_mxfp4(d, h_tiles, w2, w2_s, offsets, y, status, ws, stream=None):

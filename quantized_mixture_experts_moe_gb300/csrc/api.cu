@@ -23,6 +23,13 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, c
 int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
                             const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
 int32_t* tile_schedule_in(void* ws, const qmoe_dims* d);
+int permute_bf16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
+                        const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
+bool w4_tc_ok(const qmoe_dims* d);
+int w4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const int32_t* offsets,
+                const int32_t* tile_start, uint8_t* h_tiles, int32_t* status, cudaStream_t st);
+int w4_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
+                const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st);
 
 static int gemm_args_ok(const qmoe_dims* d, std::initializer_list<const void*> ptrs) {
     if (!dims_ok(d)) return QMOE_ERR_ARG;
@@ -54,18 +61,6 @@ extern "C" const char* qmoe_status_str(int code) {
 }
 
 extern "C" const char* qmoe_version(void) { return "qmoe-gb300 0.1 (sm_103a)"; }
-
-extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint16_t* x_bf16, const uint8_t* w1,
-                                       const uint16_t* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                                       uint16_t* h_bf16, int32_t* dev_status, void* ws, size_t ws_bytes,
-                                       qmoe_stream_t stream) {
-    (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {x_bf16, w1, w1_s, offsets, sorted_pair_ids, h_bf16, dev_status});
-    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
-    SimtArgs a = make_args(d);
-    a.act = x_bf16; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids; a.out = h_bf16;
-    return gemm_simt(0, 1, a, (cudaStream_t)stream);
-}
 
 extern "C" size_t qmoe_mx_tiles_bytes(const qmoe_dims* d, int64_t K) {
     if (!dims_ok(d) || K <= 0 || K % 128 != 0) return 0;
@@ -109,18 +104,7 @@ extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, con
     SimtArgs a = make_args(d);
     a.act = x_q; a.act_s = x_s; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids;
     a.out = h; a.dbg_acc = dbg_acc;
-    return gemm_simt(2, 1, a, (cudaStream_t)stream);
-}
-
-extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint16_t* h_bf16, const uint8_t* w2, const uint16_t* w2_s,
-                                const int32_t* offsets, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes,
-                                qmoe_stream_t stream) {
-    (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {h_bf16, w2, w2_s, offsets, y, dev_status});
-    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
-    SimtArgs a = make_args(d);
-    a.act = h_bf16; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y;
-    return gemm_simt(0, 2, a, (cudaStream_t)stream);
+    return gemm_simt_w8a8(1, a, (cudaStream_t)stream);
 }
 
 extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
@@ -133,6 +117,43 @@ extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, cons
     return mx_tc_gemm2(d, h_tiles, w2, w2_s, offsets, tile_schedule_in(ws, d), y, dev_status, (cudaStream_t)stream);
 }
 
+// ------------------------------------------------------------------ W4A16 (bf16 tensor cores)
+
+extern "C" size_t qmoe_bf16_tiles_bytes(const qmoe_dims* d, int64_t K) {
+    if (!dims_ok(d) || K <= 0 || K % 64 != 0) return 0;
+    return (size_t)bft::buffer_bytes(d, K);
+}
+
+extern "C" int qmoe_permute_bf16(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+                                 const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
+                                 qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_bf16, sorted_pair_ids, offsets, x_tiles});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (d->H % 64 != 0) return QMOE_ERR_UNSUPPORTED;
+    return permute_bf16_launch(d, x_bf16, sorted_pair_ids, offsets, tile_schedule_in(const_cast<void*>(ws), d),
+                               x_tiles, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1,
+                                       const int32_t* offsets, uint8_t* h_tiles, int32_t* dev_status, void* ws,
+                                       size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_tiles, w1, offsets, h_tiles, dev_status});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!w4_tc_ok(d)) return QMOE_ERR_UNSUPPORTED;
+    return w4_tc_gemm1(d, x_tiles, w1, offsets, tile_schedule_in(ws, d), h_tiles, dev_status, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
+                                uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {h_tiles, w2, offsets, y, dev_status});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!w4_tc_ok(d)) return QMOE_ERR_UNSUPPORTED;
+    return w4_tc_gemm2(d, h_tiles, w2, offsets, tile_schedule_in(ws, d), y, dev_status, (cudaStream_t)stream);
+}
+
 extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2,
                                const float* w2_s, const int32_t* offsets, uint16_t* y, int32_t* dbg_acc,
                                int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
@@ -142,7 +163,7 @@ extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const floa
     if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
     SimtArgs a = make_args(d);
     a.act = h_q; a.act_s = h_s; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y; a.dbg_acc = dbg_acc;
-    return gemm_simt(2, 2, a, (cudaStream_t)stream);
+    return gemm_simt_w8a8(2, a, (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------ whole layer
@@ -164,9 +185,11 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
     L.offsets = take(4 * (E + 1));
     L.sorted = take(4 * P);
     L.slot = take(4 * P);
-    L.xq = take(scheme == 0 ? 0 : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : T * H));
+    L.xq = take(scheme == 0 ? (size_t)bft::buffer_bytes(d, d->H)
+                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : T * H));
     L.xs = take(scheme == 2 ? 4 * T : 0);
-    L.h = take(scheme == 0 ? 2 * P * I : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
+    L.h = take(scheme == 0 ? (size_t)bft::buffer_bytes(d, d->I)
+                           : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
     L.hs = 0;
     L.hq8 = take(scheme == 2 ? P * I : 0);
     L.hs8 = take(scheme == 2 ? 4 * P : 0);
@@ -191,7 +214,8 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || !dev_status) return QMOE_ERR_ARG;
     const FwdLayout L = fwd_layout(d, scheme);
     if (ws_bytes < L.total) return QMOE_ERR_ARG;
-    if (d->T > 0 && (!x_bf16 || !topk_ids || !topk_w || !w1 || !w1_s || !w2 || !w2_s || !out_bf16)) return QMOE_ERR_ARG;
+    if (d->T > 0 && (!x_bf16 || !topk_ids || !topk_w || !w1 || !w2 || !out_bf16)) return QMOE_ERR_ARG;
+    if (d->T > 0 && scheme != 0 && (!w1_s || !w2_s)) return QMOE_ERR_ARG;
     char* base = static_cast<char*>(ws);
     auto at = [&](size_t off) { return static_cast<void*>(base + off); };
     int32_t* counts = (int32_t*)at(L.counts);
@@ -206,11 +230,13 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     const int64_t P = (int64_t)d->T * d->k;
     uint16_t* y = (uint16_t*)at(L.y);
     if (scheme == 0) {
-        rc = qmoe_gemm1_swiglu_w4a16(d, x_bf16, (const uint8_t*)w1, (const uint16_t*)w1_s, offsets, sorted,
-                                     (uint16_t*)at(L.h), dev_status, aws, aws_bytes, stream);
+        rc = qmoe_permute_bf16(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm2_w4a16(d, (const uint16_t*)at(L.h), (const uint8_t*)w2, (const uint16_t*)w2_s, offsets, y,
-                                  dev_status, aws, aws_bytes, stream);
+            rc = qmoe_gemm1_swiglu_w4a16(d, (const uint8_t*)at(L.xq), (const uint8_t*)w1, offsets, (uint8_t*)at(L.h),
+                                         dev_status, aws, aws_bytes, stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_gemm2_w4a16(d, (const uint8_t*)at(L.h), (const uint8_t*)w2, offsets, y, dev_status, aws,
+                                  aws_bytes, stream);
     } else if (scheme == 1) {
         rc = qmoe_permute_quant_mxfp8(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)

@@ -1,14 +1,13 @@
-// Grouped expert GEMMs, plain SIMT tiles (all schemes).
+// Grouped W8A8 expert GEMMs, plain SIMT tiles with exact int32 accumulation.
 //
 // One launch covers every expert ("perf(qmoe): group prefill expert matmuls",
 // description): the grid's x index enumerates (expert, 32-slot tile) pairs in
 // expert order, found by a per-CTA scan of the expert offsets, and y the
-// output-column tiles.  Operands are dequantised exactly to fp32 (int32 for
-// W8A8) in shared memory, so this path is also the exact reference point for
-// the tensor-core kernels.  Stage 1 computes the gate rows n and the up rows
-// I + n of the same 64 columns and applies SwiGLU and the scheme's
-// intermediate quantisation in the epilogue; stage 2 writes y rows (fp32
-// sums stored as bf16).
+// output-column tiles.  int8 x int8 products are summed in int32 ("Evaluate
+// native IU4/IU8 WMMA for grouped-INT MoE prefill on gfx1151", Constraint).
+// Stage 1 computes the gate rows n and the up rows I + n of the same 64
+// columns and applies the dequantisation and SwiGLU in the epilogue; stage 2
+// writes y rows (fp32 stored as bf16).
 #include "qmoe_common.cuh"
 #include "gemm_simt.cuh"
 
@@ -17,17 +16,6 @@ namespace qmoe {
 constexpr int BM = 32;  // slots per tile
 constexpr int BN = 64;  // output columns per tile
 constexpr int BK = 32;  // one scale block
-
-enum { S_W4A16 = 0, S_MXFP4 = 1, S_W8A8 = 2 };
-
-template <int SCHEME>
-struct Acc {
-    using T = float;
-};
-template <>
-struct Acc<S_W8A8> {
-    using T = int32_t;
-};
 
 // Finds this CTA's (expert, slot range) from the expert offsets: tile b of the
 // sequence in which expert e contributes ceil(M_e / BM) tiles.  Returns false
@@ -70,81 +58,32 @@ __device__ bool find_tile(const int32_t* __restrict__ offsets, int E, int b, int
     return s_e >= 0;
 }
 
-// ---- operand loaders: 4 consecutive K elements of an activation row
-template <int SCHEME>
-__device__ __forceinline__ void load_act4(const SimtArgs& a, int64_t row, int K, int kk, typename Acc<SCHEME>::T* o) {
-    if constexpr (SCHEME == S_W4A16) {
-        const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.act) + row * K + kk);
-        o[0] = __uint_as_float(v.x << 16);
-        o[1] = __uint_as_float(v.x & 0xFFFF0000u);
-        o[2] = __uint_as_float(v.y << 16);
-        o[3] = __uint_as_float(v.y & 0xFFFF0000u);
-    } else if constexpr (SCHEME == S_MXFP4) {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.act) + row * K + kk);
-        const float s = e8m0_to_float(static_cast<const uint8_t*>(a.act_s)[row * (K / 32) + kk / 32]);
+// ---- 4 consecutive K elements of an activation row
+__device__ __forceinline__ void load_act4(const SimtArgs& a, int64_t row, int K, int kk, int32_t* o) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(static_cast<const int8_t*>(a.act) + row * K + kk);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = e4m3_to_float((uint8_t)(v >> (8 * i))) * s;
-    } else {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(static_cast<const int8_t*>(a.act) + row * K + kk);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = (int32_t)(int8_t)(v >> (8 * i));
-    }
+    for (int i = 0; i < 4; ++i) o[i] = (int32_t)(int8_t)(v >> (8 * i));
 }
 
 // ---- NE consecutive K elements (NE = 16 or 8, from element kk) of weight row `wrow`
-template <int SCHEME, int NE>
-__device__ __forceinline__ void load_w(const SimtArgs& a, int64_t wrow, int K, int kk, typename Acc<SCHEME>::T* o) {
-    if constexpr (SCHEME == S_W8A8) {
-        const int8_t* p = static_cast<const int8_t*>(a.w) + wrow * K + kk;
-        uint32_t v[NE / 4];
-        if constexpr (NE == 16) {
-            const uint4 t = *reinterpret_cast<const uint4*>(p);
-            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-        } else {
-            const uint2 t = *reinterpret_cast<const uint2*>(p);
-            v[0] = t.x; v[1] = t.y;
-        }
-#pragma unroll
-        for (int i = 0; i < NE; ++i) o[i] = (int32_t)(int8_t)(v[i / 4] >> (8 * (i % 4)));
+template <int NE>
+__device__ __forceinline__ void load_w(const SimtArgs& a, int64_t wrow, int K, int kk, int32_t* o) {
+    const int8_t* p = static_cast<const int8_t*>(a.w) + wrow * K + kk;
+    uint32_t v[NE / 4];
+    if constexpr (NE == 16) {
+        const uint4 t = *reinterpret_cast<const uint4*>(p);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
     } else {
-        const uint8_t* p;
-        if constexpr (SCHEME == S_W4A16) {
-            p = static_cast<const uint8_t*>(a.w) + wrow * (K / 2) + kk / 2;
-        } else {
-            // tile-major pre-packed: 128x128 tiles of 8 KiB, 64 bytes per tile row
-            const int64_t KT = (K + 127) / 128;
-            p = static_cast<const uint8_t*>(a.w) + ((wrow / 128) * KT + kk / 128) * 8192 + (wrow & 127) * 64 +
-                (kk & 127) / 2;
-        }
-        uint32_t v[NE / 8];
-        if constexpr (NE == 16) {
-            const uint2 t = *reinterpret_cast<const uint2*>(p);
-            v[0] = t.x; v[1] = t.y;
-        } else {
-            v[0] = *reinterpret_cast<const uint32_t*>(p);
-        }
-        float s;
-        if constexpr (SCHEME == S_W4A16)
-            s = __half2float(__ushort_as_half(static_cast<const uint16_t*>(a.w_s)[wrow * (K / 32) + kk / 32]));
-        else {
-            // pre-packed scale atoms: (row tile, group of 4 blocks) x 512 bytes
-            const int64_t kb = kk / 32, KG = (K + 127) / 128;
-            const int64_t atom = (wrow / 128) * KG + kb / 4;
-            const int r = (int)(wrow & 127);
-            s = e8m0_to_float(static_cast<const uint8_t*>(a.w_s)[atom * 512 + 16 * (r & 31) + 4 * (r >> 5) + (kb & 3)]);
-        }
-#pragma unroll
-        for (int i = 0; i < NE; ++i) {
-            const uint32_t nib = (v[i / 8] >> (4 * (i % 8))) & 15u;  // element 2b in the low nibble of byte b
-            const float q = (SCHEME == S_W4A16) ? (float)((int)nib - 8) : e2m1_to_float(nib);
-            o[i] = q * s;
-        }
+        const uint2 t = *reinterpret_cast<const uint2*>(p);
+        v[0] = t.x; v[1] = t.y;
     }
+#pragma unroll
+    for (int i = 0; i < NE; ++i) o[i] = (int32_t)(int8_t)(v[i / 4] >> (8 * (i % 4)));
 }
 
-template <int SCHEME, int STAGE>
+template <int STAGE>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
-    using AccT = typename Acc<SCHEME>::T;
+    using AccT = int32_t;
     constexpr int NW = (STAGE == 1) ? 2 * BN : BN;  // weight rows per tile
     __shared__ AccT As[BM][BK + 1];
     __shared__ AccT Bs[NW][BK + 1];
@@ -191,13 +130,13 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
 
     for (int k0 = 0; k0 < K; k0 += BK) {
         AccT av[4] = {0, 0, 0, 0};
-        if (lvalid) load_act4<SCHEME>(a, arow, K, k0 + (tid & 7) * 4, av);
+        if (lvalid) load_act4(a, arow, K, k0 + (tid & 7) * 4, av);
 #pragma unroll
         for (int i = 0; i < 4; ++i) As[lr][(tid & 7) * 4 + i] = av[i];
         AccT wv[NE];
 #pragma unroll
         for (int i = 0; i < NE; ++i) wv[i] = 0;
-        if (wvalid) load_w<SCHEME, NE>(a, wrow, K, k0 + wk, wv);
+        if (wvalid) load_w<NE>(a, wrow, K, k0 + wk, wv);
 #pragma unroll
         for (int i = 0; i < NE; ++i) Bs[wr_local][wk + i] = wv[i];
         __syncthreads();
@@ -228,18 +167,13 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
         if (STAGE == 2) {
             if (!(rvalid && cvalid)) continue;
             float o[4];
-            if constexpr (SCHEME == S_W8A8) {
-                const float hs = static_cast<const float*>(a.act_s)[slot];
-                const float* sw = static_cast<const float*>(a.w_s) + (int64_t)e * a.H;
+            const float hs = static_cast<const float*>(a.act_s)[slot];
+            const float* sw = static_cast<const float*>(a.w_s) + (int64_t)e * a.H;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) o[c] = __fmul_rn(__fmul_rn((float)acc[0][r][c], hs), sw[col + c]);
-                if (a.dbg_acc) {
+            for (int c = 0; c < 4; ++c) o[c] = __fmul_rn(__fmul_rn((float)acc[0][r][c], hs), sw[col + c]);
+            if (a.dbg_acc) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) a.dbg_acc[(int64_t)slot * a.H + col + c] = (int32_t)acc[0][r][c];
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o[c] = (float)acc[0][r][c];
+                for (int c = 0; c < 4; ++c) a.dbg_acc[(int64_t)slot * a.H + col + c] = (int32_t)acc[0][r][c];
             }
             uint2 ob;
             ob.x = (uint32_t)float_to_bf16_bits(o[0]) | ((uint32_t)float_to_bf16_bits(o[1]) << 16);
@@ -247,64 +181,32 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
             *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + (int64_t)slot * a.H + col) = ob;
             continue;
         }
-        // stage 1 epilogue: SwiGLU, then the scheme's intermediate format
-        float h[4];
-        if constexpr (SCHEME == S_W8A8) {
-            if (rvalid && cvalid) {
-                const int64_t tok = a.sorted[slot] / a.k;
-                const float sa = static_cast<const float*>(a.act_s)[tok];
-                const float* sw = static_cast<const float*>(a.w_s) + (int64_t)e * 2 * a.I;
+        // stage 1 epilogue: dequantisation and SwiGLU
+        if (rvalid && cvalid) {
+            float h[4];
+            const int64_t tok = a.sorted[slot] / a.k;
+            const float sa = static_cast<const float*>(a.act_s)[tok];
+            const float* sw = static_cast<const float*>(a.w_s) + (int64_t)e * 2 * a.I;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float g = __fmul_rn(__fmul_rn((float)acc[0][r][c], sa), sw[col + c]);
+                const float u = __fmul_rn(__fmul_rn((float)acc[1][r][c], sa), sw[a.I + col + c]);
+                h[c] = silu_mul(g, u);
+            }
+            if (a.dbg_acc) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const float g = __fmul_rn(__fmul_rn((float)acc[0][r][c], sa), sw[col + c]);
-                    const float u = __fmul_rn(__fmul_rn((float)acc[1][r][c], sa), sw[a.I + col + c]);
-                    h[c] = silu_mul(g, u);
-                }
-                if (a.dbg_acc) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        a.dbg_acc[(int64_t)slot * 2 * a.I + col + c] = (int32_t)acc[0][r][c];
-                        a.dbg_acc[(int64_t)slot * 2 * a.I + a.I + col + c] = (int32_t)acc[1][r][c];
-                    }
-                }
-                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (int64_t)slot * a.I + col) =
-                    make_float4(h[0], h[1], h[2], h[3]);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) h[c] = silu_mul((float)acc[0][r][c], (float)acc[1][r][c]);
-            if constexpr (SCHEME == S_W4A16) {
-                if (rvalid && cvalid) {
-                    uint2 o;
-                    o.x = (uint32_t)float_to_bf16_bits(h[0]) | ((uint32_t)float_to_bf16_bits(h[1]) << 16);
-                    o.y = (uint32_t)float_to_bf16_bits(h[2]) | ((uint32_t)float_to_bf16_bits(h[3]) << 16);
-                    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + (int64_t)slot * a.I + col) = o;
-                }
-            } else {
-                // MX quantisation along I: a 32-block is 8 lanes (tx 0..7 or 8..15)
-                float amax = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-                if (rvalid && cvalid) {
-                    uint32_t codes = 0;
-                    uint8_t sb = 127;
-                    if (amax > 0.f) {
-                        const int X = mx_block_exponent(amax);
-                        const float m = exp2i(-X);
-                        sb = (uint8_t)(X + 127);
-                        codes = (uint32_t)e4m3x2_from_float(h[0] * m, h[1] * m) |
-                                ((uint32_t)e4m3x2_from_float(h[2] * m, h[3] * m) << 16);
-                    }
-                    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + (int64_t)slot * a.I + col) = codes;
-                    if ((tx & 7) == 0) static_cast<uint8_t*>(a.out_s)[(int64_t)slot * (a.I / 32) + col / 32] = sb;
+                    a.dbg_acc[(int64_t)slot * 2 * a.I + col + c] = (int32_t)acc[0][r][c];
+                    a.dbg_acc[(int64_t)slot * 2 * a.I + a.I + col + c] = (int32_t)acc[1][r][c];
                 }
             }
+            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (int64_t)slot * a.I + col) =
+                make_float4(h[0], h[1], h[2], h[3]);
         }
     }
 }
 
-template <int SCHEME, int STAGE>
+template <int STAGE>
 int gemm_simt_launch(const SimtArgs& a, cudaStream_t st) {
     const int64_t P = (int64_t)a.T * a.k;
     if (P == 0) return QMOE_OK;
@@ -313,18 +215,12 @@ int gemm_simt_launch(const SimtArgs& a, cudaStream_t st) {
     if (max_tiles > 0x7FFFFFFF) return QMOE_ERR_UNSUPPORTED;
     dim3 grid((unsigned)max_tiles, (unsigned)ceil_div(N, BN));
     if (grid.y > 65535) return QMOE_ERR_UNSUPPORTED;
-    gemm_simt_kernel<SCHEME, STAGE><<<grid, 256, 0, st>>>(a);
+    gemm_simt_kernel<STAGE><<<grid, 256, 0, st>>>(a);
     return launch_status();
 }
 
-int gemm_simt(int scheme, int stage, const SimtArgs& a, cudaStream_t st) {
-    switch (scheme * 2 + (stage - 1)) {
-        case 0: return gemm_simt_launch<S_W4A16, 1>(a, st);
-        case 1: return gemm_simt_launch<S_W4A16, 2>(a, st);
-        case 4: return gemm_simt_launch<S_W8A8, 1>(a, st);
-        case 5: return gemm_simt_launch<S_W8A8, 2>(a, st);
-    }
-    return QMOE_ERR_ARG;
+int gemm_simt_w8a8(int stage, const SimtArgs& a, cudaStream_t st) {
+    return stage == 1 ? gemm_simt_launch<1>(a, st) : gemm_simt_launch<2>(a, st);
 }
 
 }  // namespace qmoe

@@ -41,3 +41,31 @@ __host__ __device__ inline uint32_t scale_offset(int nmax, int r, int block_in_s
 
 }  // namespace mxt
 }  // namespace qmoe
+
+namespace qmoe {
+namespace bft {
+
+// bf16 activation tiles (W4A16): same token tiles as above; per (tile t,
+// K step kt of 64 elements) one block of NMAX rows x 128 bytes, row r at
+// r*128 with its 16-byte chunk c at ((c ^ (r & 7)) * 16).  No scales.
+__host__ __device__ inline int64_t block_bytes(int nmax) { return (int64_t)nmax * 128; }
+__host__ __device__ inline int64_t buffer_bytes(const qmoe_dims* d, int64_t K) {
+    const int nmax = mxt::nmax_for(d);
+    return mxt::max_tiles(d, nmax) * (K / 64) * block_bytes(nmax);
+}
+// byte offset of element `col` (0..63) of row r inside a block
+__host__ __device__ inline uint32_t elem_offset(int r, int col) {
+    const uint32_t b = (uint32_t)col * 2u;
+    return (uint32_t)r * 128u + (((b >> 4) ^ (uint32_t)(r & 7)) << 4) + (b & 15u);
+}
+
+// Pre-packed int4 weights (W4A16): per (128-row tile rt, 64-element K step
+// kt) a 4608-byte block at (rt * ceil(K/64) + kt) * 4608: 128 rows x 32 bytes
+// of codes, then 128 rows x 2 fp16 scales (the two 32-element blocks of the
+// step).  Inside each 32-bit code word the eight nibbles are reordered so the
+// low half holds elements 0, 2, 4, 6 and the high half 1, 3, 5, 7: masking
+// with 0x000F000F after a shift by 4j yields elements (2j, 2j+1) as a pair.
+constexpr int kW4Block = 4608;
+
+}  // namespace bft
+}  // namespace qmoe

@@ -9,6 +9,7 @@
 // lane r, column r / 32, byte kb -- where the MMA reads it.  Rows and blocks
 // beyond the tensor are padded with 127 (scale 1.0).
 #include "qmoe_common.cuh"
+#include "mx_tiles.cuh"
 
 namespace qmoe {
 
@@ -89,5 +90,64 @@ extern "C" int qmoe_prepack_fp4_weights(int64_t rows, int64_t K, const uint8_t* 
     const int64_t total16 = ((rows + 127) / 128) * KT * 512;
     prepack_fp4_kernel<<<(unsigned)((total16 + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
         w_rowmajor, reinterpret_cast<uint4*>(w_packed), rows, K / 2, KT, total16);
+    return launch_status();
+}
+
+// ------------------------------------------------------------------ int4 weights for the bf16 tensor-core path
+namespace qmoe {
+
+// One thread per 32-bit output word of a block (1024 code words + 128 scale words).
+__global__ void prepack_int4_kernel(const uint8_t* __restrict__ w, const uint16_t* __restrict__ s, uint32_t* __restrict__ dst,
+                                    int64_t rows, int64_t K, int64_t KT, int64_t total_words) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total_words) return;
+    const int64_t blk = i / (bft::kW4Block / 4);
+    const int wi = (int)(i % (bft::kW4Block / 4));
+    const int64_t rt = blk / KT, kt = blk - rt * KT;
+    uint32_t out = 0;
+    if (wi < 1024) {
+        const int r = wi >> 3, word = wi & 7;
+        const int64_t row = rt * 128 + r;
+        const int64_t k0 = kt * 64 + word * 8;  // eight elements k0..k0+7
+        if (row < rows && k0 < K) {
+            const uint32_t v = *reinterpret_cast<const uint32_t*>(w + row * (K / 2) + k0 / 2);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const uint32_t nib = (v >> (4 * m)) & 15u;
+                const int pos = (m & 1) ? 4 + (m >> 1) : (m >> 1);
+                out |= nib << (4 * pos);
+            }
+        } else {
+            out = 0x88888888u;  // padding decodes to 0
+        }
+    } else {
+        const int r = wi - 1024;
+        const int64_t row = rt * 128 + r;
+        const int64_t kb = kt * 2;
+        uint32_t s0 = 0, s1 = 0;
+        if (row < rows && kb * 32 < K) s0 = s[row * (K / 32) + kb];
+        if (row < rows && (kb + 1) * 32 < K) s1 = s[row * (K / 32) + kb + 1];
+        out = s0 | (s1 << 16);
+    }
+    dst[i] = out;
+}
+
+}  // namespace qmoe
+
+extern "C" size_t qmoe_int4_weights_packed_bytes(int64_t rows, int64_t K) {
+    if (rows <= 0 || K <= 0 || K % 32 != 0) return 0;
+    return (size_t)(((rows + 127) / 128) * ((K + 63) / 64) * qmoe::bft::kW4Block);
+}
+
+extern "C" int qmoe_prepack_int4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor, const uint16_t* s_fp16,
+                                         uint8_t* packed, qmoe_stream_t stream) {
+    using namespace qmoe;
+    if (rows <= 0 || K <= 0 || K % 32 != 0 || !w_rowmajor || !s_fp16 || !packed || !aligned16(packed) ||
+        (reinterpret_cast<uintptr_t>(w_rowmajor) & 3u))
+        return QMOE_ERR_ARG;
+    const int64_t KT = (K + 63) / 64;
+    const int64_t words = ((rows + 127) / 128) * KT * (bft::kW4Block / 4);
+    prepack_int4_kernel<<<(unsigned)((words + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+        w_rowmajor, s_fp16, reinterpret_cast<uint32_t*>(packed), rows, K, KT, words);
     return launch_status();
 }

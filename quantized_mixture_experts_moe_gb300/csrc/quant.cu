@@ -182,6 +182,50 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
     return launch_status();
 }
 
+// Permute bf16 activations into the bf16 tile layout (W4A16 stage-1 input):
+// one warp per expert-sorted slot, 16-byte chunks (8 elements) per lane.
+__global__ void __launch_bounds__(kPqWarps * 32)
+permute_bf16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
+                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k, int H,
+                    int nmax, int64_t P, uint8_t* __restrict__ tiles) {
+    const int lane = threadIdx.x & 31;
+    const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
+    int tile = -1, row = 0, tok = 0;
+    if (lane == 0 && slot < P && slot < offsets[E]) {
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (offsets[mid] <= slot) lo = mid; else hi = mid;
+        }
+        const int local = (int)(slot - offsets[lo]);
+        tile = tile_start[lo] + local / nmax;
+        row = local % nmax;
+        tok = sorted_pair_ids[slot] / k;
+    }
+    tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
+    if (tile < 0) return;
+    row = __shfl_sync(0xFFFFFFFFu, row, 0);
+    tok = __shfl_sync(0xFFFFFFFFu, tok, 0);
+    const uint16_t* xr = x + (int64_t)tok * H;
+    const int64_t bb = bft::block_bytes(nmax);
+    uint8_t* tbase = tiles + (int64_t)tile * (H / 64) * bb;
+    for (int j = lane; j < H / 8; j += 32) {  // 8-element chunk j: K step j/8, chunk j%8 of the 128-byte row
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + 8 * j);
+        uint8_t* blk = tbase + (int64_t)(j >> 3) * bb;
+        *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) = v;
+    }
+}
+
+int permute_bf16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
+                        const int32_t* tile_start, uint8_t* tiles, cudaStream_t st) {
+    const int64_t P = (int64_t)d->T * d->k;
+    if (P == 0) return QMOE_OK;
+    const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
+    permute_bf16_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, sorted, offsets, tile_start, d->E, d->k, d->H,
+                                                                   mxt::nmax_for(d), P, tiles);
+    return launch_status();
+}
+
 int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st) {
     const int64_t n8 = rows * cols / 8;
     if (n8 == 0) return QMOE_OK;

@@ -47,10 +47,14 @@ def align(ids: np.ndarray, E: int, T: int, k: int, H=32, I=32):
 
 
 def device_weights(w, inp):
-    """Weights as the library takes them (MXFP4 scales pre-packed)."""
+    """Weights as the library takes them (MXFP4 weights and scales pre-packed;
+    W4A16 codes pre-packed with their scales, scale slots then unused)."""
     t = {key: dev(inp[key]) for key in ("w1", "w1_s", "w2", "w2_s")}
     if w.scheme == "mxfp4":
         t["w1"], t["w1_s"], t["w2"], t["w2_s"] = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], w.H, w.I)
+    elif w.scheme == "w4a16":
+        t["w1"], t["w2"] = qb.prepack_w4a16(t["w1"], t["w1_s"], t["w2"], t["w2_s"], w.H, w.I)
+        t["w1_s"] = t["w2_s"] = None
     return t
 
 
@@ -69,10 +73,13 @@ def run_layer(w, inp, keep=False):
     y = empty((P, H), torch.int16)  # bf16 bits
     res = {}
     if w.scheme == "w4a16":
-        h = empty((P, I), torch.int16)
-        qb.qmoe_gemm1_swiglu_w4a16(d, t["x"], t["w1"], t["w1_s"], offsets, sorted_ids, h, status, ws)
-        qb.qmoe_gemm2_w4a16(d, h, t["w2"], t["w2_s"], offsets, y, status, ws)
-        res["h"] = h
+        xt = empty(qb.bf16_tiles_bytes(d, H), torch.uint8)
+        ht = empty(qb.bf16_tiles_bytes(d, I), torch.uint8)
+        qb.qmoe_permute_bf16(d, t["x"], sorted_ids, offsets, xt, ws)
+        w1, w2 = qb.prepack_w4a16(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
+        qb.qmoe_gemm1_swiglu_w4a16(d, xt, w1, offsets, ht, status, ws)
+        qb.qmoe_gemm2_w4a16(d, ht, w2, offsets, y, status, ws)
+        res.update(bxt=xt, bht=ht)
     elif w.scheme == "mxfp4":
         xt = empty(qb.mx_tiles_bytes(d, H), torch.uint8)
         ht = empty(qb.mx_tiles_bytes(d, I), torch.uint8)
@@ -105,6 +112,10 @@ def run_layer(w, inp, keep=False):
             nmax = tile_nmax(T, k, E)
             r["xq"], r["xs"] = unpack_tiles(r.pop("xt"), r["offsets"], nmax, H)
             r["hq"], r["hs"] = unpack_tiles(r.pop("ht"), r["offsets"], nmax, I)
+        elif w.scheme == "w4a16":
+            nmax = tile_nmax(T, k, E)
+            r["x_perm"] = unpack_bf16_tiles(r.pop("bxt"), r["offsets"], nmax, H)
+            r["h"] = unpack_bf16_tiles(r.pop("bht"), r["offsets"], nmax, I)
     return r
 
 
@@ -160,4 +171,36 @@ def pack_tiles(codes, scales, offsets, nmax, K, nbytes):
     co, so = _layout(nmax, K, t, r)
     buf[co] = codes[:len(slots)]
     buf[so] = scales[:len(slots)]
+    return buf
+
+
+# ------------------------------------------------------------------ bf16 activation tile layout (include/qmoe.h)
+
+def _bf16_layout(nmax, K, t, r):
+    """Byte offsets [rows, K] of each bf16 element (low byte)."""
+    KT = K // 64
+    col = np.arange(K)
+    kt, cin = col // 64, col % 64
+    chunk, byte = (2 * cin) // 16, (2 * cin) % 16
+    base = (t[:, None] * KT + kt[None, :]) * (nmax * 128)
+    return base + r[:, None] * 128 + ((chunk[None, :] ^ (r[:, None] & 7)) << 4) + byte[None, :]
+
+
+def unpack_bf16_tiles(buf, offsets, nmax, K):
+    """bf16 activation tiles -> slot-order bf16 bits [P_valid, K]."""
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    off = _bf16_layout(nmax, K, t, r)
+    return buf[off].astype(np.uint16) | (buf[off + 1].astype(np.uint16) << 8)
+
+
+def pack_bf16_tiles(rows, offsets, nmax, K, nbytes):
+    """Slot-order bf16 bits [P_valid, K] -> a bf16 activation tile buffer of nbytes."""
+    buf = np.zeros(nbytes, np.uint8)
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    off = _bf16_layout(nmax, K, t, r)
+    v = rows[:len(slots)].astype(np.uint16)
+    buf[off] = (v & 0xFF).astype(np.uint8)
+    buf[off + 1] = (v >> 8).astype(np.uint8)
     return buf

@@ -69,11 +69,17 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.qmoe_align_sort(ctypes.byref(d), null, null, null, null, null, null, null, 0, null) == -1
     assert lib.qmoe_combine(ctypes.byref(d), null, null, null, null, null) == -1
     bad = qb.dims(16, 2, 256, 100, 8)
-    assert lib.qmoe_gemm2_w4a16(ctypes.byref(bad), null, null, null, null, null, null, null, 0, null) == -1
+    assert lib.qmoe_gemm2_w4a16(ctypes.byref(bad), null, null, null, null, null, null, 0, null) == -1
     assert lib.qmoe_quant_act_mxfp8(4, 48, null, null, null, null) == -1
     misaligned = ctypes.c_void_p(0x1000 + 4)
     ok = ctypes.c_void_p(0x1000)
-    assert lib.qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), misaligned, ok, ok, ok, ok, ok, ok, null, 0, null) == -1
+    assert lib.qmoe_gemm1_swiglu_w4a16(ctypes.byref(d), misaligned, ok, ok, ok, ok, ok, 0, null) == -1
+    # W4A16 pre-pack and tile helpers: bad K, null pointers, sizes from the stated layout
+    assert lib.qmoe_prepack_int4_weights(128, 100, ok, ok, ok, null) == -1
+    assert lib.qmoe_prepack_int4_weights(128, 128, null, ok, ok, null) == -1
+    assert qb.int4_weights_packed_bytes(300, 4096) == 3 * 64 * 4608
+    assert qb.bf16_tiles_bytes(qb.dims(16, 2, 256, 128, 8), 96) == 0
+    assert lib.qmoe_permute_bf16(ctypes.byref(d), null, ok, ok, ok, ok, 1 << 20, null) == -1
     assert lib.qmoe_moe_forward(7, ctypes.byref(d), *([null] * 10), 0, null) == -1
     # MXFP4 scale pre-pack: bad K, null pointers
     assert lib.qmoe_prepack_mx_scales(128, 100, ok, ok, null) == -1
