@@ -274,8 +274,8 @@ def run_ours(args, w):
         h32 = E_((P, I), torch.float32)
         hq, hs = E_((P, I), torch.int8), E_(P, torch.float32)
     else:
-        xt = E_(qb.bf16_tiles_bytes(dims, H), torch.uint8)
-        ht = E_(qb.bf16_tiles_bytes(dims, I), torch.uint8)
+        xt = E_(qb.w4a16_x_tiles_bytes(dims), torch.uint8)
+        ht = E_(qb.w4a16_h_tiles_bytes(dims), torch.uint8)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
     g1_pairs, g2_pairs = [], []
@@ -287,7 +287,7 @@ def run_ours(args, w):
         elif w.scheme == "w8a8":
             qb.qmoe_quant_rows_int8_bf16(t["x"], xq, xs)
         else:
-            qb.qmoe_permute_bf16(dims, t["x"], sorted_ids, offsets, xt, ws)
+            qb.qmoe_permute_x_f16(dims, t["x"], sorted_ids, offsets, xt, ws)
         a, b, c = (ev(), ev(), ev()) if record else (None, None, None)
         if record:
             a.record(stream)

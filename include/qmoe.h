@@ -177,25 +177,31 @@ int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const i
                              const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                              qmoe_stream_t stream);
 
-/* bf16 activation tiles -- the layout in which the W4A16 GEMMs take their
- * activations (x for stage 1, h for stage 2): the token tiles of the MX
- * layout above (same NMAX and tile_start), per (tile t, K step kt of 64
- * elements) one block of NMAX*128 bytes at ((t * K/64) + kt) * NMAX*128,
- * row r's 64 bf16 values at r*128 with 16-byte chunk c at ((c ^ (r % 8)) * 16).
- * Rows past a tile's token count are unspecified.
- *
- * qmoe_bf16_tiles_bytes -- bytes of such a buffer for dims *d and length K
- * (K a multiple of 64; 0 otherwise). */
-size_t qmoe_bf16_tiles_bytes(const qmoe_dims* d, int64_t K);
+/* W4A16 activation tiles -- the layout in which the W4A16 GEMMs take their
+ * activations: the token tiles of the MX layout above (same NMAX and
+ * tile_start), per (tile t, K step kt of 64 elements) one block of NMAX*128
+ * bytes at ((t * K/64) + kt) * NMAX*128, row r's 64 16-bit values at r*128
+ * with 16-byte chunk c at ((c ^ (r % 8)) * 16); after the blocks a per-row
+ * tail of fp32 values.  Two kinds:
+ *   x tiles (K = H, stage-1 input): fp16 values v * 2^-e_r, where 2^-e_r is
+ *     the power of two that moves the row's largest |v| into [2^14, 2^15)
+ *     (e_r = 0 for a zero row; exact for bf16 inputs); tail: 2^e_r at
+ *     (t*NMAX + r).  qmoe_w4a16_x_tiles_bytes(d) bytes.
+ *   h tiles (K = I, stage-1 output / stage-2 input): bf16 values; tail: the
+ *     largest |h| of each 32-column group at ((t*NMAX + r) * I/32 + g).
+ *     qmoe_w4a16_h_tiles_bytes(d) bytes.
+ * Rows past a tile's token count are unspecified. */
+size_t qmoe_w4a16_x_tiles_bytes(const qmoe_dims* d);
+size_t qmoe_w4a16_h_tiles_bytes(const qmoe_dims* d);
 
-/* qmoe_permute_bf16 -- the expert-sorted permutation of the routed bf16
- * activations, written as bf16 activation tiles with K = H: slot s of expert
- * e gets row sorted_pair_ids[s] / k of x_bf16 [T, H] ([hip-ep] description:
- * one grouped launch over all experts' routed tokens).  H % 64 == 0.
- * ws = the workspace qmoe_align_sort filled for this routing. */
-int qmoe_permute_bf16(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
-                      const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
-                      qmoe_stream_t stream);
+/* qmoe_permute_x_f16 -- the expert-sorted permutation of the routed bf16
+ * activations, written as W4A16 x tiles: slot s of expert e gets row
+ * sorted_pair_ids[s] / k of x_bf16 [T, H] ([hip-ep] description: one grouped
+ * launch over all experts' routed tokens).  H % 64 == 0.  ws = the workspace
+ * qmoe_align_sort filled for this routing. */
+int qmoe_permute_x_f16(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+                       const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
+                       qmoe_stream_t stream);
 
 /* qmoe_quant_rows_int8_{bf16,f32} -- per-row symmetric int8 quantisation,
  * the activation-quantised W8A8 scheme of [gfx1151] Constraint: s = amax/127
@@ -237,12 +243,16 @@ int qmoe_prepack_fp4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor,
  * their fp16 scales [rows, K/32] into the blocks the W4A16 GEMMs read: per
  * (128-row tile rt, 64-element K step kt) one 4608-byte block at
  * (rt * ceil(K/64) + kt) * 4608 holding row r's 32 code bytes at r*32 and
- * then, at 4096 + r*4, its two fp16 scales of the step.  Inside each 32-bit
- * code word (8 elements) the nibbles are reordered so that nibble j holds
- * element 2j and nibble 4+j element 2j+1 (j = 0..3).  Padding codes are 8
- * (value 0), padding scales 0.  K % 32 == 0; packed 16-byte aligned, codes
- * 4-byte aligned.  Output size: qmoe_int4_weights_packed_bytes(rows, K).
- * No counterpart on the pages (a storage-order choice, made at load time). */
+ * then, at 4096 + r*4, its two scales of the step as fp16(s * 2^p_r), where
+ * 2^p_r is the power of two that moves the row's largest |s| into
+ * [2^10, 2^11) (p_r = 0 for an all-zero row).  After all blocks, one fp32
+ * 2^-p_r per row, ceil(rows/128)*128 of them.  Inside each 32-bit code word
+ * (8 elements) the nibbles are reordered so that nibble j holds element 2j
+ * and nibble 4+j element 2j+1 (j = 0..3).  Padding codes are 8 (value 0),
+ * padding scales 0, padding rows' factors 1.  K % 32 == 0; packed 16-byte
+ * aligned, codes 4-byte aligned.  Output size:
+ * qmoe_int4_weights_packed_bytes(rows, K).  No counterpart on the pages (a
+ * storage-order choice, made at load time). */
 size_t qmoe_int4_weights_packed_bytes(int64_t rows, int64_t K);
 int qmoe_prepack_int4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor, const uint16_t* s_fp16,
                               uint8_t* packed, qmoe_stream_t stream);
@@ -257,15 +267,16 @@ int qmoe_prepack_int4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor
  * [aiter] Changes/Test Plan (stage 1 of the grouped a8w4 kernel).
  * Only slots < offsets[E] are written.
  *
- * W4A16 (tensor cores, bf16 MMAs; needs H % 256 == 0, I % 128 == 0,
- *        E <= 512): x_tiles = qmoe_permute_bf16 output (bf16 activation
- *        tiles, K = H); w1 = qmoe_prepack_int4_weights of the int4 [E*2I, H/2]
- *        codes and their fp16 [E*2I, H/32] scales.  Each weight is
- *        dequantised on chip to bf16 as bf16(bf16(s) * (n - 8)) ([gfx1151]
- *        Problem: dequantise to bf16, then a bf16 dot), products summed in
- *        fp32; out h_tiles: h rounded to bf16 (nearest even), stored as bf16
- *        activation tiles with K = I, qmoe_bf16_tiles_bytes(d, I) bytes.
- *        ws = the workspace that qmoe_align_sort filled for this routing. */
+ * W4A16 (tensor cores, fp16 MMAs; needs H % 256 == 0, I % 128 == 0,
+ *        E <= 512): x_tiles = qmoe_permute_x_f16 output (K = H); w1 =
+ *        qmoe_prepack_int4_weights of the int4 [E*2I, H/2] codes and their
+ *        fp16 [E*2I, H/32] scales.  Each weight is dequantised on chip
+ *        ([gfx1151] Problem: dequantise, then a 16-bit dot) to
+ *        fp16((n - 8) * s * 2^p_r), one rounding of relative size <= 2^-11;
+ *        products are summed in fp32 and the sums scaled back by
+ *        2^(e_r - p_r), exactly; out h_tiles: h rounded to bf16 (nearest
+ *        even), stored as W4A16 h tiles.  ws = the workspace that
+ *        qmoe_align_sort filled for this routing. */
 int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const int32_t* offsets,
                             uint8_t* h_tiles, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
@@ -297,10 +308,11 @@ int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x
  * than inter_dim read out of bounds, so the kernels never let a K tile pass
  * the end of I).
  *
- * W4A16: h_tiles from qmoe_gemm1_swiglu_w4a16 (bf16 activation tiles,
- *        K = I); w2 = qmoe_prepack_int4_weights of the int4 [E*H, I/2] codes
- *        and fp16 [E*H, I/32] scales, dequantised as in stage 1; ws as for
- *        stage 1. */
+ * W4A16: h_tiles from qmoe_gemm1_swiglu_w4a16; w2 = qmoe_prepack_int4_weights
+ *        of the int4 [E*H, I/2] codes and fp16 [E*H, I/32] scales,
+ *        dequantised as in stage 1; each h row is scaled into fp16 by the
+ *        power of two its tail's group maxima give (as for x tiles), exactly;
+ *        ws as for stage 1. */
 int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
                      uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 

@@ -49,8 +49,9 @@ SIGNATURES = {
     "qmoe_prepack_mx_scales": ([_i64, _i64, _vp, _vp, _vp], _i32),
     "qmoe_int4_weights_packed_bytes": ([_i64, _i64], _sz),
     "qmoe_prepack_int4_weights": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
-    "qmoe_bf16_tiles_bytes": ([_DP, _i64], _sz),
-    "qmoe_permute_bf16": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_w4a16_x_tiles_bytes": ([_DP], _sz),
+    "qmoe_w4a16_h_tiles_bytes": ([_DP], _sz),
+    "qmoe_permute_x_f16": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_mx_tiles_bytes": ([_DP, _i64], _sz),
     "qmoe_permute_quant_mxfp8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -233,14 +234,18 @@ def prepack_w4a16(w1, w1_s, w2, w2_s, H: int, I: int, stream=None):
     return prepack_int4_weights(w1, w1_s, H, stream), prepack_int4_weights(w2, w2_s, I, stream)
 
 
-def bf16_tiles_bytes(d: Dims, K: int) -> int:
-    return int(lib().qmoe_bf16_tiles_bytes(ctypes.byref(d), K))
+def w4a16_x_tiles_bytes(d: Dims) -> int:
+    return int(lib().qmoe_w4a16_x_tiles_bytes(ctypes.byref(d)))
 
 
-def qmoe_permute_bf16(d, x, sorted_pair_ids, offsets, x_tiles, ws, stream=None):
+def w4a16_h_tiles_bytes(d: Dims) -> int:
+    return int(lib().qmoe_w4a16_h_tiles_bytes(ctypes.byref(d)))
+
+
+def qmoe_permute_x_f16(d, x, sorted_pair_ids, offsets, x_tiles, ws, stream=None):
     wp, wn = _ws(ws)
-    _check(lib().qmoe_permute_bf16(ctypes.byref(d), _ptr(x), _ptr(sorted_pair_ids), _ptr(offsets), _ptr(x_tiles),
-                                   wp, wn, _stream(stream)), "qmoe_permute_bf16")
+    _check(lib().qmoe_permute_x_f16(ctypes.byref(d), _ptr(x), _ptr(sorted_pair_ids), _ptr(offsets), _ptr(x_tiles),
+                                    wp, wn, _stream(stream)), "qmoe_permute_x_f16")
 
 
 def qmoe_gemm1_swiglu_w4a16(d, x_tiles, w1, offsets, h_tiles, status, ws, stream=None):

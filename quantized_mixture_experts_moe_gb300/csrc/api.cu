@@ -23,8 +23,8 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, c
 int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
                             const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
 int32_t* tile_schedule_in(void* ws, const qmoe_dims* d);
-int permute_bf16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
-                        const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
+int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
+                         const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
 bool w4_tc_ok(const qmoe_dims* d);
 int w4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const int32_t* offsets,
                 const int32_t* tile_start, uint8_t* h_tiles, int32_t* status, cudaStream_t st);
@@ -119,20 +119,25 @@ extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, cons
 
 // ------------------------------------------------------------------ W4A16 (bf16 tensor cores)
 
-extern "C" size_t qmoe_bf16_tiles_bytes(const qmoe_dims* d, int64_t K) {
-    if (!dims_ok(d) || K <= 0 || K % 64 != 0) return 0;
-    return (size_t)bft::buffer_bytes(d, K);
+extern "C" size_t qmoe_w4a16_x_tiles_bytes(const qmoe_dims* d) {
+    if (!dims_ok(d) || d->H % 64 != 0) return 0;
+    return (size_t)bft::x_tiles_bytes(d);
 }
 
-extern "C" int qmoe_permute_bf16(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+extern "C" size_t qmoe_w4a16_h_tiles_bytes(const qmoe_dims* d) {
+    if (!dims_ok(d) || d->I % 64 != 0) return 0;
+    return (size_t)bft::h_tiles_bytes(d);
+}
+
+extern "C" int qmoe_permute_x_f16(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
                                  const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                                  qmoe_stream_t stream) {
     int rc = gemm_args_ok(d, {x_bf16, sorted_pair_ids, offsets, x_tiles});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
     if (d->H % 64 != 0) return QMOE_ERR_UNSUPPORTED;
-    return permute_bf16_launch(d, x_bf16, sorted_pair_ids, offsets, tile_schedule_in(const_cast<void*>(ws), d),
-                               x_tiles, (cudaStream_t)stream);
+    return permute_x_f16_launch(d, x_bf16, sorted_pair_ids, offsets, tile_schedule_in(const_cast<void*>(ws), d),
+                                x_tiles, (cudaStream_t)stream);
 }
 
 extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1,
@@ -185,10 +190,10 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
     L.offsets = take(4 * (E + 1));
     L.sorted = take(4 * P);
     L.slot = take(4 * P);
-    L.xq = take(scheme == 0 ? (size_t)bft::buffer_bytes(d, d->H)
+    L.xq = take(scheme == 0 ? (size_t)bft::x_tiles_bytes(d)
                             : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : T * H));
     L.xs = take(scheme == 2 ? 4 * T : 0);
-    L.h = take(scheme == 0 ? (size_t)bft::buffer_bytes(d, d->I)
+    L.h = take(scheme == 0 ? (size_t)bft::h_tiles_bytes(d)
                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
     L.hs = 0;
     L.hq8 = take(scheme == 2 ? P * I : 0);
@@ -230,7 +235,7 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     const int64_t P = (int64_t)d->T * d->k;
     uint16_t* y = (uint16_t*)at(L.y);
     if (scheme == 0) {
-        rc = qmoe_permute_bf16(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
+        rc = qmoe_permute_x_f16(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)
             rc = qmoe_gemm1_swiglu_w4a16(d, (const uint8_t*)at(L.xq), (const uint8_t*)w1, offsets, (uint8_t*)at(L.h),
                                          dev_status, aws, aws_bytes, stream);

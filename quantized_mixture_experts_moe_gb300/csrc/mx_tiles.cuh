@@ -45,13 +45,26 @@ __host__ __device__ inline uint32_t scale_offset(int nmax, int r, int block_in_s
 namespace qmoe {
 namespace bft {
 
-// bf16 activation tiles (W4A16): same token tiles as above; per (tile t,
-// K step kt of 64 elements) one block of NMAX rows x 128 bytes, row r at
-// r*128 with its 16-byte chunk c at ((c ^ (r & 7)) * 16).  No scales.
+// W4A16 activation tiles: the same token tiles as above; per (tile t, K step
+// kt of 64 elements) one block of NMAX rows x 128 bytes at
+// (t * K/64 + kt) * NMAX*128, row r at r*128 with its 16-byte chunk c at
+// ((c ^ (r & 7)) * 16).  After the blocks, a per-row tail:
+//   x tiles (stage-1 input): fp16 values v * 2^-e_r, tail = one fp32 2^e_r
+//     per (tile, row);
+//   h tiles (stage-1 output): bf16 values, tail = K/32 fp32 |max| values per
+//     (tile, row), one per 32-column group.
 __host__ __device__ inline int64_t block_bytes(int nmax) { return (int64_t)nmax * 128; }
-__host__ __device__ inline int64_t buffer_bytes(const qmoe_dims* d, int64_t K) {
+__host__ __device__ inline int64_t blocks_bytes(const qmoe_dims* d, int64_t K) {
     const int nmax = mxt::nmax_for(d);
     return mxt::max_tiles(d, nmax) * (K / 64) * block_bytes(nmax);
+}
+__host__ __device__ inline int64_t x_tiles_bytes(const qmoe_dims* d) {
+    const int nmax = mxt::nmax_for(d);
+    return blocks_bytes(d, d->H) + mxt::max_tiles(d, nmax) * nmax * 4;
+}
+__host__ __device__ inline int64_t h_tiles_bytes(const qmoe_dims* d) {
+    const int nmax = mxt::nmax_for(d);
+    return blocks_bytes(d, d->I) + mxt::max_tiles(d, nmax) * nmax * (int64_t)(d->I / 32) * 4;
 }
 // byte offset of element `col` (0..63) of row r inside a block
 __host__ __device__ inline uint32_t elem_offset(int r, int col) {
@@ -62,10 +75,15 @@ __host__ __device__ inline uint32_t elem_offset(int r, int col) {
 // Pre-packed int4 weights (W4A16): per (128-row tile rt, 64-element K step
 // kt) a 4608-byte block at (rt * ceil(K/64) + kt) * 4608: 128 rows x 32 bytes
 // of codes, then 128 rows x 2 fp16 scales (the two 32-element blocks of the
-// step).  Inside each 32-bit code word the eight nibbles are reordered so the
-// low half holds elements 0, 2, 4, 6 and the high half 1, 3, 5, 7: masking
-// with 0x000F000F after a shift by 4j yields elements (2j, 2j+1) as a pair.
+// step) multiplied by the row's power of two 2^p_r.  Inside each 32-bit code
+// word the eight nibbles are reordered so the low half holds elements 0, 2,
+// 4, 6 and the high half 1, 3, 5, 7: masking with 0x000F000F after a shift
+// by 4j yields elements (2j, 2j+1) as a pair.  After all blocks, one fp32
+// 2^-p_r per row (ceil(rows/128)*128 of them).
 constexpr int kW4Block = 4608;
+__host__ __device__ inline int64_t w4_blocks_bytes(int64_t rows, int64_t K) {
+    return ((rows + 127) / 128) * ((K + 63) / 64) * kW4Block;
+}
 
 }  // namespace bft
 }  // namespace qmoe

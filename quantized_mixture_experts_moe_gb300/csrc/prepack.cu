@@ -93,12 +93,30 @@ extern "C" int qmoe_prepack_fp4_weights(int64_t rows, int64_t K, const uint8_t* 
     return launch_status();
 }
 
-// ------------------------------------------------------------------ int4 weights for the bf16 tensor-core path
+// ------------------------------------------------------------------ int4 weights for the fp16 tensor-core path
 namespace qmoe {
 
+// One thread per (padded) row: the power of two 2^p_r that moves the row's
+// largest scale into [2^10, 2^11), so every product (n - 8) * s * 2^p_r
+// (|n - 8| <= 8) stays below 2^14 in fp16 and small scales keep their
+// precision.  Stores 2^-p_r (1 for an all-zero or padding row).
+__global__ void prepack_int4_rowfac_kernel(const uint16_t* __restrict__ s, float* __restrict__ rowfac, int64_t rows,
+                                           int64_t K, int64_t rows_padded) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows_padded) return;
+    float smax = 0.f;
+    if (r < rows)
+        for (int64_t b = 0; b < K / 32; ++b)
+            smax = fmaxf(smax, fabsf(__half2float(__ushort_as_half(s[r * (K / 32) + b]))));
+    int p = 0;
+    if (smax > 0.f) p = 10 - floor_log2_pos(smax);  // smax is an fp16 value: p in [-5, 34]
+    rowfac[r] = exp2i(-p);
+}
+
 // One thread per 32-bit output word of a block (1024 code words + 128 scale words).
-__global__ void prepack_int4_kernel(const uint8_t* __restrict__ w, const uint16_t* __restrict__ s, uint32_t* __restrict__ dst,
-                                    int64_t rows, int64_t K, int64_t KT, int64_t total_words) {
+__global__ void prepack_int4_kernel(const uint8_t* __restrict__ w, const uint16_t* __restrict__ s,
+                                    const float* __restrict__ rowfac, uint32_t* __restrict__ dst, int64_t rows,
+                                    int64_t K, int64_t KT, int64_t total_words) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= total_words) return;
     const int64_t blk = i / (bft::kW4Block / 4);
@@ -124,9 +142,13 @@ __global__ void prepack_int4_kernel(const uint8_t* __restrict__ w, const uint16_
         const int r = wi - 1024;
         const int64_t row = rt * 128 + r;
         const int64_t kb = kt * 2;
+        const float f = rowfac[row];  // 2^-p_r: dividing by it is exact
         uint32_t s0 = 0, s1 = 0;
-        if (row < rows && kb * 32 < K) s0 = s[row * (K / 32) + kb];
-        if (row < rows && (kb + 1) * 32 < K) s1 = s[row * (K / 32) + kb + 1];
+        if (row < rows && kb * 32 < K)
+            s0 = __half_as_ushort(__float2half_rn(__fdiv_rn(__half2float(__ushort_as_half(s[row * (K / 32) + kb])), f)));
+        if (row < rows && (kb + 1) * 32 < K)
+            s1 = __half_as_ushort(
+                __float2half_rn(__fdiv_rn(__half2float(__ushort_as_half(s[row * (K / 32) + kb + 1])), f)));
         out = s0 | (s1 << 16);
     }
     dst[i] = out;
@@ -136,7 +158,7 @@ __global__ void prepack_int4_kernel(const uint8_t* __restrict__ w, const uint16_
 
 extern "C" size_t qmoe_int4_weights_packed_bytes(int64_t rows, int64_t K) {
     if (rows <= 0 || K <= 0 || K % 32 != 0) return 0;
-    return (size_t)(((rows + 127) / 128) * ((K + 63) / 64) * qmoe::bft::kW4Block);
+    return (size_t)(qmoe::bft::w4_blocks_bytes(rows, K) + ((rows + 127) / 128) * 128 * 4);
 }
 
 extern "C" int qmoe_prepack_int4_weights(int64_t rows, int64_t K, const uint8_t* w_rowmajor, const uint16_t* s_fp16,
@@ -146,8 +168,14 @@ extern "C" int qmoe_prepack_int4_weights(int64_t rows, int64_t K, const uint8_t*
         (reinterpret_cast<uintptr_t>(w_rowmajor) & 3u))
         return QMOE_ERR_ARG;
     const int64_t KT = (K + 63) / 64;
+    const int64_t rows_padded = ((rows + 127) / 128) * 128;
+    float* rowfac = reinterpret_cast<float*>(packed + bft::w4_blocks_bytes(rows, K));
+    prepack_int4_rowfac_kernel<<<(unsigned)((rows_padded + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+        s_fp16, rowfac, rows, K, rows_padded);
+    int rc = launch_status();
+    if (rc != QMOE_OK) return rc;
     const int64_t words = ((rows + 127) / 128) * KT * (bft::kW4Block / 4);
     prepack_int4_kernel<<<(unsigned)((words + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
-        w_rowmajor, s_fp16, reinterpret_cast<uint32_t*>(packed), rows, K, KT, words);
+        w_rowmajor, s_fp16, rowfac, reinterpret_cast<uint32_t*>(packed), rows, K, KT, words);
     return launch_status();
 }

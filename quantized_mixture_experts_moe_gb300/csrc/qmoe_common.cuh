@@ -69,6 +69,16 @@ __device__ __forceinline__ int mx_block_exponent(float amax) {
     return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 
+// Exponent e of the power of two 2^-e that moves a row with largest
+// magnitude amax into [2^14, 2^15), so that every value of the row (a bf16)
+// converts to fp16 exactly unless it is below 2^-24 of the fp16 range; 0 for
+// an all-zero row, clamped to [-112, 113] so that 2^e and 2^-e stay normal.
+__device__ __forceinline__ int f16_row_exponent(float amax) {
+    if (!(amax > 0.f)) return 0;
+    const int e = floor_log2_pos(amax) - 14;
+    return e < -112 ? -112 : (e > 113 ? 113 : e);
+}
+
 // 2^e as fp32 for e in [-127, 127] (exact; 2^-127 is subnormal).
 __device__ __forceinline__ float exp2i(int e) {
     if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);

@@ -182,12 +182,15 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
     return launch_status();
 }
 
-// Permute bf16 activations into the bf16 tile layout (W4A16 stage-1 input):
-// one warp per expert-sorted slot, 16-byte chunks (8 elements) per lane.
+// Permute bf16 activations into W4A16 x tiles: one warp per expert-sorted
+// slot.  The row's largest magnitude picks the power of two 2^-e that moves
+// it into [2^14, 2^15); every element is then written as the fp16 value
+// v * 2^-e (exact for bf16 inputs in range) in 16-byte chunks of 8 elements,
+// and 2^e goes to the tile's per-row tail for the GEMM epilogue.
 __global__ void __launch_bounds__(kPqWarps * 32)
-permute_bf16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
-                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k, int H,
-                    int nmax, int64_t P, uint8_t* __restrict__ tiles) {
+permute_x_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
+                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k, int H,
+                     int nmax, int64_t P, int64_t tail_off, uint8_t* __restrict__ tiles) {
     const int lane = threadIdx.x & 31;
     const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
     int tile = -1, row = 0, tok = 0;
@@ -207,22 +210,43 @@ permute_bf16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ 
     row = __shfl_sync(0xFFFFFFFFu, row, 0);
     tok = __shfl_sync(0xFFFFFFFFu, tok, 0);
     const uint16_t* xr = x + (int64_t)tok * H;
+    float amax = 0.f;
+    for (int j = lane; j < H / 8; j += 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + 8 * j);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(u[i] << 16)), fabsf(__uint_as_float(u[i] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int e = f16_row_exponent(amax);
+    const float m = exp2i(-e);
     const int64_t bb = bft::block_bytes(nmax);
     uint8_t* tbase = tiles + (int64_t)tile * (H / 64) * bb;
-    for (int j = lane; j < H / 8; j += 32) {  // 8-element chunk j: K step j/8, chunk j%8 of the 128-byte row
+    for (int j = lane; j < H / 8; j += 32) {  // chunk j: K step j/8, chunk j%8 of the 128-byte row
         const uint4 v = *reinterpret_cast<const uint4*>(xr + 8 * j);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 hv = __floats2half2_rn(__uint_as_float(u[i] << 16) * m, __uint_as_float(u[i] & 0xFFFF0000u) * m);
+            o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
         uint8_t* blk = tbase + (int64_t)(j >> 3) * bb;
-        *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    if (lane == 0) reinterpret_cast<float*>(tiles + tail_off)[(int64_t)tile * nmax + row] = exp2i(e);
 }
 
-int permute_bf16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
-                        const int32_t* tile_start, uint8_t* tiles, cudaStream_t st) {
+int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
+                         const int32_t* tile_start, uint8_t* tiles, cudaStream_t st) {
     const int64_t P = (int64_t)d->T * d->k;
     if (P == 0) return QMOE_OK;
     const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
-    permute_bf16_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, sorted, offsets, tile_start, d->E, d->k, d->H,
-                                                                   mxt::nmax_for(d), P, tiles);
+    permute_x_f16_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, sorted, offsets, tile_start, d->E, d->k, d->H,
+                                                                    mxt::nmax_for(d), P, bft::blocks_bytes(d, d->H),
+                                                                    tiles);
     return launch_status();
 }
 

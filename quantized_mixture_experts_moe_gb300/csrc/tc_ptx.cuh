@@ -247,6 +247,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 // bytes, 8-row groups 1024 bytes apart, tile base 1024-byte aligned.
 __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
 
+// Instruction descriptor, kind::f16 with fp16 A/B (format 0) and fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4)            // D format fp32

@@ -73,9 +73,9 @@ def run_layer(w, inp, keep=False):
     y = empty((P, H), torch.int16)  # bf16 bits
     res = {}
     if w.scheme == "w4a16":
-        xt = empty(qb.bf16_tiles_bytes(d, H), torch.uint8)
-        ht = empty(qb.bf16_tiles_bytes(d, I), torch.uint8)
-        qb.qmoe_permute_bf16(d, t["x"], sorted_ids, offsets, xt, ws)
+        xt = empty(qb.w4a16_x_tiles_bytes(d), torch.uint8)
+        ht = empty(qb.w4a16_h_tiles_bytes(d), torch.uint8)
+        qb.qmoe_permute_x_f16(d, t["x"], sorted_ids, offsets, xt, ws)
         w1, w2 = qb.prepack_w4a16(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
         qb.qmoe_gemm1_swiglu_w4a16(d, xt, w1, offsets, ht, status, ws)
         qb.qmoe_gemm2_w4a16(d, ht, w2, offsets, y, status, ws)
@@ -114,8 +114,9 @@ def run_layer(w, inp, keep=False):
             r["hq"], r["hs"] = unpack_tiles(r.pop("ht"), r["offsets"], nmax, I)
         elif w.scheme == "w4a16":
             nmax = tile_nmax(T, k, E)
-            r["x_perm"] = unpack_bf16_tiles(r.pop("bxt"), r["offsets"], nmax, H)
-            r["h"] = unpack_bf16_tiles(r.pop("bht"), r["offsets"], nmax, I)
+            nt = max_tiles(P, E, nmax)
+            r["x_f16"], r["x_fac"] = unpack_w4_x_tiles(r.pop("bxt"), r["offsets"], nmax, H, nt)
+            r["h"], r["h_gmax"] = unpack_w4_h_tiles(r.pop("bht"), r["offsets"], nmax, I, nt)
     return r
 
 
@@ -174,10 +175,14 @@ def pack_tiles(codes, scales, offsets, nmax, K, nbytes):
     return buf
 
 
-# ------------------------------------------------------------------ bf16 activation tile layout (include/qmoe.h)
+# ------------------------------------------------------------------ W4A16 activation tile layout (include/qmoe.h)
 
-def _bf16_layout(nmax, K, t, r):
-    """Byte offsets [rows, K] of each bf16 element (low byte)."""
+def max_tiles(P, E, nmax):
+    return (P + nmax - 1) // nmax + E
+
+
+def _w4_layout(nmax, K, t, r):
+    """Byte offsets [rows, K] of each 16-bit element (low byte)."""
     KT = K // 64
     col = np.arange(K)
     kt, cin = col // 64, col % 64
@@ -186,21 +191,37 @@ def _bf16_layout(nmax, K, t, r):
     return base + r[:, None] * 128 + ((chunk[None, :] ^ (r[:, None] & 7)) << 4) + byte[None, :]
 
 
-def unpack_bf16_tiles(buf, offsets, nmax, K):
-    """bf16 activation tiles -> slot-order bf16 bits [P_valid, K]."""
-    slots = np.arange(offsets[-1])
-    t, r = _tile_index(offsets, nmax, slots)
-    off = _bf16_layout(nmax, K, t, r)
+def _gather16(buf, off):
     return buf[off].astype(np.uint16) | (buf[off + 1].astype(np.uint16) << 8)
 
 
-def pack_bf16_tiles(rows, offsets, nmax, K, nbytes):
-    """Slot-order bf16 bits [P_valid, K] -> a bf16 activation tile buffer of nbytes."""
+def unpack_w4_x_tiles(buf, offsets, nmax, H, ntiles):
+    """W4A16 x tiles -> slot-order fp16 bits [P_valid, H] and per-row factors 2^e [P_valid]."""
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    tail = buf[ntiles * (H // 64) * nmax * 128:].view(np.float32)
+    return _gather16(buf, _w4_layout(nmax, H, t, r)), tail[t * nmax + r]
+
+
+def unpack_w4_h_tiles(buf, offsets, nmax, I, ntiles):
+    """W4A16 h tiles -> slot-order bf16 bits [P_valid, I] and group maxima [P_valid, I/32]."""
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    tail = buf[ntiles * (I // 64) * nmax * 128:].view(np.float32)
+    g = np.arange(I // 32)
+    return _gather16(buf, _w4_layout(nmax, I, t, r)), tail[(t * nmax + r)[:, None] * (I // 32) + g[None, :]]
+
+
+def pack_w4_h_tiles(rows, offsets, nmax, I, nbytes, ntiles):
+    """Slot-order bf16 bits [P_valid, I] -> W4A16 h tiles of nbytes (blocks + group-maxima tail)."""
     buf = np.zeros(nbytes, np.uint8)
     slots = np.arange(offsets[-1])
     t, r = _tile_index(offsets, nmax, slots)
-    off = _bf16_layout(nmax, K, t, r)
+    off = _w4_layout(nmax, I, t, r)
     v = rows[:len(slots)].astype(np.uint16)
     buf[off] = (v & 0xFF).astype(np.uint8)
     buf[off + 1] = (v >> 8).astype(np.uint8)
+    mag = ((v.astype(np.uint32) & 0x7FFF) << 16).view(np.float32).reshape(len(slots), I // 32, 32).max(axis=2)
+    tail = buf[ntiles * (I // 64) * nmax * 128:].view(np.float32)
+    tail[(t * nmax + r)[:, None] * (I // 32) + np.arange(I // 32)[None, :]] = mag
     return buf

@@ -77,9 +77,12 @@ def test_host_checks_reject_before_launch(lib):
     # W4A16 pre-pack and tile helpers: bad K, null pointers, sizes from the stated layout
     assert lib.qmoe_prepack_int4_weights(128, 100, ok, ok, ok, null) == -1
     assert lib.qmoe_prepack_int4_weights(128, 128, null, ok, ok, null) == -1
-    assert qb.int4_weights_packed_bytes(300, 4096) == 3 * 64 * 4608
-    assert qb.bf16_tiles_bytes(qb.dims(16, 2, 256, 128, 8), 96) == 0
-    assert lib.qmoe_permute_bf16(ctypes.byref(d), null, ok, ok, ok, ok, 1 << 20, null) == -1
+    assert qb.int4_weights_packed_bytes(300, 4096) == 3 * 64 * 4608 + 3 * 128 * 4
+    # x tiles: max_tiles = ceil(32/112) + 8 = 9 tiles, 4 K steps of 112 rows x 128 bytes, one factor per row
+    assert qb.w4a16_x_tiles_bytes(d) == 9 * 4 * 112 * 128 + 9 * 112 * 4
+    assert qb.w4a16_h_tiles_bytes(d) == 9 * 2 * 112 * 128 + 9 * 112 * 4 * 4
+    assert qb.w4a16_h_tiles_bytes(qb.dims(16, 2, 256, 96, 8)) == 0
+    assert lib.qmoe_permute_x_f16(ctypes.byref(d), null, ok, ok, ok, ok, 1 << 20, null) == -1
     assert lib.qmoe_moe_forward(7, ctypes.byref(d), *([null] * 10), 0, null) == -1
     # MXFP4 scale pre-pack: bad K, null pointers
     assert lib.qmoe_prepack_mx_scales(128, 100, ok, ok, null) == -1
