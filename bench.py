@@ -420,7 +420,7 @@ def run_ours(args, w):
     if rank == 0:
         line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                     ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype=dict(
-                        mxfp4="e4m3 x e2m1 (fp32 accumulate)", w4a16="bf16 (fp32 accumulate)",
+                        mxfp4="e4m3 x e2m1 (fp32 accumulate)", w4a16="f16 x f16 (int4 dequantised on chip; fp32 accumulate)",
                         w8a8="int8 (int32 accumulate)")[w.scheme], data="synthetic",
                     config=dict(workload=w.name, scheme=w.scheme, T=T, H=H, E=E, k=k, I=I,
                                 experts_touched=alg["experts_touched"],

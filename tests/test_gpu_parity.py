@@ -434,7 +434,9 @@ def test_int4_prepack_layout():
     assert np.array_equal(fac[:rows].astype(np.float64), np.exp2(-p)) and np.all(fac[rows:] == 1)
     assert fac[9] == 2.0**-34 and fac[7] == 1
     scaled = np.zeros((RT * 128, KT * 2), np.float64)
-    scaled[:rows, :K // 32] = sv * np.exp2(p)[:, None]  # exact: fp16 values times powers of two
+    # fp16 values times powers of two, rounded back to fp16 (only scales far below their row's largest, which
+    # become fp16 subnormals, round)
+    scaled[:rows, :K // 32] = (sv * np.exp2(p)[:, None]).astype(np.float16).astype(np.float64)
     words = got[:RT * KT * 4608].view(np.uint32)
     for rt in range(RT):
         for kt in range(KT):
