@@ -405,28 +405,46 @@ __global__ void __launch_bounds__(THREADS, 1) w4_gemm_kernel(const Args a) {
             if (STAGE == 1)
                 hblk = a.h_tiles + ((int64_t)t * (a.I / KSTEP) + nb * 2 + (nl >> 6)) * bft::block_bytes(NMAX);
             const int* uexp = sExp + eb * NMAX;
+            // 16 tokens per chunk, computed independently (no per-token branch, so the
+            // chains overlap), then stored under the uniform predicate c < ntok
             for (int c0 = 0; c0 < ntok; c0 += 16) {
                 uint32_t g[16], g2[16];
                 tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + c0, g);
                 tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + NMAX + c0, g2);
+                // the chunk's 16 per-token factors 2^e, one per lane, broadcast below
+                float fl = 0.f;
+                if (lane < 16 && c0 + lane < ntok)
+                    fl = (STAGE == 1) ? a.act_tail[(int64_t)t * NMAX + c0 + lane] : exp2i(uexp[c0 + lane]);
                 tc::tmem_ld_wait();
+                const int nv = min(16, ntok - c0);
+                if (STAGE == 1) {
+                    uint32_t hb[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = c0 + j;
-                    if (c >= ntok) break;
-                    if (STAGE == 1) {
-                        const float fx = a.act_tail[(int64_t)t * NMAX + c];  // 2^e of token row c
+                    for (int j = 0; j < 16; ++j) {
+                        const float fx = __shfl_sync(0xFFFFFFFFu, fl, j);
                         const float gv = __uint_as_float(g[j]) * (fx * f0);
                         const float uv = __uint_as_float(g2[j]) * (fx * f1);
-                        const uint16_t hb = float_to_bf16_bits(silu_mul(gv, uv));
-                        *reinterpret_cast<uint16_t*>(hblk + bft::elem_offset(c, nl & 63)) = hb;
-                        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb & 0x7FFFu) << 16);
-                        if (lane == j) a.h_tail[((int64_t)t * NMAX + c) * NG + nb * 4 + q] = __uint_as_float(mx);
-                    } else {
-                        const float fe = exp2i(uexp[c]);
-                        uint16_t* yr = a.y + (int64_t)(m0 + c) * a.H + 2 * nb * 128 + nl;
-                        yr[0] = float_to_bf16_bits(__uint_as_float(g[j]) * (fe * f0));
-                        yr[128] = float_to_bf16_bits(__uint_as_float(g2[j]) * (fe * f1));
+                        hb[j] = float_to_bf16_bits(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
+                    }
+                    float tmax = 0.f;  // lane j < nv: |max| over this warp's 32 columns of token c0 + j
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (j < nv) *reinterpret_cast<uint16_t*>(hblk + bft::elem_offset(c0 + j, nl & 63)) = (uint16_t)hb[j];
+                        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, (hb[j] & 0x7FFFu) << 16);
+                        if (lane == j) tmax = __uint_as_float(mx);
+                    }
+                    if (lane < nv) a.h_tail[((int64_t)t * NMAX + c0 + lane) * NG + nb * 4 + q] = tmax;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float fx = __shfl_sync(0xFFFFFFFFu, fl, j);
+                        const uint16_t v0 = float_to_bf16_bits(__uint_as_float(g[j]) * (fx * f0));
+                        const uint16_t v1 = float_to_bf16_bits(__uint_as_float(g2[j]) * (fx * f1));
+                        if (j < nv) {
+                            uint16_t* yr = a.y + (int64_t)(m0 + c0 + j) * a.H + 2 * nb * 128 + nl;
+                            yr[0] = v0;
+                            yr[128] = v1;
+                        }
                     }
                 }
             }
