@@ -31,6 +31,10 @@ from quantized_mixture_experts_moe_gb300 import inputs as gen  # noqa: E402
 
 METRIC = "grouped-MoE prefill TFLOP/s & tokens/s at T=4096; % of tensor/HBM roofline"
 UNIT = "TFLOP/s"
+# ncu DRAM bytes (read + write) of one stage-1 GEMM launch divided by its
+# algorithmic bytes, per scheme, for the kernel as it stands; None once the
+# kernel changes after the capture
+TRAFFIC_RATIO_GEMM1 = {"mxfp4": (309.222144 + 6.509056) / 292.782080}
 
 
 def parse():
@@ -356,16 +360,20 @@ def run_ours(args, w):
     fp8_peak = 2.0 * pk["bf16"]
     tensor_peak = fp8_peak if w.scheme == "mxfp4" else pk["bf16"]
     t_tc = alg["gemm1_flops"] / (tensor_peak * 1e12)
+    # DRAM bytes per stage-1 launch from one ncu capture, scaled by units processed
+    # (profiles/mx_gemm_kernel_prof_mxfp4_E64_T512.md): traffic / algorithmic bytes
+    ratio = TRAFFIC_RATIO_GEMM1.get(w.scheme)
+    traffic = ratio * alg["gemm1_bytes"] if ratio else None
     if t_hbm >= t_tc:
         achieved = alg["gemm1_bytes"] / (g1_ms * 1e-3) / 1e9
         roof = dict(kernel="gemm1_swiglu", bound="hbm", achieved=achieved, peak=pk["hbm"], unit="GB/s",
-                    frac=achieved / pk["hbm"], traffic=None,
+                    frac=achieved / pk["hbm"], traffic=traffic,
                     peak_source=f"{pk['source']} (hbm_gbs, copy)")
     else:
         achieved = alg["gemm1_flops"] / (g1_ms * 1e-3) / 1e12
         src = "measured bf16 x2 (nominal fp8:bf16 ratio)" if w.scheme == "mxfp4" else "measured bf16"
         roof = dict(kernel="gemm1_swiglu", bound="tensor", achieved=achieved, peak=tensor_peak, unit="TFLOP/s",
-                    frac=achieved / tensor_peak, traffic=None, peak_source=f"{pk['source']} {src}")
+                    frac=achieved / tensor_peak, traffic=traffic, peak_source=f"{pk['source']} {src}")
     roof["gemm1_ms"] = g1_ms
     roof["gemm2_ms"] = g2_ms
     roof["gemm1_alg_bytes"] = alg["gemm1_bytes"]
