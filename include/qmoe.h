@@ -212,6 +212,33 @@ int qmoe_quant_rows_int8_bf16(int64_t rows, int64_t cols, const uint16_t* x, int
 int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t* q, float* s,
                              qmoe_stream_t stream);
 
+/* W8A8 activation tiles -- the layout in which the W8A8 GEMMs take their
+ * activations: the blocks of the W4A16 tiles above (same NMAX, tile_start,
+ * 128-byte rows of 64 fp16 values, chunk swizzle), each value the fp16 equal
+ * to an int8 code (exact), then a per-row tail of one fp32 scale s at
+ * (t*NMAX + r).  Rows past a tile's token count are unspecified.
+ * qmoe_w8a8_tiles_bytes -- bytes of such a buffer for dims *d and length K
+ * (K % 64 == 0; 0 otherwise). */
+size_t qmoe_w8a8_tiles_bytes(const qmoe_dims* d, int64_t K);
+
+/* qmoe_permute_quant_int8 -- the expert-sorted permutation of the routed
+ * activations and their per-token int8 quantisation (the rule of
+ * qmoe_quant_rows_int8_bf16 applied to each token row of x_bf16 [T, H]) in
+ * one pass: slot s gets the codes of token sorted_pair_ids[s] / k and its
+ * scale, written as W8A8 tiles with K = H ([gfx1151] Constraint: W8A8 needs
+ * quantised activations).  H % 64 == 0.  ws = the workspace qmoe_align_sort
+ * filled for this routing. */
+int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+                            const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
+                            qmoe_stream_t stream);
+
+/* qmoe_quant_tiles_int8_f32 -- the W8A8 intermediate quantisation: each slot
+ * row of h_f32 [P, I] (slot order, from qmoe_gemm1_swiglu_w8a8) quantised
+ * with the rule of qmoe_quant_rows_int8_f32 and written as W8A8 tiles with
+ * K = I.  I % 64 == 0.  ws as above. */
+int qmoe_quant_tiles_int8_f32(const qmoe_dims* d, const float* h_f32, const int32_t* offsets, uint8_t* h_tiles,
+                              const void* ws, size_t ws_bytes, qmoe_stream_t stream);
+
 /* ---------------------------------------------------------------- weight preparation
  *
  * qmoe_prepack_mx_scales -- one-time rearrangement of E8M0 weight scales
@@ -292,14 +319,19 @@ int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tiles, const ui
                             const int32_t* offsets, uint8_t* h_tiles, int32_t* dev_status, void* ws,
                             size_t ws_bytes, qmoe_stream_t stream);
 
-/* W8A8: x_q int8 [T, H] + x_s fp32 [T] (from qmoe_quant_rows_int8_bf16);
- *        w1 int8 [E, 2I, H]; w1_s fp32 [E, 2I].  Accumulation is exact int32;
- *        g = ((float)acc * x_s[t]) * w1_s[e][n] in fp32, likewise u;
- *        out h fp32 [P, I]; dbg_acc (nullable) int32 [P, 2I] receives the raw
- *        gate/up accumulators. */
-int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x_s, const int8_t* w1,
-                           const float* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids, float* h,
-                           int32_t* dbg_acc, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
+/* W8A8 (tensor cores; needs H % 256 == 0, I % 128 == 0, H and I <= 16384,
+ *        E <= 512): x_tiles = qmoe_permute_quant_int8 output (K = H);
+ *        w1 int8 [E, 2I, H] (row-major, as given; 16-byte aligned);
+ *        w1_s fp32 [E, 2I].  The int8 x int8 products are summed exactly in
+ *        int32 ([gfx1151] Constraint): the tensor cores take the codes as
+ *        exact fp16 values, accumulate at most 1024 products in fp32 (exact
+ *        integers below 2^24) and the epilogue carries the sum on in
+ *        integers.  g = ((float)acc * s_x) * w1_s[e][n] in fp32, likewise u;
+ *        out h fp32 [P, I] in slot order; dbg_acc (nullable, 16-byte
+ *        aligned) int32 [P, 2I] receives the exact gate/up sums. */
+int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, const float* w1_s,
+                           const int32_t* offsets, float* h, int32_t* dbg_acc, int32_t* dev_status, void* ws,
+                           size_t ws_bytes, qmoe_stream_t stream);
 
 /* ---------------------------------------------------------------- stage 2: down projection
  *
@@ -323,10 +355,11 @@ int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* 
                      const int32_t* offsets, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes,
                      qmoe_stream_t stream);
 
-/* W8A8: h_q int8 [P, I] + h_s fp32 [P] (qmoe_quant_rows_int8_f32 of h);
- *        w2 int8 [E, H, I]; w2_s fp32 [E, H]; y = ((float)acc * h_s[s]) * w2_s[e][c];
- *        dbg_acc (nullable) int32 [P, H]. */
-int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2, const float* w2_s,
+/* W8A8: h_tiles = qmoe_quant_tiles_int8_f32 output (K = I); w2 int8
+ *        [E, H, I]; w2_s fp32 [E, H]; y = ((float)acc * s_h) * w2_s[e][c]
+ *        with acc the exact int32 sum (as for stage 1); dbg_acc (nullable,
+ *        16-byte aligned) int32 [P, H].  ws as for stage 1. */
+int qmoe_gemm2_w8a8(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
                     const int32_t* offsets, uint16_t* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
                     size_t ws_bytes, qmoe_stream_t stream);
 

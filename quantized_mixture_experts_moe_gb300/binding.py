@@ -56,10 +56,13 @@ SIGNATURES = {
     "qmoe_mx_tiles_bytes": ([_DP, _i64], _sz),
     "qmoe_permute_quant_mxfp8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm1_swiglu_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_w8a8_tiles_bytes": ([_DP, _i64], _sz),
+    "qmoe_permute_quant_int8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_quant_tiles_int8_f32": ([_DP, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_combine": ([_DP, _vp, _vp, _vp, _vp, _vp], _i32),
     "qmoe_forward_workspace_bytes": ([_DP, _i32], _sz),
     "qmoe_moe_forward": ([_i32, _DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -166,12 +169,6 @@ def _ws(ws):
     return _ptr(ws), (0 if ws is None else ws.numel() * ws.element_size())
 
 
-def _status(st, device=None):
-    if st is None:
-        st = torch.zeros(1, dtype=torch.int32, device=device or "cuda")
-    return st
-
-
 def mx_scales_packed_bytes(rows: int, K: int) -> int:
     return int(lib().qmoe_mx_scales_packed_bytes(rows, K))
 
@@ -271,13 +268,26 @@ def qmoe_gemm1_swiglu_mxfp4(d, x_tiles, w1, w1_s, offsets, h_tiles, status, ws, 
            "qmoe_gemm1_swiglu_mxfp4")
 
 
-def qmoe_gemm1_swiglu_w8a8(d, x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h, dbg_acc=None, status=None, ws=None,
-                           stream=None):
+def w8a8_tiles_bytes(d: Dims, K: int) -> int:
+    return int(lib().qmoe_w8a8_tiles_bytes(ctypes.byref(d), K))
+
+
+def qmoe_permute_quant_int8(d, x, sorted_pair_ids, offsets, x_tiles, ws, stream=None):
     wp, wn = _ws(ws)
-    status = _status(status, x_q.device)
-    _check(lib().qmoe_gemm1_swiglu_w8a8(ctypes.byref(d), _ptr(x_q), _ptr(x_s), _ptr(w1), _ptr(w1_s), _ptr(offsets),
-                                        _ptr(sorted_pair_ids), _ptr(h), _ptr(dbg_acc), _ptr(status), wp, wn,
-                                        _stream(stream)),
+    _check(lib().qmoe_permute_quant_int8(ctypes.byref(d), _ptr(x), _ptr(sorted_pair_ids), _ptr(offsets),
+                                         _ptr(x_tiles), wp, wn, _stream(stream)), "qmoe_permute_quant_int8")
+
+
+def qmoe_quant_tiles_int8_f32(d, h, offsets, h_tiles, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_quant_tiles_int8_f32(ctypes.byref(d), _ptr(h), _ptr(offsets), _ptr(h_tiles), wp, wn,
+                                           _stream(stream)), "qmoe_quant_tiles_int8_f32")
+
+
+def qmoe_gemm1_swiglu_w8a8(d, x_tiles, w1, w1_s, offsets, h, dbg_acc, status, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_w8a8(ctypes.byref(d), _ptr(x_tiles), _ptr(w1), _ptr(w1_s), _ptr(offsets), _ptr(h),
+                                        _ptr(dbg_acc), _ptr(status), wp, wn, _stream(stream)),
            "qmoe_gemm1_swiglu_w8a8")
 
 
@@ -293,10 +303,9 @@ def qmoe_gemm2_mxfp4(d, h_tiles, w2, w2_s, offsets, y, status, ws, stream=None):
                                   _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_mxfp4")
 
 
-def qmoe_gemm2_w8a8(d, h_q, h_s, w2, w2_s, offsets, y, dbg_acc=None, status=None, ws=None, stream=None):
+def qmoe_gemm2_w8a8(d, h_tiles, w2, w2_s, offsets, y, dbg_acc, status, ws, stream=None):
     wp, wn = _ws(ws)
-    status = _status(status, h_q.device)
-    _check(lib().qmoe_gemm2_w8a8(ctypes.byref(d), _ptr(h_q), _ptr(h_s), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
+    _check(lib().qmoe_gemm2_w8a8(ctypes.byref(d), _ptr(h_tiles), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
                                  _ptr(dbg_acc), _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_w8a8")
 
 

@@ -1,7 +1,6 @@
 // C-ABI entry points of the grouped expert GEMMs, status strings and the
 // whole-layer call.  Argument checks run on the host before any launch.
 #include "qmoe_common.cuh"
-#include "gemm_simt.cuh"
 #include "mx_tiles.cuh"
 
 namespace qmoe {
@@ -30,6 +29,16 @@ int w4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
                 const int32_t* tile_start, uint8_t* h_tiles, int32_t* status, cudaStream_t st);
 int w4_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
                 const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st);
+bool i8_tc_ok(const qmoe_dims* d);
+int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, const float* w1_s,
+                const int32_t* offsets, const int32_t* tile_start, float* h, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st);
+int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
+                const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st);
+int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool from_bf16_tokens,
+                            const int32_t* sorted, const int32_t* offsets, const int32_t* tile_start, uint8_t* tiles,
+                            cudaStream_t st);
 
 static int gemm_args_ok(const qmoe_dims* d, std::initializer_list<const void*> ptrs) {
     if (!dims_ok(d)) return QMOE_ERR_ARG;
@@ -37,12 +46,6 @@ static int gemm_args_ok(const qmoe_dims* d, std::initializer_list<const void*> p
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return QMOE_ERR_ARG;
     return QMOE_OK;
-}
-
-static SimtArgs make_args(const qmoe_dims* d) {
-    SimtArgs a{};
-    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
-    return a;
 }
 
 }  // namespace qmoe
@@ -91,20 +94,6 @@ extern "C" int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tile
     if (!mx_tc_ok(d, w1, nullptr)) return QMOE_ERR_UNSUPPORTED;
     return mx_tc_gemm1(d, x_tiles, w1, w1_s, offsets, tile_schedule_in(ws, d), h_tiles, dev_status,
                        (cudaStream_t)stream);
-}
-
-extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const int8_t* x_q, const float* x_s, const int8_t* w1,
-                                      const float* w1_s, const int32_t* offsets, const int32_t* sorted_pair_ids,
-                                      float* h, int32_t* dbg_acc, int32_t* dev_status, void* ws, size_t ws_bytes,
-                                      qmoe_stream_t stream) {
-    (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {x_q, x_s, w1, w1_s, offsets, sorted_pair_ids, h, dev_status});
-    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
-    if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
-    SimtArgs a = make_args(d);
-    a.act = x_q; a.act_s = x_s; a.w = w1; a.w_s = w1_s; a.offsets = offsets; a.sorted = sorted_pair_ids;
-    a.out = h; a.dbg_acc = dbg_acc;
-    return gemm_simt_w8a8(1, a, (cudaStream_t)stream);
 }
 
 extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
@@ -159,16 +148,57 @@ extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h_tiles, cons
     return w4_tc_gemm2(d, h_tiles, w2, offsets, tile_schedule_in(ws, d), y, dev_status, (cudaStream_t)stream);
 }
 
-extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const float* h_s, const int8_t* w2,
-                               const float* w2_s, const int32_t* offsets, uint16_t* y, int32_t* dbg_acc,
-                               int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
-    (void)ws; (void)ws_bytes;
-    int rc = gemm_args_ok(d, {h_q, h_s, w2, w2_s, offsets, y, dev_status});
+// ------------------------------------------------------------------ W8A8 (exact int32 sums on fp16 tensor cores)
+
+extern "C" size_t qmoe_w8a8_tiles_bytes(const qmoe_dims* d, int64_t K) {
+    if (!dims_ok(d) || K <= 0 || K % 64 != 0) return 0;
+    const int nmax = mxt::nmax_for(d);
+    return (size_t)(bft::blocks_bytes(d, K) + mxt::max_tiles(d, nmax) * nmax * 4);
+}
+
+extern "C" int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+                                       const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
+                                       qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_bf16, sorted_pair_ids, offsets, x_tiles});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (d->H % 64 != 0) return QMOE_ERR_UNSUPPORTED;
+    return quant_tiles_int8_launch(d, d->H, x_bf16, true, sorted_pair_ids, offsets,
+                                   tile_schedule_in(const_cast<void*>(ws), d), x_tiles, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_quant_tiles_int8_f32(const qmoe_dims* d, const float* h_f32, const int32_t* offsets,
+                                         uint8_t* h_tiles, const void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {h_f32, offsets, h_tiles});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (d->I % 64 != 0) return QMOE_ERR_UNSUPPORTED;
+    return quant_tiles_int8_launch(d, d->I, h_f32, false, nullptr, offsets,
+                                   tile_schedule_in(const_cast<void*>(ws), d), h_tiles, (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, const float* w1_s,
+                                      const int32_t* offsets, float* h, int32_t* dbg_acc, int32_t* dev_status,
+                                      void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_tiles, w1, w1_s, offsets, h, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
-    SimtArgs a = make_args(d);
-    a.act = h_q; a.act_s = h_s; a.w = w2; a.w_s = w2_s; a.offsets = offsets; a.out = y; a.dbg_acc = dbg_acc;
-    return gemm_simt_w8a8(2, a, (cudaStream_t)stream);
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!i8_tc_ok(d)) return QMOE_ERR_UNSUPPORTED;
+    return i8_tc_gemm1(d, x_tiles, w1, w1_s, offsets, tile_schedule_in(ws, d), h, dbg_acc, dev_status,
+                       (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
+                               const int32_t* offsets, uint16_t* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
+                               size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {h_tiles, w2, w2_s, offsets, y, dev_status});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!i8_tc_ok(d)) return QMOE_ERR_UNSUPPORTED;
+    return i8_tc_gemm2(d, h_tiles, w2, w2_s, offsets, tile_schedule_in(ws, d), y, dbg_acc, dev_status,
+                       (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------ whole layer
@@ -176,13 +206,13 @@ extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const int8_t* h_q, const floa
 namespace {
 
 struct FwdLayout {
-    size_t counts, offsets, sorted, slot, xq, xs, h, hs, hq8, hs8, y, align_ws, total;
+    size_t counts, offsets, sorted, slot, xq, h, ht, y, align_ws, total;
 };
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
-    const size_t T = d->T, P = (size_t)d->T * d->k, H = d->H, I = d->I, E = d->E;
+    const size_t P = (size_t)d->T * d->k, H = d->H, I = d->I, E = d->E;
     FwdLayout L{};
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
@@ -191,13 +221,10 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
     L.sorted = take(4 * P);
     L.slot = take(4 * P);
     L.xq = take(scheme == 0 ? (size_t)bft::x_tiles_bytes(d)
-                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : T * H));
-    L.xs = take(scheme == 2 ? 4 * T : 0);
+                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : qmoe_w8a8_tiles_bytes(d, d->H)));
     L.h = take(scheme == 0 ? (size_t)bft::h_tiles_bytes(d)
                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
-    L.hs = 0;
-    L.hq8 = take(scheme == 2 ? P * I : 0);
-    L.hs8 = take(scheme == 2 ? 4 * P : 0);
+    L.ht = take(scheme == 2 ? qmoe_w8a8_tiles_bytes(d, d->I) : 0);
     L.y = take(2 * P * H);
     L.align_ws = take(qmoe_workspace_bytes(d));
     L.total = o;
@@ -232,7 +259,6 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     int rc = qmoe_align_sort(d, topk_ids, counts, offsets, sorted, slot, dev_status, aws, aws_bytes, stream);
     if (rc != QMOE_OK) return rc;
     if (d->T == 0) return QMOE_OK;
-    const int64_t P = (int64_t)d->T * d->k;
     uint16_t* y = (uint16_t*)at(L.y);
     if (scheme == 0) {
         rc = qmoe_permute_x_f16(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
@@ -251,17 +277,16 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
             rc = qmoe_gemm2_mxfp4(d, (const uint8_t*)at(L.h), (const uint8_t*)w2, (const uint8_t*)w2_s, offsets, y,
                                   dev_status, aws, aws_bytes, stream);
     } else {
-        rc = qmoe_quant_rows_int8_bf16(d->T, d->H, x_bf16, (int8_t*)at(L.xq), (float*)at(L.xs), stream);
+        rc = qmoe_permute_quant_int8(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm1_swiglu_w8a8(d, (const int8_t*)at(L.xq), (const float*)at(L.xs), (const int8_t*)w1,
-                                        (const float*)w1_s, offsets, sorted, (float*)at(L.h), nullptr, dev_status, aws,
-                                        aws_bytes, stream);
+            rc = qmoe_gemm1_swiglu_w8a8(d, (const uint8_t*)at(L.xq), (const int8_t*)w1, (const float*)w1_s, offsets,
+                                        (float*)at(L.h), nullptr, dev_status, aws, aws_bytes, stream);
         if (rc == QMOE_OK)
-            rc = qmoe_quant_rows_int8_f32(P, d->I, (const float*)at(L.h), (int8_t*)at(L.hq8), (float*)at(L.hs8),
-                                          stream);
+            rc = qmoe_quant_tiles_int8_f32(d, (const float*)at(L.h), offsets, (uint8_t*)at(L.ht), aws, aws_bytes,
+                                           stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm2_w8a8(d, (const int8_t*)at(L.hq8), (const float*)at(L.hs8), (const int8_t*)w2,
-                                 (const float*)w2_s, offsets, y, nullptr, dev_status, aws, aws_bytes, stream);
+            rc = qmoe_gemm2_w8a8(d, (const uint8_t*)at(L.ht), (const int8_t*)w2, (const float*)w2_s, offsets, y,
+                                 nullptr, dev_status, aws, aws_bytes, stream);
     }
     if (rc != QMOE_OK) return rc;
     return qmoe_combine(d, y, topk_w, slot, out_bf16, stream);

@@ -1,0 +1,554 @@
+// Grouped W8A8 expert GEMMs on the 5th-generation tensor cores with exact
+// int32 sums.
+//
+// "Evaluate native IU4/IU8 WMMA for grouped-INT MoE prefill on gfx1151"
+// (Constraint) runs W8A8 as int8 x int8 products summed in int32; "perf(qmoe):
+// group prefill expert matmuls" (description) puts every expert in one launch.
+// sm_103a has no integer tcgen05 MMA in this toolkit, so the products run as
+// kind::f16 MMAs on fp16 operands that hold the int8 values exactly (every
+// integer in [-128, 127] is an fp16), with fp32 accumulation in TMEM.  A
+// product is at most 127^2 = 16129; 1024 of them stay below 2^24, so a fp32
+// sum over at most 1024 K elements is an exact integer.  The accumulator is
+// therefore drained every 1024 K elements: the epilogue splits the exact fp32
+// value v into hi * 2^13 + lo with |lo| <= 4096, adds hi to a 16-bit running
+// sum kept in TMEM and writes lo back as the fp32 accumulator, on which the
+// next 1024 K elements accumulate (|lo| + 1024 * 16129 < 2^24, exact again).
+// At the end acc = hi * 2^13 + v, the exact int32 sum, for K <= 16384
+// (|hi| <= 16384 * 16129 / 2^13 < 2^15).
+//
+//   stage 1: g = ((float)acc_g * s_x) * s_w,  u likewise,  h = silu(g) * u  (fp32)
+//   stage 2: y = ((float)acc * s_h) * s_w                                 (bf16)
+//
+// Structure (one persistent CTA per SM, 20 warps), swap-AB as in the other
+// grouped GEMMs (weights are the MMA's M = 128 rows, tokens its N):
+//   warp 0      weight producer: one TMA box per step brings the raw int8
+//               rows of both weight tiles (stage 1: a gate tile and its up
+//               partner; stage 2: two adjacent W2 row tiles), 64 K elements
+//               each, 64-byte swizzled.
+//   warp 1      activation producer: one bulk copy per step of the step's
+//               fp16 token rows, already 128-byte swizzled by the tile kernel.
+//   warps 2-3   MMA issuers, one per weight tile: A (the weight tile) from
+//               TMEM, B (tokens) from shared memory, N = tokens rounded to 16.
+//   warps 4-11  converters: one thread per weight row; int8 -> fp16 pairs
+//               written straight into TMEM as the A operand, so the converted
+//               weights never pass through shared memory.
+//   warps 12-19 epilogue: two per TMEM lane quadrant, alternate 16-token
+//               column chunks; the 1024-K drains and the final dequantisation.
+#include "qmoe_common.cuh"
+#include "mx_tiles.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace qmoe {
+namespace i8 {
+
+constexpr int WARP_W = 0, WARP_B = 1, WARP_MMA = 2;
+constexpr int WARP_CVT0 = 4, CVT_WARPS = 8;
+constexpr int WARP_EPI0 = 12, EPI_WARPS = 8;
+constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
+constexpr int KSTEP = 64;        // K elements per step
+constexpr int NS = 112;          // tokens per MMA (a schedule tile of 224 is two of these)
+constexpr int CHUNK_STEPS = 16;  // steps between drains: 1024 K elements
+constexpr int HI_SHIFT = 13;
+constexpr int MAX_E = 512;
+constexpr int MAX_K = 16384;
+
+// TMEM columns: fp32 accumulators of the two tiles, the packed 16-bit running
+// high parts (tile 0 in the low half of a column, tile 1 in the high half),
+// and a two-slot ring of A operands (a 128 x 64 fp16 tile = 32 columns).
+constexpr uint32_t R_COL = 0;
+constexpr uint32_t S_COL = 2 * NS;
+constexpr uint32_t A_COL = 384;
+constexpr int AS = 2;
+static_assert(S_COL + NS <= A_COL && A_COL + AS * 64 <= 512, "TMEM budget");
+
+constexpr int RAW_BYTES = 2 * 128 * KSTEP;  // two raw int8 tiles
+constexpr int B_BYTES = NS * 128;           // one step of fp16 token rows
+constexpr int RS = 6;
+constexpr int BS = 7;
+constexpr int RAW_OFF = 0;
+constexpr int B_OFF = RAW_OFF + RS * RAW_BYTES;
+constexpr int BAR_OFF = B_OFF + BS * B_BYTES;
+constexpr int NBAR = 2 * RS + 2 * BS + 2 * AS + 2;
+constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+constexpr int SCHED_OFF = MISC_OFF + 64;
+constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
+static_assert(B_OFF % 1024 == 0 && B_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
+static_assert(smem_bytes(MAX_E) <= 232448, "shared memory per CTA");
+
+struct Args {
+    int T, k, H, I, E;
+    int nmax;                 // schedule tile (112 or 224 tokens)
+    const uint8_t* act;       // fp16 token tiles (K = H for stage 1, I for stage 2)
+    const float* act_scale;   // per tile row: s_x (stage 1) or s_h (stage 2)
+    const float* w_scale;     // per weight row (output channel)
+    const int32_t* offsets;
+    const int32_t* tile_start;
+    float* h;                 // stage 1 output, fp32 [P, I] in slot order
+    uint16_t* y;              // stage 2 output, bf16 [P, H] in slot order
+    int32_t* dbg_acc;         // optional exact sums: [P, 2I] (stage 1) or [P, H] (stage 2)
+    int32_t* status;
+};
+
+// Unit u -> (expert e, schedule tile t, half of it, column block nb) and the
+// unit's first slot m0 and token count (<= 0 for an empty second half).
+__device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax, const int* tile_start, int E,
+                                            const int32_t* offsets, int& e, int& t, int& half, int& nb, int& m0,
+                                            int& ntok) {
+    const int th = u / NB;
+    nb = u - th * NB;
+    t = th / halves;
+    half = th - t * halves;
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tile_start[mid] <= t) lo = mid; else hi = mid;
+    }
+    e = lo;
+    m0 = offsets[e] + (t - tile_start[e]) * nmax + half * NS;
+    ntok = min(NS, offsets[e + 1] - m0);
+}
+
+__device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
+    *flag = 1;
+    atomicOr(status, QMOE_DEV_WAIT_TIMEOUT);
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
+    int w = 1;
+    if (lane == 0) w = tc::mbar_wait(bar, parity) ? 1 : 0;
+    w = __shfl_sync(0xFFFFFFFFu, w, 0);
+    __syncwarp();
+    return w != 0;
+}
+
+// Four int8 values (one word) -> two fp16 pairs holding them exactly:
+// 0x6400 | (b ^ 0x80) is the fp16 1152 + b; subtracting 1152 leaves b.
+__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    lo = __byte_perm(x, 0x64u, 0x4140);
+    hi = __byte_perm(x, 0x64u, 0x4342);
+    const uint32_t bias = 0x64806480u;
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) { tc::tmem_ld_32x32b_x16(taddr, r); }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) { tc::tmem_st_32x32b_x16(taddr, r); }
+
+// Exact fp32 integer v -> (hi, lo) with v = hi * 2^13 + lo, lo in [-4096, 4095].
+__device__ __forceinline__ void split_hi_lo(uint32_t vbits, int& hi, int& lo) {
+    const int v = __float2int_rn(__uint_as_float(vbits));
+    hi = (v + (1 << (HI_SHIFT - 1))) >> HI_SHIFT;
+    lo = v - hi * (1 << HI_SHIFT);
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sRaw = smem + RAW_OFF;
+    uint8_t* sB = smem + B_OFF;
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+    uint64_t* raw_empty = raw_full + RS;
+    uint64_t* b_full = raw_empty + RS;
+    uint64_t* b_empty = b_full + BS;
+    uint64_t* a_full = b_empty + BS;
+    uint64_t* a_empty = a_full + AS;
+    uint64_t* acc_full = a_empty + AS;
+    uint64_t* acc_empty = acc_full + 1;
+    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 8);
+    int* tile_start = reinterpret_cast<int*>(smem + SCHED_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E;
+    const int K = (STAGE == 1) ? a.H : a.I;
+    const int NB = (STAGE == 1) ? a.I / 128 : a.H / 256;
+    const int KT = K / KSTEP;
+    const int NCH = (KT + CHUNK_STEPS - 1) / CHUNK_STEPS;
+    const int halves = a.nmax / NS;
+
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = a.tile_start[i];
+    if (threadIdx.x == 32 * WARP_MMA) {
+        for (int s = 0; s < RS; ++s) {
+            tc::mbar_init(&raw_full[s], 1);
+            tc::mbar_init(&raw_empty[s], CVT_WARPS);
+        }
+        for (int s = 0; s < BS; ++s) {
+            tc::mbar_init(&b_full[s], 1);
+            tc::mbar_init(&b_empty[s], 2);  // the two issuers' commits
+        }
+        for (int s = 0; s < AS; ++s) {
+            tc::mbar_init(&a_full[s], CVT_WARPS);
+            tc::mbar_init(&a_empty[s], 2);
+        }
+        tc::mbar_init(acc_full, 2);
+        tc::mbar_init(acc_empty, EPI_WARPS);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    const int total_units = tile_start[E] * halves * NB;
+    if ((int)blockIdx.x >= total_units) return;
+
+    if (warp == WARP_MMA) {
+        tc::tmem_alloc(tmem_base_smem, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tm = *tmem_base_smem;
+
+    if (warp == WARP_W) {
+        // ------------------------------------------------ weight producer
+        if (lane == 0) {
+            tc::prefetch_tensormap(&wmap);
+            int rs = 0;
+            uint32_t ph = 0;
+            for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+                int e, t, half, nb, m0, ntok;
+                decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+                if (ntok <= 0) continue;
+                bool ok = true;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!tc::mbar_wait(&raw_empty[rs], ph ^ 1)) { set_abort(abort_flag, a.status); ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&raw_full[rs], RAW_BYTES);
+                    uint8_t* dst = sRaw + rs * RAW_BYTES;
+                    if (STAGE == 1)
+                        tc::tma_load_3d(dst, &wmap, &raw_full[rs], kt * KSTEP, nb * 128, 2 * e);
+                    else
+                        tc::tma_load_2d(dst, &wmap, &raw_full[rs], kt * KSTEP, e * a.H + nb * 256);
+                    if (++rs == RS) { rs = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == WARP_B) {
+        // ------------------------------------------------ activation producer
+        if (lane == 0) {
+            int bs = 0;
+            uint32_t ph = 0;
+            const int64_t bb = (int64_t)a.nmax * 128;
+            for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+                int e, t, half, nb, m0, ntok;
+                decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+                if (ntok <= 0) continue;
+                const uint32_t bytes = (uint32_t)((ntok + 15) & ~15) * 128u;
+                bool ok = true;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!tc::mbar_wait(&b_empty[bs], ph ^ 1)) { set_abort(abort_flag, a.status); ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&b_full[bs], bytes);
+                    tc::bulk_load(sB + bs * B_BYTES, a.act + ((int64_t)t * KT + kt) * bb + (int64_t)half * NS * 128,
+                                  bytes, &b_full[bs]);
+                    if (++bs == BS) { bs = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
+        // ------------------------------------------------ MMA issuers
+        const int iss = warp - WARP_MMA;
+        if (lane == 0) {
+            int bs = 0, as = 0;
+            uint32_t bph = 0, aph = 0, ev = 0;
+            bool pending = false;  // an accumulator event not yet handed back by the epilogue
+            for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+                int e, t, half, nb, m0, ntok;
+                decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+                if (ntok <= 0) continue;
+                const int nmma = (ntok + 15) & ~15;
+                const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
+                const uint32_t dcol = tm + R_COL + (uint32_t)(iss * NS);
+                bool ok = true;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (kt % CHUNK_STEPS == 0 && pending) {
+                        if (!tc::mbar_wait(acc_empty, (ev - 1) & 1)) { set_abort(abort_flag, a.status); ok = false; break; }
+                        pending = false;
+                    }
+                    if (!tc::mbar_wait(&b_full[bs], bph) || !tc::mbar_wait(&a_full[as], aph)) {
+                        set_abort(abort_flag, a.status);
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t b0 = tc::smem_u32(sB + bs * B_BYTES);
+                    const uint32_t a0 = tm + A_COL + (uint32_t)(as * 64 + iss * 32);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_f16_ts(dcol, a0 + 8 * kk, tc::sdesc_kmajor_sw128(b0 + 32 * kk), idesc,
+                                       (kt > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_commit(&b_empty[bs]);
+                    tc::mma_commit(&a_empty[as]);
+                    if (++bs == BS) { bs = 0; bph ^= 1; }
+                    if (++as == AS) { as = 0; aph ^= 1; }
+                    if ((kt + 1) % CHUNK_STEPS == 0 || kt == KT - 1) {
+                        tc::mma_commit(acc_full);
+                        ++ev;
+                        pending = true;
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp < WARP_EPI0) {
+        // ------------------------------------------------ converters (int8 -> fp16 into TMEM)
+        const int tile = (warp - WARP_CVT0) >> 2, q = warp & 3;
+        const int m = q * 32 + lane;  // weight row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int sw = (m >> 1) & 3;  // 64-byte swizzle of the TMA box: 16-byte chunk j at j ^ sw
+        int rs = 0, as = 0;
+        uint32_t rph = 0, aph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+            int e, t, half, nb, m0, ntok;
+            decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            if (ntok <= 0) continue;
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!warp_wait(&raw_full[rs], rph, lane) || !warp_wait(&a_empty[as], aph ^ 1, lane)) {
+                    if (lane == 0) set_abort(abort_flag, a.status);
+                    ok = false;
+                    break;
+                }
+                const uint8_t* src = sRaw + rs * RAW_BYTES + tile * (128 * KSTEP) + m * KSTEP;
+                uint4 c[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const uint4*>(src + ((j ^ sw) << 4));
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
+                const uint32_t wv[16] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w,
+                                         c[2].x, c[2].y, c[2].z, c[2].w, c[3].x, c[3].y, c[3].z, c[3].w};
+                uint32_t o0[16], o1[16];
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    i8x4_to_f16x2(wv[p], o0[2 * p], o0[2 * p + 1]);
+                    i8x4_to_f16x2(wv[8 + p], o1[2 * p], o1[2 * p + 1]);
+                }
+                const uint32_t ta = tm + lane_base + A_COL + (uint32_t)(as * 64 + tile * 32);
+                tmem_st16(ta, o0);
+                tmem_st16(ta + 16, o1);
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&a_full[as]);
+                if (++rs == RS) { rs = 0; rph ^= 1; }
+                if (++as == AS) { as = 0; aph ^= 1; }
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3, eh = (warp - WARP_EPI0) >> 2;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int n = q * 32 + lane;  // weight row within a tile = output column within its 128-column block
+        uint32_t ev = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+            int e, t, half, nb, m0, ntok;
+            decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            if (ntok <= 0) continue;
+            const float* ts = a.act_scale + (int64_t)t * a.nmax + half * NS;
+            float ws0, ws1;  // channel scales of this thread's row in the two tiles
+            int64_t col0, col1, dcol0, dcol1, ostride, dstride;
+            if (STAGE == 1) {
+                const int64_t wr = (int64_t)e * 2 * a.I + nb * 128 + n;
+                ws0 = a.w_scale[wr];
+                ws1 = a.w_scale[wr + a.I];
+                col0 = nb * 128 + n;
+                col1 = col0;
+                ostride = a.I;
+                dcol0 = col0;
+                dcol1 = a.I + col0;
+                dstride = 2 * (int64_t)a.I;
+            } else {
+                const int64_t wr = (int64_t)e * a.H + nb * 256 + n;
+                ws0 = a.w_scale[wr];
+                ws1 = a.w_scale[wr + 128];
+                col0 = nb * 256 + n;
+                col1 = col0 + 128;
+                ostride = a.H;
+                dcol0 = col0;
+                dcol1 = col1;
+                dstride = a.H;
+            }
+            for (int ch = 0; ch < NCH; ++ch, ++ev) {
+                int w = 1;
+                if (lane == 0) w = tc::mbar_wait(acc_full, ev & 1) ? 1 : 0;
+                w = __shfl_sync(0xFFFFFFFFu, w, 0);
+                __syncwarp();
+                if (!w) {
+                    if (lane == 0) set_abort(abort_flag, a.status);
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                if (ch < NCH - 1) {
+                    // drain: hi parts into the 16-bit running sums, lo back as the accumulator
+                    for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
+                        uint32_t g[16], v[16], s[16];
+                        tmem_ld16(tm + lane_base + R_COL + c0, g);
+                        tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
+                        if (ch > 0) tmem_ld16(tm + lane_base + S_COL + c0, s);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            int h0, l0, h1, l1;
+                            split_hi_lo(g[j], h0, l0);
+                            split_hi_lo(v[j], h1, l1);
+                            if (ch > 0) {
+                                h0 += (int)(int16_t)(s[j] & 0xFFFFu);
+                                h1 += (int)(int16_t)(s[j] >> 16);
+                            }
+                            s[j] = (uint32_t)(uint16_t)h0 | ((uint32_t)(uint16_t)h1 << 16);
+                            g[j] = __float_as_uint((float)l0);
+                            v[j] = __float_as_uint((float)l1);
+                        }
+                        tmem_st16(tm + lane_base + R_COL + c0, g);
+                        tmem_st16(tm + lane_base + R_COL + NS + c0, v);
+                        tmem_st16(tm + lane_base + S_COL + c0, s);
+                    }
+                    tc::tmem_st_wait();
+                } else {
+                    for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
+                        uint32_t g[16], v[16], s[16];
+                        tmem_ld16(tm + lane_base + R_COL + c0, g);
+                        tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
+                        if (NCH > 1) tmem_ld16(tm + lane_base + S_COL + c0, s);
+                        // the chunk's per-token activation scales, one per lane, broadcast below
+                        const float fl = (lane < 16 && c0 + lane < ntok) ? ts[c0 + lane] : 0.f;
+                        tc::tmem_ld_wait();
+                        const int nv = min(16, ntok - c0);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            int a0 = __float2int_rn(__uint_as_float(g[j]));
+                            int a1 = __float2int_rn(__uint_as_float(v[j]));
+                            if (NCH > 1) {
+                                a0 += (int)(int16_t)(s[j] & 0xFFFFu) * (1 << HI_SHIFT);
+                                a1 += (int)(int16_t)(s[j] >> 16) * (1 << HI_SHIFT);
+                            }
+                            const float fx = __shfl_sync(0xFFFFFFFFu, fl, j);
+                            if (j < nv) {
+                                const int64_t slot = m0 + c0 + j;
+                                const float r0 = ((float)a0 * fx) * ws0;
+                                const float r1 = ((float)a1 * fx) * ws1;
+                                if (STAGE == 1) {
+                                    a.h[slot * ostride + col0] = silu_mul(r0, r1);
+                                } else {
+                                    a.y[slot * ostride + col0] = float_to_bf16_bits(r0);
+                                    a.y[slot * ostride + col1] = float_to_bf16_bits(r1);
+                                }
+                                if (a.dbg_acc) {
+                                    a.dbg_acc[slot * dstride + dcol0] = a0;
+                                    a.dbg_acc[slot * dstride + dcol1] = a1;
+                                }
+                            }
+                        }
+                    }
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(acc_empty);
+            }
+        }
+    }
+
+    if (*abort_flag) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000ll) { }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tm, 512);
+    }
+}
+
+// Raw int8 weights viewed through a TMA map with 64-byte rows (64 K elements)
+// and the 64-byte swizzle.  Stage 1: {H, I, 2E} (gate rows of expert e are
+// plane 2e, its up rows plane 2e+1), box {64, 128, 2}: a gate tile and its up
+// partner.  Stage 2: {I, E*H}, box {64, 256}: two adjacent row tiles.
+static int make_w_map(CUtensorMap* map, const void* w, const qmoe_dims* d, int stage) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return QMOE_ERR_CUDA;
+    CUresult r;
+    if (stage == 1) {
+        cuuint64_t gdim[3] = {(cuuint64_t)d->H, (cuuint64_t)d->I, (cuuint64_t)(2 * d->E)};
+        cuuint64_t gstride[2] = {(cuuint64_t)d->H, (cuuint64_t)d->I * (cuuint64_t)d->H};
+        cuuint32_t box[3] = {KSTEP, 128, 2};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w), gdim, gstride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t gdim[2] = {(cuuint64_t)d->I, (cuuint64_t)d->E * (cuuint64_t)d->H};
+        cuuint64_t gstride[1] = {(cuuint64_t)d->I};
+        cuuint32_t box[2] = {KSTEP, 256};
+        cuuint32_t estr[2] = {1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), gdim, gstride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS ? QMOE_OK : QMOE_ERR_UNSUPPORTED;
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int STAGE>
+static int launch(const CUtensorMap& map, const Args& a, cudaStream_t st) {
+    if (cudaFuncSetAttribute(i8_gemm_kernel<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes(MAX_E)) != cudaSuccess)
+        return QMOE_ERR_LAUNCH;
+    const int grid = sm_count();
+    if (grid <= 0) return QMOE_ERR_CUDA;
+    i8_gemm_kernel<STAGE><<<grid, THREADS, smem_bytes(a.E), st>>>(map, a);
+    return launch_status();
+}
+
+}  // namespace i8
+
+bool i8_tc_ok(const qmoe_dims* d) {
+    return d->H % 256 == 0 && d->I % 128 == 0 && d->H <= i8::MAX_K && d->I <= i8::MAX_K && d->E <= i8::MAX_E;
+}
+
+int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, const float* w1_s,
+                const int32_t* offsets, const int32_t* tile_start, float* h, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st) {
+    CUtensorMap map;
+    int rc = i8::make_w_map(&map, w1, d, 1);
+    if (rc != QMOE_OK) return rc;
+    i8::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.nmax = mxt::nmax_for(d);
+    a.act = x_tiles;
+    a.act_scale = reinterpret_cast<const float*>(x_tiles + bft::blocks_bytes(d, d->H));
+    a.w_scale = w1_s;
+    a.offsets = offsets; a.tile_start = tile_start;
+    a.h = h; a.dbg_acc = dbg_acc; a.status = status;
+    return i8::launch<1>(map, a, st);
+}
+
+int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
+                const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st) {
+    CUtensorMap map;
+    int rc = i8::make_w_map(&map, w2, d, 2);
+    if (rc != QMOE_OK) return rc;
+    i8::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.nmax = mxt::nmax_for(d);
+    a.act = h_tiles;
+    a.act_scale = reinterpret_cast<const float*>(h_tiles + bft::blocks_bytes(d, d->I));
+    a.w_scale = w2_s;
+    a.offsets = offsets; a.tile_start = tile_start;
+    a.y = y; a.dbg_acc = dbg_acc; a.status = status;
+    return i8::launch<2>(map, a, st);
+}
+
+}  // namespace qmoe

@@ -47,6 +47,7 @@
 #include "qmoe_common.cuh"
 #include "mx_tiles.cuh"
 #include "tc_ptx.cuh"
+#include "tma_host.cuh"
 
 #include <mutex>
 
@@ -380,24 +381,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
 
 // ------------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 // Tile-major pre-packed FP4 weights viewed as 64-byte rows (128 elements),
 // one 128-row box per 128x128 tile: each box is a contiguous 8 KiB read,
 // unpacked by the TMA to 16-byte-aligned groups and 128-byte swizzled in
@@ -406,7 +389,7 @@ static EncodeTiledFn encode_fn() {
 // tiles occupy the first half_bytes of its block and the up tiles the next,
 // so one 128 x 128 x 2 box brings a gate tile and its up partner.
 static int make_fp4_map(CUtensorMap* map, const void* w, int64_t tiles, int64_t half_bytes, int E, int64_t KT) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return QMOE_ERR_CUDA;
     CUresult r;
     if (half_bytes > 0) {

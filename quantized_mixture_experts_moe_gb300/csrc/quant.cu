@@ -250,6 +250,99 @@ int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* s
     return launch_status();
 }
 
+// W8A8 activation tiles: one warp per expert-sorted slot.  The slot's row
+// (stage 1: its token's bf16 x row; stage 2: its own fp32 h row) is quantised
+// with the per-row int8 rule of quant_rows_int8_kernel (s = amax / 127, IEEE
+// division, nearest-even, clamped to +-127) and each code is written as the
+// fp16 value equal to it (exact) into the 128-byte-swizzled tile layout the
+// W4A16 x tiles use, 8 codes per 16-byte chunk; s goes to the per-row tail.
+__device__ __forceinline__ void load8_as_float(const uint16_t* p, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ void load8_as_float(const float* p, float (&f)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+template <typename In, bool PERMUTE>
+__global__ void __launch_bounds__(kPqWarps * 32)
+quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
+                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
+                        int K, int nmax, int64_t P, int64_t tail_off, uint8_t* __restrict__ tiles) {
+    const int lane = threadIdx.x & 31;
+    const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
+    int tile = -1, row = 0;
+    int64_t src = 0;
+    if (lane == 0 && slot < P && slot < offsets[E]) {
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (offsets[mid] <= slot) lo = mid; else hi = mid;
+        }
+        const int local = (int)(slot - offsets[lo]);
+        tile = tile_start[lo] + local / nmax;
+        row = local % nmax;
+        src = PERMUTE ? (int64_t)(sorted_pair_ids[slot] / k) : slot;
+    }
+    tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
+    if (tile < 0) return;
+    row = __shfl_sync(0xFFFFFFFFu, row, 0);
+    src = __shfl_sync(0xFFFFFFFFu, src, 0);
+    const In* xr = x + src * K;
+    float amax = 0.f;
+    for (int j = lane; j < K / 8; j += 32) {
+        float f[8];
+        load8_as_float(xr + 8 * j, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+    const int64_t bb = bft::block_bytes(nmax);
+    uint8_t* tbase = tiles + (int64_t)tile * (K / 64) * bb;
+    for (int j = lane; j < K / 8; j += 32) {  // chunk j: K step j/8, chunk j%8 of the 128-byte row
+        float f[8];
+        load8_as_float(xr + 8 * j, f);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float q0 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i], sc)), -127.f), 127.f);
+            const float q1 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i + 1], sc)), -127.f), 127.f);
+            const __half2 hv = __floats2half2_rn(q0, q1);
+            o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        uint8_t* blk = tbase + (int64_t)(j >> 3) * bb;
+        *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) reinterpret_cast<float*>(tiles + tail_off)[(int64_t)tile * nmax + row] = sc;
+}
+
+int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool from_bf16_tokens,
+                            const int32_t* sorted, const int32_t* offsets, const int32_t* tile_start, uint8_t* tiles,
+                            cudaStream_t st) {
+    const int64_t P = (int64_t)d->T * d->k;
+    if (P == 0) return QMOE_OK;
+    const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
+    const int nmax = mxt::nmax_for(d);
+    const int64_t tail = bft::blocks_bytes(d, K);
+    if (from_bf16_tokens)
+        quant_tiles_int8_kernel<uint16_t, true><<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(
+            static_cast<const uint16_t*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, P, tail, tiles);
+    else
+        quant_tiles_int8_kernel<float, false><<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(
+            static_cast<const float*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, P, tail, tiles);
+    return launch_status();
+}
+
 int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st) {
     const int64_t n8 = rows * cols / 8;
     if (n8 == 0) return QMOE_OK;

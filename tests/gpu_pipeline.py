@@ -89,16 +89,16 @@ def run_layer(w, inp, keep=False):
         qb.qmoe_gemm2_mxfp4(d, ht, w2, w2p, offsets, y, status, ws)
         res.update(xt=xt, ht=ht)
     else:
-        xq, xs = empty((T, H), torch.int8), empty(T, torch.float32)
-        qb.qmoe_quant_rows_int8_bf16(t["x"], xq, xs)
+        xt = empty(qb.w8a8_tiles_bytes(d, H), torch.uint8)
+        qb.qmoe_permute_quant_int8(d, t["x"], sorted_ids, offsets, xt, ws)
         h = empty((P, I), torch.float32)
         acc1 = empty((P, 2 * I), torch.int32) if keep else None
-        qb.qmoe_gemm1_swiglu_w8a8(d, xq, xs, t["w1"], t["w1_s"], offsets, sorted_ids, h, acc1, status, ws)
-        hq, hs = empty((P, I), torch.int8), empty(P, torch.float32)
-        qb.qmoe_quant_rows_int8_f32(h, hq, hs)
+        qb.qmoe_gemm1_swiglu_w8a8(d, xt, t["w1"], t["w1_s"], offsets, h, acc1, status, ws)
+        ht = empty(qb.w8a8_tiles_bytes(d, I), torch.uint8)
+        qb.qmoe_quant_tiles_int8_f32(d, h, offsets, ht, ws)
         acc2 = empty((P, H), torch.int32) if keep else None
-        qb.qmoe_gemm2_w8a8(d, hq, hs, t["w2"], t["w2_s"], offsets, y, acc2, status, ws)
-        res.update(xq=xq, xs=xs, h=h, hq=hq, hs=hs, acc1=acc1, acc2=acc2)
+        qb.qmoe_gemm2_w8a8(d, ht, t["w2"], t["w2_s"], offsets, y, acc2, status, ws)
+        res.update(ixt=xt, h=h, iht=ht, acc1=acc1, acc2=acc2)
     out = empty((T, H), torch.int16)
     qb.qmoe_combine(d, y, t["topk_w"], slot, out)
     torch.cuda.synchronize()
@@ -117,6 +117,11 @@ def run_layer(w, inp, keep=False):
             nt = max_tiles(P, E, nmax)
             r["x_f16"], r["x_fac"] = unpack_w4_x_tiles(r.pop("bxt"), r["offsets"], nmax, H, nt)
             r["h"], r["h_gmax"] = unpack_w4_h_tiles(r.pop("bht"), r["offsets"], nmax, I, nt)
+        else:
+            nmax = tile_nmax(T, k, E)
+            nt = max_tiles(P, E, nmax)
+            r["xq"], r["xs"] = unpack_i8_tiles(r.pop("ixt"), r["offsets"], nmax, H, nt)
+            r["hq"], r["hs"] = unpack_i8_tiles(r.pop("iht"), r["offsets"], nmax, I, nt)
     return r
 
 
@@ -224,4 +229,31 @@ def pack_w4_h_tiles(rows, offsets, nmax, I, nbytes, ntiles):
     mag = ((v.astype(np.uint32) & 0x7FFF) << 16).view(np.float32).reshape(len(slots), I // 32, 32).max(axis=2)
     tail = buf[ntiles * (I // 64) * nmax * 128:].view(np.float32)
     tail[(t * nmax + r)[:, None] * (I // 32) + np.arange(I // 32)[None, :]] = mag
+    return buf
+
+
+# ------------------------------------------------------------------ W8A8 activation tile layout (include/qmoe.h)
+
+def unpack_i8_tiles(buf, offsets, nmax, K, ntiles):
+    """W8A8 tiles -> slot-order int8 codes [P_valid, K] (stored as exact fp16 values) and scales [P_valid]."""
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    vals = _gather16(buf, _w4_layout(nmax, K, t, r)).view(np.float16).astype(np.float64)
+    q = vals.astype(np.int64)
+    assert np.array_equal(q, vals) and np.abs(q).max(initial=0) <= 127, "tile values are not int8 codes"
+    tail = buf[ntiles * (K // 64) * nmax * 128:].view(np.float32)
+    return q.astype(np.int8), tail[t * nmax + r]
+
+
+def pack_i8_tiles(codes, scales, offsets, nmax, K, nbytes, ntiles):
+    """Slot-order int8 codes [P_valid, K] + scales [P_valid] -> a W8A8 tile buffer of nbytes."""
+    buf = np.zeros(nbytes, np.uint8)
+    slots = np.arange(offsets[-1])
+    t, r = _tile_index(offsets, nmax, slots)
+    off = _w4_layout(nmax, K, t, r)
+    v = codes[:len(slots)].astype(np.float16).view(np.uint16)
+    buf[off] = (v & 0xFF).astype(np.uint8)
+    buf[off + 1] = (v >> 8).astype(np.uint8)
+    tail = buf[ntiles * (K // 64) * nmax * 128:].view(np.float32)
+    tail[t * nmax + r] = scales[:len(slots)]
     return buf

@@ -88,3 +88,26 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.qmoe_prepack_mx_scales(128, 100, ok, ok, null) == -1
     assert lib.qmoe_prepack_mx_scales(128, 128, null, ok, null) == -1
     assert qb.mx_scales_packed_bytes(300, 4096) == 3 * 32 * 512
+
+
+def test_w8a8_host_checks(lib):
+    d = qb.dims(16, 2, 256, 128, 8)
+    null = None
+    ok = ctypes.c_void_p(0x1000)
+    big = 1 << 30
+    # W8A8 tiles: the W4A16 block layout (9 tiles, K/64 steps of 112 rows x 128 bytes) + one fp32 scale per row
+    assert qb.w8a8_tiles_bytes(d, 256) == 9 * 4 * 112 * 128 + 9 * 112 * 4
+    assert qb.w8a8_tiles_bytes(d, 128) == 9 * 2 * 112 * 128 + 9 * 112 * 4
+    assert qb.w8a8_tiles_bytes(d, 96) == 0
+    # null pointers -> QMOE_ERR_ARG before any launch
+    assert lib.qmoe_permute_quant_int8(ctypes.byref(d), null, ok, ok, ok, ok, big, null) == -1
+    assert lib.qmoe_quant_tiles_int8_f32(ctypes.byref(d), ok, null, ok, ok, big, null) == -1
+    assert lib.qmoe_gemm1_swiglu_w8a8(ctypes.byref(d), ok, null, ok, ok, ok, null, ok, ok, big, null) == -1
+    assert lib.qmoe_gemm2_w8a8(ctypes.byref(d), ok, ok, ok, ok, null, null, ok, ok, big, null) == -1
+    # a misaligned debug buffer
+    odd = ctypes.c_void_p(0x1000 + 4)
+    assert lib.qmoe_gemm2_w8a8(ctypes.byref(d), ok, ok, ok, ok, ok, odd, ok, ok, big, null) == -1
+    # shapes outside the tensor-core tiles (H % 256, I % 128, K <= 16384) -> QMOE_ERR_UNSUPPORTED, no launch
+    for bad in (qb.dims(16, 2, 384, 128, 8), qb.dims(16, 2, 256, 192, 8), qb.dims(16, 2, 256, 16512, 8)):
+        assert lib.qmoe_gemm1_swiglu_w8a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2
+        assert lib.qmoe_gemm2_w8a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2

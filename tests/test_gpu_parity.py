@@ -133,7 +133,11 @@ S1_CASES = [
     gen.custom("s1_mxfp4", "mxfp4", 40, 512, 6, 3, 384, seed=22),
     gen.custom("s1_mxfp4_tc", "mxfp4", 60, 512, 6, 3, 256, seed=24),
     gen.custom("s1_mxfp4_tc_multitile", "mxfp4", 200, 256, 3, 2, 128, seed=25),
-    gen.custom("s1_w8a8", "w8a8", 40, 512, 6, 3, 192, seed=23),
+    gen.custom("s1_w8a8", "w8a8", 40, 512, 6, 3, 256, seed=23),
+    # K = 2304: two 1024-element drains and a 256-element tail
+    gen.custom("s1_w8a8_drains", "w8a8", 120, 2304, 4, 2, 128, seed=27),
+    # T*k > 96*E: 224-token schedule tiles, each run as two 112-token halves
+    gen.custom("s1_w8a8_big_tiles", "w8a8", 500, 1280, 4, 2, 256, seed=28),
 ]
 
 
@@ -170,8 +174,14 @@ def test_stage1_against_oracle(w):
         assert rel_l2(got, ref) < REL_L2
         assert np.mean(g["hq"] != dbg["hq"][order]) < 1e-3
     else:
+        rq, rs = oracle.int8_quant(gp.bf16_to_f64(d["x"]).astype(np.float32))
+        tok = order // w.k  # slot -> token
+        assert np.array_equal(g["xq"], rq[tok]) and np.array_equal(g["xs"], rs[tok])
         assert np.array_equal(g["acc1"], dbg["acc1"][order])
         assert rel_l2(g["h"], dbg["h"][order]) < 1e-5
+        # the intermediate codes follow the int8 rule on the kernel's own fp32 h
+        hq, hs = oracle.int8_quant(g["h"].astype(np.float32))
+        assert np.array_equal(g["hq"], hq) and np.array_equal(g["hs"], hs)
     assert rel_l2(gp.bf16_to_f64(g["out"]), ref_out) < REL_L2
 
 
@@ -181,7 +191,8 @@ S2_CASES = [
     gen.custom("s2_w4a16", "w4a16", 1, 512, 5, 1, 256, seed=31),
     gen.custom("s2_mxfp4", "mxfp4", 1, 768, 5, 1, 384, seed=32),
     gen.custom("s2_mxfp4_tc", "mxfp4", 1, 512, 5, 1, 256, seed=34),
-    gen.custom("s2_w8a8", "w8a8", 1, 320, 5, 1, 256, seed=33),
+    gen.custom("s2_w8a8", "w8a8", 1, 512, 5, 1, 256, seed=33),
+    gen.custom("s2_w8a8_drains", "w8a8", 1, 256, 5, 1, 1152, seed=35),
 ]
 
 
@@ -228,21 +239,52 @@ def test_stage2_against_oracle(w):
         torch.cuda.synchronize()
         assert rel_l2(yv(), ref) < 5e-3
     else:
+        ids = experts.reshape(rows, 1)
+        counts_t, off_t = gp.empty(w.E, torch.int32), gp.empty(w.E + 1, torch.int32)
+        srt, slt = gp.empty(rows, torch.int32), gp.empty(rows, torch.int32)
+        st = torch.zeros(1, dtype=torch.int32, device=gp.DEV)
+        ws = qb.alloc_workspace(qb.workspace_bytes(d))
+        qb.qmoe_align_sort(d, gp.dev(ids), counts_t, off_t, srt, slt, st, ws)
+        nmax = gp.tile_nmax(rows, 1, w.E)
+        ht = gp.pack_i8_tiles(s2["h"], s2["h_s"], offsets, nmax, w.I, qb.w8a8_tiles_bytes(d, w.I),
+                              gp.max_tiles(rows, w.E, nmax))
         acc = gp.empty((rows, w.H), torch.int32)
-        qb.qmoe_gemm2_w8a8(d, gp.dev(s2["h"]), gp.dev(s2["h_s"]), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), t_off, y,
-                           acc)
+        qb.qmoe_gemm2_w8a8(d, gp.dev(ht), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), off_t, y, acc, st, ws)
         ref, racc = oracle.stage2("w8a8", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"],
                                   acc=True)
         torch.cuda.synchronize()
+        assert int(st.item()) == 0
         assert np.array_equal(gp.host(acc), racc)
         # y = ((float)acc * s_h) * s_w is exact fp32 on both sides; both round it to bf16
         ref_bf16 = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
         assert np.array_equal(gp.host(y), ref_bf16)
 
 
-def test_w8a8_adversarial_accumulators_exact():
-    # all-+-127 operands: the largest-magnitude int32 sums a K=4096 row makes
-    w = gen.custom("adv", "w8a8", 1, 4096, 2, 1, 1024, seed=5)
+def _stage2_w8a8_direct(w, h, hs, w2, w2s, experts):
+    """Stage 2 alone on given int8 codes (slot order, experts ascending)."""
+    rows = len(h)
+    counts = np.bincount(experts, minlength=w.E).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    d = qb.dims(rows, 1, w.H, w.I, w.E)
+    counts_t, off_t = gp.empty(w.E, torch.int32), gp.empty(w.E + 1, torch.int32)
+    srt, slt = gp.empty(rows, torch.int32), gp.empty(rows, torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=gp.DEV)
+    ws = qb.alloc_workspace(qb.workspace_bytes(d))
+    qb.qmoe_align_sort(d, gp.dev(experts.reshape(rows, 1).astype(np.int32)), counts_t, off_t, srt, slt, st, ws)
+    nmax = gp.tile_nmax(rows, 1, w.E)
+    ht = gp.pack_i8_tiles(h, hs, offsets, nmax, w.I, qb.w8a8_tiles_bytes(d, w.I), gp.max_tiles(rows, w.E, nmax))
+    y, acc = gp.empty((rows, w.H), torch.int16), gp.empty((rows, w.H), torch.int32)
+    qb.qmoe_gemm2_w8a8(d, gp.dev(ht), gp.dev(w2), gp.dev(w2s), off_t, y, acc, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return gp.host(acc)
+
+
+@pytest.mark.parametrize("K", [1024, 4096])
+def test_w8a8_adversarial_accumulators_exact(K):
+    # all-+-127 operands: the largest-magnitude int32 sums a row of length K makes
+    # (127^2 * 4096 = 66,064,384 is far past 2^24, where fp32 stops being exact)
+    w = gen.custom("adv", "w8a8", 1, 256, 2, 1, K, seed=5)
     rows = 64
     h = np.full((rows, w.I), 127, np.int8)
     h[1::2] = -127
@@ -251,14 +293,27 @@ def test_w8a8_adversarial_accumulators_exact():
     hs = np.full(rows, 1e-3, np.float32)
     w2s = np.full((w.E, w.H), 1e-3, np.float32)
     experts = np.repeat(np.arange(w.E, dtype=np.int32), rows // w.E)
-    offsets = np.array([0, rows // 2, rows], np.int32)
-    d = qb.dims(rows, 1, w.H, w.I, w.E)
-    y, acc = gp.empty((rows, w.H), torch.int16), gp.empty((rows, w.H), torch.int32)
-    qb.qmoe_gemm2_w8a8(d, gp.dev(h), gp.dev(hs), gp.dev(w2), gp.dev(w2s), gp.dev(offsets), y, acc)
-    torch.cuda.synchronize()
+    got = _stage2_w8a8_direct(w, h, hs, w2, w2s, experts)
     _, racc = oracle.stage2("w8a8", w.H, w.I, w.E, experts, h, hs, w2, w2s, acc=True)
-    assert np.array_equal(gp.host(acc), racc)
+    assert np.array_equal(got, racc)
     assert np.abs(racc).max() == 127 * 127 * w.I
+
+
+def test_w8a8_stage1_adversarial_accumulators_exact():
+    # every activation code +-127 and every weight +-127 along K = H = 4096
+    w = gen.custom("adv1", "w8a8", 8, 4096, 2, 1, 128, seed=6)
+    d = gen.make_all(w)
+    sign = np.where(np.arange(w.H) % 5 == 0, -1.0, 1.0).astype(np.float32)
+    d["x"] = gen.bf16_bits_from_f32(np.tile(sign, (w.T, 1)) * np.arange(1, w.T + 1, dtype=np.float32)[:, None])
+    w1 = np.where(np.arange(w.H) % 5 == 0, -127, 127).astype(np.int8)
+    d["w1"] = np.tile(w1, (w.E, 2 * w.I, 1))
+    d["w1"][:, 1::2] *= -1
+    d["w1_s"] = np.full((w.E, 2 * w.I), 1e-9, np.float32)
+    g = gp.run_layer(w, d, keep=True)
+    _, dbg, _ = oracle.moe_forward(w.scheme, dims(w), d, debug=True)
+    order = oracle.align_sort(d["topk_ids"], w.E)["sorted_pair_ids"]
+    assert np.array_equal(g["acc1"], dbg["acc1"][order])
+    assert np.abs(dbg["acc1"]).max() == 127 * 127 * w.H
 
 
 # ------------------------------------------------------------------ combine
@@ -288,7 +343,7 @@ def test_combine_against_oracle_and_deterministic():
 SMALL = [
     gen.WORKLOADS["tiny_w4a16"],
     gen.custom("e2e_mxfp4_ragged", "mxfp4", 50, 1024, 12, 4, 128, seed=41),
-    gen.custom("e2e_w8a8_ragged", "w8a8", 50, 1024, 12, 4, 160, seed=42),
+    gen.custom("e2e_w8a8_ragged", "w8a8", 50, 1024, 12, 4, 256, seed=42),
     gen.custom("e2e_w4a16_ragged", "w4a16", 50, 1024, 12, 4, 256, seed=43),
     gen.custom("e2e_w4a16_big_tiles", "w4a16", 700, 512, 8, 2, 256, seed=47),
     gen.custom("e2e_zipf_mxfp4", "mxfp4", 64, 512, 64, 8, 128, routing="zipf", seed=44),
@@ -313,8 +368,7 @@ def test_layer_ragged_expert_loads(scheme):
     rng = np.random.default_rng(77)
     ids = gen.routing_with_counts(rng, counts, 2)
     T = ids.shape[0]
-    I = 96 if scheme == "w8a8" else 128  # tensor-core paths: I % 128 == 0, H % 256 == 0
-    w = gen.custom(f"ragged_{scheme}", scheme, T, 256, len(counts), 2, I, seed=78)
+    w = gen.custom(f"ragged_{scheme}", scheme, T, 256, len(counts), 2, 128, seed=78)  # H % 256, I % 128
     d = gen.make_all(w, routing=(ids, gen.routing_weights(rng, T, 2)))
     g = gp.run_layer(w, d)
     ref = oracle.moe_forward(scheme, dims(w), d)
