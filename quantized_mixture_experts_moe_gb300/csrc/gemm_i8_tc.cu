@@ -11,7 +11,7 @@
 // sum over at most 1024 K elements is an exact integer.  The accumulator is
 // therefore drained every 1024 K elements: the epilogue splits the exact fp32
 // value v into hi * 2^13 + lo with |lo| <= 4096, adds hi to a 16-bit running
-// sum kept in TMEM and writes lo back as the fp32 accumulator, on which the
+// sum kept in shared memory and writes lo back as the fp32 accumulator, on which the
 // next 1024 K elements accumulate (|lo| + 1024 * 16129 < 2^24, exact again).
 // At the end acc = hi * 2^13 + v, the exact int32 sum, for K <= 16384
 // (|hi| <= 16384 * 16129 / 2^13 < 2^15).
@@ -46,34 +46,40 @@ constexpr int WARP_W = 0, WARP_B = 1, WARP_MMA = 2;
 constexpr int WARP_CVT0 = 4, CVT_WARPS = 8;
 constexpr int WARP_EPI0 = 12, EPI_WARPS = 8;
 constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
-constexpr int KSTEP = 64;        // K elements per step
+constexpr int KSTEP = 128;       // K elements per step (two 64-element halves)
 constexpr int NS = 112;          // tokens per MMA (a schedule tile of 224 is two of these)
-constexpr int CHUNK_STEPS = 16;  // steps between drains: 1024 K elements
+constexpr int CHUNK_STEPS = 8;   // steps between drains: 1024 K elements
 constexpr int HI_SHIFT = 13;
 constexpr int MAX_E = 512;
 constexpr int MAX_K = 16384;
 
-// TMEM columns: fp32 accumulators of the two tiles, the packed 16-bit running
-// high parts (tile 0 in the low half of a column, tile 1 in the high half),
-// and a two-slot ring of A operands (a 128 x 64 fp16 tile = 32 columns).
+// TMEM columns: the fp32 accumulators of the two tiles, then a two-slot
+// ring of A operands (a 128 x 128 fp16 tile = 64 columns, two per slot).  The
+// 16-bit running high parts live in shared memory, one 32-bit word per
+// (token, row): tile 0 in the low half, tile 1 in the high half.
 constexpr uint32_t R_COL = 0;
-constexpr uint32_t S_COL = 2 * NS;
-constexpr uint32_t A_COL = 384;
+constexpr uint32_t A_COL = 256;
 constexpr int AS = 2;
-static_assert(S_COL + NS <= A_COL && A_COL + AS * 64 <= 512, "TMEM budget");
+constexpr int A_SLOT_COLS = 2 * KSTEP / 2;  // two tiles x KSTEP/2 fp16 pairs
+static_assert(R_COL + 2 * NS <= A_COL && A_COL + AS * A_SLOT_COLS <= 512, "TMEM budget");
 
-constexpr int RAW_BYTES = 2 * 128 * KSTEP;  // two raw int8 tiles
-constexpr int B_BYTES = NS * 128;           // one step of fp16 token rows
-constexpr int RS = 6;
-constexpr int BS = 7;
+constexpr int HALF_RAW = 2 * 128 * 64;      // one 64-element half of both raw int8 tiles (one TMA box)
+constexpr int RAW_BYTES = 2 * HALF_RAW;
+constexpr int HALF_B = NS * 128;            // one 64-element half of the step's fp16 token rows
+constexpr int B_BYTES = 2 * HALF_B;
+constexpr int RS = 2;
+constexpr int BS = 3;
+static_assert(BS >= AS + 1, "a step's done barrier is not reused before the converter has waited on it");
 constexpr int RAW_OFF = 0;
 constexpr int B_OFF = RAW_OFF + RS * RAW_BYTES;
-constexpr int BAR_OFF = B_OFF + BS * B_BYTES;
-constexpr int NBAR = 2 * RS + 2 * BS + 2 * AS + 2;
+constexpr int S_OFF = B_OFF + BS * B_BYTES;
+constexpr int S_BYTES = NS * 128 * 4;
+constexpr int BAR_OFF = S_OFF + S_BYTES;
+constexpr int NBAR = 2 * RS + 2 * BS + AS + 2;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SCHED_OFF = MISC_OFF + 64;
 constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
-static_assert(B_OFF % 1024 == 0 && B_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
+static_assert(B_OFF % 1024 == 0 && HALF_B % 1024 == 0 && HALF_RAW % 1024 == 0, "swizzled tiles 1024-aligned");
 static_assert(smem_bytes(MAX_E) <= 232448, "shared memory per CTA");
 
 struct Args {
@@ -114,6 +120,11 @@ __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
     atomicOr(status, QMOE_DEV_WAIT_TIMEOUT);
 }
 
+// The abort flag as one value for the whole warp (lane 0's read).
+__device__ __forceinline__ bool warp_flag(volatile int* flag) {
+    return __shfl_sync(0xFFFFFFFFu, *flag, 0) != 0;
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
     int w = 1;
     if (lane == 0) w = tc::mbar_wait(bar, parity) ? 1 : 0;
@@ -149,13 +160,13 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sRaw = smem + RAW_OFF;
     uint8_t* sB = smem + B_OFF;
+    uint32_t* sS = reinterpret_cast<uint32_t*>(smem + S_OFF);  // [token][row] packed high parts
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
     uint64_t* raw_empty = raw_full + RS;
     uint64_t* b_full = raw_empty + RS;
-    uint64_t* b_empty = b_full + BS;
-    uint64_t* a_full = b_empty + BS;
-    uint64_t* a_empty = a_full + AS;
-    uint64_t* acc_full = a_empty + AS;
+    uint64_t* done = b_full + BS;  // step g completed (both issuers' MMAs): frees B slot g % BS and A slot g % AS
+    uint64_t* a_full = done + BS;
+    uint64_t* acc_full = a_full + AS;
     uint64_t* acc_empty = acc_full + 1;
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 8);
@@ -177,12 +188,9 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
         }
         for (int s = 0; s < BS; ++s) {
             tc::mbar_init(&b_full[s], 1);
-            tc::mbar_init(&b_empty[s], 2);  // the two issuers' commits
+            tc::mbar_init(&done[s], 2);  // the two issuers' commits
         }
-        for (int s = 0; s < AS; ++s) {
-            tc::mbar_init(&a_full[s], CVT_WARPS);
-            tc::mbar_init(&a_empty[s], 2);
-        }
+        for (int s = 0; s < AS; ++s) tc::mbar_init(&a_full[s], CVT_WARPS);
         tc::mbar_init(acc_full, 2);
         tc::mbar_init(acc_empty, EPI_WARPS);
         *abort_flag = 0;
@@ -216,10 +224,14 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                     if (!tc::mbar_wait(&raw_empty[rs], ph ^ 1)) { set_abort(abort_flag, a.status); ok = false; break; }
                     tc::mbar_arrive_expect_tx(&raw_full[rs], RAW_BYTES);
                     uint8_t* dst = sRaw + rs * RAW_BYTES;
-                    if (STAGE == 1)
-                        tc::tma_load_3d(dst, &wmap, &raw_full[rs], kt * KSTEP, nb * 128, 2 * e);
-                    else
-                        tc::tma_load_2d(dst, &wmap, &raw_full[rs], kt * KSTEP, e * a.H + nb * 256);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (STAGE == 1)
+                            tc::tma_load_3d(dst + hh * HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh, nb * 128, 2 * e);
+                        else
+                            tc::tma_load_2d(dst + hh * HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh,
+                                            e * a.H + nb * 256);
+                    }
                     if (++rs == RS) { rs = 0; ph ^= 1; }
                 }
                 if (!ok) break;
@@ -238,58 +250,58 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                 const uint32_t bytes = (uint32_t)((ntok + 15) & ~15) * 128u;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!tc::mbar_wait(&b_empty[bs], ph ^ 1)) { set_abort(abort_flag, a.status); ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&b_full[bs], bytes);
-                    tc::bulk_load(sB + bs * B_BYTES, a.act + ((int64_t)t * KT + kt) * bb + (int64_t)half * NS * 128,
-                                  bytes, &b_full[bs]);
+                    if (!tc::mbar_wait(&done[bs], ph ^ 1)) { set_abort(abort_flag, a.status); ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&b_full[bs], 2 * bytes);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+                        tc::bulk_load(sB + bs * B_BYTES + hh * HALF_B,
+                                      a.act + ((int64_t)t * (2 * KT) + 2 * kt + hh) * bb + (int64_t)half * NS * 128, bytes,
+                                      &b_full[bs]);
                     if (++bs == BS) { bs = 0; ph ^= 1; }
                 }
                 if (!ok) break;
             }
         }
     } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
-        // ------------------------------------------------ MMA issuers
+        // ------------------------------------------------ MMA issuers (warp-uniform; one elected lane issues)
         const int iss = warp - WARP_MMA;
-        if (lane == 0) {
-            int bs = 0, as = 0;
-            uint32_t bph = 0, aph = 0, ev = 0;
-            bool pending = false;  // an accumulator event not yet handed back by the epilogue
-            for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
-                int e, t, half, nb, m0, ntok;
-                decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
-                if (ntok <= 0) continue;
-                const int nmma = (ntok + 15) & ~15;
-                const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
-                const uint32_t dcol = tm + R_COL + (uint32_t)(iss * NS);
-                bool ok = true;
-                for (int kt = 0; kt < KT; ++kt) {
-                    if (kt % CHUNK_STEPS == 0 && pending) {
-                        if (!tc::mbar_wait(acc_empty, (ev - 1) & 1)) { set_abort(abort_flag, a.status); ok = false; break; }
-                        pending = false;
-                    }
-                    if (!tc::mbar_wait(&b_full[bs], bph) || !tc::mbar_wait(&a_full[as], aph)) {
-                        set_abort(abort_flag, a.status);
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    const uint32_t b0 = tc::smem_u32(sB + bs * B_BYTES);
-                    const uint32_t a0 = tm + A_COL + (uint32_t)(as * 64 + iss * 32);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_f16_ts(dcol, a0 + 8 * kk, tc::sdesc_kmajor_sw128(b0 + 32 * kk), idesc,
-                                       (kt > 0 || kk > 0) ? 1u : 0u);
-                    tc::mma_commit(&b_empty[bs]);
-                    tc::mma_commit(&a_empty[as]);
-                    if (++bs == BS) { bs = 0; bph ^= 1; }
-                    if (++as == AS) { as = 0; aph ^= 1; }
-                    if ((kt + 1) % CHUNK_STEPS == 0 || kt == KT - 1) {
-                        tc::mma_commit(acc_full);
-                        ++ev;
-                        pending = true;
-                    }
+        int bs = 0, as = 0;
+        uint32_t bph = 0, aph = 0, ev = 0;
+        bool pending = false;  // an accumulator event not yet handed back by the epilogue
+        for (int u = blockIdx.x; u < total_units && !warp_flag(abort_flag); u += gridDim.x) {
+            int e, t, half, nb, m0, ntok;
+            decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            if (ntok <= 0) continue;
+            const int nmma = (ntok + 15) & ~15;
+            const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
+            const uint32_t dcol = tm + R_COL + (uint32_t)(iss * NS);
+            bool ok = true;
+            for (int kt = 0; kt < KT; ++kt) {
+                if (kt % CHUNK_STEPS == 0 && pending) {
+                    if (!warp_wait(acc_empty, (ev - 1) & 1, lane)) { ok = false; break; }
+                    pending = false;
                 }
-                if (!ok) break;
+                if (!warp_wait(&b_full[bs], bph, lane) || !warp_wait(&a_full[as], aph, lane)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t b0 = tc::smem_u32(sB + bs * B_BYTES);
+                const uint32_t a0 = tm + A_COL + (uint32_t)(as * A_SLOT_COLS + iss * (KSTEP / 2));
+#pragma unroll
+                for (int kk = 0; kk < KSTEP / 16; ++kk)
+                    tc::mma_f16_ts_elect(dcol, a0 + 8 * kk,
+                                         tc::sdesc_kmajor_sw128(b0 + (kk >> 2) * HALF_B + 32 * (kk & 3)), idesc,
+                                         (kt > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit_elect(&done[bs]);
+                if (++bs == BS) { bs = 0; bph ^= 1; }
+                if (++as == AS) { as = 0; aph ^= 1; }
+                if ((kt + 1) % CHUNK_STEPS == 0 || kt == KT - 1) {
+                    tc::mma_commit_elect(acc_full);
+                    ++ev;
+                    pending = true;
+                }
+            }
+            if (!ok) {
+                if (lane == 0) set_abort(abort_flag, a.status);
+                break;
             }
         }
         __syncwarp();
@@ -299,42 +311,54 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
         const int m = q * 32 + lane;  // weight row within the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int sw = (m >> 1) & 3;  // 64-byte swizzle of the TMA box: 16-byte chunk j at j ^ sw
-        int rs = 0, as = 0;
-        uint32_t rph = 0, aph = 0;
+        int rs = 0;
+        uint32_t rph = 0;
+        uint32_t gs = 0;  // steps converted so far (all units): A slot gs % AS, done barrier gs % BS
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
             decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
             if (ntok <= 0) continue;
-            for (int kt = 0; kt < KT; ++kt) {
-                if (!warp_wait(&raw_full[rs], rph, lane) || !warp_wait(&a_empty[as], aph ^ 1, lane)) {
+            for (int kt = 0; kt < KT; ++kt, ++gs) {
+                if (!warp_wait(&raw_full[rs], rph, lane)) {
                     if (lane == 0) set_abort(abort_flag, a.status);
                     ok = false;
                     break;
                 }
-                const uint8_t* src = sRaw + rs * RAW_BYTES + tile * (128 * KSTEP) + m * KSTEP;
-                uint4 c[4];
+                const uint8_t* src = sRaw + rs * RAW_BYTES + tile * (128 * 64) + m * 64;
+                uint4 c[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const uint4*>(src + ((j ^ sw) << 4));
+                for (int j = 0; j < 8; ++j)
+                    c[j] = *reinterpret_cast<const uint4*>(src + (j >> 2) * HALF_RAW + (((j & 3) ^ sw) << 4));
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
-                const uint32_t wv[16] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w,
-                                         c[2].x, c[2].y, c[2].z, c[2].w, c[3].x, c[3].y, c[3].z, c[3].w};
-                uint32_t o0[16], o1[16];
+                if (++rs == RS) { rs = 0; rph ^= 1; }
+                // 128 int8 values -> 64 fp16 pairs, 16 per TMEM store
+                uint32_t o[4][16];
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    i8x4_to_f16x2(wv[p], o0[2 * p], o0[2 * p + 1]);
-                    i8x4_to_f16x2(wv[8 + p], o1[2 * p], o1[2 * p + 1]);
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t wv[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        i8x4_to_f16x2(wv[p], o[j >> 1][(j & 1) * 8 + 2 * p], o[j >> 1][(j & 1) * 8 + 2 * p + 1]);
                 }
-                const uint32_t ta = tm + lane_base + A_COL + (uint32_t)(as * 64 + tile * 32);
-                tmem_st16(ta, o0);
-                tmem_st16(ta + 16, o1);
+                // the A slot is free once the MMAs of step gs - AS have completed
+                if (gs >= (uint32_t)AS) {
+                    const uint32_t j = gs - AS;
+                    if (!warp_wait(&done[j % BS], (j / BS) & 1u, lane)) {
+                        if (lane == 0) set_abort(abort_flag, a.status);
+                        ok = false;
+                        break;
+                    }
+                }
+                const int as = (int)(gs % AS);
+                const uint32_t ta = tm + lane_base + A_COL + (uint32_t)(as * A_SLOT_COLS + tile * (KSTEP / 2));
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tmem_st16(ta + 16 * q4, o[q4]);
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&a_full[as]);
-                if (++rs == RS) { rs = 0; rph ^= 1; }
-                if (++as == AS) { as = 0; aph ^= 1; }
             }
         }
     } else {
@@ -386,35 +410,35 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                 if (ch < NCH - 1) {
                     // drain: hi parts into the 16-bit running sums, lo back as the accumulator
                     for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
-                        uint32_t g[16], v[16], s[16];
+                        uint32_t g[16], v[16];
                         tmem_ld16(tm + lane_base + R_COL + c0, g);
                         tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
-                        if (ch > 0) tmem_ld16(tm + lane_base + S_COL + c0, s);
                         tc::tmem_ld_wait();
+                        uint32_t* sr = sS + c0 * 128 + n;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             int h0, l0, h1, l1;
                             split_hi_lo(g[j], h0, l0);
                             split_hi_lo(v[j], h1, l1);
                             if (ch > 0) {
-                                h0 += (int)(int16_t)(s[j] & 0xFFFFu);
-                                h1 += (int)(int16_t)(s[j] >> 16);
+                                const uint32_t w = sr[j * 128];
+                                h0 += (int)(int16_t)(w & 0xFFFFu);
+                                h1 += (int)(int16_t)(w >> 16);
                             }
-                            s[j] = (uint32_t)(uint16_t)h0 | ((uint32_t)(uint16_t)h1 << 16);
+                            sr[j * 128] = (uint32_t)(uint16_t)h0 | ((uint32_t)(uint16_t)h1 << 16);
                             g[j] = __float_as_uint((float)l0);
                             v[j] = __float_as_uint((float)l1);
                         }
                         tmem_st16(tm + lane_base + R_COL + c0, g);
                         tmem_st16(tm + lane_base + R_COL + NS + c0, v);
-                        tmem_st16(tm + lane_base + S_COL + c0, s);
                     }
                     tc::tmem_st_wait();
                 } else {
                     for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
-                        uint32_t g[16], v[16], s[16];
+                        uint32_t g[16], v[16];
                         tmem_ld16(tm + lane_base + R_COL + c0, g);
                         tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
-                        if (NCH > 1) tmem_ld16(tm + lane_base + S_COL + c0, s);
+                        const uint32_t* sr = sS + c0 * 128 + n;
                         // the chunk's per-token activation scales, one per lane, broadcast below
                         const float fl = (lane < 16 && c0 + lane < ntok) ? ts[c0 + lane] : 0.f;
                         tc::tmem_ld_wait();
@@ -424,8 +448,9 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                             int a0 = __float2int_rn(__uint_as_float(g[j]));
                             int a1 = __float2int_rn(__uint_as_float(v[j]));
                             if (NCH > 1) {
-                                a0 += (int)(int16_t)(s[j] & 0xFFFFu) * (1 << HI_SHIFT);
-                                a1 += (int)(int16_t)(s[j] >> 16) * (1 << HI_SHIFT);
+                                const uint32_t w = sr[j * 128];
+                                a0 += (int)(int16_t)(w & 0xFFFFu) * (1 << HI_SHIFT);
+                                a1 += (int)(int16_t)(w >> 16) * (1 << HI_SHIFT);
                             }
                             const float fx = __shfl_sync(0xFFFFFFFFu, fl, j);
                             if (j < nv) {
@@ -433,7 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                                 const float r0 = ((float)a0 * fx) * ws0;
                                 const float r1 = ((float)a1 * fx) * ws1;
                                 if (STAGE == 1) {
-                                    a.h[slot * ostride + col0] = silu_mul(r0, r1);
+                                    a.h[slot * ostride + col0] = __fdividef(r0, 1.0f + __expf(-r0)) * r1;
                                 } else {
                                     a.y[slot * ostride + col0] = float_to_bf16_bits(r0);
                                     a.y[slot * ostride + col1] = float_to_bf16_bits(r1);
@@ -465,8 +490,8 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
     }
 }
 
-// Raw int8 weights viewed through a TMA map with 64-byte rows (64 K elements)
-// and the 64-byte swizzle.  Stage 1: {H, I, 2E} (gate rows of expert e are
+// Raw int8 weights viewed through a TMA map with 64-byte rows (64 K elements,
+// half a step) and the 64-byte swizzle.  Stage 1: {H, I, 2E} (gate rows of expert e are
 // plane 2e, its up rows plane 2e+1), box {64, 128, 2}: a gate tile and its up
 // partner.  Stage 2: {I, E*H}, box {64, 256}: two adjacent row tiles.
 static int make_w_map(CUtensorMap* map, const void* w, const qmoe_dims* d, int stage) {
@@ -476,7 +501,7 @@ static int make_w_map(CUtensorMap* map, const void* w, const qmoe_dims* d, int s
     if (stage == 1) {
         cuuint64_t gdim[3] = {(cuuint64_t)d->H, (cuuint64_t)d->I, (cuuint64_t)(2 * d->E)};
         cuuint64_t gstride[2] = {(cuuint64_t)d->H, (cuuint64_t)d->I * (cuuint64_t)d->H};
-        cuuint32_t box[3] = {KSTEP, 128, 2};
+        cuuint32_t box[3] = {64, 128, 2};
         cuuint32_t estr[3] = {1, 1, 1};
         r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w), gdim, gstride, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -484,7 +509,7 @@ static int make_w_map(CUtensorMap* map, const void* w, const qmoe_dims* d, int s
     } else {
         cuuint64_t gdim[2] = {(cuuint64_t)d->I, (cuuint64_t)d->E * (cuuint64_t)d->H};
         cuuint64_t gstride[1] = {(cuuint64_t)d->I};
-        cuuint32_t box[2] = {KSTEP, 256};
+        cuuint32_t box[2] = {64, 256};
         cuuint32_t estr[2] = {1, 1};
         r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), gdim, gstride, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
