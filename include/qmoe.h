@@ -215,10 +215,14 @@ int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t*
 /* W8A8 activation tiles -- the layout in which the W8A8 GEMMs take their
  * activations: the blocks of the W4A16 tiles above (same NMAX, tile_start,
  * 128-byte rows of 64 fp16 values, chunk swizzle), each value the fp16 equal
- * to an int8 code (exact), then a per-row tail of one fp32 scale s at
- * (t*NMAX + r).  Rows past a tile's token count are unspecified.
+ * to an int8 code (exact); then a per-row tail of one fp32 scale s at
+ * (t*NMAX + r); then, for each 112-row half h of a tile (NMAX/112 halves)
+ * and each 128-element K step j, the int32 max over the half's rows of
+ * sum |code| over the step, at ((t*(NMAX/112) + h) * K/128 + j): the GEMMs
+ * bound their partial sums with it.  Rows past a tile's token count are
+ * unspecified.
  * qmoe_w8a8_tiles_bytes -- bytes of such a buffer for dims *d and length K
- * (K % 64 == 0; 0 otherwise). */
+ * (K % 128 == 0 and K <= 16384; 0 otherwise). */
 size_t qmoe_w8a8_tiles_bytes(const qmoe_dims* d, int64_t K);
 
 /* qmoe_permute_quant_int8 -- the expert-sorted permutation of the routed
@@ -226,8 +230,8 @@ size_t qmoe_w8a8_tiles_bytes(const qmoe_dims* d, int64_t K);
  * qmoe_quant_rows_int8_bf16 applied to each token row of x_bf16 [T, H]) in
  * one pass: slot s gets the codes of token sorted_pair_ids[s] / k and its
  * scale, written as W8A8 tiles with K = H ([gfx1151] Constraint: W8A8 needs
- * quantised activations).  H % 64 == 0.  ws = the workspace qmoe_align_sort
- * filled for this routing. */
+ * quantised activations).  H % 128 == 0, H <= 16384.  ws = the workspace
+ * qmoe_align_sort filled for this routing. */
 int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
                             const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                             qmoe_stream_t stream);
@@ -235,7 +239,7 @@ int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf16, const in
 /* qmoe_quant_tiles_int8_f32 -- the W8A8 intermediate quantisation: each slot
  * row of h_f32 [P, I] (slot order, from qmoe_gemm1_swiglu_w8a8) quantised
  * with the rule of qmoe_quant_rows_int8_f32 and written as W8A8 tiles with
- * K = I.  I % 64 == 0.  ws as above. */
+ * K = I.  I % 128 == 0, I <= 16384.  ws as above. */
 int qmoe_quant_tiles_int8_f32(const qmoe_dims* d, const float* h_f32, const int32_t* offsets, uint8_t* h_tiles,
                               const void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
@@ -324,11 +328,12 @@ int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tiles, const ui
  *        w1 int8 [E, 2I, H] (row-major, as given; 16-byte aligned);
  *        w1_s fp32 [E, 2I].  The int8 x int8 products are summed exactly in
  *        int32 ([gfx1151] Constraint): the tensor cores take the codes as
- *        exact fp16 values, accumulate at most 1024 products in fp32 (exact
- *        integers below 2^24) and the epilogue carries the sum on in
- *        integers.  g = ((float)acc * s_x) * w1_s[e][n] in fp32, likewise u;
- *        out h fp32 [P, I] in slot order; dbg_acc (nullable, 16-byte
- *        aligned) int32 [P, 2I] receives the exact gate/up sums. */
+ *        exact fp16 values and accumulate in fp32, and the epilogue carries
+ *        the sum on in integers whenever the tiles' step maxima say a fp32
+ *        partial sum could otherwise reach 2^24.  g = ((float)acc * s_x) *
+ *        w1_s[e][n] in fp32, likewise u; out h fp32 [P, I] in slot order;
+ *        dbg_acc (nullable, 16-byte aligned) int32 [P, 2I] receives the exact
+ *        gate/up sums. */
 int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, const float* w1_s,
                            const int32_t* offsets, float* h, int32_t* dbg_acc, int32_t* dev_status, void* ws,
                            size_t ws_bytes, qmoe_stream_t stream);

@@ -151,9 +151,10 @@ extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h_tiles, cons
 // ------------------------------------------------------------------ W8A8 (exact int32 sums on fp16 tensor cores)
 
 extern "C" size_t qmoe_w8a8_tiles_bytes(const qmoe_dims* d, int64_t K) {
-    if (!dims_ok(d) || K <= 0 || K % 64 != 0) return 0;
+    if (!dims_ok(d) || K <= 0 || K % 128 != 0 || K > 16384) return 0;
     const int nmax = mxt::nmax_for(d);
-    return (size_t)(bft::blocks_bytes(d, K) + mxt::max_tiles(d, nmax) * nmax * 4);
+    const int64_t tiles = mxt::max_tiles(d, nmax);
+    return (size_t)(bft::blocks_bytes(d, K) + tiles * nmax * 4 + tiles * (nmax / 112) * (K / 128) * 4);
 }
 
 extern "C" int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
@@ -162,7 +163,7 @@ extern "C" int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf1
     int rc = gemm_args_ok(d, {x_bf16, sorted_pair_ids, offsets, x_tiles});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
-    if (d->H % 64 != 0) return QMOE_ERR_UNSUPPORTED;
+    if (d->H % 128 != 0 || d->H > 16384) return QMOE_ERR_UNSUPPORTED;
     return quant_tiles_int8_launch(d, d->H, x_bf16, true, sorted_pair_ids, offsets,
                                    tile_schedule_in(const_cast<void*>(ws), d), x_tiles, (cudaStream_t)stream);
 }
@@ -172,7 +173,7 @@ extern "C" int qmoe_quant_tiles_int8_f32(const qmoe_dims* d, const float* h_f32,
     int rc = gemm_args_ok(d, {h_f32, offsets, h_tiles});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
-    if (d->I % 64 != 0) return QMOE_ERR_UNSUPPORTED;
+    if (d->I % 128 != 0 || d->I > 16384) return QMOE_ERR_UNSUPPORTED;
     return quant_tiles_int8_launch(d, d->I, h_f32, false, nullptr, offsets,
                                    tile_schedule_in(const_cast<void*>(ws), d), h_tiles, (cudaStream_t)stream);
 }

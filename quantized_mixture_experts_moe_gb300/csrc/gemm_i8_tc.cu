@@ -7,25 +7,28 @@
 // sm_103a has no integer tcgen05 MMA in this toolkit, so the products run as
 // kind::f16 MMAs on fp16 operands that hold the int8 values exactly (every
 // integer in [-128, 127] is an fp16), with fp32 accumulation in TMEM.  A
-// product is at most 127^2 = 16129; 1024 of them stay below 2^24, so a fp32
-// sum over at most 1024 K elements is an exact integer.  The accumulator is
-// therefore drained every 1024 K elements: the epilogue splits the exact fp32
-// value v into hi * 2^13 + lo with |lo| <= 4096, adds hi to a 16-bit running
-// sum kept in shared memory and writes lo back as the fp32 accumulator, on which the
-// next 1024 K elements accumulate (|lo| + 1024 * 16129 < 2^24, exact again).
-// At the end acc = hi * 2^13 + v, the exact int32 sum, for K <= 16384
-// (|hi| <= 16384 * 16129 / 2^13 < 2^15).
+// product is at most 128 * 127 in magnitude, and a fp32 sum stays an exact
+// integer while it is below 2^24.  The accumulator is therefore drained
+// before that bound can be reached: the tile kernel records, per 128-element
+// K step, the largest sum |x| over a sub-tile's rows, and the GEMM closes a
+// chunk of steps whenever 128 * (the chunk's summed maxima) could pass
+// 2^24 - 4096 (at most every 1024 K elements, usually far less often).  The
+// epilogue splits the exact fp32 value v into hi * 2^13 + lo with |lo| <=
+// 4096, adds hi to a 16-bit running sum kept in shared memory and writes lo
+// back as the fp32 accumulator, on which the next chunk accumulates.  At the
+// end acc = hi * 2^13 + v, the exact int32 sum, for K <= 16384
+// (|hi| <= 16384 * 128 * 127 / 2^13 < 2^15).
 //
 //   stage 1: g = ((float)acc_g * s_x) * s_w,  u likewise,  h = silu(g) * u  (fp32)
 //   stage 2: y = ((float)acc * s_h) * s_w                                 (bf16)
 //
 // Structure (one persistent CTA per SM, 20 warps), swap-AB as in the other
 // grouped GEMMs (weights are the MMA's M = 128 rows, tokens its N):
-//   warp 0      weight producer: one TMA box per step brings the raw int8
-//               rows of both weight tiles (stage 1: a gate tile and its up
-//               partner; stage 2: two adjacent W2 row tiles), 64 K elements
-//               each, 64-byte swizzled.
-//   warp 1      activation producer: one bulk copy per step of the step's
+//   warp 0      weight producer: two TMA boxes per 128-element step bring the
+//               raw int8 rows of both weight tiles (stage 1: a gate tile and
+//               its up partner; stage 2: two adjacent W2 row tiles), 64 K
+//               elements per box, 64-byte swizzled.
+//   warp 1      activation producer: two bulk copies per step of the step's
 //               fp16 token rows, already 128-byte swizzled by the tile kernel.
 //   warps 2-3   MMA issuers, one per weight tile: A (the weight tile) from
 //               TMEM, B (tokens) from shared memory, N = tokens rounded to 16.
@@ -48,7 +51,10 @@ constexpr int WARP_EPI0 = 12, EPI_WARPS = 8;
 constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
 constexpr int KSTEP = 128;       // K elements per step (two 64-element halves)
 constexpr int NS = 112;          // tokens per MMA (a schedule tile of 224 is two of these)
-constexpr int CHUNK_STEPS = 8;   // steps between drains: 1024 K elements
+// Drains keep every fp32 partial sum below 2^24: a chunk of steps may add at
+// most L1_BOUND * 128 (|w| <= 128 for int8 weights, sum |x| over the chunk's
+// steps <= L1_BOUND for every row) on top of a remainder |lo| <= 4096.
+constexpr int L1_BOUND = ((1 << 24) - 4097) / 128;
 constexpr int HI_SHIFT = 13;
 constexpr int MAX_E = 512;
 constexpr int MAX_K = 16384;
@@ -92,6 +98,7 @@ struct Args {
     const int32_t* tile_start;
     float* h;                 // stage 1 output, fp32 [P, I] in slot order
     uint16_t* y;              // stage 2 output, bf16 [P, H] in slot order
+    const int32_t* l1max;     // per (sub-tile, step): the largest sum |x| over the sub-tile's rows
     int32_t* dbg_acc;         // optional exact sums: [P, 2I] (stage 1) or [P, H] (stage 2)
     int32_t* status;
 };
@@ -154,6 +161,32 @@ __device__ __forceinline__ void split_hi_lo(uint32_t vbits, int& hi, int& lo) {
     lo = v - hi * (1 << HI_SHIFT);
 }
 
+// A unit's chunk starts (warp-uniform; every lane of the warp calls it): bit
+// kt set when a new chunk, and so a drain before it, starts at step kt > 0.
+// Chunks are grown greedily while the sum of the per-step L1 maxima stays
+// within L1_BOUND, which bounds every partial sum of every row of the unit.
+__device__ __forceinline__ void chunk_starts(const int32_t* l1, int KT, int lane, uint32_t (&starts)[4]) {
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        starts[i] = 0;
+        const int v = (32 * i + lane < KT) ? l1[32 * i + lane] : 0;
+        for (int k2 = 0; k2 < 32 && 32 * i + k2 < KT; ++k2) {
+            const int m = __shfl_sync(0xFFFFFFFFu, v, k2);
+            if (run > 0 && run + m > L1_BOUND) {
+                starts[i] |= 1u << k2;
+                run = 0;
+            }
+            run += m;
+        }
+    }
+}
+
+__device__ __forceinline__ bool bit_at(const uint32_t (&b)[4], int kt) {
+    const uint32_t w = (kt < 32) ? b[0] : (kt < 64) ? b[1] : (kt < 96) ? b[2] : b[3];
+    return kt < 128 && ((w >> (kt & 31)) & 1u);
+}
+
 template <int STAGE>
 __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const Args a) {
     extern __shared__ uint8_t smem_raw[];
@@ -177,7 +210,6 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
     const int K = (STAGE == 1) ? a.H : a.I;
     const int NB = (STAGE == 1) ? a.I / 128 : a.H / 256;
     const int KT = K / KSTEP;
-    const int NCH = (KT + CHUNK_STEPS - 1) / CHUNK_STEPS;
     const int halves = a.nmax / NS;
 
     for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = a.tile_start[i];
@@ -275,9 +307,11 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
             const int nmma = (ntok + 15) & ~15;
             const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
             const uint32_t dcol = tm + R_COL + (uint32_t)(iss * NS);
+            uint32_t starts[4];
+            chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
             bool ok = true;
             for (int kt = 0; kt < KT; ++kt) {
-                if (kt % CHUNK_STEPS == 0 && pending) {
+                if (pending) {
                     if (!warp_wait(acc_empty, (ev - 1) & 1, lane)) { ok = false; break; }
                     pending = false;
                 }
@@ -293,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                 tc::mma_commit_elect(&done[bs]);
                 if (++bs == BS) { bs = 0; bph ^= 1; }
                 if (++as == AS) { as = 0; aph ^= 1; }
-                if ((kt + 1) % CHUNK_STEPS == 0 || kt == KT - 1) {
+                if (kt == KT - 1 || bit_at(starts, kt + 1)) {
                     tc::mma_commit_elect(acc_full);
                     ++ev;
                     pending = true;
@@ -396,7 +430,19 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                 dcol1 = col1;
                 dstride = a.H;
             }
-            for (int ch = 0; ch < NCH; ++ch, ++ev) {
+            uint32_t starts[4];
+            chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
+            const int nev = 1 + __popc(starts[0]) + __popc(starts[1]) + __popc(starts[2]) + __popc(starts[3]);
+            // this warp's per-token activation scales (chunk i: token 16 * eh + 32 * i + lane, lanes < 16),
+            // fetched before the accumulator is ready
+            float fls[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = 16 * eh + 32 * i + lane;
+                fls[i] = (lane < 16 && c < ntok) ? ts[c] : 0.f;
+            }
+            bool last_final = false;
+            for (int ch = 0; ch < nev; ++ch, ++ev) {
                 int w = 1;
                 if (lane == 0) w = tc::mbar_wait(acc_full, ev & 1) ? 1 : 0;
                 w = __shfl_sync(0xFFFFFFFFu, w, 0);
@@ -407,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                     break;
                 }
                 tc::tc_fence_after();
-                if (ch < NCH - 1) {
+                if (ch < nev - 1) {
                     // drain: hi parts into the 16-bit running sums, lo back as the accumulator
                     for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
                         uint32_t g[16], v[16];
@@ -415,16 +461,23 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                         tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
                         tc::tmem_ld_wait();
                         uint32_t* sr = sS + c0 * 128 + n;
+                        // the high parts so far (none before the first drain), then this chunk's added;
+                        // the branch stays outside the unrolled loops so their 16 chains interleave
+                        uint32_t sw[16];
+                        if (ch > 0) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) sw[j] = sr[j * 128];
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) sw[j] = 0;
+                        }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             int h0, l0, h1, l1;
                             split_hi_lo(g[j], h0, l0);
                             split_hi_lo(v[j], h1, l1);
-                            if (ch > 0) {
-                                const uint32_t w = sr[j * 128];
-                                h0 += (int)(int16_t)(w & 0xFFFFu);
-                                h1 += (int)(int16_t)(w >> 16);
-                            }
+                            h0 += (int)(int16_t)(sw[j] & 0xFFFFu);
+                            h1 += (int)(int16_t)(sw[j] >> 16);
                             sr[j * 128] = (uint32_t)(uint16_t)h0 | ((uint32_t)(uint16_t)h1 << 16);
                             g[j] = __float_as_uint((float)l0);
                             v[j] = __float_as_uint((float)l1);
@@ -434,46 +487,79 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                     }
                     tc::tmem_st_wait();
                 } else {
-                    for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
+                    // final, first pass: the outputs into this thread's shared-memory words (where the
+                    // running high parts were), so the accumulator can be handed back before the stores
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c0 = 16 * eh + 32 * i;
+                        if (c0 >= ntok) break;
                         uint32_t g[16], v[16];
                         tmem_ld16(tm + lane_base + R_COL + c0, g);
                         tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
-                        const uint32_t* sr = sS + c0 * 128 + n;
-                        // the chunk's per-token activation scales, one per lane, broadcast below
-                        const float fl = (lane < 16 && c0 + lane < ntok) ? ts[c0 + lane] : 0.f;
+                        uint32_t* sr = sS + c0 * 128 + n;
+                        const float fl = fls[i];
                         tc::tmem_ld_wait();
-                        const int nv = min(16, ntok - c0);
+                        // high parts from the drains (none when there were none), as floats
+                        float hf0[16], hf1[16];
+                        if (nev > 1) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            int a0 = __float2int_rn(__uint_as_float(g[j]));
-                            int a1 = __float2int_rn(__uint_as_float(v[j]));
-                            if (NCH > 1) {
+                            for (int j = 0; j < 16; ++j) {
                                 const uint32_t w = sr[j * 128];
-                                a0 += (int)(int16_t)(w & 0xFFFFu) * (1 << HI_SHIFT);
-                                a1 += (int)(int16_t)(w >> 16) * (1 << HI_SHIFT);
+                                hf0[j] = (float)(int16_t)(w & 0xFFFFu);
+                                hf1[j] = (float)(int16_t)(w >> 16);
                             }
-                            const float fx = __shfl_sync(0xFFFFFFFFu, fl, j);
-                            if (j < nv) {
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) hf0[j] = hf1[j] = 0.f;
+                        }
+                        if (a.dbg_acc) {
+                            const int nv = min(16, ntok - c0);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                if (j >= nv) break;
                                 const int64_t slot = m0 + c0 + j;
-                                const float r0 = ((float)a0 * fx) * ws0;
-                                const float r1 = ((float)a1 * fx) * ws1;
-                                if (STAGE == 1) {
-                                    a.h[slot * ostride + col0] = __fdividef(r0, 1.0f + __expf(-r0)) * r1;
-                                } else {
-                                    a.y[slot * ostride + col0] = float_to_bf16_bits(r0);
-                                    a.y[slot * ostride + col1] = float_to_bf16_bits(r1);
-                                }
-                                if (a.dbg_acc) {
-                                    a.dbg_acc[slot * dstride + dcol0] = a0;
-                                    a.dbg_acc[slot * dstride + dcol1] = a1;
-                                }
+                                a.dbg_acc[slot * dstride + dcol0] =
+                                    (int)hf0[j] * (1 << HI_SHIFT) + __float2int_rn(__uint_as_float(g[j]));
+                                a.dbg_acc[slot * dstride + dcol1] =
+                                    (int)hf1[j] * (1 << HI_SHIFT) + __float2int_rn(__uint_as_float(v[j]));
                             }
                         }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            // (float) of the exact sum hi * 2^13 + v: the fma rounds the exact value once
+                            const float f0 = __fmaf_rn(hf0[j], (float)(1 << HI_SHIFT), __uint_as_float(g[j]));
+                            const float f1 = __fmaf_rn(hf1[j], (float)(1 << HI_SHIFT), __uint_as_float(v[j]));
+                            const float fx = __shfl_sync(0xFFFFFFFFu, fl, j);
+                            const float r0 = (f0 * fx) * ws0;
+                            const float r1 = (f1 * fx) * ws1;
+                            if (STAGE == 1)
+                                sr[j * 128] = __float_as_uint(__fdividef(r0, 1.0f + __expf(-r0)) * r1);
+                            else
+                                sr[j * 128] = (uint32_t)float_to_bf16_bits(r0) | ((uint32_t)float_to_bf16_bits(r1) << 16);
+                        }
                     }
+                    last_final = true;
                 }
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(acc_empty);
+            }
+            if (last_final) {
+                // final, second pass: shared memory -> outputs, overlapping the next unit's MMAs
+                for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
+                    const uint32_t* sr = sS + c0 * 128 + n;
+                    const int nv = min(16, ntok - c0);
+                    for (int j = 0; j < nv; ++j) {
+                        const int64_t slot = m0 + c0 + j;
+                        const uint32_t w = sr[j * 128];
+                        if (STAGE == 1) {
+                            a.h[slot * ostride + col0] = __uint_as_float(w);
+                        } else {
+                            a.y[slot * ostride + col0] = (uint16_t)(w & 0xFFFFu);
+                            a.y[slot * ostride + col1] = (uint16_t)(w >> 16);
+                        }
+                    }
+                }
             }
         }
     }
@@ -553,6 +639,8 @@ int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, co
     a.nmax = mxt::nmax_for(d);
     a.act = x_tiles;
     a.act_scale = reinterpret_cast<const float*>(x_tiles + bft::blocks_bytes(d, d->H));
+    a.l1max = reinterpret_cast<const int32_t*>(x_tiles + bft::blocks_bytes(d, d->H) +
+                                               mxt::max_tiles(d, a.nmax) * a.nmax * 4);
     a.w_scale = w1_s;
     a.offsets = offsets; a.tile_start = tile_start;
     a.h = h; a.dbg_acc = dbg_acc; a.status = status;
@@ -570,6 +658,8 @@ int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, co
     a.nmax = mxt::nmax_for(d);
     a.act = h_tiles;
     a.act_scale = reinterpret_cast<const float*>(h_tiles + bft::blocks_bytes(d, d->I));
+    a.l1max = reinterpret_cast<const int32_t*>(h_tiles + bft::blocks_bytes(d, d->I) +
+                                               mxt::max_tiles(d, a.nmax) * a.nmax * 4);
     a.w_scale = w2_s;
     a.offsets = offsets; a.tile_start = tile_start;
     a.y = y; a.dbg_acc = dbg_acc; a.status = status;

@@ -250,12 +250,19 @@ int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* s
     return launch_status();
 }
 
-// W8A8 activation tiles: one warp per expert-sorted slot.  The slot's row
-// (stage 1: its token's bf16 x row; stage 2: its own fp32 h row) is quantised
+// W8A8 activation tiles: one CTA per 112-row sub-tile (a schedule tile of
+// 224 rows is two of them), one warp per row at a time.  The row (stage 1: the
+// slot's token row of bf16 x; stage 2: the slot's own fp32 h row) is quantised
 // with the per-row int8 rule of quant_rows_int8_kernel (s = amax / 127, IEEE
 // division, nearest-even, clamped to +-127) and each code is written as the
 // fp16 value equal to it (exact) into the 128-byte-swizzled tile layout the
 // W4A16 x tiles use, 8 codes per 16-byte chunk; s goes to the per-row tail.
+// The CTA also records, for every 128-element K step, the largest L1 norm
+// sum |q| over its rows: the GEMM uses it to bound its fp32 partial sums.
+constexpr int kTqWarps = 16;
+constexpr int kTqSub = 112;
+constexpr int kTqMaxSteps = 128;  // K <= 16384
+
 __device__ __forceinline__ void load8_as_float(const uint16_t* p, float (&f)[8]) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -273,57 +280,81 @@ __device__ __forceinline__ void load8_as_float(const float* p, float (&f)[8]) {
 }
 
 template <typename In, bool PERMUTE>
-__global__ void __launch_bounds__(kPqWarps * 32)
+__global__ void __launch_bounds__(kTqWarps * 32)
 quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
-                        int K, int nmax, int64_t P, int64_t tail_off, uint8_t* __restrict__ tiles) {
-    const int lane = threadIdx.x & 31;
-    const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
-    int tile = -1, row = 0;
-    int64_t src = 0;
-    if (lane == 0 && slot < P && slot < offsets[E]) {
-        int lo = 0, hi = E;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (offsets[mid] <= slot) lo = mid; else hi = mid;
+                        int K, int nmax, int64_t tail_off, int64_t l1_off, uint8_t* __restrict__ tiles) {
+    __shared__ int s_l1[kTqMaxSteps];
+    __shared__ int s_info[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int halves = nmax / kTqSub;
+    const int t = blockIdx.x / halves, half = blockIdx.x - t * halves;
+    const int KT = K / 128;
+    for (int i = threadIdx.x; i < KT; i += blockDim.x) s_l1[i] = 0;
+    if (threadIdx.x == 0) {
+        s_info[1] = 0;
+        if (t < tile_start[E]) {
+            int lo = 0, hi = E;  // the expert whose tiles contain t
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (tile_start[mid] <= t) lo = mid; else hi = mid;
+            }
+            const int m0 = offsets[lo] + (t - tile_start[lo]) * nmax + half * kTqSub;
+            s_info[0] = m0;
+            s_info[1] = max(0, min(kTqSub, offsets[lo + 1] - m0));
         }
-        const int local = (int)(slot - offsets[lo]);
-        tile = tile_start[lo] + local / nmax;
-        row = local % nmax;
-        src = PERMUTE ? (int64_t)(sorted_pair_ids[slot] / k) : slot;
     }
-    tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
-    if (tile < 0) return;
-    row = __shfl_sync(0xFFFFFFFFu, row, 0);
-    src = __shfl_sync(0xFFFFFFFFu, src, 0);
-    const In* xr = x + src * K;
-    float amax = 0.f;
-    for (int j = lane; j < K / 8; j += 32) {
-        float f[8];
-        load8_as_float(xr + 8 * j, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+    __syncthreads();
+    const int m0 = s_info[0], n = s_info[1];
+    if (n == 0) return;
     const int64_t bb = bft::block_bytes(nmax);
-    uint8_t* tbase = tiles + (int64_t)tile * (K / 64) * bb;
-    for (int j = lane; j < K / 8; j += 32) {  // chunk j: K step j/8, chunk j%8 of the 128-byte row
-        float f[8];
-        load8_as_float(xr + 8 * j, f);
-        uint32_t o[4];
+    uint8_t* tbase = tiles + (int64_t)t * (K / 64) * bb;
+    for (int r = warp; r < n; r += kTqWarps) {
+        const int64_t slot = m0 + r;
+        const int row = half * kTqSub + r;  // row within the schedule tile
+        const int64_t src = PERMUTE ? (int64_t)(sorted_pair_ids[slot] / k) : slot;
+        const In* xr = x + src * K;
+        float amax = 0.f;
+        for (int j = lane; j < K / 8; j += 32) {
+            float f[8];
+            load8_as_float(xr + 8 * j, f);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float q0 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i], sc)), -127.f), 127.f);
-            const float q1 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i + 1], sc)), -127.f), 127.f);
-            const __half2 hv = __floats2half2_rn(q0, q1);
-            o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
         }
-        uint8_t* blk = tbase + (int64_t)(j >> 3) * bb;
-        *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+        // chunk j (8 codes): K step j/8 of 64 (block), chunk j%8 of its 128-byte row; 128-element step j/16
+        for (int j0 = 0; j0 < K / 8; j0 += 32) {  // warp-uniform trip count (the shuffles below)
+            const int j = j0 + lane;
+            int l1 = 0;
+            if (j < K / 8) {
+                float f[8];
+                load8_as_float(xr + 8 * j, f);
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float q0 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i], sc)), -127.f), 127.f);
+                    const float q1 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i + 1], sc)), -127.f), 127.f);
+                    l1 += abs((int)q0) + abs((int)q1);
+                    const __half2 hv = __floats2half2_rn(q0, q1);
+                    o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                }
+                uint8_t* blk = tbase + (int64_t)(j >> 3) * bb;
+                *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            // lanes 0-15 hold step j0/16, lanes 16-31 step j0/16 + 1
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+            const int step = (j0 >> 4) + (lane >> 4);
+            if ((lane & 15) == 0 && step < KT) atomicMax(&s_l1[step], l1);
+        }
+        if (lane == 0) reinterpret_cast<float*>(tiles + tail_off)[(int64_t)t * nmax + row] = sc;
     }
-    if (lane == 0) reinterpret_cast<float*>(tiles + tail_off)[(int64_t)tile * nmax + row] = sc;
+    __syncthreads();
+    int* l1 = reinterpret_cast<int*>(tiles + l1_off) + ((int64_t)t * halves + half) * KT;
+    for (int i = threadIdx.x; i < KT; i += blockDim.x) l1[i] = s_l1[i];
 }
 
 int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool from_bf16_tokens,
@@ -331,15 +362,17 @@ int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool f
                             cudaStream_t st) {
     const int64_t P = (int64_t)d->T * d->k;
     if (P == 0) return QMOE_OK;
-    const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
+    if (K % 128 != 0 || K / 128 > kTqMaxSteps) return QMOE_ERR_UNSUPPORTED;
     const int nmax = mxt::nmax_for(d);
+    const int64_t blocks = mxt::max_tiles(d, nmax) * (nmax / kTqSub);
     const int64_t tail = bft::blocks_bytes(d, K);
+    const int64_t l1 = tail + mxt::max_tiles(d, nmax) * nmax * 4;
     if (from_bf16_tokens)
-        quant_tiles_int8_kernel<uint16_t, true><<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(
-            static_cast<const uint16_t*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, P, tail, tiles);
+        quant_tiles_int8_kernel<uint16_t, true><<<(unsigned)blocks, kTqWarps * 32, 0, st>>>(
+            static_cast<const uint16_t*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail, l1, tiles);
     else
-        quant_tiles_int8_kernel<float, false><<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(
-            static_cast<const float*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, P, tail, tiles);
+        quant_tiles_int8_kernel<float, false><<<(unsigned)blocks, kTqWarps * 32, 0, st>>>(
+            static_cast<const float*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail, l1, tiles);
     return launch_status();
 }
 

@@ -120,8 +120,10 @@ def run_layer(w, inp, keep=False):
         else:
             nmax = tile_nmax(T, k, E)
             nt = max_tiles(P, E, nmax)
-            r["xq"], r["xs"] = unpack_i8_tiles(r.pop("ixt"), r["offsets"], nmax, H, nt)
-            r["hq"], r["hs"] = unpack_i8_tiles(r.pop("iht"), r["offsets"], nmax, I, nt)
+            xt, ht = r.pop("ixt"), r.pop("iht")
+            r["xq"], r["xs"] = unpack_i8_tiles(xt, r["offsets"], nmax, H, nt)
+            r["hq"], r["hs"] = unpack_i8_tiles(ht, r["offsets"], nmax, I, nt)
+            r["x_l1"], r["h_l1"] = unpack_i8_l1max(xt, nmax, H, nt), unpack_i8_l1max(ht, nmax, I, nt)
     return r
 
 
@@ -241,12 +243,14 @@ def unpack_i8_tiles(buf, offsets, nmax, K, ntiles):
     vals = _gather16(buf, _w4_layout(nmax, K, t, r)).view(np.float16).astype(np.float64)
     q = vals.astype(np.int64)
     assert np.array_equal(q, vals) and np.abs(q).max(initial=0) <= 127, "tile values are not int8 codes"
-    tail = buf[ntiles * (K // 64) * nmax * 128:].view(np.float32)
+    tail_off = ntiles * (K // 64) * nmax * 128
+    tail = buf[tail_off:tail_off + ntiles * nmax * 4].view(np.float32)
     return q.astype(np.int8), tail[t * nmax + r]
 
 
 def pack_i8_tiles(codes, scales, offsets, nmax, K, nbytes, ntiles):
-    """Slot-order int8 codes [P_valid, K] + scales [P_valid] -> a W8A8 tile buffer of nbytes."""
+    """Slot-order int8 codes [P_valid, K] + scales [P_valid] -> a W8A8 tile buffer of nbytes, with the
+    per-(112-row half, 128-element step) maxima of sum |code| the layout in include/qmoe.h states."""
     buf = np.zeros(nbytes, np.uint8)
     slots = np.arange(offsets[-1])
     t, r = _tile_index(offsets, nmax, slots)
@@ -254,6 +258,25 @@ def pack_i8_tiles(codes, scales, offsets, nmax, K, nbytes, ntiles):
     v = codes[:len(slots)].astype(np.float16).view(np.uint16)
     buf[off] = (v & 0xFF).astype(np.uint8)
     buf[off + 1] = (v >> 8).astype(np.uint8)
-    tail = buf[ntiles * (K // 64) * nmax * 128:].view(np.float32)
+    tail_off = ntiles * (K // 64) * nmax * 128
+    tail = buf[tail_off:tail_off + ntiles * nmax * 4].view(np.float32)
     tail[t * nmax + r] = scales[:len(slots)]
+    l1 = i8_step_l1max(codes[:len(slots)], t, r, nmax, K, ntiles)
+    buf[tail_off + ntiles * nmax * 4:tail_off + ntiles * nmax * 4 + l1.size * 4] = l1.view(np.uint8)
     return buf
+
+
+def i8_step_l1max(codes, t, r, nmax, K, ntiles):
+    """int32 [ntiles * nmax/112 * K/128]: per (tile, 112-row half, 128-element step), the max over the
+    half's rows of sum |code| over the step."""
+    halves = nmax // 112
+    steps = np.abs(codes.astype(np.int64)).reshape(len(codes), K // 128, 128).sum(axis=2)
+    out = np.zeros((ntiles * halves, K // 128), np.int64)
+    np.maximum.at(out, t * halves + r // 112, steps)
+    return out.astype(np.int32).ravel()
+
+
+def unpack_i8_l1max(buf, nmax, K, ntiles):
+    off = ntiles * (K // 64) * nmax * 128 + ntiles * nmax * 4
+    n = ntiles * (nmax // 112) * (K // 128)
+    return buf[off:off + 4 * n].view(np.int32)

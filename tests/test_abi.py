@@ -95,10 +95,12 @@ def test_w8a8_host_checks(lib):
     null = None
     ok = ctypes.c_void_p(0x1000)
     big = 1 << 30
-    # W8A8 tiles: the W4A16 block layout (9 tiles, K/64 steps of 112 rows x 128 bytes) + one fp32 scale per row
-    assert qb.w8a8_tiles_bytes(d, 256) == 9 * 4 * 112 * 128 + 9 * 112 * 4
-    assert qb.w8a8_tiles_bytes(d, 128) == 9 * 2 * 112 * 128 + 9 * 112 * 4
-    assert qb.w8a8_tiles_bytes(d, 96) == 0
+    # W8A8 tiles: the W4A16 block layout (9 tiles, K/64 steps of 112 rows x 128 bytes), one fp32 scale per
+    # row, one int32 step maximum per (112-row half, 128-element step)
+    assert qb.w8a8_tiles_bytes(d, 256) == 9 * 4 * 112 * 128 + 9 * 112 * 4 + 9 * 1 * 2 * 4
+    assert qb.w8a8_tiles_bytes(d, 128) == 9 * 2 * 112 * 128 + 9 * 112 * 4 + 9 * 1 * 1 * 4
+    assert qb.w8a8_tiles_bytes(d, 96) == 0 and qb.w8a8_tiles_bytes(d, 192) == 0
+    assert qb.w8a8_tiles_bytes(d, 16512) == 0
     # null pointers -> QMOE_ERR_ARG before any launch
     assert lib.qmoe_permute_quant_int8(ctypes.byref(d), null, ok, ok, ok, ok, big, null) == -1
     assert lib.qmoe_quant_tiles_int8_f32(ctypes.byref(d), ok, null, ok, ok, big, null) == -1

@@ -182,6 +182,14 @@ def test_stage1_against_oracle(w):
         # the intermediate codes follow the int8 rule on the kernel's own fp32 h
         hq, hs = oracle.int8_quant(g["h"].astype(np.float32))
         assert np.array_equal(g["hq"], hq) and np.array_equal(g["hs"], hs)
+        # the tiles' per-(half tile, 128-step) maxima of sum |code|, which bound the GEMMs' fp32 partial sums
+        nmax = gp.tile_nmax(w.T, w.k, w.E)
+        nt = gp.max_tiles(w.P, w.E, nmax)
+        t, r = gp._tile_index(g["offsets"], nmax, np.arange(g["offsets"][-1]))
+        used = np.unique(t * (nmax // 112) + r // 112)
+        for key, codes, K in (("x_l1", g["xq"], w.H), ("h_l1", g["hq"], w.I)):
+            ref = gp.i8_step_l1max(codes, t, r, nmax, K, nt).reshape(-1, K // 128)
+            assert np.array_equal(g[key].reshape(-1, K // 128)[used], ref[used]), key
     assert rel_l2(gp.bf16_to_f64(g["out"]), ref_out) < REL_L2
 
 
