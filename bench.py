@@ -280,6 +280,7 @@ def run_ours(args, w):
     else:
         xt = E_(qb.w4a16_x_tiles_bytes(dims), torch.uint8)
         ht = E_(qb.w4a16_h_tiles_bytes(dims), torch.uint8)
+        h16 = E_(qb.w4a16_h16_tiles_bytes(dims), torch.uint8)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
     g1_pairs, g2_pairs = [], []
@@ -309,14 +310,15 @@ def run_ours(args, w):
             qb.qmoe_quant_tiles_int8_f32(dims, h32, offsets, ht, ws)
             qb.qmoe_gemm2_w8a8(dims, ht, t["w2"], t["w2_s"], offsets, y, None, status, ws)
         else:
-            qb.qmoe_gemm2_w4a16(dims, ht, t["w2"], offsets, y, status, ws)
+            qb.qmoe_w4a16_h_to_f16(dims, ht, offsets, h16, ws)
+            qb.qmoe_gemm2_w4a16(dims, h16, t["w2"], offsets, y, status, ws)
         if record:
             c.record(stream)
             g1_pairs.append((a, b))
             g2_pairs.append((b, c))
         qb.qmoe_combine(dims, y, t["topk_w"], slot, out)
 
-    launches_per_step = 4 + 1 + 2 + (1 if w.scheme == "w8a8" else 0) + 1
+    launches_per_step = 4 + 1 + 2 + (1 if w.scheme in ("w8a8", "w4a16") else 0) + 1
 
     def barrier():
         if world > 1:

@@ -194,6 +194,18 @@ int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const i
 size_t qmoe_w4a16_x_tiles_bytes(const qmoe_dims* d);
 size_t qmoe_w4a16_h_tiles_bytes(const qmoe_dims* d);
 
+/* h16 tiles (K = I, stage-2 input): the x-tile form of h -- fp16 values
+ * h * 2^-e_r with e_r chosen from the row's largest |h| as for x tiles, tail
+ * 2^e_r at (t*NMAX + r).  qmoe_w4a16_h16_tiles_bytes(d) bytes (0 unless
+ * I % 64 == 0).
+ * qmoe_w4a16_h_to_f16 -- h tiles (from qmoe_gemm1_swiglu_w4a16) -> h16 tiles,
+ * exactly for rows whose values stay within fp16's range after the scaling,
+ * reading the group maxima of the h tail.  The input is not modified.  ws =
+ * the workspace qmoe_align_sort filled for this routing. */
+size_t qmoe_w4a16_h16_tiles_bytes(const qmoe_dims* d);
+int qmoe_w4a16_h_to_f16(const qmoe_dims* d, const uint8_t* h_tiles, const int32_t* offsets, uint8_t* h16_tiles,
+                        const void* ws, size_t ws_bytes, qmoe_stream_t stream);
+
 /* qmoe_permute_x_f16 -- the expert-sorted permutation of the routed bf16
  * activations, written as W4A16 x tiles: slot s of expert e gets row
  * sorted_pair_ids[s] / k of x_bf16 [T, H] ([hip-ep] description: one grouped
@@ -345,12 +357,12 @@ int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const uint8_t* x_tiles, const int
  * than inter_dim read out of bounds, so the kernels never let a K tile pass
  * the end of I).
  *
- * W4A16: h_tiles from qmoe_gemm1_swiglu_w4a16; w2 = qmoe_prepack_int4_weights
- *        of the int4 [E*H, I/2] codes and fp16 [E*H, I/32] scales,
- *        dequantised as in stage 1; each h row is scaled into fp16 by the
- *        power of two its tail's group maxima give (as for x tiles), exactly;
- *        ws as for stage 1. */
-int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
+ * W4A16: h16_tiles from qmoe_w4a16_h_to_f16 (h rows already scaled into
+ *        fp16 by powers of two); w2 = qmoe_prepack_int4_weights of the int4
+ *        [E*H, I/2] codes and fp16 [E*H, I/32] scales, dequantised on chip as
+ *        in stage 1; fp16 MMAs, fp32 sums scaled back by 2^(e_r - p_r); ws as
+ *        for stage 1. */
+int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h16_tiles, const uint8_t* w2, const int32_t* offsets,
                      uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream);
 
 /* MXFP4 x FP8: h_tiles from qmoe_gemm1_swiglu_mxfp4; w2 = qmoe_prepack_fp4_weights

@@ -51,6 +51,8 @@ SIGNATURES = {
     "qmoe_prepack_int4_weights": ([_i64, _i64, _vp, _vp, _vp, _vp], _i32),
     "qmoe_w4a16_x_tiles_bytes": ([_DP], _sz),
     "qmoe_w4a16_h_tiles_bytes": ([_DP], _sz),
+    "qmoe_w4a16_h16_tiles_bytes": ([_DP], _sz),
+    "qmoe_w4a16_h_to_f16": ([_DP, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_permute_x_f16": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_mx_tiles_bytes": ([_DP, _i64], _sz),
@@ -239,6 +241,16 @@ def w4a16_h_tiles_bytes(d: Dims) -> int:
     return int(lib().qmoe_w4a16_h_tiles_bytes(ctypes.byref(d)))
 
 
+def w4a16_h16_tiles_bytes(d: Dims) -> int:
+    return int(lib().qmoe_w4a16_h16_tiles_bytes(ctypes.byref(d)))
+
+
+def qmoe_w4a16_h_to_f16(d, h_tiles, offsets, h16_tiles, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_w4a16_h_to_f16(ctypes.byref(d), _ptr(h_tiles), _ptr(offsets), _ptr(h16_tiles), wp, wn,
+                                     _stream(stream)), "qmoe_w4a16_h_to_f16")
+
+
 def qmoe_permute_x_f16(d, x, sorted_pair_ids, offsets, x_tiles, ws, stream=None):
     wp, wn = _ws(ws)
     _check(lib().qmoe_permute_x_f16(ctypes.byref(d), _ptr(x), _ptr(sorted_pair_ids), _ptr(offsets), _ptr(x_tiles),
@@ -291,9 +303,9 @@ def qmoe_gemm1_swiglu_w8a8(d, x_tiles, w1, w1_s, offsets, h, dbg_acc, status, ws
            "qmoe_gemm1_swiglu_w8a8")
 
 
-def qmoe_gemm2_w4a16(d, h_tiles, w2, offsets, y, status, ws, stream=None):
+def qmoe_gemm2_w4a16(d, h16_tiles, w2, offsets, y, status, ws, stream=None):
     wp, wn = _ws(ws)
-    _check(lib().qmoe_gemm2_w4a16(ctypes.byref(d), _ptr(h_tiles), _ptr(w2), _ptr(offsets), _ptr(y), _ptr(status),
+    _check(lib().qmoe_gemm2_w4a16(ctypes.byref(d), _ptr(h16_tiles), _ptr(w2), _ptr(offsets), _ptr(y), _ptr(status),
                                   wp, wn, _stream(stream)), "qmoe_gemm2_w4a16")
 
 

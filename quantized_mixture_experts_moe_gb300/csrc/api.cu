@@ -27,7 +27,7 @@ int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* s
 bool w4_tc_ok(const qmoe_dims* d);
 int w4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const int32_t* offsets,
                 const int32_t* tile_start, uint8_t* h_tiles, int32_t* status, cudaStream_t st);
-int w4_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
+int w4_tc_gemm2(const qmoe_dims* d, const uint8_t* h16_tiles, const uint8_t* w2, const int32_t* offsets,
                 const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st);
 bool i8_tc_ok(const qmoe_dims* d);
 int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, const float* w1_s,
@@ -36,6 +36,8 @@ int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, co
 int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
                 const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* dbg_acc, int32_t* status,
                 cudaStream_t st);
+int h_to_f16_launch(const qmoe_dims* d, const uint8_t* h_tiles, const int32_t* offsets, const int32_t* tile_start,
+                    uint8_t* out, cudaStream_t st);
 int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool from_bf16_tokens,
                             const int32_t* sorted, const int32_t* offsets, const int32_t* tile_start, uint8_t* tiles,
                             cudaStream_t st);
@@ -118,6 +120,22 @@ extern "C" size_t qmoe_w4a16_h_tiles_bytes(const qmoe_dims* d) {
     return (size_t)bft::h_tiles_bytes(d);
 }
 
+extern "C" size_t qmoe_w4a16_h16_tiles_bytes(const qmoe_dims* d) {
+    if (!dims_ok(d) || d->I % 64 != 0) return 0;
+    const int nmax = mxt::nmax_for(d);
+    return (size_t)(bft::blocks_bytes(d, d->I) + mxt::max_tiles(d, nmax) * nmax * 4);
+}
+
+extern "C" int qmoe_w4a16_h_to_f16(const qmoe_dims* d, const uint8_t* h_tiles, const int32_t* offsets,
+                                   uint8_t* h16_tiles, const void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {h_tiles, offsets, h16_tiles});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (d->I % 64 != 0) return QMOE_ERR_UNSUPPORTED;
+    return h_to_f16_launch(d, h_tiles, offsets, tile_schedule_in(const_cast<void*>(ws), d), h16_tiles,
+                           (cudaStream_t)stream);
+}
+
 extern "C" int qmoe_permute_x_f16(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
                                  const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                                  qmoe_stream_t stream) {
@@ -139,13 +157,13 @@ extern "C" int qmoe_gemm1_swiglu_w4a16(const qmoe_dims* d, const uint8_t* x_tile
     return w4_tc_gemm1(d, x_tiles, w1, offsets, tile_schedule_in(ws, d), h_tiles, dev_status, (cudaStream_t)stream);
 }
 
-extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const int32_t* offsets,
+extern "C" int qmoe_gemm2_w4a16(const qmoe_dims* d, const uint8_t* h16_tiles, const uint8_t* w2, const int32_t* offsets,
                                 uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
-    int rc = gemm_args_ok(d, {h_tiles, w2, offsets, y, dev_status});
+    int rc = gemm_args_ok(d, {h16_tiles, w2, offsets, y, dev_status});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
     if (!w4_tc_ok(d)) return QMOE_ERR_UNSUPPORTED;
-    return w4_tc_gemm2(d, h_tiles, w2, offsets, tile_schedule_in(ws, d), y, dev_status, (cudaStream_t)stream);
+    return w4_tc_gemm2(d, h16_tiles, w2, offsets, tile_schedule_in(ws, d), y, dev_status, (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------ W8A8 (exact int32 sums on fp16 tensor cores)
@@ -225,7 +243,7 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
                             : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : qmoe_w8a8_tiles_bytes(d, d->H)));
     L.h = take(scheme == 0 ? (size_t)bft::h_tiles_bytes(d)
                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
-    L.ht = take(scheme == 2 ? qmoe_w8a8_tiles_bytes(d, d->I) : 0);
+    L.ht = take(scheme == 2 ? qmoe_w8a8_tiles_bytes(d, d->I) : (scheme == 0 ? qmoe_w4a16_h16_tiles_bytes(d) : 0));
     L.y = take(2 * P * H);
     L.align_ws = take(qmoe_workspace_bytes(d));
     L.total = o;
@@ -267,7 +285,9 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
             rc = qmoe_gemm1_swiglu_w4a16(d, (const uint8_t*)at(L.xq), (const uint8_t*)w1, offsets, (uint8_t*)at(L.h),
                                          dev_status, aws, aws_bytes, stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm2_w4a16(d, (const uint8_t*)at(L.h), (const uint8_t*)w2, offsets, y, dev_status, aws,
+            rc = qmoe_w4a16_h_to_f16(d, (const uint8_t*)at(L.h), offsets, (uint8_t*)at(L.ht), aws, aws_bytes, stream);
+        if (rc == QMOE_OK)
+            rc = qmoe_gemm2_w4a16(d, (const uint8_t*)at(L.ht), (const uint8_t*)w2, offsets, y, dev_status, aws,
                                   aws_bytes, stream);
     } else if (scheme == 1) {
         rc = qmoe_permute_quant_mxfp8(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);

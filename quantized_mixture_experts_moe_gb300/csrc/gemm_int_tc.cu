@@ -42,15 +42,16 @@
 #include "tc_ptx.cuh"
 #include "tma_host.cuh"
 
+#include <cstring>
+
 namespace qmoe {
-namespace i8 {
+namespace ig {
 
 constexpr int WARP_W = 0, WARP_B = 1, WARP_MMA = 2;
 constexpr int WARP_CVT0 = 4, CVT_WARPS = 8;
 constexpr int WARP_EPI0 = 12, EPI_WARPS = 8;
 constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
 constexpr int KSTEP = 128;       // K elements per step (two 64-element halves)
-constexpr int NS = 112;          // tokens per MMA (a schedule tile of 224 is two of these)
 // Drains keep every fp32 partial sum below 2^24: a chunk of steps may add at
 // most L1_BOUND * 128 (|w| <= 128 for int8 weights, sum |x| over the chunk's
 // steps <= L1_BOUND for every row) on top of a remainder |lo| <= 4096.
@@ -58,45 +59,56 @@ constexpr int L1_BOUND = ((1 << 24) - 4097) / 128;
 constexpr int HI_SHIFT = 13;
 constexpr int MAX_E = 512;
 constexpr int MAX_K = 16384;
-
-// TMEM columns: the fp32 accumulators of the two tiles, then a two-slot
-// ring of A operands (a 128 x 128 fp16 tile = 64 columns, two per slot).  The
-// 16-bit running high parts live in shared memory, one 32-bit word per
-// (token, row): tile 0 in the low half, tile 1 in the high half.
-constexpr uint32_t R_COL = 0;
-constexpr uint32_t A_COL = 256;
-constexpr int AS = 2;
+constexpr int AS = 2;            // A slots in TMEM
 constexpr int A_SLOT_COLS = 2 * KSTEP / 2;  // two tiles x KSTEP/2 fp16 pairs
-static_assert(R_COL + 2 * NS <= A_COL && A_COL + AS * A_SLOT_COLS <= 512, "TMEM budget");
+constexpr int BS = 3;            // activation slots
 
-constexpr int HALF_RAW = 2 * 128 * 64;      // one 64-element half of both raw int8 tiles (one TMA box)
-constexpr int RAW_BYTES = 2 * HALF_RAW;
-constexpr int HALF_B = NS * 128;            // one 64-element half of the step's fp16 token rows
-constexpr int B_BYTES = 2 * HALF_B;
-constexpr int RS = 2;
-constexpr int BS = 3;
-static_assert(BS >= AS + 1, "a step's done barrier is not reused before the converter has waited on it");
-constexpr int RAW_OFF = 0;
-constexpr int B_OFF = RAW_OFF + RS * RAW_BYTES;
-constexpr int S_OFF = B_OFF + BS * B_BYTES;
-constexpr int S_BYTES = NS * 128 * 4;
-constexpr int BAR_OFF = S_OFF + S_BYTES;
-constexpr int NBAR = 2 * RS + 2 * BS + AS + 2;
-constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-constexpr int SCHED_OFF = MISC_OFF + 64;
-constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
-static_assert(B_OFF % 1024 == 0 && HALF_B % 1024 == 0 && HALF_RAW % 1024 == 0, "swizzled tiles 1024-aligned");
-static_assert(smem_bytes(MAX_E) <= 232448, "shared memory per CTA");
+// Per weight format:
+//   W8 (int8, exact int32 sums): tokens per MMA NS = 112 (a 224-row schedule
+//      tile is two of them), raw int8 rows by TMA, two raw slots;
+//   W4 (int4 + fp16 scales):     NS = 128 (a 224-row tile is 128 + 96), raw
+//      pre-packed blocks by bulk copy, three raw slots.
+// TMEM columns: the fp32 accumulators of the two tiles (2 * NS), then the A
+// ring from column 256.  Shared memory: raw ring, activation ring, and
+// NS x 128 words staging the drains' high parts (W8) and the final outputs.
+template <bool W4>
+struct Cfg {
+    static constexpr int NS = W4 ? 128 : 112;
+    static constexpr int HALF_RAW = W4 ? 2 * bft::kW4Block : 2 * 128 * 64;  // one 64-element half, both tiles
+    static constexpr int RAW_BYTES = 2 * HALF_RAW;
+    static constexpr int RS = W4 ? 3 : 2;
+    static constexpr int HALF_B = NS * 128;  // one 64-element half of the step's fp16 token rows
+    static constexpr int B_BYTES = 2 * HALF_B;
+    static constexpr uint32_t R_COL = 0;
+    static constexpr uint32_t A_COL = 256;
+    static constexpr int RAW_OFF = 0;
+    static constexpr int B_OFF = (RAW_OFF + RS * RAW_BYTES + 1023) / 1024 * 1024;
+    static constexpr int S_OFF = B_OFF + BS * B_BYTES;
+    static constexpr int S_BYTES = NS * 128 * 4;
+    static constexpr int BAR_OFF = S_OFF + S_BYTES;
+    static constexpr int NBAR = 2 * RS + 2 * BS + AS + 2;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int SCHED_OFF = MISC_OFF + 64;
+    static constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
+    static_assert(R_COL + 2 * NS <= A_COL && A_COL + AS * A_SLOT_COLS <= 512, "TMEM budget");
+    static_assert(BS >= AS + 1, "a step's done barrier is not reused before the converter has waited on it");
+    static_assert(B_OFF % 1024 == 0 && HALF_B % 1024 == 0, "swizzled activation tiles 1024-aligned");
+    static_assert(W4 || HALF_RAW % 1024 == 0, "swizzled raw int8 tiles 1024-aligned");
+    static_assert(smem_bytes(MAX_E) <= 232448, "shared memory per CTA");
+};
 
 struct Args {
     int T, k, H, I, E;
     int nmax;                 // schedule tile (112 or 224 tokens)
     const uint8_t* act;       // fp16 token tiles (K = H for stage 1, I for stage 2)
-    const float* act_scale;   // per tile row: s_x (stage 1) or s_h (stage 2)
-    const float* w_scale;     // per weight row (output channel)
+    const float* act_scale;   // per tile row: s_x / s_h (W8) or the power of two 2^e (W4)
+    const uint8_t* wq;        // W4: pre-packed int4 blocks (W8 weights come through the tensor map)
+    const float* w_scale;     // per weight row: channel scale (W8) or 2^-p (W4)
+    float* h_tail;            // W4 stage 1: |max| per tile row and 32-column group of h
     const int32_t* offsets;
     const int32_t* tile_start;
-    float* h;                 // stage 1 output, fp32 [P, I] in slot order
+    float* h;                 // W8 stage 1 output, fp32 [P, I] in slot order
+    uint8_t* h_tiles;         // W4 stage 1 output, bf16 tiles (K = I)
     uint16_t* y;              // stage 2 output, bf16 [P, H] in slot order
     const int32_t* l1max;     // per (sub-tile, step): the largest sum |x| over the sub-tile's rows
     int32_t* dbg_acc;         // optional exact sums: [P, 2I] (stage 1) or [P, H] (stage 2)
@@ -105,6 +117,7 @@ struct Args {
 
 // Unit u -> (expert e, schedule tile t, half of it, column block nb) and the
 // unit's first slot m0 and token count (<= 0 for an empty second half).
+template <int NS>
 __device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax, const int* tile_start, int E,
                                             const int32_t* offsets, int& e, int& t, int& half, int& nb, int& m0,
                                             int& ntok) {
@@ -119,7 +132,7 @@ __device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax,
     }
     e = lo;
     m0 = offsets[e] + (t - tile_start[e]) * nmax + half * NS;
-    ntok = min(NS, offsets[e + 1] - m0);
+    ntok = min(min(NS, nmax - half * NS), offsets[e + 1] - m0);
 }
 
 __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
@@ -149,6 +162,20 @@ __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t
     const uint32_t bias = 0x64806480u;
     asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
     asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
+}
+
+// Eight int4 codes (one reordered word) times an f16x2 scale -> four f16x2
+// pairs in K order.  0x6400 | n is the fp16 value 1024 + n; subtracting 1032
+// gives n - 8 exactly; the product is the one rounding.
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t s2, uint32_t* out) {
+    const uint32_t magic = 0x64006400u, bias = 0x64086408u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | magic;
+        asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(v) : "r"(bias));
+        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(v) : "r"(s2));
+        out[j] = v;
+    }
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) { tc::tmem_ld_32x32b_x16(taddr, r); }
@@ -187,34 +214,35 @@ __device__ __forceinline__ bool bit_at(const uint32_t (&b)[4], int kt) {
     return kt < 128 && ((w >> (kt & 31)) & 1u);
 }
 
-template <int STAGE>
-__global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const Args a) {
+template <int STAGE, bool W4>
+__global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const Args a) {
+    using C = Cfg<W4>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sRaw = smem + RAW_OFF;
-    uint8_t* sB = smem + B_OFF;
-    uint32_t* sS = reinterpret_cast<uint32_t*>(smem + S_OFF);  // [token][row] packed high parts
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-    uint64_t* raw_empty = raw_full + RS;
-    uint64_t* b_full = raw_empty + RS;
+    uint8_t* sRaw = smem + C::RAW_OFF;
+    uint8_t* sB = smem + C::B_OFF;
+    uint32_t* sS = reinterpret_cast<uint32_t*>(smem + C::S_OFF);  // [token][row] packed high parts
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* raw_empty = raw_full + C::RS;
+    uint64_t* b_full = raw_empty + C::RS;
     uint64_t* done = b_full + BS;  // step g completed (both issuers' MMAs): frees B slot g % BS and A slot g % AS
     uint64_t* a_full = done + BS;
     uint64_t* acc_full = a_full + AS;
     uint64_t* acc_empty = acc_full + 1;
-    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + MISC_OFF);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 8);
-    int* tile_start = reinterpret_cast<int*>(smem + SCHED_OFF);
+    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
+    int* tile_start = reinterpret_cast<int*>(smem + C::SCHED_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E;
     const int K = (STAGE == 1) ? a.H : a.I;
     const int NB = (STAGE == 1) ? a.I / 128 : a.H / 256;
     const int KT = K / KSTEP;
-    const int halves = a.nmax / NS;
+    const int halves = (a.nmax + C::NS - 1) / C::NS;
 
     for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = a.tile_start[i];
     if (threadIdx.x == 32 * WARP_MMA) {
-        for (int s = 0; s < RS; ++s) {
+        for (int s = 0; s < C::RS; ++s) {
             tc::mbar_init(&raw_full[s], 1);
             tc::mbar_init(&raw_empty[s], CVT_WARPS);
         }
@@ -249,22 +277,37 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
             uint32_t ph = 0;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, t, half, nb, m0, ntok;
-                decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
                 if (ntok <= 0) continue;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&raw_empty[rs], ph ^ 1)) { set_abort(abort_flag, a.status); ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&raw_full[rs], RAW_BYTES);
-                    uint8_t* dst = sRaw + rs * RAW_BYTES;
+                    tc::mbar_arrive_expect_tx(&raw_full[rs], C::RAW_BYTES);
+                    uint8_t* dst = sRaw + rs * C::RAW_BYTES;
+                    if constexpr (W4) {
+                        // pre-packed blocks (row tile, 64-element K block): [half hh][tile i]
+                        const int KB = K / 64;
+                        const int64_t rt0 = (STAGE == 1) ? (int64_t)e * (2 * a.I / 128) + nb : (int64_t)e * (a.H / 128) + 2 * nb;
+                        const int64_t rt1 = (STAGE == 1) ? rt0 + a.I / 128 : rt0 + 1;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (STAGE == 1)
-                            tc::tma_load_3d(dst + hh * HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh, nb * 128, 2 * e);
-                        else
-                            tc::tma_load_2d(dst + hh * HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh,
-                                            e * a.H + nb * 256);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            tc::bulk_load(dst + (2 * hh) * bft::kW4Block, a.wq + (rt0 * KB + 2 * kt + hh) * bft::kW4Block,
+                                          bft::kW4Block, &raw_full[rs]);
+                            tc::bulk_load(dst + (2 * hh + 1) * bft::kW4Block,
+                                          a.wq + (rt1 * KB + 2 * kt + hh) * bft::kW4Block, bft::kW4Block, &raw_full[rs]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            if (STAGE == 1)
+                                tc::tma_load_3d(dst + hh * C::HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh,
+                                                nb * 128, 2 * e);
+                            else
+                                tc::tma_load_2d(dst + hh * C::HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh,
+                                                e * a.H + nb * 256);
+                        }
                     }
-                    if (++rs == RS) { rs = 0; ph ^= 1; }
+                    if (++rs == C::RS) { rs = 0; ph ^= 1; }
                 }
                 if (!ok) break;
             }
@@ -277,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
             const int64_t bb = (int64_t)a.nmax * 128;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, t, half, nb, m0, ntok;
-                decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
                 if (ntok <= 0) continue;
                 const uint32_t bytes = (uint32_t)((ntok + 15) & ~15) * 128u;
                 bool ok = true;
@@ -286,8 +329,8 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                     tc::mbar_arrive_expect_tx(&b_full[bs], 2 * bytes);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh)
-                        tc::bulk_load(sB + bs * B_BYTES + hh * HALF_B,
-                                      a.act + ((int64_t)t * (2 * KT) + 2 * kt + hh) * bb + (int64_t)half * NS * 128, bytes,
+                        tc::bulk_load(sB + bs * C::B_BYTES + hh * C::HALF_B,
+                                      a.act + ((int64_t)t * (2 * KT) + 2 * kt + hh) * bb + (int64_t)half * C::NS * 128, bytes,
                                       &b_full[bs]);
                     if (++bs == BS) { bs = 0; ph ^= 1; }
                 }
@@ -302,13 +345,13 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
         bool pending = false;  // an accumulator event not yet handed back by the epilogue
         for (int u = blockIdx.x; u < total_units && !warp_flag(abort_flag); u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
             if (ntok <= 0) continue;
             const int nmma = (ntok + 15) & ~15;
             const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
-            const uint32_t dcol = tm + R_COL + (uint32_t)(iss * NS);
-            uint32_t starts[4];
-            chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
+            const uint32_t dcol = tm + C::R_COL + (uint32_t)(iss * C::NS);
+            uint32_t starts[4] = {0u, 0u, 0u, 0u};
+            if constexpr (!W4) chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
             bool ok = true;
             for (int kt = 0; kt < KT; ++kt) {
                 if (pending) {
@@ -317,12 +360,12 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                 }
                 if (!warp_wait(&b_full[bs], bph, lane) || !warp_wait(&a_full[as], aph, lane)) { ok = false; break; }
                 tc::tc_fence_after();
-                const uint32_t b0 = tc::smem_u32(sB + bs * B_BYTES);
-                const uint32_t a0 = tm + A_COL + (uint32_t)(as * A_SLOT_COLS + iss * (KSTEP / 2));
+                const uint32_t b0 = tc::smem_u32(sB + bs * C::B_BYTES);
+                const uint32_t a0 = tm + C::A_COL + (uint32_t)(as * A_SLOT_COLS + iss * (KSTEP / 2));
 #pragma unroll
                 for (int kk = 0; kk < KSTEP / 16; ++kk)
                     tc::mma_f16_ts_elect(dcol, a0 + 8 * kk,
-                                         tc::sdesc_kmajor_sw128(b0 + (kk >> 2) * HALF_B + 32 * (kk & 3)), idesc,
+                                         tc::sdesc_kmajor_sw128(b0 + (kk >> 2) * C::HALF_B + 32 * (kk & 3)), idesc,
                                          (kt > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit_elect(&done[bs]);
                 if (++bs == BS) { bs = 0; bph ^= 1; }
@@ -351,7 +394,7 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
             if (ntok <= 0) continue;
             for (int kt = 0; kt < KT; ++kt, ++gs) {
                 if (!warp_wait(&raw_full[rs], rph, lane)) {
@@ -359,22 +402,46 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                     ok = false;
                     break;
                 }
-                const uint8_t* src = sRaw + rs * RAW_BYTES + tile * (128 * 64) + m * 64;
-                uint4 c[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    c[j] = *reinterpret_cast<const uint4*>(src + (j >> 2) * HALF_RAW + (((j & 3) ^ sw) << 4));
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
-                if (++rs == RS) { rs = 0; rph ^= 1; }
-                // 128 int8 values -> 64 fp16 pairs, 16 per TMEM store
+                // 128 weights of this row -> 64 fp16 pairs, 16 per TMEM store
                 uint32_t o[4][16];
+                if constexpr (W4) {
+                    uint4 cw[2][2];
+                    uint32_t sc[2];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t wv[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint8_t* src = sRaw + rs * C::RAW_BYTES + (2 * hh + tile) * bft::kW4Block;
+                        cw[hh][0] = *reinterpret_cast<const uint4*>(src + m * 32);
+                        cw[hh][1] = *reinterpret_cast<const uint4*>(src + m * 32 + 16);
+                        sc[hh] = *reinterpret_cast<const uint32_t*>(src + 4096 + m * 4);
+                    }
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
+                    if (++rs == C::RS) { rs = 0; rph ^= 1; }
 #pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        i8x4_to_f16x2(wv[p], o[j >> 1][(j & 1) * 8 + 2 * p], o[j >> 1][(j & 1) * 8 + 2 * p + 1]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t s2a = (sc[hh] & 0xFFFFu) * 0x10001u, s2b = (sc[hh] >> 16) * 0x10001u;
+                        const uint32_t wv[8] = {cw[hh][0].x, cw[hh][0].y, cw[hh][0].z, cw[hh][0].w,
+                                                cw[hh][1].x, cw[hh][1].y, cw[hh][1].z, cw[hh][1].w};
+#pragma unroll
+                        for (int w8 = 0; w8 < 8; ++w8)
+                            dequant8(wv[w8], w8 < 4 ? s2a : s2b, &o[2 * hh + (w8 >> 2)][(w8 & 3) * 4]);
+                    }
+                } else {
+                    const uint8_t* src = sRaw + rs * C::RAW_BYTES + tile * (128 * 64) + m * 64;
+                    uint4 c[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        c[j] = *reinterpret_cast<const uint4*>(src + (j >> 2) * C::HALF_RAW + (((j & 3) ^ sw) << 4));
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
+                    if (++rs == C::RS) { rs = 0; rph ^= 1; }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t wv[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+#pragma unroll
+                        for (int p = 0; p < 4; ++p)
+                            i8x4_to_f16x2(wv[p], o[j >> 1][(j & 1) * 8 + 2 * p], o[j >> 1][(j & 1) * 8 + 2 * p + 1]);
+                    }
                 }
                 // the A slot is free once the MMAs of step gs - AS have completed
                 if (gs >= (uint32_t)AS) {
@@ -386,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                     }
                 }
                 const int as = (int)(gs % AS);
-                const uint32_t ta = tm + lane_base + A_COL + (uint32_t)(as * A_SLOT_COLS + tile * (KSTEP / 2));
+                const uint32_t ta = tm + lane_base + C::A_COL + (uint32_t)(as * A_SLOT_COLS + tile * (KSTEP / 2));
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) tmem_st16(ta + 16 * q4, o[q4]);
                 tc::tmem_st_wait();
@@ -404,9 +471,9 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
             if (ntok <= 0) continue;
-            const float* ts = a.act_scale + (int64_t)t * a.nmax + half * NS;
+            const float* ts = a.act_scale + (int64_t)t * a.nmax + half * C::NS;
             float ws0, ws1;  // channel scales of this thread's row in the two tiles
             int64_t col0, col1, dcol0, dcol1, ostride, dstride;
             if (STAGE == 1) {
@@ -430,8 +497,8 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                 dcol1 = col1;
                 dstride = a.H;
             }
-            uint32_t starts[4];
-            chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
+            uint32_t starts[4] = {0u, 0u, 0u, 0u};
+            if constexpr (!W4) chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
             const int nev = 1 + __popc(starts[0]) + __popc(starts[1]) + __popc(starts[2]) + __popc(starts[3]);
             // this warp's per-token activation scales (chunk i: token 16 * eh + 32 * i + lane, lanes < 16),
             // fetched before the accumulator is ready
@@ -457,8 +524,8 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                     // drain: hi parts into the 16-bit running sums, lo back as the accumulator
                     for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
                         uint32_t g[16], v[16];
-                        tmem_ld16(tm + lane_base + R_COL + c0, g);
-                        tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
+                        tmem_ld16(tm + lane_base + C::R_COL + c0, g);
+                        tmem_ld16(tm + lane_base + C::R_COL + C::NS + c0, v);
                         tc::tmem_ld_wait();
                         uint32_t* sr = sS + c0 * 128 + n;
                         // the high parts so far (none before the first drain), then this chunk's added;
@@ -482,8 +549,8 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                             g[j] = __float_as_uint((float)l0);
                             v[j] = __float_as_uint((float)l1);
                         }
-                        tmem_st16(tm + lane_base + R_COL + c0, g);
-                        tmem_st16(tm + lane_base + R_COL + NS + c0, v);
+                        tmem_st16(tm + lane_base + C::R_COL + c0, g);
+                        tmem_st16(tm + lane_base + C::R_COL + C::NS + c0, v);
                     }
                     tc::tmem_st_wait();
                 } else {
@@ -494,8 +561,8 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                         const int c0 = 16 * eh + 32 * i;
                         if (c0 >= ntok) break;
                         uint32_t g[16], v[16];
-                        tmem_ld16(tm + lane_base + R_COL + c0, g);
-                        tmem_ld16(tm + lane_base + R_COL + NS + c0, v);
+                        tmem_ld16(tm + lane_base + C::R_COL + c0, g);
+                        tmem_ld16(tm + lane_base + C::R_COL + C::NS + c0, v);
                         uint32_t* sr = sS + c0 * 128 + n;
                         const float fl = fls[i];
                         tc::tmem_ld_wait();
@@ -512,7 +579,7 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
 #pragma unroll
                             for (int j = 0; j < 16; ++j) hf0[j] = hf1[j] = 0.f;
                         }
-                        if (a.dbg_acc) {
+                        if (!W4 && a.dbg_acc) {
                             const int nv = min(16, ntok - c0);
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
@@ -532,9 +599,10 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                             const float fx = __shfl_sync(0xFFFFFFFFu, fl, j);
                             const float r0 = (f0 * fx) * ws0;
                             const float r1 = (f1 * fx) * ws1;
-                            if (STAGE == 1)
-                                sr[j * 128] = __float_as_uint(__fdividef(r0, 1.0f + __expf(-r0)) * r1);
-                            else
+                            if (STAGE == 1) {
+                                const float h = __fdividef(r0, 1.0f + __expf(-r0)) * r1;
+                                sr[j * 128] = W4 ? (uint32_t)float_to_bf16_bits(h) : __float_as_uint(h);
+                            } else
                                 sr[j * 128] = (uint32_t)float_to_bf16_bits(r0) | ((uint32_t)float_to_bf16_bits(r1) << 16);
                         }
                     }
@@ -544,7 +612,23 @@ __global__ void __launch_bounds__(THREADS, 1) i8_gemm_kernel(const __grid_consta
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(acc_empty);
             }
-            if (last_final) {
+            if (last_final && W4 && STAGE == 1) {
+                // final, second pass (W4 stage 1): bf16 h into the h tiles, and each 32-column
+                // group's largest |h| (this warp's 32 columns) into the tile tail
+                const int NG = a.I / 32;
+                uint8_t* hblk = a.h_tiles + ((int64_t)t * (a.I / 64) + nb * 2 + (n >> 6)) * bft::block_bytes(a.nmax);
+                for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
+                    const uint32_t* sr = sS + c0 * 128 + n;
+                    const int nv = min(16, ntok - c0);
+                    for (int j = 0; j < nv; ++j) {  // warp-uniform: every lane takes part in the reduction
+                        const int row = half * C::NS + c0 + j;  // row within the schedule tile
+                        const uint32_t w = sr[j * 128];
+                        *reinterpret_cast<uint16_t*>(hblk + bft::elem_offset(row, n & 63)) = (uint16_t)w;
+                        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, (w & 0x7FFFu) << 16);
+                        if (lane == 0) a.h_tail[((int64_t)t * a.nmax + row) * NG + nb * 4 + q] = __uint_as_float(mx);
+                    }
+                }
+            } else if (last_final) {
                 // final, second pass: shared memory -> outputs, overlapping the next unit's MMAs
                 for (int c0 = 16 * eh; c0 < ntok; c0 += 32) {
                     const uint32_t* sr = sS + c0 * 128 + n;
@@ -611,30 +695,31 @@ static int sm_count() {
     return n;
 }
 
-template <int STAGE>
+template <int STAGE, bool W4>
 static int launch(const CUtensorMap& map, const Args& a, cudaStream_t st) {
-    if (cudaFuncSetAttribute(i8_gemm_kernel<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes(MAX_E)) != cudaSuccess)
+    using C = Cfg<W4>;
+    if (cudaFuncSetAttribute(int_gemm_kernel<STAGE, W4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::smem_bytes(MAX_E)) != cudaSuccess)
         return QMOE_ERR_LAUNCH;
     const int grid = sm_count();
     if (grid <= 0) return QMOE_ERR_CUDA;
-    i8_gemm_kernel<STAGE><<<grid, THREADS, smem_bytes(a.E), st>>>(map, a);
+    int_gemm_kernel<STAGE, W4><<<grid, THREADS, C::smem_bytes(a.E), st>>>(map, a);
     return launch_status();
 }
 
-}  // namespace i8
+}  // namespace ig
 
 bool i8_tc_ok(const qmoe_dims* d) {
-    return d->H % 256 == 0 && d->I % 128 == 0 && d->H <= i8::MAX_K && d->I <= i8::MAX_K && d->E <= i8::MAX_E;
+    return d->H % 256 == 0 && d->I % 128 == 0 && d->H <= ig::MAX_K && d->I <= ig::MAX_K && d->E <= ig::MAX_E;
 }
 
 int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, const float* w1_s,
                 const int32_t* offsets, const int32_t* tile_start, float* h, int32_t* dbg_acc, int32_t* status,
                 cudaStream_t st) {
     CUtensorMap map;
-    int rc = i8::make_w_map(&map, w1, d, 1);
+    int rc = ig::make_w_map(&map, w1, d, 1);
     if (rc != QMOE_OK) return rc;
-    i8::Args a{};
+    ig::Args a{};
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.nmax = mxt::nmax_for(d);
     a.act = x_tiles;
@@ -644,16 +729,16 @@ int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, co
     a.w_scale = w1_s;
     a.offsets = offsets; a.tile_start = tile_start;
     a.h = h; a.dbg_acc = dbg_acc; a.status = status;
-    return i8::launch<1>(map, a, st);
+    return ig::launch<1, false>(map, a, st);
 }
 
 int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
                 const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* dbg_acc, int32_t* status,
                 cudaStream_t st) {
     CUtensorMap map;
-    int rc = i8::make_w_map(&map, w2, d, 2);
+    int rc = ig::make_w_map(&map, w2, d, 2);
     if (rc != QMOE_OK) return rc;
-    i8::Args a{};
+    ig::Args a{};
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.nmax = mxt::nmax_for(d);
     a.act = h_tiles;
@@ -663,7 +748,44 @@ int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, co
     a.w_scale = w2_s;
     a.offsets = offsets; a.tile_start = tile_start;
     a.y = y; a.dbg_acc = dbg_acc; a.status = status;
-    return i8::launch<2>(map, a, st);
+    return ig::launch<2, false>(map, a, st);
+}
+
+// ------------------------------------------------------------------ W4A16
+
+bool w4_tc_ok(const qmoe_dims* d) { return d->H % 256 == 0 && d->I % 128 == 0 && d->E <= ig::MAX_E; }
+
+int w4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const int32_t* offsets,
+                const int32_t* tile_start, uint8_t* h_tiles, int32_t* status, cudaStream_t st) {
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));  // W4 weights come by bulk copy
+    ig::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.nmax = mxt::nmax_for(d);
+    a.act = x_tiles;
+    a.act_scale = reinterpret_cast<const float*>(x_tiles + bft::blocks_bytes(d, d->H));
+    a.wq = w1;
+    a.w_scale = reinterpret_cast<const float*>(w1 + bft::w4_blocks_bytes((int64_t)d->E * 2 * d->I, d->H));
+    a.offsets = offsets; a.tile_start = tile_start;
+    a.h_tiles = h_tiles;
+    a.h_tail = reinterpret_cast<float*>(h_tiles + bft::blocks_bytes(d, d->I));
+    a.status = status;
+    return ig::launch<1, true>(map, a, st);
+}
+
+int w4_tc_gemm2(const qmoe_dims* d, const uint8_t* h16_tiles, const uint8_t* w2, const int32_t* offsets,
+                const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st) {
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    ig::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.nmax = mxt::nmax_for(d);
+    a.act = h16_tiles;
+    a.act_scale = reinterpret_cast<const float*>(h16_tiles + bft::blocks_bytes(d, d->I));
+    a.wq = w2;
+    a.w_scale = reinterpret_cast<const float*>(w2 + bft::w4_blocks_bytes((int64_t)d->E * d->H, d->I));
+    a.offsets = offsets; a.tile_start = tile_start; a.y = y; a.status = status;
+    return ig::launch<2, true>(map, a, st);
 }
 
 }  // namespace qmoe

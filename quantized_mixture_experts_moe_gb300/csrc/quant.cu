@@ -376,6 +376,69 @@ int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool f
     return launch_status();
 }
 
+// W4A16 h tiles (bf16, with per-32-column group maxima) -> fp16 tiles for
+// the down projection: one warp per expert-sorted slot.  The row's largest
+// magnitude (the largest of its group maxima) picks the power of two 2^-e that
+// moves it into [2^14, 2^15) (as for the x tiles); every bf16 value v of the
+// row becomes the fp16 value v * 2^-e (exact in range) at the same place of
+// the same tile layout, and 2^e goes to the output's per-row tail.
+__global__ void __launch_bounds__(kPqWarps * 32)
+h_to_f16_kernel(const uint8_t* __restrict__ h_tiles, const float* __restrict__ gmax, const int32_t* __restrict__ offsets,
+                const int32_t* __restrict__ tile_start, int E, int I, int nmax, int64_t P, uint8_t* __restrict__ out,
+                float* __restrict__ fac) {
+    const int lane = threadIdx.x & 31;
+    const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
+    int tile = -1, row = 0;
+    if (lane == 0 && slot < P && slot < offsets[E]) {
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (offsets[mid] <= slot) lo = mid; else hi = mid;
+        }
+        const int local = (int)(slot - offsets[lo]);
+        tile = tile_start[lo] + local / nmax;
+        row = local % nmax;
+    }
+    tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
+    if (tile < 0) return;
+    row = __shfl_sync(0xFFFFFFFFu, row, 0);
+    const int NG = I / 32;
+    const float* gm = gmax + ((int64_t)tile * nmax + row) * NG;
+    float amax = 0.f;
+    for (int g = lane; g < NG; g += 32) amax = fmaxf(amax, gm[g]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int e = f16_row_exponent(amax);
+    const float m = exp2i(-e);
+    const int64_t bb = bft::block_bytes(nmax);
+    const int64_t base = (int64_t)tile * (I / 64) * bb + row * 128;
+    for (int j = lane; j < I / 8; j += 32) {  // chunk j: K step j/8; the chunk's place is the same in both layouts
+        const int64_t off = base + (int64_t)(j >> 3) * bb + (((j & 7) ^ (row & 7)) << 4);
+        const uint4 v = *reinterpret_cast<const uint4*>(h_tiles + off);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 hv = __floats2half2_rn(__uint_as_float(u[i] << 16) * m, __uint_as_float(u[i] & 0xFFFF0000u) * m);
+            o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        *reinterpret_cast<uint4*>(out + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) fac[(int64_t)tile * nmax + row] = exp2i(e);
+}
+
+int h_to_f16_launch(const qmoe_dims* d, const uint8_t* h_tiles, const int32_t* offsets, const int32_t* tile_start,
+                    uint8_t* out, cudaStream_t st) {
+    const int64_t P = (int64_t)d->T * d->k;
+    if (P == 0) return QMOE_OK;
+    const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
+    const int64_t tail = bft::blocks_bytes(d, d->I);
+    h_to_f16_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(
+        h_tiles, reinterpret_cast<const float*>(h_tiles + tail), offsets, tile_start, d->E, d->I, mxt::nmax_for(d), P,
+        out, reinterpret_cast<float*>(out + tail));
+    return launch_status();
+}
+
 int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st) {
     const int64_t n8 = rows * cols / 8;
     if (n8 == 0) return QMOE_OK;

@@ -78,8 +78,10 @@ def run_layer(w, inp, keep=False):
         qb.qmoe_permute_x_f16(d, t["x"], sorted_ids, offsets, xt, ws)
         w1, w2 = qb.prepack_w4a16(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
         qb.qmoe_gemm1_swiglu_w4a16(d, xt, w1, offsets, ht, status, ws)
-        qb.qmoe_gemm2_w4a16(d, ht, w2, offsets, y, status, ws)
-        res.update(bxt=xt, bht=ht)
+        h16 = empty(qb.w4a16_h16_tiles_bytes(d), torch.uint8)
+        qb.qmoe_w4a16_h_to_f16(d, ht, offsets, h16, ws)
+        qb.qmoe_gemm2_w4a16(d, h16, w2, offsets, y, status, ws)
+        res.update(bxt=xt, bht=ht, bh16=h16)
     elif w.scheme == "mxfp4":
         xt = empty(qb.mx_tiles_bytes(d, H), torch.uint8)
         ht = empty(qb.mx_tiles_bytes(d, I), torch.uint8)
@@ -117,6 +119,7 @@ def run_layer(w, inp, keep=False):
             nt = max_tiles(P, E, nmax)
             r["x_f16"], r["x_fac"] = unpack_w4_x_tiles(r.pop("bxt"), r["offsets"], nmax, H, nt)
             r["h"], r["h_gmax"] = unpack_w4_h_tiles(r.pop("bht"), r["offsets"], nmax, I, nt)
+            r["h_f16"], r["h_fac"] = unpack_w4_x_tiles(r.pop("bh16"), r["offsets"], nmax, I, nt)
         else:
             nmax = tile_nmax(T, k, E)
             nt = max_tiles(P, E, nmax)
@@ -203,7 +206,7 @@ def _gather16(buf, off):
 
 
 def unpack_w4_x_tiles(buf, offsets, nmax, H, ntiles):
-    """W4A16 x tiles -> slot-order fp16 bits [P_valid, H] and per-row factors 2^e [P_valid]."""
+    """W4A16 x (or h16) tiles -> slot-order fp16 bits [P_valid, K] and per-row factors 2^e [P_valid]."""
     slots = np.arange(offsets[-1])
     t, r = _tile_index(offsets, nmax, slots)
     tail = buf[ntiles * (H // 64) * nmax * 128:].view(np.float32)

@@ -82,6 +82,8 @@ def test_host_checks_reject_before_launch(lib):
     assert qb.w4a16_x_tiles_bytes(d) == 9 * 4 * 112 * 128 + 9 * 112 * 4
     assert qb.w4a16_h_tiles_bytes(d) == 9 * 2 * 112 * 128 + 9 * 112 * 4 * 4
     assert qb.w4a16_h_tiles_bytes(qb.dims(16, 2, 256, 96, 8)) == 0
+    assert qb.w4a16_h16_tiles_bytes(d) == 9 * 2 * 112 * 128 + 9 * 112 * 4
+    assert lib.qmoe_w4a16_h_to_f16(ctypes.byref(d), null, ok, ok, ok, 1 << 20, null) == -1
     assert lib.qmoe_permute_x_f16(ctypes.byref(d), null, ok, ok, ok, ok, 1 << 20, null) == -1
     assert lib.qmoe_moe_forward(7, ctypes.byref(d), *([null] * 10), 0, null) == -1
     # MXFP4 scale pre-pack: bad K, null pointers

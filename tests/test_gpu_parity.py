@@ -163,6 +163,12 @@ def test_stage1_against_oracle(w):
         assert rel_l2(got, ref) < W4_H_REL_L2
         # the tail holds each 32-column group's largest |h|
         assert np.array_equal(g["h_gmax"].astype(np.float64), np.abs(got).reshape(len(got), -1, 32).max(axis=2))
+        # the down projection's fp16 form of h: the same values, each row scaled by its power of two
+        back = g["h_f16"].view(np.float16).astype(np.float64) * g["h_fac"][:, None].astype(np.float64)
+        assert np.array_equal(back, got)
+        hmax = np.abs(got).max(axis=1)
+        nz = hmax > 0
+        assert np.all((hmax[nz] / g["h_fac"][nz] >= 2.0**14) & (hmax[nz] / g["h_fac"][nz] < 2.0**15))
     elif w.scheme == "mxfp4":
         rq, rs = oracle.quant_act("mxfp4", d["x"])
         tok = order // w.k  # slot -> token
@@ -226,7 +232,9 @@ def test_stage2_against_oracle(w):
         nmax = gp.tile_nmax(rows, 1, w.E)
         ht = gp.pack_w4_h_tiles(s2["h"], offsets, nmax, w.I, qb.w4a16_h_tiles_bytes(d), gp.max_tiles(rows, w.E, nmax))
         w2p = qb.prepack_int4_weights(gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), w.I)
-        qb.qmoe_gemm2_w4a16(d, gp.dev(ht), w2p, off_t, y, st, ws)
+        h16 = gp.empty(qb.w4a16_h16_tiles_bytes(d), torch.uint8)
+        qb.qmoe_w4a16_h_to_f16(d, gp.dev(ht), off_t, h16, ws)
+        qb.qmoe_gemm2_w4a16(d, h16, w2p, off_t, y, st, ws)
         ref = oracle.stage2("w4a16", w.H, w.I, w.E, experts, s2["h"], None, wts["w2"], wts["w2_s"])
         torch.cuda.synchronize()
         assert int(st.item()) == 0
