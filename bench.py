@@ -34,7 +34,10 @@ UNIT = "TFLOP/s"
 # ncu DRAM bytes (read + write) of one stage-1 GEMM launch divided by its
 # algorithmic bytes, per scheme, for the kernel as it stands; None once the
 # kernel changes after the capture
-TRAFFIC_RATIO_GEMM1 = {"mxfp4": (309.222144 + 6.509056) / 292.782080}
+TRAFFIC_RATIO_GEMM1 = {
+    "mxfp4": (309.222144 + 6.509056) / 292.782080,  # profiles/mx_gemm_kernel_prof_mxfp4_E64_T512.md
+    "w8a8": (160.090880 + 29.705728) / 108.130304,   # profiles/int_gemm_kernel_w8a8.md
+}
 
 
 def parse():
@@ -363,7 +366,7 @@ def run_ours(args, w):
     tensor_peak = fp8_peak if w.scheme == "mxfp4" else pk["bf16"]
     t_tc = alg["gemm1_flops"] / (tensor_peak * 1e12)
     # DRAM bytes per stage-1 launch from one ncu capture, scaled by units processed
-    # (profiles/mx_gemm_kernel_prof_mxfp4_E64_T512.md): traffic / algorithmic bytes
+    # (the capture's traffic / algorithmic bytes, times this launch's algorithmic bytes)
     ratio = TRAFFIC_RATIO_GEMM1.get(w.scheme)
     traffic = ratio * alg["gemm1_bytes"] if ratio else None
     if t_hbm >= t_tc:
