@@ -250,6 +250,19 @@ int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* s
     return launch_status();
 }
 
+// rint(v / s) with the IEEE quotient, clamped to +-127, usually without a
+// division: r = v * inv (inv = 1/s rounded once) is within |v/s| * 2^-23 +
+// 2^-18 < 2^-16 of the exact quotient for |v / s| <= 127.5 (and the clamp
+// decides everything beyond), so when r is at least 1e-4 away from a
+// half-integer the correctly rounded quotient rounds to the same integer;
+// the rare values nearer a tie take the IEEE division.
+__device__ __forceinline__ float rint_quot_clamped(float v, float s, float inv) {
+    const float r = v * inv;
+    const float frac = r - floorf(r);
+    const float q = (fabsf(frac - 0.5f) > 1e-4f) ? rintf(r) : rintf(__fdiv_rn(v, s));
+    return fminf(fmaxf(q, -127.f), 127.f);
+}
+
 // W8A8 activation tiles: one CTA per 112-row sub-tile (a schedule tile of
 // 224 rows is two of them), one warp per row at a time.  The row (stage 1: the
 // slot's token row of bf16 x; stage 2: the slot's own fp32 h row) is quantised
@@ -324,6 +337,7 @@ quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ so
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+        const float inv = __frcp_rn(sc);
         // chunk j (8 codes): K step j/8 of 64 (block), chunk j%8 of its 128-byte row; 128-element step j/16
         for (int j0 = 0; j0 < K / 8; j0 += 32) {  // warp-uniform trip count (the shuffles below)
             const int j = j0 + lane;
@@ -334,8 +348,8 @@ quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ so
                 uint32_t o[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float q0 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i], sc)), -127.f), 127.f);
-                    const float q1 = fminf(fmaxf(rintf(__fdiv_rn(f[2 * i + 1], sc)), -127.f), 127.f);
+                    const float q0 = rint_quot_clamped(f[2 * i], sc, inv);
+                    const float q1 = rint_quot_clamped(f[2 * i + 1], sc, inv);
                     l1 += abs((int)q0) + abs((int)q1);
                     const __half2 hv = __floats2half2_rn(q0, q1);
                     o[i] = *reinterpret_cast<const uint32_t*>(&hv);
