@@ -51,7 +51,6 @@ constexpr int WARP_W = 0, WARP_B = 1, WARP_MMA = 2;
 constexpr int WARP_CVT0 = 4, CVT_WARPS = 8;
 constexpr int WARP_EPI0 = 12, EPI_WARPS = 8;
 constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
-constexpr int KSTEP = 128;       // K elements per step (two 64-element halves)
 // Drains keep every fp32 partial sum below 2^24: a chunk of steps may add at
 // most L1_BOUND * 128 (|w| <= 128 for int8 weights, sum |x| over the chunk's
 // steps <= L1_BOUND for every row) on top of a remainder |lo| <= 4096.
@@ -59,28 +58,34 @@ constexpr int L1_BOUND = ((1 << 24) - 4097) / 128;
 constexpr int HI_SHIFT = 13;
 constexpr int MAX_E = 512;
 constexpr int MAX_K = 16384;
-constexpr int AS = 2;            // A slots in TMEM
-constexpr int A_SLOT_COLS = 2 * KSTEP / 2;  // two tiles x KSTEP/2 fp16 pairs
-constexpr int BS = 3;            // activation slots
 
 // Per weight format:
 //   W8 (int8, exact int32 sums): tokens per MMA NS = 112 (a 224-row schedule
-//      tile is two of them), raw int8 rows by TMA, two raw slots;
-//   W4 (int4 + fp16 scales):     NS = 128 (a 224-row tile is 128 + 96), raw
-//      pre-packed blocks by bulk copy, three raw slots.
+//      tile is two of them), 128-element steps, raw int8 rows by TMA;
+//   W4 (int4 + fp16 scales):     NS = 160 (a 224-row tile is 160 + 64, so an
+//      expert with up to 160 pairs is one unit), 64-element steps in a
+//      three-slot A ring (the wider accumulators leave 192 TMEM columns),
+//      raw pre-packed blocks by bulk copy.
 // TMEM columns: the fp32 accumulators of the two tiles (2 * NS), then the A
-// ring from column 256.  Shared memory: raw ring, activation ring, and
-// NS x 128 words staging the drains' high parts (W8) and the final outputs.
+// ring.  Shared memory: raw ring, activation ring, and NS x 128 words staging
+// the drains' high parts (W8) and the final outputs.
 template <bool W4>
 struct Cfg {
-    static constexpr int NS = W4 ? 128 : 112;
+    static constexpr int NS = W4 ? 160 : 112;
+    static constexpr int AS = W4 ? 3 : 2;         // A slots in TMEM
+    static constexpr int BS = AS + 1;             // activation slots
+    static constexpr int KSTEP = W4 ? 64 : 128;  // K elements per step
+    static constexpr int HPS = KSTEP / 64;        // 64-element halves per step
+    static constexpr int A_SLOT_COLS = KSTEP;     // two tiles x KSTEP/2 fp16 pairs
     static constexpr int HALF_RAW = W4 ? 2 * bft::kW4Block : 2 * 128 * 64;  // one 64-element half, both tiles
-    static constexpr int RAW_BYTES = 2 * HALF_RAW;
-    static constexpr int RS = W4 ? 3 : 2;
+    static constexpr int RAW_BYTES = HPS * HALF_RAW;
+    static constexpr int RS = W4 ? 4 : 2;         // raw weight slots
     static constexpr int HALF_B = NS * 128;  // one 64-element half of the step's fp16 token rows
-    static constexpr int B_BYTES = 2 * HALF_B;
+    static constexpr int B_BYTES = HPS * HALF_B;
+    static constexpr int CHUNKS = NS / 16;   // 16-token column chunks of an accumulator
+    static constexpr int EPI_CHUNKS = (CHUNKS + 1) / 2;  // per epilogue warp (the warp pair alternates)
     static constexpr uint32_t R_COL = 0;
-    static constexpr uint32_t A_COL = 256;
+    static constexpr uint32_t A_COL = 2 * NS;
     static constexpr int RAW_OFF = 0;
     static constexpr int B_OFF = (RAW_OFF + RS * RAW_BYTES + 1023) / 1024 * 1024;
     static constexpr int S_OFF = B_OFF + BS * B_BYTES;
@@ -90,7 +95,7 @@ struct Cfg {
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SCHED_OFF = MISC_OFF + 64;
     static constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
-    static_assert(R_COL + 2 * NS <= A_COL && A_COL + AS * A_SLOT_COLS <= 512, "TMEM budget");
+    static_assert(R_COL + 2 * NS <= A_COL && A_COL + AS * A_SLOT_COLS <= 512 && NS % 16 == 0, "TMEM budget");
     static_assert(BS >= AS + 1, "a step's done barrier is not reused before the converter has waited on it");
     static_assert(B_OFF % 1024 == 0 && HALF_B % 1024 == 0, "swizzled activation tiles 1024-aligned");
     static_assert(W4 || HALF_RAW % 1024 == 0, "swizzled raw int8 tiles 1024-aligned");
@@ -225,9 +230,9 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* raw_empty = raw_full + C::RS;
     uint64_t* b_full = raw_empty + C::RS;
-    uint64_t* done = b_full + BS;  // step g completed (both issuers' MMAs): frees B slot g % BS and A slot g % AS
-    uint64_t* a_full = done + BS;
-    uint64_t* acc_full = a_full + AS;
+    uint64_t* done = b_full + C::BS;  // step g completed (both issuers' MMAs): frees B slot g % C::BS and A slot g % C::AS
+    uint64_t* a_full = done + C::BS;
+    uint64_t* acc_full = a_full + C::AS;
     uint64_t* acc_empty = acc_full + 1;
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
     const int E = a.E;
     const int K = (STAGE == 1) ? a.H : a.I;
     const int NB = (STAGE == 1) ? a.I / 128 : a.H / 256;
-    const int KT = K / KSTEP;
+    const int KT = K / C::KSTEP;
     const int halves = (a.nmax + C::NS - 1) / C::NS;
 
     for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = a.tile_start[i];
@@ -246,11 +251,11 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             tc::mbar_init(&raw_full[s], 1);
             tc::mbar_init(&raw_empty[s], CVT_WARPS);
         }
-        for (int s = 0; s < BS; ++s) {
+        for (int s = 0; s < C::BS; ++s) {
             tc::mbar_init(&b_full[s], 1);
             tc::mbar_init(&done[s], 2);  // the two issuers' commits
         }
-        for (int s = 0; s < AS; ++s) tc::mbar_init(&a_full[s], CVT_WARPS);
+        for (int s = 0; s < C::AS; ++s) tc::mbar_init(&a_full[s], CVT_WARPS);
         tc::mbar_init(acc_full, 2);
         tc::mbar_init(acc_empty, EPI_WARPS);
         *abort_flag = 0;
@@ -290,20 +295,22 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                         const int64_t rt0 = (STAGE == 1) ? (int64_t)e * (2 * a.I / 128) + nb : (int64_t)e * (a.H / 128) + 2 * nb;
                         const int64_t rt1 = (STAGE == 1) ? rt0 + a.I / 128 : rt0 + 1;
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            tc::bulk_load(dst + (2 * hh) * bft::kW4Block, a.wq + (rt0 * KB + 2 * kt + hh) * bft::kW4Block,
-                                          bft::kW4Block, &raw_full[rs]);
+                        for (int hh = 0; hh < C::HPS; ++hh) {
+                            tc::bulk_load(dst + (2 * hh) * bft::kW4Block,
+                                          a.wq + (rt0 * KB + C::HPS * kt + hh) * bft::kW4Block, bft::kW4Block,
+                                          &raw_full[rs]);
                             tc::bulk_load(dst + (2 * hh + 1) * bft::kW4Block,
-                                          a.wq + (rt1 * KB + 2 * kt + hh) * bft::kW4Block, bft::kW4Block, &raw_full[rs]);
+                                          a.wq + (rt1 * KB + C::HPS * kt + hh) * bft::kW4Block, bft::kW4Block,
+                                          &raw_full[rs]);
                         }
                     } else {
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
+                        for (int hh = 0; hh < C::HPS; ++hh) {
                             if (STAGE == 1)
-                                tc::tma_load_3d(dst + hh * C::HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh,
+                                tc::tma_load_3d(dst + hh * C::HALF_RAW, &wmap, &raw_full[rs], kt * C::KSTEP + 64 * hh,
                                                 nb * 128, 2 * e);
                             else
-                                tc::tma_load_2d(dst + hh * C::HALF_RAW, &wmap, &raw_full[rs], kt * KSTEP + 64 * hh,
+                                tc::tma_load_2d(dst + hh * C::HALF_RAW, &wmap, &raw_full[rs], kt * C::KSTEP + 64 * hh,
                                                 e * a.H + nb * 256);
                         }
                     }
@@ -326,13 +333,13 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&done[bs], ph ^ 1)) { set_abort(abort_flag, a.status); ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&b_full[bs], 2 * bytes);
+                    tc::mbar_arrive_expect_tx(&b_full[bs], C::HPS * bytes);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
+                    for (int hh = 0; hh < C::HPS; ++hh)
                         tc::bulk_load(sB + bs * C::B_BYTES + hh * C::HALF_B,
-                                      a.act + ((int64_t)t * (2 * KT) + 2 * kt + hh) * bb + (int64_t)half * C::NS * 128, bytes,
+                                      a.act + ((int64_t)t * (K / 64) + C::HPS * kt + hh) * bb + (int64_t)half * C::NS * 128, bytes,
                                       &b_full[bs]);
-                    if (++bs == BS) { bs = 0; ph ^= 1; }
+                    if (++bs == C::BS) { bs = 0; ph ^= 1; }
                 }
                 if (!ok) break;
             }
@@ -361,15 +368,15 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                 if (!warp_wait(&b_full[bs], bph, lane) || !warp_wait(&a_full[as], aph, lane)) { ok = false; break; }
                 tc::tc_fence_after();
                 const uint32_t b0 = tc::smem_u32(sB + bs * C::B_BYTES);
-                const uint32_t a0 = tm + C::A_COL + (uint32_t)(as * A_SLOT_COLS + iss * (KSTEP / 2));
+                const uint32_t a0 = tm + C::A_COL + (uint32_t)(as * C::A_SLOT_COLS + iss * (C::KSTEP / 2));
 #pragma unroll
-                for (int kk = 0; kk < KSTEP / 16; ++kk)
+                for (int kk = 0; kk < C::KSTEP / 16; ++kk)
                     tc::mma_f16_ts_elect(dcol, a0 + 8 * kk,
                                          tc::sdesc_kmajor_sw128(b0 + (kk >> 2) * C::HALF_B + 32 * (kk & 3)), idesc,
                                          (kt > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit_elect(&done[bs]);
-                if (++bs == BS) { bs = 0; bph ^= 1; }
-                if (++as == AS) { as = 0; aph ^= 1; }
+                if (++bs == C::BS) { bs = 0; bph ^= 1; }
+                if (++as == C::AS) { as = 0; aph ^= 1; }
                 if (kt == KT - 1 || bit_at(starts, kt + 1)) {
                     tc::mma_commit_elect(acc_full);
                     ++ev;
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         const int sw = (m >> 1) & 3;  // 64-byte swizzle of the TMA box: 16-byte chunk j at j ^ sw
         int rs = 0;
         uint32_t rph = 0;
-        uint32_t gs = 0;  // steps converted so far (all units): A slot gs % AS, done barrier gs % BS
+        uint32_t gs = 0;  // steps converted so far (all units): A slot gs % C::AS, done barrier gs % C::BS
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
@@ -402,13 +409,13 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                     ok = false;
                     break;
                 }
-                // 128 weights of this row -> 64 fp16 pairs, 16 per TMEM store
-                uint32_t o[4][16];
+                // KSTEP weights of this row -> KSTEP/2 fp16 pairs, 16 per TMEM store
+                uint32_t o[2 * C::HPS][16];
                 if constexpr (W4) {
-                    uint4 cw[2][2];
-                    uint32_t sc[2];
+                    uint4 cw[C::HPS][2];
+                    uint32_t sc[C::HPS];
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < C::HPS; ++hh) {
                         const uint8_t* src = sRaw + rs * C::RAW_BYTES + (2 * hh + tile) * bft::kW4Block;
                         cw[hh][0] = *reinterpret_cast<const uint4*>(src + m * 32);
                         cw[hh][1] = *reinterpret_cast<const uint4*>(src + m * 32 + 16);
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                     if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
                     if (++rs == C::RS) { rs = 0; rph ^= 1; }
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < C::HPS; ++hh) {
                         const uint32_t s2a = (sc[hh] & 0xFFFFu) * 0x10001u, s2b = (sc[hh] >> 16) * 0x10001u;
                         const uint32_t wv[8] = {cw[hh][0].x, cw[hh][0].y, cw[hh][0].z, cw[hh][0].w,
                                                 cw[hh][1].x, cw[hh][1].y, cw[hh][1].z, cw[hh][1].w};
@@ -443,19 +450,19 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                             i8x4_to_f16x2(wv[p], o[j >> 1][(j & 1) * 8 + 2 * p], o[j >> 1][(j & 1) * 8 + 2 * p + 1]);
                     }
                 }
-                // the A slot is free once the MMAs of step gs - AS have completed
-                if (gs >= (uint32_t)AS) {
-                    const uint32_t j = gs - AS;
-                    if (!warp_wait(&done[j % BS], (j / BS) & 1u, lane)) {
+                // the A slot is free once the MMAs of step gs - C::AS have completed
+                if (gs >= (uint32_t)C::AS) {
+                    const uint32_t j = gs - C::AS;
+                    if (!warp_wait(&done[j % C::BS], (j / C::BS) & 1u, lane)) {
                         if (lane == 0) set_abort(abort_flag, a.status);
                         ok = false;
                         break;
                     }
                 }
-                const int as = (int)(gs % AS);
-                const uint32_t ta = tm + lane_base + C::A_COL + (uint32_t)(as * A_SLOT_COLS + tile * (KSTEP / 2));
+                const int as = (int)(gs % C::AS);
+                const uint32_t ta = tm + lane_base + C::A_COL + (uint32_t)(as * C::A_SLOT_COLS + tile * (C::KSTEP / 2));
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tmem_st16(ta + 16 * q4, o[q4]);
+                for (int q4 = 0; q4 < 2 * C::HPS; ++q4) tmem_st16(ta + 16 * q4, o[q4]);
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
@@ -502,9 +509,9 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             const int nev = 1 + __popc(starts[0]) + __popc(starts[1]) + __popc(starts[2]) + __popc(starts[3]);
             // this warp's per-token activation scales (chunk i: token 16 * eh + 32 * i + lane, lanes < 16),
             // fetched before the accumulator is ready
-            float fls[4];
+            float fls[C::EPI_CHUNKS];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < C::EPI_CHUNKS; ++i) {
                 const int c = 16 * eh + 32 * i + lane;
                 fls[i] = (lane < 16 && c < ntok) ? ts[c] : 0.f;
             }
@@ -557,7 +564,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                     // final, first pass: the outputs into this thread's shared-memory words (where the
                     // running high parts were), so the accumulator can be handed back before the stores
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < C::EPI_CHUNKS; ++i) {
                         const int c0 = 16 * eh + 32 * i;
                         if (c0 >= ntok) break;
                         uint32_t g[16], v[16];
