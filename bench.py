@@ -60,6 +60,23 @@ def dist_env():
     return rank, world, local
 
 
+def rank_workload(w, rank):
+    """Rank r's replica: its own tokens (seed + 7919 r), the same expert weights."""
+    return gen.Workload(w.name, w.scheme, w.T, w.H, w.E, w.k, w.I, w.routing, w.seed + 7919 * rank, w.wseed)
+
+
+def max_over_ranks(value, world, device):
+    """The largest of the ranks' values (every rank gets it); the value itself at world 1."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ algorithmic work
 
 def weight_bytes_per_row(scheme, K):
@@ -244,7 +261,7 @@ def run_ours(args, w):
     qb.lib()
 
     # each rank: its own tokens (seed + rank), the same expert weights
-    wr = gen.Workload(w.name, w.scheme, w.T, w.H, w.E, w.k, w.I, w.routing, w.seed + 7919 * rank, w.wseed)
+    wr = rank_workload(w, rank)
     d = gen.make_all(wr)
     T, k, H, I, E, P = wr.T, wr.k, wr.H, wr.I, wr.E, wr.P
 
@@ -347,12 +364,7 @@ def run_ours(args, w):
     ms = start.elapsed_time(end) / args.steps
     g1_ms = statistics.mean(a.elapsed_time(b) for a, b in g1_pairs)
     g2_ms = statistics.mean(a.elapsed_time(b) for a, b in g2_pairs)
-    if world > 1:
-        import torch.distributed as dist
-
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(ms, world, dev)
     assert int(status.item()) == 0, "device status flagged an error"
 
     alg = algorithmic(wr, d["topk_ids"])
@@ -414,12 +426,7 @@ def run_ours(args, w):
         e2.record(stream)
         barrier()
         ems = s2.elapsed_time(e2) / args.steps
-        if world > 1:
-            import torch.distributed as dist
-
-            tm = torch.tensor([ems], device=dev)
-            dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-            ems = float(tm.item())
+        ems = max_over_ranks(ems, world, dev)
         h2d = hx.numel() * 2 + hid.numel() * 4 + hw.numel() * 4
         e2e = dict(value=flops_step * world / (ems * 1e-3) / 1e12, unit=UNIT, ms_per_step=ems,
                    h2d_bytes_per_step=h2d, d2h_bytes_per_step=hout.numel() * 2,
