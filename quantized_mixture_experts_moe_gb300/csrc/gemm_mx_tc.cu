@@ -79,13 +79,19 @@ struct Cfg {
     static constexpr int SFA_BYTES = AT * 512;
     static constexpr int SFB_BYTES = NSFB * 512;
     static constexpr int SLOT_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    // stage 1 epilogue: per epilogue warp a 16-token x 32-column transpose
+    // buffer of h (rows padded to 36 floats: the 16-byte reads of 8 rows at
+    // a time hit distinct banks)
+    static constexpr int EPI_ROW = 36;
+    static constexpr int EPI_BYTES = (STAGE == 1) ? EPI_WARPS * 16 * EPI_ROW * 4 : 0;
     // ring depth: as many whole steps as fit in the 227 KB of shared memory
-    static constexpr int S = (220 * 1024 - 8 * 1024) / SLOT_BYTES;
+    static constexpr int S = (220 * 1024 - 8 * 1024 - EPI_BYTES) / SLOT_BYTES;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + S * A_BYTES;
     static constexpr int SFA_OFF = B_OFF + S * B_BYTES;
     static constexpr int SFB_OFF = SFA_OFF + S * SFA_BYTES;
-    static constexpr int BAR_OFF = SFB_OFF + S * SFB_BYTES;
+    static constexpr int EPI_OFF = SFB_OFF + S * SFB_BYTES;
+    static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
     static constexpr int NBAR = 2 * S + 2 * ACC_BUFS;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SCHED_OFF = MISC_OFF + 64;
@@ -302,6 +308,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         const int q = warp & 3;                       // TMEM lane quadrant this warp may access
         const int half = (warp - WARP_EPI0) >> 2;     // which 16-column chunks it takes
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        float* epi = reinterpret_cast<float*>(smem + C::EPI_OFF) + (warp - WARP_EPI0) * 16 * C::EPI_ROW;
         int ab = 0;
         uint32_t pacc = 0;
         for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
@@ -317,36 +324,57 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             const uint32_t dcol = ab * C::ACC_COLS;
             // stage 1 writes h block (tile t, K step nb of the down projection)
             uint8_t* hblk = (STAGE == 1) ? a.h_tiles + ((int64_t)t * (a.I / 128) + nb) * mxt::block_bytes(NMAX) : nullptr;
+            // Chunks of 16 tokens, alternating between the quadrant's two
+            // warps; per chunk the accumulator pair (stage 1: gate, up; stage 2:
+            // column blocks 2nb, 2nb + 1).
             for (int c0 = 16 * half; c0 < ntok; c0 += 32) {
-                uint32_t g[16];
+                uint32_t g[16], g2[16];
                 tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + c0, g);
+                tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + NMAX + c0, g2);
+                tc::tmem_ld_wait();
                 if (STAGE == 1) {
-                    uint32_t uu[16];
-                    tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + NMAX + c0, uu);
-                    tc::tmem_ld_wait();
+                    // h for the chunk (lane = column of the 32-column MX block,
+                    // j = token), transposed through shared memory so that each
+                    // lane then holds 16 columns of one token: lanes t and t + 16
+                    // share token c0 + t.  Columns past ntok are computed but
+                    // not stored.
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int c = c0 + j;
-                        if (c >= ntok) break;  // warp-uniform
                         const float gv = __uint_as_float(g[j]);
-                        const float h = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(uu[j]);
-                        float amax = fabsf(h);
+                        epi[j * C::EPI_ROW + lane] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(g2[j]);
+                    }
+                    __syncwarp();
+                    const int tok = lane & 15, hh = lane >> 4;
+                    float v[16];
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                        uint8_t code = 0, sb = 127;
-                        if (amax > 0.f) {
-                            const int X = mx_block_exponent(amax);
-                            sb = (uint8_t)(X + 127);
-                            code = (uint8_t)(e4m3x2_from_float(h * exp2i(-X), 0.f) & 0xFF);
-                        }
-                        hblk[mxt::code_offset(c, q * 32 + lane)] = code;
-                        if (lane == 0) hblk[mxt::scale_offset(NMAX, c, q)] = sb;
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = *reinterpret_cast<const float4*>(epi + tok * C::EPI_ROW + hh * 16 + 4 * i);
+                        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+                    }
+                    __syncwarp();
+                    float amax = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 16));
+                    uint32_t sb = 127;
+                    uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+                    if (amax > 0.f) {
+                        const int X = mx_block_exponent(amax);
+                        sb = (uint32_t)(X + 127);
+                        const float sc = exp2i(-X);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            w[i] = (uint32_t)e4m3x2_from_float(v[4 * i] * sc, v[4 * i + 1] * sc) |
+                                   ((uint32_t)e4m3x2_from_float(v[4 * i + 2] * sc, v[4 * i + 3] * sc) << 16);
+                        codes = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    if (c0 + tok < ntok) {
+                        *reinterpret_cast<uint4*>(hblk + mxt::code_offset(c0 + tok, q * 32 + hh * 16)) = codes;
+                        if (hh == 0) hblk[mxt::scale_offset(NMAX, c0 + tok, q)] = (uint8_t)sb;
                     }
                 } else {
-                    // stage 2: column blocks 2nb (accumulator 0) and 2nb + 1 (accumulator 1)
-                    uint32_t g2[16];
-                    tc::tmem_ld_32x32b_x16(tm + lane_addr + dcol + NMAX + c0, g2);
-                    tc::tmem_ld_wait();
+                    // stage 2: token rows of y, 64 contiguous bytes per block and token
                     const int n0 = 2 * nb * 128 + q * 32 + lane;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
