@@ -69,6 +69,13 @@ WORKLOADS = {
             _mk(f"decode_T{T}", "mxfp4", T, 4096, 512, 10, 1024, "zipf", 1004 + T, 1002)
             for T in (1, 4, 16, 64)
         ],
+        # tensor-parallel shards of the MXFP4 layer: TP2 keeps inter 512 of
+        # the 1024 columns per rank, TP4 keeps 256 (same experts, hidden, top-k)
+        *[
+            _mk(f"mxfp4_tp{tp}_T{T}", "mxfp4", T, 4096, 512, 10, 1024 // tp, "uniform", 1005 + tp + T, 1005 + tp)
+            for tp in (2, 4)
+            for T in (16, 256, 1024, 4096, 8192)
+        ],
         # profiling stand-in for the T=4096 MXFP4 layer: same per-expert load
         # (about 80 tokens), 64 experts so a capture holds ~0.5 GB of weights
         _mk("prof_mxfp4_E64_T512", "mxfp4", 512, 4096, 64, 10, 1024, "uniform", 1005),

@@ -455,7 +455,9 @@ def _full_inputs(w):
 
 
 FULL = ["decode_T1", "decode_T4", "decode_T16", "decode_T64", "mxfp4_T256", "mxfp4_T1024", "mxfp4_T4096",
-        "mxfp4_T8192", "w4a16_T2048", "w8a8_T8192"]
+        "mxfp4_T8192", "w4a16_T2048", "w8a8_T8192",
+        # tensor-parallel shards: inter 512 (TP2) and 256 (TP4)
+        "mxfp4_tp2_T4096", "mxfp4_tp2_T8192", "mxfp4_tp4_T16", "mxfp4_tp4_T4096"]
 
 
 @pytest.mark.parametrize("name", FULL)
