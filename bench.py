@@ -315,7 +315,7 @@ def run_ours(args, w):
     def step(marks=None):
         qb.qmoe_align_sort(dims, t["topk_ids"], counts, offsets, sorted_ids, slot, status, ws)
         if w.scheme == "mxfp4":
-            qb.qmoe_permute_quant_mxfp8(dims, t["x"], sorted_ids, offsets, xt, ws)
+            qb.qmoe_permute_quant_mxfp8(dims, t["x"], slot, offsets, xt, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_permute_quant_int8(dims, t["x"], sorted_ids, offsets, xt, ws)
         else:

@@ -170,10 +170,12 @@ size_t qmoe_mx_tiles_bytes(const qmoe_dims* d, int64_t K);
 
 /* qmoe_permute_quant_mxfp8 -- the expert-sorted permutation of the routed
  * activations and their MX quantisation (rule of qmoe_quant_act_mxfp8) in one
- * pass: slot s of expert e (offsets[e] <= s < offsets[e+1]) gets the codes of
- * token sorted_pair_ids[s] / k, written as MX activation tiles with K = H.
+ * pass: for every pair p = t*k + j with pair_slot[p] >= 0 (the inverse
+ * permutation from qmoe_align_sort), slot pair_slot[p] of its expert gets the
+ * codes of token t, written as MX activation tiles with K = H.  Each token
+ * row is read and quantised once and written to its k slots.
  * ws = the workspace qmoe_align_sort filled for this routing. */
-int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* pair_slot,
                              const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                              qmoe_stream_t stream);
 

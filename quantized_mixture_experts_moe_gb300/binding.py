@@ -267,9 +267,9 @@ def mx_tiles_bytes(d: Dims, K: int) -> int:
     return int(lib().qmoe_mx_tiles_bytes(ctypes.byref(d), K))
 
 
-def qmoe_permute_quant_mxfp8(d, x, sorted_pair_ids, offsets, x_tiles, ws, stream=None):
+def qmoe_permute_quant_mxfp8(d, x, pair_slot, offsets, x_tiles, ws, stream=None):
     wp, wn = _ws(ws)
-    _check(lib().qmoe_permute_quant_mxfp8(ctypes.byref(d), _ptr(x), _ptr(sorted_pair_ids), _ptr(offsets),
+    _check(lib().qmoe_permute_quant_mxfp8(ctypes.byref(d), _ptr(x), _ptr(pair_slot), _ptr(offsets),
                                           _ptr(x_tiles), wp, wn, _stream(stream)), "qmoe_permute_quant_mxfp8")
 
 

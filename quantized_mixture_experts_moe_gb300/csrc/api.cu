@@ -19,7 +19,7 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
                 cudaStream_t st);
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
                 const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st);
-int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
+int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* pair_slot, const int32_t* offsets,
                             const int32_t* tile_start, uint8_t* tiles, cudaStream_t st);
 int32_t* tile_schedule_in(void* ws, const qmoe_dims* d);
 int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
@@ -76,14 +76,14 @@ static bool mx_ws_ok(const qmoe_dims* d, const void* ws, size_t ws_bytes) {
     return ws && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && ws_bytes >= qmoe_workspace_bytes(d);
 }
 
-extern "C" int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
+extern "C" int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* pair_slot,
                                         const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                                         qmoe_stream_t stream) {
-    int rc = gemm_args_ok(d, {x_bf16, sorted_pair_ids, offsets, x_tiles});
+    int rc = gemm_args_ok(d, {x_bf16, pair_slot, offsets, x_tiles});
     if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
     if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
     if (d->H % 128 != 0) return QMOE_ERR_UNSUPPORTED;
-    return permute_quant_mx_launch(d, x_bf16, sorted_pair_ids, offsets,
+    return permute_quant_mx_launch(d, x_bf16, pair_slot, offsets,
                                    tile_schedule_in(const_cast<void*>(ws), d), x_tiles, (cudaStream_t)stream);
 }
 
@@ -290,7 +290,7 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
             rc = qmoe_gemm2_w4a16(d, (const uint8_t*)at(L.ht), (const uint8_t*)w2, offsets, y, dev_status, aws,
                                   aws_bytes, stream);
     } else if (scheme == 1) {
-        rc = qmoe_permute_quant_mxfp8(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
+        rc = qmoe_permute_quant_mxfp8(d, x_bf16, slot, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)
             rc = qmoe_gemm1_swiglu_mxfp4(d, (const uint8_t*)at(L.xq), (const uint8_t*)w1, (const uint8_t*)w1_s,
                                          offsets, (uint8_t*)at(L.h), dev_status, aws, aws_bytes, stream);

@@ -81,12 +81,13 @@ quant_rows_int8_kernel(const In* __restrict__ x, int64_t cols, int8_t* __restric
     if (threadIdx.x == 0) s[row] = sc;
 }
 
-// Permute + MX-quantise: one warp per expert-sorted slot (8 per CTA).  The
-// slot's token row of bf16 x is quantised with the same rule as
-// quant_mx_bf16_kernel and written straight into the MX activation tile
-// layout (mx_tiles.cuh), so the tensor-core GEMM reads it with bulk copies.
-// A lane owns 16 consecutive elements per pass; neighbouring lanes pair up
-// into one 32-element block.
+// Permute + MX-quantise, token-major: one warp per (token, 1024-element
+// segment of its row), 8 per CTA.  The segment of bf16 x is read once,
+// quantised with the same rule as quant_mx_bf16_kernel, and written to the
+// slot of each of the token's k routed pairs in the MX activation tile layout
+// (mx_tiles.cuh), so the tensor-core GEMM reads it with bulk copies.  A lane
+// owns 16 consecutive elements of each half of the segment; neighbouring
+// lanes pair up into one 32-element block.
 constexpr int kPqWarps = 8;
 
 __device__ __forceinline__ void mx_quant16(const uint4 v0, const uint4 v1, uint4& codes, uint8_t& sb) {
@@ -117,68 +118,77 @@ __device__ __forceinline__ void mx_quant16(const uint4 v0, const uint4 v1, uint4
 }
 
 __global__ void __launch_bounds__(kPqWarps * 32)
-permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
+permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_slot,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
-                        int H, int nmax, int64_t P, uint8_t* __restrict__ tiles) {
+                        int H, int nmax, int T, uint8_t* __restrict__ tiles) {
     const int lane = threadIdx.x & 31;
-    const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
-    int tile = -1, row = 0, tok = 0;
-    if (lane == 0 && slot < P && slot < offsets[E]) {
-        int lo = 0, hi = E;  // largest e with offsets[e] <= slot
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (offsets[mid] <= slot) lo = mid; else hi = mid;
-        }
-        const int local = (int)(slot - offsets[lo]);
-        tile = tile_start[lo] + local / nmax;
-        row = local % nmax;
-        tok = sorted_pair_ids[slot] / k;
-    }
-    tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
-    if (tile < 0) return;  // warp-uniform
-    row = __shfl_sync(0xFFFFFFFFu, row, 0);
-    tok = __shfl_sync(0xFFFFFFFFu, tok, 0);
+    const int nseg = H / 1024 + (H % 1024 != 0);  // 1024-element segments of a row
+    const int64_t wid = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
+    if (wid >= (int64_t)T * nseg) return;  // warp-uniform
+    const int tok = (int)(wid / nseg), seg = (int)(wid % nseg);
     const uint16_t* xr = x + (int64_t)tok * H;
     const int KT = H / 128;
     const int64_t bb = mxt::block_bytes(nmax);
-    uint8_t* tbase = tiles + (int64_t)tile * KT * bb;
     const int nchunk = H / 16;
-    // warp-uniform trip count: every lane reaches the pairwise shuffle
-    for (int j0 = 0; j0 < nchunk; j0 += 64) {
-        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
-        const int ja = j0 + lane, jb = j0 + 32 + lane;
-        if (ja < nchunk) {
-            a0 = *reinterpret_cast<const uint4*>(xr + 16 * ja);
-            a1 = *reinterpret_cast<const uint4*>(xr + 16 * ja + 8);
+    // this segment's 64 chunks of 16 elements, two per lane; every lane
+    // reaches the pairwise shuffle
+    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
+    const int ja = seg * 64 + lane, jb = seg * 64 + 32 + lane;
+    if (ja < nchunk) {
+        a0 = *reinterpret_cast<const uint4*>(xr + 16 * ja);
+        a1 = *reinterpret_cast<const uint4*>(xr + 16 * ja + 8);
+    }
+    if (jb < nchunk) {
+        b0 = *reinterpret_cast<const uint4*>(xr + 16 * jb);
+        b1 = *reinterpret_cast<const uint4*>(xr + 16 * jb + 8);
+    }
+    uint4 ca, cb;
+    uint8_t sa, sbb;
+    mx_quant16(a0, a1, ca, sa);
+    mx_quant16(b0, b1, cb, sbb);
+    for (int j0 = 0; j0 < k; j0 += 32) {
+        // lane i finds pair j0 + i's tile and row (tile -1: invalid expert id)
+        int dtile = -1, drow = 0;
+        if (j0 + lane < k) {
+            const int slot = pair_slot[(int64_t)tok * k + j0 + lane];
+            if (slot >= 0 && slot < offsets[E]) {
+                int lo = 0, hi = E;  // largest e with offsets[e] <= slot
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (offsets[mid] <= slot) lo = mid; else hi = mid;
+                }
+                const int local = slot - offsets[lo];
+                dtile = tile_start[lo] + local / nmax;
+                drow = local % nmax;
+            }
         }
-        if (jb < nchunk) {
-            b0 = *reinterpret_cast<const uint4*>(xr + 16 * jb);
-            b1 = *reinterpret_cast<const uint4*>(xr + 16 * jb + 8);
-        }
-        uint4 ca, cb;
-        uint8_t sa, sbb;
-        mx_quant16(a0, a1, ca, sa);
-        mx_quant16(b0, b1, cb, sbb);
-        if (ja < nchunk) {
-            uint8_t* blk = tbase + (int64_t)(ja >> 3) * bb;
-            *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (ja & 7) * 16)) = ca;
-            if ((ja & 1) == 0) blk[mxt::scale_offset(nmax, row, (ja >> 1) & 3)] = sa;
-        }
-        if (jb < nchunk) {
-            uint8_t* blk = tbase + (int64_t)(jb >> 3) * bb;
-            *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (jb & 7) * 16)) = cb;
-            if ((jb & 1) == 0) blk[mxt::scale_offset(nmax, row, (jb >> 1) & 3)] = sbb;
+        const int jn = min(32, k - j0);
+        for (int j = 0; j < jn; ++j) {
+            const int tile = __shfl_sync(0xFFFFFFFFu, dtile, j);
+            const int row = __shfl_sync(0xFFFFFFFFu, drow, j);
+            if (tile < 0) continue;  // warp-uniform
+            uint8_t* tbase = tiles + (int64_t)tile * KT * bb;
+            if (ja < nchunk) {
+                uint8_t* blk = tbase + (int64_t)(ja >> 3) * bb;
+                *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (ja & 7) * 16)) = ca;
+                if ((ja & 1) == 0) blk[mxt::scale_offset(nmax, row, (ja >> 1) & 3)] = sa;
+            }
+            if (jb < nchunk) {
+                uint8_t* blk = tbase + (int64_t)(jb >> 3) * bb;
+                *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (jb & 7) * 16)) = cb;
+                if ((jb & 1) == 0) blk[mxt::scale_offset(nmax, row, (jb >> 1) & 3)] = sbb;
+            }
         }
     }
 }
 
-int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* sorted, const int32_t* offsets,
+int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* pair_slot, const int32_t* offsets,
                             const int32_t* tile_start, uint8_t* tiles, cudaStream_t st) {
-    const int64_t P = (int64_t)d->T * d->k;
-    if (P == 0) return QMOE_OK;
-    const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
-    permute_quant_mx_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, sorted, offsets, tile_start, d->E, d->k,
-                                                                       d->H, mxt::nmax_for(d), P, tiles);
+    if ((int64_t)d->T * d->k == 0) return QMOE_OK;
+    const int64_t warps = (int64_t)d->T * (d->H / 1024 + (d->H % 1024 != 0));
+    const int64_t blocks = (warps + kPqWarps - 1) / kPqWarps;
+    permute_quant_mx_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, pair_slot, offsets, tile_start, d->E, d->k,
+                                                                       d->H, mxt::nmax_for(d), d->T, tiles);
     return launch_status();
 }
 

@@ -85,7 +85,7 @@ def run_layer(w, inp, keep=False):
     elif w.scheme == "mxfp4":
         xt = empty(qb.mx_tiles_bytes(d, H), torch.uint8)
         ht = empty(qb.mx_tiles_bytes(d, I), torch.uint8)
-        qb.qmoe_permute_quant_mxfp8(d, t["x"], sorted_ids, offsets, xt, ws)
+        qb.qmoe_permute_quant_mxfp8(d, t["x"], slot, offsets, xt, ws)
         w1, w1p, w2, w2p = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
         qb.qmoe_gemm1_swiglu_mxfp4(d, xt, w1, w1p, offsets, ht, status, ws)
         qb.qmoe_gemm2_mxfp4(d, ht, w2, w2p, offsets, y, status, ws)
