@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qmoe_oracle.c")
 _LIB = os.path.join(_HERE, "libqmoe_oracle.so")
 
-SCHEME_ID = {"w4a16": 0, "mxfp4": 1, "w8a8": 2}
+SCHEME_ID = {"w4a16": 0, "mxfp4": 1, "w8a8": 2, "w4a8": 3}
 
 
 def build(force: bool = False) -> str:
@@ -132,7 +132,7 @@ def quant_act(scheme: str, x_bf16: np.ndarray):
     if scheme == "mxfp4":
         q = np.empty((rows, cols), np.uint8)
         s = np.empty((rows, cols // 32), np.uint8)
-    elif scheme == "w8a8":
+    elif scheme in ("w8a8", "w4a8"):
         q = np.empty((rows, cols), np.int8)
         s = np.empty(rows, np.float32)
     else:

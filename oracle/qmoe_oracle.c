@@ -40,6 +40,13 @@
  *            gives scale byte 127 and zero codes (OCP MX v1.0 conversion).
  *   int8     per row: s = amax / 127 (fp32; 1 when amax == 0),
  *            q = clamp(rint(v / s), -127, 127) in fp32.
+ *
+ * W4A8 (the gfx1151 page, Constraint: int4 weights widened to 8-bit integers
+ * before an integer MMA, with 8-bit activations): weights are int4 codes in
+ * the int4 byte layout above with one fp32 scale per output channel (a scale
+ * inside the K sum would break the integer dot), activations and the
+ * intermediate are int8 per row, and everything after the weight decode is
+ * the W8A8 arithmetic.
  */
 #include <math.h>
 #include <stdint.h>
@@ -49,7 +56,10 @@
 #include <omp.h>
 #endif
 
-enum { SCHEME_W4A16 = 0, SCHEME_MXFP4 = 1, SCHEME_W8A8 = 2 };
+enum { SCHEME_W4A16 = 0, SCHEME_MXFP4 = 1, SCHEME_W8A8 = 2, SCHEME_W4A8 = 3 };
+
+/* schemes whose dots are exact integer sums of int8-range codes */
+static int integer_scheme(int scheme) { return scheme == SCHEME_W8A8 || scheme == SCHEME_W4A8; }
 
 /* ------------------------------------------------------------ decoders */
 
@@ -176,7 +186,7 @@ int oracle_quant_act(int scheme, int64_t rows, int64_t cols, const uint16_t* x, 
         for (int64_t i = 0; i < cols; ++i) buf[i] = (float)oracle_bf16_to_double(x[r * cols + i]);
         if (scheme == SCHEME_MXFP4)
             oracle_mx_quant(buf, cols, q + r * cols, (uint8_t*)s + r * (cols / 32));
-        else if (scheme == SCHEME_W8A8)
+        else if (integer_scheme(scheme))
             oracle_int8_quant(buf, 1, cols, (int8_t*)q + r * cols, (float*)s + r);
         else {
             free(buf);
@@ -256,6 +266,21 @@ static void dequant_row(int scheme, const uint8_t* w, const void* ws, int64_t R,
     }
 }
 
+/* Integer codes of row `row` of expert e of a [E, R, K] weight (W8A8: int8
+ * as stored; W4A8: int4 nibbles n -> n - 8) into out[K]. */
+static void int_row(int scheme, const void* w, int64_t R, int64_t K, int e, int64_t row, int8_t* out) {
+    if (scheme == SCHEME_W8A8) {
+        memcpy(out, (const int8_t*)w + ((int64_t)e * R + row) * K, (size_t)K);
+        return;
+    }
+    const uint8_t* wr = (const uint8_t*)w + ((int64_t)e * R + row) * (K / 2);
+    for (int64_t kk = 0; kk < K; ++kk) {
+        uint8_t byte = wr[kk / 2];
+        uint8_t nib = (kk & 1) ? (byte >> 4) : (byte & 15);
+        out[kk] = (int8_t)((int)oracle_int4_to_double(nib));
+    }
+}
+
 static double dot(const double* a, const double* b, int64_t n) {
     double acc = 0.0;
     for (int64_t i = 0; i < n; ++i) acc += a[i] * b[i];
@@ -284,9 +309,10 @@ typedef struct {
 static int down_row(const model_t* m, int e, const hrow_t* h, double* wrow, double* y, int32_t* acc_out) {
     int H = m->H, I = m->I;
     int err = 0;
+    int8_t* wr = integer_scheme(m->scheme) ? (int8_t*)malloc((size_t)I) : NULL;
     for (int c = 0; c < H; ++c) {
-        if (m->scheme == SCHEME_W8A8) {
-            const int8_t* wr = (const int8_t*)m->w2 + ((int64_t)e * H + c) * I;
+        if (integer_scheme(m->scheme)) {
+            int_row(m->scheme, m->w2, H, I, e, c, wr);
             int64_t acc = idot8(h->hq8, wr, I);
             if (acc > INT32_MAX || acc < INT32_MIN) err = 1;
             if (acc_out) acc_out[c] = (int32_t)acc;
@@ -298,6 +324,7 @@ static int down_row(const model_t* m, int e, const hrow_t* h, double* wrow, doub
             y[c] = dot(h->hd, wrow, I);
         }
     }
+    free(wr);
     return err;
 }
 
@@ -305,8 +332,8 @@ static int down_row(const model_t* m, int e, const hrow_t* h, double* wrow, doub
  * intermediates: row r goes through expert experts[r].
  *   W4A16: h bf16 bits [rows, I]
  *   MXFP4: h e4m3 [rows, I], h_s E8M0 [rows, I/32]
- *   W8A8:  h int8 [rows, I], h_s fp32 [rows]
- * y is double [rows, H]; acc2 (W8A8, nullable) int32 [rows, H]. */
+ *   W8A8, W4A8: h int8 [rows, I], h_s fp32 [rows]
+ * y is double [rows, H]; acc2 (W8A8, W4A8; nullable) int32 [rows, H]. */
 int oracle_stage2(int scheme, int64_t rows, int H, int I, int E, const int32_t* experts, const void* h,
                   const void* h_s, const void* w2, const void* w2s, double* y, int32_t* acc2) {
     model_t m = {scheme, H, I, E, NULL, NULL, w2, w2s};
@@ -346,11 +373,12 @@ int oracle_stage2(int scheme, int64_t rows, int H, int I, int E, const int32_t* 
  *   W4A16: w1 int4 [E, 2I, H/2], w1s fp16 [E, 2I, H/32]; w2 [E, H, I/2], w2s [E, H, I/32]
  *   MXFP4: same with E2M1 bytes and E8M0 scales
  *   W8A8:  w1 int8 [E, 2I, H], w1s fp32 [E, 2I]; w2 int8 [E, H, I], w2s fp32 [E, H]
+ *   W4A8:  as W8A8 with int4 bytes w1 [E, 2I, H/2] and w2 [E, H, I/2]
  * Outputs: out double [ntok, H].  Debug outputs (each nullable), row i*k + j:
  *   dbg_h    fp32 [ntok*k, I]  intermediate before Q_h
  *   dbg_hq   Q_h codes [ntok*k, I] (bf16 bits for W4A16, e4m3, int8)
  *   dbg_hs   Q_h scales (E8M0 [ntok*k, I/32] or fp32 [ntok*k])
- *   dbg_acc1 int32 [ntok*k, 2I] (W8A8 gate/up accumulators)
+ *   dbg_acc1 int32 [ntok*k, 2I] (W8A8, W4A8 gate/up accumulators)
  *   dbg_y    double [ntok*k, H] down projection before the weighted sum
  * Pairs whose id is outside [0, E) contribute nothing; the return value is
  * minus the number of such pairs (0 when all are valid), or -2^30 when an
@@ -375,6 +403,8 @@ int64_t oracle_moe_forward(int scheme, int64_t T, int k, int H, int I, int E, co
         uint8_t* q8 = (uint8_t*)malloc(H > I ? H : I);
         uint8_t* s8 = (uint8_t*)malloc((H > I ? H : I) / 32 + 1);
         int8_t* hq8 = (int8_t*)malloc(I);
+        int8_t* wg = (int8_t*)malloc(H);
+        int8_t* wu = (int8_t*)malloc(H);
         float sa = 1.0f;
 
         /* the token's activation as the scheme consumes it */
@@ -382,7 +412,7 @@ int64_t oracle_moe_forward(int scheme, int64_t T, int k, int H, int I, int E, co
         if (scheme == SCHEME_MXFP4) {
             oracle_mx_quant(xf, H, q8, s8);
             for (int c = 0; c < H; ++c) a[c] = oracle_e4m3_to_double(q8[c]) * oracle_e8m0_to_double(s8[c / 32]);
-        } else if (scheme == SCHEME_W8A8) {
+        } else if (integer_scheme(scheme)) {
             oracle_int8_quant(xf, 1, H, (int8_t*)q8, &sa);
         } else {
             for (int c = 0; c < H; ++c) a[c] = (double)xf[c];
@@ -401,9 +431,9 @@ int64_t oracle_moe_forward(int scheme, int64_t T, int k, int H, int I, int E, co
             /* gate/up projection and SwiGLU, h[n] for n < I */
             for (int n = 0; n < I; ++n) {
                 double g, u;
-                if (scheme == SCHEME_W8A8) {
-                    const int8_t* wg = (const int8_t*)w1 + ((int64_t)e * 2 * I + n) * H;
-                    const int8_t* wu = (const int8_t*)w1 + ((int64_t)e * 2 * I + I + n) * H;
+                if (integer_scheme(scheme)) {
+                    int_row(scheme, w1, 2 * I, H, e, n, wg);
+                    int_row(scheme, w1, 2 * I, H, e, I + n, wu);
                     int64_t ag = idot8((const int8_t*)q8, wg, H);
                     int64_t au = idot8((const int8_t*)q8, wu, H);
                     if (ag > INT32_MAX || ag < INT32_MIN || au > INT32_MAX || au < INT32_MIN) overflow = 1;
@@ -463,6 +493,8 @@ int64_t oracle_moe_forward(int scheme, int64_t T, int k, int H, int I, int E, co
         free(q8);
         free(s8);
         free(hq8);
+        free(wg);
+        free(wu);
     }
     if (overflow) return -(1 << 30);
     return -invalid;

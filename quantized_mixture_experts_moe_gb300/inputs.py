@@ -10,7 +10,9 @@ Workloads follow the shapes the source pages describe:
   * "perf(qmoe): group prefill expert matmuls" -- symmetric int4 expert
     projections (W4A16 here, per-32 fp16 scales).
   * "Evaluate native IU4/IU8 WMMA for grouped-INT MoE prefill on gfx1151",
-    Constraint -- int8 x int8 with int32 accumulation (W8A8 here).
+    Constraint -- int8 x int8 with int32 accumulation (W8A8 here), and int4
+    weights widened to 8-bit integers before the integer MMA (W4A8 here:
+    int4 codes with per-output-channel fp32 scales, int8 activations).
   * the aiter tuned grouped-fmoe page, Changes -- model_dim 4096, 512 experts,
     top-10, inter_dim 1024, fp8 activations with MXFP4 weights.
 The pages measure on real models and GSM8K; none is available here, so every
@@ -25,7 +27,7 @@ import math
 
 import numpy as np
 
-SCHEMES = ("w4a16", "mxfp4", "w8a8")
+SCHEMES = ("w4a16", "mxfp4", "w8a8", "w4a8")
 
 
 @dataclasses.dataclass(frozen=True)
@@ -65,6 +67,8 @@ WORKLOADS = {
             for T in (256, 1024, 4096, 8192)
         ],
         _mk("w8a8_T8192", "w8a8", 8192, 4096, 64, 8, 1408, "uniform", 1003),
+        # int4 weights widened to 8-bit integers, int8 activations: the W8A8 layer's shape
+        _mk("w4a8_T8192", "w4a8", 8192, 4096, 64, 8, 1408, "uniform", 1010),
         *[
             _mk(f"decode_T{T}", "mxfp4", T, 4096, 512, 10, 1024, "zipf", 1004 + T, 1002)
             for T in (1, 4, 16, 64)
@@ -186,9 +190,9 @@ def int8_values(rng, shape):
     return rng.integers(-127, 128, size=shape, dtype=np.int8)
 
 
-def int8_channel_scales(rng, shape, K):
-    """Per-output-channel fp32 scales U(0.5, 1.5) / (127 * sqrt(K))."""
-    return (rng.uniform(0.5, 1.5, size=shape) / (127.0 * math.sqrt(K))).astype(np.float32)
+def int8_channel_scales(rng, shape, K, qmax=127.0):
+    """Per-output-channel fp32 scales U(0.5, 1.5) / (qmax * sqrt(K))."""
+    return (rng.uniform(0.5, 1.5, size=shape) / (qmax * math.sqrt(K))).astype(np.float32)
 
 
 # ---------------------------------------------------------------- bundles
@@ -237,6 +241,13 @@ def make_weights(w: Workload):
             w2=int8_values(rng, (E, H, I)),
             w2_s=int8_channel_scales(rng, (E, H), I),
         )
+    if w.scheme == "w4a8":
+        return dict(
+            w1=int4_bytes(rng, (E, 2 * I, H // 2)),
+            w1_s=int8_channel_scales(rng, (E, 2 * I), H, 7.0),
+            w2=int4_bytes(rng, (E, H, I // 2)),
+            w2_s=int8_channel_scales(rng, (E, H), I, 7.0),
+        )
     raise ValueError(w.scheme)
 
 
@@ -260,7 +271,7 @@ def make_stage2_inputs(w: Workload, rows: int):
         codes = _raw_bytes(rng, rows * I).reshape(rows, I)
         codes[(codes & 0x7F) == 0x7F] ^= 0x01  # no NaN codes: 0x7F/0xFF -> 0x7E/0xFE
         return dict(experts=experts, h=codes, h_s=e8m0_bytes(rng, (rows, I // 32), 118, 126))
-    if w.scheme == "w8a8":
+    if w.scheme in ("w8a8", "w4a8"):
         return dict(
             experts=experts,
             h=int8_values(rng, (rows, I)),

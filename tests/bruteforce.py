@@ -72,17 +72,20 @@ def moe_dense(scheme, dims, inp):
         for j in range(k):
             mask[t, ids[t, j]] += tw[t, j]
     out = np.zeros((T, H), np.float64)
-    if scheme == "w8a8":
+    if scheme in ("w8a8", "w4a8"):
+        # W4A8: int4 codes widened to integers (nibble n -> n - 8), then the W8A8 arithmetic
+        ints = (lambda w: w.astype(np.int64)) if scheme == "w8a8" else \
+            (lambda w: unpack_nibbles(w).astype(np.int64) - 8)
         xq, xs = int8_rows(x.astype(np.float32))
         for e in range(E):
-            w1 = inp["w1"][e].astype(np.int64)  # [2I, H]
+            w1 = ints(inp["w1"][e])  # [2I, H]
             acc = xq @ w1.T  # exact integers
             sw = inp["w1_s"][e]
             gu = (acc.astype(np.float32) * xs[:, None]).astype(np.float32) * sw[None, :]
             g, u = gu[:, :I].astype(np.float64), gu[:, I:].astype(np.float64)
             h = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
             hq, hs = int8_rows(h)
-            acc2 = hq @ inp["w2"][e].astype(np.int64).T
+            acc2 = hq @ ints(inp["w2"][e]).T
             y = (acc2.astype(np.float32) * hs[:, None]).astype(np.float32) * inp["w2_s"][e][None, :]
             out += mask[:, e:e + 1] * y.astype(np.float64)
         return out

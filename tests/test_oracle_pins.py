@@ -191,7 +191,7 @@ def _tiny(scheme, T=12, H=128, E=6, k=2, I=64, seed=5):
     return w, gen.make_all(w)
 
 
-@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8", "w4a8"])
 def test_forward_matches_dense_bruteforce(scheme):
     w, d = _tiny(scheme)
     dims = (w.T, w.k, w.H, w.I, w.E)
@@ -251,6 +251,35 @@ def test_w8a8_accumulators_exact():
     assert np.array_equal(y, dbg["y"])
 
 
+def test_w4a8_is_w8a8_on_the_widened_codes():
+    # W4A8 reduces to W8A8 once the int4 nibbles are written out as int8 values
+    w, d = _tiny("w4a8", seed=19)
+    dims = (w.T, w.k, w.H, w.I, w.E)
+    out4, dbg4, _ = oracle.moe_forward("w4a8", dims, d, debug=True)
+    widen = lambda b: (bf.unpack_nibbles(b).astype(np.int16) - 8).astype(np.int8)
+    d8 = dict(d, w1=widen(d["w1"]), w2=widen(d["w2"]))
+    assert d8["w1"].min() >= -7 and d8["w1"].max() <= 7
+    out8, dbg8, _ = oracle.moe_forward("w8a8", dims, d8, debug=True)
+    assert np.array_equal(out4, out8)
+    assert np.array_equal(dbg4["acc1"], dbg8["acc1"])
+    # the gate/up accumulators are the integer products of the widened codes
+    xq, _ = oracle.quant_act("w4a8", d["x"])
+    for t in range(w.T):
+        for j in range(w.k):
+            e = d["topk_ids"][t, j]
+            assert np.array_equal(dbg4["acc1"][t * w.k + j], d8["w1"][e].astype(np.int64) @ xq[t].astype(np.int64))
+
+
+def test_w4a8_largest_sums_fit_fp32_exactly():
+    # |code| <= 7 and |x| <= 127: every partial sum of a K <= 16384 dot stays below 2^24
+    assert 7 * 127 * 16384 < 2 ** 24
+    K = 16384
+    a = np.full(K, 127, np.int64)
+    w_ = np.full(K, -7, np.int64)
+    s = int(a @ w_)
+    assert s == -7 * 127 * K and float(np.float32(s)) == s
+
+
 def test_w8a8_adversarial_extremes_fit_int32():
     # all +-127 operands: the largest |dot| a K=4096 row can reach
     K = 4096
@@ -260,7 +289,7 @@ def test_w8a8_adversarial_extremes_fit_int32():
     assert ref == -127 * 127 * K and abs(ref) < 2 ** 31
 
 
-@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8", "w4a8"])
 def test_invariants(scheme):
     w, d = _tiny(scheme, seed=11)
     dims = (w.T, w.k, w.H, w.I, w.E)
@@ -281,7 +310,8 @@ def test_invariants(scheme):
     # x = 0 and W2 = 0 give 0
     d5 = dict(d, x=np.zeros_like(d["x"]))
     assert not oracle.moe_forward(scheme, dims, d5).any()
-    zero_w2 = np.zeros_like(d["w2"]) if scheme == "w8a8" else np.full_like(d["w2"], 0x88 if scheme == "w4a16" else 0)
+    zero_w2 = np.zeros_like(d["w2"]) if scheme == "w8a8" else \
+        np.full_like(d["w2"], 0x88 if scheme in ("w4a16", "w4a8") else 0)
     d6 = dict(d, w2=zero_w2)
     assert not oracle.moe_forward(scheme, dims, d6).any()
     # a token subset returns exactly those rows
