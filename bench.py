@@ -87,6 +87,8 @@ def weight_bytes_per_row(scheme, K):
         return K // 2 + 2 * (K // 32)
     if scheme == "mxfp4":
         return K // 2 + K // 32
+    if scheme == "w4a8":
+        return K // 2 + 4
     return K + 4
 
 
@@ -295,7 +297,7 @@ def run_ours(args, w):
     if w.scheme == "mxfp4":
         xt = E_(qb.mx_tiles_bytes(dims, H), torch.uint8)
         ht = E_(qb.mx_tiles_bytes(dims, I), torch.uint8)
-    elif w.scheme == "w8a8":
+    elif w.scheme in ("w8a8", "w4a8"):
         xt = E_(qb.w8a8_tiles_bytes(dims, H), torch.uint8)
         h32 = E_((P, I), torch.float32)
         ht = E_(qb.w8a8_tiles_bytes(dims, I), torch.uint8)
@@ -316,7 +318,7 @@ def run_ours(args, w):
         qb.qmoe_align_sort(dims, t["topk_ids"], counts, offsets, sorted_ids, slot, status, ws)
         if w.scheme == "mxfp4":
             qb.qmoe_permute_quant_mxfp8(dims, t["x"], slot, offsets, xt, ws)
-        elif w.scheme == "w8a8":
+        elif w.scheme in ("w8a8", "w4a8"):
             qb.qmoe_permute_quant_int8(dims, t["x"], sorted_ids, offsets, xt, ws)
         else:
             qb.qmoe_permute_x_f16(dims, t["x"], sorted_ids, offsets, xt, ws)
@@ -326,6 +328,8 @@ def run_ours(args, w):
             qb.qmoe_gemm1_swiglu_mxfp4(dims, xt, t["w1"], t["w1_s"], offsets, ht, status, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_gemm1_swiglu_w8a8(dims, xt, t["w1"], t["w1_s"], offsets, h32, None, status, ws)
+        elif w.scheme == "w4a8":
+            qb.qmoe_gemm1_swiglu_w4a8(dims, xt, t["w1"], t["w1_s"], offsets, h32, None, status, ws)
         else:
             qb.qmoe_gemm1_swiglu_w4a16(dims, xt, t["w1"], offsets, ht, status, ws)
         if marks:
@@ -335,6 +339,9 @@ def run_ours(args, w):
         elif w.scheme == "w8a8":
             qb.qmoe_quant_tiles_int8_f32(dims, h32, offsets, ht, ws)
             qb.qmoe_gemm2_w8a8(dims, ht, t["w2"], t["w2_s"], offsets, y, None, status, ws)
+        elif w.scheme == "w4a8":
+            qb.qmoe_quant_tiles_int8_f32(dims, h32, offsets, ht, ws)
+            qb.qmoe_gemm2_w4a8(dims, ht, t["w2"], t["w2_s"], offsets, y, None, status, ws)
         else:
             qb.qmoe_w4a16_h_to_f16(dims, ht, offsets, h16, ws)
             qb.qmoe_gemm2_w4a16(dims, h16, t["w2"], offsets, y, status, ws)
@@ -342,7 +349,7 @@ def run_ours(args, w):
             marks[2].record()
         qb.qmoe_combine(dims, y, t["topk_w"], slot, out)
 
-    launches_per_step = 4 + 1 + 2 + (1 if w.scheme in ("w8a8", "w4a16") else 0) + 1
+    launches_per_step = 4 + 1 + 2 + (1 if w.scheme in ("w8a8", "w4a8", "w4a16") else 0) + 1
 
     def barrier():
         if world > 1:
@@ -476,7 +483,8 @@ def run_ours(args, w):
         line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                     ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype=dict(
                         mxfp4="e4m3 x e2m1 (fp32 accumulate)", w4a16="f16 x f16 (int4 dequantised on chip; fp32 accumulate)",
-                        w8a8="int8 codes as exact f16 (exact int32 sums)")[w.scheme], data="synthetic",
+                        w8a8="int8 codes as exact f16 (exact int32 sums)",
+                        w4a8="int4 x int8 codes as exact f16 (exact int32 sums)")[w.scheme], data="synthetic",
                     config=dict(workload=w.name, scheme=w.scheme, T=T, H=H, E=E, k=k, I=I,
                                 experts_touched=alg["experts_touched"],
                                 l2=(f"L2 flushed before every timed step (2 x L2 written outside the step's events): "

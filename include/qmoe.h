@@ -352,6 +352,19 @@ int qmoe_gemm1_swiglu_w8a8(const qmoe_dims* d, const uint8_t* x_tiles, const int
                            const int32_t* offsets, float* h, int32_t* dbg_acc, int32_t* dev_status, void* ws,
                            size_t ws_bytes, qmoe_stream_t stream);
 
+/* W4A8 ([gfx1151] Constraint: int4 weights widened to 8-bit integers before
+ *        the integer MMA, with int8 activations).  As W8A8 in every argument
+ *        and rule except the weights: w1 holds int4 codes q in [-7, 7] as
+ *        bytes [E, 2I, H/2] (byte i of a row: code 2i in the low nibble, code
+ *        2i+1 in the high nibble, stored n = q + 8; 16-byte aligned), with
+ *        one fp32 scale per output channel in w1_s [E, 2I].  The codes are
+ *        widened on chip to exact fp16 integers; |q| <= 7 keeps every fp32
+ *        partial sum below 2^24 for H, I <= 16384, so the sums are exact with
+ *        no carry passes.  dbg_acc as for W8A8. */
+int qmoe_gemm1_swiglu_w4a8(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const float* w1_s,
+                           const int32_t* offsets, float* h, int32_t* dbg_acc, int32_t* dev_status, void* ws,
+                           size_t ws_bytes, qmoe_stream_t stream);
+
 /* ---------------------------------------------------------------- stage 2: down projection
  *
  * y[s][c] = W2[e][c] . hq[s] for c < H, slots of expert e as above, summed
@@ -382,6 +395,12 @@ int qmoe_gemm2_w8a8(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2
                     const int32_t* offsets, uint16_t* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
                     size_t ws_bytes, qmoe_stream_t stream);
 
+/* W4A8: as W8A8 stage 2 with w2 int4 codes [E, H, I/2] (layout of stage 1)
+ *        and w2_s fp32 [E, H]. */
+int qmoe_gemm2_w4a8(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const float* w2_s,
+                    const int32_t* offsets, uint16_t* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
+                    size_t ws_bytes, qmoe_stream_t stream);
+
 /* ---------------------------------------------------------------- combine
  *
  * qmoe_combine -- out[t][c] = bf16( sum_{j=0..k-1} topk_w[t][j] * y[pair_slot[t*k+j]][c] ),
@@ -396,9 +415,9 @@ int qmoe_combine(const qmoe_dims* d, const uint16_t* y, const float* topk_w, con
 /* ---------------------------------------------------------------- whole layer
  *
  * One call for the whole path: routing, activation quantisation (MXFP4,
- * W8A8), stage 1, intermediate quantisation (W8A8), stage 2 and combine, all
- * launched in order on `stream`.  scheme: 0 = W4A16, 1 = MXFP4 x FP8,
- * 2 = W8A8.  Weights and scales as for the per-stage calls (MXFP4 weights
+ * W8A8, W4A8), stage 1, intermediate quantisation (W8A8, W4A8), stage 2 and
+ * combine, all launched in order on `stream`.  scheme: 0 = W4A16, 1 = MXFP4
+ * x FP8, 2 = W8A8, 3 = W4A8.  Weights and scales as for the per-stage calls (MXFP4 weights
  * and scales pre-packed; W4A16 weights pre-packed with their scales, so
  * w1_s and w2_s are ignored and may be NULL for scheme 0).  All
  * intermediates live in the caller's workspace of

@@ -275,9 +275,8 @@ static void int_row(int scheme, const void* w, int64_t R, int64_t K, int e, int6
     }
     const uint8_t* wr = (const uint8_t*)w + ((int64_t)e * R + row) * (K / 2);
     for (int64_t kk = 0; kk < K; ++kk) {
-        uint8_t byte = wr[kk / 2];
-        uint8_t nib = (kk & 1) ? (byte >> 4) : (byte & 15);
-        out[kk] = (int8_t)((int)oracle_int4_to_double(nib));
+        uint8_t code = (uint8_t)((wr[kk / 2] >> (4 * (kk % 2))) & 15);
+        out[kk] = (int8_t)((int)oracle_int4_to_double(code));
     }
 }
 

@@ -16,7 +16,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmoe.so")
 
-SCHEME_ID = {"w4a16": 0, "mxfp4": 1, "w8a8": 2}
+SCHEME_ID = {"w4a16": 0, "mxfp4": 1, "w8a8": 2, "w4a8": 3}
 DEV_BAD_EXPERT_ID = 1
 DEV_WAIT_TIMEOUT = 2
 
@@ -65,6 +65,8 @@ SIGNATURES = {
     "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_w4a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm2_w4a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_combine": ([_DP, _vp, _vp, _vp, _vp, _vp], _i32),
     "qmoe_forward_workspace_bytes": ([_DP, _i32], _sz),
     "qmoe_moe_forward": ([_i32, _DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -324,6 +326,19 @@ def qmoe_gemm2_w8a8(d, h_tiles, w2, w2_s, offsets, y, dbg_acc, status, ws, strea
 def qmoe_combine(d, y, topk_w, pair_slot, out, stream=None):
     _check(lib().qmoe_combine(ctypes.byref(d), _ptr(y), _ptr(topk_w), _ptr(pair_slot), _ptr(out), _stream(stream)),
            "qmoe_combine")
+
+
+def qmoe_gemm1_swiglu_w4a8(d, x_tiles, w1, w1_s, offsets, h, dbg_acc, status, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_w4a8(ctypes.byref(d), _ptr(x_tiles), _ptr(w1), _ptr(w1_s), _ptr(offsets), _ptr(h),
+                                        _ptr(dbg_acc), _ptr(status), wp, wn, _stream(stream)),
+           "qmoe_gemm1_swiglu_w4a8")
+
+
+def qmoe_gemm2_w4a8(d, h_tiles, w2, w2_s, offsets, y, dbg_acc, status, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm2_w4a8(ctypes.byref(d), _ptr(h_tiles), _ptr(w2), _ptr(w2_s), _ptr(offsets), _ptr(y),
+                                 _ptr(dbg_acc), _ptr(status), wp, wn, _stream(stream)), "qmoe_gemm2_w4a8")
 
 
 def qmoe_moe_forward(scheme, d, x, topk_ids, topk_w, w1, w1_s, w2, w2_s, out, dev_status, ws, stream=None):

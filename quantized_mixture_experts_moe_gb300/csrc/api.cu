@@ -36,6 +36,12 @@ int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, co
 int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
                 const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* dbg_acc, int32_t* status,
                 cudaStream_t st);
+int i4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const float* w1_s,
+                const int32_t* offsets, const int32_t* tile_start, float* h, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st);
+int i4_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const float* w2_s,
+                const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st);
 int h_to_f16_launch(const qmoe_dims* d, const uint8_t* h_tiles, const int32_t* offsets, const int32_t* tile_start,
                     uint8_t* out, cudaStream_t st);
 int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool from_bf16_tokens,
@@ -220,6 +226,32 @@ extern "C" int qmoe_gemm2_w8a8(const qmoe_dims* d, const uint8_t* h_tiles, const
                        (cudaStream_t)stream);
 }
 
+// ------------------------------------------------------------------ W4A8 (int4 weights widened to exact integers)
+
+extern "C" int qmoe_gemm1_swiglu_w4a8(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const float* w1_s,
+                                      const int32_t* offsets, float* h, int32_t* dbg_acc, int32_t* dev_status,
+                                      void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_tiles, w1, w1_s, offsets, h, dev_status});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!i8_tc_ok(d)) return QMOE_ERR_UNSUPPORTED;
+    return i4_tc_gemm1(d, x_tiles, w1, w1_s, offsets, tile_schedule_in(ws, d), h, dbg_acc, dev_status,
+                       (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm2_w4a8(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const float* w2_s,
+                               const int32_t* offsets, uint16_t* y, int32_t* dbg_acc, int32_t* dev_status, void* ws,
+                               size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {h_tiles, w2, w2_s, offsets, y, dev_status});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (dbg_acc && !aligned16(dbg_acc)) return QMOE_ERR_ARG;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!i8_tc_ok(d)) return QMOE_ERR_UNSUPPORTED;
+    return i4_tc_gemm2(d, h_tiles, w2, w2_s, offsets, tile_schedule_in(ws, d), y, dbg_acc, dev_status,
+                       (cudaStream_t)stream);
+}
+
 // ------------------------------------------------------------------ whole layer
 
 namespace {
@@ -239,11 +271,12 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
     L.offsets = take(4 * (E + 1));
     L.sorted = take(4 * P);
     L.slot = take(4 * P);
+    // schemes 2 (W8A8) and 3 (W4A8) share the integer activation path
     L.xq = take(scheme == 0 ? (size_t)bft::x_tiles_bytes(d)
                             : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : qmoe_w8a8_tiles_bytes(d, d->H)));
     L.h = take(scheme == 0 ? (size_t)bft::h_tiles_bytes(d)
                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
-    L.ht = take(scheme == 2 ? qmoe_w8a8_tiles_bytes(d, d->I) : (scheme == 0 ? qmoe_w4a16_h16_tiles_bytes(d) : 0));
+    L.ht = take(scheme >= 2 ? qmoe_w8a8_tiles_bytes(d, d->I) : (scheme == 0 ? qmoe_w4a16_h16_tiles_bytes(d) : 0));
     L.y = take(2 * P * H);
     L.align_ws = take(qmoe_workspace_bytes(d));
     L.total = o;
@@ -253,7 +286,7 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
 }  // namespace
 
 extern "C" size_t qmoe_forward_workspace_bytes(const qmoe_dims* d, int scheme) {
-    if (!dims_ok(d) || scheme < 0 || scheme > 2) return 0;
+    if (!dims_ok(d) || scheme < 0 || scheme > 3) return 0;
     return fwd_layout(d, scheme).total;
 }
 
@@ -261,7 +294,7 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
                                 const float* topk_w, const void* w1, const void* w1_s, const void* w2,
                                 const void* w2_s, uint16_t* out_bf16, int32_t* dev_status, void* ws, size_t ws_bytes,
                                 qmoe_stream_t stream) {
-    if (!dims_ok(d) || scheme < 0 || scheme > 2) return QMOE_ERR_ARG;
+    if (!dims_ok(d) || scheme < 0 || scheme > 3) return QMOE_ERR_ARG;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || !dev_status) return QMOE_ERR_ARG;
     const FwdLayout L = fwd_layout(d, scheme);
     if (ws_bytes < L.total) return QMOE_ERR_ARG;
@@ -300,14 +333,20 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     } else {
         rc = qmoe_permute_quant_int8(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm1_swiglu_w8a8(d, (const uint8_t*)at(L.xq), (const int8_t*)w1, (const float*)w1_s, offsets,
-                                        (float*)at(L.h), nullptr, dev_status, aws, aws_bytes, stream);
+            rc = scheme == 2 ? qmoe_gemm1_swiglu_w8a8(d, (const uint8_t*)at(L.xq), (const int8_t*)w1, (const float*)w1_s,
+                                                      offsets, (float*)at(L.h), nullptr, dev_status, aws, aws_bytes,
+                                                      stream)
+                             : qmoe_gemm1_swiglu_w4a8(d, (const uint8_t*)at(L.xq), (const uint8_t*)w1, (const float*)w1_s,
+                                                      offsets, (float*)at(L.h), nullptr, dev_status, aws, aws_bytes,
+                                                      stream);
         if (rc == QMOE_OK)
             rc = qmoe_quant_tiles_int8_f32(d, (const float*)at(L.h), offsets, (uint8_t*)at(L.ht), aws, aws_bytes,
                                            stream);
         if (rc == QMOE_OK)
-            rc = qmoe_gemm2_w8a8(d, (const uint8_t*)at(L.ht), (const int8_t*)w2, (const float*)w2_s, offsets, y,
-                                 nullptr, dev_status, aws, aws_bytes, stream);
+            rc = scheme == 2 ? qmoe_gemm2_w8a8(d, (const uint8_t*)at(L.ht), (const int8_t*)w2, (const float*)w2_s,
+                                               offsets, y, nullptr, dev_status, aws, aws_bytes, stream)
+                             : qmoe_gemm2_w4a8(d, (const uint8_t*)at(L.ht), (const uint8_t*)w2, (const float*)w2_s,
+                                               offsets, y, nullptr, dev_status, aws, aws_bytes, stream);
     }
     if (rc != QMOE_OK) return rc;
     return qmoe_combine(d, y, topk_w, slot, out_bf16, stream);

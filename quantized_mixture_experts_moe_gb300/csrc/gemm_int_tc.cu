@@ -62,6 +62,11 @@ constexpr int MAX_K = 16384;
 // Per weight format:
 //   W8 (int8, exact int32 sums): tokens per MMA NS = 112 (a 224-row schedule
 //      tile is two of them), 128-element steps, raw int8 rows by TMA;
+//   I4 (int4 codes with per-channel scales, int8 activations, exact int32
+//      sums): W8 in everything but the weights, which arrive as packed int4
+//      rows by TMA (one 64-byte row per 128-element step) and are widened to
+//      exact fp16 integers by the converters.  |code| <= 7 keeps every partial
+//      sum of a K <= 16384 dot below 2^24, so no drains are needed;
 //   W4 (int4 + fp16 scales):     NS = 160 (a 224-row tile is 160 + 64, so an
 //      expert with up to 160 pairs is one unit), 64-element steps in a
 //      three-slot A ring (the wider accumulators leave 192 TMEM columns),
@@ -69,8 +74,12 @@ constexpr int MAX_K = 16384;
 // TMEM columns: the fp32 accumulators of the two tiles (2 * NS), then the A
 // ring.  Shared memory: raw ring, activation ring, and NS x 128 words staging
 // the drains' high parts (W8) and the final outputs.
-template <bool W4>
+enum { FMT_W8 = 0, FMT_W4 = 1, FMT_I4 = 2 };
+
+template <int FMT>
 struct Cfg {
+    static constexpr bool W4 = (FMT == FMT_W4);
+    static constexpr bool I4 = (FMT == FMT_I4);
     static constexpr int NS = W4 ? 160 : 112;
     static constexpr int AS = W4 ? 3 : 2;         // A slots in TMEM
     static constexpr int BS = AS + 1;             // activation slots
@@ -78,8 +87,8 @@ struct Cfg {
     static constexpr int HPS = KSTEP / 64;        // 64-element halves per step
     static constexpr int A_SLOT_COLS = KSTEP;     // two tiles x KSTEP/2 fp16 pairs
     static constexpr int HALF_RAW = W4 ? 2 * bft::kW4Block : 2 * 128 * 64;  // one 64-element half, both tiles
-    static constexpr int RAW_BYTES = HPS * HALF_RAW;
-    static constexpr int RS = W4 ? 4 : 2;         // raw weight slots
+    static constexpr int RAW_BYTES = I4 ? HALF_RAW : HPS * HALF_RAW;  // I4: a whole step in one 64-byte row
+    static constexpr int RS = (W4 || I4) ? 4 : 2;  // raw weight slots
     static constexpr int HALF_B = NS * 128;  // one 64-element half of the step's fp16 token rows
     static constexpr int B_BYTES = HPS * HALF_B;
     static constexpr int CHUNKS = NS / 16;   // 16-token column chunks of an accumulator
@@ -98,7 +107,7 @@ struct Cfg {
     static_assert(R_COL + 2 * NS <= A_COL && A_COL + AS * A_SLOT_COLS <= 512 && NS % 16 == 0, "TMEM budget");
     static_assert(BS >= AS + 1, "a step's done barrier is not reused before the converter has waited on it");
     static_assert(B_OFF % 1024 == 0 && HALF_B % 1024 == 0, "swizzled activation tiles 1024-aligned");
-    static_assert(W4 || HALF_RAW % 1024 == 0, "swizzled raw int8 tiles 1024-aligned");
+    static_assert(W4 || HALF_RAW % 1024 == 0, "swizzled raw int8 / int4 tiles 1024-aligned");
     static_assert(smem_bytes(MAX_E) <= 232448, "shared memory per CTA");
 };
 
@@ -183,6 +192,23 @@ __device__ __forceinline__ void dequant8(uint32_t w, uint32_t s2, uint32_t* out)
     }
 }
 
+// Eight int4 codes (byte i: codes 2i, 2i+1 in its low, high nibble; stored
+// n = q + 8) -> four fp16 pairs holding q exactly: the nibbles are spread
+// into the low bytes of fp16 1024 + n (0x64nn) with byte permutes, then 1032
+// is subtracted.
+__device__ __forceinline__ void i4x8_to_f16x2(uint32_t w, uint32_t* out) {
+    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t n03 = __byte_perm(lo, hi, 0x5140), n47 = __byte_perm(lo, hi, 0x7362);
+    const uint32_t magic = 0x64646464u, bias = 0x64086408u;
+    uint32_t v[4] = {__byte_perm(n03, magic, 0x4140), __byte_perm(n03, magic, 0x4342), __byte_perm(n47, magic, 0x4140),
+                     __byte_perm(n47, magic, 0x4342)};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(v[j]) : "r"(bias));
+        out[j] = v[j];
+    }
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) { tc::tmem_ld_32x32b_x16(taddr, r); }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) { tc::tmem_st_32x32b_x16(taddr, r); }
 
@@ -219,9 +245,10 @@ __device__ __forceinline__ bool bit_at(const uint32_t (&b)[4], int kt) {
     return kt < 128 && ((w >> (kt & 31)) & 1u);
 }
 
-template <int STAGE, bool W4>
+template <int STAGE, int FMT>
 __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const Args a) {
-    using C = Cfg<W4>;
+    using C = Cfg<FMT>;
+    constexpr bool W4 = C::W4, I4 = C::I4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sRaw = smem + C::RAW_OFF;
@@ -303,6 +330,12 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                                           a.wq + (rt1 * KB + C::HPS * kt + hh) * bft::kW4Block, bft::kW4Block,
                                           &raw_full[rs]);
                         }
+                    } else if constexpr (I4) {
+                        // packed int4 rows: the step's 128 elements are 64 bytes
+                        if (STAGE == 1)
+                            tc::tma_load_3d(dst, &wmap, &raw_full[rs], kt * 64, nb * 128, 2 * e);
+                        else
+                            tc::tma_load_2d(dst, &wmap, &raw_full[rs], kt * 64, e * a.H + nb * 256);
                     } else {
 #pragma unroll
                         for (int hh = 0; hh < C::HPS; ++hh) {
@@ -358,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
             const uint32_t dcol = tm + C::R_COL + (uint32_t)(iss * C::NS);
             uint32_t starts[4] = {0u, 0u, 0u, 0u};
-            if constexpr (!W4) chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
+            if constexpr (FMT == FMT_W8) chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
             bool ok = true;
             for (int kt = 0; kt < KT; ++kt) {
                 if (pending) {
@@ -433,6 +466,21 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                         for (int w8 = 0; w8 < 8; ++w8)
                             dequant8(wv[w8], w8 < 4 ? s2a : s2b, &o[2 * hh + (w8 >> 2)][(w8 & 3) * 4]);
                     }
+                } else if constexpr (I4) {
+                    // one 64-byte row: 128 int4 codes (n = q + 8), element 2i in the low nibble of byte i
+                    const uint8_t* src = sRaw + rs * C::RAW_BYTES + tile * (128 * 64) + m * 64;
+                    uint4 c[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const uint4*>(src + ((j ^ sw) << 4));
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&raw_empty[rs]);
+                    if (++rs == C::RS) { rs = 0; rph ^= 1; }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t wv[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) i4x8_to_f16x2(wv[p], &o[j][4 * p]);
+                    }
                 } else {
                     const uint8_t* src = sRaw + rs * C::RAW_BYTES + tile * (128 * 64) + m * 64;
                     uint4 c[8];
@@ -505,7 +553,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                 dstride = a.H;
             }
             uint32_t starts[4] = {0u, 0u, 0u, 0u};
-            if constexpr (!W4) chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
+            if constexpr (FMT == FMT_W8) chunk_starts(a.l1max + (int64_t)(t * halves + half) * KT, KT, lane, starts);
             const int nev = 1 + __popc(starts[0]) + __popc(starts[1]) + __popc(starts[2]) + __popc(starts[3]);
             // this warp's per-token activation scales (chunk i: token 16 * eh + 32 * i + lane, lanes < 16),
             // fetched before the accumulator is ready
@@ -668,24 +716,27 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
 }
 
 // Raw int8 weights viewed through a TMA map with 64-byte rows (64 K elements,
-// half a step) and the 64-byte swizzle.  Stage 1: {H, I, 2E} (gate rows of expert e are
+// half a step; for packed int4 weights a whole 128-element step) and the
+// 64-byte swizzle.  Stage 1: {H, I, 2E} (gate rows of expert e are
 // plane 2e, its up rows plane 2e+1), box {64, 128, 2}: a gate tile and its up
 // partner.  Stage 2: {I, E*H}, box {64, 256}: two adjacent row tiles.
-static int make_w_map(CUtensorMap* map, const void* w, const qmoe_dims* d, int stage) {
+static int make_w_map(CUtensorMap* map, const void* w, const qmoe_dims* d, int stage, bool int4 = false) {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return QMOE_ERR_CUDA;
     CUresult r;
+    // row bytes: K int8 values, or K/2 bytes of packed int4 codes
+    const cuuint64_t H = int4 ? d->H / 2 : d->H, I = int4 ? d->I / 2 : d->I;
     if (stage == 1) {
-        cuuint64_t gdim[3] = {(cuuint64_t)d->H, (cuuint64_t)d->I, (cuuint64_t)(2 * d->E)};
-        cuuint64_t gstride[2] = {(cuuint64_t)d->H, (cuuint64_t)d->I * (cuuint64_t)d->H};
+        cuuint64_t gdim[3] = {H, (cuuint64_t)d->I, (cuuint64_t)(2 * d->E)};
+        cuuint64_t gstride[2] = {H, (cuuint64_t)d->I * H};
         cuuint32_t box[3] = {64, 128, 2};
         cuuint32_t estr[3] = {1, 1, 1};
         r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w), gdim, gstride, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
-        cuuint64_t gdim[2] = {(cuuint64_t)d->I, (cuuint64_t)d->E * (cuuint64_t)d->H};
-        cuuint64_t gstride[1] = {(cuuint64_t)d->I};
+        cuuint64_t gdim[2] = {I, (cuuint64_t)d->E * (cuuint64_t)d->H};
+        cuuint64_t gstride[1] = {I};
         cuuint32_t box[2] = {64, 256};
         cuuint32_t estr[2] = {1, 1};
         r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), gdim, gstride, box, estr,
@@ -702,15 +753,15 @@ static int sm_count() {
     return n;
 }
 
-template <int STAGE, bool W4>
+template <int STAGE, int FMT>
 static int launch(const CUtensorMap& map, const Args& a, cudaStream_t st) {
-    using C = Cfg<W4>;
-    if (cudaFuncSetAttribute(int_gemm_kernel<STAGE, W4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    using C = Cfg<FMT>;
+    if (cudaFuncSetAttribute(int_gemm_kernel<STAGE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::smem_bytes(MAX_E)) != cudaSuccess)
         return QMOE_ERR_LAUNCH;
     const int grid = sm_count();
     if (grid <= 0) return QMOE_ERR_CUDA;
-    int_gemm_kernel<STAGE, W4><<<grid, THREADS, C::smem_bytes(a.E), st>>>(map, a);
+    int_gemm_kernel<STAGE, FMT><<<grid, THREADS, C::smem_bytes(a.E), st>>>(map, a);
     return launch_status();
 }
 
@@ -736,7 +787,7 @@ int i8_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const int8_t* w1, co
     a.w_scale = w1_s;
     a.offsets = offsets; a.tile_start = tile_start;
     a.h = h; a.dbg_acc = dbg_acc; a.status = status;
-    return ig::launch<1, false>(map, a, st);
+    return ig::launch<1, ig::FMT_W8>(map, a, st);
 }
 
 int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, const float* w2_s,
@@ -755,7 +806,43 @@ int i8_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const int8_t* w2, co
     a.w_scale = w2_s;
     a.offsets = offsets; a.tile_start = tile_start;
     a.y = y; a.dbg_acc = dbg_acc; a.status = status;
-    return ig::launch<2, false>(map, a, st);
+    return ig::launch<2, ig::FMT_W8>(map, a, st);
+}
+
+// ------------------------------------------------------------------ W4A8 (int4 weights, int8 activations)
+
+int i4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const float* w1_s,
+                const int32_t* offsets, const int32_t* tile_start, float* h, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st) {
+    CUtensorMap map;
+    int rc = ig::make_w_map(&map, w1, d, 1, true);
+    if (rc != QMOE_OK) return rc;
+    ig::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.nmax = mxt::nmax_for(d);
+    a.act = x_tiles;
+    a.act_scale = reinterpret_cast<const float*>(x_tiles + bft::blocks_bytes(d, d->H));
+    a.w_scale = w1_s;
+    a.offsets = offsets; a.tile_start = tile_start;
+    a.h = h; a.dbg_acc = dbg_acc; a.status = status;
+    return ig::launch<1, ig::FMT_I4>(map, a, st);
+}
+
+int i4_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const float* w2_s,
+                const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* dbg_acc, int32_t* status,
+                cudaStream_t st) {
+    CUtensorMap map;
+    int rc = ig::make_w_map(&map, w2, d, 2, true);
+    if (rc != QMOE_OK) return rc;
+    ig::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.nmax = mxt::nmax_for(d);
+    a.act = h_tiles;
+    a.act_scale = reinterpret_cast<const float*>(h_tiles + bft::blocks_bytes(d, d->I));
+    a.w_scale = w2_s;
+    a.offsets = offsets; a.tile_start = tile_start;
+    a.y = y; a.dbg_acc = dbg_acc; a.status = status;
+    return ig::launch<2, ig::FMT_I4>(map, a, st);
 }
 
 // ------------------------------------------------------------------ W4A16
@@ -777,7 +864,7 @@ int w4_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
     a.h_tiles = h_tiles;
     a.h_tail = reinterpret_cast<float*>(h_tiles + bft::blocks_bytes(d, d->I));
     a.status = status;
-    return ig::launch<1, true>(map, a, st);
+    return ig::launch<1, ig::FMT_W4>(map, a, st);
 }
 
 int w4_tc_gemm2(const qmoe_dims* d, const uint8_t* h16_tiles, const uint8_t* w2, const int32_t* offsets,
@@ -792,7 +879,7 @@ int w4_tc_gemm2(const qmoe_dims* d, const uint8_t* h16_tiles, const uint8_t* w2,
     a.wq = w2;
     a.w_scale = reinterpret_cast<const float*>(w2 + bft::w4_blocks_bytes((int64_t)d->E * d->H, d->I));
     a.offsets = offsets; a.tile_start = tile_start; a.y = y; a.status = status;
-    return ig::launch<2, true>(map, a, st);
+    return ig::launch<2, ig::FMT_W4>(map, a, st);
 }
 
 }  // namespace qmoe

@@ -95,11 +95,14 @@ def run_layer(w, inp, keep=False):
         qb.qmoe_permute_quant_int8(d, t["x"], sorted_ids, offsets, xt, ws)
         h = empty((P, I), torch.float32)
         acc1 = empty((P, 2 * I), torch.int32) if keep else None
-        qb.qmoe_gemm1_swiglu_w8a8(d, xt, t["w1"], t["w1_s"], offsets, h, acc1, status, ws)
+        # W8A8 and W4A8 share the integer activation path; only the weights differ
+        g1, g2 = (qb.qmoe_gemm1_swiglu_w8a8, qb.qmoe_gemm2_w8a8) if w.scheme == "w8a8" else \
+            (qb.qmoe_gemm1_swiglu_w4a8, qb.qmoe_gemm2_w4a8)
+        g1(d, xt, t["w1"], t["w1_s"], offsets, h, acc1, status, ws)
         ht = empty(qb.w8a8_tiles_bytes(d, I), torch.uint8)
         qb.qmoe_quant_tiles_int8_f32(d, h, offsets, ht, ws)
         acc2 = empty((P, H), torch.int32) if keep else None
-        qb.qmoe_gemm2_w8a8(d, ht, t["w2"], t["w2_s"], offsets, y, acc2, status, ws)
+        g2(d, ht, t["w2"], t["w2_s"], offsets, y, acc2, status, ws)
         res.update(ixt=xt, h=h, iht=ht, acc1=acc1, acc2=acc2)
     out = empty((T, H), torch.int16)
     qb.qmoe_combine(d, y, t["topk_w"], slot, out)

@@ -138,6 +138,9 @@ S1_CASES = [
     gen.custom("s1_w8a8_drains", "w8a8", 120, 2304, 4, 2, 128, seed=27),
     # T*k > 96*E: 224-token schedule tiles, each run as two 112-token halves
     gen.custom("s1_w8a8_big_tiles", "w8a8", 500, 1280, 4, 2, 256, seed=28),
+    gen.custom("s1_w4a8", "w4a8", 40, 512, 6, 3, 256, seed=29),
+    # K = 2304 (18 steps), 224-token schedule tiles
+    gen.custom("s1_w4a8_big_tiles", "w4a8", 500, 2304, 4, 2, 256, seed=30),
 ]
 
 
@@ -207,6 +210,7 @@ S2_CASES = [
     gen.custom("s2_mxfp4_tc", "mxfp4", 1, 512, 5, 1, 256, seed=34),
     gen.custom("s2_w8a8", "w8a8", 1, 512, 5, 1, 256, seed=33),
     gen.custom("s2_w8a8_drains", "w8a8", 1, 256, 5, 1, 1152, seed=35),
+    gen.custom("s2_w4a8", "w4a8", 1, 512, 5, 1, 1152, seed=36),
 ]
 
 
@@ -265,8 +269,9 @@ def test_stage2_against_oracle(w):
         ht = gp.pack_i8_tiles(s2["h"], s2["h_s"], offsets, nmax, w.I, qb.w8a8_tiles_bytes(d, w.I),
                               gp.max_tiles(rows, w.E, nmax))
         acc = gp.empty((rows, w.H), torch.int32)
-        qb.qmoe_gemm2_w8a8(d, gp.dev(ht), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), off_t, y, acc, st, ws)
-        ref, racc = oracle.stage2("w8a8", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"],
+        g2 = qb.qmoe_gemm2_w8a8 if w.scheme == "w8a8" else qb.qmoe_gemm2_w4a8
+        g2(d, gp.dev(ht), gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), off_t, y, acc, st, ws)
+        ref, racc = oracle.stage2(w.scheme, w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"],
                                   acc=True)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
@@ -276,7 +281,7 @@ def test_stage2_against_oracle(w):
         assert np.array_equal(gp.host(y), ref_bf16)
 
 
-def _stage2_w8a8_direct(w, h, hs, w2, w2s, experts):
+def _stage2_int_direct(w, h, hs, w2, w2s, experts):
     """Stage 2 alone on given int8 codes (slot order, experts ascending)."""
     rows = len(h)
     counts = np.bincount(experts, minlength=w.E).astype(np.int32)
@@ -290,7 +295,8 @@ def _stage2_w8a8_direct(w, h, hs, w2, w2s, experts):
     nmax = gp.tile_nmax(rows, 1, w.E)
     ht = gp.pack_i8_tiles(h, hs, offsets, nmax, w.I, qb.w8a8_tiles_bytes(d, w.I), gp.max_tiles(rows, w.E, nmax))
     y, acc = gp.empty((rows, w.H), torch.int16), gp.empty((rows, w.H), torch.int32)
-    qb.qmoe_gemm2_w8a8(d, gp.dev(ht), gp.dev(w2), gp.dev(w2s), off_t, y, acc, st, ws)
+    g2 = qb.qmoe_gemm2_w8a8 if w.scheme == "w8a8" else qb.qmoe_gemm2_w4a8
+    g2(d, gp.dev(ht), gp.dev(w2), gp.dev(w2s), off_t, y, acc, st, ws)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     return gp.host(acc)
@@ -309,10 +315,32 @@ def test_w8a8_adversarial_accumulators_exact(K):
     hs = np.full(rows, 1e-3, np.float32)
     w2s = np.full((w.E, w.H), 1e-3, np.float32)
     experts = np.repeat(np.arange(w.E, dtype=np.int32), rows // w.E)
-    got = _stage2_w8a8_direct(w, h, hs, w2, w2s, experts)
+    got = _stage2_int_direct(w, h, hs, w2, w2s, experts)
     _, racc = oracle.stage2("w8a8", w.H, w.I, w.E, experts, h, hs, w2, w2s, acc=True)
     assert np.array_equal(got, racc)
     assert np.abs(racc).max() == 127 * 127 * w.I
+
+
+def test_w4a8_extreme_codes_exact_at_largest_K():
+    # every |h| = 127 against every |code| = 7 at K = 16384: partial sums up to
+    # 7 * 127 * 16384, just under 2^24, with no carry passes
+    K = 16384
+    w = gen.custom("adv4", "w4a8", 1, 256, 2, 1, K, seed=8)
+    rng = np.random.default_rng(8)
+    rows = 40
+    experts = np.sort(rng.integers(0, w.E, size=rows)).astype(np.int32)
+    h = np.where(rng.random((rows, K)) < 0.5, 127, -127).astype(np.int8)
+    h[: rows // 2] = 127  # half the rows all +127: sums of one sign
+    hs = np.full(rows, 1e-3, np.float32)
+    # nibbles 1 (code -7) or 15 (code +7); the first expert's first rows all +7
+    nib = np.where(rng.random((w.E, w.H, K)) < 0.5, 1, 15).astype(np.uint8)
+    nib[0, :16] = 15
+    w2 = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+    w2s = np.full((w.E, w.H), 1e-3, np.float32)
+    got = _stage2_int_direct(w, h, hs, w2, w2s, experts)
+    _, racc = oracle.stage2("w4a8", w.H, w.I, w.E, experts, h, hs, w2, w2s, acc=True)
+    assert np.array_equal(got, racc)
+    assert np.abs(racc).max() >= 7 * 127 * K - 14 * 127 * 64
 
 
 def test_w8a8_stage1_adversarial_accumulators_exact():
@@ -360,6 +388,7 @@ SMALL = [
     gen.WORKLOADS["tiny_w4a16"],
     gen.custom("e2e_mxfp4_ragged", "mxfp4", 50, 1024, 12, 4, 128, seed=41),
     gen.custom("e2e_w8a8_ragged", "w8a8", 50, 1024, 12, 4, 256, seed=42),
+    gen.custom("e2e_w4a8_ragged", "w4a8", 50, 1024, 12, 4, 256, seed=48),
     gen.custom("e2e_w4a16_ragged", "w4a16", 50, 1024, 12, 4, 256, seed=43),
     gen.custom("e2e_w4a16_big_tiles", "w4a16", 700, 512, 8, 2, 256, seed=47),
     gen.custom("e2e_zipf_mxfp4", "mxfp4", 64, 512, 64, 8, 128, routing="zipf", seed=44),
@@ -377,7 +406,7 @@ def test_layer_small(w):
     assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
 
 
-@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8", "w4a8"])
 def test_layer_ragged_expert_loads(scheme):
     # expert loads 0, 1, 127, 129 (tile tails on both sides of 128) plus empties
     counts = [0, 1, 127, 129, 0, 3, 0, 4]
@@ -413,7 +442,7 @@ def test_layer_zero_tokens():
     assert out.shape == (0, 256) and int(status.item()) == 0
 
 
-@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8", "w4a8"])
 def test_forward_entry_point_matches_stagewise_and_is_deterministic(scheme):
     w = gen.custom(f"fwd_{scheme}", scheme, 33, 512, 10, 4, 128, seed=61)  # I, H multiples of 128
     d = gen.make_all(w)
@@ -455,7 +484,7 @@ def _full_inputs(w):
 
 
 FULL = ["decode_T1", "decode_T4", "decode_T16", "decode_T64", "mxfp4_T256", "mxfp4_T1024", "mxfp4_T4096",
-        "mxfp4_T8192", "w4a16_T2048", "w8a8_T8192",
+        "mxfp4_T8192", "w4a16_T2048", "w8a8_T8192", "w4a8_T8192",
         # tensor-parallel shards: inter 512 (TP2) and 256 (TP4)
         "mxfp4_tp2_T4096", "mxfp4_tp2_T8192", "mxfp4_tp4_T16", "mxfp4_tp4_T4096"]
 

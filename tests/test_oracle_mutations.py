@@ -26,8 +26,11 @@ MUTATIONS = [
     ("routing weight dropped", "for (int c = 0; c < H; ++c) o[c] += wt * y[c];",
      "for (int c = 0; c < H; ++c) o[c] += y[c];"),
     ("w8a8 channel scale dropped", "float gf = ((float)ag * sa) * sw[n];", "float gf = ((float)ag * sa);"),
-    ("w8a8 w2 transposed", "const int8_t* wr = (const int8_t*)m->w2 + ((int64_t)e * H + c) * I;",
-     "const int8_t* wr = (const int8_t*)m->w2 + (int64_t)e * H * I + c;"),
+    ("int8 weights transposed", "memcpy(out, (const int8_t*)w + ((int64_t)e * R + row) * K, (size_t)K);",
+     "memcpy(out, (const int8_t*)w + (int64_t)e * R * K + row, (size_t)K);"),
+    ("w4a8 nibble order", "uint8_t code = (uint8_t)((wr[kk / 2] >> (4 * (kk % 2))) & 15);",
+     "uint8_t code = (uint8_t)((wr[kk / 2] >> (4 - 4 * (kk % 2))) & 15);"),
+    ("w4a8 gate/up swapped", "int_row(scheme, w1, 2 * I, H, e, I + n, wu);", "int_row(scheme, w1, 2 * I, H, e, n, wu);"),
     ("int8 rounding", "float t = rintf(vr[i] / sc);", "float t = truncf(vr[i] / sc);"),
     ("stable order", "int32_t s = cursor[e]++;", "int32_t s = offsets[e + 1] - 1 - (cursor[e]++ - offsets[e]);"),
     ("scale block index", "sc = oracle_e8m0_to_double(((const uint8_t*)ws)[sbase + kk / 32]);",
