@@ -86,6 +86,8 @@ WORKLOADS = {
         # profiling stand-in for the T=8192 W8A8 layer: same per-expert load
         # (about 1024 tokens), 8 experts (~0.14 GB of weights)
         _mk("prof_w8a8_E8_T1024", "w8a8", 1024, 4096, 8, 8, 1408, "uniform", 1006),
+        # the same stand-in for the W4A8 layer
+        _mk("prof_w4a8_E8_T1024", "w4a8", 1024, 4096, 8, 8, 1408, "uniform", 1011),
     ]
 }
 
