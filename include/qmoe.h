@@ -88,6 +88,31 @@ const char* qmoe_status_str(int code);
 /* Library version string (static). */
 const char* qmoe_version(void);
 
+/* ---------------------------------------------------------------- token-tile table
+ *
+ * Every call below cuts each expert's slots into token tiles of NMAX = 112 or
+ * 224 rows (the activation tile layouts, the tile schedule qmoe_align_sort
+ * writes, the GEMMs' work units).  Without rules NMAX is 224 when T*k > 96*E,
+ * else 112.  A tuned table (the aiter tuned grouped-fmoe page, Changes: one
+ * configuration row per model shape and token bucket) replaces that choice:
+ *
+ * qmoe_tile_rule -- matches dims with H, I, E, k equal to the rule's (0 = any)
+ *   and t_min <= T <= t_max; nmax is 112 or 224.
+ * qmoe_set_tile_rules -- replaces the table with rules[0..n) (n = 0 clears it);
+ *   the first matching rule wins.  QMOE_ERR_ARG for a bad rule (table
+ *   unchanged).  Host state shared by the process: set it before sizing
+ *   buffers and workspaces for a shape, and not while calls for that shape are
+ *   in flight, since every size and schedule of the shape follows NMAX.
+ * qmoe_tile_nmax -- the NMAX the library uses for *d. */
+typedef struct {
+    int32_t H, I, E, k;
+    int64_t t_min, t_max;
+    int32_t nmax;
+    int32_t reserved;
+} qmoe_tile_rule;
+int qmoe_set_tile_rules(const qmoe_tile_rule* rules, int n);
+int qmoe_tile_nmax(const qmoe_dims* d);
+
 /* ---------------------------------------------------------------- routing
  *
  * Bytes of device workspace the routing and GEMM calls need for dims *d

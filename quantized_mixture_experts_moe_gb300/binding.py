@@ -30,6 +30,13 @@ class Dims(ctypes.Structure):
                 ("E", ctypes.c_int32)]
 
 
+class TileRule(ctypes.Structure):
+    """qmoe_tile_rule: dims with these H, I, E, k (0 = any) and t_min <= T <= t_max use token tile nmax."""
+    _fields_ = [("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("t_min", ctypes.c_int64), ("t_max", ctypes.c_int64), ("nmax", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 _DP = ctypes.POINTER(Dims)
 
@@ -65,6 +72,8 @@ SIGNATURES = {
     "qmoe_gemm2_w4a16": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_w8a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_set_tile_rules": ([ctypes.POINTER(TileRule), _i32], _i32),
+    "qmoe_tile_nmax": ([_DP], _i32),
     "qmoe_gemm1_swiglu_w4a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm2_w4a8": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_combine": ([_DP, _vp, _vp, _vp, _vp, _vp], _i32),
@@ -87,7 +96,41 @@ def lib():
             fn.argtypes = args
             fn.restype = res
         _lib = L
+        # the tuned token-tile table shipped beside the library (QMOE_TILE_TABLE: another
+        # file, or "none" for the built-in rule alone)
+        path = os.environ.get("QMOE_TILE_TABLE", TILE_TABLE_PATH)
+        if path != "none" and os.path.exists(path):
+            set_tile_rules(read_tile_table(path))
     return _lib
+
+
+TILE_TABLE_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tile_table.csv")
+TILE_TABLE_FIELDS = ("scheme", "H", "I", "E", "k", "t_min", "t_max", "nmax")
+
+
+def read_tile_table(path):
+    """Rules from a tile-table CSV (header row; one rule per line, first match wins).  The
+    scheme column records what the row was measured on; the library's rule is per shape."""
+    import csv
+
+    with open(path) as f:
+        rows = [r for r in csv.DictReader(line for line in f if not line.startswith("#"))]
+    return [dict(H=int(r["H"]), I=int(r["I"]), E=int(r["E"]), k=int(r["k"]), t_min=int(r["t_min"]),
+                 t_max=int(r["t_max"]), nmax=int(r["nmax"])) for r in rows]
+
+
+def set_tile_rules(rules):
+    """Replace the library's token-tile table (a list of dicts with H, I, E, k, t_min, t_max, nmax)."""
+    arr = (TileRule * max(1, len(rules)))()
+    for i, r in enumerate(rules):
+        arr[i] = TileRule(r.get("H", 0), r.get("I", 0), r.get("E", 0), r.get("k", 0), r.get("t_min", 0),
+                          r.get("t_max", 2**62), r["nmax"], 0)
+    _check(lib().qmoe_set_tile_rules(arr, len(rules)), "qmoe_set_tile_rules")
+
+
+def tile_nmax(d: Dims) -> int:
+    """The token tile (112 or 224) the library uses for dims d."""
+    return int(lib().qmoe_tile_nmax(ctypes.byref(d)))
 
 
 def _ptr(t):

@@ -1,9 +1,10 @@
 // The MX activation tile layout shared by the permute/quantise kernel and the
 // block-scaled tensor-core GEMMs.
 //
-// Tokens of an expert are cut into tiles of up to NMAX slots (NMAX = 112, or
-// 224 when the average expert load exceeds 96 pairs); tile_start[e] is the
-// prefix over experts of ceil(count[e] / NMAX).  For a reduction length K an
+// Tokens of an expert are cut into tiles of up to NMAX slots; tile_start[e]
+// is the prefix over experts of ceil(count[e] / NMAX).  NMAX is 112 or 224:
+// the first matching rule of the tile table (qmoe_set_tile_rules) picks it,
+// else 224 when the average expert load exceeds 96 pairs.  For a reduction length K an
 // activation buffer holds, per (tile t, K step kt of 128 elements), one block
 //   [NMAX rows x 128 bytes]  E4M3 codes, row r at r*128, its 16-byte chunk c
 //                            at ((c ^ (r & 7)) * 16)  (128-byte swizzle)
@@ -19,15 +20,16 @@
 namespace qmoe {
 namespace mxt {
 
-__host__ __device__ inline int nmax_for(const qmoe_dims* d) {
-    return ((int64_t)d->T * d->k > (int64_t)96 * d->E) ? 224 : 112;
-}
+// the rule used when no tile-table rule matches
+inline int nmax_default(const qmoe_dims* d) { return ((int64_t)d->T * d->k > (int64_t)96 * d->E) ? 224 : 112; }
+// the token tile for these dims (tile_table.cu; host only)
+int nmax_for(const qmoe_dims* d);
 __host__ __device__ inline int nsfb(int nmax) { return (nmax + 127) / 128; }
 __host__ __device__ inline int64_t block_bytes(int nmax) { return (int64_t)nmax * 128 + nsfb(nmax) * 512; }
 __host__ __device__ inline int64_t max_tiles(const qmoe_dims* d, int nmax) {
     return ((int64_t)d->T * d->k + nmax - 1) / nmax + d->E;
 }
-__host__ __device__ inline int64_t buffer_bytes(const qmoe_dims* d, int64_t K) {
+inline int64_t buffer_bytes(const qmoe_dims* d, int64_t K) {
     const int nmax = nmax_for(d);
     return max_tiles(d, nmax) * (K / 128) * block_bytes(nmax);
 }
@@ -54,15 +56,15 @@ namespace bft {
 //   h tiles (stage-1 output): bf16 values, tail = K/32 fp32 |max| values per
 //     (tile, row), one per 32-column group.
 __host__ __device__ inline int64_t block_bytes(int nmax) { return (int64_t)nmax * 128; }
-__host__ __device__ inline int64_t blocks_bytes(const qmoe_dims* d, int64_t K) {
+inline int64_t blocks_bytes(const qmoe_dims* d, int64_t K) {
     const int nmax = mxt::nmax_for(d);
     return mxt::max_tiles(d, nmax) * (K / 64) * block_bytes(nmax);
 }
-__host__ __device__ inline int64_t x_tiles_bytes(const qmoe_dims* d) {
+inline int64_t x_tiles_bytes(const qmoe_dims* d) {
     const int nmax = mxt::nmax_for(d);
     return blocks_bytes(d, d->H) + mxt::max_tiles(d, nmax) * nmax * 4;
 }
-__host__ __device__ inline int64_t h_tiles_bytes(const qmoe_dims* d) {
+inline int64_t h_tiles_bytes(const qmoe_dims* d) {
     const int nmax = mxt::nmax_for(d);
     return blocks_bytes(d, d->I) + mxt::max_tiles(d, nmax) * nmax * (int64_t)(d->I / 32) * 4;
 }

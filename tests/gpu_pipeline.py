@@ -114,17 +114,17 @@ def run_layer(w, inp, keep=False):
             if v is not None:
                 r[key] = host(v, np.uint16) if v.dtype == torch.int16 else host(v)
         if w.scheme == "mxfp4":
-            nmax = tile_nmax(T, k, E)
+            nmax = tile_nmax(T, k, E, H, I)
             r["xq"], r["xs"] = unpack_tiles(r.pop("xt"), r["offsets"], nmax, H)
             r["hq"], r["hs"] = unpack_tiles(r.pop("ht"), r["offsets"], nmax, I)
         elif w.scheme == "w4a16":
-            nmax = tile_nmax(T, k, E)
+            nmax = tile_nmax(T, k, E, H, I)
             nt = max_tiles(P, E, nmax)
             r["x_f16"], r["x_fac"] = unpack_w4_x_tiles(r.pop("bxt"), r["offsets"], nmax, H, nt)
             r["h"], r["h_gmax"] = unpack_w4_h_tiles(r.pop("bht"), r["offsets"], nmax, I, nt)
             r["h_f16"], r["h_fac"] = unpack_w4_x_tiles(r.pop("bh16"), r["offsets"], nmax, I, nt)
         else:
-            nmax = tile_nmax(T, k, E)
+            nmax = tile_nmax(T, k, E, H, I)
             nt = max_tiles(P, E, nmax)
             xt, ht = r.pop("ixt"), r.pop("iht")
             r["xq"], r["xs"] = unpack_i8_tiles(xt, r["offsets"], nmax, H, nt)
@@ -135,8 +135,9 @@ def run_layer(w, inp, keep=False):
 
 # ------------------------------------------------------------------ MX activation tile layout (include/qmoe.h)
 
-def tile_nmax(T, k, E):
-    return 224 if T * k > 96 * E else 112
+def tile_nmax(T, k, E, H, I):
+    """The token tile the library uses for these dims (its tile table or default rule)."""
+    return qb.tile_nmax(qb.dims(T, k, H, I, E))
 
 
 def tile_schedule(offsets, nmax):

@@ -115,3 +115,32 @@ def test_w8a8_host_checks(lib):
     for bad in (qb.dims(16, 2, 384, 128, 8), qb.dims(16, 2, 256, 192, 8), qb.dims(16, 2, 256, 16512, 8)):
         assert lib.qmoe_gemm1_swiglu_w8a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2
         assert lib.qmoe_gemm2_w8a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2
+
+
+def test_tile_rules_host_only(lib):
+    d = qb.dims(4096, 10, 4096, 1024, 512)
+    small = qb.dims(1000, 10, 4096, 1024, 512)
+    try:
+        qb.set_tile_rules([])
+        assert qb.tile_nmax(d) == 112 and qb.tile_nmax(qb.dims(8192, 10, 4096, 1024, 512)) == 224  # built-in rule
+        # an exact-shape rule for one token bucket; first match wins; 0 = any
+        qb.set_tile_rules([dict(H=4096, I=1024, E=512, k=10, t_min=4000, t_max=5000, nmax=224),
+                           dict(H=0, I=0, E=512, k=0, t_min=0, t_max=10**9, nmax=112)])
+        assert qb.tile_nmax(d) == 224 and qb.tile_nmax(small) == 112
+        # buffer sizes follow the table
+        assert qb.mx_tiles_bytes(d, 4096) == (40960 // 224 + 1 + 512) * 32 * (224 * 128 + 2 * 512)
+        # bad rules are refused and leave the table as it was
+        for bad in (dict(nmax=128), dict(nmax=112, t_min=5, t_max=4), dict(nmax=224, H=-1)):
+            with pytest.raises(qb.QmoeError):
+                qb.set_tile_rules([bad])
+        assert qb.tile_nmax(d) == 224
+    finally:
+        qb.set_tile_rules([])
+    assert qb.tile_nmax(d) == 112
+
+
+def test_packaged_tile_table_parses():
+    if not os.path.exists(qb.TILE_TABLE_PATH):
+        pytest.skip("no tile table shipped")
+    rules = qb.read_tile_table(qb.TILE_TABLE_PATH)
+    assert rules and all(r["nmax"] in (112, 224) and r["t_min"] <= r["t_max"] for r in rules)

@@ -9,6 +9,8 @@ their dequantised values plus a mismatch-rate bound, because fp32 and double
 intermediates may straddle a rounding boundary.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -192,7 +194,7 @@ def test_stage1_against_oracle(w):
         hq, hs = oracle.int8_quant(g["h"].astype(np.float32))
         assert np.array_equal(g["hq"], hq) and np.array_equal(g["hs"], hs)
         # the tiles' per-(half tile, 128-step) maxima of sum |code|, which bound the GEMMs' fp32 partial sums
-        nmax = gp.tile_nmax(w.T, w.k, w.E)
+        nmax = gp.tile_nmax(w.T, w.k, w.E, w.H, w.I)
         nt = gp.max_tiles(w.P, w.E, nmax)
         t, r = gp._tile_index(g["offsets"], nmax, np.arange(g["offsets"][-1]))
         used = np.unique(t * (nmax // 112) + r // 112)
@@ -233,7 +235,7 @@ def test_stage2_against_oracle(w):
         st = torch.zeros(1, dtype=torch.int32, device=gp.DEV)
         ws = qb.alloc_workspace(qb.workspace_bytes(d))
         qb.qmoe_align_sort(d, gp.dev(ids), counts_t, off_t, srt, slt, st, ws)
-        nmax = gp.tile_nmax(rows, 1, w.E)
+        nmax = gp.tile_nmax(rows, 1, w.E, w.H, w.I)
         ht = gp.pack_w4_h_tiles(s2["h"], offsets, nmax, w.I, qb.w4a16_h_tiles_bytes(d), gp.max_tiles(rows, w.E, nmax))
         w2p = qb.prepack_int4_weights(gp.dev(wts["w2"]), gp.dev(wts["w2_s"]), w.I)
         h16 = gp.empty(qb.w4a16_h16_tiles_bytes(d), torch.uint8)
@@ -251,7 +253,7 @@ def test_stage2_against_oracle(w):
         st = torch.zeros(1, dtype=torch.int32, device=gp.DEV)
         ws = qb.alloc_workspace(qb.workspace_bytes(d))
         qb.qmoe_align_sort(d, gp.dev(ids), counts_t, off_t, srt, slt, st, ws)
-        ht = gp.pack_tiles(s2["h"], s2["h_s"], offsets, gp.tile_nmax(rows, 1, w.E), w.I, qb.mx_tiles_bytes(d, w.I))
+        ht = gp.pack_tiles(s2["h"], s2["h_s"], offsets, gp.tile_nmax(rows, 1, w.E, w.H, w.I), w.I, qb.mx_tiles_bytes(d, w.I))
         w2p = qb.prepack_mx_scales(gp.dev(wts["w2_s"]), w.I)
         w2w = qb.prepack_fp4_weights(gp.dev(wts["w2"]), w.I)
         qb.qmoe_gemm2_mxfp4(d, gp.dev(ht), w2w, w2p, off_t, y, st, ws)
@@ -265,7 +267,7 @@ def test_stage2_against_oracle(w):
         st = torch.zeros(1, dtype=torch.int32, device=gp.DEV)
         ws = qb.alloc_workspace(qb.workspace_bytes(d))
         qb.qmoe_align_sort(d, gp.dev(ids), counts_t, off_t, srt, slt, st, ws)
-        nmax = gp.tile_nmax(rows, 1, w.E)
+        nmax = gp.tile_nmax(rows, 1, w.E, w.H, w.I)
         ht = gp.pack_i8_tiles(s2["h"], s2["h_s"], offsets, nmax, w.I, qb.w8a8_tiles_bytes(d, w.I),
                               gp.max_tiles(rows, w.E, nmax))
         acc = gp.empty((rows, w.H), torch.int32)
@@ -292,7 +294,7 @@ def _stage2_int_direct(w, h, hs, w2, w2s, experts):
     st = torch.zeros(1, dtype=torch.int32, device=gp.DEV)
     ws = qb.alloc_workspace(qb.workspace_bytes(d))
     qb.qmoe_align_sort(d, gp.dev(experts.reshape(rows, 1).astype(np.int32)), counts_t, off_t, srt, slt, st, ws)
-    nmax = gp.tile_nmax(rows, 1, w.E)
+    nmax = gp.tile_nmax(rows, 1, w.E, w.H, w.I)
     ht = gp.pack_i8_tiles(h, hs, offsets, nmax, w.I, qb.w8a8_tiles_bytes(d, w.I), gp.max_tiles(rows, w.E, nmax))
     y, acc = gp.empty((rows, w.H), torch.int16), gp.empty((rows, w.H), torch.int32)
     g2 = qb.qmoe_gemm2_w8a8 if w.scheme == "w8a8" else qb.qmoe_gemm2_w4a8
@@ -457,6 +459,23 @@ def test_forward_entry_point_matches_stagewise_and_is_deterministic(scheme):
         assert int(status.item()) == 0
     assert np.array_equal(outs[0], outs[1])
     assert np.array_equal(outs[0], stage["out"])
+
+
+@pytest.mark.parametrize("scheme", ["mxfp4", "w8a8", "w4a8", "w4a16"])
+@pytest.mark.parametrize("nmax", [112, 224])
+def test_layer_with_each_token_tile(scheme, nmax):
+    # the tile table may pick either token tile for any shape: both match the oracle
+    w = gen.custom(f"tile{nmax}_{scheme}", scheme, 150, 512, 6, 4, 256, seed=81)  # ~100 pairs per expert
+    d = gen.make_all(w)
+    try:
+        qb.set_tile_rules([dict(H=w.H, I=w.I, E=w.E, k=w.k, t_min=w.T, t_max=w.T, nmax=nmax)])
+        assert qb.tile_nmax(qb.dims(w.T, w.k, w.H, w.I, w.E)) == nmax
+        g = gp.run_layer(w, d, keep=True)
+    finally:
+        qb.set_tile_rules(qb.read_tile_table(qb.TILE_TABLE_PATH) if os.path.exists(qb.TILE_TABLE_PATH) else [])
+    ref = oracle.moe_forward(w.scheme, dims(w), d)
+    assert g["status"] == 0
+    assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
 
 
 def test_argument_errors_raise():
