@@ -5,7 +5,8 @@
 // group prefill expert matmuls", description).  The order here is the stable
 // one: within an expert, slots follow ascending pair id p = t*k + j.
 //
-// Three launches, none of which lets an atomic decide an order:
+// Up to 2048 pairs (one chunk) a single CTA does all of it in one launch;
+// above, three launches, none of which lets an atomic decide an order:
 //   1. hist:    each CTA owns a contiguous chunk of kChunk pairs and counts
 //               them per expert (shared-memory counters).
 //   2. scan:    one CTA turns the [chunk][expert] histograms into per-chunk
@@ -14,7 +15,7 @@
 //   3. scatter: each CTA walks its chunk again in pair order; a pair's slot
 //               is its chunk base + the running count of earlier equal ids,
 //               so the result is the stable counting sort.
-// (A fourth, tiny launch derives the GEMMs' token-tile schedule.)
+// The scan also derives the GEMMs' token-tile schedule.
 #include "qmoe_common.cuh"
 #include "mx_tiles.cuh"
 
@@ -29,6 +30,50 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+// Exclusive scan of one value per thread over a 1024-thread CTA; `total`
+// receives the sum (every thread).  ws: 33 ints of shared memory.
+__device__ int block_exclusive_scan(int v, int32_t* ws, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) ws[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = ws[lane];
+        int wi = w;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += u;
+        }
+        ws[lane] = wi - w;
+        if (lane == 31) ws[32] = wi;
+    }
+    __syncthreads();
+    const int r = ws[warp] + incl - v;
+    total = ws[32];
+    __syncthreads();  // ws may be reused right after
+    return r;
+}
+
+// Token-tile schedule for the tensor-core GEMMs from the counts of experts
+// e0..e1 (this thread's, E <= 4 * 1024): tile_start[e] = prefix over experts
+// of ceil(count[e] / nmax), tile_start[E] = number of tiles.
+__device__ void write_tile_schedule(const int (&cnt)[4], int e0, int e1, int E, int nmax, int32_t* ws,
+                                    int32_t* __restrict__ tile_start) {
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += (cnt[e - e0] + nmax - 1) / nmax;
+    int total;
+    int base = block_exclusive_scan(local, ws, total);
+    for (int e = e0; e < e1; ++e) {
+        tile_start[e] = base;
+        base += (cnt[e - e0] + nmax - 1) / nmax;
+    }
+    if (threadIdx.x == 0) tile_start[E] = total;
 }
 
 // Per-chunk expert histogram: counts do not depend on order, so shared-memory
@@ -58,15 +103,16 @@ align_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks
 }
 
 // One CTA: per expert, chunk bases exclusive over chunks (loads issued eight
-// at a time so they overlap), counts, offsets, and the -1 tail of sorted ids.
+// at a time so they overlap), counts, offsets, the -1 tail of sorted ids and
+// (tile_start non-null) the token-tile schedule.
 __global__ void __launch_bounds__(kScanThreads)
-align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int32_t* __restrict__ counts,
-                  int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids) {
-    __shared__ int32_t warp_sums[32];
-    __shared__ int32_t total_valid;
+align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int nmax, int32_t* __restrict__ counts,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ tile_start) {
+    __shared__ int32_t ws[33];
     const int tid = threadIdx.x;
-    const int per = (E + kScanThreads - 1) / kScanThreads;
-    const int e0 = tid * per, e1 = min(E, e0 + per);
+    const int per = (E + kScanThreads - 1) / kScanThreads;  // <= 4 (E <= kMaxExperts)
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int cnt[4] = {0, 0, 0, 0};
     int local = 0;
     for (int e = e0; e < e1; ++e) {
         int run = 0;
@@ -81,53 +127,26 @@ align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int
             }
         }
         counts[e] = run;
+        cnt[e - e0] = run;
         local += run;
     }
-    // exclusive block scan of the per-thread expert sums
-    const int lane = tid & 31, warp = tid >> 5;
-    int incl = local;
-    for (int o = 1; o < 32; o <<= 1) {
-        int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = warp_sums[lane];
-        int wi = w;
-        for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-            if (lane >= o) wi += v;
-        }
-        warp_sums[lane] = wi - w;
-        if (lane == 31) total_valid = wi;
-    }
-    __syncthreads();
-    int base = warp_sums[warp] + incl - local;
+    int total_valid;
+    int base = block_exclusive_scan(local, ws, total_valid);
     for (int e = e0; e < e1; ++e) {
         offsets[e] = base;
         for (int c = 0; c < nchunks; ++c) hist[(size_t)c * E + e] += base;
-        base += counts[e];
+        base += cnt[e - e0];
     }
     if (tid == 0) offsets[E] = total_valid;
     for (int64_t s = (int64_t)total_valid + tid; s < P; s += kScanThreads) sorted_pair_ids[s] = -1;
+    if (tile_start) write_tile_schedule(cnt, e0, e1, E, nmax, ws, tile_start);
 }
 
-// Stable scatter: the CTA walks its chunk in two rounds of 1024 pairs; inside
-// a round the 32 warps take turns (in pair order) on the per-expert cursors,
-// each warp ranking equal ids among its lanes with match-any.  A pair's slot
-// is therefore its chunk base + the number of earlier pairs of the same
-// expert in the chunk: the stable counting sort.
-__global__ void __launch_bounds__(kThreads)
-align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
-                     const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_pair_ids,
-                     int32_t* __restrict__ pair_slot) {
-    extern __shared__ int32_t cur[];
+// The chunk's pairs in pair order onto their slots: cur[e] enters as the
+// chunk's first slot of expert e and is advanced past the chunk's pairs.
+__device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E, int64_t p0, int32_t* cur,
+                              int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pair_slot) {
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int32_t* base = hist + (size_t)blockIdx.x * E;
-    for (int e = tid; e < E; e += kThreads) cur[e] = base[e];
-    __syncthreads();
-    const int64_t p0 = (int64_t)blockIdx.x * kChunk;
     for (int round = 0; round < kChunk / kThreads; ++round) {
         const int64_t p = p0 + round * kThreads + tid;
         int e = -1;
@@ -151,39 +170,64 @@ align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchu
     }
 }
 
-// Token-tile schedule for the tensor-core GEMMs: tile_start[e] = prefix over
-// experts of ceil(counts[e] / nmax), tile_start[E] = number of tiles.  One CTA.
-__global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ offsets, int E, int nmax,
-                                                             int32_t* __restrict__ tile_start) {
-    __shared__ int32_t warp_sums[32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (E + 1023) / 1024;
-    const int e0 = tid * per, e1 = min(E, e0 + per);
+// Stable scatter: the CTA walks its chunk in two rounds of 1024 pairs; inside
+// a round the 32 warps take turns (in pair order) on the per-expert cursors,
+// each warp ranking equal ids among its lanes with match-any.  A pair's slot
+// is therefore its chunk base + the number of earlier pairs of the same
+// expert in the chunk: the stable counting sort.
+__global__ void __launch_bounds__(kThreads)
+align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
+                     const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_pair_ids,
+                     int32_t* __restrict__ pair_slot) {
+    extern __shared__ int32_t cur[];
+    const int tid = threadIdx.x;
+    const int32_t* base = hist + (size_t)blockIdx.x * E;
+    for (int e = tid; e < E; e += kThreads) cur[e] = base[e];
+    __syncthreads();
+    scatter_chunk(ids, P, E, (int64_t)blockIdx.x * kChunk, cur, sorted_pair_ids, pair_slot);
+}
+
+// One CTA for at most one chunk of pairs: histogram, scan (counts, offsets,
+// tile schedule) and the stable scatter of the three-launch path, in one launch.
+__global__ void __launch_bounds__(kThreads)
+align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, int32_t* __restrict__ counts,
+                   int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids,
+                   int32_t* __restrict__ pair_slot, int32_t* __restrict__ tile_start, int32_t* __restrict__ dev_status) {
+    extern __shared__ int32_t cur[];  // per-expert counts, then cursors
+    __shared__ int32_t ws[33];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += kThreads) cur[e] = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int64_t p = tid; p < P; p += kThreads) {
+        const int e = ids[p];
+        if (e >= 0 && e < E)
+            atomicAdd(&cur[e], 1);
+        else
+            bad = 1;
+    }
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(dev_status, QMOE_DEV_BAD_EXPERT_ID);
+    const int per = (E + kThreads - 1) / kThreads;  // <= 4
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int cnt[4] = {0, 0, 0, 0};
     int local = 0;
-    for (int e = e0; e < e1; ++e) local += (offsets[e + 1] - offsets[e] + nmax - 1) / nmax;
-    int incl = local;
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int w = warp_sums[lane];
-        int wi = w;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-            if (lane >= o) wi += v;
-        }
-        warp_sums[lane] = wi - w;
-        if (lane == 31) tile_start[E] = wi;
-    }
-    __syncthreads();
-    int base = warp_sums[warp] + incl - local;
     for (int e = e0; e < e1; ++e) {
-        tile_start[e] = base;
-        base += (offsets[e + 1] - offsets[e] + nmax - 1) / nmax;
+        cnt[e - e0] = cur[e];
+        local += cnt[e - e0];
     }
+    int total_valid;
+    int base = block_exclusive_scan(local, ws, total_valid);  // also orders the reads above before the writes
+    for (int e = e0; e < e1; ++e) {
+        counts[e] = cnt[e - e0];
+        offsets[e] = base;
+        cur[e] = base;
+        base += cnt[e - e0];
+    }
+    if (tid == 0) offsets[E] = total_valid;
+    for (int64_t s = (int64_t)total_valid + tid; s < P; s += kThreads) sorted_pair_ids[s] = -1;
+    if (tile_start) write_tile_schedule(cnt, e0, e1, E, nmax, ws, tile_start);
+    __syncthreads();
+    scatter_chunk(ids, P, E, 0, cur, sorted_pair_ids, pair_slot);
 }
 
 size_t align_ws_bytes(int64_t P, int E) {
@@ -193,18 +237,23 @@ size_t align_ws_bytes(int64_t P, int E) {
 
 int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int32_t* offsets,
                       int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
-                      cudaStream_t stream) {
+                      int nmax, int32_t* tile_start, cudaStream_t stream) {
     const int nchunks = (int)((P + kChunk - 1) / kChunk);
     const size_t smem = (size_t)E * sizeof(int32_t);
     if (smem > 48 * 1024) {
         cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(align_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     }
-    if (nchunks > 0) align_hist_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, dev_status);
-    align_scan_kernel<<<1, kScanThreads, 0, stream>>>(hist, P, E, nchunks, counts, offsets, sorted_pair_ids);
-    if (nchunks > 0)
-        align_scatter_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, sorted_pair_ids,
-                                                                  pair_slot);
+    if (nchunks <= 1) {
+        align_small_kernel<<<1, kThreads, smem, stream>>>(ids, P, E, nmax, counts, offsets, sorted_pair_ids, pair_slot,
+                                                          tile_start, dev_status);
+        return launch_status();
+    }
+    align_hist_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, dev_status);
+    align_scan_kernel<<<1, kScanThreads, 0, stream>>>(hist, P, E, nchunks, nmax, counts, offsets, sorted_pair_ids,
+                                                      tile_start);
+    align_scatter_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, sorted_pair_ids, pair_slot);
     return launch_status();
 }
 
@@ -234,9 +283,7 @@ extern "C" int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int3
     if (d->E > kMaxExperts) return QMOE_ERR_UNSUPPORTED;
     if (ws_bytes < align_ws_bytes(P, d->E)) return QMOE_ERR_ARG;
     if (ws_bytes < qmoe_workspace_bytes(d)) return QMOE_ERR_ARG;
-    int rc = align_sort_launch(P, d->E, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status,
-                               static_cast<int32_t*>(ws), (cudaStream_t)stream);
-    if (rc != QMOE_OK) return rc;
-    tile_schedule_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(offsets, d->E, mxt::nmax_for(d), tile_schedule_in(ws, d));
-    return launch_status();
+    return align_sort_launch(P, d->E, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status,
+                             static_cast<int32_t*>(ws), mxt::nmax_for(d), tile_schedule_in(ws, d),
+                             (cudaStream_t)stream);
 }

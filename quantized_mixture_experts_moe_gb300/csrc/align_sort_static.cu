@@ -16,7 +16,7 @@ namespace qmoe {
 size_t align_ws_bytes(int64_t P, int E);
 int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int32_t* offsets,
                       int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
-                      cudaStream_t stream);
+                      int nmax, int32_t* tile_start, cudaStream_t stream);
 }  // namespace qmoe
 
 // The scratch every call shares: QMOE_STATIC_SCRATCH_BYTES bytes on every GPU
@@ -68,6 +68,7 @@ extern "C" int qmoe_align_sort_static_scratch(const qmoe_dims* d, const int32_t*
     int st = QMOE_OK;
     int32_t* scratch = scratch_on_current_device(&st);
     if (st != QMOE_OK) return st;
-    return align_sort_launch(P, d->E, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status, scratch,
-                             (cudaStream_t)stream);
+    // no GEMM tile schedule here: the GEMM calls take the routing workspace that holds it
+    return align_sort_launch(P, d->E, topk_ids, counts, offsets, sorted_pair_ids, pair_slot, dev_status, scratch, 0,
+                             nullptr, (cudaStream_t)stream);
 }

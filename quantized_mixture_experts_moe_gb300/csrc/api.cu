@@ -7,7 +7,7 @@ namespace qmoe {
 size_t align_ws_bytes(int64_t P, int E);
 int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int32_t* offsets,
                       int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
-                      cudaStream_t stream);
+                      int nmax, int32_t* tile_start, cudaStream_t stream);
 int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
 template <typename In>
 int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float* s, cudaStream_t st);
