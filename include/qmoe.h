@@ -90,14 +90,16 @@ const char* qmoe_version(void);
 
 /* ---------------------------------------------------------------- token-tile table
  *
- * Every call below cuts each expert's slots into token tiles of NMAX = 112 or
- * 224 rows (the activation tile layouts, the tile schedule qmoe_align_sort
+ * Every call below cuts each expert's slots into token tiles of NMAX = 16, 112
+ * or 224 rows (the activation tile layouts, the tile schedule qmoe_align_sort
  * writes, the GEMMs' work units).  Without rules NMAX is 224 when T*k > 96*E,
  * else 112.  A tuned table (the aiter tuned grouped-fmoe page, Changes: one
  * configuration row per model shape and token bucket) replaces that choice:
  *
  * qmoe_tile_rule -- matches dims with H, I, E, k equal to the rule's (0 = any)
- *   and t_min <= T <= t_max; nmax is 112 or 224.
+ *   and t_min <= T <= t_max; nmax is 16, 112 or 224 (16 shrinks each
+ *   pipeline slot of the MXFP4 GEMMs, so small batches keep more weight
+ *   loads in flight).
  * qmoe_set_tile_rules -- replaces the table with rules[0..n) (n = 0 clears it);
  *   the first matching rule wins.  QMOE_ERR_ARG for a bad rule (table
  *   unchanged).  Host state shared by the process: set it before sizing
@@ -255,9 +257,10 @@ int qmoe_quant_rows_int8_f32(int64_t rows, int64_t cols, const float* x, int8_t*
  * activations: the blocks of the W4A16 tiles above (same NMAX, tile_start,
  * 128-byte rows of 64 fp16 values, chunk swizzle), each value the fp16 equal
  * to an int8 code (exact); then a per-row tail of one fp32 scale s at
- * (t*NMAX + r); then, for each 112-row half h of a tile (NMAX/112 halves)
- * and each 128-element K step j, the int32 max over the half's rows of
- * sum |code| over the step, at ((t*(NMAX/112) + h) * K/128 + j): the GEMMs
+ * (t*NMAX + r); then, for each 112-row part h of a tile (ceil(NMAX/112)
+ * parts; a 16-row tile is one short part) and each 128-element K step j, the
+ * int32 max over the part's rows of sum |code| over the step, at
+ * ((t*ceil(NMAX/112) + h) * K/128 + j): the GEMMs
  * bound their partial sums with it.  Rows past a tile's token count are
  * unspecified.
  * qmoe_w8a8_tiles_bytes -- bytes of such a buffer for dims *d and length K

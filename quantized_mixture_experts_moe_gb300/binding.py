@@ -129,7 +129,7 @@ def set_tile_rules(rules):
 
 
 def tile_nmax(d: Dims) -> int:
-    """The token tile (112 or 224) the library uses for dims d."""
+    """The token tile (16, 112 or 224) the library uses for dims d."""
     return int(lib().qmoe_tile_nmax(ctypes.byref(d)))
 
 

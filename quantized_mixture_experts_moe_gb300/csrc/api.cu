@@ -178,7 +178,7 @@ extern "C" size_t qmoe_w8a8_tiles_bytes(const qmoe_dims* d, int64_t K) {
     if (!dims_ok(d) || K <= 0 || K % 128 != 0 || K > 16384) return 0;
     const int nmax = mxt::nmax_for(d);
     const int64_t tiles = mxt::max_tiles(d, nmax);
-    return (size_t)(bft::blocks_bytes(d, K) + tiles * nmax * 4 + tiles * (nmax / 112) * (K / 128) * 4);
+    return (size_t)(bft::blocks_bytes(d, K) + tiles * nmax * 4 + tiles * ((nmax + 111) / 112) * (K / 128) * 4);
 }
 
 extern "C" int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,

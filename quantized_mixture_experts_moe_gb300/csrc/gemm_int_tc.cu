@@ -113,7 +113,7 @@ struct Cfg {
 
 struct Args {
     int T, k, H, I, E;
-    int nmax;                 // schedule tile (112 or 224 tokens)
+    int nmax;                 // schedule tile (16, 112 or 224 tokens)
     const uint8_t* act;       // fp16 token tiles (K = H for stage 1, I for stage 2)
     const float* act_scale;   // per tile row: s_x / s_h (W8) or the power of two 2^e (W4)
     const uint8_t* wq;        // W4: pre-packed int4 blocks (W8 weights come through the tensor map)

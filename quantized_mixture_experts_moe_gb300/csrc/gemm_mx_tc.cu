@@ -107,7 +107,8 @@ struct Cfg {
 };
 
 constexpr int MAX_E = 512;  // schedule prefix kept in shared memory
-static_assert(Cfg<1, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<1, 224>::smem_bytes(MAX_E) <= 232448 &&
+static_assert(Cfg<1, 16>::smem_bytes(MAX_E) <= 232448 && Cfg<2, 16>::smem_bytes(MAX_E) <= 232448 &&
+                  Cfg<1, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<1, 224>::smem_bytes(MAX_E) <= 232448 &&
                   Cfg<2, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<2, 224>::smem_bytes(MAX_E) <= 232448,
               "shared memory per CTA");
 
@@ -490,8 +491,10 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
     const int64_t KT = d->H / 128;
     const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * KT;
     const int64_t half = (int64_t)(d->I / 128) * KT * 8192;  // bytes of one expert's gate (or up) tiles
-    return mxt::nmax_for(d) == 224 ? mx::launch_cfg<1, 224>(w1, tiles, half, a, st)
-                                   : mx::launch_cfg<1, 112>(w1, tiles, half, a, st);
+    const int nmax = mxt::nmax_for(d);
+    return nmax == 224 ? mx::launch_cfg<1, 224>(w1, tiles, half, a, st)
+                       : (nmax == 16 ? mx::launch_cfg<1, 16>(w1, tiles, half, a, st)
+                                     : mx::launch_cfg<1, 112>(w1, tiles, half, a, st));
 }
 
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
@@ -500,8 +503,10 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, c
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = h_tiles; a.w_s = w2_s; a.offsets = offsets; a.tile_start = tile_start; a.y = y; a.status = status;
     const int64_t tiles = (int64_t)d->E * d->H / 128 * (d->I / 128);
-    return mxt::nmax_for(d) == 224 ? mx::launch_cfg<2, 224>(w2, tiles, 0, a, st)
-                                   : mx::launch_cfg<2, 112>(w2, tiles, 0, a, st);
+    const int nmax = mxt::nmax_for(d);
+    return nmax == 224 ? mx::launch_cfg<2, 224>(w2, tiles, 0, a, st)
+                       : (nmax == 16 ? mx::launch_cfg<2, 16>(w2, tiles, 0, a, st)
+                                     : mx::launch_cfg<2, 112>(w2, tiles, 0, a, st));
 }
 
 bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2) { return mx::mx_tc_supported(d, w1, w2); }

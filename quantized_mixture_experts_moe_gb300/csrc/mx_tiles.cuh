@@ -2,7 +2,7 @@
 // block-scaled tensor-core GEMMs.
 //
 // Tokens of an expert are cut into tiles of up to NMAX slots; tile_start[e]
-// is the prefix over experts of ceil(count[e] / NMAX).  NMAX is 112 or 224:
+// is the prefix over experts of ceil(count[e] / NMAX).  NMAX is 16, 112 or 224:
 // the first matching rule of the tile table (qmoe_set_tile_rules) picks it,
 // else 224 when the average expert load exceeds 96 pairs.  For a reduction length K an
 // activation buffer holds, per (tile t, K step kt of 128 elements), one block

@@ -310,7 +310,7 @@ quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ so
     __shared__ int s_l1[kTqMaxSteps];
     __shared__ int s_info[2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int halves = nmax / kTqSub;
+    const int halves = (nmax + kTqSub - 1) / kTqSub;
     const int t = blockIdx.x / halves, half = blockIdx.x - t * halves;
     const int KT = K / 128;
     for (int i = threadIdx.x; i < KT; i += blockDim.x) s_l1[i] = 0;
@@ -324,7 +324,8 @@ quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ so
             }
             const int m0 = offsets[lo] + (t - tile_start[lo]) * nmax + half * kTqSub;
             s_info[0] = m0;
-            s_info[1] = max(0, min(kTqSub, offsets[lo + 1] - m0));
+            // rows of this half that exist in the tile (a 16-row tile has one short half)
+            s_info[1] = max(0, min(min(kTqSub, nmax - half * kTqSub), offsets[lo + 1] - m0));
         }
     }
     __syncthreads();
@@ -388,7 +389,7 @@ int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool f
     if (P == 0) return QMOE_OK;
     if (K % 128 != 0 || K / 128 > kTqMaxSteps) return QMOE_ERR_UNSUPPORTED;
     const int nmax = mxt::nmax_for(d);
-    const int64_t blocks = mxt::max_tiles(d, nmax) * (nmax / kTqSub);
+    const int64_t blocks = mxt::max_tiles(d, nmax) * ((nmax + kTqSub - 1) / kTqSub);
     const int64_t tail = bft::blocks_bytes(d, K);
     const int64_t l1 = tail + mxt::max_tiles(d, nmax) * nmax * 4;
     if (from_bf16_tokens)

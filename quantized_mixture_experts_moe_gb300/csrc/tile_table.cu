@@ -38,7 +38,7 @@ extern "C" int qmoe_set_tile_rules(const qmoe_tile_rule* rules, int n) {
     if (n < 0 || (n > 0 && !rules) || n > 4096) return QMOE_ERR_ARG;
     for (int i = 0; i < n; ++i) {
         const qmoe_tile_rule& r = rules[i];
-        if ((r.nmax != 112 && r.nmax != 224) || r.H < 0 || r.I < 0 || r.E < 0 || r.k < 0 || r.t_min < 0 ||
+        if ((r.nmax != 16 && r.nmax != 112 && r.nmax != 224) || r.H < 0 || r.I < 0 || r.E < 0 || r.k < 0 || r.t_min < 0 ||
             r.t_max < r.t_min)
             return QMOE_ERR_ARG;
     }

@@ -5,13 +5,13 @@
 In the manner of the tuned grouped-fmoe configuration rows (the aiter tuned
 grouped-fmoe page, Changes: one row per model shape, TP degree and token
 bucket 1-256, 1024, 4096, 8192), each workload's layer is run through
-qmoe_moe_forward with the token tile pinned to 112 and to 224 rows.  Per
+qmoe_moe_forward with the token tile pinned to 16, 112 and 224 rows.  Per
 (shape, token bucket) the tile with the smaller total step time over the
 bucket's workloads becomes a rule.
 
 Checks, per workload:
-  * the two tiles' outputs agree to rel L2 < 5e-3 (they differ only in the
-    order of fp32 sums; the tests compare each against the CPU oracle);
+  * the tiles' outputs agree to rel L2 < 5e-3 (they differ only in the order
+    of fp32 sums; the tests compare each against the CPU oracle);
   * no K tile passes the end of K: every kernel steps K in 128-element tiles,
     so a shape with H % 256 or I % 128 is excluded rather than tuned.
 """
@@ -30,6 +30,7 @@ import torch
 from quantized_mixture_experts_moe_gb300 import binding as qb
 from quantized_mixture_experts_moe_gb300 import inputs as gen
 
+TILES = (16, 112, 224)
 BUCKETS = [(1, 256), (257, 1024), (1025, 4096), (4097, 8192), (8193, 2**31 - 1)]
 DEFAULT_WORKLOADS = [
     "decode_T1", "decode_T4", "decode_T16", "decode_T64",
@@ -85,7 +86,7 @@ def measure(w, steps=10):
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if small else None
     res, outs = {}, {}
     dims = qb.dims(w.T, w.k, w.H, w.I, w.E)
-    for nmax in (112, 224):
+    for nmax in TILES:
         qb.set_tile_rules([dict(H=w.H, I=w.I, E=w.E, k=w.k, t_min=w.T, t_max=w.T, nmax=nmax)])
         ws = qb.alloc_workspace(qb.forward_workspace_bytes(dims, w.scheme), dev)
         out = torch.empty((w.T, w.H), dtype=torch.int16, device=dev)
@@ -93,9 +94,9 @@ def measure(w, steps=10):
         res[nmax] = time_layer(w, t, out, status, ws, steps, flush)
         outs[nmax] = (out.cpu().numpy().astype(np.uint32) << 16).view(np.float32).astype(np.float64)
         del ws
-    a, b = outs[112], outs[224]
-    rel = float(np.linalg.norm(a - b) / max(np.linalg.norm(a), 1e-300))
-    return dict(us_112=res[112], us_224=res[224], rel=rel)
+    ref = outs[112]
+    rel = max(float(np.linalg.norm(outs[n] - ref) / max(np.linalg.norm(ref), 1e-300)) for n in TILES)
+    return dict(**{f"us_{n}": res[n] for n in TILES}, rel=rel)
 
 
 def main(argv=None):
@@ -112,27 +113,26 @@ def main(argv=None):
             print(f"{name}: excluded (K tiles would pass the end of K)", file=sys.stderr)
             continue
         ok = m["rel"] < 5e-3
-        print(f"{name:22s} 112: {m['us_112']:9.1f} us  224: {m['us_224']:9.1f} us  rel L2 between tiles "
+        print(f"{name:22s} " + "  ".join(f"{n}: {m[f'us_{n}']:8.1f} us" for n in TILES) + "  rel L2 between tiles "
               f"{m['rel']:.2e} {'ok' if ok else 'MISMATCH'}", file=sys.stderr)
         if not ok:
             continue
         key = (w.scheme, w.H, w.I, w.E, w.k, bucket_of(w.T))
-        g = groups.setdefault(key, dict(us_112=0.0, us_224=0.0, reps=[]))
-        g["us_112"] += m["us_112"]
-        g["us_224"] += m["us_224"]
+        g = groups.setdefault(key, dict(**{f"us_{n}": 0.0 for n in TILES}, reps=[]))
+        for n in TILES:
+            g[f"us_{n}"] += m[f"us_{n}"]
         g["reps"].append(w.T)
     qb.set_tile_rules([])
     rows = []
     for (scheme, H, I, E, k, (lo, hi)), g in sorted(groups.items(), key=lambda x: (x[0][:5], x[0][5][0])):
-        nmax = 112 if g["us_112"] <= g["us_224"] else 224
+        nmax = min(TILES, key=lambda n: (g[f"us_{n}"], n != 112))  # ties keep the 112-row tile
         rows.append(dict(scheme=scheme, H=H, I=I, E=E, k=k, t_min=lo, t_max=hi, nmax=nmax,
-                         t_measured=" ".join(map(str, g["reps"])), us_112=f"{g['us_112']:.1f}",
-                         us_224=f"{g['us_224']:.1f}"))
+                         t_measured=" ".join(map(str, g["reps"])), **{f"us_{n}": f"{g[f'us_{n}']:.1f}" for n in TILES}))
     with open(args.out, "w", newline="") as f:
         f.write("# token-tile table written by quantized_mixture_experts_moe_gb300.tune on "
                 f"{torch.cuda.get_device_name()}: per (shape, token bucket) the tile with the smaller\n"
-                "# summed step time over the bucket's measured token counts (us_112, us_224)\n")
-        wr = csv.DictWriter(f, fieldnames=[*qb.TILE_TABLE_FIELDS, "t_measured", "us_112", "us_224"])
+                "# summed step time over the bucket's measured token counts (us_16, us_112, us_224)\n")
+        wr = csv.DictWriter(f, fieldnames=[*qb.TILE_TABLE_FIELDS, "t_measured", *[f"us_{n}" for n in TILES]])
         wr.writeheader()
         wr.writerows(rows)
     print(f"wrote {len(rows)} rules to {args.out}", file=sys.stderr)

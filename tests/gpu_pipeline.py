@@ -274,9 +274,9 @@ def pack_i8_tiles(codes, scales, offsets, nmax, K, nbytes, ntiles):
 
 
 def i8_step_l1max(codes, t, r, nmax, K, ntiles):
-    """int32 [ntiles * nmax/112 * K/128]: per (tile, 112-row half, 128-element step), the max over the
+    """int32 [ntiles * ceil(nmax/112) * K/128]: per (tile, 112-row half, 128-element step), the max over the
     half's rows of sum |code| over the step."""
-    halves = nmax // 112
+    halves = (nmax + 111) // 112
     steps = np.abs(codes.astype(np.int64)).reshape(len(codes), K // 128, 128).sum(axis=2)
     out = np.zeros((ntiles * halves, K // 128), np.int64)
     np.maximum.at(out, t * halves + r // 112, steps)
@@ -285,5 +285,5 @@ def i8_step_l1max(codes, t, r, nmax, K, ntiles):
 
 def unpack_i8_l1max(buf, nmax, K, ntiles):
     off = ntiles * (K // 64) * nmax * 128 + ntiles * nmax * 4
-    n = ntiles * (nmax // 112) * (K // 128)
+    n = ntiles * ((nmax + 111) // 112) * (K // 128)
     return buf[off:off + 4 * n].view(np.int32)

@@ -143,4 +143,4 @@ def test_packaged_tile_table_parses():
     if not os.path.exists(qb.TILE_TABLE_PATH):
         pytest.skip("no tile table shipped")
     rules = qb.read_tile_table(qb.TILE_TABLE_PATH)
-    assert rules and all(r["nmax"] in (112, 224) and r["t_min"] <= r["t_max"] for r in rules)
+    assert rules and all(r["nmax"] in (16, 112, 224) and r["t_min"] <= r["t_max"] for r in rules)

@@ -462,7 +462,7 @@ def test_forward_entry_point_matches_stagewise_and_is_deterministic(scheme):
 
 
 @pytest.mark.parametrize("scheme", ["mxfp4", "w8a8", "w4a8", "w4a16"])
-@pytest.mark.parametrize("nmax", [112, 224])
+@pytest.mark.parametrize("nmax", [16, 112, 224])
 def test_layer_with_each_token_tile(scheme, nmax):
     # the tile table may pick either token tile for any shape: both match the oracle
     w = gen.custom(f"tile{nmax}_{scheme}", scheme, 150, 512, 6, 4, 256, seed=81)  # ~100 pairs per expert
