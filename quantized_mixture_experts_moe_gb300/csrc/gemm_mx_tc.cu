@@ -82,10 +82,14 @@ struct Cfg {
     // stage 1 epilogue: per epilogue warp a 16-token x 32-column transpose
     // buffer of h (rows padded to 36 floats: the 16-byte reads of 8 rows at
     // a time hit distinct banks)
+    // (16-token tiles have a single chunk, so only the first four warps ever use it)
     static constexpr int EPI_ROW = 36;
-    static constexpr int EPI_BYTES = (STAGE == 1) ? EPI_WARPS * 16 * EPI_ROW * 4 : 0;
+    static constexpr int EPI_BYTES = (STAGE == 1) ? (NMAX == 16 ? 4 : EPI_WARPS) * 16 * EPI_ROW * 4 : 0;
     // ring depth: as many whole steps as fit in the 227 KB of shared memory
-    static constexpr int S = (220 * 1024 - 8 * 1024 - EPI_BYTES) / SLOT_BYTES;
+    // next to 1 KB of alignment slack, the epilogue buffer, and barriers for
+    // up to 16 slots, the misc words and the schedule of up to MAX_E experts
+    static constexpr int FIXED_BYTES = 2 * 16 * 8 + 64 + (512 + 1) * 4;
+    static constexpr int S = (232448 - 1024 - EPI_BYTES - FIXED_BYTES) / SLOT_BYTES;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + S * A_BYTES;
     static constexpr int SFA_OFF = B_OFF + S * B_BYTES;
@@ -103,7 +107,7 @@ struct Cfg {
     static constexpr uint32_t SF_SLOT = 4 + NSFB * 4;
     static_assert(SF_COL + 2 * AT * SF_SLOT <= 512, "TMEM budget");
     static_assert(NMAX % 16 == 0 && NMAX <= 256, "N tile");
-    static_assert(S >= 2, "ring");
+    static_assert(S >= 2 && S <= 16, "ring");
 };
 
 constexpr int MAX_E = 512;  // schedule prefix kept in shared memory
