@@ -1,5 +1,6 @@
-// Grouped W8A8 expert GEMMs on the 5th-generation tensor cores with exact
-// int32 sums.
+// Grouped integer-weight expert GEMMs on the 5th-generation tensor cores:
+// W8A8 and W4A8 with exact int32 sums, and W4A16 (int4 codes with per-32
+// fp16 scales, dequantised on chip, fp16 activations).
 //
 // "Evaluate native IU4/IU8 WMMA for grouped-INT MoE prefill on gfx1151"
 // (Constraint) runs W8A8 as int8 x int8 products summed in int32; "perf(qmoe):
@@ -22,21 +23,28 @@
 //   stage 1: g = ((float)acc_g * s_x) * s_w,  u likewise,  h = silu(g) * u  (fp32)
 //   stage 2: y = ((float)acc * s_h) * s_w                                 (bf16)
 //
+// W4A8 uses the W8A8 path with int4 codes (|q| <= 7) in place of int8: its
+// partial sums stay below 2^24 for K <= 16384, so it needs no drains.  W4A16
+// dequantises (n - 8) * s on chip, one fp16 rounding per weight, and sums in
+// fp32 like any float GEMM.
+//
 // Structure (one persistent CTA per SM, 20 warps), swap-AB as in the other
 // grouped GEMMs (weights are the MMA's M = 128 rows, tokens its N):
-//   warp 0      weight producer: two TMA boxes per 128-element step bring the
-//               raw int8 rows of both weight tiles (stage 1: a gate tile and
-//               its up partner; stage 2: two adjacent W2 row tiles), 64 K
-//               elements per box, 64-byte swizzled.
-//   warp 1      activation producer: two bulk copies per step of the step's
-//               fp16 token rows, already 128-byte swizzled by the tile kernel.
+//   warp 0      weight producer: per step the raw weights of both weight
+//               tiles (stage 1: a gate tile and its up partner; stage 2: two
+//               adjacent W2 row tiles): W8A8 two TMA boxes of int8 rows (64
+//               K elements each), W4A8 one TMA box of packed int4 rows, W4A16
+//               bulk copies of pre-packed blocks; 64-byte swizzled by TMA.
+//   warp 1      activation producer: bulk copies per step of the step's fp16
+//               token rows, already 128-byte swizzled by the tile kernel.
 //   warps 2-3   MMA issuers, one per weight tile: A (the weight tile) from
 //               TMEM, B (tokens) from shared memory, N = tokens rounded to 16.
-//   warps 4-11  converters: one thread per weight row; int8 -> fp16 pairs
-//               written straight into TMEM as the A operand, so the converted
-//               weights never pass through shared memory.
+//   warps 4-11  converters: one thread per weight row; int8 / int4 / int4 x
+//               scale -> fp16 pairs written straight into TMEM as the A
+//               operand, so the converted weights never pass through shared
+//               memory.
 //   warps 12-19 epilogue: two per TMEM lane quadrant, alternate 16-token
-//               column chunks; the 1024-K drains and the final dequantisation.
+//               column chunks; the drains (W8A8) and the final dequantisation.
 #include "qmoe_common.cuh"
 #include "mx_tiles.cuh"
 #include "tc_ptx.cuh"

@@ -8,7 +8,7 @@
 //            E4M3 codes + E8M0 scales per 32 columns of I;
 //   stage 2: y = W2 . h, accumulated in fp32, stored as bf16.
 //
-// Structure (one persistent CTA per SM, 15 warps):
+// Structure (one persistent CTA per SM, 12 warps):
 //   warp 0     weight producer: per pipeline step one TMA load (a 4D box) of
 //              the step's two FP4 weight tiles (stage 1: a gate tile and its
 //              up partner; stage 2: two adjacent row tiles of W2) from
@@ -16,25 +16,25 @@
 //              is one contiguous 8 KiB read, unpacked by the tensor map into
 //              the 16-byte-aligned form the MMA reads -- plus bulk copies of
 //              the matching 512-byte scale atoms.
-//   warps 1-4  activation producers, taking pipeline steps round-robin:
-//              gather the unit's token rows (stage 1: token = sorted pair id
-//              / k; stage 2: contiguous slots) with cp.async into the
-//              128-byte-swizzled K-major layout, and their E8M0 scales into
-//              atom layout; each publishes its step after its copies land.
-//   warps 5-6  MMA issuers (warp 5 also owns tensor memory), one per weight
+//   warp 1     activation producer: per step two bulk copies of the step's
+//              block of the stage-ready MX activation tiles (the token rows,
+//              already 128-byte swizzled, and their scale atoms).
+//   warps 2-3  MMA issuers (warp 2 also owns tensor memory), one per weight
 //              tile: one lane copies its scale atoms into TMEM and issues the
 //              MMAs (M = 128 weight rows, N = tokens rounded up to 16, K = 32
 //              per instruction), one commit per step.  Two issuers halve the
 //              serial instruction stream each thread issues.
-//   warps 7-14 epilogue (two warps per TMEM lane quadrant, alternating
-//              16-token chunks): TMEM -> registers, SwiGLU + MX quantisation
-//              (stage 1) or fp32 stores (stage 2).
+//   warps 4-11 epilogue (two warps per TMEM lane quadrant, alternating
+//              16-token chunks): TMEM -> registers, then SwiGLU + MX
+//              quantisation through a shared-memory transpose (stage 1) or
+//              bf16 stores (stage 2).
 // Every tcgen05 or TMA instruction costs the issuing thread on the order of
 // a hundred cycles, so a step carries as much data per instruction as the
 // hardware allows: one ring slot holds a whole step (weights, activations,
-// both scale sets) behind a single full/empty barrier pair.  Two accumulator
-// buffers in TMEM (112-token tiles) let the epilogue of one unit overlap the
-// MMAs of the next.
+// both scale sets) behind a single full/empty barrier pair, and the ring is
+// as deep as shared memory allows (3 to 6 steps with 224- to 16-token tiles).
+// Two accumulator buffers in TMEM (16- and 112-token tiles) let the epilogue
+// of one unit overlap the MMAs of the next; 224-token tiles have one.
 //
 // The weights are the A operand ("swap AB"): per-expert token counts are
 // small at prefill sizes (about 80 at T = 4096), so tokens take the MMA's N
