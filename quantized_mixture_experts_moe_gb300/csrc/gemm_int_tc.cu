@@ -574,7 +574,9 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             bool last_final = false;
             for (int ch = 0; ch < nev; ++ch, ++ev) {
                 int w = 1;
-                if (lane == 0) w = tc::mbar_wait(acc_full, ev & 1) ? 1 : 0;
+                // sleeping between polls leaves the issue slots to the converter warps on the
+                // same schedulers; W8A8 drains mid-unit, so it polls more often
+                if (lane == 0) w = tc::mbar_wait_sleep(acc_full, ev & 1, 4000000000ll, FMT == FMT_W8 ? 128u : 512u) ? 1 : 0;
                 w = __shfl_sync(0xFFFFFFFFu, w, 0);
                 __syncwarp();
                 if (!w) {

@@ -60,11 +60,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
 // Like mbar_wait, but sleeps between polls: for waiters off the critical path
 // (epilogue warps waiting for an accumulator), so they do not take issue
 // slots from the producer and MMA warps.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long limit_cycles = 4000000000ll) {
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long limit_cycles = 4000000000ll,
+                                                unsigned sleep_ns = 256) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        __nanosleep(256);
+        __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > limit_cycles) return false;
     }
