@@ -304,10 +304,12 @@ def _stage2_int_direct(w, h, hs, w2, w2s, experts):
     return gp.host(acc)
 
 
-@pytest.mark.parametrize("K", [1024, 4096])
+@pytest.mark.parametrize("K", [1024, 4096, 16384])
 def test_w8a8_adversarial_accumulators_exact(K):
     # all-+-127 operands: the largest-magnitude int32 sums a row of length K makes
-    # (127^2 * 4096 = 66,064,384 is far past 2^24, where fp32 stops being exact)
+    # (127^2 * 4096 = 66,064,384 is far past 2^24, where fp32 stops being exact;
+    # at K = 16384, the largest supported, the carried high parts reach 32,258 of
+    # their 16-bit range)
     w = gen.custom("adv", "w8a8", 1, 256, 2, 1, K, seed=5)
     rows = 64
     h = np.full((rows, w.I), 127, np.int8)
