@@ -366,14 +366,42 @@ def run_ours(args, w):
         step()
     barrier()
 
-    # The K timed steps, each between its own events (step start, stage-1
-    # start/end, stage-2 end, step end), replayed as one CUDA graph: a step
-    # is a handful of dependent launches, and at decode sizes launch gaps
-    # would otherwise cost as much as the kernels.
+    # The whole-layer call, as a user makes it (the GEMMs may then start
+    # streaming weights before the kernel ahead of them completes).
+    fws = qb.alloc_workspace(qb.forward_workspace_bytes(dims, w.scheme), dev)
+
+    def fwd_step():
+        qb.qmoe_moe_forward(w.scheme, dims, t["x"], t["topk_ids"], t["topk_w"], t["w1"], t["w1_s"], t["w2"], t["w2_s"],
+                            out, status, fws)
+
+    for _ in range(args.warmup):
+        fwd_step()
+    barrier()
+
+    # Two replays of K steps, each one CUDA graph (a step is a handful of
+    # dependent launches; at decode sizes launch gaps would otherwise cost as
+    # much as the kernels):
+    #   timed:  the K steps through qmoe_moe_forward, each step between two
+    #           events -> ms_per_step, value;
+    #   stages: the same K steps through the stage entry points with events
+    #           around each GEMM -> the GEMMs' durations for the roofline.
+    #           An event between two kernels costs a few microseconds (the
+    #           next launch cannot overlap it), which is why the timed replay
+    #           has none inside a step.
     K = args.steps
-    marks = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)] for _ in range(K)]
+    ext = lambda: torch.cuda.Event(enable_timing=True, external=True)
+    step_marks = [(ext(), ext()) for _ in range(K)]
+    marks = [[ext() for _ in range(5)] for _ in range(K)]
 
     def timed_steps():
+        for i in range(K):
+            if flush:
+                flush_buf.fill_(i & 0x7F)
+            step_marks[i][0].record()
+            fwd_step()
+            step_marks[i][1].record()
+
+    def stage_steps():
         for i in range(K):
             if flush:
                 flush_buf.fill_(i & 0x7F)
@@ -382,32 +410,43 @@ def run_ours(args, w):
             step(m[1:4])
             m[4].record()
 
-    graph, launch = None, "eager"
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.graph(g, stream=cs):
+            body()
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        g.replay()  # uploads the graph: K more untimed warm-up steps
+        barrier()
+        return g
+
+    graphs, launch = None, "eager"
     if not args.eager:
         try:
-            g = torch.cuda.CUDAGraph()
-            cs = torch.cuda.Stream(dev)
-            cs.wait_stream(torch.cuda.current_stream(dev))
-            with torch.cuda.graph(g, stream=cs):
-                timed_steps()
-            torch.cuda.current_stream(dev).wait_stream(cs)
-            g.replay()  # uploads the graph: K more untimed warm-up steps
-            barrier()
-            graph, launch = g, "one CUDA graph of the K timed steps"
-        except Exception as ex:  # the eager loop below times the same launches
+            graphs = (capture(timed_steps), capture(stage_steps))
+            launch = ("one CUDA graph of the K timed steps (qmoe_moe_forward, dependent launches); GEMM times "
+                      "from a second graph of the K steps through the stage calls with events around each GEMM")
+        except Exception as ex:  # the eager loops below time the same launches
             torch.cuda.synchronize(dev)
             launch = f"eager (graph capture failed: {type(ex).__name__})"
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
     barrier()
-    if graph is not None:
-        graph.replay()
+    if graphs is not None:
+        graphs[0].replay()
     else:
         timed_steps()
     barrier()
+    if graphs is not None:
+        graphs[1].replay()
+    else:
+        stage_steps()
+    barrier()
     clk = clocks.stop()
-    ms = statistics.mean(m[0].elapsed_time(m[4]) for m in marks)
+    ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in step_marks)
+    ms_stages = statistics.mean(m[0].elapsed_time(m[4]) for m in marks)
     g1_ms = statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
     g2_ms = statistics.mean(m[2].elapsed_time(m[3]) for m in marks)
     ms = max_over_ranks(ms, world, dev)
@@ -437,6 +476,7 @@ def run_ours(args, w):
                     frac=achieved / tensor_peak, traffic=traffic, peak_source=f"{pk['source']} {src}")
     roof["gemm1_ms"] = g1_ms
     roof["gemm2_ms"] = g2_ms
+    roof["stage_calls_ms_per_step"] = ms_stages
     roof["gemm1_alg_bytes"] = alg["gemm1_bytes"]
     roof["gemm2_alg_bytes"] = alg["gemm2_bytes"]
     roof["gemm2_hbm_frac"] = alg["gemm2_bytes"] / (g2_ms * 1e-3) / 1e9 / pk["hbm"]
@@ -447,7 +487,6 @@ def run_ours(args, w):
         hx = t["x"].cpu().pin_memory()
         hid = t["topk_ids"].cpu().pin_memory()
         hw = t["topk_w"].cpu().pin_memory()
-        fws = qb.alloc_workspace(qb.forward_workspace_bytes(dims, w.scheme), dev)
         # two slots of device inputs and outputs and of pinned results: step i
         # copies its inputs in and its result out on their own streams while
         # the neighbouring steps compute

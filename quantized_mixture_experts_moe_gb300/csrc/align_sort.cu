@@ -83,6 +83,7 @@ align_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks
                   int32_t* __restrict__ dev_status) {
     extern __shared__ int32_t cnt[];
     const int tid = threadIdx.x;
+    pdl_sync();
     for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
     __syncthreads();
     const int64_t p0 = (int64_t)blockIdx.x * kChunk;
@@ -110,6 +111,7 @@ align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int
                   int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ tile_start) {
     __shared__ int32_t ws[33];
     const int tid = threadIdx.x;
+    pdl_sync();
     const int per = (E + kScanThreads - 1) / kScanThreads;  // <= 4 (E <= kMaxExperts)
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
     int cnt[4] = {0, 0, 0, 0};
@@ -148,14 +150,19 @@ __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E,
                               int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pair_slot) {
     const int tid = threadIdx.x, warp = tid >> 5;
     for (int round = 0; round < kChunk / kThreads; ++round) {
-        const int64_t p = p0 + round * kThreads + tid;
+        const int64_t r0 = p0 + round * kThreads;
+        if (r0 >= P) break;  // CTA-uniform
+        // only warps that hold pairs of this round take a turn
+        const int64_t warps_left = (P - r0 + 31) / 32;
+        const int nw = warps_left < kThreads / 32 ? (int)warps_left : kThreads / 32;
+        const int64_t p = r0 + tid;
         int e = -1;
         if (p < P) e = ids[p];
         const bool valid = (p < P) && e >= 0 && e < E;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
         const uint32_t before = peers & lanemask_lt();
         int slot = -1;
-        for (int w = 0; w < kThreads / 32; ++w) {
+        for (int w = 0; w < nw; ++w) {
             if (warp == w) {
                 if (valid) slot = cur[e] + __popc(before);
                 __syncwarp();
@@ -181,6 +188,7 @@ align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchu
                      int32_t* __restrict__ pair_slot) {
     extern __shared__ int32_t cur[];
     const int tid = threadIdx.x;
+    pdl_sync();
     const int32_t* base = hist + (size_t)blockIdx.x * E;
     for (int e = tid; e < E; e += kThreads) cur[e] = base[e];
     __syncthreads();
@@ -196,6 +204,7 @@ align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, 
     extern __shared__ int32_t cur[];  // per-expert counts, then cursors
     __shared__ int32_t ws[33];
     const int tid = threadIdx.x;
+    pdl_sync();
     for (int e = tid; e < E; e += kThreads) cur[e] = 0;
     __syncthreads();
     int bad = 0;
@@ -245,16 +254,17 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
         cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(align_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     }
-    if (nchunks <= 1) {
-        align_small_kernel<<<1, kThreads, smem, stream>>>(ids, P, E, nmax, counts, offsets, sorted_pair_ids, pair_slot,
-                                                          tile_start, dev_status);
-        return launch_status();
-    }
-    align_hist_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, dev_status);
-    align_scan_kernel<<<1, kScanThreads, 0, stream>>>(hist, P, E, nchunks, nmax, counts, offsets, sorted_pair_ids,
-                                                      tile_start);
-    align_scatter_kernel<<<nchunks, kThreads, smem, stream>>>(ids, P, E, nchunks, hist, sorted_pair_ids, pair_slot);
-    return launch_status();
+    if (nchunks <= 1)
+        return launch_pdl(align_small_kernel, 1, kThreads, smem, stream, ids, P, E, nmax, counts, offsets,
+                          sorted_pair_ids, pair_slot, tile_start, dev_status);
+    int rc = launch_pdl(align_hist_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist, dev_status);
+    if (rc == QMOE_OK)
+        rc = launch_pdl(align_scan_kernel, 1, kScanThreads, 0, stream, hist, P, E, nchunks, nmax, counts, offsets,
+                        sorted_pair_ids, tile_start);
+    if (rc == QMOE_OK)
+        rc = launch_pdl(align_scatter_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist,
+                        sorted_pair_ids, pair_slot);
+    return rc;
 }
 
 // Where the tile schedule lives inside the routing workspace.

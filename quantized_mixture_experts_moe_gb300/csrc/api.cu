@@ -312,6 +312,13 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
     if (rc != QMOE_OK) return rc;
     if (d->T == 0) return QMOE_OK;
     uint16_t* y = (uint16_t*)at(L.y);
+    // Every GEMM below is launched at least two kernels after the routing
+    // sort, so it may read the schedule and stream weights before its
+    // predecessor completes.
+    struct EarlyWeights {
+        EarlyWeights() { launch_ctx().weights_early = true; }
+        ~EarlyWeights() { launch_ctx().weights_early = false; }
+    } early;
     if (scheme == 0) {
         rc = qmoe_permute_x_f16(d, x_bf16, sorted, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
         if (rc == QMOE_OK)

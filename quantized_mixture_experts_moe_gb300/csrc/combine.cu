@@ -15,6 +15,7 @@ combine_kernel(const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
                uint16_t* __restrict__ out, int T, int k, int H) {
     const int c8 = blockIdx.x * blockDim.x + threadIdx.x;  // column group of 8
     const int t = blockIdx.y;
+    pdl_sync();
     if (c8 * 8 >= H) return;
     float acc[8];
 #pragma unroll
@@ -43,8 +44,7 @@ int combine_launch(const qmoe_dims* d, const uint16_t* y, const float* topk_w, c
                    uint16_t* out, cudaStream_t st) {
     if (d->T == 0) return QMOE_OK;
     dim3 grid((unsigned)ceil_div(d->H / 8, 256), (unsigned)d->T);
-    combine_kernel<<<grid, 256, 0, st>>>(y, topk_w, pair_slot, out, d->T, d->k, d->H);
-    return launch_status();
+    return launch_pdl(combine_kernel, grid, 256, 0, st, y, topk_w, pair_slot, out, d->T, d->k, d->H);
 }
 
 }  // namespace qmoe

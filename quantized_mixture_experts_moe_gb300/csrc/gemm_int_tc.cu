@@ -135,6 +135,7 @@ struct Args {
     const int32_t* l1max;     // per (sub-tile, step): the largest sum |x| over the sub-tile's rows
     int32_t* dbg_acc;         // optional exact sums: [P, 2I] (stage 1) or [P, H] (stage 2)
     int32_t* status;
+    int weights_early;        // weight producer and converters may run before the predecessor kernel completes
 };
 
 // Unit u -> (expert e, schedule tile t, half of it, column block nb) and the
@@ -153,8 +154,10 @@ __device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax,
         if (tile_start[mid] <= t) lo = mid; else hi = mid;
     }
     e = lo;
-    m0 = offsets[e] + (t - tile_start[e]) * nmax + half * NS;
-    ntok = min(min(NS, nmax - half * NS), offsets[e + 1] - m0);
+    // offsets come from the routing sort, which may have completed after this
+    // kernel started (dependent launch): read them from L2
+    m0 = __ldcg(offsets + e) + (t - tile_start[e]) * nmax + half * NS;
+    ntok = min(min(NS, nmax - half * NS), __ldcg(offsets + e + 1) - m0);
 }
 
 __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
@@ -280,7 +283,13 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
     const int KT = K / C::KSTEP;
     const int halves = (a.nmax + C::NS - 1) / C::NS;
 
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = a.tile_start[i];
+    // Dependent launch: by default everything waits for the predecessor
+    // kernel.  With weights_early (set by the whole-layer call, whose routing
+    // sort ran two launches back) the weight producer and the converters,
+    // which read only the schedule and the weights, start before that; the
+    // warps that read the predecessor's output wait.
+    if (!a.weights_early) pdl_sync();
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = __ldcg(a.tile_start + i);
     if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::RS; ++s) {
             tc::mbar_init(&raw_full[s], 1);
@@ -298,7 +307,10 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
     }
     __syncthreads();
     const int total_units = tile_start[E] * halves * NB;
-    if ((int)blockIdx.x >= total_units) return;
+    if ((int)blockIdx.x >= total_units) {
+        pdl_wait();  // the grid still completes only after its predecessor
+        return;
+    }
 
     if (warp == WARP_MMA) {
         tc::tmem_alloc(tmem_base_smem, 512);
@@ -362,6 +374,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         }
     } else if (warp == WARP_B) {
         // ------------------------------------------------ activation producer
+        if (a.weights_early) pdl_sync();
         if (lane == 0) {
             int bs = 0;
             uint32_t ph = 0;
@@ -387,6 +400,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         }
     } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
         // ------------------------------------------------ MMA issuers (warp-uniform; one elected lane issues)
+        if (a.weights_early) pdl_sync();
         const int iss = warp - WARP_MMA;
         int bs = 0, as = 0;
         uint32_t bph = 0, aph = 0, ev = 0;
@@ -527,6 +541,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         }
     } else {
         // ------------------------------------------------ epilogue
+        if (a.weights_early) pdl_sync();
         const int q = warp & 3, eh = (warp - WARP_EPI0) >> 2;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int n = q * 32 + lane;  // weight row within a tile = output column within its 128-column block
@@ -771,8 +786,9 @@ static int launch(const CUtensorMap& map, const Args& a, cudaStream_t st) {
         return QMOE_ERR_LAUNCH;
     const int grid = sm_count();
     if (grid <= 0) return QMOE_ERR_CUDA;
-    int_gemm_kernel<STAGE, FMT><<<grid, THREADS, C::smem_bytes(a.E), st>>>(map, a);
-    return launch_status();
+    Args b = a;
+    b.weights_early = launch_ctx().weights_early ? 1 : 0;
+    return launch_pdl(int_gemm_kernel<STAGE, FMT>, grid, THREADS, C::smem_bytes(a.E), st, map, b);
 }
 
 }  // namespace ig

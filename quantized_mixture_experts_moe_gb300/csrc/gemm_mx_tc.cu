@@ -125,6 +125,7 @@ struct Args {
     uint8_t* h_tiles;           // stage 1 output: h as MX activation tiles (K = I)
     uint16_t* y;                // stage 2 output: bf16, slot order
     int32_t* status;
+    int weights_early;          // the weight producer may run before the predecessor kernel completes
 };
 
 template <int NMAX>
@@ -138,8 +139,10 @@ __device__ __forceinline__ void decode_unit(int u, int NB, const int* tile_start
         if (tile_start[mid] <= t) lo = mid; else hi = mid;
     }
     e = lo;
-    m0 = offsets[e] + (t - tile_start[e]) * NMAX;
-    ntok = min(NMAX, offsets[e + 1] - m0);
+    // offsets come from the routing sort, which may have completed after this
+    // kernel started (dependent launch): read them from L2
+    m0 = __ldcg(offsets + e) + (t - tile_start[e]) * NMAX;
+    ntok = min(NMAX, __ldcg(offsets + e + 1) - m0);
 }
 
 __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
@@ -178,8 +181,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     const int NB = (STAGE == 1) ? NOUT / 128 : NOUT / 256;  // stage 2 units cover two column blocks
     const int KT = K / KSTAGE;
 
+    // Dependent launch: by default everything waits for the predecessor
+    // kernel.  With weights_early (set by the whole-layer call, whose routing
+    // sort ran two launches back) only the warps that consume the
+    // predecessor's output wait; the schedule is read and weights stream
+    // before that.
+    if (!a.weights_early) pdl_sync();
+
     // ---- token-tile schedule (computed with the routing sort)
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = a.tile_start[i];
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = __ldcg(a.tile_start + i);
     if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::S; ++s) {
             tc::mbar_init(&full[s], 2);        // weight producer (with tx bytes) + activation producer
@@ -194,7 +204,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     }
     __syncthreads();
     const int total_units = tile_start[E] * NB;
-    if ((int)blockIdx.x >= total_units) return;  // no work: nothing allocated yet
+    if ((int)blockIdx.x >= total_units) {  // no work: nothing allocated yet
+        pdl_wait();  // the grid still completes only after its predecessor
+        return;
+    }
 
     if (warp == WARP_MMA) {
         tc::tmem_alloc(tmem_base_smem, 512);
@@ -241,6 +254,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // ------------------------------------------------ activation producer (bulk copies)
         // A step's activations are one block of the MX tile layout: the
         // first nmma rows of codes (already swizzled) and the scale atoms.
+        if (a.weights_early) pdl_sync();
         if (lane == 0) {
             int slot = 0;
             uint32_t phase = 0;
@@ -266,6 +280,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // atoms to TMEM, issues its four MMAs per step and commits; the slot
         // frees after both commits.
         const int iss = warp - WARP_MMA;
+        if (a.weights_early) pdl_sync();
         if (lane == 0 && iss < C::AT) {
             int slot = 0, sf = 0, ab = 0;
             uint32_t phase = 0, pacc = 0;
@@ -310,6 +325,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue warps
+        if (a.weights_early) pdl_sync();
         const int q = warp & 3;                       // TMEM lane quadrant this warp may access
         const int half = (warp - WARP_EPI0) >> 2;     // which 16-column chunks it takes
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
@@ -474,8 +490,7 @@ static int launch_cfg(const void* w, int64_t tiles, int64_t half_bytes, const Ar
         return QMOE_ERR_LAUNCH;
     const int grid = num_sms();
     if (grid <= 0) return QMOE_ERR_CUDA;
-    mx_gemm_kernel<STAGE, NMAX><<<grid, THREADS, smem, st>>>(map, a);
-    return launch_status();
+    return launch_pdl(mx_gemm_kernel<STAGE, NMAX>, grid, THREADS, smem, st, map, a);
 }
 
 }  // namespace mx
@@ -492,6 +507,7 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = x_tiles; a.w_s = w1_s; a.offsets = offsets; a.tile_start = tile_start;
     a.h_tiles = h_tiles; a.status = status;
+    a.weights_early = launch_ctx().weights_early ? 1 : 0;
     const int64_t KT = d->H / 128;
     const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * KT;
     const int64_t half = (int64_t)(d->I / 128) * KT * 8192;  // bytes of one expert's gate (or up) tiles
@@ -506,6 +522,7 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, c
     mx::Args a{};
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = h_tiles; a.w_s = w2_s; a.offsets = offsets; a.tile_start = tile_start; a.y = y; a.status = status;
+    a.weights_early = launch_ctx().weights_early ? 1 : 0;
     const int64_t tiles = (int64_t)d->E * d->H / 128 * (d->I / 128);
     const int nmax = mxt::nmax_for(d);
     return nmax == 224 ? mx::launch_cfg<2, 224>(w2, tiles, 0, a, st)

@@ -27,6 +27,58 @@ inline int launch_status() {
 
 inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// ------------------------------------------------------------------ dependent launches
+//
+// Every kernel of the layer is launched with programmatic stream
+// serialization: it may be scheduled while its predecessor in the stream is
+// still running, so its launch and prologue hide behind the predecessor's
+// tail.  The kernel then calls pdl_wait() before it touches anything its
+// predecessor reads or writes (griddepcontrol.wait returns once the
+// predecessor grid has completed and its memory operations are visible), and
+// pdl_trigger() only after that wait.  Hence when a kernel is launched, the
+// kernel two places before it in the stream has completed.  Launched without
+// the attribute (or with no predecessor kernel) both are no-ops.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_sync() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+#ifndef QMOE_PDL
+#define QMOE_PDL 1
+#endif
+
+// One launch of `kernel` on `st` that may overlap its predecessor's tail.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = QMOE_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...) == cudaSuccess ? QMOE_OK : QMOE_ERR_LAUNCH;
+}
+
+// Host-thread launch context.  The whole-layer call sets weights_early while
+// it launches its GEMMs: it knows that the routing sort, which writes the
+// token-tile schedule and offsets, ran at least two launches earlier, so a
+// GEMM may read them, and start streaming weights, before its pdl_wait().
+struct LaunchCtx {
+    bool weights_early = false;
+};
+inline LaunchCtx& launch_ctx() {
+    static thread_local LaunchCtx c;
+    return c;
+}
+
 // ------------------------------------------------------------------ format decoding
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }

@@ -17,6 +17,7 @@ namespace qmoe {
 // One thread per 8 consecutive bf16 values; 4 lanes form one 32-block.
 __global__ void __launch_bounds__(256)
 quant_mx_bf16_kernel(const uint4* __restrict__ x, int64_t n8, uint2* __restrict__ q, uint8_t* __restrict__ s) {
+    pdl_sync();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const bool active = i < n8;
     uint4 v = active ? x[i] : make_uint4(0, 0, 0, 0);
@@ -61,6 +62,7 @@ __device__ __forceinline__ float load_as_float<float>(const float* p, int64_t i)
 template <typename In>
 __global__ void __launch_bounds__(256)
 quant_rows_int8_kernel(const In* __restrict__ x, int64_t cols, int8_t* __restrict__ q, float* __restrict__ s) {
+    pdl_sync();
     __shared__ float red[8];
     const int64_t row = blockIdx.x;
     const In* xr = x + row * cols;
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(kPqWarps * 32)
 permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_slot,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
                         int H, int nmax, int T, uint8_t* __restrict__ tiles) {
+    pdl_sync();
     const int lane = threadIdx.x & 31;
     const int nseg = H / 1024 + (H % 1024 != 0);  // 1024-element segments of a row
     const int64_t wid = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
@@ -187,9 +190,8 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
     if ((int64_t)d->T * d->k == 0) return QMOE_OK;
     const int64_t warps = (int64_t)d->T * (d->H / 1024 + (d->H % 1024 != 0));
     const int64_t blocks = (warps + kPqWarps - 1) / kPqWarps;
-    permute_quant_mx_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, pair_slot, offsets, tile_start, d->E, d->k,
-                                                                       d->H, mxt::nmax_for(d), d->T, tiles);
-    return launch_status();
+    return launch_pdl(permute_quant_mx_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, pair_slot, offsets,
+                      tile_start, d->E, d->k, d->H, mxt::nmax_for(d), d->T, tiles);
 }
 
 // Permute bf16 activations into W4A16 x tiles: one warp per expert-sorted
@@ -201,6 +203,7 @@ __global__ void __launch_bounds__(kPqWarps * 32)
 permute_x_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k, int H,
                      int nmax, int64_t P, int64_t tail_off, uint8_t* __restrict__ tiles) {
+    pdl_sync();
     const int lane = threadIdx.x & 31;
     const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
     int tile = -1, row = 0, tok = 0;
@@ -254,10 +257,8 @@ int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* s
     const int64_t P = (int64_t)d->T * d->k;
     if (P == 0) return QMOE_OK;
     const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
-    permute_x_f16_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(x, sorted, offsets, tile_start, d->E, d->k, d->H,
-                                                                    mxt::nmax_for(d), P, bft::blocks_bytes(d, d->H),
-                                                                    tiles);
-    return launch_status();
+    return launch_pdl(permute_x_f16_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, sorted, offsets, tile_start,
+                      d->E, d->k, d->H, mxt::nmax_for(d), P, bft::blocks_bytes(d, d->H), tiles);
 }
 
 // rint(v / s) with the IEEE quotient, clamped to +-127, usually without a
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(kTqWarps * 32)
 quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
                         int K, int nmax, int64_t tail_off, int64_t l1_off, uint8_t* __restrict__ tiles) {
+    pdl_sync();
     __shared__ int s_l1[kTqMaxSteps];
     __shared__ int s_info[2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,12 +395,12 @@ int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool f
     const int64_t tail = bft::blocks_bytes(d, K);
     const int64_t l1 = tail + mxt::max_tiles(d, nmax) * nmax * 4;
     if (from_bf16_tokens)
-        quant_tiles_int8_kernel<uint16_t, true><<<(unsigned)blocks, kTqWarps * 32, 0, st>>>(
-            static_cast<const uint16_t*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail, l1, tiles);
-    else
-        quant_tiles_int8_kernel<float, false><<<(unsigned)blocks, kTqWarps * 32, 0, st>>>(
-            static_cast<const float*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail, l1, tiles);
-    return launch_status();
+        return launch_pdl(quant_tiles_int8_kernel<uint16_t, true>, (unsigned)blocks, kTqWarps * 32, 0, st,
+                          static_cast<const uint16_t*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail,
+                          l1, tiles);
+    return launch_pdl(quant_tiles_int8_kernel<float, false>, (unsigned)blocks, kTqWarps * 32, 0, st,
+                      static_cast<const float*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail, l1,
+                      tiles);
 }
 
 // W4A16 h tiles (bf16, with per-32-column group maxima) -> fp16 tiles for
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(kPqWarps * 32)
 h_to_f16_kernel(const uint8_t* __restrict__ h_tiles, const float* __restrict__ gmax, const int32_t* __restrict__ offsets,
                 const int32_t* __restrict__ tile_start, int E, int I, int nmax, int64_t P, uint8_t* __restrict__ out,
                 float* __restrict__ fac) {
+    pdl_sync();
     const int lane = threadIdx.x & 31;
     const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
     int tile = -1, row = 0;
@@ -458,26 +461,23 @@ int h_to_f16_launch(const qmoe_dims* d, const uint8_t* h_tiles, const int32_t* o
     if (P == 0) return QMOE_OK;
     const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
     const int64_t tail = bft::blocks_bytes(d, d->I);
-    h_to_f16_kernel<<<(unsigned)blocks, kPqWarps * 32, 0, st>>>(
-        h_tiles, reinterpret_cast<const float*>(h_tiles + tail), offsets, tile_start, d->E, d->I, mxt::nmax_for(d), P,
-        out, reinterpret_cast<float*>(out + tail));
-    return launch_status();
+    return launch_pdl(h_to_f16_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, h_tiles,
+                      reinterpret_cast<const float*>(h_tiles + tail), offsets, tile_start, d->E, d->I,
+                      mxt::nmax_for(d), P, out, reinterpret_cast<float*>(out + tail));
 }
 
 int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st) {
     const int64_t n8 = rows * cols / 8;
     if (n8 == 0) return QMOE_OK;
     const int64_t blocks = (n8 + 255) / 256;
-    quant_mx_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n8,
-                                                          reinterpret_cast<uint2*>(q), s);
-    return launch_status();
+    return launch_pdl(quant_mx_bf16_kernel, (unsigned)blocks, 256, 0, st, reinterpret_cast<const uint4*>(x), n8,
+                      reinterpret_cast<uint2*>(q), s);
 }
 
 template <typename In>
 int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float* s, cudaStream_t st) {
     if (rows == 0) return QMOE_OK;
-    quant_rows_int8_kernel<In><<<(unsigned)rows, 256, 0, st>>>(x, cols, q, s);
-    return launch_status();
+    return launch_pdl(quant_rows_int8_kernel<In>, (unsigned)rows, 256, 0, st, x, cols, q, s);
 }
 template int quant_int8_launch<uint16_t>(int64_t, int64_t, const uint16_t*, int8_t*, float*, cudaStream_t);
 template int quant_int8_launch<float>(int64_t, int64_t, const float*, int8_t*, float*, cudaStream_t);

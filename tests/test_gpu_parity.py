@@ -463,6 +463,34 @@ def test_forward_entry_point_matches_stagewise_and_is_deterministic(scheme):
     assert np.array_equal(outs[0], stage["out"])
 
 
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8", "w4a8"])
+def test_forward_back_to_back_calls_share_a_workspace(scheme):
+    # Consecutive whole-layer calls on one stream, no synchronisation between
+    # them, one workspace: each kernel may start before the one ahead of it
+    # completes (dependent launches), and the next call's routing sort
+    # rewrites the buffers the previous call's combine reads.  Every call must
+    # still equal the same batch run alone, stage by stage.
+    H, E, k, I = 512, 10, 4, 256
+    ws_ = [gen.Workload(f"b2b_{scheme}_{i}", scheme, T, H, E, k, I, "uniform", 300 + i, 299)
+           for i, T in enumerate((40, 7, 33, 1))]
+    ds = [gen.make_all(w) for w in ws_]
+    wt = gp.device_weights(ws_[0], ds[0])
+    qd = lambda w: qb.dims(w.T, w.k, w.H, w.I, w.E)
+    ws = qb.alloc_workspace(max(qb.forward_workspace_bytes(qd(w), scheme) for w in ws_))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ins = [{key: gp.dev(d[key]) for key in ("x", "topk_ids", "topk_w")} for d in ds]
+    outs = [gp.empty((w.T, H), torch.int16) for w in ws_]
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for w, t, out in zip(ws_, ins, outs):
+            qb.qmoe_moe_forward(scheme, qd(w), t["x"], t["topk_ids"], t["topk_w"], wt["w1"], wt["w1_s"], wt["w2"],
+                                wt["w2_s"], out, status, ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for w, d, out in zip(ws_, ds, outs):
+        assert np.array_equal(gp.host(out, np.uint16), gp.run_layer(w, d)["out"]), w.name
+
+
 @pytest.mark.parametrize("scheme", ["mxfp4", "w8a8", "w4a8", "w4a16"])
 @pytest.mark.parametrize("nmax", [16, 112, 224])
 def test_layer_with_each_token_tile(scheme, nmax):
