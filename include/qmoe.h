@@ -118,7 +118,8 @@ int qmoe_tile_nmax(const qmoe_dims* d);
 /* ---------------------------------------------------------------- routing
  *
  * Bytes of device workspace the routing and GEMM calls need for dims *d
- * (scratch for per-chunk histograms and the GEMM tile schedule). */
+ * (scratch for per-chunk histograms, the GEMM tile schedule and each slot's
+ * row in the token tiles). */
 size_t qmoe_workspace_bytes(const qmoe_dims* d);
 
 /* qmoe_align_sort -- expert-sorted permutation of the routed pairs.
@@ -134,7 +135,8 @@ size_t qmoe_workspace_bytes(const qmoe_dims* d);
  * out  pair_slot       int32 [P]; pair id -> slot, -1 for an invalid id
  * i/o  dev_status      int32 [1]; bit QMOE_DEV_BAD_EXPERT_ID is OR-ed in
  * ws   workspace of qmoe_workspace_bytes(d) bytes, 256-byte aligned; besides
- *      scratch it receives the token-tile schedule the MXFP4 calls read
+ *      scratch it receives the token-tile schedule and each slot's token-tile
+ *      row, which the permute, intermediate and GEMM calls read
  * The result is bit-identical run to run (no atomics decide an order). */
 int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
                     int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, void* ws,
@@ -182,9 +184,9 @@ int qmoe_quant_act_mxfp8(int64_t rows, int64_t cols, const uint16_t* x_bf16, uin
 
 /* MX activation tiles -- the layout in which the MXFP4 GEMMs take their
  * activations (x for stage 1, h for stage 2).  The valid slots of each expert
- * are cut into token tiles of NMAX rows (NMAX = 112, or 224 when T*k > 96*E;
- * tile_start = prefix over experts of ceil(count / NMAX), kept by
- * qmoe_align_sort in its workspace).  For reduction length K the buffer holds,
+ * are cut into token tiles of NMAX rows (NMAX = qmoe_tile_nmax(d), see the
+ * token-tile table; tile_start = prefix over experts of ceil(count / NMAX),
+ * kept by qmoe_align_sort in its workspace).  For reduction length K the buffer holds,
  * per (tile t, K step kt of 128), a block of NMAX*128 + ceil(NMAX/128)*512
  * bytes at ((t * K/128) + kt) * that size:
  *   row r's 128 E4M3 codes at r*128, 16-byte chunk c at ((c ^ (r % 8)) * 16);

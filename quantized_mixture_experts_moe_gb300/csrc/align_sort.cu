@@ -15,7 +15,9 @@
 //   3. scatter: each CTA walks its chunk again in pair order; a pair's slot
 //               is its chunk base + the running count of earlier equal ids,
 //               so the result is the stable counting sort.
-// The scan also derives the GEMMs' token-tile schedule.
+// The scan also derives the GEMMs' token-tile schedule, and the scatter
+// gives every slot its row in the token tiles (so the permute kernels look
+// it up instead of searching the offsets).
 #include "qmoe_common.cuh"
 #include "mx_tiles.cuh"
 
@@ -108,7 +110,8 @@ align_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks
 // (tile_start non-null) the token-tile schedule.
 __global__ void __launch_bounds__(kScanThreads)
 align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int nmax, int32_t* __restrict__ counts,
-                  int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ tile_start) {
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ tile_start,
+                  int32_t* __restrict__ slot_dest) {
     __shared__ int32_t ws[33];
     const int tid = threadIdx.x;
     pdl_sync();
@@ -140,14 +143,22 @@ align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int
         base += cnt[e - e0];
     }
     if (tid == 0) offsets[E] = total_valid;
-    for (int64_t s = (int64_t)total_valid + tid; s < P; s += kScanThreads) sorted_pair_ids[s] = -1;
+    for (int64_t s = (int64_t)total_valid + tid; s < P; s += kScanThreads) {
+        sorted_pair_ids[s] = -1;
+        if (slot_dest) slot_dest[s] = -1;
+    }
     if (tile_start) write_tile_schedule(cnt, e0, e1, E, nmax, ws, tile_start);
 }
 
 // The chunk's pairs in pair order onto their slots: cur[e] enters as the
 // chunk's first slot of expert e and is advanced past the chunk's pairs.
+// With slot_dest, each slot also gets its token-tile row
+// tile_start[e] * nmax + (slot - offsets[e]) (offsets and tile_start are
+// complete in global memory: written before this CTA's barrier, or by an
+// earlier kernel; read from L2).
 __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E, int64_t p0, int32_t* cur,
-                              int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pair_slot) {
+                              int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pair_slot,
+                              const int32_t* offsets, const int32_t* tile_start, int nmax, int32_t* slot_dest) {
     const int tid = threadIdx.x, warp = tid >> 5;
     for (int round = 0; round < kChunk / kThreads; ++round) {
         const int64_t r0 = p0 + round * kThreads;
@@ -172,7 +183,10 @@ __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E,
         }
         if (p < P) {
             pair_slot[p] = slot;
-            if (valid) sorted_pair_ids[slot] = (int32_t)p;
+            if (valid) {
+                sorted_pair_ids[slot] = (int32_t)p;
+                if (slot_dest) slot_dest[slot] = __ldcg(tile_start + e) * nmax + slot - __ldcg(offsets + e);
+            }
         }
     }
 }
@@ -185,14 +199,16 @@ __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E,
 __global__ void __launch_bounds__(kThreads)
 align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
                      const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_pair_ids,
-                     int32_t* __restrict__ pair_slot) {
+                     int32_t* __restrict__ pair_slot, const int32_t* __restrict__ offsets,
+                     const int32_t* __restrict__ tile_start, int nmax, int32_t* __restrict__ slot_dest) {
     extern __shared__ int32_t cur[];
     const int tid = threadIdx.x;
     pdl_sync();
     const int32_t* base = hist + (size_t)blockIdx.x * E;
     for (int e = tid; e < E; e += kThreads) cur[e] = base[e];
     __syncthreads();
-    scatter_chunk(ids, P, E, (int64_t)blockIdx.x * kChunk, cur, sorted_pair_ids, pair_slot);
+    scatter_chunk(ids, P, E, (int64_t)blockIdx.x * kChunk, cur, sorted_pair_ids, pair_slot, offsets, tile_start, nmax,
+                  slot_dest);
 }
 
 // One CTA for at most one chunk of pairs: histogram, scan (counts, offsets,
@@ -200,7 +216,8 @@ align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchu
 __global__ void __launch_bounds__(kThreads)
 align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, int32_t* __restrict__ counts,
                    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids,
-                   int32_t* __restrict__ pair_slot, int32_t* __restrict__ tile_start, int32_t* __restrict__ dev_status) {
+                   int32_t* __restrict__ pair_slot, int32_t* __restrict__ tile_start, int32_t* __restrict__ slot_dest,
+                   int32_t* __restrict__ dev_status) {
     extern __shared__ int32_t cur[];  // per-expert counts, then cursors
     __shared__ int32_t ws[33];
     const int tid = threadIdx.x;
@@ -233,10 +250,13 @@ align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, 
         base += cnt[e - e0];
     }
     if (tid == 0) offsets[E] = total_valid;
-    for (int64_t s = (int64_t)total_valid + tid; s < P; s += kThreads) sorted_pair_ids[s] = -1;
+    for (int64_t s = (int64_t)total_valid + tid; s < P; s += kThreads) {
+        sorted_pair_ids[s] = -1;
+        if (slot_dest) slot_dest[s] = -1;
+    }
     if (tile_start) write_tile_schedule(cnt, e0, e1, E, nmax, ws, tile_start);
     __syncthreads();
-    scatter_chunk(ids, P, E, 0, cur, sorted_pair_ids, pair_slot);
+    scatter_chunk(ids, P, E, 0, cur, sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest);
 }
 
 size_t align_ws_bytes(int64_t P, int E) {
@@ -249,6 +269,7 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
                       int nmax, int32_t* tile_start, cudaStream_t stream) {
     const int nchunks = (int)((P + kChunk - 1) / kChunk);
     const size_t smem = (size_t)E * sizeof(int32_t);
+    int32_t* slot_dest = tile_start ? tile_start + schedule_ints(E) : nullptr;
     if (smem > 48 * 1024) {
         cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -256,14 +277,14 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
     }
     if (nchunks <= 1)
         return launch_pdl(align_small_kernel, 1, kThreads, smem, stream, ids, P, E, nmax, counts, offsets,
-                          sorted_pair_ids, pair_slot, tile_start, dev_status);
+                          sorted_pair_ids, pair_slot, tile_start, slot_dest, dev_status);
     int rc = launch_pdl(align_hist_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist, dev_status);
     if (rc == QMOE_OK)
         rc = launch_pdl(align_scan_kernel, 1, kScanThreads, 0, stream, hist, P, E, nchunks, nmax, counts, offsets,
-                        sorted_pair_ids, tile_start);
+                        sorted_pair_ids, tile_start, slot_dest);
     if (rc == QMOE_OK)
         rc = launch_pdl(align_scatter_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist,
-                        sorted_pair_ids, pair_slot);
+                        sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest);
     return rc;
 }
 
@@ -277,8 +298,8 @@ int32_t* tile_schedule_in(void* ws, const qmoe_dims* d) {
 extern "C" size_t qmoe_workspace_bytes(const qmoe_dims* d) {
     if (!qmoe::dims_ok(d)) return 0;
     const int64_t P = (int64_t)d->T * d->k;
-    // histograms + room for the GEMM schedule (tile offsets over experts)
-    return qmoe::align_ws_bytes(P, d->E) + (size_t)((d->E + 1 + 64) * 4 + 255) / 256 * 256;
+    // histograms, the GEMM schedule (tile offsets over experts), each slot's token-tile row
+    return qmoe::align_ws_bytes(P, d->E) + (size_t)qmoe::schedule_ints(d->E) * 4 + (size_t)(P * 4 + 255) / 256 * 256;
 }
 
 extern "C" int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,

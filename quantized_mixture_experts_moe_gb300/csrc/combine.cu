@@ -20,16 +20,30 @@ combine_kernel(const uint16_t* __restrict__ y, const float* __restrict__ topk_w,
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-        const int slot = pair_slot[(int64_t)t * k + j];
-        if (slot < 0) continue;
-        const float w = topk_w[(int64_t)t * k + j];
-        const uint4 v = *reinterpret_cast<const uint4*>(y + (int64_t)slot * H + c8 * 8);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    // groups of up to 8 pairs: their slots and weights, then their y rows, are
+    // loaded together (independent loads in flight), then summed in j order
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        int slot[8];
+        float w[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(w, __uint_as_float(u[i] << 16), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        for (int j = 0; j < 8; ++j) {
+            const bool in = j0 + j < k;
+            slot[j] = in ? pair_slot[(int64_t)t * k + j0 + j] : -1;
+            w[j] = in ? topk_w[(int64_t)t * k + j0 + j] : 0.f;
+        }
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = slot[j] >= 0 ? *reinterpret_cast<const uint4*>(y + (int64_t)slot[j] * H + c8 * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (slot[j] < 0) continue;
+            const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(w[j], __uint_as_float(u[i] << 16), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(w[j], __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+            }
         }
     }
     uint4 o;

@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
     // sort ran two launches back) the weight producer and the converters,
     // which read only the schedule and the weights, start before that; the
     // warps that read the predecessor's output wait.
-    if (!a.weights_early) pdl_sync();
+    if (!a.weights_early) pdl_wait();
     for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = __ldcg(a.tile_start + i);
     if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::RS; ++s) {
@@ -371,10 +371,13 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
                 }
                 if (!ok) break;
             }
+            // every load issued: the next kernel may launch (after this CTA's own wait)
+            pdl_wait();
+            pdl_trigger();
         }
     } else if (warp == WARP_B) {
         // ------------------------------------------------ activation producer
-        if (a.weights_early) pdl_sync();
+        if (a.weights_early) pdl_wait();
         if (lane == 0) {
             int bs = 0;
             uint32_t ph = 0;
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         }
     } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
         // ------------------------------------------------ MMA issuers (warp-uniform; one elected lane issues)
-        if (a.weights_early) pdl_sync();
+        if (a.weights_early) pdl_wait();
         const int iss = warp - WARP_MMA;
         int bs = 0, as = 0;
         uint32_t bph = 0, aph = 0, ev = 0;
@@ -541,7 +544,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         }
     } else {
         // ------------------------------------------------ epilogue
-        if (a.weights_early) pdl_sync();
+        if (a.weights_early) pdl_wait();
         const int q = warp & 3, eh = (warp - WARP_EPI0) >> 2;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int n = q * 32 + lane;  // weight row within a tile = output column within its 128-column block

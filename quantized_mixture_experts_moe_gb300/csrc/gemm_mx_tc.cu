@@ -186,7 +186,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     // sort ran two launches back) only the warps that consume the
     // predecessor's output wait; the schedule is read and weights stream
     // before that.
-    if (!a.weights_early) pdl_sync();
+    if (!a.weights_early) pdl_wait();
 
     // ---- token-tile schedule (computed with the routing sort)
     for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = __ldcg(a.tile_start + i);
@@ -249,12 +249,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                     if (++slot == C::S) { slot = 0; phase ^= 1; }
                 }
             }
+            // every load issued: the next kernel may launch (after this CTA's own wait)
+            pdl_wait();
+            pdl_trigger();
         }
     } else if (warp == WARP_B) {
         // ------------------------------------------------ activation producer (bulk copies)
         // A step's activations are one block of the MX tile layout: the
         // first nmma rows of codes (already swizzled) and the scale atoms.
-        if (a.weights_early) pdl_sync();
+        if (a.weights_early) pdl_wait();
         if (lane == 0) {
             int slot = 0;
             uint32_t phase = 0;
@@ -280,7 +283,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // atoms to TMEM, issues its four MMAs per step and commits; the slot
         // frees after both commits.
         const int iss = warp - WARP_MMA;
-        if (a.weights_early) pdl_sync();
+        if (a.weights_early) pdl_wait();
         if (lane == 0 && iss < C::AT) {
             int slot = 0, sf = 0, ab = 0;
             uint32_t phase = 0, pacc = 0;
@@ -325,7 +328,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue warps
-        if (a.weights_early) pdl_sync();
+        if (a.weights_early) pdl_wait();
         const int q = warp & 3;                       // TMEM lane quadrant this warp may access
         const int half = (warp - WARP_EPI0) >> 2;     // which 16-column chunks it takes
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;

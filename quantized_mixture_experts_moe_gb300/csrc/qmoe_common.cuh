@@ -27,6 +27,13 @@ inline int launch_status() {
 
 inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// The routing workspace holds, after the per-chunk histograms, the token-tile
+// schedule (E + 1 ints, padded to 256 bytes with room for 64 more) and then
+// one int per slot: the slot's row in the token tiles, tile * NMAX + row (-1
+// past the routed slots).  These are the ints from the schedule's start to
+// the per-slot rows.
+inline int64_t schedule_ints(int E) { return ((int64_t)(E + 1 + 64) * 4 + 255) / 256 * 64; }
+
 // ------------------------------------------------------------------ dependent launches
 //
 // Every kernel of the layer is launched with programmatic stream
@@ -36,8 +43,12 @@ inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 // predecessor reads or writes (griddepcontrol.wait returns once the
 // predecessor grid has completed and its memory operations are visible), and
 // pdl_trigger() only after that wait.  Hence when a kernel is launched, the
-// kernel two places before it in the stream has completed.  Launched without
-// the attribute (or with no predecessor kernel) both are no-ops.
+// kernel two places before it in the stream has completed.  The small kernels
+// trigger right after their wait; the GEMMs trigger once their weight
+// producer has issued its last load, so that their successor's CTAs do not
+// take bandwidth from the GEMM's last units, which finish the launch.
+// Launched without the attribute (or with no predecessor kernel) both are
+// no-ops.
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -49,7 +60,6 @@ __device__ __forceinline__ void pdl_sync() {
 #ifndef QMOE_PDL
 #define QMOE_PDL 1
 #endif
-
 // One launch of `kernel` on `st` that may overlap its predecessor's tail.
 template <typename... KArgs, typename... Args>
 inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -121,8 +121,8 @@ __device__ __forceinline__ void mx_quant16(const uint4 v0, const uint4 v1, uint4
 
 __global__ void __launch_bounds__(kPqWarps * 32)
 permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_slot,
-                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
-                        int H, int nmax, int T, uint8_t* __restrict__ tiles) {
+                        const int32_t* __restrict__ slot_dest, int k, int H, int nmax, int T,
+                        uint8_t* __restrict__ tiles) {
     pdl_sync();
     const int lane = threadIdx.x & 31;
     const int nseg = H / 1024 + (H % 1024 != 0);  // 1024-element segments of a row
@@ -150,19 +150,14 @@ permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restric
     mx_quant16(a0, a1, ca, sa);
     mx_quant16(b0, b1, cb, sbb);
     for (int j0 = 0; j0 < k; j0 += 32) {
-        // lane i finds pair j0 + i's tile and row (tile -1: invalid expert id)
+        // lane i looks up pair j0 + i's tile and row (tile -1: invalid expert id)
         int dtile = -1, drow = 0;
         if (j0 + lane < k) {
             const int slot = pair_slot[(int64_t)tok * k + j0 + lane];
-            if (slot >= 0 && slot < offsets[E]) {
-                int lo = 0, hi = E;  // largest e with offsets[e] <= slot
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (offsets[mid] <= slot) lo = mid; else hi = mid;
-                }
-                const int local = slot - offsets[lo];
-                dtile = tile_start[lo] + local / nmax;
-                drow = local % nmax;
+            const int dst = slot >= 0 ? slot_dest[slot] : -1;
+            if (dst >= 0) {
+                dtile = dst / nmax;
+                drow = dst - dtile * nmax;
             }
         }
         const int jn = min(32, k - j0);
@@ -190,8 +185,8 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
     if ((int64_t)d->T * d->k == 0) return QMOE_OK;
     const int64_t warps = (int64_t)d->T * (d->H / 1024 + (d->H % 1024 != 0));
     const int64_t blocks = (warps + kPqWarps - 1) / kPqWarps;
-    return launch_pdl(permute_quant_mx_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, pair_slot, offsets,
-                      tile_start, d->E, d->k, d->H, mxt::nmax_for(d), d->T, tiles);
+    return launch_pdl(permute_quant_mx_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, pair_slot,
+                      tile_start + schedule_ints(d->E), d->k, d->H, mxt::nmax_for(d), d->T, tiles);
 }
 
 // Permute bf16 activations into W4A16 x tiles: one warp per expert-sorted
@@ -201,22 +196,20 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
 // and 2^e goes to the tile's per-row tail for the GEMM epilogue.
 __global__ void __launch_bounds__(kPqWarps * 32)
 permute_x_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
-                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k, int H,
-                     int nmax, int64_t P, int64_t tail_off, uint8_t* __restrict__ tiles) {
+                     const int32_t* __restrict__ slot_dest, int k, int H, int nmax, int64_t P, int64_t tail_off,
+                     uint8_t* __restrict__ tiles) {
     pdl_sync();
     const int lane = threadIdx.x & 31;
     const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
     int tile = -1, row = 0, tok = 0;
-    if (lane == 0 && slot < P && slot < offsets[E]) {
-        int lo = 0, hi = E;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (offsets[mid] <= slot) lo = mid; else hi = mid;
+    if (lane == 0 && slot < P) {
+        const int dst = slot_dest[slot];  // -1 past the routed slots
+        const int p = sorted_pair_ids[slot];
+        if (dst >= 0) {
+            tile = dst / nmax;
+            row = dst - tile * nmax;
+            tok = p / k;
         }
-        const int local = (int)(slot - offsets[lo]);
-        tile = tile_start[lo] + local / nmax;
-        row = local % nmax;
-        tok = sorted_pair_ids[slot] / k;
     }
     tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
     if (tile < 0) return;
@@ -257,8 +250,9 @@ int permute_x_f16_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* s
     const int64_t P = (int64_t)d->T * d->k;
     if (P == 0) return QMOE_OK;
     const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
-    return launch_pdl(permute_x_f16_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, sorted, offsets, tile_start,
-                      d->E, d->k, d->H, mxt::nmax_for(d), P, bft::blocks_bytes(d, d->H), tiles);
+    return launch_pdl(permute_x_f16_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, sorted,
+                      tile_start + schedule_ints(d->E), d->k, d->H, mxt::nmax_for(d), P, bft::blocks_bytes(d, d->H),
+                      tiles);
 }
 
 // rint(v / s) with the IEEE quotient, clamped to +-127, usually without a
@@ -410,22 +404,19 @@ int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool f
 // row becomes the fp16 value v * 2^-e (exact in range) at the same place of
 // the same tile layout, and 2^e goes to the output's per-row tail.
 __global__ void __launch_bounds__(kPqWarps * 32)
-h_to_f16_kernel(const uint8_t* __restrict__ h_tiles, const float* __restrict__ gmax, const int32_t* __restrict__ offsets,
-                const int32_t* __restrict__ tile_start, int E, int I, int nmax, int64_t P, uint8_t* __restrict__ out,
+h_to_f16_kernel(const uint8_t* __restrict__ h_tiles, const float* __restrict__ gmax,
+                const int32_t* __restrict__ slot_dest, int I, int nmax, int64_t P, uint8_t* __restrict__ out,
                 float* __restrict__ fac) {
     pdl_sync();
     const int lane = threadIdx.x & 31;
     const int64_t slot = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
     int tile = -1, row = 0;
-    if (lane == 0 && slot < P && slot < offsets[E]) {
-        int lo = 0, hi = E;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (offsets[mid] <= slot) lo = mid; else hi = mid;
+    if (lane == 0 && slot < P) {
+        const int dst = slot_dest[slot];  // -1 past the routed slots
+        if (dst >= 0) {
+            tile = dst / nmax;
+            row = dst - tile * nmax;
         }
-        const int local = (int)(slot - offsets[lo]);
-        tile = tile_start[lo] + local / nmax;
-        row = local % nmax;
     }
     tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
     if (tile < 0) return;
@@ -462,7 +453,7 @@ int h_to_f16_launch(const qmoe_dims* d, const uint8_t* h_tiles, const int32_t* o
     const int64_t blocks = (P + kPqWarps - 1) / kPqWarps;
     const int64_t tail = bft::blocks_bytes(d, d->I);
     return launch_pdl(h_to_f16_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, h_tiles,
-                      reinterpret_cast<const float*>(h_tiles + tail), offsets, tile_start, d->E, d->I,
+                      reinterpret_cast<const float*>(h_tiles + tail), tile_start + schedule_ints(d->E), d->I,
                       mxt::nmax_for(d), P, out, reinterpret_cast<float*>(out + tail));
 }
 
