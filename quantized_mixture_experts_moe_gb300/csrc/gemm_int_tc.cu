@@ -143,7 +143,7 @@ struct Args {
 template <int NS>
 __device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax, const int* tile_start, int E,
                                             const int32_t* offsets, int& e, int& t, int& half, int& nb, int& m0,
-                                            int& ntok) {
+                                            int& ntok, bool l2) {
     const int th = u / NB;
     nb = u - th * NB;
     t = th / halves;
@@ -154,10 +154,12 @@ __device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax,
         if (tile_start[mid] <= t) lo = mid; else hi = mid;
     }
     e = lo;
-    // offsets come from the routing sort, which may have completed after this
-    // kernel started (dependent launch): read them from L2
-    m0 = __ldcg(offsets + e) + (t - tile_start[e]) * nmax + half * NS;
-    ntok = min(min(NS, nmax - half * NS), __ldcg(offsets + e + 1) - m0);
+    // l2: a role that runs before this kernel's dependent-launch wait reads
+    // the routing sort's offsets from L2 (the sort completed before the launch)
+    const int o0 = l2 ? __ldcg(offsets + e) : offsets[e];
+    const int o1 = l2 ? __ldcg(offsets + e + 1) : offsets[e + 1];
+    m0 = o0 + (t - tile_start[e]) * nmax + half * NS;
+    ntok = min(min(NS, nmax - half * NS), o1 - m0);
 }
 
 __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             uint32_t ph = 0;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, t, half, nb, m0, ntok;
-                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, a.weights_early != 0);
                 if (ntok <= 0) continue;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             const int64_t bb = (int64_t)a.nmax * 128;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, t, half, nb, m0, ntok;
-                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
                 if (ntok <= 0) continue;
                 const uint32_t bytes = (uint32_t)((ntok + 15) & ~15) * 128u;
                 bool ok = true;
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         bool pending = false;  // an accumulator event not yet handed back by the epilogue
         for (int u = blockIdx.x; u < total_units && !warp_flag(abort_flag); u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
             if (ntok <= 0) continue;
             const int nmma = (ntok + 15) & ~15;
             const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, a.weights_early != 0);
             if (ntok <= 0) continue;
             for (int kt = 0; kt < KT; ++kt, ++gs) {
                 if (!warp_wait(&raw_full[rs], rph, lane)) {
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
             if (ntok <= 0) continue;
             const float* ts = a.act_scale + (int64_t)t * a.nmax + half * C::NS;
             float ws0, ws1;  // channel scales of this thread's row in the two tiles

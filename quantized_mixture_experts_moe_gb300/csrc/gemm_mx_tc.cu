@@ -130,7 +130,7 @@ struct Args {
 
 template <int NMAX>
 __device__ __forceinline__ void decode_unit(int u, int NB, const int* tile_start, int E, const int32_t* offsets,
-                                            int& e, int& m0, int& ntok, int& nb, int& t) {
+                                            int& e, int& m0, int& ntok, int& nb, int& t, bool l2) {
     t = u / NB;
     nb = u - t * NB;
     int lo = 0, hi = E;
@@ -139,10 +139,12 @@ __device__ __forceinline__ void decode_unit(int u, int NB, const int* tile_start
         if (tile_start[mid] <= t) lo = mid; else hi = mid;
     }
     e = lo;
-    // offsets come from the routing sort, which may have completed after this
-    // kernel started (dependent launch): read them from L2
-    m0 = __ldcg(offsets + e) + (t - tile_start[e]) * NMAX;
-    ntok = min(NMAX, __ldcg(offsets + e + 1) - m0);
+    // l2: a role that runs before this kernel's dependent-launch wait reads
+    // the routing sort's offsets from L2 (the sort completed before the launch)
+    const int o0 = l2 ? __ldcg(offsets + e) : offsets[e];
+    const int o1 = l2 ? __ldcg(offsets + e + 1) : offsets[e + 1];
+    m0 = o0 + (t - tile_start[e]) * NMAX;
+    ntok = min(NMAX, o1 - m0);
 }
 
 __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
@@ -228,7 +230,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             const int64_t up_tiles = (int64_t)(a.I / 128) * KT;  // gate tile -> up tile distance (stage 1)
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb, t;
-                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t, a.weights_early != 0);
                 const int rt0 = (STAGE == 1) ? (e * rows_per_e + nb * 128) / 128 : (e * rows_per_e + nb * 256) / 128;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&empty[slot], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
@@ -264,7 +266,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             const int64_t bb = mxt::block_bytes(NMAX);
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb, t;
-                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t, false);
                 const uint32_t rows_bytes = (uint32_t)((ntok + 15) & ~15) * 128u;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&empty[slot], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
@@ -290,7 +292,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             const uint32_t sf_base = C::SF_COL + iss * 2 * C::SF_SLOT;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb, t;
-                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
+                decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t, false);
                 const int nmma = (ntok + 15) & ~15;
                 if (!tc::mbar_wait(&acc_empty[ab], pacc ^ 1)) { set_abort(abort_flag, a.status); break; }
                 tc::tc_fence_after();
@@ -337,7 +339,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         uint32_t pacc = 0;
         for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
             int e, m0, ntok, nb, t;
-            decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t);
+            decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t, false);
             int w = 1;
             if (lane == 0) w = tc::mbar_wait_sleep(&acc_full[ab], pacc) ? 1 : 0;
             if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {

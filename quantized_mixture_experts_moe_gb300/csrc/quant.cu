@@ -119,15 +119,13 @@ __device__ __forceinline__ void mx_quant16(const uint4 v0, const uint4 v1, uint4
     }
 }
 
-__global__ void __launch_bounds__(kPqWarps * 32)
-permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_slot,
-                        const int32_t* __restrict__ slot_dest, int k, int H, int nmax, int T,
-                        uint8_t* __restrict__ tiles) {
-    pdl_sync();
+// One (token, segment) item of the permute; wid < T * nseg, warp-uniform.
+__device__ __forceinline__ void permute_quant_mx_item(int64_t wid, const uint16_t* __restrict__ x,
+                                                      const int32_t* __restrict__ pair_slot,
+                                                      const int32_t* __restrict__ slot_dest, int k, int H, int nmax,
+                                                      uint8_t* __restrict__ tiles) {
     const int lane = threadIdx.x & 31;
     const int nseg = H / 1024 + (H % 1024 != 0);  // 1024-element segments of a row
-    const int64_t wid = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5);
-    if (wid >= (int64_t)T * nseg) return;  // warp-uniform
     const int tok = (int)(wid / nseg), seg = (int)(wid % nseg);
     const uint16_t* xr = x + (int64_t)tok * H;
     const int KT = H / 128;
@@ -180,11 +178,38 @@ permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restric
     }
 }
 
+// Items are strided over a grid of the CTAs that fit on the GPU at once, so
+// the last wave is not left mostly idle.
+__global__ void __launch_bounds__(kPqWarps * 32)
+permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_slot,
+                        const int32_t* __restrict__ slot_dest, int k, int H, int nmax, int T,
+                        uint8_t* __restrict__ tiles) {
+    pdl_sync();
+    const int64_t items = (int64_t)T * (H / 1024 + (H % 1024 != 0));
+    for (int64_t wid = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5); wid < items;
+         wid += (int64_t)gridDim.x * kPqWarps)
+        permute_quant_mx_item(wid, x, pair_slot, slot_dest, k, H, nmax, tiles);
+}
+
+// CTAs of `kernel` that fit on the current GPU at once (0 on error).
+template <typename K>
+static int64_t resident_ctas(K kernel, int threads) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess)
+        return 0;
+    return (int64_t)sms * per_sm;
+}
+
 int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* pair_slot, const int32_t* offsets,
                             const int32_t* tile_start, uint8_t* tiles, cudaStream_t st) {
     if ((int64_t)d->T * d->k == 0) return QMOE_OK;
     const int64_t warps = (int64_t)d->T * (d->H / 1024 + (d->H % 1024 != 0));
-    const int64_t blocks = (warps + kPqWarps - 1) / kPqWarps;
+    int64_t blocks = (warps + kPqWarps - 1) / kPqWarps;
+    const int64_t fit = resident_ctas(permute_quant_mx_kernel, kPqWarps * 32);
+    if (fit <= 0) return QMOE_ERR_CUDA;
+    if (blocks > fit) blocks = fit;
     return launch_pdl(permute_quant_mx_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, pair_slot,
                       tile_start + schedule_ints(d->E), d->k, d->H, mxt::nmax_for(d), d->T, tiles);
 }
