@@ -73,6 +73,12 @@ struct Cfg {
     // two adjacent 128-column blocks of W2; both share the step's activations
     static constexpr int AT = 2;
     static constexpr int ACC_BUFS = (AT * NMAX * 2 <= 448) ? 2 : 1;
+    // L2 eviction hints on the loads (weights evict-first, activations
+    // evict-last) for 16-row tiles, which the tile table picks for small
+    // batches: there each expert has one tile and its weights pass once.
+    // Measured on GB300 with L2 flushed: decode T=16 114.6 -> 103.2 us/step;
+    // at larger tiles they were neutral to 0.5% slower.
+    static constexpr bool L2_HINTS = (NMAX == 16);
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
@@ -224,6 +230,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // ------------------------------------------------ weight producer (TMA)
         if (lane == 0) {
             tc::prefetch_tensormap(&mapW);
+            // 16-row tiles (small batches): one tile per expert, its weights streamed once
+            const uint64_t pol = C::L2_HINTS ? tc::l2_evict_first() : 0ull;
             int slot = 0;
             uint32_t phase = 0;
             const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
@@ -239,14 +247,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                     const int64_t t0 = (int64_t)rt0 * KT + kt;
                     if (STAGE == 1) {
                         // 4D view {row bytes, rows within a half, gate/up half, expert}: one box = both tiles
-                        tc::tma_load_4d(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, (nb * KT + kt) * 128, 0, e);
-                        tc::bulk_load(dS, a.w_s + t0 * 512, 512, &full[slot]);
-                        tc::bulk_load(dS + 512, a.w_s + (t0 + up_tiles) * 512, 512, &full[slot]);
+                        tc::tma_load_4d_hint(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, (nb * KT + kt) * 128, 0, e,
+                                             pol, C::L2_HINTS);
+                        tc::bulk_load_hint(dS, a.w_s + t0 * 512, 512, &full[slot], pol, C::L2_HINTS);
+                        tc::bulk_load_hint(dS + 512, a.w_s + (t0 + up_tiles) * 512, 512, &full[slot], pol,
+                                           C::L2_HINTS);
                     } else {
                         // 4D view {row bytes, tile rows, K tile, row tile}: one box = row tiles rt0, rt0 + 1
-                        tc::tma_load_4d(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, 0, kt, rt0);
-                        tc::bulk_load(dS, a.w_s + t0 * 512, 512, &full[slot]);
-                        tc::bulk_load(dS + 512, a.w_s + (t0 + KT) * 512, 512, &full[slot]);
+                        tc::tma_load_4d_hint(sA + slot * C::A_BYTES, &mapW, &full[slot], 0, 0, kt, rt0, pol,
+                                             C::L2_HINTS);
+                        tc::bulk_load_hint(dS, a.w_s + t0 * 512, 512, &full[slot], pol, C::L2_HINTS);
+                        tc::bulk_load_hint(dS + 512, a.w_s + (t0 + KT) * 512, 512, &full[slot], pol, C::L2_HINTS);
                     }
                     if (++slot == C::S) { slot = 0; phase ^= 1; }
                 }
@@ -261,6 +272,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // first nmma rows of codes (already swizzled) and the scale atoms.
         if (a.weights_early) pdl_wait();
         if (lane == 0) {
+            const uint64_t pol = C::L2_HINTS ? tc::l2_evict_last() : 0ull;  // re-read by the expert's column blocks
             int slot = 0;
             uint32_t phase = 0;
             const int64_t bb = mxt::block_bytes(NMAX);
@@ -272,8 +284,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                     if (!tc::mbar_wait(&empty[slot], phase ^ 1)) { set_abort(abort_flag, a.status); break; }
                     tc::mbar_arrive_expect_tx(&full[slot], rows_bytes + C::SFB_BYTES);
                     const uint8_t* blk = a.act + ((int64_t)t * KT + kt) * bb;
-                    tc::bulk_load(sB + slot * C::B_BYTES, blk, rows_bytes, &full[slot]);
-                    tc::bulk_load(sSFB + slot * C::SFB_BYTES, blk + NMAX * 128, C::SFB_BYTES, &full[slot]);
+                    tc::bulk_load_hint(sB + slot * C::B_BYTES, blk, rows_bytes, &full[slot], pol, C::L2_HINTS);
+                    tc::bulk_load_hint(sSFB + slot * C::SFB_BYTES, blk + NMAX * 128, C::SFB_BYTES, &full[slot], pol,
+                                       C::L2_HINTS);
                     if (++slot == C::S) { slot = 0; phase ^= 1; }
                 }
             }

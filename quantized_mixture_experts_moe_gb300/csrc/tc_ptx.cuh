@@ -115,6 +115,57 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
+// ------------------------------------------------------------------ L2 eviction priority
+//
+// Where each expert's weights are streamed once per step (one token tile per
+// expert), weight loads may carry an evict-first policy and activation-tile
+// loads an evict-last one, so the weight stream does not push other data out
+// of L2.  The *_hint loads take the policy and whether to apply it (use =
+// false: the plain load).
+#ifndef QMOE_L2_HINTS
+#define QMOE_L2_HINTS 1
+#endif
+
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy, bool use) {
+#if QMOE_L2_HINTS
+    if (!use) return bulk_load(dst, src, bytes, bar);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+#else
+    bulk_load(dst, src, bytes, bar);
+#endif
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                                 int w, uint64_t policy, bool use) {
+#if QMOE_L2_HINTS
+    if (!use) return tma_load_4d(dst, map, bar, x, y, z, w);
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+        "%4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+        : "memory");
+#else
+    tma_load_4d(dst, map, bar, x, y, z, w);
+#endif
+}
+
 // L2 prefetches (no shared memory, no completion tracking): bring a future
 // tile into L2 so the later shared-memory load is an L2 hit.
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
