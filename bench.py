@@ -37,7 +37,7 @@ L2_BYTES = 129 * 10**6  # GB300 L2
 # algorithmic bytes, per scheme, for the kernel as it stands; None once the
 # kernel changes after the capture
 TRAFFIC_RATIO_GEMM1 = {
-    "mxfp4": (309.254144 + 6.402560) / 292.782080,  # profiles/mx_gemm_kernel_prof_mxfp4_E64_T512.md
+    "mxfp4": (309.287424 + 6.629376) / 292.782080,  # profiles/mx_gemm_kernel_prof_mxfp4_E64_T512.md
     "w8a8": (160.009216 + 28.690944) / 108.130304,   # profiles/int_gemm_kernel_w8a8.md
     "w4a8": (113.458432 + 23.438336) / 61.992960,    # profiles/int_gemm_kernel_w4a8.md
 }
