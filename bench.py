@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -139,7 +140,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples (the JSON line carries their summary); QMOE_CLOCKS_DIR keeps them elsewhere
+        self.path = os.path.join(os.environ.get("QMOE_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"qmoe_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:

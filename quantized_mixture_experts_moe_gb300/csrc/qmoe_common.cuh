@@ -60,6 +60,7 @@ __device__ __forceinline__ void pdl_sync() {
 #ifndef QMOE_PDL
 #define QMOE_PDL 1
 #endif
+
 // One launch of `kernel` on `st` that may overlap its predecessor's tail.
 template <typename... KArgs, typename... Args>
 inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
