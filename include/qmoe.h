@@ -203,7 +203,9 @@ size_t qmoe_mx_tiles_bytes(const qmoe_dims* d, int64_t K);
  * permutation from qmoe_align_sort), slot pair_slot[p] of its expert gets the
  * codes of token t, written as MX activation tiles with K = H.  Each token
  * row is read and quantised once and written to its k slots.
- * ws = the workspace qmoe_align_sort filled for this routing. */
+ * ws = the workspace qmoe_align_sort filled for this routing; the kernel
+ * reads each pair's token-tile row from it (pair_slot and offsets must be
+ * that call's outputs). */
 int qmoe_permute_quant_mxfp8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* pair_slot,
                              const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                              qmoe_stream_t stream);
@@ -274,8 +276,11 @@ size_t qmoe_w8a8_tiles_bytes(const qmoe_dims* d, int64_t K);
  * qmoe_quant_rows_int8_bf16 applied to each token row of x_bf16 [T, H]) in
  * one pass: slot s gets the codes of token sorted_pair_ids[s] / k and its
  * scale, written as W8A8 tiles with K = H ([gfx1151] Constraint: W8A8 needs
- * quantised activations).  H % 128 == 0, H <= 16384.  ws = the workspace
- * qmoe_align_sort filled for this routing. */
+ * quantised activations).  Each token row is read and quantised once and
+ * written to its k slots.  H % 128 == 0, H <= 16384.  ws = the workspace
+ * qmoe_align_sort filled for this routing; the kernel reads each pair's
+ * token-tile row from it (sorted_pair_ids and offsets must be that call's
+ * outputs). */
 int qmoe_permute_quant_int8(const qmoe_dims* d, const uint16_t* x_bf16, const int32_t* sorted_pair_ids,
                             const int32_t* offsets, uint8_t* x_tiles, const void* ws, size_t ws_bytes,
                             qmoe_stream_t stream);

@@ -155,10 +155,12 @@ align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int
 // With slot_dest, each slot also gets its token-tile row
 // tile_start[e] * nmax + (slot - offsets[e]) (offsets and tile_start are
 // complete in global memory: written before this CTA's barrier, or by an
-// earlier kernel; read from L2).
+// earlier kernel; read from L2), and pair_dest[p] the same row of pair p
+// (-1 for an invalid id).
 __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E, int64_t p0, int32_t* cur,
                               int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pair_slot,
-                              const int32_t* offsets, const int32_t* tile_start, int nmax, int32_t* slot_dest) {
+                              const int32_t* offsets, const int32_t* tile_start, int nmax, int32_t* slot_dest,
+                              int32_t* pair_dest) {
     const int tid = threadIdx.x, warp = tid >> 5;
     for (int round = 0; round < kChunk / kThreads; ++round) {
         const int64_t r0 = p0 + round * kThreads;
@@ -183,10 +185,15 @@ __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E,
         }
         if (p < P) {
             pair_slot[p] = slot;
+            int dst = -1;
             if (valid) {
                 sorted_pair_ids[slot] = (int32_t)p;
-                if (slot_dest) slot_dest[slot] = __ldcg(tile_start + e) * nmax + slot - __ldcg(offsets + e);
+                if (slot_dest) {
+                    dst = __ldcg(tile_start + e) * nmax + slot - __ldcg(offsets + e);
+                    slot_dest[slot] = dst;
+                }
             }
+            if (pair_dest) pair_dest[p] = dst;
         }
     }
 }
@@ -200,7 +207,8 @@ __global__ void __launch_bounds__(kThreads)
 align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
                      const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_pair_ids,
                      int32_t* __restrict__ pair_slot, const int32_t* __restrict__ offsets,
-                     const int32_t* __restrict__ tile_start, int nmax, int32_t* __restrict__ slot_dest) {
+                     const int32_t* __restrict__ tile_start, int nmax, int32_t* __restrict__ slot_dest,
+                     int32_t* __restrict__ pair_dest) {
     extern __shared__ int32_t cur[];
     const int tid = threadIdx.x;
     pdl_sync();
@@ -208,7 +216,7 @@ align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchu
     for (int e = tid; e < E; e += kThreads) cur[e] = base[e];
     __syncthreads();
     scatter_chunk(ids, P, E, (int64_t)blockIdx.x * kChunk, cur, sorted_pair_ids, pair_slot, offsets, tile_start, nmax,
-                  slot_dest);
+                  slot_dest, pair_dest);
 }
 
 // One CTA for at most one chunk of pairs: histogram, scan (counts, offsets,
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(kThreads)
 align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, int32_t* __restrict__ counts,
                    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids,
                    int32_t* __restrict__ pair_slot, int32_t* __restrict__ tile_start, int32_t* __restrict__ slot_dest,
-                   int32_t* __restrict__ dev_status) {
+                   int32_t* __restrict__ pair_dest, int32_t* __restrict__ dev_status) {
     extern __shared__ int32_t cur[];  // per-expert counts, then cursors
     __shared__ int32_t ws[33];
     const int tid = threadIdx.x;
@@ -256,7 +264,7 @@ align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, 
     }
     if (tile_start) write_tile_schedule(cnt, e0, e1, E, nmax, ws, tile_start);
     __syncthreads();
-    scatter_chunk(ids, P, E, 0, cur, sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest);
+    scatter_chunk(ids, P, E, 0, cur, sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest, pair_dest);
 }
 
 size_t align_ws_bytes(int64_t P, int E) {
@@ -270,6 +278,7 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
     const int nchunks = (int)((P + kChunk - 1) / kChunk);
     const size_t smem = (size_t)E * sizeof(int32_t);
     int32_t* slot_dest = tile_start ? tile_start + schedule_ints(E) : nullptr;
+    int32_t* pair_dest = slot_dest ? slot_dest + slot_ints(P) : nullptr;
     if (smem > 48 * 1024) {
         cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -277,14 +286,14 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
     }
     if (nchunks <= 1)
         return launch_pdl(align_small_kernel, 1, kThreads, smem, stream, ids, P, E, nmax, counts, offsets,
-                          sorted_pair_ids, pair_slot, tile_start, slot_dest, dev_status);
+                          sorted_pair_ids, pair_slot, tile_start, slot_dest, pair_dest, dev_status);
     int rc = launch_pdl(align_hist_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist, dev_status);
     if (rc == QMOE_OK)
         rc = launch_pdl(align_scan_kernel, 1, kScanThreads, 0, stream, hist, P, E, nchunks, nmax, counts, offsets,
                         sorted_pair_ids, tile_start, slot_dest);
     if (rc == QMOE_OK)
         rc = launch_pdl(align_scatter_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist,
-                        sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest);
+                        sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest, pair_dest);
     return rc;
 }
 
@@ -298,8 +307,8 @@ int32_t* tile_schedule_in(void* ws, const qmoe_dims* d) {
 extern "C" size_t qmoe_workspace_bytes(const qmoe_dims* d) {
     if (!qmoe::dims_ok(d)) return 0;
     const int64_t P = (int64_t)d->T * d->k;
-    // histograms, the GEMM schedule (tile offsets over experts), each slot's token-tile row
-    return qmoe::align_ws_bytes(P, d->E) + (size_t)qmoe::schedule_ints(d->E) * 4 + (size_t)(P * 4 + 255) / 256 * 256;
+    // histograms, the GEMM schedule (tile offsets over experts), each slot's and each pair's token-tile row
+    return qmoe::align_ws_bytes(P, d->E) + (size_t)(qmoe::schedule_ints(d->E) + 2 * qmoe::slot_ints(P)) * 4;
 }
 
 extern "C" int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,

@@ -28,11 +28,13 @@ inline int launch_status() {
 inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 // The routing workspace holds, after the per-chunk histograms, the token-tile
-// schedule (E + 1 ints, padded to 256 bytes with room for 64 more) and then
-// one int per slot: the slot's row in the token tiles, tile * NMAX + row (-1
-// past the routed slots).  These are the ints from the schedule's start to
-// the per-slot rows.
+// schedule (E + 1 ints, padded to 256 bytes with room for 64 more), then one
+// int per slot: the slot's row in the token tiles, tile * NMAX + row (-1 past
+// the routed slots), then one int per pair: the pair's row (-1 for an
+// invalid expert id).  schedule_ints: ints from the schedule's start to the
+// per-slot rows; slot_ints: from the per-slot rows to the per-pair rows.
 inline int64_t schedule_ints(int E) { return ((int64_t)(E + 1 + 64) * 4 + 255) / 256 * 64; }
+inline int64_t slot_ints(int64_t P) { return (P * 4 + 255) / 256 * 64; }
 
 // ------------------------------------------------------------------ dependent launches
 //

@@ -121,8 +121,7 @@ __device__ __forceinline__ void mx_quant16(const uint4 v0, const uint4 v1, uint4
 
 // One (token, segment) item of the permute; wid < T * nseg, warp-uniform.
 __device__ __forceinline__ void permute_quant_mx_item(int64_t wid, const uint16_t* __restrict__ x,
-                                                      const int32_t* __restrict__ pair_slot,
-                                                      const int32_t* __restrict__ slot_dest, int k, int H, int nmax,
+                                                      const int32_t* __restrict__ pair_dest, int k, int H, int nmax,
                                                       uint8_t* __restrict__ tiles) {
     const int lane = threadIdx.x & 31;
     const int nseg = H / 1024 + (H % 1024 != 0);  // 1024-element segments of a row
@@ -151,8 +150,7 @@ __device__ __forceinline__ void permute_quant_mx_item(int64_t wid, const uint16_
         // lane i looks up pair j0 + i's tile and row (tile -1: invalid expert id)
         int dtile = -1, drow = 0;
         if (j0 + lane < k) {
-            const int slot = pair_slot[(int64_t)tok * k + j0 + lane];
-            const int dst = slot >= 0 ? slot_dest[slot] : -1;
+            const int dst = pair_dest[(int64_t)tok * k + j0 + lane];
             if (dst >= 0) {
                 dtile = dst / nmax;
                 drow = dst - dtile * nmax;
@@ -181,14 +179,13 @@ __device__ __forceinline__ void permute_quant_mx_item(int64_t wid, const uint16_
 // Items are strided over a grid of the CTAs that fit on the GPU at once, so
 // the last wave is not left mostly idle.
 __global__ void __launch_bounds__(kPqWarps * 32)
-permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_slot,
-                        const int32_t* __restrict__ slot_dest, int k, int H, int nmax, int T,
-                        uint8_t* __restrict__ tiles) {
+permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_dest, int k, int H,
+                        int nmax, int T, uint8_t* __restrict__ tiles) {
     pdl_sync();
     const int64_t items = (int64_t)T * (H / 1024 + (H % 1024 != 0));
     for (int64_t wid = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5); wid < items;
          wid += (int64_t)gridDim.x * kPqWarps)
-        permute_quant_mx_item(wid, x, pair_slot, slot_dest, k, H, nmax, tiles);
+        permute_quant_mx_item(wid, x, pair_dest, k, H, nmax, tiles);
 }
 
 // CTAs of `kernel` that fit on the current GPU at once (0 on error).
@@ -210,8 +207,10 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
     const int64_t fit = resident_ctas(permute_quant_mx_kernel, kPqWarps * 32);
     if (fit <= 0) return QMOE_ERR_CUDA;
     if (blocks > fit) blocks = fit;
-    return launch_pdl(permute_quant_mx_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, pair_slot,
-                      tile_start + schedule_ints(d->E), d->k, d->H, mxt::nmax_for(d), d->T, tiles);
+    // each pair's token-tile row, written by the routing sort beside the schedule
+    const int32_t* pair_dest = tile_start + schedule_ints(d->E) + slot_ints((int64_t)d->T * d->k);
+    return launch_pdl(permute_quant_mx_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, pair_dest, d->k, d->H,
+                      mxt::nmax_for(d), d->T, tiles);
 }
 
 // Permute bf16 activations into W4A16 x tiles: one warp per expert-sorted
@@ -294,8 +293,10 @@ __device__ __forceinline__ float rint_quot_clamped(float v, float s, float inv) 
 }
 
 // W8A8 activation tiles: one CTA per 112-row sub-tile (a schedule tile of
-// 224 rows is two of them), one warp per row at a time.  The row (stage 1: the
-// slot's token row of bf16 x; stage 2: the slot's own fp32 h row) is quantised
+// 224 rows is two of them), one warp per row at a time.  The row (the slot's
+// own fp32 h row for stage 2; with PERMUTE, the slot's token row of bf16 x,
+// which the launch now leaves to the token-major permute_quant_int8_kernel
+// below) is quantised
 // with the per-row int8 rule of quant_rows_int8_kernel (s = amax / 127, IEEE
 // division, nearest-even, clamped to +-127) and each code is written as the
 // fp16 value equal to it (exact) into the 128-byte-swizzled tile layout the
@@ -403,6 +404,80 @@ quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ so
     for (int i = threadIdx.x; i < KT; i += blockDim.x) l1[i] = s_l1[i];
 }
 
+// Permute + int8 quantisation of the stage-1 activations, token-major: one
+// warp per token row of bf16 x (strided over a grid of resident CTAs).  The
+// row is read and quantised once, with the rule of quant_tiles_int8_kernel,
+// and its codes (as equal fp16 values) go to the row of each of the token's k
+// routed pairs in the W8A8 tile layout, its scale to each row's tail.  Each
+// row's per-128-step sum |q| is max-ed into its 112-row half tile's entry by
+// global atomics; the launch zeroes those entries first.
+__global__ void __launch_bounds__(kPqWarps * 32)
+permute_quant_int8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_dest, int k, int K,
+                          int nmax, int T, int64_t tail_off, int64_t l1_off, uint8_t* __restrict__ tiles) {
+    pdl_sync();
+    const int lane = threadIdx.x & 31;
+    const int halves = (nmax + kTqSub - 1) / kTqSub;
+    const int KT = K / 128, NC = K / 8;  // 128-element steps, 8-code chunks
+    const int64_t bb = bft::block_bytes(nmax);
+    float* tail = reinterpret_cast<float*>(tiles + tail_off);
+    int* l1g = reinterpret_cast<int*>(tiles + l1_off);
+    for (int64_t tok = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5); tok < T;
+         tok += (int64_t)gridDim.x * kPqWarps) {
+        const uint16_t* xr = x + tok * K;
+        float amax = 0.f;
+        for (int j = lane; j < NC; j += 32) {
+            float f[8];
+            load8_as_float(xr + 8 * j, f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+        const float inv = __frcp_rn(sc);
+        for (int p0 = 0; p0 < k; p0 += 32) {
+            // lane i: the token-tile row tile * nmax + row of pair p0 + i (-1: invalid expert id)
+            const int dst = (p0 + lane < k) ? pair_dest[tok * k + p0 + lane] : -1;
+            if (dst >= 0) tail[dst] = sc;
+            const int pn = min(32, k - p0);
+            for (int j0 = 0; j0 < NC; j0 += 32) {  // warp-uniform trip count (the shuffles below)
+                const int j = j0 + lane;
+                int l1 = 0;
+                uint4 code = make_uint4(0u, 0u, 0u, 0u);
+                if (j < NC) {
+                    float f[8];
+                    load8_as_float(xr + 8 * j, f);
+                    uint32_t o[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float q0 = rint_quot_clamped(f[2 * i], sc, inv);
+                        const float q1 = rint_quot_clamped(f[2 * i + 1], sc, inv);
+                        l1 += abs((int)q0) + abs((int)q1);
+                        const __half2 hv = __floats2half2_rn(q0, q1);
+                        o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    code = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                // lanes 0-15 hold step j0/16, lanes 16-31 step j0/16 + 1
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+                const int step = (j0 >> 4) + (lane >> 4);
+                for (int q = 0; q < pn; ++q) {
+                    const int d = __shfl_sync(0xFFFFFFFFu, dst, q);
+                    if (d < 0) continue;  // warp-uniform
+                    const int tile = d / nmax, row = d - tile * nmax;
+                    if (j < NC) {
+                        uint8_t* blk = tiles + ((int64_t)tile * (K / 64) + (j >> 3)) * bb;
+                        *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) = code;
+                    }
+                    if ((lane & 15) == 0 && step < KT)
+                        atomicMax(l1g + ((int64_t)tile * halves + row / kTqSub) * KT + step, l1);
+                }
+            }
+        }
+    }
+}
+
 int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool from_bf16_tokens,
                             const int32_t* sorted, const int32_t* offsets, const int32_t* tile_start, uint8_t* tiles,
                             cudaStream_t st) {
@@ -413,10 +488,18 @@ int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool f
     const int64_t blocks = mxt::max_tiles(d, nmax) * ((nmax + kTqSub - 1) / kTqSub);
     const int64_t tail = bft::blocks_bytes(d, K);
     const int64_t l1 = tail + mxt::max_tiles(d, nmax) * nmax * 4;
-    if (from_bf16_tokens)
-        return launch_pdl(quant_tiles_int8_kernel<uint16_t, true>, (unsigned)blocks, kTqWarps * 32, 0, st,
-                          static_cast<const uint16_t*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail,
-                          l1, tiles);
+    if (from_bf16_tokens) {
+        // token-major: each token row quantised once for its k pairs
+        const size_t l1_bytes = (size_t)(blocks * (K / 128) * 4);
+        if (cudaMemsetAsync(tiles + l1, 0, l1_bytes, st) != cudaSuccess) return QMOE_ERR_LAUNCH;
+        int64_t grid = ((int64_t)d->T + kPqWarps - 1) / kPqWarps;
+        const int64_t fit = resident_ctas(permute_quant_int8_kernel, kPqWarps * 32);
+        if (fit <= 0) return QMOE_ERR_CUDA;
+        if (grid > fit) grid = fit;
+        const int32_t* pair_dest = tile_start + schedule_ints(d->E) + slot_ints(P);
+        return launch_pdl(permute_quant_int8_kernel, (unsigned)grid, kPqWarps * 32, 0, st,
+                          static_cast<const uint16_t*>(x), pair_dest, d->k, (int)K, nmax, d->T, tail, l1, tiles);
+    }
     return launch_pdl(quant_tiles_int8_kernel<float, false>, (unsigned)blocks, kTqWarps * 32, 0, st,
                       static_cast<const float*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail, l1,
                       tiles);
