@@ -9,6 +9,8 @@
 //    WMMA ... on gfx1151", Constraint: integer MMAs need quantised
 //    activations): s = amax / 127 (1 if amax = 0), q = clamp(rint(v/s), +-127),
 //    all in fp32 with IEEE division.
+#include <algorithm>
+
 #include "qmoe_common.cuh"
 #include "mx_tiles.cuh"
 
@@ -292,18 +294,14 @@ __device__ __forceinline__ float rint_quot_clamped(float v, float s, float inv) 
     return fminf(fmaxf(q, -127.f), 127.f);
 }
 
-// W8A8 activation tiles: one CTA per 112-row sub-tile (a schedule tile of
-// 224 rows is two of them), one warp per row at a time.  The row (the slot's
-// own fp32 h row for stage 2; with PERMUTE, the slot's token row of bf16 x,
-// which the launch now leaves to the token-major permute_quant_int8_kernel
-// below) is quantised
-// with the per-row int8 rule of quant_rows_int8_kernel (s = amax / 127, IEEE
-// division, nearest-even, clamped to +-127) and each code is written as the
-// fp16 value equal to it (exact) into the 128-byte-swizzled tile layout the
-// W4A16 x tiles use, 8 codes per 16-byte chunk; s goes to the per-row tail.
-// The CTA also records, for every 128-element K step, the largest L1 norm
-// sum |q| over its rows: the GEMM uses it to bound its fp32 partial sums.
-constexpr int kTqWarps = 16;
+// W8A8 activation tiles.  Each row is quantised with the per-row int8 rule of
+// quant_rows_int8_kernel (s = amax / 127, IEEE division, nearest-even,
+// clamped to +-127) and each code is written as the fp16 value equal to it
+// (exact) into the 128-byte-swizzled tile layout the W4A16 x tiles use, 8
+// codes per 16-byte chunk; s goes to the per-row tail.  For every 112-row
+// part of a tile and 128-element K step the tiles also record the largest L1
+// norm sum |q| over the part's rows: the GEMM uses it to bound its fp32
+// partial sums.
 constexpr int kTqSub = 112;
 constexpr int kTqMaxSteps = 128;  // K <= 16384
 
@@ -323,97 +321,21 @@ __device__ __forceinline__ void load8_as_float(const float* p, float (&f)[8]) {
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-template <typename In, bool PERMUTE>
-__global__ void __launch_bounds__(kTqWarps * 32)
-quant_tiles_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ sorted_pair_ids,
-                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start, int E, int k,
-                        int K, int nmax, int64_t tail_off, int64_t l1_off, uint8_t* __restrict__ tiles) {
-    pdl_sync();
-    __shared__ int s_l1[kTqMaxSteps];
-    __shared__ int s_info[2];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int halves = (nmax + kTqSub - 1) / kTqSub;
-    const int t = blockIdx.x / halves, half = blockIdx.x - t * halves;
-    const int KT = K / 128;
-    for (int i = threadIdx.x; i < KT; i += blockDim.x) s_l1[i] = 0;
-    if (threadIdx.x == 0) {
-        s_info[1] = 0;
-        if (t < tile_start[E]) {
-            int lo = 0, hi = E;  // the expert whose tiles contain t
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (tile_start[mid] <= t) lo = mid; else hi = mid;
-            }
-            const int m0 = offsets[lo] + (t - tile_start[lo]) * nmax + half * kTqSub;
-            s_info[0] = m0;
-            // rows of this half that exist in the tile (a 16-row tile has one short half)
-            s_info[1] = max(0, min(min(kTqSub, nmax - half * kTqSub), offsets[lo + 1] - m0));
-        }
-    }
-    __syncthreads();
-    const int m0 = s_info[0], n = s_info[1];
-    if (n == 0) return;
-    const int64_t bb = bft::block_bytes(nmax);
-    uint8_t* tbase = tiles + (int64_t)t * (K / 64) * bb;
-    for (int r = warp; r < n; r += kTqWarps) {
-        const int64_t slot = m0 + r;
-        const int row = half * kTqSub + r;  // row within the schedule tile
-        const int64_t src = PERMUTE ? (int64_t)(sorted_pair_ids[slot] / k) : slot;
-        const In* xr = x + src * K;
-        float amax = 0.f;
-        for (int j = lane; j < K / 8; j += 32) {
-            float f[8];
-            load8_as_float(xr + 8 * j, f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, 127.0f);
-        const float inv = __frcp_rn(sc);
-        // chunk j (8 codes): K step j/8 of 64 (block), chunk j%8 of its 128-byte row; 128-element step j/16
-        for (int j0 = 0; j0 < K / 8; j0 += 32) {  // warp-uniform trip count (the shuffles below)
-            const int j = j0 + lane;
-            int l1 = 0;
-            if (j < K / 8) {
-                float f[8];
-                load8_as_float(xr + 8 * j, f);
-                uint32_t o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float q0 = rint_quot_clamped(f[2 * i], sc, inv);
-                    const float q1 = rint_quot_clamped(f[2 * i + 1], sc, inv);
-                    l1 += abs((int)q0) + abs((int)q1);
-                    const __half2 hv = __floats2half2_rn(q0, q1);
-                    o[i] = *reinterpret_cast<const uint32_t*>(&hv);
-                }
-                uint8_t* blk = tbase + (int64_t)(j >> 3) * bb;
-                *reinterpret_cast<uint4*>(blk + row * 128 + (((j & 7) ^ (row & 7)) << 4)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            // lanes 0-15 hold step j0/16, lanes 16-31 step j0/16 + 1
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
-            const int step = (j0 >> 4) + (lane >> 4);
-            if ((lane & 15) == 0 && step < KT) atomicMax(&s_l1[step], l1);
-        }
-        if (lane == 0) reinterpret_cast<float*>(tiles + tail_off)[(int64_t)t * nmax + row] = sc;
-    }
-    __syncthreads();
-    int* l1 = reinterpret_cast<int*>(tiles + l1_off) + ((int64_t)t * halves + half) * KT;
-    for (int i = threadIdx.x; i < KT; i += blockDim.x) l1[i] = s_l1[i];
-}
-
-// Permute + int8 quantisation of the stage-1 activations, token-major: one
-// warp per token row of bf16 x (strided over a grid of resident CTAs).  The
-// row is read and quantised once, with the rule of quant_tiles_int8_kernel,
-// and its codes (as equal fp16 values) go to the row of each of the token's k
-// routed pairs in the W8A8 tile layout, its scale to each row's tail.  Each
-// row's per-128-step sum |q| is max-ed into its 112-row half tile's entry by
-// global atomics; the launch zeroes those entries first.
+// int8 quantisation into W8A8 tiles, one warp per source row (strided over a
+// grid of resident CTAs).  The row is read and quantised once, with the rule
+// above, and its codes (as equal fp16 values) go to k
+// token-tile rows dest[row * k + j] (-1: none) in the W8A8 tile layout, its
+// scale to each row's tail.  Each row's per-128-step sum |q| is max-ed into
+// its 112-row half tile's entry by global atomics; the launch zeroes those
+// entries first.
+//   stage 1: rows = the T token rows of bf16 x, dest = each pair's row (the
+//            routing sort's per-pair rows), k = top-k: a token row is
+//            quantised once for its k pairs;
+//   stage 2: rows = the P slot rows of fp32 h, dest = each slot's row, k = 1.
+template <typename In>
 __global__ void __launch_bounds__(kPqWarps * 32)
-permute_quant_int8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_dest, int k, int K,
-                          int nmax, int T, int64_t tail_off, int64_t l1_off, uint8_t* __restrict__ tiles) {
+permute_quant_int8_kernel(const In* __restrict__ x, const int32_t* __restrict__ pair_dest, int k, int K,
+                          int nmax, int64_t T, int64_t tail_off, int64_t l1_off, uint8_t* __restrict__ tiles) {
     pdl_sync();
     const int lane = threadIdx.x & 31;
     const int halves = (nmax + kTqSub - 1) / kTqSub;
@@ -423,7 +345,11 @@ permute_quant_int8_kernel(const uint16_t* __restrict__ x, const int32_t* __restr
     int* l1g = reinterpret_cast<int*>(tiles + l1_off);
     for (int64_t tok = (int64_t)blockIdx.x * kPqWarps + (threadIdx.x >> 5); tok < T;
          tok += (int64_t)gridDim.x * kPqWarps) {
-        const uint16_t* xr = x + tok * K;
+        // destinations of the first 32 pairs; a row with none (invalid ids, or a slot past the routed
+        // ones) is not read
+        const int dst0 = (lane < k) ? pair_dest[tok * k + lane] : -1;
+        if (k <= 32 && __ballot_sync(0xFFFFFFFFu, dst0 >= 0) == 0) continue;
+        const In* xr = x + tok * K;
         float amax = 0.f;
         for (int j = lane; j < NC; j += 32) {
             float f[8];
@@ -437,7 +363,7 @@ permute_quant_int8_kernel(const uint16_t* __restrict__ x, const int32_t* __restr
         const float inv = __frcp_rn(sc);
         for (int p0 = 0; p0 < k; p0 += 32) {
             // lane i: the token-tile row tile * nmax + row of pair p0 + i (-1: invalid expert id)
-            const int dst = (p0 + lane < k) ? pair_dest[tok * k + p0 + lane] : -1;
+            const int dst = p0 == 0 ? dst0 : ((p0 + lane < k) ? pair_dest[tok * k + p0 + lane] : -1);
             if (dst >= 0) tail[dst] = sc;
             const int pn = min(32, k - p0);
             for (int j0 = 0; j0 < NC; j0 += 32) {  // warp-uniform trip count (the shuffles below)
@@ -488,21 +414,21 @@ int quant_tiles_int8_launch(const qmoe_dims* d, int64_t K, const void* x, bool f
     const int64_t blocks = mxt::max_tiles(d, nmax) * ((nmax + kTqSub - 1) / kTqSub);
     const int64_t tail = bft::blocks_bytes(d, K);
     const int64_t l1 = tail + mxt::max_tiles(d, nmax) * nmax * 4;
-    if (from_bf16_tokens) {
-        // token-major: each token row quantised once for its k pairs
-        const size_t l1_bytes = (size_t)(blocks * (K / 128) * 4);
-        if (cudaMemsetAsync(tiles + l1, 0, l1_bytes, st) != cudaSuccess) return QMOE_ERR_LAUNCH;
-        int64_t grid = ((int64_t)d->T + kPqWarps - 1) / kPqWarps;
-        const int64_t fit = resident_ctas(permute_quant_int8_kernel, kPqWarps * 32);
-        if (fit <= 0) return QMOE_ERR_CUDA;
-        if (grid > fit) grid = fit;
-        const int32_t* pair_dest = tile_start + schedule_ints(d->E) + slot_ints(P);
-        return launch_pdl(permute_quant_int8_kernel, (unsigned)grid, kPqWarps * 32, 0, st,
-                          static_cast<const uint16_t*>(x), pair_dest, d->k, (int)K, nmax, d->T, tail, l1, tiles);
-    }
-    return launch_pdl(quant_tiles_int8_kernel<float, false>, (unsigned)blocks, kTqWarps * 32, 0, st,
-                      static_cast<const float*>(x), sorted, offsets, tile_start, d->E, d->k, (int)K, nmax, tail, l1,
-                      tiles);
+    // one warp per source row: token rows (each quantised once for its k pairs), or slot rows of h
+    const size_t l1_bytes = (size_t)(blocks * (K / 128) * 4);
+    if (cudaMemsetAsync(tiles + l1, 0, l1_bytes, st) != cudaSuccess) return QMOE_ERR_LAUNCH;
+    const int32_t* slot_dest = tile_start + schedule_ints(d->E);
+    const int64_t rows = from_bf16_tokens ? (int64_t)d->T : P;
+    const int64_t fit = from_bf16_tokens ? resident_ctas(permute_quant_int8_kernel<uint16_t>, kPqWarps * 32)
+                                         : resident_ctas(permute_quant_int8_kernel<float>, kPqWarps * 32);
+    if (fit <= 0) return QMOE_ERR_CUDA;
+    const int64_t grid = std::min<int64_t>((rows + kPqWarps - 1) / kPqWarps, fit);
+    if (from_bf16_tokens)
+        return launch_pdl(permute_quant_int8_kernel<uint16_t>, (unsigned)grid, kPqWarps * 32, 0, st,
+                          static_cast<const uint16_t*>(x), slot_dest + slot_ints(P), d->k, (int)K, nmax, rows, tail,
+                          l1, tiles);
+    return launch_pdl(permute_quant_int8_kernel<float>, (unsigned)grid, kPqWarps * 32, 0, st,
+                      static_cast<const float*>(x), slot_dest, 1, (int)K, nmax, rows, tail, l1, tiles);
 }
 
 // W4A16 h tiles (bf16, with per-32-column group maxima) -> fp16 tiles for
