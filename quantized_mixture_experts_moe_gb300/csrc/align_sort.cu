@@ -16,8 +16,8 @@
 //               is its chunk base + the running count of earlier equal ids,
 //               so the result is the stable counting sort.
 // The scan also derives the GEMMs' token-tile schedule, and the scatter
-// gives every slot its row in the token tiles (so the permute kernels look
-// it up instead of searching the offsets).
+// gives every slot and every pair its row in the token tiles (so the permute
+// and intermediate kernels look it up instead of searching the offsets).
 #include "qmoe_common.cuh"
 #include "mx_tiles.cuh"
 
