@@ -57,6 +57,8 @@ def test_workspace_bytes_host_only(lib):
     d = qb.dims(4096, 10, 4096, 1024, 512)
     n = qb.workspace_bytes(d)
     assert n >= 4 * 512 * ((40960 + 2047) // 2048)
+    # plus the tile schedule (E + 1 ints) and one token-tile row per slot and per pair
+    assert n >= 4 * 512 * ((40960 + 2047) // 2048) + 4 * 513 + 2 * 4 * 40960
     assert qb.forward_workspace_bytes(d, "mxfp4") > 40960 * 4096 * 4  # holds y
     bad = qb.dims(16, 2, 250, 128, 8)  # H not a multiple of 32
     assert qb.workspace_bytes(bad) == 0
@@ -115,6 +117,13 @@ def test_w8a8_host_checks(lib):
     for bad in (qb.dims(16, 2, 384, 128, 8), qb.dims(16, 2, 256, 192, 8), qb.dims(16, 2, 256, 16512, 8)):
         assert lib.qmoe_gemm1_swiglu_w8a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2
         assert lib.qmoe_gemm2_w8a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2
+    # W4A8 (int4 weights, the same activation tiles): the same host checks
+    assert lib.qmoe_gemm1_swiglu_w4a8(ctypes.byref(d), ok, null, ok, ok, ok, null, ok, ok, big, null) == -1
+    assert lib.qmoe_gemm2_w4a8(ctypes.byref(d), ok, ok, ok, ok, null, null, ok, ok, big, null) == -1
+    assert lib.qmoe_gemm2_w4a8(ctypes.byref(d), ok, ok, ok, ok, ok, odd, ok, ok, big, null) == -1
+    for bad in (qb.dims(16, 2, 384, 128, 8), qb.dims(16, 2, 256, 192, 8)):
+        assert lib.qmoe_gemm1_swiglu_w4a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2
+        assert lib.qmoe_gemm2_w4a8(ctypes.byref(bad), ok, ok, ok, ok, ok, null, ok, ok, big, null) == -2
 
 
 def test_tile_rules_host_only(lib):
