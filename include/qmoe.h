@@ -123,8 +123,9 @@ int qmoe_tile_nmax(const qmoe_dims* d);
 size_t qmoe_workspace_bytes(const qmoe_dims* d);
 
 /* qmoe_align_sort -- expert-sorted permutation of the routed pairs.
- * [hip-ep] description ("grouped" launches with a "deterministic scatter
- * order"); [aiter] Changes (two-stage grouped kernel over sorted tokens).
+ * [hip-ep] description (all experts grouped into one launch, the scatter
+ * back kept in a deterministic order); [aiter] Changes (two-stage grouped
+ * kernel over sorted tokens).
  *
  * in   topk_ids        int32 [T, k], expert id of pair p = t*k + j
  * out  counts          int32 [E], pairs routed to each expert

@@ -2,8 +2,8 @@
 //
 // out[t][c] = bf16( sum_{j=0..k-1} w[t][j] * y[slot(t, j)][c] ), summed in fp32
 // with j ascending from 0: the fixed order makes the result bit-reproducible
-// ("perf(qmoe): group prefill expert matmuls", description: "preserving
-// deterministic scatter order").  y rows are bf16.  Each thread owns 8
+// ("perf(qmoe): group prefill expert matmuls", description: the scatter back
+// keeps a deterministic order).  y rows are bf16.  Each thread owns 8
 // consecutive columns of one token (16-byte loads of every y row, 16-byte
 // bf16 stores).
 #include "qmoe_common.cuh"

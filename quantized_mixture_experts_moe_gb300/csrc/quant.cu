@@ -2,7 +2,7 @@
 //
 //  * MX (E4M3 codes + one E8M0 scale per 32 columns) for the fp8 activations
 //    that feed the MXFP4 expert GEMMs (aiter tuned grouped-fmoe page,
-//    Changes: "fp8 act, MXFP4 weight").  Rule (OCP MX v1.0): per block,
+//    Changes: fp8 activations with MXFP4 weights).  Rule (OCP MX v1.0): per block,
 //    X = 2^(floor(log2 amax) - 8), code = nearest-even E4M3 of v / X,
 //    saturated to +-448; amax = 0 -> scale byte 127, zero codes.
 //  * Per-row symmetric int8 for the W8A8 scheme ("Evaluate native IU4/IU8
