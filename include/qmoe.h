@@ -162,8 +162,13 @@ int qmoe_align_sort(const qmoe_dims* d, const int32_t* topk_ids, int32_t* counts
  * workspace for them.
  *
  * The first call on a device looks up the array's device address on the
- * current device (once per device); make that first call before any stream
- * capture.  Every call on a device shares the one array and it keeps the last
+ * current device (kept once it succeeds; a failed lookup returns
+ * QMOE_ERR_CUDA and is tried again on the next call).  With lazy module
+ * loading (the CUDA default) that lookup is also what loads the library's
+ * device code onto the GPU and places the array there, so the first call is
+ * not itself free of allocation: make it once per device at start-up, before
+ * any region that must not allocate and before any stream capture.  Later
+ * calls allocate nothing.  Every call on a device shares the one array and it keeps the last
  * call's contents; nothing in it needs to start at zero (each call rewrites
  * all it reads).  Calls whose executions overlap on the GPU (different
  * streams, or different host threads) race on the array: serialise them. */

@@ -27,27 +27,29 @@ static __device__ __align__(256) int32_t g_align_scratch[QMOE_STATIC_SCRATCH_BYT
 namespace {
 
 constexpr int kMaxDevices = 64;
-int32_t* g_scratch_ptr[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+int32_t* g_scratch_ptr[kMaxDevices];  // written once per device, under g_scratch_mu, after a successful lookup
+std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device.  The host-side
 // name g_align_scratch is only a stand-in for the symbol, never a device
-// address, so it is resolved once per device with that device current.
+// address, so it is resolved per device with that device current.  Only a
+// successful lookup is kept: a failed one (say, a transient error while the
+// module loads) is tried again on the next call.
 int32_t* scratch_on_current_device(int* status) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         *status = QMOE_ERR_CUDA;
         return nullptr;
     }
-    std::call_once(g_scratch_once[dev], [dev] {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
         void* p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_align_scratch);
+        if (cudaGetSymbolAddress(&p, g_align_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();  // clear the lookup error so a later launch check does not report it
+            *status = QMOE_ERR_CUDA;
+            return nullptr;
+        }
         g_scratch_ptr[dev] = static_cast<int32_t*>(p);
-    });
-    if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev]) {
-        *status = QMOE_ERR_CUDA;
-        return nullptr;
     }
     *status = QMOE_OK;
     return g_scratch_ptr[dev];

@@ -30,6 +30,10 @@ REL_L2 = 5e-3
 # a CPU model of this arithmetic puts at rel L2 ~1.0e-3 against the oracle's
 # rounded h.  Bound: 2e-3.
 W4_H_REL_L2 = 2e-3
+# one stage's bf16 y against the double oracle: the bf16 rounding of y is
+# ~1.1e-3 rel L2 by itself; 2e-3 leaves room for the fp32 sums and the fp16
+# weight rounding (W4A16) without hiding a stage-2 defect twice that size
+Y_BF16_REL_L2 = 2e-3
 
 
 def rel_l2(got, ref):
@@ -244,7 +248,9 @@ def test_stage2_against_oracle(w):
         ref = oracle.stage2("w4a16", w.H, w.I, w.E, experts, s2["h"], None, wts["w2"], wts["w2_s"])
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        assert rel_l2(yv(), ref) < 5e-3
+        # y is stored as bf16: that rounding alone is ~1.1e-3 rel L2; the single
+        # fp16 rounding of each dequantised weight adds ~2e-4 in quadrature
+        assert rel_l2(yv(), ref) < Y_BF16_REL_L2
     elif w.scheme == "mxfp4":
         # the routing sort fills the workspace's tile schedule for these expert loads
         ids = experts.reshape(rows, 1)
@@ -259,7 +265,16 @@ def test_stage2_against_oracle(w):
         qb.qmoe_gemm2_mxfp4(d, gp.dev(ht), w2w, w2p, off_t, y, st, ws)
         ref = oracle.stage2("mxfp4", w.H, w.I, w.E, experts, s2["h"], s2["h_s"], wts["w2"], wts["w2_s"])
         torch.cuda.synchronize()
-        assert rel_l2(yv(), ref) < 5e-3
+        # every E2M1 x E4M3 product and its scales are exact in fp32, so the
+        # kernel's fp32 sum sits ~1e-7 from the double one; rounded to bf16 the
+        # two agree except where a sum straddles a rounding boundary, and then
+        # by one bf16 step
+        got = yv()
+        ref_b = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).double().numpy()
+        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref_b), 1e-30))) - 7)
+        assert (np.abs(got - ref_b) <= ulp).all()
+        assert np.mean(got != ref_b) < 1e-3
+        assert rel_l2(got, ref) < Y_BF16_REL_L2
     else:
         ids = experts.reshape(rows, 1)
         counts_t, off_t = gp.empty(w.E, torch.int32), gp.empty(w.E + 1, torch.int32)
@@ -408,6 +423,26 @@ def test_layer_small(w):
     ref = oracle.moe_forward(w.scheme, dims(w), d)
     assert g["status"] == 0
     assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
+
+
+@pytest.mark.parametrize("scheme", ["mxfp4", "w8a8"])
+@pytest.mark.parametrize("k", [33, 40])
+def test_layer_topk_above_32(scheme, k):
+    # the token-major permutes walk a token's pairs 32 at a time and the combine
+    # 8 at a time: k = 33 and 40 run both loops past their first chunk, with a
+    # ragged last chunk ([hip-ep] description: fixed-order scatter back)
+    w = gen.custom(f"topk{k}_{scheme}", scheme, 24, 512, 48, k, 128, seed=90 + k)
+    d = gen.make_all(w)
+    g = gp.run_layer(w, d)
+    ref = oracle.moe_forward(w.scheme, dims(w), d)
+    assert g["status"] == 0
+    assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
+    wt = gp.device_weights(w, d)
+    out, status = qb.moe_forward(scheme, gp.dev(d["x"]), gp.dev(d["topk_ids"]), gp.dev(d["topk_w"]),
+                                 wt["w1"], wt["w1_s"], wt["w2"], wt["w2_s"], I=w.I, E=w.E)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(gp.host(out, np.uint16), g["out"])
 
 
 @pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8", "w4a8"])

@@ -31,6 +31,10 @@ MUTATIONS = [
     ("w4a8 nibble order", "uint8_t code = (uint8_t)((wr[kk / 2] >> (4 * (kk % 2))) & 15);",
      "uint8_t code = (uint8_t)((wr[kk / 2] >> (4 - 4 * (kk % 2))) & 15);"),
     ("w4a8 gate/up swapped", "int_row(scheme, w1, 2 * I, H, e, I + n, wu);", "int_row(scheme, w1, 2 * I, H, e, n, wu);"),
+    ("combine weight dropped",
+     "for (int c = 0; c < H; ++c) out[t * H + c] += w * (double)y[(int64_t)s * H + c];",
+     "for (int c = 0; c < H; ++c) out[t * H + c] += (double)y[(int64_t)s * H + c];"),
+    ("combine unrouted pair read", "if (s < 0) continue;", "if (s < 0) s = 0;"),
     ("int8 rounding", "float t = rintf(vr[i] / sc);", "float t = truncf(vr[i] / sc);"),
     ("stable order", "int32_t s = cursor[e]++;", "int32_t s = offsets[e + 1] - 1 - (cursor[e]++ - offsets[e]);"),
     ("scale block index", "sc = oracle_e8m0_to_double(((const uint8_t*)ws)[sbase + kk / 32]);",

@@ -357,3 +357,55 @@ def test_activation_quant_mx_exact_from_bf16():
     x = bf.bf16_bits_to_f64(d["x"])
     deq = np.vectorize(oracle.e4m3_to_double)(q) * np.repeat(np.exp2(s.astype(np.float64) - 127), 32, axis=1)
     assert np.array_equal(deq, bf.mx_values(x.astype(np.float32)))
+
+
+def test_combine_hand_computed():
+    # two tokens, top-2, two columns; pair 3 is unrouted (slot -1).  Rows of y
+    # are in slot order.  [hip-ep] description: the scatter back is a fixed-order
+    # weighted sum over the token's routed pairs.
+    y = np.array([[1.0, -2.0], [0.5, 4.0], [3.0, 0.25]], np.float32)
+    topk_w = np.array([[0.25, 0.75], [2.0, -1.0]], np.float32)
+    pair_slot = np.array([2, 0, 1, -1], np.int32)
+    # token 0: 0.25*(3, 0.25) + 0.75*(1, -2) = (1.5, -1.4375)
+    # token 1: 2*(0.5, 4); its second pair is skipped
+    out = oracle.combine(y, topk_w, pair_slot)
+    assert out.tolist() == [[1.5, -1.4375], [1.0, 8.0]]
+
+
+def test_combine_matches_einsum_over_gathered_rows():
+    rng = np.random.default_rng(23)
+    T, k, H = 37, 5, 48
+    P = T * k
+    y = rng.standard_normal((P + 3, H)).astype(np.float32)  # three spare rows nothing points at
+    topk_w = rng.uniform(0.05, 1.0, (T, k)).astype(np.float32)
+    pair_slot = rng.permutation(P + 3)[:P].astype(np.int32)
+    pair_slot[[4, 17, 100]] = -1
+    got = oracle.combine(y, topk_w, pair_slot)
+    rows = y.astype(np.float64)[np.maximum(pair_slot, 0)].reshape(T, k, H)
+    mask = (pair_slot >= 0).reshape(T, k).astype(np.float64)
+    ref = np.einsum("tj,tjh->th", topk_w.astype(np.float64) * mask, rows)
+    assert np.allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("scheme", ["w4a16", "mxfp4", "w8a8"])
+def test_combine_of_forward_rows_gives_forward_output(scheme):
+    # the forward's own per-pair y rows (pair order, so pair_slot is the
+    # identity), rounded to fp32, recombine to its output within that rounding;
+    # an unrouted pair removes exactly its weighted row
+    w, d = _tiny(scheme, seed=29)
+    dims = (w.T, w.k, w.H, w.I, w.E)
+    out, dbg, _ = oracle.moe_forward(scheme, dims, d, debug=True)
+    y32 = dbg["y"].astype(np.float32)
+    P = w.T * w.k
+    ident = np.arange(P, dtype=np.int32)
+    got = oracle.combine(y32, d["topk_w"], ident)
+    bound = (np.abs(d["topk_w"].astype(np.float64))[:, :, None] *
+             np.abs(dbg["y"]).reshape(w.T, w.k, w.H)).sum(1) * 2.0 ** -23 + 1e-300
+    assert (np.abs(got - out) <= bound).all()
+    cut = ident.copy()
+    cut[2 * w.k + 1] = -1
+    got2 = oracle.combine(y32, d["topk_w"], cut)
+    removed = float(d["topk_w"][2, 1]) * y32[2 * w.k + 1].astype(np.float64)
+    assert np.allclose(got[2] - got2[2], removed, rtol=1e-12, atol=1e-12 * np.abs(removed).max())
+    others = np.arange(w.T) != 2
+    assert np.array_equal(got[others], got2[others])
