@@ -111,7 +111,7 @@ struct Cfg {
     static constexpr int NBAR = 2 * RS + 2 * BS + AS + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SCHED_OFF = MISC_OFF + 64;
-    static constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
+    static constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + 2 * (size_t)(E + 1) * 4 + 1024; }
     static_assert(R_COL + 2 * NS <= A_COL && A_COL + AS * A_SLOT_COLS <= 512 && NS % 16 == 0, "TMEM budget");
     static_assert(BS >= AS + 1, "a step's done barrier is not reused before the converter has waited on it");
     static_assert(B_OFF % 1024 == 0 && HALF_B % 1024 == 0, "swizzled activation tiles 1024-aligned");
@@ -139,27 +139,60 @@ struct Args {
 };
 
 // Unit u -> (expert e, schedule tile t, half of it, column block nb) and the
-// unit's first slot m0 and token count (<= 0 for an empty second half).
+// unit's first slot m0 and token count (always > 0).  Units enumerate only
+// the non-empty token halves: sub_start is the prefix over experts of their
+// sub-unit counts (full tiles x halves, plus the halves the last tile fills),
+// and an expert's sub-units j run over (tile j / halves, half j % halves).  So
+// a static round-robin over units hands every CTA the same number of real
+// units; with the empty halves in the enumeration some CTAs drew one or two
+// more than others.
 template <int NS>
-__device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax, const int* tile_start, int E,
-                                            const int32_t* offsets, int& e, int& t, int& half, int& nb, int& m0,
-                                            int& ntok, bool l2) {
+__device__ __forceinline__ void decode_unit(int u, int NB, int halves, int nmax, const int* tile_start,
+                                            const int* sub_start, int E, const int32_t* offsets, int& e, int& t,
+                                            int& half, int& nb, int& m0, int& ntok, bool l2) {
     const int th = u / NB;
     nb = u - th * NB;
-    t = th / halves;
-    half = th - t * halves;
     int lo = 0, hi = E;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (tile_start[mid] <= t) lo = mid; else hi = mid;
+        if (sub_start[mid] <= th) lo = mid; else hi = mid;
     }
     e = lo;
+    const int j = th - sub_start[e];
+    const int jt = j / halves;
+    half = j - jt * halves;
+    t = tile_start[e] + jt;
     // l2: a role that runs before this kernel's dependent-launch wait reads
     // the routing sort's offsets from L2 (the sort completed before the launch)
     const int o0 = l2 ? __ldcg(offsets + e) : offsets[e];
     const int o1 = l2 ? __ldcg(offsets + e + 1) : offsets[e + 1];
-    m0 = o0 + (t - tile_start[e]) * nmax + half * NS;
+    m0 = o0 + jt * nmax + half * NS;
     ntok = min(min(NS, nmax - half * NS), o1 - m0);
+}
+
+// sub_start[0..E]: prefix over experts of ceil-split sub-units (one warp; the
+// offsets are complete: read through L2 as the schedule is).
+template <int NS>
+__device__ __forceinline__ void build_sub_start(const int32_t* offsets, int E, int nmax, int halves, int* sub_start,
+                                                int lane) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int c = 0;
+        if (e < E) {
+            const int cnt = __ldcg(offsets + e + 1) - __ldcg(offsets + e);
+            const int full = cnt / nmax, rem = cnt - full * nmax;
+            c = full * halves + (rem + NS - 1) / NS;
+        }
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, c, s);
+            if (lane >= s) c += v;
+        }
+        if (e < E) sub_start[e + 1] = carry + c;
+        carry += __shfl_sync(0xFFFFFFFFu, c, 31);
+    }
+    if (lane == 0) sub_start[0] = 0;
 }
 
 __device__ __forceinline__ void set_abort(volatile int* flag, int32_t* status) {
@@ -277,6 +310,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
     int* tile_start = reinterpret_cast<int*>(smem + C::SCHED_OFF);
+    int* sub_start = tile_start + (a.E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E;
@@ -292,6 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
     // warps that read the predecessor's output wait.
     if (!a.weights_early) pdl_wait();
     for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = __ldcg(a.tile_start + i);
+    if (warp == WARP_CVT0) build_sub_start<C::NS>(a.offsets, E, a.nmax, halves, sub_start, lane);
     if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::RS; ++s) {
             tc::mbar_init(&raw_full[s], 1);
@@ -308,7 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         tc::fence_barrier_init();
     }
     __syncthreads();
-    const int total_units = tile_start[E] * halves * NB;
+    const int total_units = sub_start[E] * NB;
     if ((int)blockIdx.x >= total_units) {
         pdl_wait();  // the grid still completes only after its predecessor
         return;
@@ -331,7 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             uint32_t ph = 0;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, t, half, nb, m0, ntok;
-                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, a.weights_early != 0);
+                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, sub_start, E, a.offsets, e, t, half, nb, m0, ntok, a.weights_early != 0);
                 if (ntok <= 0) continue;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
@@ -386,7 +421,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
             const int64_t bb = (int64_t)a.nmax * 128;
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, t, half, nb, m0, ntok;
-                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
+                decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, sub_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
                 if (ntok <= 0) continue;
                 const uint32_t bytes = (uint32_t)((ntok + 15) & ~15) * 128u;
                 bool ok = true;
@@ -412,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         bool pending = false;  // an accumulator event not yet handed back by the epilogue
         for (int u = blockIdx.x; u < total_units && !warp_flag(abort_flag); u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, sub_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
             if (ntok <= 0) continue;
             const int nmma = (ntok + 15) & ~15;
             const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
@@ -461,7 +496,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, a.weights_early != 0);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, sub_start, E, a.offsets, e, t, half, nb, m0, ntok, a.weights_early != 0);
             if (ntok <= 0) continue;
             for (int kt = 0; kt < KT; ++kt, ++gs) {
                 if (!warp_wait(&raw_full[rs], rph, lane)) {
@@ -554,7 +589,7 @@ __global__ void __launch_bounds__(THREADS, 1) int_gemm_kernel(const __grid_const
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
             int e, t, half, nb, m0, ntok;
-            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
+            decode_unit<C::NS>(u, NB, halves, a.nmax, tile_start, sub_start, E, a.offsets, e, t, half, nb, m0, ntok, false);
             if (ntok <= 0) continue;
             const float* ts = a.act_scale + (int64_t)t * a.nmax + half * C::NS;
             float ws0, ws1;  // channel scales of this thread's row in the two tiles
