@@ -224,17 +224,26 @@ __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t
     asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
 }
 
-// Eight int4 codes (one reordered word) times an f16x2 scale -> four f16x2
-// pairs in K order.  0x6400 | n is the fp16 value 1024 + n; subtracting 1032
-// gives n - 8 exactly; the product is the one rounding.
+// Eight int4 codes (one reordered word: pair j = nibbles j and j + 4) times
+// an f16x2 scale -> four f16x2 pairs in K order, with one shift per word.
+// Masking nibbles 0/4 (or, after the shift by 8, 2/6) into 0x6400 gives the
+// fp16 values 1024 + n, from which subtracting 1032 leaves n - 8; masking
+// nibbles 1/5 (3/7) in place gives 1024 + 16 n, and (1024 + 16 n) / 16 - 72
+// is n - 8 in one exact fma.  The product with the scale is the one rounding.
 __device__ __forceinline__ void dequant8(uint32_t w, uint32_t s2, uint32_t* out) {
     const uint32_t magic = 0x64006400u, bias = 0x64086408u;
+    const uint32_t sixteenth = 0x2C002C00u, m72 = 0xD480D480u;  // 1/16, -72
+    const uint32_t w8 = w >> 8;
+    uint32_t v[4] = {(w & 0x000F000Fu) | magic, (w & 0x00F000F0u) | magic, (w8 & 0x000F000Fu) | magic,
+                     (w8 & 0x00F000F0u) | magic};
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(v[0]) : "r"(bias));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(v[1]) : "r"(sixteenth), "r"(m72));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(v[2]) : "r"(bias));
+    asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(v[3]) : "r"(sixteenth), "r"(m72));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | magic;
-        asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(v) : "r"(bias));
-        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(v) : "r"(s2));
-        out[j] = v;
+        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(v[j]) : "r"(s2));
+        out[j] = v[j];
     }
 }
 

@@ -79,8 +79,8 @@ __host__ __device__ inline uint32_t elem_offset(int r, int col) {
 // of codes, then 128 rows x 2 fp16 scales (the two 32-element blocks of the
 // step) multiplied by the row's power of two 2^p_r.  Inside each 32-bit code
 // word the eight nibbles are reordered so the low half holds elements 0, 2,
-// 4, 6 and the high half 1, 3, 5, 7: masking with 0x000F000F after a shift
-// by 4j yields elements (2j, 2j+1) as a pair.  After all blocks, one fp32
+// 4, 6 and the high half 1, 3, 5, 7: nibbles j and j + 4 are the pair
+// (2j, 2j+1), which one mask lifts into the two halves of an f16x2.  After all blocks, one fp32
 // 2^-p_r per row (ceil(rows/128)*128 of them).
 constexpr int kW4Block = 4608;
 __host__ __device__ inline int64_t w4_blocks_bytes(int64_t rows, int64_t K) {

@@ -48,11 +48,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete, giving up after
 // `limit_cycles` SM clocks.  Returns false on timeout (the caller records it
 // and winds down); never spins forever.
+// The clock is read once per 16 polls: a waiting warp shares its scheduler
+// with warps doing real work, and a poll loop that also reads and compares
+// the clock each time spends most of its instructions on the timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_cycles = 4000000000ll) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > limit_cycles) return false;
     }
 }
