@@ -34,13 +34,22 @@ METRIC = "grouped-MoE prefill TFLOP/s & tokens/s at T=4096; % of tensor/HBM roof
 UNIT = "TFLOP/s"
 L2_BYTES = 129 * 10**6  # GB300 L2
 
-# ncu DRAM bytes (read + write) of one stage-1 GEMM launch divided by its
-# algorithmic bytes, per scheme, for the kernel as it stands; None once the
-# kernel changes after the capture
+# DRAM bytes (read + write) of one stage-1 GEMM launch from an ncu capture,
+# divided by that launch's algorithmic bytes.  Keyed by workload where the
+# capture ran on the workload itself, else by scheme (a capture on a smaller
+# workload with the same tokens per expert, whose traffic scales with the
+# units processed).  An entry is removed when its kernel changes.
 TRAFFIC_RATIO_GEMM1 = {
-    "mxfp4": (309.287424 + 6.629376) / 292.782080,  # profiles/mx_gemm_kernel_prof_mxfp4_E64_T512.md
-    "w8a8": (160.009216 + 28.690944) / 108.130304,   # profiles/int_gemm_kernel_w8a8.md
-    "w4a8": (113.458432 + 23.438336) / 61.992960,    # profiles/int_gemm_kernel_w4a8.md
+    # MXFP4, 512 tokens over 64 experts (~80 per expert, as at T=4096 over 512), 112-row tiles
+    "mxfp4": (309258496 + 6330624) / 287375360,
+    # MXFP4 decode, 16-row tiles, on the workloads themselves
+    "decode_T1": (45416448 + 161024) / 44568704,
+    "decode_T4": (127116032 + 2582016) / 124797440,
+    # W4A16 on the workload itself (T=2048)
+    "w4a16": (298661120 + 18805248) / 234881024,
+    # W8A8 and W4A8, 1024 tokens over 8 experts (~1024 per expert, as at T=8192 over 64)
+    "w8a8": (160118016 + 29393152) / 96563200,
+    "w4a8": (113460992 + 22359552) / 50425856,
 }
 
 
@@ -107,17 +116,21 @@ def touched_experts(ids, E):
 
 
 def algorithmic(w, ids):
-    """Per-launch algorithmic bytes and flops of the two grouped GEMMs:
-    weights (with scales) of the experts the batch touches, activations read
-    once per pair, intermediate written/read once, y written once."""
+    """Per-launch algorithmic bytes and flops of the two grouped GEMMs.
+    Algorithmic bytes count what the method itself must move: the weights
+    (with scales) of the experts the batch touches, plus the activations x
+    read once (stage 1).  What the implementation moves on top (the
+    expert-sorted copy of x read per routed pair, the intermediate h written
+    and read, y written in slot order) is reported apart as overhead bytes."""
     Et = touched_experts(ids, w.E)
     P = w.P
-    g1_bytes = (Et * 2 * w.I * weight_bytes_per_row(w.scheme, w.H) + w.T * act_bytes_per_row(w.scheme, w.H)
-                + P * act_bytes_per_row(w.scheme, w.I))
-    g2_bytes = (Et * w.H * weight_bytes_per_row(w.scheme, w.I) + P * act_bytes_per_row(w.scheme, w.I)
-                + P * w.H * 2)
-    return dict(experts_touched=Et, gemm1_bytes=g1_bytes, gemm2_bytes=g2_bytes,
-                gemm1_flops=4.0 * P * w.H * w.I, gemm2_flops=2.0 * P * w.H * w.I)
+    xa, ha = act_bytes_per_row(w.scheme, w.H), act_bytes_per_row(w.scheme, w.I)
+    g1_bytes = Et * 2 * w.I * weight_bytes_per_row(w.scheme, w.H) + w.T * xa
+    g2_bytes = Et * w.H * weight_bytes_per_row(w.scheme, w.I)
+    g1_over = (P - w.T) * xa + P * ha  # per-pair activation rows beyond x once; h written
+    g2_over = P * ha + P * w.H * 2     # h read; y written
+    return dict(experts_touched=Et, gemm1_bytes=g1_bytes, gemm2_bytes=g2_bytes, gemm1_overhead_bytes=g1_over,
+                gemm2_overhead_bytes=g2_over, gemm1_flops=4.0 * P * w.H * w.I, gemm2_flops=2.0 * P * w.H * w.I)
 
 
 def peaks():
@@ -315,7 +328,8 @@ def run_ours(args, w):
     # timed steps then run behind an L2 flush (a 2xL2 write outside the
     # per-step events) so every step streams its weights from HBM.
     alg = algorithmic(wr, d["topk_ids"])
-    flush = alg["gemm1_bytes"] + alg["gemm2_bytes"] < 4 * L2_BYTES
+    touched = alg["gemm1_bytes"] + alg["gemm2_bytes"] + alg["gemm1_overhead_bytes"] + alg["gemm2_overhead_bytes"]
+    flush = touched < 4 * L2_BYTES
     flush_buf = E_((2 * L2_BYTES,), torch.uint8) if flush else None
 
     def step(marks=None):
@@ -448,10 +462,11 @@ def run_ours(args, w):
         stage_steps()
     barrier()
     clk = clocks.stop()
-    ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in step_marks)
-    ms_stages = statistics.mean(m[0].elapsed_time(m[4]) for m in marks)
-    g1_ms = statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
-    g2_ms = statistics.mean(m[2].elapsed_time(m[3]) for m in marks)
+    # medians over the K timed steps
+    ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in step_marks)
+    ms_stages = statistics.median(m[0].elapsed_time(m[4]) for m in marks)
+    g1_ms = statistics.median(m[1].elapsed_time(m[2]) for m in marks)
+    g2_ms = statistics.median(m[2].elapsed_time(m[3]) for m in marks)
     ms = max_over_ranks(ms, world, dev)
     assert int(status.item()) == 0, "device status flagged an error"
     pk = peaks()
@@ -465,7 +480,9 @@ def run_ours(args, w):
     t_tc = alg["gemm1_flops"] / (tensor_peak * 1e12)
     # DRAM bytes per stage-1 launch from one ncu capture, scaled by units processed
     # (the capture's traffic / algorithmic bytes, times this launch's algorithmic bytes)
-    ratio = TRAFFIC_RATIO_GEMM1.get(w.scheme)
+    ratio = TRAFFIC_RATIO_GEMM1.get(w.name)
+    if ratio is None and not (w.scheme == "mxfp4" and qb.tile_nmax(dims) == 16):
+        ratio = TRAFFIC_RATIO_GEMM1.get(w.scheme)  # the scheme's capture used 112-row tiles
     traffic = ratio * alg["gemm1_bytes"] if ratio else None
     if t_hbm >= t_tc:
         achieved = alg["gemm1_bytes"] / (g1_ms * 1e-3) / 1e9
@@ -482,7 +499,10 @@ def run_ours(args, w):
     roof["stage_calls_ms_per_step"] = ms_stages
     roof["gemm1_alg_bytes"] = alg["gemm1_bytes"]
     roof["gemm2_alg_bytes"] = alg["gemm2_bytes"]
+    roof["overhead_bytes"] = dict(gemm1=alg["gemm1_overhead_bytes"], gemm2=alg["gemm2_overhead_bytes"])
+    # stage 2 against HBM on its algorithmic bytes (W2 and scales), and with its overhead bytes added
     roof["gemm2_hbm_frac"] = alg["gemm2_bytes"] / (g2_ms * 1e-3) / 1e9 / pk["hbm"]
+    roof["gemm2_hbm_frac_with_overhead"] = (alg["gemm2_bytes"] + alg["gemm2_overhead_bytes"]) / (g2_ms * 1e-3) / 1e9 / pk["hbm"]
 
     # end to end through the whole-layer entry point with host buffers
     e2e = None
@@ -561,7 +581,7 @@ def run_ours(args, w):
                 run()
                 em[i][1].record()
             barrier()
-            ems = statistics.mean(a.elapsed_time(b_) for a, b_ in em)
+            ems = statistics.median(a.elapsed_time(b_) for a, b_ in em)
             mode = f"one step at a time, L2 flushed between steps, {how}"
         else:
             s0, s1 = ev(), ev()
@@ -593,10 +613,10 @@ def run_ours(args, w):
                     config=dict(workload=w.name, scheme=w.scheme, T=T, H=H, E=E, k=k, I=I,
                                 experts_touched=alg["experts_touched"],
                                 l2=(f"L2 flushed before every timed step (2 x L2 written outside the step's events): "
-                                    f"the step touches only {(alg['gemm1_bytes'] + alg['gemm2_bytes']) / 1e9:.3f} GB"
+                                    f"the step touches only {touched / 1e9:.3f} GB"
                                     if flush else
                                     "inputs larger than L2: each step streams the touched experts' weights "
-                                    f"({(alg['gemm1_bytes'] + alg['gemm2_bytes']) / 1e9:.2f} GB)"),
+                                    f"({touched / 1e9:.2f} GB)"),
                                 launch=launch,
                                 parallelism=f"replicas x{world}"),
                     tokens_per_s=tokens_per_s, roofline=roof, cpu_baseline=cpu, e2e=e2e,
