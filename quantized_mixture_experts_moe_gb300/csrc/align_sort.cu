@@ -6,15 +6,16 @@
 // one: within an expert, slots follow ascending pair id p = t*k + j.
 //
 // Up to 2048 pairs (one chunk) a single CTA does all of it in one launch;
-// above, three launches, none of which lets an atomic decide an order:
+// above, two launches, none of which lets an atomic decide an order:
 //   1. hist:    each CTA owns a contiguous chunk of kChunk pairs and counts
 //               them per expert (shared-memory counters).
-//   2. scan:    one CTA turns the [chunk][expert] histograms into per-chunk
-//               base slots (exclusive over chunks within an expert, plus the
-//               expert's offset) and writes counts and offsets.
-//   3. scatter: each CTA walks its chunk again in pair order; a pair's slot
-//               is its chunk base + the running count of earlier equal ids,
-//               so the result is the stable counting sort.
+//   2. scatter: each CTA sums the [chunk][expert] histograms into per-expert
+//               totals and its chunk's base slots (the exclusive prefix over
+//               chunks plus the expert's offset, from a block scan), then
+//               walks its chunk in pair order: a pair's slot is its chunk base
+//               plus the number of earlier pairs of the same expert, counted
+//               per warp, so the result is the stable counting sort.  CTA 0
+//               writes counts and offsets.
 // The scan also derives the GEMMs' token-tile schedule, and the scatter
 // gives every slot and every pair its row in the token tiles (so the permute
 // and intermediate kernels look it up instead of searching the offsets).
@@ -26,7 +27,6 @@ namespace qmoe {
 constexpr int kChunk = 2048;          // pairs per chunk (one CTA)
 constexpr int kThreads = 1024;        // threads per CTA in hist/scatter (two rounds per chunk)
 constexpr int kMaxExperts = 4096;     // shared-memory counter bound
-constexpr int kScanThreads = 1024;
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -62,22 +62,6 @@ __device__ int block_exclusive_scan(int v, int32_t* ws, int& total) {
     return r;
 }
 
-// Token-tile schedule for the tensor-core GEMMs from the counts of experts
-// e0..e1 (this thread's, E <= 4 * 1024): tile_start[e] = prefix over experts
-// of ceil(count[e] / nmax), tile_start[E] = number of tiles.
-__device__ void write_tile_schedule(const int (&cnt)[4], int e0, int e1, int E, int nmax, int32_t* ws,
-                                    int32_t* __restrict__ tile_start) {
-    int local = 0;
-    for (int e = e0; e < e1; ++e) local += (cnt[e - e0] + nmax - 1) / nmax;
-    int total;
-    int base = block_exclusive_scan(local, ws, total);
-    for (int e = e0; e < e1; ++e) {
-        tile_start[e] = base;
-        base += (cnt[e - e0] + nmax - 1) / nmax;
-    }
-    if (threadIdx.x == 0) tile_start[E] = total;
-}
-
 // Per-chunk expert histogram: counts do not depend on order, so shared-memory
 // atomics are fine here.
 __global__ void __launch_bounds__(kThreads)
@@ -105,83 +89,114 @@ align_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks
     for (int e = tid; e < E; e += kThreads) out[e] = cnt[e];
 }
 
-// One CTA: per expert, chunk bases exclusive over chunks (loads issued eight
-// at a time so they overlap), counts, offsets, the -1 tail of sorted ids and
-// (tile_start non-null) the token-tile schedule.
-__global__ void __launch_bounds__(kScanThreads)
-align_scan_kernel(int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int nmax, int32_t* __restrict__ counts,
-                  int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ tile_start,
-                  int32_t* __restrict__ slot_dest) {
-    __shared__ int32_t ws[33];
+// Per-expert totals and this chunk's bases from the [chunk][expert] histogram
+// (every CTA of the scatter launch does this for itself), then the offsets and
+// the token-tile schedule by block scans: offs/tst are this CTA's copies in
+// shared memory; CTA 0 also writes counts, offsets, tile_start and the -1 tail
+// of the sorted ids to global memory.
+__device__ void scan_chunk_bases(const int32_t* __restrict__ hist, int64_t P, int E, int nchunks, int chunk, int nmax,
+                                 int32_t* cur, int32_t* offs, int32_t* tst, int32_t* ws, int32_t* __restrict__ counts,
+                                 int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids,
+                                 int32_t* __restrict__ tile_start, int32_t* __restrict__ slot_dest) {
     const int tid = threadIdx.x;
-    pdl_sync();
-    const int per = (E + kScanThreads - 1) / kScanThreads;  // <= 4 (E <= kMaxExperts)
+    const bool writer = chunk == 0;
+    const int per = (E + kThreads - 1) / kThreads;  // <= 4 (E <= kMaxExperts)
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-    int cnt[4] = {0, 0, 0, 0};
+    int cnt[4] = {0, 0, 0, 0}, pre[4] = {0, 0, 0, 0};
     int local = 0;
     for (int e = e0; e < e1; ++e) {
-        int run = 0;
-        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+        int run = 0, mine = 0;
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {  // loads issued eight at a time so they overlap
             int32_t v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = (c0 + j < nchunks) ? hist[(size_t)(c0 + j) * E + e] : 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                if (c0 + j < nchunks) hist[(size_t)(c0 + j) * E + e] = run;
+                if (c0 + j == chunk) mine = run;
                 run += v[j];
             }
         }
-        counts[e] = run;
         cnt[e - e0] = run;
+        pre[e - e0] = mine;
         local += run;
     }
     int total_valid;
     int base = block_exclusive_scan(local, ws, total_valid);
     for (int e = e0; e < e1; ++e) {
-        offsets[e] = base;
-        for (int c = 0; c < nchunks; ++c) hist[(size_t)c * E + e] += base;
+        offs[e] = base;
+        cur[e] = base + pre[e - e0];
+        if (writer) {
+            counts[e] = cnt[e - e0];
+            offsets[e] = base;
+        }
         base += cnt[e - e0];
     }
-    if (tid == 0) offsets[E] = total_valid;
-    for (int64_t s = (int64_t)total_valid + tid; s < P; s += kScanThreads) {
-        sorted_pair_ids[s] = -1;
-        if (slot_dest) slot_dest[s] = -1;
+    if (tid == 0) {
+        offs[E] = total_valid;
+        if (writer) offsets[E] = total_valid;
     }
-    if (tile_start) write_tile_schedule(cnt, e0, e1, E, nmax, ws, tile_start);
+    if (tile_start) {
+        int lt = 0;
+        for (int e = e0; e < e1; ++e) lt += (cnt[e - e0] + nmax - 1) / nmax;
+        int ntiles;
+        int tb = block_exclusive_scan(lt, ws, ntiles);
+        for (int e = e0; e < e1; ++e) {
+            tst[e] = tb;
+            if (writer) tile_start[e] = tb;
+            tb += (cnt[e - e0] + nmax - 1) / nmax;
+        }
+        if (tid == 0) {
+            tst[E] = ntiles;
+            if (writer) tile_start[E] = ntiles;
+        }
+    }
+    if (writer)
+        for (int64_t s = (int64_t)total_valid + tid; s < P; s += kThreads) {
+            sorted_pair_ids[s] = -1;
+            if (slot_dest) slot_dest[s] = -1;
+        }
 }
 
 // The chunk's pairs in pair order onto their slots: cur[e] enters as the
-// chunk's first slot of expert e and is advanced past the chunk's pairs.
-// With slot_dest, each slot also gets its token-tile row
-// tile_start[e] * nmax + (slot - offsets[e]) (offsets and tile_start are
-// complete in global memory: written before this CTA's barrier, or by an
-// earlier kernel; read from L2), and pair_dest[p] the same row of pair p
+// chunk's first slot of expert e and is advanced past the chunk's pairs.  Per
+// round of 1024 pairs each warp counts its pairs per expert (one byte per
+// warp and expert in wcnt: at most 32); a pair's slot is cur[e] plus the
+// counts of the earlier warps plus its rank among its own warp's equal ids,
+// so the order is the stable one with four barriers a round.  With
+// slot_dest, each slot also gets its token-tile row
+// tst[e] * nmax + (slot - offs[e]), and pair_dest[p] the same row of pair p
 // (-1 for an invalid id).
 __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E, int64_t p0, int32_t* cur,
-                              int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pair_slot,
-                              const int32_t* offsets, const int32_t* tile_start, int nmax, int32_t* slot_dest,
+                              uint8_t* wcnt, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pair_slot,
+                              const int32_t* offs, const int32_t* tst, int nmax, int32_t* slot_dest,
                               int32_t* pair_dest) {
     const int tid = threadIdx.x, warp = tid >> 5;
+    uint32_t* wz = reinterpret_cast<uint32_t*>(wcnt);  // 32 * E bytes: a multiple of 4
     for (int round = 0; round < kChunk / kThreads; ++round) {
         const int64_t r0 = p0 + round * kThreads;
         if (r0 >= P) break;  // CTA-uniform
-        // only warps that hold pairs of this round take a turn
-        const int64_t warps_left = (P - r0 + 31) / 32;
-        const int nw = warps_left < kThreads / 32 ? (int)warps_left : kThreads / 32;
+        for (int i = tid; i < 8 * E; i += kThreads) wz[i] = 0u;
+        __syncthreads();
         const int64_t p = r0 + tid;
         int e = -1;
         if (p < P) e = ids[p];
         const bool valid = (p < P) && e >= 0 && e < E;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
         const uint32_t before = peers & lanemask_lt();
+        if (valid && before == 0) wcnt[warp * E + e] = (uint8_t)__popc(peers);
+        __syncthreads();
         int slot = -1;
-        for (int w = 0; w < nw; ++w) {
-            if (warp == w) {
-                if (valid) slot = cur[e] + __popc(before);
-                __syncwarp();
-                if (valid && before == 0) cur[e] += __popc(peers);
-            }
-            __syncthreads();
+        if (valid) {
+            int pre = 0;
+            for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
+            slot = cur[e] + pre + __popc(before);
+        }
+        __syncthreads();  // every read of cur for this round is done
+        for (int ee = tid; ee < E; ee += kThreads) {
+            int add = 0;
+#pragma unroll 8
+            for (int w = 0; w < 32; ++w) add += wcnt[w * E + ee];
+            cur[ee] += add;
         }
         if (p < P) {
             pair_slot[p] = slot;
@@ -189,44 +204,55 @@ __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E,
             if (valid) {
                 sorted_pair_ids[slot] = (int32_t)p;
                 if (slot_dest) {
-                    dst = __ldcg(tile_start + e) * nmax + slot - __ldcg(offsets + e);
+                    dst = tst[e] * nmax + slot - offs[e];
                     slot_dest[slot] = dst;
                 }
             }
             if (pair_dest) pair_dest[p] = dst;
         }
+        __syncthreads();  // wcnt and cur settled before the next round
     }
 }
 
-// Stable scatter: the CTA walks its chunk in two rounds of 1024 pairs; inside
-// a round the 32 warps take turns (in pair order) on the per-expert cursors,
-// each warp ranking equal ids among its lanes with match-any.  A pair's slot
-// is therefore its chunk base + the number of earlier pairs of the same
-// expert in the chunk: the stable counting sort.
+// Shared memory of the scan-and-scatter kernels: cur[E], offs[E+1], tst[E+1] ints, then the
+// per-warp expert counts (32 x E bytes).
+inline size_t scatter_smem_bytes(int E) { return (size_t)(3 * E + 2) * 4 + (size_t)32 * E; }
+
+// Second launch of the multi-chunk path: each CTA derives its chunk's bases
+// (and the offsets and tile schedule) from the histograms, then scatters its
+// chunk.  CTA 0 writes the per-expert outputs.
 __global__ void __launch_bounds__(kThreads)
-align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
-                     const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_pair_ids,
-                     int32_t* __restrict__ pair_slot, const int32_t* __restrict__ offsets,
-                     const int32_t* __restrict__ tile_start, int nmax, int32_t* __restrict__ slot_dest,
-                     int32_t* __restrict__ pair_dest) {
-    extern __shared__ int32_t cur[];
-    const int tid = threadIdx.x;
+align_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nchunks,
+                          const int32_t* __restrict__ hist, int nmax, int32_t* __restrict__ counts,
+                          int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids,
+                          int32_t* __restrict__ pair_slot, int32_t* __restrict__ tile_start,
+                          int32_t* __restrict__ slot_dest, int32_t* __restrict__ pair_dest) {
+    extern __shared__ int32_t sm[];
+    int32_t* cur = sm;
+    int32_t* offs = cur + E;
+    int32_t* tst = offs + E + 1;
+    uint8_t* wcnt = reinterpret_cast<uint8_t*>(tst + E + 1);
+    __shared__ int32_t ws[33];
     pdl_sync();
-    const int32_t* base = hist + (size_t)blockIdx.x * E;
-    for (int e = tid; e < E; e += kThreads) cur[e] = base[e];
+    scan_chunk_bases(hist, P, E, nchunks, blockIdx.x, nmax, cur, offs, tst, ws, counts, offsets, sorted_pair_ids,
+                     tile_start, slot_dest);
     __syncthreads();
-    scatter_chunk(ids, P, E, (int64_t)blockIdx.x * kChunk, cur, sorted_pair_ids, pair_slot, offsets, tile_start, nmax,
+    scatter_chunk(ids, P, E, (int64_t)blockIdx.x * kChunk, cur, wcnt, sorted_pair_ids, pair_slot, offs, tst, nmax,
                   slot_dest, pair_dest);
 }
 
 // One CTA for at most one chunk of pairs: histogram, scan (counts, offsets,
-// tile schedule) and the stable scatter of the three-launch path, in one launch.
+// tile schedule) and the stable scatter, in one launch.
 __global__ void __launch_bounds__(kThreads)
 align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, int32_t* __restrict__ counts,
                    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair_ids,
                    int32_t* __restrict__ pair_slot, int32_t* __restrict__ tile_start, int32_t* __restrict__ slot_dest,
                    int32_t* __restrict__ pair_dest, int32_t* __restrict__ dev_status) {
-    extern __shared__ int32_t cur[];  // per-expert counts, then cursors
+    extern __shared__ int32_t sm[];
+    int32_t* cur = sm;  // per-expert counts, then cursors
+    int32_t* offs = cur + E;
+    int32_t* tst = offs + E + 1;
+    uint8_t* wcnt = reinterpret_cast<uint8_t*>(tst + E + 1);
     __shared__ int32_t ws[33];
     const int tid = threadIdx.x;
     pdl_sync();
@@ -254,17 +280,35 @@ align_small_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int nmax, 
     for (int e = e0; e < e1; ++e) {
         counts[e] = cnt[e - e0];
         offsets[e] = base;
+        offs[e] = base;
         cur[e] = base;
         base += cnt[e - e0];
     }
-    if (tid == 0) offsets[E] = total_valid;
+    if (tid == 0) {
+        offsets[E] = total_valid;
+        offs[E] = total_valid;
+    }
     for (int64_t s = (int64_t)total_valid + tid; s < P; s += kThreads) {
         sorted_pair_ids[s] = -1;
         if (slot_dest) slot_dest[s] = -1;
     }
-    if (tile_start) write_tile_schedule(cnt, e0, e1, E, nmax, ws, tile_start);
+    if (tile_start) {
+        int lt = 0;
+        for (int e = e0; e < e1; ++e) lt += (cnt[e - e0] + nmax - 1) / nmax;
+        int ntiles;
+        int tb = block_exclusive_scan(lt, ws, ntiles);
+        for (int e = e0; e < e1; ++e) {
+            tst[e] = tb;
+            tile_start[e] = tb;
+            tb += (cnt[e - e0] + nmax - 1) / nmax;
+        }
+        if (tid == 0) {
+            tst[E] = ntiles;
+            tile_start[E] = ntiles;
+        }
+    }
     __syncthreads();
-    scatter_chunk(ids, P, E, 0, cur, sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest, pair_dest);
+    scatter_chunk(ids, P, E, 0, cur, wcnt, sorted_pair_ids, pair_slot, offs, tst, nmax, slot_dest, pair_dest);
 }
 
 size_t align_ws_bytes(int64_t P, int E) {
@@ -276,24 +320,23 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
                       int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
                       int nmax, int32_t* tile_start, cudaStream_t stream) {
     const int nchunks = (int)((P + kChunk - 1) / kChunk);
-    const size_t smem = (size_t)E * sizeof(int32_t);
+    const size_t hsmem = (size_t)E * sizeof(int32_t);
+    const size_t ssmem = scatter_smem_bytes(E);
     int32_t* slot_dest = tile_start ? tile_start + schedule_ints(E) : nullptr;
     int32_t* pair_dest = slot_dest ? slot_dest + slot_ints(P) : nullptr;
-    if (smem > 48 * 1024) {
-        cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(align_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (hsmem > 48 * 1024)
+        cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem);
+    if (ssmem > 48 * 1024) {
+        cudaFuncSetAttribute(align_scan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+        cudaFuncSetAttribute(align_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
     }
     if (nchunks <= 1)
-        return launch_pdl(align_small_kernel, 1, kThreads, smem, stream, ids, P, E, nmax, counts, offsets,
+        return launch_pdl(align_small_kernel, 1, kThreads, ssmem, stream, ids, P, E, nmax, counts, offsets,
                           sorted_pair_ids, pair_slot, tile_start, slot_dest, pair_dest, dev_status);
-    int rc = launch_pdl(align_hist_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist, dev_status);
+    int rc = launch_pdl(align_hist_kernel, nchunks, kThreads, hsmem, stream, ids, P, E, nchunks, hist, dev_status);
     if (rc == QMOE_OK)
-        rc = launch_pdl(align_scan_kernel, 1, kScanThreads, 0, stream, hist, P, E, nchunks, nmax, counts, offsets,
-                        sorted_pair_ids, tile_start, slot_dest);
-    if (rc == QMOE_OK)
-        rc = launch_pdl(align_scatter_kernel, nchunks, kThreads, smem, stream, ids, P, E, nchunks, hist,
-                        sorted_pair_ids, pair_slot, offsets, tile_start, nmax, slot_dest, pair_dest);
+        rc = launch_pdl(align_scan_scatter_kernel, nchunks, kThreads, ssmem, stream, ids, P, E, nchunks, hist, nmax,
+                        counts, offsets, sorted_pair_ids, pair_slot, tile_start, slot_dest, pair_dest);
     return rc;
 }
 

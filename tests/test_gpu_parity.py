@@ -548,6 +548,30 @@ def test_layer_with_each_token_tile(scheme, nmax):
     assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
 
 
+@pytest.mark.parametrize("scheme", ["w4a16", "w8a8", "w4a8", "mxfp4"])
+def test_layer_token_halves_at_their_edges(scheme):
+    # 224-row tiles: the integer GEMMs split a tile into token halves (112 + 112, or 160 + 64 for
+    # W4A16) and enumerate only the non-empty ones; expert loads just below, at and above each
+    # half and tile boundary, plus empty experts between them
+    counts = [0, 1, 111, 112, 113, 0, 159, 160, 161, 224, 225, 0, 335, 336, 449]
+    rng = np.random.default_rng(91)
+    ids = gen.routing_with_counts(rng, counts, 1)
+    T = ids.shape[0]
+    w = gen.custom(f"halves_{scheme}", scheme, T, 256, len(counts), 1, 128, seed=92)  # H % 256, I % 128
+    d = gen.make_all(w, routing=(ids, gen.routing_weights(rng, T, 1)))
+    try:
+        qb.set_tile_rules([dict(H=w.H, I=w.I, E=w.E, k=w.k, t_min=w.T, t_max=w.T, nmax=224)])
+        assert qb.tile_nmax(qb.dims(w.T, w.k, w.H, w.I, w.E)) == 224
+        g = gp.run_layer(w, d, keep=True)
+    finally:
+        qb.set_tile_rules(qb.read_tile_table(qb.TILE_TABLE_PATH) if os.path.exists(qb.TILE_TABLE_PATH) else [])
+    ref = oracle.moe_forward(w.scheme, dims(w), d)
+    assert g["status"] == 0
+    assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
+    # every routed token's output row is produced (no unit skipped)
+    assert (np.abs(gp.bf16_to_f64(g["out"])).max(axis=1) > 0).all()
+
+
 def test_argument_errors_raise():
     w = gen.custom("err", "w4a16", 4, 256, 4, 2, 64, seed=1)
     d = gen.make_all(w)
