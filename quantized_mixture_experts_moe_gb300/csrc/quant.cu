@@ -148,6 +148,14 @@ __device__ __forceinline__ void permute_quant_mx_item(int64_t wid, const uint16_
     uint8_t sa, sbb;
     mx_quant16(a0, a1, ca, sa);
     mx_quant16(b0, b1, cb, sbb);
+    // a K step's four scale bytes are contiguous in a row's atom: the first lane of each 8-lane group
+    // (one 128-element step) gathers them from the group's even lanes and stores one word
+    uint32_t wa = 0, wb = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        wa |= (uint32_t)(__shfl_sync(0xFFFFFFFFu, (uint32_t)sa, (lane & ~7) + 2 * b) & 0xFFu) << (8 * b);
+        wb |= (uint32_t)(__shfl_sync(0xFFFFFFFFu, (uint32_t)sbb, (lane & ~7) + 2 * b) & 0xFFu) << (8 * b);
+    }
     for (int j0 = 0; j0 < k; j0 += 32) {
         // lane i looks up pair j0 + i's tile and row (tile -1: invalid expert id)
         int dtile = -1, drow = 0;
@@ -167,12 +175,12 @@ __device__ __forceinline__ void permute_quant_mx_item(int64_t wid, const uint16_
             if (ja < nchunk) {
                 uint8_t* blk = tbase + (int64_t)(ja >> 3) * bb;
                 *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (ja & 7) * 16)) = ca;
-                if ((ja & 1) == 0) blk[mxt::scale_offset(nmax, row, (ja >> 1) & 3)] = sa;
+                if ((ja & 7) == 0) *reinterpret_cast<uint32_t*>(blk + mxt::scale_offset(nmax, row, 0)) = wa;
             }
             if (jb < nchunk) {
                 uint8_t* blk = tbase + (int64_t)(jb >> 3) * bb;
                 *reinterpret_cast<uint4*>(blk + mxt::code_offset(row, (jb & 7) * 16)) = cb;
-                if ((jb & 1) == 0) blk[mxt::scale_offset(nmax, row, (jb >> 1) & 3)] = sbb;
+                if ((jb & 7) == 0) *reinterpret_cast<uint32_t*>(blk + mxt::scale_offset(nmax, row, 0)) = wb;
             }
         }
     }
