@@ -186,8 +186,8 @@ __device__ __forceinline__ void permute_quant_mx_item(int64_t wid, const uint16_
     }
 }
 
-// Items are strided over a grid of the CTAs that fit on the GPU at once, so
-// the last wave is not left mostly idle.
+// Items are strided over a grid of up to four waves of the CTAs that fit on
+// the GPU at once.
 __global__ void __launch_bounds__(kPqWarps * 32)
 permute_quant_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_dest, int k, int H,
                         int nmax, int T, uint8_t* __restrict__ tiles) {
@@ -216,7 +216,9 @@ int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t
     int64_t blocks = (warps + kPqWarps - 1) / kPqWarps;
     const int64_t fit = resident_ctas(permute_quant_mx_kernel, kPqWarps * 32);
     if (fit <= 0) return QMOE_ERR_CUDA;
-    if (blocks > fit) blocks = fit;
+    // up to four waves: an item's k scattered row stores are latency-bound, and more warps in flight
+    // (about one item each at T=4096) beat fewer warps striding over several (41.6 -> 37.1 us at T=4096)
+    if (blocks > 4 * fit) blocks = 4 * fit;
     // each pair's token-tile row, written by the routing sort beside the schedule
     const int32_t* pair_dest = tile_start + schedule_ints(d->E) + slot_ints((int64_t)d->T * d->k);
     return launch_pdl(permute_quant_mx_kernel, (unsigned)blocks, kPqWarps * 32, 0, st, x, pair_dest, d->k, d->H,
