@@ -79,6 +79,18 @@ struct Cfg {
     // Measured on GB300 with L2 flushed: decode T=16 114.6 -> 103.2 us/step;
     // at larger tiles they were neutral to 0.5% slower.
     static constexpr bool L2_HINTS = (NMAX == 16);
+    // 112- and 224-token tiles: the weight producer also asks L2 for the
+    // weight tiles PF_AHEAD steps past its newest load (across units), so the
+    // ring's own loads find them there.  The ring holds only 3 or 4 steps,
+    // and a timing variant with 5 showed the weight stream is limited by how
+    // much is in flight.  Measured on GB300 at T = 4096: stage 1 424 -> 416 us,
+    // stage 2 254 -> 248 us (distances 2-6 gave 415-416 us in stage 1, 8
+    // gave 417, 16 gave 438).  With 16-token tiles (6-step ring, weights
+    // evict-first) it made every decode size 2-8% slower, so it is off there,
+    // and so it is for units shorter than 8 steps (stage 2 of the I = 512 and
+    // 256 shards: 152 -> 162 and 121 -> 125 us with it).
+    static constexpr bool L2_PREFETCH = (NMAX != 16);
+    static constexpr int PF_AHEAD = 4;
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
@@ -132,6 +144,8 @@ struct Args {
     uint16_t* y;                // stage 2 output: bf16, slot order
     int32_t* status;
     int weights_early;          // the weight producer may run before the predecessor kernel completes
+    const uint8_t* w;           // the pre-packed weights (for L2 prefetches; the loads go through the tensor map)
+    int64_t gate_bytes;         // stage 1: bytes of one expert's gate tiles (its up tiles follow)
 };
 
 template <int NMAX>
@@ -236,6 +250,37 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             uint32_t phase = 0;
             const int rows_per_e = (STAGE == 1) ? 2 * a.I : a.H;
             const int64_t up_tiles = (int64_t)(a.I / 128) * KT;  // gate tile -> up tile distance (stage 1)
+            // L2 prefetch cursor: unit pu, step pk, its two 8 KiB weight tiles at pA, pB (+ pk * 8 KiB)
+            int pu = blockIdx.x, pk = 0;
+            const uint8_t* pA = nullptr;
+            const uint8_t* pB = nullptr;
+            auto pf_unit = [&]() {
+                if (pu >= total_units) return;
+                int e, m0, ntok, nb, t;
+                decode_unit<NMAX>(pu, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t, a.weights_early != 0);
+                if (STAGE == 1) {
+                    pA = a.w + (int64_t)e * 2 * a.gate_bytes + (int64_t)nb * KT * 8192;
+                    pB = pA + a.gate_bytes;
+                } else {
+                    pA = a.w + (int64_t)((e * rows_per_e + nb * 256) / 128) * KT * 8192;
+                    pB = pA + (int64_t)KT * 8192;
+                }
+            };
+            auto pf_step = [&]() {
+                if (pu >= total_units) return;
+                tc::bulk_prefetch_l2(pA + (int64_t)pk * 8192, 8192);
+                tc::bulk_prefetch_l2(pB + (int64_t)pk * 8192, 8192);
+                if (++pk == KT) {
+                    pk = 0;
+                    pu += gridDim.x;
+                    pf_unit();
+                }
+            };
+            const bool prefetch = C::L2_PREFETCH && KT >= 8;
+            if (prefetch) {
+                pf_unit();
+                for (int i = 0; i < C::PF_AHEAD; ++i) pf_step();
+            }
             for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
                 int e, m0, ntok, nb, t;
                 decode_unit<NMAX>(u, NB, tile_start, E, a.offsets, e, m0, ntok, nb, t, a.weights_early != 0);
@@ -259,6 +304,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                         tc::bulk_load_hint(dS, a.w_s + t0 * 512, 512, &full[slot], pol, C::L2_HINTS);
                         tc::bulk_load_hint(dS + 512, a.w_s + (t0 + KT) * 512, 512, &full[slot], pol, C::L2_HINTS);
                     }
+                    if (prefetch) pf_step();
                     if (++slot == C::S) { slot = 0; phase ^= 1; }
                 }
             }
@@ -526,6 +572,8 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
     a.act = x_tiles; a.w_s = w1_s; a.offsets = offsets; a.tile_start = tile_start;
     a.h_tiles = h_tiles; a.status = status;
     a.weights_early = launch_ctx().weights_early ? 1 : 0;
+    a.w = w1;
+    a.gate_bytes = (int64_t)(d->I / 128) * (d->H / 128) * 8192;
     const int64_t KT = d->H / 128;
     const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * KT;
     const int64_t half = (int64_t)(d->I / 128) * KT * 8192;  // bytes of one expert's gate (or up) tiles
@@ -541,6 +589,7 @@ int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, c
     a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
     a.act = h_tiles; a.w_s = w2_s; a.offsets = offsets; a.tile_start = tile_start; a.y = y; a.status = status;
     a.weights_early = launch_ctx().weights_early ? 1 : 0;
+    a.w = w2;
     const int64_t tiles = (int64_t)d->E * d->H / 128 * (d->I / 128);
     const int nmax = mxt::nmax_for(d);
     return nmax == 224 ? mx::launch_cfg<2, 224>(w2, tiles, 0, a, st)
