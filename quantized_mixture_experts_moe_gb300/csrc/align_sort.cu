@@ -191,7 +191,7 @@ __device__ void scatter_chunk(const int32_t* __restrict__ ids, int64_t P, int E,
             for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
             slot = cur[e] + pre + __popc(before);
         }
-        __syncthreads();  // every read of cur for this round is done
+        __syncthreads();  // every read of cur for these 1024 pairs is done
         for (int ee = tid; ee < E; ee += kThreads) {
             int add = 0;
 #pragma unroll 8
