@@ -491,7 +491,7 @@ def run_ours(args, w):
                     peak_source=f"{pk['source']} (hbm_gbs, copy)")
     else:
         achieved = alg["gemm1_flops"] / (g1_ms * 1e-3) / 1e12
-        src = "measured bf16 x2 (nominal fp8:bf16 ratio)" if w.scheme == "mxfp4" else "measured bf16"
+        src = "bf16 x2 (nominal fp8:bf16 ratio)" if w.scheme == "mxfp4" else "bf16"
         roof = dict(kernel="gemm1_swiglu", bound="tensor", achieved=achieved, peak=tensor_peak, unit="TFLOP/s",
                     frac=achieved / tensor_peak, traffic=traffic, peak_source=f"{pk['source']} {src}")
     roof["gemm1_ms"] = g1_ms

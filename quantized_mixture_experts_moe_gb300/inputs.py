@@ -83,6 +83,9 @@ WORKLOADS = {
         # profiling stand-in for the T=4096 MXFP4 layer: same per-expert load
         # (about 80 tokens), 64 experts so a capture holds ~0.5 GB of weights
         _mk("prof_mxfp4_E64_T512", "mxfp4", 512, 4096, 64, 10, 1024, "uniform", 1005),
+        # profiling stand-in for the routing sort, permute and combine of the T=4096 MXFP4
+        # layer: the same 4096 tokens and 40960 pairs, 16 experts (~70 MB of weights)
+        _mk("prof_small_E16_T4096", "mxfp4", 4096, 4096, 16, 10, 1024, "uniform", 1008),
         # profiling stand-in for the T=8192 W8A8 layer: same per-expert load
         # (about 1024 tokens), 8 experts (~0.14 GB of weights)
         _mk("prof_w8a8_E8_T1024", "w8a8", 1024, 4096, 8, 8, 1408, "uniform", 1006),
