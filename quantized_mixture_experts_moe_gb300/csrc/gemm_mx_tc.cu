@@ -89,8 +89,9 @@ struct Cfg {
     // evict-first) it made every decode size 2-8% slower, so it is off there,
     // and so it is for units shorter than 8 steps (stage 2 of the I = 512 and
     // 256 shards: 152 -> 162 and 121 -> 125 us with it).
+    // Stage 2 with 224-token tiles (T = 8192) prefers 8 steps ahead: 408 -> 395 us there.
     static constexpr bool L2_PREFETCH = (NMAX != 16);
-    static constexpr int PF_AHEAD = 4;
+    static constexpr int PF_AHEAD = (STAGE == 2 && NMAX == 224) ? 8 : 4;
     static constexpr int NSFB = (NMAX + 127) / 128;      // activation scale atoms per step
     static constexpr int A_BYTES = AT * 128 * 128;
     static constexpr int B_BYTES = ((NMAX + 7) / 8) * 1024;
