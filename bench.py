@@ -251,7 +251,7 @@ def run_reference(args, w):
         oracle.moe_forward(w.scheme, dims, d, tokens=toks)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    t = sum(times) / len(times)
+    t = statistics.median(times)  # median step, as for our arm
     value = 6.0 * n * w.k * w.H * w.I / t / 1e12
     sample = f"{n} of {w.T} tokens per step (all k={w.k} pairs each)"
     line = dict(metric=METRIC, value=value, unit=UNIT, impl="reference", n_gpus=args.gpus, steps=args.steps,
