@@ -615,6 +615,14 @@ def test_full_size_sampled_rows(name):
     # every row is finite and the layer is not trivially zero
     allout = gp.bf16_to_f64(g["out"])
     assert np.isfinite(allout).all() and np.abs(allout).max() > 0
+    # the whole-layer call, launched as bench.py times it (dependent launches, weights read before the
+    # wait on the previous kernel, L2 prefetches), gives the same bits as the stage calls
+    wt = gp.device_weights(w, d)
+    out, status = qb.moe_forward(w.scheme, gp.dev(d["x"]), gp.dev(d["topk_ids"]), gp.dev(d["topk_w"]), wt["w1"],
+                                 wt["w1_s"], wt["w2"], wt["w2_s"], I=w.I, E=w.E)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(gp.host(out, np.uint16), g["out"])
 
 
 def test_w4a16_unsupported_shapes_rejected_on_host():
