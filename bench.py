@@ -311,8 +311,14 @@ def run_ours(args, w):
     ws = qb.alloc_workspace(qb.workspace_bytes(dims), dev)
     y = E_((P, H), torch.int16)  # bf16 bits
     out = E_((T, H), torch.int16)
+    # MXFP4 stage 1 in the form the whole-layer call picks: token-major MX x gathered by the GEMM, or
+    # the permuted MX tiles
+    gathers = w.scheme == "mxfp4" and qb.mx_layer_gathers(dims)
     if w.scheme == "mxfp4":
-        xt = E_(qb.mx_tiles_bytes(dims, H), torch.uint8)
+        if gathers:
+            xq, xs = E_((T, H), torch.uint8), E_((T, H // 32), torch.uint8)
+        else:
+            xt = E_(qb.mx_tiles_bytes(dims, H), torch.uint8)
         ht = E_(qb.mx_tiles_bytes(dims, I), torch.uint8)
     elif w.scheme in ("w8a8", "w4a8"):
         xt = E_(qb.w8a8_tiles_bytes(dims, H), torch.uint8)
@@ -334,7 +340,9 @@ def run_ours(args, w):
 
     def step(marks=None):
         qb.qmoe_align_sort(dims, t["topk_ids"], counts, offsets, sorted_ids, slot, status, ws)
-        if w.scheme == "mxfp4":
+        if gathers:
+            qb.qmoe_quant_act_mxfp8(t["x"], xq, xs)
+        elif w.scheme == "mxfp4":
             qb.qmoe_permute_quant_mxfp8(dims, t["x"], slot, offsets, xt, ws)
         elif w.scheme in ("w8a8", "w4a8"):
             qb.qmoe_permute_quant_int8(dims, t["x"], sorted_ids, offsets, xt, ws)
@@ -342,7 +350,9 @@ def run_ours(args, w):
             qb.qmoe_permute_x_f16(dims, t["x"], sorted_ids, offsets, xt, ws)
         if marks:
             marks[0].record()
-        if w.scheme == "mxfp4":
+        if gathers:
+            qb.qmoe_gemm1_swiglu_mxfp4_gather(dims, xq, xs, sorted_ids, t["w1"], t["w1_s"], offsets, ht, status, ws)
+        elif w.scheme == "mxfp4":
             qb.qmoe_gemm1_swiglu_mxfp4(dims, xt, t["w1"], t["w1_s"], offsets, ht, status, ws)
         elif w.scheme == "w8a8":
             qb.qmoe_gemm1_swiglu_w8a8(dims, xt, t["w1"], t["w1_s"], offsets, h32, None, status, ws)
@@ -481,8 +491,8 @@ def run_ours(args, w):
     # DRAM bytes per stage-1 launch from one ncu capture, scaled by units processed
     # (the capture's traffic / algorithmic bytes, times this launch's algorithmic bytes)
     ratio = TRAFFIC_RATIO_GEMM1.get(w.name)
-    if ratio is None and not (w.scheme == "mxfp4" and qb.tile_nmax(dims) == 16):
-        ratio = TRAFFIC_RATIO_GEMM1.get(w.scheme)  # the scheme's capture used 112-row tiles
+    if ratio is None and not (w.scheme == "mxfp4" and (qb.tile_nmax(dims) == 16 or gathers)):
+        ratio = TRAFFIC_RATIO_GEMM1.get(w.scheme)  # the scheme's capture: 112-row tiles, stage 1 from permuted tiles
     traffic = ratio * alg["gemm1_bytes"] if ratio else None
     if t_hbm >= t_tc:
         achieved = alg["gemm1_bytes"] / (g1_ms * 1e-3) / 1e9
@@ -618,6 +628,8 @@ def run_ours(args, w):
                                     "inputs larger than L2: each step streams the touched experts' weights "
                                     f"({touched / 1e9:.2f} GB)"),
                                 launch=launch,
+                                stage1_input=("token-major MX x gathered by the GEMM" if gathers
+                                              else "permuted MX tiles") if w.scheme == "mxfp4" else None,
                                 parallelism=f"replicas x{world}"),
                     tokens_per_s=tokens_per_s, roofline=roof, cpu_baseline=cpu, e2e=e2e,
                     gpu_launches=launches_per_step * args.steps, clocks=clk)

@@ -378,6 +378,30 @@ int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tiles, const ui
                             const int32_t* offsets, uint8_t* h_tiles, int32_t* dev_status, void* ws,
                             size_t ws_bytes, qmoe_stream_t stream);
 
+/* MXFP4 x FP8, gathering form: the same stage 1 (same weights, output, rules
+ *        and limits) reading the activations token-major instead of from
+ *        permuted tiles, as x plus the routing sort's order.  x_q uint8 [T, H]
+ *        and x_s uint8 [T, H/32] = qmoe_quant_act_mxfp8 of x_bf16 [T, H]
+ *        (16-byte aligned); sorted_pair_ids = the qmoe_align_sort output for
+ *        this routing.  Row r of expert e's slots (slot offsets[e] + r) takes
+ *        token sorted_pair_ids[offsets[e] + r] / k; the kernel copies that
+ *        token's codes and scales into each pipeline step, so no expanded copy
+ *        of x is written.  The result equals qmoe_gemm1_swiglu_mxfp4 on the
+ *        qmoe_permute_quant_mxfp8 tiles of the same x, bit for bit ([aiter]
+ *        Changes: fp8 activations into the stage-1 grouped GEMM). */
+int qmoe_gemm1_swiglu_mxfp4_gather(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s,
+                                   const int32_t* sorted_pair_ids, const uint8_t* w1, const uint8_t* w1_s,
+                                   const int32_t* offsets, uint8_t* h_tiles, int32_t* dev_status, void* ws,
+                                   size_t ws_bytes, qmoe_stream_t stream);
+
+/* qmoe_mx_layer_gathers -- 1 if qmoe_moe_forward runs MXFP4 stage 1 in the
+ *        gathering form for these dims (qmoe_quant_act_mxfp8, then
+ *        qmoe_gemm1_swiglu_mxfp4_gather), 0 if through qmoe_permute_quant_mxfp8
+ *        and qmoe_gemm1_swiglu_mxfp4; 0 for invalid dims.  Host only.  The two
+ *        give the same bits; the choice is by speed: the gathering form when
+ *        the token tile has 112 or 224 rows and I <= 512. */
+int qmoe_mx_layer_gathers(const qmoe_dims* d);
+
 /* W8A8 (tensor cores; needs H % 256 == 0, I % 128 == 0, H and I <= 16384,
  *        E <= 512): x_tiles = qmoe_permute_quant_int8 output (K = H);
  *        w1 int8 [E, 2I, H] (row-major, as given; 16-byte aligned);

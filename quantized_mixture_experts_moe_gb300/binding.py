@@ -65,6 +65,8 @@ SIGNATURES = {
     "qmoe_mx_tiles_bytes": ([_DP, _i64], _sz),
     "qmoe_permute_quant_mxfp8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_gemm1_swiglu_mxfp4_gather": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "qmoe_mx_layer_gathers": ([_DP], _i32),
     "qmoe_w8a8_tiles_bytes": ([_DP, _i64], _sz),
     "qmoe_permute_quant_int8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_quant_tiles_int8_f32": ([_DP, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -323,6 +325,19 @@ def qmoe_gemm1_swiglu_mxfp4(d, x_tiles, w1, w1_s, offsets, h_tiles, status, ws, 
     _check(lib().qmoe_gemm1_swiglu_mxfp4(ctypes.byref(d), _ptr(x_tiles), _ptr(w1), _ptr(w1_s), _ptr(offsets),
                                          _ptr(h_tiles), _ptr(status), wp, wn, _stream(stream)),
            "qmoe_gemm1_swiglu_mxfp4")
+
+
+def qmoe_gemm1_swiglu_mxfp4_gather(d, x_q, x_s, sorted_pair_ids, w1, w1_s, offsets, h_tiles, status, ws,
+                                   stream=None):
+    wp, wn = _ws(ws)
+    _check(lib().qmoe_gemm1_swiglu_mxfp4_gather(ctypes.byref(d), _ptr(x_q), _ptr(x_s), _ptr(sorted_pair_ids),
+                                                _ptr(w1), _ptr(w1_s), _ptr(offsets), _ptr(h_tiles), _ptr(status),
+                                                wp, wn, _stream(stream)),
+           "qmoe_gemm1_swiglu_mxfp4_gather")
+
+
+def mx_layer_gathers(d: Dims) -> bool:
+    return bool(lib().qmoe_mx_layer_gathers(ctypes.byref(d)))
 
 
 def w8a8_tiles_bytes(d: Dims, K: int) -> int:

@@ -17,6 +17,9 @@ bool mx_tc_ok(const qmoe_dims* d, const void* w1, const void* w2);
 int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, const uint8_t* w1_s,
                 const int32_t* offsets, const int32_t* tile_start, uint8_t* h_tiles, int32_t* status,
                 cudaStream_t st);
+int mx_tc_gemm1_gather(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const int32_t* sorted,
+                       const uint8_t* w1, const uint8_t* w1_s, const int32_t* offsets, const int32_t* tile_start,
+                       uint8_t* h_tiles, int32_t* status, cudaStream_t st);
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
                 const int32_t* offsets, const int32_t* tile_start, uint16_t* y, int32_t* status, cudaStream_t st);
 int permute_quant_mx_launch(const qmoe_dims* d, const uint16_t* x, const int32_t* pair_slot, const int32_t* offsets,
@@ -102,6 +105,18 @@ extern "C" int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tile
     if (!mx_tc_ok(d, w1, nullptr)) return QMOE_ERR_UNSUPPORTED;
     return mx_tc_gemm1(d, x_tiles, w1, w1_s, offsets, tile_schedule_in(ws, d), h_tiles, dev_status,
                        (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_gemm1_swiglu_mxfp4_gather(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s,
+                                              const int32_t* sorted_pair_ids, const uint8_t* w1, const uint8_t* w1_s,
+                                              const int32_t* offsets, uint8_t* h_tiles, int32_t* dev_status, void* ws,
+                                              size_t ws_bytes, qmoe_stream_t stream) {
+    int rc = gemm_args_ok(d, {x_q, x_s, sorted_pair_ids, w1, w1_s, offsets, h_tiles, dev_status});
+    if (rc != QMOE_OK || (int64_t)d->T * d->k == 0) return rc;
+    if (!mx_ws_ok(d, ws, ws_bytes)) return QMOE_ERR_ARG;
+    if (!mx_tc_ok(d, w1, nullptr)) return QMOE_ERR_UNSUPPORTED;
+    return mx_tc_gemm1_gather(d, x_q, x_s, sorted_pair_ids, w1, w1_s, offsets, tile_schedule_in(ws, d), h_tiles,
+                              dev_status, (cudaStream_t)stream);
 }
 
 extern "C" int qmoe_gemm2_mxfp4(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,
@@ -254,6 +269,21 @@ extern "C" int qmoe_gemm2_w4a8(const qmoe_dims* d, const uint8_t* h_tiles, const
 
 // ------------------------------------------------------------------ whole layer
 
+// Which stage-1 input the whole-layer call gives the MXFP4 GEMM.  The
+// permute writes every routed row once per pair (k expanded copies of x) and
+// the GEMM streams them with bulk copies; the gathering form skips that copy
+// but fetches each tile's rows once per 128-column block of h with cp.async,
+// a slower path per byte.  With 112- or 224-row tiles and at most four column
+// blocks (I <= 512) the saved copy wins, measured on GB300 at H 4096, E 512,
+// top-10 (ms per step, tiles -> gather): I 256 T 4096 368.5 -> 339.9, I 512
+// T 4096 492.5 -> 487.4, I 512 T 8192 815.0 -> 790.5; with I 1024 it loses (T
+// 1024 635.2 -> 684.0, T 4096 768.9 -> 814.0, T 8192 1188.8 -> 1209.6), and
+// 16-row tiles are even or slower (T 16 at I 256 71.5 -> 71.4).
+extern "C" int qmoe_mx_layer_gathers(const qmoe_dims* d) {
+    if (!dims_ok(d)) return 0;
+    return (mxt::nmax_for(d) != 16 && d->I <= 512) ? 1 : 0;
+}
+
 namespace {
 
 struct FwdLayout {
@@ -272,8 +302,10 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
     L.sorted = take(4 * P);
     L.slot = take(4 * P);
     // schemes 2 (W8A8) and 3 (W4A8) share the integer activation path
-    L.xq = take(scheme == 0 ? (size_t)bft::x_tiles_bytes(d)
-                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->H) : qmoe_w8a8_tiles_bytes(d, d->H)));
+    // MXFP4: the MX x tiles, or token-major MX x (codes [T, H], then scales [T, H/32]) when stage 1 gathers
+    const size_t mx_x = qmoe_mx_layer_gathers(d) ? up256((size_t)d->T * H) + (size_t)d->T * (H / 32)
+                                                 : (size_t)mxt::buffer_bytes(d, d->H);
+    L.xq = take(scheme == 0 ? (size_t)bft::x_tiles_bytes(d) : (scheme == 1 ? mx_x : qmoe_w8a8_tiles_bytes(d, d->H)));
     L.h = take(scheme == 0 ? (size_t)bft::h_tiles_bytes(d)
                            : (scheme == 1 ? (size_t)mxt::buffer_bytes(d, d->I) : 4 * P * I));
     L.ht = take(scheme >= 2 ? qmoe_w8a8_tiles_bytes(d, d->I) : (scheme == 0 ? qmoe_w4a16_h16_tiles_bytes(d) : 0));
@@ -330,10 +362,20 @@ extern "C" int qmoe_moe_forward(int scheme, const qmoe_dims* d, const uint16_t* 
             rc = qmoe_gemm2_w4a16(d, (const uint8_t*)at(L.ht), (const uint8_t*)w2, offsets, y, dev_status, aws,
                                   aws_bytes, stream);
     } else if (scheme == 1) {
-        rc = qmoe_permute_quant_mxfp8(d, x_bf16, slot, offsets, (uint8_t*)at(L.xq), aws, aws_bytes, stream);
-        if (rc == QMOE_OK)
-            rc = qmoe_gemm1_swiglu_mxfp4(d, (const uint8_t*)at(L.xq), (const uint8_t*)w1, (const uint8_t*)w1_s,
-                                         offsets, (uint8_t*)at(L.h), dev_status, aws, aws_bytes, stream);
+        uint8_t* xq = (uint8_t*)at(L.xq);
+        if (qmoe_mx_layer_gathers(d)) {
+            // x quantised once per token (token-major); stage 1 gathers each routed row from it
+            uint8_t* xs = xq + up256((size_t)d->T * d->H);
+            rc = qmoe_quant_act_mxfp8(d->T, d->H, x_bf16, xq, xs, stream);
+            if (rc == QMOE_OK)
+                rc = qmoe_gemm1_swiglu_mxfp4_gather(d, xq, xs, sorted, (const uint8_t*)w1, (const uint8_t*)w1_s,
+                                                    offsets, (uint8_t*)at(L.h), dev_status, aws, aws_bytes, stream);
+        } else {
+            rc = qmoe_permute_quant_mxfp8(d, x_bf16, slot, offsets, xq, aws, aws_bytes, stream);
+            if (rc == QMOE_OK)
+                rc = qmoe_gemm1_swiglu_mxfp4(d, xq, (const uint8_t*)w1, (const uint8_t*)w1_s, offsets,
+                                             (uint8_t*)at(L.h), dev_status, aws, aws_bytes, stream);
+        }
         if (rc == QMOE_OK)
             rc = qmoe_gemm2_mxfp4(d, (const uint8_t*)at(L.h), (const uint8_t*)w2, (const uint8_t*)w2_s, offsets, y,
                                   dev_status, aws, aws_bytes, stream);

@@ -18,7 +18,10 @@
 //              the matching 512-byte scale atoms.
 //   warp 1     activation producer: per step two bulk copies of the step's
 //              block of the stage-ready MX activation tiles (the token rows,
-//              already 128-byte swizzled, and their scale atoms).
+//              already 128-byte swizzled, and their scale atoms); or, in
+//              stage 1 from token-major MX x, a gather: the 32 lanes copy each
+//              routed token's 128 codes and 4 scale bytes of the step with
+//              cp.async into the same swizzled slot layout.
 //   warps 2-3  MMA issuers (warp 2 also owns tensor memory), one per weight
 //              tile: one lane copies its scale atoms into TMEM and issues the
 //              MMAs (M = 128 weight rows, N = tokens rounded up to 16, K = 32
@@ -62,11 +65,13 @@ constexpr int WARP_MMA = 2;                 // TMEM owner + MMA issuer for weigh
 constexpr int WARP_MMA2 = WARP_MMA + 1;     // stage 1: second issuer (up accumulator)
 constexpr int WARP_EPI0 = WARP_MMA2 + 1;    // epilogue warps
 constexpr int EPI_WARPS = 8;                // two per TMEM lane quadrant, splitting the token columns
-constexpr int THREADS = (WARP_EPI0 + EPI_WARPS) * 32;
+constexpr int WARP_G1 = WARP_EPI0 + EPI_WARPS;  // stage-1 gather: warps after the epilogue join warp 1
 constexpr int KSTAGE = 128;                 // K elements per pipeline step (4 MMAs of K = 32)
 constexpr uint32_t FP4_TILE_TX = 128 * 64;  // bytes one 128x128 FP4 tile moves (packed)
 
-template <int STAGE, int NMAX_>
+// GATHER: stage 1 gathers token-major x (its own instantiation, so the
+// permuted-tile kernels keep their 12 warps and their code)
+template <int STAGE, int NMAX_, bool GATHER = false>
 struct Cfg {
     static constexpr int NMAX = NMAX_;
     // weight tiles per step, one per MMA issuer: stage 1 gate + up, stage 2
@@ -107,7 +112,14 @@ struct Cfg {
     // ring depth: as many whole steps as fit in the 227 KB of shared memory
     // next to 1 KB of alignment slack, the epilogue buffer, and barriers for
     // up to 16 slots, the misc words and the schedule of up to MAX_E experts
-    static constexpr int FIXED_BYTES = 2 * 16 * 8 + 64 + (512 + 1) * 4;
+    // Stage-1 gather warps (warp 1 and GW - 1 more): one warp copies ~6 bytes
+    // a clock with cp.async, against the ~15-30 KB of token rows a 112- or
+    // 224-row step needs every ~800-1400 clocks (at T = 4096, stage 1 took
+    // 1005 us with one warp, 528 with four, 497 with eight).
+    static constexpr int GW = (STAGE == 1 && GATHER) ? (NMAX == 16 ? 1 : 8) : 0;
+    static constexpr int THREADS = (WARP_G1 + (GW > 1 ? GW - 1 : 0)) * 32;
+    static constexpr int TOK_BYTES = GW * NMAX * 4;  // per gather warp: the unit's token per row
+    static constexpr int FIXED_BYTES = 2 * 16 * 8 + 64 + TOK_BYTES + (512 + 1) * 4;
     static constexpr int S = (232448 - 1024 - EPI_BYTES - FIXED_BYTES) / SLOT_BYTES;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + S * A_BYTES;
@@ -117,7 +129,8 @@ struct Cfg {
     static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
     static constexpr int NBAR = 2 * S + 2 * ACC_BUFS;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int SCHED_OFF = MISC_OFF + 64;
+    static constexpr int TOK_OFF = MISC_OFF + 64;
+    static constexpr int SCHED_OFF = TOK_OFF + TOK_BYTES;
     static constexpr size_t smem_bytes(int E) { return (size_t)SCHED_OFF + (size_t)(E + 1) * 4 + 1024; }
     // TMEM columns: accumulators, then a 2-slot ring for scale factors
     static constexpr uint32_t ACC_COLS = AT * NMAX;
@@ -132,7 +145,9 @@ struct Cfg {
 constexpr int MAX_E = 512;  // schedule prefix kept in shared memory
 static_assert(Cfg<1, 16>::smem_bytes(MAX_E) <= 232448 && Cfg<2, 16>::smem_bytes(MAX_E) <= 232448 &&
                   Cfg<1, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<1, 224>::smem_bytes(MAX_E) <= 232448 &&
-                  Cfg<2, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<2, 224>::smem_bytes(MAX_E) <= 232448,
+                  Cfg<2, 112>::smem_bytes(MAX_E) <= 232448 && Cfg<2, 224>::smem_bytes(MAX_E) <= 232448 &&
+                  Cfg<1, 16, true>::smem_bytes(MAX_E) <= 232448 && Cfg<1, 112, true>::smem_bytes(MAX_E) <= 232448 &&
+                  Cfg<1, 224, true>::smem_bytes(MAX_E) <= 232448,
               "shared memory per CTA");
 
 struct Args {
@@ -147,6 +162,11 @@ struct Args {
     int weights_early;          // the weight producer may run before the predecessor kernel completes
     const uint8_t* w;           // the pre-packed weights (for L2 prefetches; the loads go through the tensor map)
     int64_t gate_bytes;         // stage 1: bytes of one expert's gate tiles (its up tiles follow)
+    // stage-1 gather (xq non-null): token-major MX x, codes [T, H] and scales
+    // [T, H/32], and the routing sort's slot -> pair map (token = pair / k)
+    const uint8_t* xq;
+    const uint8_t* xs;
+    const int32_t* sorted;
 };
 
 template <int NMAX>
@@ -179,10 +199,60 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
     return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
 }
 
-template <int STAGE, int NMAX>
-__global__ void __launch_bounds__(THREADS, 1)
+// Stage-1 activation producer, gather form (warp g of C::GW, each taking an
+// interleaved share of the chunks and rows).  Per step each routed
+// token row of the unit's tile gets its 128 E4M3 codes (eight 16-byte
+// cp.async, 8 lanes per row, so a warp instruction reads four whole 128-byte
+// rows) at the swizzled position the MX tile layout gives it, and its 4 scale
+// bytes at its place in the scale atom.  Rows past the tile's token count are
+// left as they are: they only feed accumulator columns the epilogue never
+// stores.  Every lane then makes one arrival on the slot's full barrier that
+// the hardware delivers once the lane's copies have landed
+// (cp.async.mbarrier.arrive.noinc; the barrier expects the weight producer
+// and these 32 * GW), so no warp waits for its own copies; the MMA issuer
+// orders the landed bytes before its tensor-core reads with a proxy fence
+// after the barrier wait.
+template <typename C, int NMAX>
+__device__ __forceinline__ void gather_x(const Args& a, uint8_t* sB, uint8_t* sSFB, uint64_t* full, uint64_t* empty,
+                                         int* tok_row, const int* tile_start, int total_units, int NB, int KT,
+                                         volatile int* abort_flag, int lane, int g) {
+    const uint64_t pol = tc::l2_evict_last();  // x rows are read by every column block of each of their experts
+    const int64_t xs_row = a.H / 32;
+    int slot = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && !*abort_flag && ok; u += gridDim.x) {
+        int e, m0, ntok, nb, t;
+        decode_unit<NMAX>(u, NB, tile_start, a.E, a.offsets, e, m0, ntok, nb, t, false);
+        __syncwarp();  // every lane is done with the previous unit's rows
+        for (int r = lane; r < ntok; r += 32) tok_row[r] = a.sorted[m0 + r] / a.k;
+        __syncwarp();
+        for (int kt = 0; kt < KT; ++kt) {
+            if (!warp_wait(&empty[slot], phase ^ 1, lane)) {
+                if (lane == 0) set_abort(abort_flag, a.status);
+                ok = false;
+                break;
+            }
+            uint8_t* dB = sB + slot * C::B_BYTES;
+            uint8_t* dS = sSFB + slot * C::SFB_BYTES;
+            for (int i = g * 32 + lane; i < ntok * 8; i += 32 * C::GW) {
+                const int r = i >> 3, c = i & 7;
+                tc::cp_async_16_hint(dB + mxt::code_offset(r, c * 16), a.xq + (int64_t)tok_row[r] * a.H + kt * 128 + c * 16,
+                                     pol);
+            }
+            for (int r = g * 32 + lane; r < ntok; r += 32 * C::GW)
+                tc::cp_async_4(dS + (mxt::scale_offset(NMAX, r, 0) - NMAX * 128), a.xs + (int64_t)tok_row[r] * xs_row + kt * 4);
+            tc::cp_async_mbar_arrive_noinc(&full[slot]);
+            if (++slot == C::S) { slot = 0; phase ^= 1; }
+        }
+    }
+    tc::cp_async_wait<0>();
+}
+
+template <int STAGE, int NMAX, bool GATHER>
+__global__ void __launch_bounds__(Cfg<STAGE, NMAX, GATHER>::THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
-    using C = Cfg<STAGE, NMAX>;
+    using C = Cfg<STAGE, NMAX, GATHER>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::A_OFF;
@@ -215,7 +285,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
     for (int i = threadIdx.x; i <= E; i += blockDim.x) tile_start[i] = __ldcg(a.tile_start + i);
     if (threadIdx.x == 32 * WARP_MMA) {
         for (int s = 0; s < C::S; ++s) {
-            tc::mbar_init(&full[s], 2);        // weight producer (with tx bytes) + activation producer
+            // weight producer (with tx bytes) + activation producer (its 32 lanes when it gathers)
+            tc::mbar_init(&full[s], GATHER ? 1 + 32 * C::GW : 2);
             tc::mbar_init(&empty[s], C::AT);   // one commit per MMA issuer
         }
         for (int b = 0; b < C::ACC_BUFS; ++b) {
@@ -318,7 +389,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
         // A step's activations are one block of the MX tile layout: the
         // first nmma rows of codes (already swizzled) and the scale atoms.
         if (a.weights_early) pdl_wait();
-        if (lane == 0) {
+        if constexpr (GATHER) {
+            gather_x<C, NMAX>(a, sB, sSFB, full, empty, reinterpret_cast<int*>(smem + C::TOK_OFF), tile_start,
+                              total_units, NB, KT, abort_flag, lane, 0);
+        } else if (lane == 0) {
             const uint64_t pol = C::L2_HINTS ? tc::l2_evict_last() : 0ull;  // re-read by the expert's column blocks
             int slot = 0;
             uint32_t phase = 0;
@@ -361,6 +435,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(&full[slot], phase)) { set_abort(abort_flag, a.status); ok = false; break; }
                     tc::tc_fence_after();
+                    // gathered activations were written by cp.async (generic proxy): order them before the
+                    // tensor core's reads of the slot
+                    if constexpr (GATHER) tc::fence_proxy_async_smem();
                     const uint32_t sfa_col = sf_base + sf * C::SF_SLOT;
                     const uint32_t sfb_col = sfa_col + 4;
                     const uint32_t sfa_addr = tc::smem_u32(sSFA + slot * C::SFA_BYTES + iss * 512);
@@ -388,6 +465,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap mapW, const Args a) {
             }
         }
         __syncwarp();
+    } else if (warp >= WARP_G1) {
+        // ------------------------------------------------ more stage-1 gather warps
+        if constexpr (GATHER) {
+            if (a.weights_early) pdl_wait();
+            const int g = warp - WARP_G1 + 1;
+            gather_x<C, NMAX>(a, sB, sSFB, full, empty, reinterpret_cast<int*>(smem + C::TOK_OFF) + g * NMAX, tile_start,
+                              total_units, NB, KT, abort_flag, lane, g);
+        }
     } else {
         // ------------------------------------------------ epilogue warps
         if (a.weights_early) pdl_wait();
@@ -542,20 +627,20 @@ bool mx_tc_supported(const qmoe_dims* d, const void* w1, const void* w2) {
            tiles2 * 128 < (1ll << 31) && (!w1 || a32(w1)) && (!w2 || a32(w2));
 }
 
-template <int STAGE, int NMAX>
+template <int STAGE, int NMAX, bool GATHER = false>
 static int launch_cfg(const void* w, int64_t tiles, int64_t half_bytes, const Args& a, cudaStream_t st) {
-    using C = Cfg<STAGE, NMAX>;
+    using C = Cfg<STAGE, NMAX, GATHER>;
     CUtensorMap map;
     const int64_t KT = (STAGE == 1) ? a.H / 128 : a.I / 128;
     int rc = make_fp4_map(&map, w, tiles, half_bytes, a.E, KT);
     if (rc != QMOE_OK) return rc;
     const size_t smem = C::smem_bytes(a.E);
-    if (cudaFuncSetAttribute(mx_gemm_kernel<STAGE, NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mx_gemm_kernel<STAGE, NMAX, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::smem_bytes(MAX_E)) != cudaSuccess)
         return QMOE_ERR_LAUNCH;
     const int grid = num_sms();
     if (grid <= 0) return QMOE_ERR_CUDA;
-    return launch_pdl(mx_gemm_kernel<STAGE, NMAX>, grid, THREADS, smem, st, map, a);
+    return launch_pdl(mx_gemm_kernel<STAGE, NMAX, GATHER>, grid, C::THREADS, smem, st, map, a);
 }
 
 }  // namespace mx
@@ -582,6 +667,26 @@ int mx_tc_gemm1(const qmoe_dims* d, const uint8_t* x_tiles, const uint8_t* w1, c
     return nmax == 224 ? mx::launch_cfg<1, 224>(w1, tiles, half, a, st)
                        : (nmax == 16 ? mx::launch_cfg<1, 16>(w1, tiles, half, a, st)
                                      : mx::launch_cfg<1, 112>(w1, tiles, half, a, st));
+}
+
+int mx_tc_gemm1_gather(const qmoe_dims* d, const uint8_t* x_q, const uint8_t* x_s, const int32_t* sorted,
+                       const uint8_t* w1, const uint8_t* w1_s, const int32_t* offsets, const int32_t* tile_start,
+                       uint8_t* h_tiles, int32_t* status, cudaStream_t st) {
+    mx::Args a{};
+    a.T = d->T; a.k = d->k; a.H = d->H; a.I = d->I; a.E = d->E;
+    a.act = nullptr; a.w_s = w1_s; a.offsets = offsets; a.tile_start = tile_start;
+    a.h_tiles = h_tiles; a.status = status;
+    a.weights_early = launch_ctx().weights_early ? 1 : 0;
+    a.w = w1;
+    a.gate_bytes = (int64_t)(d->I / 128) * (d->H / 128) * 8192;
+    a.xq = x_q; a.xs = x_s; a.sorted = sorted;
+    const int64_t KT = d->H / 128;
+    const int64_t tiles = (int64_t)d->E * 2 * d->I / 128 * KT;
+    const int64_t half = (int64_t)(d->I / 128) * KT * 8192;
+    const int nmax = mxt::nmax_for(d);
+    return nmax == 224 ? mx::launch_cfg<1, 224, true>(w1, tiles, half, a, st)
+                       : (nmax == 16 ? mx::launch_cfg<1, 16, true>(w1, tiles, half, a, st)
+                                     : mx::launch_cfg<1, 112, true>(w1, tiles, half, a, st));
 }
 
 int mx_tc_gemm2(const qmoe_dims* d, const uint8_t* h_tiles, const uint8_t* w2, const uint8_t* w2_s,

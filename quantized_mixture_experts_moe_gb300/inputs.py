@@ -83,6 +83,9 @@ WORKLOADS = {
         # profiling stand-in for the T=4096 MXFP4 layer: same per-expert load
         # (about 80 tokens), 64 experts so a capture holds ~0.5 GB of weights
         _mk("prof_mxfp4_E64_T512", "mxfp4", 512, 4096, 64, 10, 1024, "uniform", 1005),
+        # profiling stand-in for the gathering stage 1 of the TP4 shard (I 256) at T=4096: same
+        # per-expert load (about 80 tokens), 128 experts (~0.14 GB of stage-1 weights, above L2)
+        _mk("prof_mxfp4_tp4_E128_T1024", "mxfp4", 1024, 4096, 128, 10, 256, "uniform", 1012),
         # profiling stand-in for the routing sort, permute and combine of the T=4096 MXFP4
         # layer: the same 4096 tokens and 40960 pairs, 16 experts (~70 MB of weights)
         _mk("prof_small_E16_T4096", "mxfp4", 4096, 4096, 16, 10, 1024, "uniform", 1008),

@@ -59,7 +59,8 @@ def test_workspace_bytes_host_only(lib):
     assert n >= 4 * 512 * ((40960 + 2047) // 2048)
     # plus the tile schedule (E + 1 ints) and one token-tile row per slot and per pair
     assert n >= 4 * 512 * ((40960 + 2047) // 2048) + 4 * 513 + 2 * 4 * 40960
-    assert qb.forward_workspace_bytes(d, "mxfp4") > 40960 * 4096 * 4  # holds y
+    # holds y (bf16, slot order) and the token-major MX x (codes and scales)
+    assert qb.forward_workspace_bytes(d, "mxfp4") > 40960 * 4096 * 2 + 4096 * 4096 * 33 // 32
     bad = qb.dims(16, 2, 250, 128, 8)  # H not a multiple of 32
     assert qb.workspace_bytes(bad) == 0
 

@@ -476,6 +476,46 @@ def test_layer_invalid_ids_flagged_and_skipped():
     assert rel_l2(gp.bf16_to_f64(g["out"]), ref) < REL_L2
 
 
+@pytest.mark.parametrize("nmax", [16, 112, 224])
+def test_mxfp4_stage1_gather_equals_permuted_tiles(nmax):
+    # Stage 1 reading token-major MX x through the routing order writes the same h tiles, bit for
+    # bit, as stage 1 reading the permuted tiles: expert loads on both sides of each tile size,
+    # empty experts, and two invalid expert ids (pairs without a slot)
+    counts = [0, 1, 15, 16, 17, 0, 111, 112, 113, 223, 225, 3]
+    rng = np.random.default_rng(95)
+    ids = gen.routing_with_counts(rng, counts, 2)
+    ids[1, 0], ids[5, 1] = len(counts), -1
+    T, k, H, I, E = ids.shape[0], 2, 512, 256, len(counts)
+    w = gen.custom(f"gather{nmax}", "mxfp4", T, H, E, k, I, seed=96)
+    d = gen.make_all(w, routing=(ids, gen.routing_weights(rng, T, k)))
+    dd = qb.dims(T, k, H, I, E)
+    t = {key: gp.dev(v) for key, v in d.items()}
+    try:
+        qb.set_tile_rules([dict(H=H, I=I, E=E, k=k, t_min=T, t_max=T, nmax=nmax)])
+        assert qb.tile_nmax(dd) == nmax
+        P = T * k
+        counts_d, offsets = gp.empty(E, torch.int32), gp.empty(E + 1, torch.int32)
+        sorted_ids, slot = gp.empty(P, torch.int32), gp.empty(P, torch.int32)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = qb.alloc_workspace(qb.workspace_bytes(dd))
+        qb.qmoe_align_sort(dd, t["topk_ids"], counts_d, offsets, sorted_ids, slot, status, ws)
+        w1, w1p, _, _ = qb.prepack_mxfp4(t["w1"], t["w1_s"], t["w2"], t["w2_s"], H, I)
+        xt = gp.empty(qb.mx_tiles_bytes(dd, H), torch.uint8)
+        qb.qmoe_permute_quant_mxfp8(dd, t["x"], slot, offsets, xt, ws)
+        h_tiles = torch.zeros(qb.mx_tiles_bytes(dd, I), dtype=torch.uint8, device="cuda")
+        qb.qmoe_gemm1_swiglu_mxfp4(dd, xt, w1, w1p, offsets, h_tiles, status, ws)
+        xq, xs = gp.empty((T, H), torch.uint8), gp.empty((T, H // 32), torch.uint8)
+        qb.qmoe_quant_act_mxfp8(t["x"], xq, xs)
+        h_gather = torch.zeros_like(h_tiles)
+        qb.qmoe_gemm1_swiglu_mxfp4_gather(dd, xq, xs, sorted_ids, w1, w1p, offsets, h_gather, status, ws)
+        torch.cuda.synchronize()
+    finally:
+        qb.set_tile_rules(qb.read_tile_table(qb.TILE_TABLE_PATH) if os.path.exists(qb.TILE_TABLE_PATH) else [])
+    assert int(status.item()) == qb.DEV_BAD_EXPERT_ID  # the sort flags the two ids; nothing else
+    assert np.array_equal(gp.host(h_gather), gp.host(h_tiles))
+    assert gp.host(h_gather).any()
+
+
 def test_layer_zero_tokens():
     w = gen.custom("empty", "w4a16", 0, 256, 8, 2, 128, seed=1)
     d = gen.make_all(w)
