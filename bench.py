@@ -42,6 +42,9 @@ L2_BYTES = 129 * 10**6  # GB300 L2
 TRAFFIC_RATIO_GEMM1 = {
     # MXFP4, 512 tokens over 64 experts (~80 per expert, as at T=4096 over 512), 112-row tiles
     "mxfp4": (309262592 + 6259456) / 287375360,
+    # MXFP4 TP4 shard (I 256) with stage 1 gathering x: 1024 tokens over 128 experts (~80 per expert,
+    # as at T=4096 over 512), 112-row tiles
+    "mxfp4_tp4_T4096": (147034368 + 3652352) / 146931712,
     # MXFP4 decode, 16-row tiles, on the workloads themselves
     "decode_T1": (45416448 + 161024) / 44568704,
     "decode_T4": (127116032 + 2582016) / 124797440,

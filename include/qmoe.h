@@ -399,7 +399,7 @@ int qmoe_gemm1_swiglu_mxfp4_gather(const qmoe_dims* d, const uint8_t* x_q, const
  *        qmoe_gemm1_swiglu_mxfp4_gather), 0 if through qmoe_permute_quant_mxfp8
  *        and qmoe_gemm1_swiglu_mxfp4; 0 for invalid dims.  Host only.  The two
  *        give the same bits; the choice is by speed: the gathering form when
- *        the token tile has 112 or 224 rows and I <= 512. */
+ *        the token tile has 112 or 224 rows, I <= 512 and T*k >= 64*E. */
 int qmoe_mx_layer_gathers(const qmoe_dims* d);
 
 /* W8A8 (tensor cores; needs H % 256 == 0, I % 128 == 0, H and I <= 16384,

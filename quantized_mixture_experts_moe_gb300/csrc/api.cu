@@ -273,15 +273,17 @@ extern "C" int qmoe_gemm2_w4a8(const qmoe_dims* d, const uint8_t* h_tiles, const
 // permute writes every routed row once per pair (k expanded copies of x) and
 // the GEMM streams them with bulk copies; the gathering form skips that copy
 // but fetches each tile's rows once per 128-column block of h with cp.async,
-// a slower path per byte.  With 112- or 224-row tiles and at most four column
-// blocks (I <= 512) the saved copy wins, measured on GB300 at H 4096, E 512,
-// top-10 (ms per step, tiles -> gather): I 256 T 4096 368.5 -> 339.9, I 512
-// T 4096 492.5 -> 487.4, I 512 T 8192 815.0 -> 790.5; with I 1024 it loses (T
-// 1024 635.2 -> 684.0, T 4096 768.9 -> 814.0, T 8192 1188.8 -> 1209.6), and
-// 16-row tiles are even or slower (T 16 at I 256 71.5 -> 71.4).
+// a slower path per byte.  The saved copy wins with at most four column
+// blocks (I <= 512), 112- or 224-row tiles and at least 64 pairs per expert
+// on average.  Measured on GB300 at H 4096, E 512, top-10 (us per step,
+// permuted tiles -> gather): I 256: T 1024 243.8 -> 241.6, T 4096 368.6 ->
+// 337.9, T 8192 606.7 -> 546.9; I 512: T 1024 372.6 -> 382.9, T 4096 491.3 ->
+// 481.7, T 8192 814.8 -> 783.2; I 1024: T 1024 635.2 -> 684.0, T 4096 768.9 ->
+// 814.0, T 8192 1188.8 -> 1209.6; 16-row tiles even or slower (I 256 T 16
+// 71.5 -> 71.4).
 extern "C" int qmoe_mx_layer_gathers(const qmoe_dims* d) {
     if (!dims_ok(d)) return 0;
-    return (mxt::nmax_for(d) != 16 && d->I <= 512) ? 1 : 0;
+    return (mxt::nmax_for(d) != 16 && d->I <= 512 && (int64_t)d->T * d->k >= (int64_t)64 * d->E) ? 1 : 0;
 }
 
 namespace {

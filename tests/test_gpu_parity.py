@@ -571,6 +571,33 @@ def test_forward_back_to_back_calls_share_a_workspace(scheme):
         assert np.array_equal(gp.host(out, np.uint16), gp.run_layer(w, d)["out"]), w.name
 
 
+def test_forward_switches_mxfp4_stage1_form_between_calls():
+    # The whole-layer call gathers x in stage 1 for some shapes and reads permuted tiles for
+    # others (qmoe_mx_layer_gathers).  Calls of both kinds back to back on one stream and one
+    # workspace, no synchronisation between them: each equals its batch run through the stage
+    # calls (permuted tiles), bit for bit.
+    H, E, k, I = 512, 8, 4, 256
+    ws_ = [gen.Workload(f"sw_{i}", "mxfp4", T, H, E, k, I, "uniform", 400 + i, 399)
+           for i, T in enumerate((200, 7, 161, 40))]
+    qd = lambda w: qb.dims(w.T, w.k, w.H, w.I, w.E)
+    assert [qb.mx_layer_gathers(qd(w)) for w in ws_] == [True, False, True, False]
+    ds = [gen.make_all(w) for w in ws_]
+    wt = gp.device_weights(ws_[0], ds[0])
+    ws = qb.alloc_workspace(max(qb.forward_workspace_bytes(qd(w), "mxfp4") for w in ws_))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ins = [{key: gp.dev(d[key]) for key in ("x", "topk_ids", "topk_w")} for d in ds]
+    outs = [gp.empty((w.T, H), torch.int16) for w in ws_]
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for w, t, out in zip(ws_, ins, outs):
+            qb.qmoe_moe_forward("mxfp4", qd(w), t["x"], t["topk_ids"], t["topk_w"], wt["w1"], wt["w1_s"], wt["w2"],
+                                wt["w2_s"], out, status, ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for w, d, out in zip(ws_, ds, outs):
+        assert np.array_equal(gp.host(out, np.uint16), gp.run_layer(w, d)["out"]), w.name
+
+
 @pytest.mark.parametrize("scheme", ["mxfp4", "w8a8", "w4a8", "w4a16"])
 @pytest.mark.parametrize("nmax", [16, 112, 224])
 def test_layer_with_each_token_tile(scheme, nmax):
