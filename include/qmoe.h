@@ -384,7 +384,8 @@ int qmoe_gemm1_swiglu_mxfp4(const qmoe_dims* d, const uint8_t* x_tiles, const ui
  *        and x_s uint8 [T, H/32] = qmoe_quant_act_mxfp8 of x_bf16 [T, H]
  *        (16-byte aligned); sorted_pair_ids = the qmoe_align_sort output for
  *        this routing.  Row r of expert e's slots (slot offsets[e] + r) takes
- *        token sorted_pair_ids[offsets[e] + r] / k; the kernel copies that
+ *        token sorted_pair_ids[offsets[e] + r] / k (an entry outside [0, T*k)
+ *        is not read, and that row's output is undefined); the kernel copies that
  *        token's codes and scales into each pipeline step, so no expanded copy
  *        of x is written.  The result equals qmoe_gemm1_swiglu_mxfp4 on the
  *        qmoe_permute_quant_mxfp8 tiles of the same x, bit for bit ([aiter]

@@ -225,7 +225,11 @@ __device__ __forceinline__ void gather_x(const Args& a, uint8_t* sB, uint8_t* sS
         int e, m0, ntok, nb, t;
         decode_unit<NMAX>(u, NB, tile_start, a.E, a.offsets, e, m0, ntok, nb, t, false);
         __syncwarp();  // every lane is done with the previous unit's rows
-        for (int r = lane; r < ntok; r += 32) tok_row[r] = a.sorted[m0 + r] / a.k;
+        // a pair id outside [0, T*k) (not a routing sort's output) is not read: its row keeps stale data
+        for (int r = lane; r < ntok; r += 32) {
+            const int p = a.sorted[m0 + r];
+            tok_row[r] = (p >= 0 && (int64_t)p < (int64_t)a.T * a.k) ? p / a.k : -1;
+        }
         __syncwarp();
         for (int kt = 0; kt < KT; ++kt) {
             if (!warp_wait(&empty[slot], phase ^ 1, lane)) {
@@ -237,11 +241,16 @@ __device__ __forceinline__ void gather_x(const Args& a, uint8_t* sB, uint8_t* sS
             uint8_t* dS = sSFB + slot * C::SFB_BYTES;
             for (int i = g * 32 + lane; i < ntok * 8; i += 32 * C::GW) {
                 const int r = i >> 3, c = i & 7;
-                tc::cp_async_16_hint(dB + mxt::code_offset(r, c * 16), a.xq + (int64_t)tok_row[r] * a.H + kt * 128 + c * 16,
-                                     pol);
+                const int tok = tok_row[r];
+                if (tok >= 0)
+                    tc::cp_async_16_hint(dB + mxt::code_offset(r, c * 16), a.xq + (int64_t)tok * a.H + kt * 128 + c * 16,
+                                         pol);
             }
-            for (int r = g * 32 + lane; r < ntok; r += 32 * C::GW)
-                tc::cp_async_4(dS + (mxt::scale_offset(NMAX, r, 0) - NMAX * 128), a.xs + (int64_t)tok_row[r] * xs_row + kt * 4);
+            for (int r = g * 32 + lane; r < ntok; r += 32 * C::GW) {
+                const int tok = tok_row[r];
+                if (tok >= 0)
+                    tc::cp_async_4(dS + (mxt::scale_offset(NMAX, r, 0) - NMAX * 128), a.xs + (int64_t)tok * xs_row + kt * 4);
+            }
             tc::cp_async_mbar_arrive_noinc(&full[slot]);
             if (++slot == C::S) { slot = 0; phase ^= 1; }
         }

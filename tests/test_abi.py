@@ -65,6 +65,23 @@ def test_workspace_bytes_host_only(lib):
     assert qb.workspace_bytes(bad) == 0
 
 
+def test_mx_layer_stage1_choice_host_only(lib):
+    # the whole-layer call gathers x in MXFP4 stage 1 only with 112/224-row tiles, I <= 512 and
+    # at least 64 pairs per expert; host-only, no GPU needed
+    rules = qb.read_tile_table(qb.TILE_TABLE_PATH) if os.path.exists(qb.TILE_TABLE_PATH) else []
+    try:
+        qb.set_tile_rules([])  # built-in tile rule: 224 rows above 96 pairs per expert, else 112
+        assert qb.mx_layer_gathers(qb.dims(4096, 10, 4096, 256, 512))      # 80 pairs per expert, 112 rows
+        assert qb.mx_layer_gathers(qb.dims(8192, 10, 4096, 512, 512))      # 160 per expert, 224 rows
+        assert not qb.mx_layer_gathers(qb.dims(4096, 10, 4096, 1024, 512))  # I 1024
+        assert not qb.mx_layer_gathers(qb.dims(1024, 10, 4096, 256, 512))   # 20 pairs per expert
+        qb.set_tile_rules([dict(H=4096, I=256, E=512, k=10, t_min=1, t_max=8192, nmax=16)])
+        assert not qb.mx_layer_gathers(qb.dims(4096, 10, 4096, 256, 512))  # 16-row tiles
+        assert not qb.mx_layer_gathers(qb.dims(16, 2, 250, 128, 8))         # invalid dims
+    finally:
+        qb.set_tile_rules(rules)
+
+
 def test_host_checks_reject_before_launch(lib):
     d = qb.dims(16, 2, 256, 128, 8)
     null = None
