@@ -110,6 +110,15 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.qmoe_prepack_mx_scales(128, 100, ok, ok, null) == -1
     assert lib.qmoe_prepack_mx_scales(128, 128, null, ok, null) == -1
     assert qb.mx_scales_packed_bytes(300, 4096) == 3 * 32 * 512
+    # MXFP4 stage 1, gathering form: null or misaligned inputs, a short workspace, an unsupported
+    # shape (H % 256) -- all refused on the host before any launch
+    g1g = lambda dd, xq, xs, srt, ws_bytes: lib.qmoe_gemm1_swiglu_mxfp4_gather(
+        ctypes.byref(dd), xq, xs, srt, ok, ok, ok, ok, ok, ok, ws_bytes, null)
+    assert g1g(d, null, ok, ok, 1 << 30) == -1
+    assert g1g(d, ok, misaligned, ok, 1 << 30) == -1
+    assert g1g(d, ok, ok, null, 1 << 30) == -1
+    assert g1g(d, ok, ok, ok, 0) == -1
+    assert g1g(qb.dims(16, 2, 128, 128, 8), ok, ok, ok, 1 << 30) == -2
 
 
 def test_w8a8_host_checks(lib):
