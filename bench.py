@@ -380,10 +380,10 @@ def run_ours(args, w):
             marks[2].record()
         qb.qmoe_combine(dims, y, t["topk_w"], slot, out)
 
-    # routing sort (one fused launch up to 2048 pairs, else histogram, scan, scatter), permute/quantise,
-    # the two GEMMs, the intermediate pass of the integer and W4A16 paths, combine
-    sort_launches = 1 if P <= 2048 else 3
-    launches_per_step = sort_launches + 1 + 2 + (1 if w.scheme in ("w8a8", "w4a8", "w4a16") else 0) + 1
+    # the kernels one timed step (one whole-layer call) launches, as the library counts them: routing
+    # sort (one launch up to 2048 pairs, else two), activation quantisation, the two GEMMs, the
+    # intermediate pass of the integer and W4A16 paths, and the combine
+    launches_per_step = qb.forward_launches(dims, w.scheme)
 
     def barrier():
         if world > 1:

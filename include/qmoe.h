@@ -403,6 +403,13 @@ int qmoe_gemm1_swiglu_mxfp4_gather(const qmoe_dims* d, const uint8_t* x_q, const
  *        the token tile has 112 or 224 rows, I <= 512 and T*k >= 64*E. */
 int qmoe_mx_layer_gathers(const qmoe_dims* d);
 
+/* qmoe_forward_launches -- how many kernels one qmoe_moe_forward call with
+ *        these dims and scheme launches (0 for invalid arguments).  Host only.
+ *        The routing sort is one launch up to 2048 pairs and two above; then
+ *        the activation quantisation, the two GEMMs, the W4A16 / integer
+ *        intermediate pass, and the combine. */
+int qmoe_forward_launches(const qmoe_dims* d, int scheme);
+
 /* W8A8 (tensor cores; needs H % 256 == 0, I % 128 == 0, H and I <= 16384,
  *        E <= 512): x_tiles = qmoe_permute_quant_int8 output (K = H);
  *        w1 int8 [E, 2I, H] (row-major, as given; 16-byte aligned);

@@ -67,6 +67,7 @@ SIGNATURES = {
     "qmoe_gemm1_swiglu_mxfp4": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_gemm1_swiglu_mxfp4_gather": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_mx_layer_gathers": ([_DP], _i32),
+    "qmoe_forward_launches": ([_DP, _i32], _i32),
     "qmoe_w8a8_tiles_bytes": ([_DP, _i64], _sz),
     "qmoe_permute_quant_int8": ([_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "qmoe_quant_tiles_int8_f32": ([_DP, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -334,6 +335,10 @@ def qmoe_gemm1_swiglu_mxfp4_gather(d, x_q, x_s, sorted_pair_ids, w1, w1_s, offse
                                                 _ptr(w1), _ptr(w1_s), _ptr(offsets), _ptr(h_tiles), _ptr(status),
                                                 wp, wn, _stream(stream)),
            "qmoe_gemm1_swiglu_mxfp4_gather")
+
+
+def forward_launches(d: Dims, scheme: str) -> int:
+    return int(lib().qmoe_forward_launches(ctypes.byref(d), SCHEME_ID[scheme]))
 
 
 def mx_layer_gathers(d: Dims) -> bool:

@@ -340,6 +340,10 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
     return rc;
 }
 
+// Kernels align_sort_launch starts for P pairs: one CTA's single launch up to
+// one chunk, else the histogram and the scan-and-scatter.
+int align_sort_launches(int64_t P) { return (P + kChunk - 1) / kChunk <= 1 ? 1 : 2; }
+
 // Where the tile schedule lives inside the routing workspace.
 int32_t* tile_schedule_in(void* ws, const qmoe_dims* d) {
     return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + align_ws_bytes((int64_t)d->T * d->k, d->E));

@@ -9,6 +9,7 @@ int align_sort_launch(int64_t P, int E, const int32_t* ids, int32_t* counts, int
                       int32_t* sorted_pair_ids, int32_t* pair_slot, int32_t* dev_status, int32_t* hist,
                       int nmax, int32_t* tile_start, cudaStream_t stream);
 int quant_mx_launch(int64_t rows, int64_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
+int align_sort_launches(int64_t P);
 template <typename In>
 int quant_int8_launch(int64_t rows, int64_t cols, const In* x, int8_t* q, float* s, cudaStream_t st);
 int combine_launch(const qmoe_dims* d, const uint16_t* y, const float* topk_w, const int32_t* pair_slot,
@@ -318,6 +319,17 @@ FwdLayout fwd_layout(const qmoe_dims* d, int scheme) {
 }
 
 }  // namespace
+
+extern "C" int qmoe_forward_launches(const qmoe_dims* d, int scheme) {
+    if (!dims_ok(d) || scheme < 0 || scheme > 3) return 0;
+    int n = align_sort_launches((int64_t)d->T * d->k);  // routing sort
+    if (d->T == 0) return n;
+    n += 1;                                          // activation quantisation (into tiles, or token-major)
+    n += 2;                                          // the two grouped GEMMs
+    if (scheme != 1) n += 1;                         // W4A16 h -> fp16 rows, or the integer intermediate pass
+    n += 1;                                          // combine
+    return n;
+}
 
 extern "C" size_t qmoe_forward_workspace_bytes(const qmoe_dims* d, int scheme) {
     if (!dims_ok(d) || scheme < 0 || scheme > 3) return 0;

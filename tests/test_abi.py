@@ -82,6 +82,23 @@ def test_mx_layer_stage1_choice_host_only(lib):
         qb.set_tile_rules(rules)
 
 
+def test_forward_launch_count_host_only(lib):
+    # kernels one whole-layer call launches: routing sort (1 up to 2048 pairs, else 2), activation
+    # quantisation, two GEMMs, the W4A16 / integer intermediate pass, and the combine
+    rules = qb.read_tile_table(qb.TILE_TABLE_PATH) if os.path.exists(qb.TILE_TABLE_PATH) else []
+    try:
+        qb.set_tile_rules([dict(H=4096, I=1024, E=512, k=10, t_min=1, t_max=256, nmax=16)])
+        assert qb.forward_launches(qb.dims(4096, 10, 4096, 1024, 512), "mxfp4") == 6
+        assert qb.forward_launches(qb.dims(1, 10, 4096, 1024, 512), "mxfp4") == 5
+        assert qb.forward_launches(qb.dims(8192, 8, 4096, 1408, 64), "w8a8") == 7
+        assert qb.forward_launches(qb.dims(8192, 8, 4096, 1408, 64), "w4a8") == 7
+        assert qb.forward_launches(qb.dims(100, 8, 2048, 768, 128), "w4a16") == 6
+        assert qb.forward_launches(qb.dims(0, 8, 2048, 768, 128), "w4a16") == 1
+        assert qb.forward_launches(qb.dims(16, 2, 250, 128, 8), "mxfp4") == 0
+    finally:
+        qb.set_tile_rules(rules)
+
+
 def test_host_checks_reject_before_launch(lib):
     d = qb.dims(16, 2, 256, 128, 8)
     null = None

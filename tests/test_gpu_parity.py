@@ -598,6 +598,43 @@ def test_forward_switches_mxfp4_stage1_form_between_calls():
         assert np.array_equal(gp.host(out, np.uint16), gp.run_layer(w, d)["out"]), w.name
 
 
+def test_forward_16row_tiles_back_to_back_with_unrouted_token():
+    # The whole-layer MXFP4 call with 16-row token tiles (the decode form) against the stage calls,
+    # bit for bit: ragged loads, invalid ids (one token with none of its pairs routed, whose row must
+    # come out zero), calls of several sizes back to back on one workspace, outputs pre-filled with
+    # NaN so no row is left unwritten.
+    H, E, k, I = 512, 12, 4, 256
+    ws_ = [gen.Workload(f"fz_{i}", "mxfp4", T, H, E, k, I, "uniform", 500 + i, 499)
+           for i, T in enumerate((37, 5, 1, 16))]
+    ds = [gen.make_all(w) for w in ws_]
+    ds[0]["topk_ids"] = ds[0]["topk_ids"].copy()
+    ds[0]["topk_ids"][3, :] = -1
+    ds[0]["topk_ids"][7, 2] = E
+    qd = lambda w: qb.dims(w.T, w.k, w.H, w.I, w.E)
+    try:
+        qb.set_tile_rules([dict(H=H, I=I, E=E, k=k, t_min=1, t_max=64, nmax=16)])
+        for w in ws_:
+            assert qb.tile_nmax(qd(w)) == 16 and qb.forward_launches(qd(w), "mxfp4") == 5
+        wt = gp.device_weights(ws_[0], ds[0])
+        ws = qb.alloc_workspace(max(qb.forward_workspace_bytes(qd(w), "mxfp4") for w in ws_))
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ins = [{key: gp.dev(d[key]) for key in ("x", "topk_ids", "topk_w")} for d in ds]
+        outs = [torch.full((w.T, H), 0x7FC0, dtype=torch.int16, device="cuda") for w in ws_]
+        torch.cuda.synchronize()
+        for _ in range(2):
+            for w, t, out in zip(ws_, ins, outs):
+                qb.qmoe_moe_forward("mxfp4", qd(w), t["x"], t["topk_ids"], t["topk_w"], wt["w1"], wt["w1_s"],
+                                    wt["w2"], wt["w2_s"], out, status, ws)
+        torch.cuda.synchronize()
+        refs = [gp.run_layer(w, d) for w, d in zip(ws_, ds)]
+    finally:
+        qb.set_tile_rules(qb.read_tile_table(qb.TILE_TABLE_PATH) if os.path.exists(qb.TILE_TABLE_PATH) else [])
+    assert int(status.item()) == qb.DEV_BAD_EXPERT_ID
+    for w, out, ref in zip(ws_, outs, refs):
+        assert np.array_equal(gp.host(out, np.uint16), ref["out"]), w.name
+    assert not refs[0]["out"][3].any()  # the token with no routed pair
+
+
 @pytest.mark.parametrize("scheme", ["mxfp4", "w8a8", "w4a8", "w4a16"])
 @pytest.mark.parametrize("nmax", [16, 112, 224])
 def test_layer_with_each_token_tile(scheme, nmax):
