@@ -8,7 +8,8 @@
 //            E4M3 codes + E8M0 scales per 32 columns of I;
 //   stage 2: y = W2 . h, accumulated in fp32, stored as bf16.
 //
-// Structure (one persistent CTA per SM, 12 warps):
+// Structure (one persistent CTA per SM, 12 warps; 19 in the gathering stage-1
+// form, whose 7 extra gather warps join warp 1):
 //   warp 0     weight producer: per pipeline step one TMA load (a 4D box) of
 //              the step's two FP4 weight tiles (stage 1: a gate tile and its
 //              up partner; stage 2: two adjacent row tiles of W2) from
